@@ -1,0 +1,242 @@
+"""CPU oracle for the MoE routing / permute / MXFP8 expert-FFN path.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product
+library (``routing_permute_mxfp8_gb300``) never does, and shares no code
+with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, OpenMP
+over independent rows); this module builds it with gcc and wraps it for
+numpy arrays.  Each wrapper names the page passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+_lib = None
+
+E5M2 = 23
+E4M3 = 24
+DT_F32, DT_F16, DT_BF16 = 0, 1, 27
+
+
+def build() -> str:
+    """Compile oracle.c (gcc -O2, OpenMP) into oracle/_oracle.so."""
+    tmp = _LIB_PATH + ".tmp"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"],
+                   check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        build()
+    L = ctypes.CDLL(_LIB_PATH)
+    p, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    u8, u16 = ctypes.c_uint8, ctypes.c_uint16
+    L.orc_num_threads.restype = i32
+    L.orc_fp8_value.argtypes, L.orc_fp8_value.restype = [u8, i32], d
+    L.orc_fp8_round.argtypes, L.orc_fp8_round.restype = [d, i32], u8
+    L.orc_fp8_round_array.argtypes, L.orc_fp8_round_array.restype = [p, i64, i32, p], None
+    L.orc_bf16_round.argtypes, L.orc_bf16_round.restype = [d], u16
+    L.orc_mx_block.argtypes, L.orc_mx_block.restype = [p, i64, i32, p, p], None
+    L.orc_mx_quantize_rows.argtypes, L.orc_mx_quantize_rows.restype = [p, i64, i64, i32, p, p, i64], None
+    L.orc_mx_quantize_src.argtypes, L.orc_mx_quantize_src.restype = [p, i32, i64, i64, i32, p, p, i64], None
+    L.orc_route.argtypes, L.orc_route.restype = [p, i32, i64, i64, i64, p, p, p], i64
+    L.orc_permute.argtypes, L.orc_permute.restype = [p, i32, i64, i64, p, i64, i32, p, p, i64], None
+    L.orc_expert_row.argtypes = [p, p, i32, p, p, p, p, i32, i64, i64, i32, p, p, p]
+    L.orc_expert_row.restype = None
+    L.orc_mega_moe_tokens.argtypes = [p, p, p, i32, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                      i32, i32, i32, p, i64, p, p, p, p]
+    L.orc_mega_moe_tokens.restype = None
+    _lib = L
+    return L
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def fp8_value(code: int, fmt: int) -> float:
+    """Value of one FP8 code (format definition of FLOAT8_E4M3FN / FLOAT8_E5M2)."""
+    return float(_load().orc_fp8_value(code, fmt))
+
+
+def fp8_round(t: float, fmt: int) -> int:
+    """FP8 code of t: saturate, nearest, ties to even, sign kept."""
+    return int(_load().orc_fp8_round(float(t), fmt))
+
+
+def fp8_round_array(t, fmt: int) -> np.ndarray:
+    t = np.ascontiguousarray(t, dtype=np.float64)
+    out = np.zeros(t.shape, dtype=np.uint8)
+    _load().orc_fp8_round_array(_ptr(t), t.size, fmt, _ptr(out))
+    return out
+
+
+def bf16_round(t: float) -> int:
+    return int(_load().orc_bf16_round(float(t)))
+
+
+def mx_block(v, fmt: int):
+    """Q_MX of one group (MegaMoE A8W8-FP stage 1): returns (codes uint8[n], scale code)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    q = np.zeros(v.size, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.uint8)
+    _load().orc_mx_block(_ptr(v), v.size, fmt, _ptr(q), _ptr(s))
+    return q, int(s[0])
+
+
+def mx_quantize_f64(x: np.ndarray, fmt: int, s_cols: int | None = None):
+    """Q_MX along the last axis of a 2-D double matrix; scales [rows, s_cols]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, cols = x.shape
+    s_cols = (cols + 31) // 32 if s_cols is None else s_cols
+    q = np.zeros((rows, cols), dtype=np.uint8)
+    s = np.zeros((rows, s_cols), dtype=np.uint8)
+    _load().orc_mx_quantize_rows(_ptr(x), rows, cols, fmt, _ptr(q), _ptr(s), s_cols)
+    return q, s
+
+
+def mx_quantize(x: np.ndarray, dtype: int, fmt: int, s_cols: int | None = None):
+    """Q_MX along the last axis of a 2-D matrix given as fp32 (float32 array)
+    or as bf16 / fp16 bit patterns (uint16 array, dtype DT_BF16 / DT_F16)."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    s_cols = (cols + 31) // 32 if s_cols is None else s_cols
+    q = np.zeros((rows, cols), dtype=np.uint8)
+    s = np.zeros((rows, s_cols), dtype=np.uint8)
+    _load().orc_mx_quantize_src(_ptr(x), dtype, rows, cols, fmt, _ptr(q), _ptr(s), s_cols)
+    return q, s
+
+
+def route(ids: np.ndarray, num_experts: int):
+    """keyValueSort + inverse map + histogram (MoeInitRoutingV3 steps 1-3).
+
+    Returns (sorted_row_idx int32[R], expanded_row_idx int32[R], counts int64[E], n_invalid).
+    """
+    ids = np.ascontiguousarray(ids)
+    is64 = 1 if ids.dtype == np.int64 else 0
+    if not is64:
+        ids = ids.astype(np.int32, copy=False)
+    n = ids.shape[0]
+    k = ids.shape[1] if ids.ndim == 2 else 1
+    rows = n * k
+    srt = np.empty(rows, dtype=np.int32)
+    exp = np.empty(rows, dtype=np.int32)
+    cnt = np.empty(num_experts, dtype=np.int64)
+    bad = _load().orc_route(_ptr(ids), is64, n, k, num_experts, _ptr(srt), _ptr(exp), _ptr(cnt))
+    return srt, exp, cnt, int(bad)
+
+
+def permute(x: np.ndarray, dtype: int, k: int, sorted_row_idx: np.ndarray, m_out: int, fmt: int = -1):
+    """Gather (+ optional Q_MX) of token rows in sorted order (MoeInitRoutingV3
+    step 5 / moe_token_permute).  fmt = -1 copies; 23 / 24 quantise with
+    scales [m_out, AlignUp(CeilDiv(H, 32), 2)]."""
+    x = np.ascontiguousarray(x)
+    h = x.shape[1]
+    srt = np.ascontiguousarray(sorted_row_idx, dtype=np.int32)
+    s_cols = ((h + 31) // 32 + 1) // 2 * 2
+    if fmt < 0:
+        out = np.zeros((m_out, h), dtype=x.dtype)
+        sc = np.zeros((0,), dtype=np.uint8)
+        _load().orc_permute(_ptr(x), dtype, h, k, _ptr(srt), m_out, -1, _ptr(out), None, 0)
+    else:
+        out = np.zeros((m_out, h), dtype=np.uint8)
+        sc = np.zeros((m_out, s_cols), dtype=np.uint8)
+        _load().orc_permute(_ptr(x), dtype, h, k, _ptr(srt), m_out, fmt, _ptr(out), _ptr(sc), s_cols)
+    return out, sc
+
+
+def expert_row(xq, xs, x_fmt, w1, s1, w2, s2, w_fmt, a_fmt):
+    """One expanded row through one expert (A8W8-FP stages 2-3, swiglu).
+
+    xq uint8[H], xs uint8[H/32]; w1 [2I, H], s1 [2I, 2*ceil(H/64)];
+    w2 [H, I], s2 [H, 2*ceil(I/64)].  Returns (aq uint8[I], as uint8[I/32], o float64[H]).
+    """
+    h = xq.size
+    inter = w2.shape[1]
+    aq = np.zeros(inter, dtype=np.uint8)
+    a_s = np.zeros((inter + 31) // 32, dtype=np.uint8)
+    o = np.zeros(h, dtype=np.float64)
+    arrs = [np.ascontiguousarray(a) for a in (xq, xs, w1, s1, w2, s2)]
+    _load().orc_expert_row(_ptr(arrs[0]), _ptr(arrs[1]), x_fmt, _ptr(arrs[2]), _ptr(arrs[3]),
+                           _ptr(arrs[4]), _ptr(arrs[5]), w_fmt, h, inter, a_fmt, _ptr(aq), _ptr(a_s),
+                           _ptr(o))
+    return aq, a_s, o
+
+
+def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None,
+                    shared=None, shared_w_fmt=None, want_act=False):
+    """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP stages 1-4).
+
+    x_bf16 uint16[N, H]; ids int32[N, K]; gate float32[N, K] or bf16 bits uint16[N, K];
+    w1 uint8[E, 2I, H], s1 uint8[E, 2I, 2*ceil(H/64)], w2 uint8[E, H, I],
+    s2 uint8[E, H, 2*ceil(I/64)]; shared = (sw1, ss1, sw2, ss2) with a leading
+    shared-expert dimension, or None.
+    Returns (y float64[T, H], y_bf16 uint16[T, H]) and, with want_act, the
+    activation codes uint8[T, K, I] and scales uint8[T, K, I/32].
+    """
+    n, h = x_bf16.shape
+    k = ids.shape[1]
+    e, two_i, _ = w1.shape
+    inter = two_i // 2
+    tokens = np.arange(n, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    t = tokens.size
+    y = np.zeros((t, h), dtype=np.float64)
+    yb = np.zeros((t, h), dtype=np.uint16)
+    gate = np.ascontiguousarray(gate)
+    gate_is_bf16 = 1 if gate.dtype == np.uint16 else 0
+    if shared is None:
+        sw = [None] * 4
+        n_sh = 0
+        shared_w_fmt = w_fmt
+    else:
+        sw = [np.ascontiguousarray(a) for a in shared]
+        n_sh = sw[0].shape[0]
+        shared_w_fmt = w_fmt if shared_w_fmt is None else shared_w_fmt
+    aq = np.zeros((t, k, inter), dtype=np.uint8) if want_act else None
+    a_s = np.zeros((t, k, (inter + 31) // 32), dtype=np.uint8) if want_act else None
+    arrs = [np.ascontiguousarray(a) for a in (x_bf16, ids.astype(np.int32, copy=False), w1, s1, w2, s2)]
+    _load().orc_mega_moe_tokens(
+        _ptr(arrs[0]), _ptr(arrs[1]), _ptr(gate), gate_is_bf16, _ptr(arrs[2]), _ptr(arrs[3]),
+        _ptr(arrs[4]), _ptr(arrs[5]), _ptr(sw[0]), _ptr(sw[1]), _ptr(sw[2]), _ptr(sw[3]), n_sh, h, k,
+        e, inter, x_fmt, w_fmt, shared_w_fmt, _ptr(tokens), t, _ptr(y), _ptr(yb), _ptr(aq), _ptr(a_s))
+    if want_act:
+        return y, yb, aq, a_s
+    return y, yb
+
+
+def quantized_weights(cfg, which: int, shared: bool = False, fmt: int | None = None):
+    """fp32 N(0, 0.02) source weights of every expert (seeded generator) MX-quantised
+    by the oracle along the reduction dimension.  Returns (codes [E, N_out, K_red],
+    scales [E, N_out, 2*ceil(K_red/64)]) in the MegaMoE weight / weightScales layouts."""
+    import synth
+    fmt = cfg.weight_fmt if fmt is None else fmt
+    n_exp = cfg.shared if shared else cfg.e
+    if which == 1:
+        n_out, k_red = 2 * cfg.inter, cfg.h
+    else:
+        n_out, k_red = cfg.h, cfg.inter
+    s_cols = 2 * ((k_red + 63) // 64)
+    q = np.empty((n_exp, n_out, k_red), dtype=np.uint8)
+    s = np.empty((n_exp, n_out, s_cols), dtype=np.uint8)
+    for ex in range(n_exp):
+        w = synth.weight_f32(cfg, which, ex, shared=shared)
+        q[ex], s[ex] = mx_quantize(w, DT_F32, fmt, s_cols)
+    return q, s

@@ -1,0 +1,353 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No test here compares the oracle with itself or with the CUDA path: FP8
+values come from torch's float8 decode, rounding from an exhaustive code
+search, sorts from numpy's stable argsort, GEMMs from numpy matmul, the
+worked example and the hand-computed MX blocks from tests/golden/.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+import synth
+from tests import _pins as P
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FMTS = [P.E4M3, P.E5M2]
+
+
+# ---------------------------------------------------------------- FP8 codes
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_decode_matches_torch(fmt):
+    tab = P.fp8_table(fmt)
+    for c in range(256):
+        v = oracle.fp8_value(c, fmt)
+        if np.isnan(tab[c]):
+            assert np.isnan(v), c
+        else:
+            assert v == tab[c], (c, v, tab[c])
+
+
+def test_fp8_closed_forms():
+    # largest finite values, smallest subnormals, one, infinities / NaN
+    assert oracle.fp8_value(0x7E, P.E4M3) == 448.0
+    assert oracle.fp8_value(0x01, P.E4M3) == 2.0 ** -9
+    assert oracle.fp8_value(0x08, P.E4M3) == 2.0 ** -6
+    assert oracle.fp8_value(0x38, P.E4M3) == 1.0
+    assert np.isnan(oracle.fp8_value(0x7F, P.E4M3))
+    assert oracle.fp8_value(0x7B, P.E5M2) == 57344.0
+    assert oracle.fp8_value(0x01, P.E5M2) == 2.0 ** -16
+    assert oracle.fp8_value(0x3C, P.E5M2) == 1.0
+    assert oracle.fp8_value(0x7C, P.E5M2) == np.inf
+
+
+def _hard_values(fmt, n, seed):
+    rng = np.random.default_rng(seed)
+    tab = P.fp8_table(fmt)
+    fin = np.sort(np.unique(np.abs(tab[np.isfinite(tab)])))
+    mids = (fin[1:] + fin[:-1]) / 2                      # exact ties
+    near = np.concatenate([mids * (1 + 1e-12), mids * (1 - 1e-12)])
+    mag = np.exp2(rng.uniform(-24, np.log2(P.MAXV[fmt]) + 1, n))
+    rnd = mag * rng.choice([-1.0, 1.0], n)
+    special = np.array([0.0, -0.0, P.MAXV[fmt], -P.MAXV[fmt], P.MAXV[fmt] * 1.07, 1e30, -1e30,
+                        2.0 ** -30, -(2.0 ** -30)])
+    grid = np.concatenate([fin, -fin])
+    allv = np.concatenate([rnd, mids, -mids, near, -near, grid, special])
+    return allv
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_round_brute_force(fmt):
+    t = _hard_values(fmt, 1_000_000, 1 + fmt)
+    got = oracle.fp8_round_array(t, fmt)
+    want = P.brute_round(t, fmt)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(t[i], got[i], want[i]) for i in bad[:10]]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_round_matches_torch_in_range(fmt):
+    rng = np.random.default_rng(7)
+    t = rng.uniform(-P.MAXV[fmt], P.MAXV[fmt], 200_000).astype(np.float32)
+    t = np.concatenate([t, (t / 1e3).astype(np.float32), (t / 1e6).astype(np.float32)])
+    want = torch.from_numpy(t).to(P._TORCH[fmt]).view(torch.uint8).numpy()
+    got = oracle.fp8_round_array(t.astype(np.float64), fmt)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------ MX quantiser
+def _golden_blocks():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "mx_blocks.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        fmt, sc, vals, codes = [f.strip() for f in line.split("|")]
+        rows.append((int(fmt), int(sc), [float(v) for v in vals.split()],
+                     [int(c, 16) for c in codes.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("block", _golden_blocks())
+def test_mx_hand_blocks(block):
+    fmt, sc, vals, codes = block
+    v = np.zeros(32)
+    v[: len(vals)] = vals
+    q, s = oracle.mx_block(v, fmt)
+    assert s == sc
+    assert list(q[: len(codes)]) == codes
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_scale_puts_amax_in_top_binade(fmt):
+    """With s = code - 127, amax * 2^-s lies in [2^emax, 2^(emax+1)) unless the
+    scale is clamped: the group's largest element uses the format's top binade."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4000, 32)) * np.exp2(rng.integers(-40, 40, (4000, 1)))
+    for r in range(x.shape[0]):
+        _, s = oracle.mx_block(x[r], fmt)
+        t = np.abs(x[r]).max() * 2.0 ** -(s - 127)
+        top = {P.E4M3: 256.0, P.E5M2: 32768.0}[fmt]
+        assert top <= t < 2 * top
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_roundtrip_bound(fmt):
+    """|DQ(Q(v)) - v| <= half the local FP8 spacing times 2^s for unsaturated
+    elements; saturated ones decode to the largest finite value."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((2000, 32)) * np.exp2(rng.integers(-10, 10, (2000, 1)))
+    tab = P.fp8_table(fmt)
+    fin = np.sort(np.unique(np.abs(tab[np.isfinite(tab)])))
+    for r in range(x.shape[0]):
+        q, s = oracle.mx_block(x[r], fmt)
+        sc = 2.0 ** (s - 127)
+        t = np.abs(x[r]) / sc
+        back = np.abs(tab[q])
+        for ti, bi in zip(t, back):
+            if ti >= P.MAXV[fmt]:
+                assert bi == P.MAXV[fmt]
+                continue
+            i = np.searchsorted(fin, ti)
+            lo = fin[max(i - 1, 0)]
+            hi = fin[min(i, fin.size - 1)]
+            assert abs(bi - ti) <= (hi - lo) / 2 + 1e-300
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_rows_match_brute_force(fmt):
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((64, 256)) * np.exp2(rng.integers(-6, 6, (64, 1)))
+    x[3, 32:64] = 0.0
+    x[4, :32] = -0.0
+    q, s = oracle.mx_quantize_f64(x, fmt)
+    qb, sb = P.brute_mx_rows(x, fmt)
+    assert np.array_equal(s, sb)
+    assert np.array_equal(q, qb)
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(2)
+    t = (rng.standard_normal(100_000) * np.exp2(rng.integers(-60, 60, 100_000))).astype(np.float32)
+    want = torch.from_numpy(t).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_round(float(v)) for v in t[:20000]], dtype=np.uint16)
+    assert np.array_equal(got, want[:20000])
+
+
+# ------------------------------------------------------------------ routing
+def test_route_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "permute_example.json")))
+    ids = np.array(g["indices"], dtype=np.int32)
+    srt, exp, cnt, bad = oracle.route(ids, 2)
+    assert bad == 0
+    assert srt.tolist() == g["sorted_indices_first"]
+    assert exp.tolist() == g["sorted_indices"]
+    assert cnt.tolist() == g["counts"]
+    assert (srt // ids.shape[1]).tolist() == g["source_tokens"]
+    # shapes printed by the page
+    x = np.arange(4 * g["hidden"], dtype=np.uint16).reshape(4, g["hidden"])
+    out, sc = oracle.permute(x, oracle.DT_F16, 2, srt, g["num_out_tokens"])
+    assert list(out.shape) == g["shape_permuted_truncated"]
+    assert list(exp.shape) == g["shape_sorted_indices"]
+    assert list(sc.shape) == g["shape_scale_unquantized"]
+    out, sc = oracle.permute(x, oracle.DT_F16, 2, srt, 8, fmt=P.E5M2)
+    assert list(out.shape) == g["shape_permuted_mxfp8"]
+    assert list(sc.shape) == g["shape_scale_mxfp8"]
+
+
+@pytest.mark.parametrize("n,k,e,distinct", [(1000, 8, 64, True), (777, 4, 5, False), (1, 1, 1, True),
+                                            (4096, 8, 256, True)])
+def test_route_matches_numpy_stable_argsort(n, k, e, distinct):
+    rng = np.random.default_rng(n + k + e)
+    if distinct:
+        ids = np.argsort(rng.random((n, e)), axis=1)[:, :k].astype(np.int32)
+    else:
+        ids = rng.integers(0, e, (n, k)).astype(np.int32)
+    srt, exp, cnt, bad = oracle.route(ids, e)
+    flat = ids.reshape(-1)
+    want = np.argsort(flat, kind="stable")
+    assert bad == 0
+    assert np.array_equal(srt, want)
+    inv = np.empty_like(want)
+    inv[want] = np.arange(want.size)
+    assert np.array_equal(exp, inv)
+    assert np.array_equal(cnt, np.bincount(flat, minlength=e))
+    # invariants: permutation, sorted keys, stability, totals
+    assert np.array_equal(np.sort(srt), np.arange(n * k))
+    keys = flat[srt]
+    assert np.all(np.diff(keys) >= 0)
+    same = np.diff(keys) == 0
+    assert np.all(np.diff(srt)[same] > 0)
+    assert cnt.sum() == n * k
+
+
+def test_route_int64_and_invalid_ids():
+    ids = np.array([[0, 5], [2, -1], [1, 0]], dtype=np.int64)
+    srt, exp, cnt, bad = oracle.route(ids, 3)
+    assert bad == 2
+    assert srt.tolist() == [0, 5, 4, 2, -1, -1]
+    assert exp.tolist() == [0, -1, 3, -1, 2, 1]
+    assert cnt.tolist() == [2, 1, 1]
+
+
+# ------------------------------------------------------------------ permute
+@pytest.mark.parametrize("fmt", [-1, P.E4M3, P.E5M2])
+def test_permute_matches_gather(fmt):
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, h=160)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    srt, exp, cnt, _ = oracle.route(ids, cfg.e)
+    m = cfg.rows - 7
+    out, sc = oracle.permute(x, oracle.DT_BF16, cfg.k, srt, m, fmt=fmt)
+    src = x[srt[:m] // cfg.k]
+    if fmt < 0:
+        assert np.array_equal(out, src)
+        return
+    qb, sb = P.brute_mx_rows(P.bf16_bits_to_f64(src), fmt)
+    assert np.array_equal(out, qb)
+    g = (cfg.h + 31) // 32
+    assert sc.shape == (m, (g + 1) // 2 * 2)
+    assert np.array_equal(sc[:, :g], sb)
+    assert np.all(sc[:, g:] == 0)
+
+
+# ---------------------------------------------------------------- expert FFN
+def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None):
+    """Grouped-by-expert FFN with numpy matmuls on dequantised operands, from
+    the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort."""
+    (w1, s1, w2, s2) = w
+    fx = cfg.dispatch_fmt
+    xq, xs = P.brute_mx_rows(P.bf16_bits_to_f64(x), fx)
+    n, h = x.shape
+    k = ids.shape[1]
+    inter = cfg.inter
+    order = np.argsort(ids.reshape(-1), kind="stable")
+    pos = np.empty_like(order)
+    pos[order] = np.arange(order.size)
+    rows = order // k
+    o_all = np.zeros((order.size, h))
+    aq_all = np.zeros((order.size, inter), dtype=np.uint8)
+
+    def ffn(rows_q, rows_s, W1, S1, W2, S2, wfmt):
+        xd = P.dequant_rows(rows_q, rows_s, fx)
+        w1d = P.dequant_rows(W1, S1, wfmt)
+        hv = xd @ w1d.T
+        g, u = hv[:, :inter], hv[:, inter:]
+        a = (g * expit(g) * u).astype(np.float32).astype(np.float64)
+        aq, a_s = P.brute_mx_rows(a, fx)
+        o = P.dequant_rows(aq, a_s, fx) @ P.dequant_rows(W2, S2, wfmt).T
+        return aq, o
+
+    flat = ids.reshape(-1)[order]
+    for e in range(cfg.e):
+        sel = np.nonzero(flat == e)[0]
+        if sel.size == 0:
+            continue
+        aq, o = ffn(xq[rows[sel]], xs[rows[sel]], w1[e], s1[e], w2[e], s2[e], cfg.weight_fmt)
+        o_all[sel] = o
+        aq_all[sel] = aq
+    gw = P.bf16_bits_to_f64(gate) if gate.dtype == np.uint16 else gate.astype(np.float64)
+    y = np.zeros((n, h))
+    for kk in range(k):
+        y += gw[:, kk:kk + 1] * o_all[pos.reshape(n, k)[:, kk]]
+    if shared is not None:
+        for s in range(shared[0].shape[0]):
+            _, o = ffn(xq, xs, shared[0][s], shared[1][s], shared[2][s], shared[3][s], cfg.weight_fmt)
+            y += o
+    return y, aq_all[pos.reshape(n, k)]
+
+
+def _weights(cfg, shared=False):
+    w1, s1 = oracle.quantized_weights(cfg, 1, shared=shared)
+    w2, s2 = oracle.quantized_weights(cfg, 2, shared=shared)
+    return w1, s1, w2, s2
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}),
+    ("tiny", dict(dispatch_fmt=P.E5M2, gate_dtype="bf16", routing="zipf")),
+    ("tiny", dict(n=16, shared=1)),
+    ("tiny", dict(n=24, e=1, k=1)),     # K = 1, one expert: a dense two-layer FFN
+])
+def test_mega_moe_matches_numpy_grouped(name, kw):
+    cfg = synth.CONFIGS[name].scaled(**kw)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    if cfg.e == 1:
+        gate = np.ones_like(gate, dtype=np.float32)
+    w = _weights(cfg)
+    sh = _weights(cfg, shared=True) if cfg.shared else None
+    y, yb, aq, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt,
+                                          shared=sh, want_act=True)
+    y_ref, aq_ref = _numpy_grouped_moe(cfg, x, ids, gate, w, shared=sh)
+    assert np.array_equal(aq, aq_ref)
+    scale = np.abs(y_ref).max()
+    assert np.max(np.abs(y - y_ref)) <= 1e-11 * scale
+    want_b = torch.from_numpy(y_ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    got_b = P.bf16_bits_to_f64(yb)
+    assert np.max(np.abs(got_b - want_b)) <= 2.0 ** -8 * np.abs(want_b).max()
+
+
+def test_mega_moe_metamorphic():
+    cfg = synth.CONFIGS["tiny"].scaled(n=32)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    w = _weights(cfg)
+    y, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt)
+    perm = np.random.default_rng(0).permutation(cfg.n)
+    yp, _ = oracle.mega_moe_tokens(x[perm], ids[perm], gate[perm], *w, cfg.dispatch_fmt, cfg.weight_fmt)
+    assert np.array_equal(yp, y[perm])
+    y2, _ = oracle.mega_moe_tokens(x, ids, gate * 2, *w, cfg.dispatch_fmt, cfg.weight_fmt)
+    assert np.array_equal(y2, 2 * y)
+    sub = np.array([5, 0, 31])
+    ys, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, tokens=sub)
+    assert np.array_equal(ys, y[sub])
+
+
+def test_swiglu_special_values():
+    """Row with G = 0 gives A = 0; the silu reading is z / (1 + e^-z)."""
+    cfg = synth.CONFIGS["tiny"].scaled(e=1, k=1, n=1)
+    h, inter = cfg.h, cfg.inter
+    s_cols1, s_cols2 = 2 * ((h + 63) // 64), 2 * ((inter + 63) // 64)
+    xq = np.full(h, 0x38, dtype=np.uint8)          # 1.0
+    xs = np.full(h // 32, 127, dtype=np.uint8)
+    w1 = np.zeros((2 * inter, h), dtype=np.uint8)
+    w1[inter:, 0] = 0x38                             # up row = x[0] = 1, gate = 0
+    w1[0, 0] = 0x40                                  # gate[0] = 2
+    s1 = np.full((2 * inter, s_cols1), 127, dtype=np.uint8)
+    w2 = np.zeros((h, inter), dtype=np.uint8)
+    w2[:, 0] = 0x38
+    s2 = np.full((h, s_cols2), 127, dtype=np.uint8)
+    aq, a_s, o = oracle.expert_row(xq, xs, P.E4M3, w1, s1, w2, s2, P.E4M3, P.E4M3)
+    a0 = np.float32(2.0 * expit(2.0))
+    assert np.all(P.fp8_table(P.E4M3)[aq[1:32]] == 0)
+    deq = P.fp8_table(P.E4M3)[aq[0]] * 2.0 ** (int(a_s[0]) - 127)
+    assert abs(deq - a0) <= a0 * 2 ** -3
+    assert np.allclose(o, deq)
