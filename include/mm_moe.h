@@ -1,0 +1,251 @@
+/*
+ * mm_moe.h -- C ABI of the GB300 (sm_103a) MoE routing / permute / MXFP8
+ * expert-FFN library (libmm_moe.so).
+ *
+ * Operations and the pages that define them:
+ *   mm_moe_init_routing   MoeInitRoutingV3 (CANN ops-transformer,
+ *                         moe/moe_init_routing_v3): "计算公式" steps 1-3 and 5,
+ *                         parameter table (quantMode, expertTokensNumType,
+ *                         rowIdxType, expandedScaleOut).
+ *   mm_moe_token_permute  moe_token_permute article ("CANN ops-transformer 的
+ *                         moe_token_permute 算子"): sections 功能说明,
+ *                         参数说明, 返回值说明, 约束说明.
+ *   mm_mega_moe           MegaMoE README (ops-transformer, mc2/mega_moe):
+ *                         "A8W8-FP quantization scenario" stages 1-4,
+ *                         "Activation function formulas" (swiglu), parameter
+ *                         table and the MXFP constraints on weight shapes;
+ *                         run at epWorldSize = 1, so dispatch and combine are
+ *                         a local permute and a local weighted sum.
+ *   mm_mx_quantize        the Q_MX operation of the same README (group 32,
+ *                         shared E8M0 exponent, FP8 elements).
+ *
+ * Conventions shared by every entry point
+ *   Memory     every pointer is a device pointer unless stated otherwise.
+ *              The caller owns every buffer; the library allocates no device
+ *              memory.  Entry points that need scratch memory say how much
+ *              through a *_workspace_size query; the caller passes a device
+ *              buffer of at least that many bytes, 256-byte aligned.
+ *   Streams    `stream` is a cudaStream_t (NULL = legacy default stream).
+ *              All work is enqueued asynchronously on it; the call returns
+ *              before the GPU finishes.  Calls on one stream may reuse one
+ *              workspace; concurrent calls need separate workspaces.
+ *   Errors     the return value is checked before anything is enqueued:
+ *              invalid shapes or codes give MM_ERR_INVALID_ARG, valid but
+ *              unimplemented options MM_ERR_UNSUPPORTED, a short workspace
+ *              MM_ERR_WORKSPACE (nothing is truncated silently), a failed
+ *              CUDA call MM_ERR_CUDA.  Data-dependent problems found on the
+ *              GPU are OR-ed as MM_DEVERR_* bits into *dev_err (an int32 in
+ *              device memory, may be NULL); kernels never trap.
+ *   Flatten    the expanded row j of token i and choice k is j = i*K + k
+ *              (row-major flatten of the [N, K] index matrix).
+ *   Layouts    all matrices are row-major and dense.
+ */
+#ifndef MM_MOE_H_
+#define MM_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,
+  MM_ERR_UNSUPPORTED = 2,
+  MM_ERR_WORKSPACE = 3,
+  MM_ERR_CUDA = 4
+} mm_status;
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define MM_DEVERR_EXPERT_RANGE 1 /* an expert id outside [0, expert_num): row left out */
+#define MM_DEVERR_DUPLICATE_ID 2 /* a token lists one expert twice (MegaMoE forbids it) */
+#define MM_DEVERR_TIMEOUT 4      /* a bounded wait inside a kernel gave up */
+
+/* Element type codes.  The FP8 codes are the MegaMoE dtype codes
+ * (dispatchQuantOutDtype: 23 = FLOAT8_E5M2, 24 = FLOAT8_E4M3FN). */
+#define MM_DT_FLOAT32 0
+#define MM_DT_FLOAT16 1
+#define MM_DT_INT32 3
+#define MM_DT_INT64 9
+#define MM_DT_FP8_E5M2 23
+#define MM_DT_FP8_E4M3FN 24
+#define MM_DT_BFLOAT16 27
+
+/* Quant-mode codes of moe_token_permute and MoeInitRoutingV3:
+ * -1 none, 2 MXFP8 E5M2, 3 MXFP8 E4M3FN (9, MXFP4, is not implemented). */
+#define MM_QUANT_NONE (-1)
+#define MM_QUANT_MXFP8_E5M2 2
+#define MM_QUANT_MXFP8_E4M3FN 3
+
+/* Layouts of the E8M0 weight scales passed to mm_mega_moe. */
+#define MM_WSCALE_ROWS 0     /* the pages' (E, N_out, CeilDiv(K_red, 64), 2) */
+#define MM_WSCALE_PREPARED 1 /* output of mm_prepare_weight_scales */
+
+/* Human-readable name of a status code (static string). */
+const char* mm_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mm_version(void);
+
+/* ------------------------------------------------------------------------
+ * mm_moe_init_routing -- MoeInitRoutingV3, Dropless, active expert range
+ * [0, expert_num), quantMode -1 / 2 / 3.
+ *
+ *   sortedRowIdx          = keyValueSort(expertIdx, rowIdx)      (step 1)
+ *   expandedRowIdx[sortedRowIdx[d]] = d                           (step 2)
+ *   expert_tokens         = histogram of the sorted ids           (step 3)
+ *   expandedX[d]          = Q(x[sortedRowIdx[d] / K])             (step 5)
+ * Ties in the sort keep ascending j (a stable sort), so rows of one expert
+ * are in ascending token order.
+ *
+ * x                 [num_rows, h] of x_dtype (bf16 / fp16 / fp32; quantised
+ *                   modes take bf16 or fp16).  Row size in bytes must be a
+ *                   multiple of 16.
+ * expert_idx        [num_rows, k] int32, values in [0, expert_num).
+ * quant_mode        MM_QUANT_NONE (expanded_x has x's type) or an MXFP8 mode
+ *                   (expanded_x FP8, h a multiple of 16).
+ * expert_tokens_num_type  0: expert_tokens is the inclusive cumsum of the
+ *                   counts; 1: the counts (expertTokensNumType 0 / 1).
+ * expanded_x        [num_rows*k, h] output.
+ * expanded_scale    [num_rows*k, AlignUp(CeilDiv(h, 32), 2)] E8M0 output in
+ *                   MXFP8 modes (padding column 0); ignored otherwise.
+ * expanded_row_idx  [num_rows*k] int32 scatter index (rowIdxType 1), or NULL.
+ * sorted_row_idx    [num_rows*k] int32 gather index (rowIdxType 0), or NULL.
+ * expert_tokens     [expert_num] int64, or NULL.
+ * Rows whose id is out of range are left out: their expanded_row_idx is -1,
+ * the tail of sorted_row_idx is -1, the matching tail rows of expanded_x are
+ * not written, and MM_DEVERR_EXPERT_RANGE is raised.
+ * Limits: num_rows*k < 16777215 (the sort limit of the permute article),
+ * 1 <= expert_num <= 10240.
+ * ---------------------------------------------------------------------- */
+mm_status mm_moe_init_routing_workspace_size(int64_t num_rows, int64_t k, int64_t expert_num,
+                                             size_t* bytes);
+mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_idx,
+                              int64_t num_rows, int64_t h, int64_t k, int64_t expert_num,
+                              int quant_mode, int expert_tokens_num_type, void* expanded_x,
+                              uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                              int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mm_moe_token_permute -- moe_token_permute with padded_mode = false.
+ *
+ *   sortedIndicesFirst = stable argSort(indices.flatten())
+ *   sorted_indices     = argSort(sortedIndicesFirst)   (the inverse map)
+ *   permuted[d]        = Q(tokens[sortedIndicesFirst[d] / topk]),  d < M
+ *
+ * tokens          [n, h] of tokens_dtype (fp16 / bf16 / fp32; quantised modes
+ *                 take fp16 / bf16).
+ * indices         [n, topk] (topk = 1 for 1-D indices) of indices_dtype
+ *                 (MM_DT_INT32 / MM_DT_INT64), values in [0, num_experts).
+ * num_experts     exclusive upper bound of the index values.  The article's
+ *                 API infers it from the data; here the caller states it
+ *                 (the counting sort needs the key range).
+ * num_out_tokens  0: M = F = n*topk; > 0: M = min(num_out_tokens, F);
+ *                 < 0: M = max(F + num_out_tokens, 0).
+ * padded_mode     must be 0 (MM_ERR_UNSUPPORTED otherwise, as in the article).
+ * quant_mode      MM_QUANT_NONE, MM_QUANT_MXFP8_E5M2, MM_QUANT_MXFP8_E4M3FN.
+ * permuted_tokens [M, h] output (tokens' type, or FP8).
+ * expanded_scale  [M, AlignUp(CeilDiv(h, 32), 2)] E8M0 output (MXFP8 modes).
+ * sorted_indices  [F] int32 output, never truncated.
+ * Limits: F < 16777215.
+ * ---------------------------------------------------------------------- */
+int64_t mm_moe_token_permute_out_rows(int64_t num_indices, int64_t num_out_tokens);
+mm_status mm_moe_token_permute_workspace_size(int64_t num_indices, int64_t num_experts,
+                                              size_t* bytes);
+mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void* indices,
+                               int indices_dtype, int64_t n, int64_t topk, int64_t h,
+                               int64_t num_experts, int64_t num_out_tokens, int padded_mode,
+                               int quant_mode, void* permuted_tokens, uint8_t* expanded_scale,
+                               int32_t* sorted_indices, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mm_mega_moe -- MegaMoE, A8W8-FP scenario, epWorldSize = 1:
+ *
+ *   X_hat_e, S_X,e = Q_MX(x[T_e])                                 stage 1
+ *   G_e = DQ(X_hat_e) DQ(W1_e^(G))^T, U_e = DQ(X_hat_e) DQ(W1_e^(U))^T
+ *   A_e = SiLU(G_e) * U_e,  A_hat_e, S_A,e = Q_MX(A_e)             stage 2
+ *   O_e = DQ(A_hat_e) DQ(W2_e)^T                                  stage 3
+ *   Y[i] = sum_k W[i,k] O[pi(i,k)] + sum_s O_s^shared[i]          stage 4
+ *
+ * x                  [bs, h] bf16.
+ * topk_ids           [bs, k] int32, distinct per token, in [0, moe_expert_num).
+ * topk_weights       [bs, k], topk_weights_dtype MM_DT_FLOAT32 or MM_DT_BFLOAT16.
+ * weight1            [E, 2*intermediate, h] FP8 (weight_dtype 23 / 24); rows
+ *                    [0, I) are the gate (SiLU) branch, [I, 2I) the up branch.
+ * weight2            [E, h, intermediate] FP8 of the same type.
+ * weight_scales1/2   E8M0, MM_WSCALE_ROWS: [E, 2I, CeilDiv(h,64), 2] and
+ *                    [E, h, CeilDiv(I,64), 2]; MM_WSCALE_PREPARED: the
+ *                    outputs of mm_prepare_weight_scales for those arrays.
+ * shared_weight*     same layouts with leading dimension shared_expert_num
+ *                    (0..4; NULL when 0); shared_weight_dtype 23 / 24.
+ * ep_world_size      must be 1.
+ * max_recv_token_num 0, or >= bs*k (the rows this rank receives at ep = 1).
+ * dispatch_quant_mode must be 4 (MX quantisation inside the operator);
+ * dispatch_quant_out_dtype 23 / 24 is also the type of A_hat.
+ * combine_quant_mode must be 0; activation must be "swiglu" (or NULL) with
+ *                    no parameters (clamp disabled).
+ * y                  [bs, h] bf16 output.
+ * expert_token_nums  [E] int32 output (rows per expert), or NULL.
+ * expanded_row_idx   [bs*k] int32 output pi(i, k) (position of row j = i*k+k'
+ *                    in expert-sorted order), or NULL.
+ * act_q, act_scale   optional diagnostic outputs of A_hat in expert-sorted
+ *                    row order: [bs*k, I] FP8 and [bs*k, I/32] E8M0; NULL to skip.
+ * Shape limits: h and intermediate multiples of 128; k <= 32;
+ * moe_expert_num <= 2048.
+ * ---------------------------------------------------------------------- */
+mm_status mm_mega_moe_workspace_size(int64_t bs, int64_t h, int64_t k, int64_t moe_expert_num,
+                                     int64_t intermediate, int64_t shared_expert_num,
+                                     int weight_scale_layout, size_t* bytes);
+mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_weights,
+                      int topk_weights_dtype, const uint8_t* weight1, const uint8_t* weight2,
+                      const uint8_t* weight_scales1, const uint8_t* weight_scales2,
+                      int weight_dtype, int weight_scale_layout, const uint8_t* shared_weight1,
+                      const uint8_t* shared_weight2, const uint8_t* shared_weight_scales1,
+                      const uint8_t* shared_weight_scales2, int shared_weight_dtype,
+                      int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
+                      int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
+                      int64_t max_recv_token_num, int64_t dispatch_quant_mode,
+                      int64_t dispatch_quant_out_dtype, int64_t combine_quant_mode,
+                      const char* activation, const float* activation_params,
+                      int64_t n_activation_params, void* y, int32_t* expert_token_nums,
+                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Weight preparation (one-time, at weight-load time).
+ *
+ * mm_prepare_weight_scales rearranges E8M0 weight scales from the pages'
+ * (E, N_out, CeilDiv(K_red, 64), 2) layout into the tile layout the grouped
+ * GEMMs read (MM_WSCALE_PREPARED), the way the pages require FRACTAL_NZ
+ * weight formats for some scenarios.  src and dst are device buffers;
+ * dst holds mm_prepared_weight_scales_size bytes.  K_red must be a multiple
+ * of 128.
+ * ---------------------------------------------------------------------- */
+mm_status mm_prepared_weight_scales_size(int64_t experts, int64_t n_out, int64_t k_red,
+                                         size_t* bytes);
+mm_status mm_prepare_weight_scales(const uint8_t* src, int64_t experts, int64_t n_out,
+                                   int64_t k_red, uint8_t* dst, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mm_mx_quantize -- Q_MX along each row (MegaMoE A8W8-FP stage 1): groups of
+ * 32 consecutive elements share one E8M0 exponent s = floor(log2 amax) -
+ * emax (8 for E4M3FN, 15 for E5M2), clamped to [-127, 127]; elements are
+ * FP8(v * 2^-s), nearest-even, saturated to the largest finite value.
+ *
+ * src     [rows, cols] of src_dtype (fp32 / bf16 / fp16); cols a multiple of 16.
+ * q       [rows, cols] FP8 output of out_dtype (23 / 24).
+ * scales  [rows, scale_cols] E8M0 output, scale_cols >= CeilDiv(cols, 32);
+ *         columns past CeilDiv(cols, 32) are written as 0.
+ * ---------------------------------------------------------------------- */
+mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t cols, int out_dtype,
+                         uint8_t* q, uint8_t* scales, int64_t scale_cols, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_MOE_H_ */

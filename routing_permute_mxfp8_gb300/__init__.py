@@ -1,0 +1,277 @@
+"""GB300 (sm_103a) MoE routing, token permute with MX quantisation and the
+MXFP8 expert FFN (MegaMoE at ep_world_size = 1).
+
+This module only marshals arguments: it allocates outputs and workspaces as
+torch tensors and calls the C ABI of ``libmm_moe.so`` (declared in
+``include/mm_moe.h``) on the current CUDA stream.  Every step runs in the
+library's CUDA kernels; there is no other implementation to fall back on,
+and every entry point raises if the library is not built or a call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MMError", "lib_path", "load", "mm_version", "mm_moe_init_routing", "mm_moe_token_permute",
+    "mm_mega_moe", "mm_mega_moe_workspace_size", "mm_prepare_weight_scales", "mm_mx_quantize",
+    "DT_FP8_E5M2", "DT_FP8_E4M3FN", "QUANT_NONE", "QUANT_MXFP8_E5M2", "QUANT_MXFP8_E4M3FN",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libmm_moe.so")
+_lib = None
+
+DT_F32, DT_F16, DT_I32, DT_I64, DT_BF16 = 0, 1, 3, 9, 27
+DT_FP8_E5M2, DT_FP8_E4M3FN = 23, 24
+QUANT_NONE, QUANT_MXFP8_E5M2, QUANT_MXFP8_E4M3FN = -1, 2, 3
+WSCALE_ROWS, WSCALE_PREPARED = 0, 1
+
+_TORCH_DT = {torch.float32: DT_F32, torch.float16: DT_F16, torch.bfloat16: DT_BF16,
+             torch.int32: DT_I32, torch.int64: DT_I64,
+             torch.float8_e5m2: DT_FP8_E5M2, torch.float8_e4m3fn: DT_FP8_E4M3FN}
+_FP8_TORCH = {DT_FP8_E5M2: torch.float8_e5m2, DT_FP8_E4M3FN: torch.float8_e4m3fn}
+_QUANT_FMT = {QUANT_MXFP8_E5M2: DT_FP8_E5M2, QUANT_MXFP8_E4M3FN: DT_FP8_E4M3FN}
+
+
+class MMError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libmm_moe.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise MMError(f"{_LIB_PATH} is missing: build it with `python -m routing_permute_mxfp8_gb300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    psz = ctypes.POINTER(ctypes.c_size_t)
+    L.mm_status_string.argtypes, L.mm_status_string.restype = [i32], ctypes.c_char_p
+    L.mm_version.restype = i32
+    L.mm_moe_init_routing_workspace_size.argtypes = [i64, i64, i64, psz]
+    L.mm_moe_init_routing.argtypes = [p, i32, p, i64, i64, i64, i64, i32, i32, p, p, p, p, p, p, sz, p, p]
+    L.mm_moe_token_permute_out_rows.argtypes, L.mm_moe_token_permute_out_rows.restype = [i64, i64], i64
+    L.mm_moe_token_permute_workspace_size.argtypes = [i64, i64, psz]
+    L.mm_moe_token_permute.argtypes = [p, i32, p, i32, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, sz, p, p]
+    L.mm_mega_moe_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, psz]
+    L.mm_mega_moe.argtypes = ([p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
+                               i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, sz, p, p])
+    L.mm_prepared_weight_scales_size.argtypes = [i64, i64, i64, psz]
+    L.mm_prepare_weight_scales.argtypes = [p, i64, i64, i64, p, p]
+    L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
+    for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
+                 "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
+                 "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def mm_version() -> int:
+    return int(load().mm_version())
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load().mm_status_string(status).decode()
+        raise MMError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dt(t) -> int:
+    if t.dtype not in _TORCH_DT:
+        raise MMError(f"unsupported dtype {t.dtype}")
+    return _TORCH_DT[t.dtype]
+
+
+def _scale_cols(h: int) -> int:
+    return ((h + 31) // 32 + 1) // 2 * 2
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise MMError("inputs must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is not None:
+        if workspace.numel() < nbytes:
+            raise MMError(f"workspace holds {workspace.numel()} bytes, {nbytes} needed")
+        return workspace
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def _dev_err(dev_err):
+    return None if dev_err is None else _ptr(dev_err)
+
+
+# --------------------------------------------------------------------------- routing / permute
+def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_NONE,
+                        expert_tokens_num_type: int = 1, *, workspace=None, dev_err=None):
+    """MoeInitRoutingV3 (Dropless, full expert range).
+
+    Returns (expanded_x [N*K, H], expanded_row_idx [N*K] int32 (scatter),
+    expert_tokens [E] int64 (count or cumsum), expanded_scale [N*K, AlignUp(H/32, 2)]
+    uint8 E8M0 (empty without quantisation), sorted_row_idx [N*K] int32 (gather)).
+    """
+    _need_cuda(x, expert_idx)
+    L = load()
+    n, h = x.shape
+    k = expert_idx.shape[1] if expert_idx.dim() == 2 else 1
+    rows = n * k
+    dev = x.device
+    out_dt = x.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
+    expanded_x = torch.empty((rows, h), dtype=out_dt, device=dev)
+    scale = (torch.empty((rows, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
+             else torch.empty((0,), dtype=torch.uint8, device=dev))
+    exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    srt_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    tokens = torch.empty(expert_num, dtype=torch.int64, device=dev)
+    need = ctypes.c_size_t(0)
+    _check(L.mm_moe_init_routing_workspace_size(n, k, expert_num, ctypes.byref(need)), "mm_moe_init_routing")
+    ws = _workspace(need.value, dev, workspace)
+    _check(L.mm_moe_init_routing(_ptr(x), _dt(x), _ptr(expert_idx), n, h, k, expert_num, quant_mode,
+                                 expert_tokens_num_type, _ptr(expanded_x), _ptr(scale) if scale.numel() else None,
+                                 _ptr(exp_idx), _ptr(srt_idx), _ptr(tokens), _ptr(ws), ws.numel(),
+                                 _dev_err(dev_err), _stream(dev)), "mm_moe_init_routing")
+    return expanded_x, exp_idx, tokens, scale, srt_idx
+
+
+def mm_moe_token_permute(tokens, indices, num_experts: int, num_out_tokens=None, padded_mode: bool = False,
+                         quant_mode: int = QUANT_NONE, *, workspace=None, dev_err=None):
+    """moe_token_permute: returns (permuted_tokens [M, H], sorted_indices [F] int32,
+    expanded_scale [M, AlignUp(H/32, 2)] uint8 E8M0 or an empty tensor)."""
+    _need_cuda(tokens, indices)
+    L = load()
+    n, h = tokens.shape
+    topk = indices.shape[1] if indices.dim() == 2 else 1
+    f = indices.numel()
+    nout = 0 if num_out_tokens is None else int(num_out_tokens)
+    m = int(L.mm_moe_token_permute_out_rows(f, nout))
+    dev = tokens.device
+    out_dt = tokens.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
+    permuted = torch.empty((m, h), dtype=out_dt, device=dev)
+    scale = (torch.empty((m, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
+             else torch.empty((0,), dtype=torch.float32, device=dev))
+    sorted_indices = torch.empty(f, dtype=torch.int32, device=dev)
+    need = ctypes.c_size_t(0)
+    _check(L.mm_moe_token_permute_workspace_size(f, num_experts, ctypes.byref(need)), "mm_moe_token_permute")
+    ws = _workspace(need.value, dev, workspace)
+    _check(L.mm_moe_token_permute(_ptr(tokens), _dt(tokens), _ptr(indices), _dt(indices), n, topk, h, num_experts,
+                                  nout, int(bool(padded_mode)), quant_mode,
+                                  _ptr(permuted) if m else None,
+                                  _ptr(scale) if (quant_mode != QUANT_NONE and m) else None,
+                                  _ptr(sorted_indices), _ptr(ws), ws.numel(), _dev_err(dev_err), _stream(dev)),
+           "mm_moe_token_permute")
+    return permuted, sorted_indices, scale
+
+
+# --------------------------------------------------------------------------- MegaMoE
+def mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, intermediate, shared_expert_num=0,
+                               weight_scale_layout=WSCALE_ROWS) -> int:
+    need = ctypes.c_size_t(0)
+    _check(load().mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, intermediate, shared_expert_num,
+                                             weight_scale_layout, ctypes.byref(need)), "mm_mega_moe_workspace_size")
+    return need.value
+
+
+def _fp8_code(t, default):
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return _TORCH_DT[t.dtype]
+    return default
+
+
+def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2, moe_expert_num: int, *,
+                weight_dtype: int = DT_FP8_E4M3FN, weight_scale_layout: int = WSCALE_ROWS,
+                shared_weight1=None, shared_weight2=None, shared_weight_scales1=None, shared_weight_scales2=None,
+                shared_weight_dtype: int | None = None, ep_world_size: int = 1, max_recv_token_num: int = 0,
+                dispatch_quant_mode: int = 4, dispatch_quant_out_dtype: int = DT_FP8_E4M3FN,
+                combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
+                out=None, workspace=None, dev_err=None, want_expanded_row_idx=False, want_act=False):
+    """MegaMoE forward, A8W8-FP, ep_world_size = 1.
+
+    x [BS, H] bf16; topk_ids [BS, K] int32; topk_weights [BS, K] fp32 / bf16;
+    weight1 [E, 2I, H] and weight2 [E, H, I] FP8 (torch float8 or uint8 with
+    weight_dtype); weight_scales1 / 2 uint8 E8M0 in the pages' layout
+    (weight_scale_layout=0) or prepared by mm_prepare_weight_scales (1).
+    Returns (y [BS, H] bf16, expert_token_nums [E] int32) and, on request,
+    expanded_row_idx [BS*K] int32 and A_hat codes / scales in sorted order.
+    """
+    _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
+    L = load()
+    bs, h = x.shape
+    k = topk_ids.shape[1]
+    inter = weight2.shape[2]
+    s_num = 0 if shared_weight1 is None else shared_weight1.shape[0]
+    dev = x.device
+    wdt = _fp8_code(weight1, weight_dtype)
+    swdt = wdt if shared_weight1 is None else _fp8_code(shared_weight1, wdt if shared_weight_dtype is None
+                                                         else shared_weight_dtype)
+    y = out if out is not None else torch.empty((bs, h), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(moe_expert_num, dtype=torch.int32, device=dev)
+    exp_idx = torch.empty(bs * k, dtype=torch.int32, device=dev) if want_expanded_row_idx else None
+    act_q = torch.empty((bs * k, inter), dtype=torch.uint8, device=dev) if want_act else None
+    act_s = torch.empty((bs * k, inter // 32), dtype=torch.uint8, device=dev) if want_act else None
+    need = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, inter, s_num, weight_scale_layout)
+    ws = _workspace(need, dev, workspace)
+    params = list(activation_params)
+    parr = (ctypes.c_float * max(len(params), 1))(*params) if params else None
+    gdt = _dt(topk_weights)
+    _check(L.mm_mega_moe(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), gdt, _ptr(weight1), _ptr(weight2), _ptr(weight_scales1),
+        _ptr(weight_scales2), wdt, weight_scale_layout, _ptr(shared_weight1), _ptr(shared_weight2),
+        _ptr(shared_weight_scales1), _ptr(shared_weight_scales2), swdt, s_num, bs, h, k, moe_expert_num,
+        ep_world_size, inter, max_recv_token_num, dispatch_quant_mode, dispatch_quant_out_dtype,
+        combine_quant_mode, activation.encode() if activation else None, parr, len(params), _ptr(y), _ptr(counts),
+        _ptr(exp_idx), _ptr(act_q), _ptr(act_s), _ptr(ws), ws.numel(), _dev_err(dev_err), _stream(dev)),
+        "mm_mega_moe")
+    res = [y, counts]
+    if want_expanded_row_idx:
+        res.append(exp_idx)
+    if want_act:
+        res += [act_q, act_s]
+    return tuple(res)
+
+
+def mm_prepare_weight_scales(scales, k_red: int):
+    """Rearrange E8M0 weight scales [E, N_out, CeilDiv(K_red, 64), 2] (or [E, N_out, K_red/32])
+    into the tile layout of the grouped GEMMs (weight_scale_layout = 1)."""
+    _need_cuda(scales)
+    L = load()
+    e, n_out = scales.shape[0], scales.shape[1]
+    need = ctypes.c_size_t(0)
+    _check(L.mm_prepared_weight_scales_size(e, n_out, k_red, ctypes.byref(need)), "mm_prepare_weight_scales")
+    dst = torch.empty(need.value, dtype=torch.uint8, device=scales.device)
+    _check(L.mm_prepare_weight_scales(_ptr(scales), e, n_out, k_red, _ptr(dst), _stream(scales.device)),
+           "mm_prepare_weight_scales")
+    return dst
+
+
+def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None = None):
+    """Q_MX along the last dimension of a 2-D fp32 / bf16 / fp16 tensor.
+    Returns (codes [rows, cols] uint8, scales [rows, scale_cols] uint8 E8M0)."""
+    _need_cuda(src)
+    L = load()
+    rows, cols = src.shape
+    sc = _scale_cols(cols) if scale_cols is None else scale_cols
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=src.device)
+    s = torch.empty((rows, sc), dtype=torch.uint8, device=src.device)
+    _check(L.mm_mx_quantize(_ptr(src), _dt(src), rows, cols, out_dtype, _ptr(q), _ptr(s), sc,
+                            _stream(src.device)), "mm_mx_quantize")
+    return q, s

@@ -1,0 +1,487 @@
+// C-ABI entry points of libmm_moe: argument checks (before anything is
+// enqueued), workspace carving and the launch sequence of each operation.
+#include <float.h>
+#include <math.h>
+#include <string.h>
+
+#include "mm_route.cuh"
+
+using namespace mm;
+
+namespace {
+
+constexpr int64_t kSortLimit = 16777215;  // permute article, 约束说明
+
+// Carves 256-byte aligned pieces out of a workspace; with base == nullptr it
+// only adds up the sizes.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(int64_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += (size_t)round_up(count * (int64_t)sizeof(T), 256);
+    return p;
+  }
+};
+
+bool is_src_dtype(int dt) { return dt == MM_DT_BFLOAT16 || dt == MM_DT_FLOAT16 || dt == MM_DT_FLOAT32; }
+int dt_size(int dt) { return dt == MM_DT_FLOAT32 ? 4 : 2; }
+bool is_fp8(int64_t dt) { return dt == MM_DT_FP8_E4M3FN || dt == MM_DT_FP8_E5M2; }
+int quant_fmt(int quant_mode) {
+  return quant_mode == MM_QUANT_MXFP8_E5M2 ? MM_DT_FP8_E5M2
+                                           : (quant_mode == MM_QUANT_MXFP8_E4M3FN ? MM_DT_FP8_E4M3FN : -1);
+}
+mm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MM_OK : MM_ERR_CUDA; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ---- mm_moe_init_routing / mm_moe_token_permute share the routing part ----
+struct RoutingWs {
+  int32_t* hist;
+  int32_t* offsets;
+  int32_t* exp_idx;
+};
+
+RoutingWs carve_routing(Carver& c, const RoutePlan& p) {
+  RoutingWs w;
+  w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
+  w.offsets = c.take<int32_t>(p.num_experts + 1);
+  w.exp_idx = c.take<int32_t>(p.rows);
+  return w;
+}
+
+// ---- mm_mega_moe ----
+struct MegaDims {
+  int64_t bs, h, k, e, inter, s, rows, rows_cap;
+};
+
+struct MegaWs {
+  int32_t *hist, *offsets, *seg_rows, *seg_mprefix, *exp_idx, *pad_row;
+  uint8_t *xq, *xsf, *aq, *asf;
+  __nv_bfloat16* o;
+  uint8_t *wsf1, *wsf2, *swsf1, *swsf2;
+};
+
+MegaDims mega_dims(int64_t bs, int64_t h, int64_t k, int64_t e, int64_t inter, int64_t s) {
+  MegaDims d;
+  d.bs = bs;
+  d.h = h;
+  d.k = k;
+  d.e = e;
+  d.inter = inter;
+  d.s = s;
+  d.rows = bs * k;
+  // each segment pads to whole 128-row tiles
+  d.rows_cap = kBM * (ceil_div(d.rows, kBM) + e) + s * round_up(bs, kBM);
+  return d;
+}
+
+MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_layout) {
+  MegaWs w;
+  const int64_t nseg = d.e + d.s;
+  w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
+  w.offsets = c.take<int32_t>(d.e + 1);
+  w.seg_rows = c.take<int32_t>(nseg);
+  w.seg_mprefix = c.take<int32_t>(nseg + 1);
+  w.exp_idx = c.take<int32_t>(d.rows);
+  w.pad_row = c.take<int32_t>(d.rows);
+  w.xq = c.take<uint8_t>(d.rows_cap * d.h);
+  w.xsf = c.take<uint8_t>(d.rows_cap / kBM * (d.h / 128) * kSfChunk);
+  w.aq = c.take<uint8_t>(d.rows_cap * d.inter);
+  w.asf = c.take<uint8_t>(d.rows_cap / kBM * (d.inter / 128) * kSfChunk);
+  w.o = c.take<__nv_bfloat16>(d.rows_cap * d.h);
+  w.wsf1 = w.wsf2 = w.swsf1 = w.swsf2 = nullptr;
+  if (wscale_layout == MM_WSCALE_ROWS) {
+    w.wsf1 = c.take<uint8_t>(d.e * prepared_nblocks(2 * d.inter) * (d.h / 128) * kSfChunk);
+    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h) * (d.inter / 128) * kSfChunk);
+    if (d.s > 0) {
+      w.swsf1 = c.take<uint8_t>(d.s * prepared_nblocks(2 * d.inter) * (d.h / 128) * kSfChunk);
+      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h) * (d.inter / 128) * kSfChunk);
+    }
+  }
+  return w;
+}
+
+mm_status check_mega_shapes(int64_t bs, int64_t h, int64_t k, int64_t e, int64_t inter, int64_t s) {
+  if (bs < 0 || h <= 0 || k <= 0 || e <= 0 || inter <= 0 || s < 0) return MM_ERR_INVALID_ARG;
+  if (k > 32 || k > e || e > 2048 || s > 4) return MM_ERR_INVALID_ARG;
+  if (bs * k >= kSortLimit) return MM_ERR_INVALID_ARG;
+  if (h % 128 != 0 || inter % 128 != 0) return MM_ERR_UNSUPPORTED;
+  if (h < 256) return MM_ERR_UNSUPPORTED;
+  return MM_OK;
+}
+
+bool activation_is_plain_swiglu(const char* act, const float* params, int64_t n) {
+  if (act && strcmp(act, "swiglu") != 0) return false;
+  if (n == 0) return true;
+  if (n != 1 || !params) return false;
+  const float c = params[0];  // clamp 0 or the float maximum disables clamping
+  return c == 0.0f || c >= FLT_MAX;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mm_status_string(int status) {
+  switch (status) {
+    case MM_OK: return "ok";
+    case MM_ERR_INVALID_ARG: return "invalid argument";
+    case MM_ERR_UNSUPPORTED: return "unsupported option";
+    case MM_ERR_WORKSPACE: return "workspace too small";
+    case MM_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int mm_version(void) { return 100; }
+
+// ------------------------------------------------------------------------
+mm_status mm_moe_init_routing_workspace_size(int64_t num_rows, int64_t k, int64_t expert_num, size_t* bytes) {
+  if (!bytes || num_rows < 0 || k <= 0 || expert_num <= 0 || expert_num > 10240) return MM_ERR_INVALID_ARG;
+  if (num_rows * k >= kSortLimit) return MM_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_routing(c, route_plan(num_rows * k, (int)expert_num));
+  *bytes = c.off;
+  return MM_OK;
+}
+
+mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows, int64_t h,
+                              int64_t k, int64_t expert_num, int quant_mode, int expert_tokens_num_type,
+                              void* expanded_x, uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                              int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  size_t need = 0;
+  mm_status s = mm_moe_init_routing_workspace_size(num_rows, k, expert_num, &need);
+  if (s != MM_OK) return s;
+  if (h <= 0 || !is_src_dtype(x_dtype)) return MM_ERR_INVALID_ARG;
+  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
+    return MM_ERR_UNSUPPORTED;
+  if (expert_tokens_num_type != 0 && expert_tokens_num_type != 1) return MM_ERR_UNSUPPORTED;
+  const bool quant = quant_mode != MM_QUANT_NONE;
+  if (quant ? (h % 16 != 0) : ((h * dt_size(x_dtype)) % 16 != 0)) return MM_ERR_UNSUPPORTED;
+  const int64_t rows = num_rows * k;
+  if (rows == 0) return MM_OK;
+  if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(expanded_x)) return MM_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const RoutePlan plan = route_plan(rows, (int)expert_num);
+  Carver c(workspace);
+  RoutingWs w = carve_routing(c, plan);
+  RouteOutputs o;
+  o.expanded_row_idx = expanded_row_idx ? expanded_row_idx : w.exp_idx;
+  o.sorted_row_idx = sorted_row_idx;
+  o.expert_tokens = expert_tokens;
+  o.tokens_cumsum = expert_tokens_num_type == 0;
+  cudaError_t e = launch_route(plan, expert_idx, false, w.hist, w.offsets, o, dev_err, st);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
+  PermuteArgs a = {};
+  a.src = x;
+  a.src_dtype = x_dtype;
+  a.n = num_rows;
+  a.h = h;
+  a.k = (int)k;
+  a.dest = o.expanded_row_idx;
+  a.dest_limit = rows;
+  a.out_fmt = quant_fmt(quant_mode);
+  a.out = expanded_x;
+  a.scales = expanded_scale;
+  a.scale_cols = round_up(ceil_div(h, 32), 2);
+  a.dev_err = dev_err;
+  return cuda_status(launch_permute(a, st));
+}
+
+// ------------------------------------------------------------------------
+int64_t mm_moe_token_permute_out_rows(int64_t num_indices, int64_t num_out_tokens) {
+  if (num_out_tokens == 0) return num_indices;
+  if (num_out_tokens > 0) return num_out_tokens < num_indices ? num_out_tokens : num_indices;
+  const int64_t m = num_indices + num_out_tokens;
+  return m > 0 ? m : 0;
+}
+
+mm_status mm_moe_token_permute_workspace_size(int64_t num_indices, int64_t num_experts, size_t* bytes) {
+  if (!bytes || num_indices < 0 || num_indices >= kSortLimit || num_experts <= 0 || num_experts > 10240)
+    return MM_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_routing(c, route_plan(num_indices, (int)num_experts));
+  *bytes = c.off;
+  return MM_OK;
+}
+
+mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void* indices, int indices_dtype,
+                               int64_t n, int64_t topk, int64_t h, int64_t num_experts, int64_t num_out_tokens,
+                               int padded_mode, int quant_mode, void* permuted_tokens, uint8_t* expanded_scale,
+                               int32_t* sorted_indices, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_err, void* stream) {
+  if (n < 0 || topk <= 0 || h <= 0 || !is_src_dtype(tokens_dtype)) return MM_ERR_INVALID_ARG;
+  if (indices_dtype != MM_DT_INT32 && indices_dtype != MM_DT_INT64) return MM_ERR_INVALID_ARG;
+  size_t need = 0;
+  const int64_t f = n * topk;
+  mm_status s = mm_moe_token_permute_workspace_size(f, num_experts, &need);
+  if (s != MM_OK) return s;
+  if (padded_mode != 0) return MM_ERR_UNSUPPORTED;
+  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
+    return MM_ERR_UNSUPPORTED;
+  const bool quant = quant_mode != MM_QUANT_NONE;
+  if (quant && tokens_dtype == MM_DT_FLOAT32) return MM_ERR_UNSUPPORTED;  // the article: fp16 / bf16
+  if (quant ? (h % 16 != 0) : ((h * dt_size(tokens_dtype)) % 16 != 0)) return MM_ERR_UNSUPPORTED;
+  if (f == 0) return MM_OK;
+  const int64_t m = mm_moe_token_permute_out_rows(f, num_out_tokens);
+  if (!tokens || !indices || !sorted_indices || (m > 0 && !permuted_tokens) || (quant && m > 0 && !expanded_scale))
+    return MM_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || (m > 0 && !aligned16(permuted_tokens))) return MM_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const RoutePlan plan = route_plan(f, (int)num_experts);
+  Carver c(workspace);
+  RoutingWs w = carve_routing(c, plan);
+  RouteOutputs o;
+  o.expanded_row_idx = sorted_indices;
+  cudaError_t e = launch_route(plan, indices, indices_dtype == MM_DT_INT64, w.hist, w.offsets, o, dev_err, st);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
+  if (m == 0) return MM_OK;
+  PermuteArgs a = {};
+  a.src = tokens;
+  a.src_dtype = tokens_dtype;
+  a.n = n;
+  a.h = h;
+  a.k = (int)topk;
+  a.dest = sorted_indices;
+  a.dest_limit = m;
+  a.out_fmt = quant_fmt(quant_mode);
+  a.out = permuted_tokens;
+  a.scales = expanded_scale;
+  a.scale_cols = round_up(ceil_div(h, 32), 2);
+  a.dev_err = dev_err;
+  return cuda_status(launch_permute(a, st));
+}
+
+// ------------------------------------------------------------------------
+mm_status mm_mega_moe_workspace_size(int64_t bs, int64_t h, int64_t k, int64_t moe_expert_num,
+                                     int64_t intermediate, int64_t shared_expert_num, int weight_scale_layout,
+                                     size_t* bytes) {
+  if (!bytes) return MM_ERR_INVALID_ARG;
+  mm_status s = check_mega_shapes(bs, h, k, moe_expert_num, intermediate, shared_expert_num);
+  if (s != MM_OK) return s;
+  if (weight_scale_layout != MM_WSCALE_ROWS && weight_scale_layout != MM_WSCALE_PREPARED)
+    return MM_ERR_INVALID_ARG;
+  const MegaDims d = mega_dims(bs, h, k, moe_expert_num, intermediate, shared_expert_num);
+  Carver c(nullptr);
+  carve_mega(c, d, route_plan(d.rows, (int)d.e), weight_scale_layout);
+  *bytes = c.off;
+  return MM_OK;
+}
+
+mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_weights, int topk_weights_dtype,
+                      const uint8_t* weight1, const uint8_t* weight2, const uint8_t* weight_scales1,
+                      const uint8_t* weight_scales2, int weight_dtype, int weight_scale_layout,
+                      const uint8_t* shared_weight1, const uint8_t* shared_weight2,
+                      const uint8_t* shared_weight_scales1, const uint8_t* shared_weight_scales2,
+                      int shared_weight_dtype, int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
+                      int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
+                      int64_t max_recv_token_num, int64_t dispatch_quant_mode, int64_t dispatch_quant_out_dtype,
+                      int64_t combine_quant_mode, const char* activation, const float* activation_params,
+                      int64_t n_activation_params, void* y, int32_t* expert_token_nums,
+                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  size_t need = 0;
+  mm_status s = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, intermediate, shared_expert_num,
+                                           weight_scale_layout, &need);
+  if (s != MM_OK) return s;
+  if (ep_world_size != 1) return MM_ERR_UNSUPPORTED;
+  if (combine_quant_mode != 0) return MM_ERR_UNSUPPORTED;
+  if (dispatch_quant_mode != 4) return MM_ERR_UNSUPPORTED;
+  if (!is_fp8(dispatch_quant_out_dtype) || !is_fp8(weight_dtype)) return MM_ERR_UNSUPPORTED;
+  if (shared_expert_num > 0 && !is_fp8(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
+  if (!activation_is_plain_swiglu(activation, activation_params, n_activation_params)) return MM_ERR_UNSUPPORTED;
+  if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
+  const int64_t rows = bs * k;
+  if (max_recv_token_num != 0 && max_recv_token_num < rows) return MM_ERR_INVALID_ARG;
+  if (bs == 0) return MM_OK;
+  if (!x || !topk_ids || !topk_weights || !weight1 || !weight2 || !weight_scales1 || !weight_scales2 || !y)
+    return MM_ERR_INVALID_ARG;
+  if (shared_expert_num > 0 &&
+      (!shared_weight1 || !shared_weight2 || !shared_weight_scales1 || !shared_weight_scales2))
+    return MM_ERR_INVALID_ARG;
+  if ((act_q == nullptr) != (act_scale == nullptr)) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(weight1) || !aligned16(weight2) ||
+      !aligned16(weight_scales1) || !aligned16(weight_scales2) || (act_q && !aligned16(act_q)))
+    return MM_ERR_INVALID_ARG;
+  if (shared_expert_num > 0 && (!aligned16(shared_weight1) || !aligned16(shared_weight2) ||
+                                !aligned16(shared_weight_scales1) || !aligned16(shared_weight_scales2)))
+    return MM_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const MegaDims d = mega_dims(bs, h, k, moe_expert_num, intermediate, shared_expert_num);
+  const RoutePlan plan = route_plan(d.rows, (int)d.e);
+  Carver c(workspace);
+  MegaWs w = carve_mega(c, d, plan, weight_scale_layout);
+  cudaError_t e;
+
+  // 0. weight scales into the GEMM tile layout (skipped when prepared once)
+  const uint8_t *wsf1 = weight_scales1, *wsf2 = weight_scales2;
+  const uint8_t *swsf1 = shared_weight_scales1, *swsf2 = shared_weight_scales2;
+  if (weight_scale_layout == MM_WSCALE_ROWS) {
+    if ((e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, w.wsf1, st)) != cudaSuccess)
+      return MM_ERR_CUDA;
+    if ((e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, w.wsf2, st)) != cudaSuccess)
+      return MM_ERR_CUDA;
+    wsf1 = w.wsf1;
+    wsf2 = w.wsf2;
+    if (d.s > 0) {
+      if ((e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, w.swsf1, st)) != cudaSuccess)
+        return MM_ERR_CUDA;
+      if ((e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, w.swsf2, st)) != cudaSuccess)
+        return MM_ERR_CUDA;
+      swsf1 = w.swsf1;
+      swsf2 = w.swsf2;
+    }
+  }
+
+  // 1. routing: stable counting sort, inverse map, counts, GEMM segment table
+  RouteOutputs o;
+  o.expanded_row_idx = expanded_row_idx ? expanded_row_idx : w.exp_idx;
+  o.pad_row = w.pad_row;
+  o.expert_token_nums = expert_token_nums;
+  o.seg_rows = w.seg_rows;
+  o.seg_mprefix = w.seg_mprefix;
+  o.n_shared = (int)d.s;
+  o.shared_rows = (int)d.bs;
+  if ((e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st)) != cudaSuccess)
+    return MM_ERR_CUDA;
+
+  // 2. dispatch: MX quantisation of each token, stored at its K expert rows
+  //    (and once per shared expert) in the padded grouped layout
+  PermuteArgs pa = {};
+  pa.src = x;
+  pa.src_dtype = MM_DT_BFLOAT16;
+  pa.n = d.bs;
+  pa.h = d.h;
+  pa.k = (int)d.k;
+  pa.dest = w.pad_row;
+  pa.dest_limit = d.rows_cap;
+  pa.ids = topk_ids;
+  pa.n_extra = (int)d.s;
+  pa.extra_base = w.seg_mprefix + d.e;
+  pa.out_fmt = (int)dispatch_quant_out_dtype;
+  pa.out = w.xq;
+  pa.scales = w.xsf;
+  pa.scale_cols = 0;
+  pa.dev_err = dev_err;
+  if ((e = launch_permute(pa, st)) != cudaSuccess) return MM_ERR_CUDA;
+
+  // 3. GEMM1 + swiglu + MX requantisation
+  GemmLaunch g1 = {};
+  g1.mode = 1;
+  g1.a = w.xq;
+  g1.rows_cap = d.rows_cap;
+  g1.sfa = w.xsf;
+  g1.b = weight1;
+  g1.sfb = wsf1;
+  g1.b_sh = shared_weight1;
+  g1.sfb_sh = swsf1;
+  g1.n_routed = (int)d.e;
+  g1.n_shared = (int)d.s;
+  g1.seg_rows = w.seg_rows;
+  g1.seg_mprefix = w.seg_mprefix;
+  g1.K = d.h;
+  g1.N = 2 * d.inter;
+  g1.a_fmt = (int)dispatch_quant_out_dtype;
+  g1.b_fmt = weight_dtype;
+  g1.b_fmt_sh = shared_weight_dtype;
+  g1.inter = (int)d.inter;
+  g1.act_q = w.aq;
+  g1.act_sf = w.asf;
+  g1.dev_err = dev_err;
+  if ((e = launch_gemm(g1, st)) != cudaSuccess) return MM_ERR_CUDA;
+
+  // 4. GEMM2 -> bf16 expert rows
+  GemmLaunch g2 = g1;
+  g2.mode = 2;
+  g2.a = w.aq;
+  g2.sfa = w.asf;
+  g2.b = weight2;
+  g2.sfb = wsf2;
+  g2.b_sh = shared_weight2;
+  g2.sfb_sh = swsf2;
+  g2.K = d.inter;
+  g2.N = d.h;
+  g2.act_q = nullptr;
+  g2.act_sf = nullptr;
+  g2.out = w.o;
+  if ((e = launch_gemm(g2, st)) != cudaSuccess) return MM_ERR_CUDA;
+
+  // 5. combine
+  CombineArgs ca;
+  ca.o = w.o;
+  ca.pad_row = w.pad_row;
+  ca.gate = topk_weights;
+  ca.gate_bf16 = topk_weights_dtype == MM_DT_BFLOAT16;
+  ca.n_shared = (int)d.s;
+  ca.seg_mprefix = w.seg_mprefix;
+  ca.n_routed = (int)d.e;
+  ca.n = d.bs;
+  ca.h = d.h;
+  ca.k = (int)d.k;
+  ca.y = static_cast<__nv_bfloat16*>(y);
+  if ((e = launch_combine(ca, st)) != cudaSuccess) return MM_ERR_CUDA;
+
+  // optional diagnostic copy of A_hat in expert-sorted order
+  if (act_q) {
+    UnpadArgs ua;
+    ua.src_q = w.aq;
+    ua.src_sf = w.asf;
+    ua.pad_row = w.pad_row;
+    ua.expanded_row_idx = o.expanded_row_idx;
+    ua.rows = d.rows;
+    ua.cols = d.inter;
+    ua.dst_q = act_q;
+    ua.dst_sf = act_scale;
+    if ((e = launch_unpad(ua, st)) != cudaSuccess) return MM_ERR_CUDA;
+  }
+  return MM_OK;
+}
+
+// ------------------------------------------------------------------------
+mm_status mm_prepared_weight_scales_size(int64_t experts, int64_t n_out, int64_t k_red, size_t* bytes) {
+  if (!bytes || experts <= 0 || n_out <= 0 || k_red <= 0 || k_red % 128 != 0) return MM_ERR_INVALID_ARG;
+  *bytes = (size_t)(experts * prepared_nblocks(n_out) * (k_red / 128) * kSfChunk);
+  return MM_OK;
+}
+
+mm_status mm_prepare_weight_scales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red,
+                                   uint8_t* dst, void* stream) {
+  size_t need;
+  mm_status s = mm_prepared_weight_scales_size(experts, n_out, k_red, &need);
+  if (s != MM_OK) return s;
+  if (!src || !dst || (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))
+    return MM_ERR_INVALID_ARG;
+  return cuda_status(launch_prepare_wscales(src, experts, n_out, k_red, dst, static_cast<cudaStream_t>(stream)));
+}
+
+mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t cols, int out_dtype, uint8_t* q,
+                         uint8_t* scales, int64_t scale_cols, void* stream) {
+  if (rows < 0 || cols <= 0 || !is_src_dtype(src_dtype) || !is_fp8(out_dtype)) return MM_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return MM_ERR_UNSUPPORTED;
+  if (scale_cols < ceil_div(cols, 32)) return MM_ERR_INVALID_ARG;
+  if (rows == 0) return MM_OK;
+  if (!src || !q || !scales || !aligned16(src) || !aligned16(q)) return MM_ERR_INVALID_ARG;
+  PermuteArgs a = {};
+  a.src = src;
+  a.src_dtype = src_dtype;
+  a.n = rows;
+  a.h = cols;
+  a.k = 1;
+  a.dest = nullptr;
+  a.dest_limit = rows;
+  a.out_fmt = out_dtype;
+  a.out = q;
+  a.scales = scales;
+  a.scale_cols = scale_cols;
+  return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

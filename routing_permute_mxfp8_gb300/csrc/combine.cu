@@ -1,0 +1,65 @@
+// Combine (MegaMoE README, A8W8-FP stage 4 at epWorldSize = 1):
+//   Y[i] = sum_k W[i,k] * O[pi(i,k)] + sum_s O_s^shared[i]
+// One block per token.  The expert rows are gathered with 16-byte loads,
+// accumulated in fp32 in the order k = 0..K-1 then the shared experts, and
+// rounded to bf16 once.  No atomics, so the result is deterministic.
+#include "mm_route.cuh"
+
+namespace mm {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxTerms = 36;  // top-K <= 32 plus up to 4 shared experts
+
+__global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
+  __shared__ int32_t rows[kMaxTerms];
+  __shared__ float w[kMaxTerms];
+  const int64_t i = blockIdx.x;
+  const int nterm = a.k + a.n_shared;
+  if (threadIdx.x < a.k) {
+    const int64_t j = i * a.k + threadIdx.x;
+    rows[threadIdx.x] = a.pad_row[j];
+    w[threadIdx.x] = a.gate_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.gate)[j])
+                                 : static_cast<const float*>(a.gate)[j];
+  } else if (threadIdx.x < nterm) {
+    const int s = threadIdx.x - a.k;
+    rows[threadIdx.x] = a.seg_mprefix[a.n_routed + s] * kBM + (int32_t)i;
+    w[threadIdx.x] = 1.0f;
+  }
+  __syncthreads();
+  for (int64_t c = (int64_t)threadIdx.x * 8; c < a.h; c += kThreads * 8) {
+    float acc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+    for (int t = 0; t < nterm; ++t) {
+      const int32_t r = rows[t];
+      if (r < 0) continue;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.o + (int64_t)r * a.h + c));
+      float f[8];
+      bf16x8_to_f32(v, f);
+      const float wt = w[t];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
+    }
+    uint4 o;
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[4], acc[5]);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[6], acc[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&p0);
+    o.y = *reinterpret_cast<uint32_t*>(&p1);
+    o.z = *reinterpret_cast<uint32_t*>(&p2);
+    o.w = *reinterpret_cast<uint32_t*>(&p3);
+    *reinterpret_cast<uint4*>(a.y + i * a.h + c) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+  if (a.n <= 0) return cudaSuccess;
+  k_combine<<<(unsigned)a.n, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

@@ -1,0 +1,434 @@
+// Grouped block-scaled FP8 GEMMs of the expert FFN on tcgen05 (sm_103a).
+//
+// MegaMoE README, A8W8-FP scenario:
+//   stage 2  G_e, U_e = DQ_MX(X_hat_e) . DQ_MX(W1_e^(G|U))   then
+//            A_e = SiLU(G_e) * U_e (swiglu, "Activation function formulas"),
+//            A_hat_e, S_A,e = Q_MX(A_e) in the dispatch FP8 type
+//   stage 3  O_e = DQ_MX(A_hat_e) . DQ_MX(W2_e)
+// DQ_MX happens inside the MMA: tcgen05.mma kind::mxf8f6f4 with one E8M0
+// scale per 32 k for every row of A and of B (scale_vec::1X).
+//
+// Layout.  The expanded rows of every expert (and of each shared expert,
+// which sees all tokens) form a segment padded to a multiple of 128 rows,
+// so an M tile never straddles two experts.  One persistent kernel walks a
+// flat tile list (segment, n tile, m tile) ordered expert-major and
+// n-major inside an expert, so the m tiles that share a weight strip run
+// on neighbouring CTAs at the same time and the strip comes from HBM once.
+//
+// CTA = 6 warps: warp 0 issues TMA (A tile 128x128 B, B tile 256x128 B,
+// 128B swizzle) and bulk copies of the scale tiles into a 4-stage ring;
+// warp 1 copies the scales to TMEM (tcgen05.cp) and issues the MMAs
+// (M=128, N=256, K=32, four per k-block) into a 256-column fp32 TMEM
+// accumulator; warps 2-5 drain the accumulator (tcgen05.ld, one row per
+// thread) and run the epilogue:
+//   GEMM1: columns [0,128) are gate, [128,256) up, for the same 128
+//          intermediate columns -> swiglu -> one MX group per 32 columns,
+//          entirely within a thread; writes A_hat (FP8) and its scales
+//          directly in GEMM2's operand layouts.
+//   GEMM2: fp32 -> bf16 rows of O.
+// Every wait is bounded; a timeout sets MM_DEVERR_TIMEOUT and the CTA
+// drains its own copies and MMAs, frees TMEM and returns.
+#include "mm_route.cuh"
+
+namespace mm {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
+constexpr uint32_t kBBytes = 256 * kBK;   // 32 KB
+constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+}
+
+struct GemmArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const uint8_t* sfb_sh;
+  const int32_t* seg_rows;
+  const int32_t* seg_mprefix;
+  int nseg, n_routed;
+  int K, N;
+  int n_tiles;
+  int nb;         // 128-row blocks per expert in the prepared B scales
+  uint32_t idesc, idesc_sh;
+  int inter;
+  uint8_t* act_q;
+  uint8_t* act_sf;
+  __nv_bfloat16* out;
+  int32_t* dev_err;
+};
+
+struct TileInfo {
+  int seg, mt, nt;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, const int32_t* mpre, int nseg, int n_tiles) {
+  int lo = 0, hi = nseg;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (mpre[mid] * n_tiles <= t)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  TileInfo ti;
+  ti.seg = lo;
+  const int local = t - mpre[lo] * n_tiles;
+  const int mts = mpre[lo + 1] - mpre[lo];
+  ti.nt = local / mts;
+  ti.mt = local - ti.nt * mts;
+  return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int kMode, int kActFmt>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmBs, const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = base;
+  uint8_t* smB = smA + kStages * kABytes;
+  uint8_t* smSFA = smB + kStages * kBBytes;
+  uint8_t* smSFB = smSFA + kStages * 512;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smSFB + kStages * 1024);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* mpre = reinterpret_cast<int32_t*>(tmem_holder + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nseg = g.nseg;
+  for (int i = threadIdx.x; i <= nseg; i += kThreads) mpre[i] = g.seg_mprefix[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (nseg > g.n_routed) prefetch_tensormap(&tmBs);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int total = mpre[nseg] * g.n_tiles;
+  const int kblocks = g.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0, armed = 0, arm_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+        const bool sh = ti.seg >= g.n_routed;
+        const int e = sh ? ti.seg - g.n_routed : ti.seg;
+        const CUtensorMap* mb = sh ? &tmBs : &tmB;
+        const uint8_t* sfb = (sh ? g.sfb_sh : g.sfb) + (int64_t)e * g.nb * kblocks * 512;
+        const int am = mpre[ti.seg] + ti.mt;
+        int nb0, nb1, bn0, bn1;
+        if (kMode == 1) {
+          nb0 = ti.nt;
+          nb1 = g.inter / 128 + ti.nt;
+          bn0 = ti.nt * 128;
+          bn1 = g.inter + ti.nt * 128;
+        } else {
+          nb0 = 2 * ti.nt;
+          nb1 = 2 * ti.nt + 1;
+          bn0 = ti.nt * 256;
+          bn1 = 0;
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bounded(&empty[stage], phase ^ 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageTx);
+          armed |= 1u << stage;
+          arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], kb * kBK, am * kBM);
+          tma_load_3d(smB + stage * kBBytes, mb, &full[stage], kb * kBK, bn0, e);
+          if (kMode == 1) tma_load_3d(smB + stage * kBBytes + kABytes, mb, &full[stage], kb * kBK, bn1, e);
+          bulk_load(smSFA + stage * 512, g.sfa + ((int64_t)am * kblocks + kb) * 512, 512, &full[stage]);
+          bulk_load(smSFB + stage * 1024, sfb + ((int64_t)nb0 * kblocks + kb) * 512, 512, &full[stage]);
+          bulk_load(smSFB + stage * 1024 + 512, sfb + ((int64_t)nb1 * kblocks + kb) * 512, 512, &full[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
+      // every copy this thread started must land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if ((armed >> s) & 1u) wait_bounded(&full[s], (arm_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+        const uint32_t idb = ti.seg >= g.n_routed ? g.idesc_sh : g.idesc;
+        if (!wait_bounded(acc_empty, acc_phase ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bounded(&full[stage], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfc = tmem + kAccCols + stage * 16;
+          tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(smSFA + stage * 512), 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(smSFB + stage * 1024), 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfc + 8, smem_desc(smem_u32(smSFB + stage * 1024 + 512), 0, 128, 0));
+          const uint32_t a0 = smem_u32(smA + stage * kABytes);
+          const uint32_t b0 = smem_u32(smB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            tc_mma_mxf8(tmem, smem_desc(a0 + 32 * k, 0, 1024, 2), smem_desc(b0 + 32 * k, 0, 1024, 2),
+                        idesc_with_sf(idb, (uint32_t)k), sfc, sfc + 4, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1;
+      }
+      if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
+      tc_commit(drain);  // all MMAs / copies of this thread complete before TMEM is freed
+      wait_bounded(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+      if (!wait_bounded(acc_full, acc_phase)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      const bool valid = r < g.seg_rows[ti.seg] - ti.mt * kBM;
+      const int64_t grow = (int64_t)(mpre[ti.seg] + ti.mt) * kBM + r;
+      if (kMode == 1) {
+        uint32_t sfw = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t gv[32], uv[32];
+          tmem_ld_32x32b_x32(trow + c * 32, gv);
+          tmem_ld_32x32b_x32(trow + 128 + c * 32, uv);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+          }
+          float a[32];
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gf = __uint_as_float(gv[j]);
+            const float uf = __uint_as_float(uv[j]);
+            a[j] = gf / (1.0f + expf(-gf)) * uf;
+            amax = fmaxf(amax, fabsf(a[j]));
+          }
+          float inv;
+          const uint32_t code = mx_scale(amax, fmt_emax<kActFmt>(), inv);
+          sfw |= code << (8 * c);
+          if (valid) {
+            const uint2 p0 = pack8_fp8<kActFmt>(a, inv), p1 = pack8_fp8<kActFmt>(a + 8, inv);
+            const uint2 p2 = pack8_fp8<kActFmt>(a + 16, inv), p3 = pack8_fp8<kActFmt>(a + 24, inv);
+            uint8_t* dst = g.act_q + grow * g.inter + ti.nt * 128 + c * 32;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(p2.x, p2.y, p3.x, p3.y);
+          }
+        }
+        if (valid) *reinterpret_cast<uint32_t*>(g.act_sf + sf_tile_offset(grow, ti.nt * 4, g.inter / 128)) = sfw;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(trow + c * 32, v);
+          tmem_ld_wait();
+          if (c == 7) {
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+          }
+          const int64_t col = (int64_t)ti.nt * 256 + c * 32;
+          if (valid && col < g.N) {
+            uint4* dst = reinterpret_cast<uint4*>(g.out + grow * g.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                  pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
+        }
+      }
+      acc_phase ^= 1;
+    }
+    if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// FP8 byte matrix [outer][inner] (inner contiguous), box inner 128 B, 128B swizzle.
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  EncodeTiledFn f = encode_fn();
+  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Stacked weights [E][N][K] FP8.
+bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e, uint32_t box_rows) {
+  cuuint64_t dims[3] = {k, n, e};
+  cuuint64_t strides[2] = {k, n * k};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  EncodeTiledFn f = encode_fn();
+  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : 0; }
+
+template <int kMode, int kActFmt>
+cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbs,
+                const GemmArgs& g, int grid, size_t smem, cudaStream_t st) {
+  auto kern = k_gemm_mx<kMode, kActFmt>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(ma, mb, mbs, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  }
+  return n;
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
+  const int nseg = L.n_routed + L.n_shared;
+  const uint32_t box_rows = L.mode == 1 ? 128 : 256;
+  CUtensorMap ma, mb, mbs;
+  if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM)) return cudaErrorInvalidValue;
+  if (!map_3d(&mb, L.b, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_routed, box_rows)) return cudaErrorInvalidValue;
+  if (L.n_shared > 0) {
+    if (!map_3d(&mbs, L.b_sh, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_shared, box_rows))
+      return cudaErrorInvalidValue;
+  } else {
+    mbs = mb;
+  }
+  GemmArgs g;
+  g.sfa = L.sfa;
+  g.sfb = L.sfb;
+  g.sfb_sh = L.n_shared > 0 ? L.sfb_sh : L.sfb;
+  g.seg_rows = L.seg_rows;
+  g.seg_mprefix = L.seg_mprefix;
+  g.nseg = nseg;
+  g.n_routed = L.n_routed;
+  g.K = (int)L.K;
+  g.N = (int)L.N;
+  g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, 256);
+  g.nb = (int)prepared_nblocks(L.N);
+  g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, 256);
+  g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, 256);
+  g.inter = L.inter;
+  g.act_q = L.act_q;
+  g.act_sf = L.act_sf;
+  g.out = L.out;
+  g.dev_err = L.dev_err;
+  // upper bound of the tile count decides how many persistent CTAs to start
+  const int64_t max_mtiles = L.rows_cap / kBM;
+  int64_t grid = max_mtiles * g.n_tiles;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  const size_t smem = 1024 + (size_t)kStages * (kABytes + kBBytes + 512 + 1024) + 8 * (2 * kStages + 3) + 16 +
+                      4 * (size_t)(nseg + 1);
+  if (smem > 232448) return cudaErrorInvalidValue;
+  if (L.mode == 1) {
+    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2>(L, ma, mb, mbs, g, (int)grid, smem, st);
+    return run<1, MM_DT_FP8_E4M3FN>(L, ma, mb, mbs, g, (int)grid, smem, st);
+  }
+  return run<2, MM_DT_FP8_E4M3FN>(L, ma, mb, mbs, g, (int)grid, smem, st);
+}
+
+}  // namespace mm

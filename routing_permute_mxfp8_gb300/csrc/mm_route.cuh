@@ -1,0 +1,126 @@
+// Internal interfaces between the C-ABI layer and the kernel files.
+#pragma once
+
+#include "mm_common.cuh"
+
+namespace mm {
+
+// ---- routing (route.cu) ----------------------------------------------------
+struct RoutePlan {
+  int64_t rows;         // R = N * K flattened ids
+  int num_experts;      // E
+  int chunk;            // ids per warp chunk (multiple of 32)
+  int units;            // number of chunks
+  int warps_per_block;  // chunks per block (smem: warps * E * 4 bytes)
+};
+
+struct RouteOutputs {
+  int32_t* expanded_row_idx = nullptr;   // [R] scatter index (or null)
+  int32_t* sorted_row_idx = nullptr;     // [R] gather index (or null)
+  int32_t* pad_row = nullptr;            // [R] row in the 128-row padded grouped layout (or null)
+  int64_t* expert_tokens = nullptr;      // [E] int64 counts / cumsum (or null)
+  int tokens_cumsum = 0;
+  int32_t* expert_token_nums = nullptr;  // [E] int32 counts (or null)
+  int32_t* seg_rows = nullptr;           // [E + S] rows per GEMM segment (or null)
+  int32_t* seg_mprefix = nullptr;        // [E + S + 1] prefix of 128-row tiles (or null)
+  int n_shared = 0;                      // S shared segments ...
+  int shared_rows = 0;                   // ... of this many rows each
+};
+
+struct RouteScanArgs {
+  int32_t* hist;
+  int num_experts, units;
+  int64_t rows;
+  int32_t* offsets;
+  int32_t* sorted_row_idx;
+  int64_t* expert_tokens;
+  int tokens_cumsum;
+  int32_t* expert_token_nums;
+  int32_t* seg_rows;
+  int32_t* seg_mprefix;
+  int n_shared, shared_rows;
+};
+
+RoutePlan route_plan(int64_t rows, int num_experts);
+size_t route_workspace_bytes(const RoutePlan& p);
+// hist: [E * units] int32, offsets: [E + 1] int32 (both workspace)
+cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
+                         RouteOutputs o, int32_t* dev_err, cudaStream_t st);
+
+// ---- permute / quantise (permute.cu) -------------------------------------
+struct PermuteArgs {
+  const void* src;          // [n, h] source rows
+  int src_dtype;            // MM_DT_BFLOAT16 / FLOAT16 / FLOAT32
+  int64_t n, h;             // rows, row length (elements)
+  int k;                    // destinations per row from dest[] (row i -> dest[i*k + t])
+  const int32_t* dest;      // [n*k] destination rows (< 0: skipped; null: identity, k must be 1)
+  int64_t dest_limit;       // destinations >= dest_limit are skipped (num_out_tokens)
+  const int32_t* ids;       // [n, k] expert ids for the duplicate check (or null)
+  int n_extra;              // extra destinations per row: extra_base[s] * 128 + i
+  const int32_t* extra_base;  // [n_extra] tile index of each extra segment (device)
+  int out_fmt;              // -1 copy, 23 / 24 FP8
+  void* out;                // [*, h] output rows
+  uint8_t* scales;          // E8M0 output
+  int64_t scale_cols;       // row layout: scale row stride; 0 = GEMM tile layout
+  int32_t* dev_err;
+};
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
+
+// tile layout of E8M0 weight scales (mm_prepare_weight_scales)
+int64_t prepared_nblocks(int64_t n_out);
+cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red,
+                                   uint8_t* dst, cudaStream_t st);
+
+// ---- grouped GEMMs (gemm.cu) ----------------------------------------------
+struct GemmLaunch {
+  int mode;                   // 1: GEMM1 + swiglu + MX requant; 2: GEMM2 -> bf16
+  const uint8_t* a;           // [rows_cap, K] FP8 A (padded grouped layout)
+  int64_t rows_cap;
+  const uint8_t* sfa;         // A scales, tile layout
+  const uint8_t* b;           // routed weights [E, N, K] FP8
+  const uint8_t* sfb;         // routed prepared scales
+  const uint8_t* b_sh;        // shared weights [S, N, K] (or null)
+  const uint8_t* sfb_sh;
+  int n_routed, n_shared;
+  const int32_t* seg_rows;    // [n_routed + n_shared]
+  const int32_t* seg_mprefix; // [n_routed + n_shared + 1]
+  int64_t K, N;
+  int a_fmt, b_fmt, b_fmt_sh; // 23 / 24
+  int inter;                  // mode 1: I (= N / 2)
+  uint8_t* act_q;             // mode 1 outputs
+  uint8_t* act_sf;
+  __nv_bfloat16* out;         // mode 2 output [rows_cap, N]
+  int32_t* dev_err;
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+
+// ---- combine (combine.cu) --------------------------------------------------
+struct CombineArgs {
+  const __nv_bfloat16* o;     // [rows_cap, h] expert outputs (padded grouped layout)
+  const int32_t* pad_row;     // [n*k]
+  const void* gate;           // [n, k] fp32 or bf16
+  int gate_bf16;
+  int n_shared;
+  const int32_t* seg_mprefix; // shared segment s starts at tile seg_mprefix[n_routed + s]
+  int n_routed;
+  int64_t n, h;
+  int k;
+  __nv_bfloat16* y;           // [n, h]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+// diagnostic: padded grouped rows -> expert-sorted dense rows
+struct UnpadArgs {
+  const uint8_t* src_q;       // [rows_cap, cols]
+  const uint8_t* src_sf;      // tile layout, cols/128 groups4
+  const int32_t* pad_row;     // [rows]
+  const int32_t* expanded_row_idx;  // [rows]
+  int64_t rows, cols;
+  uint8_t* dst_q;             // [rows, cols]
+  uint8_t* dst_sf;            // [rows, cols/32]
+};
+cudaError_t launch_unpad(const UnpadArgs& a, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace mm

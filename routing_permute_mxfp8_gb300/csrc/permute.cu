@@ -1,0 +1,247 @@
+// Token permute fused with MX quantisation (dispatch), and weight-scale
+// preparation.
+//
+// moe_token_permute article, 功能说明 / 返回值说明, and MoeInitRoutingV3
+// step 5: output row d takes the source token of its flattened index; in
+// MXFP8 modes every group of 32 consecutive elements shares one E8M0
+// exponent (MegaMoE README, A8W8-FP stage 1, Q_MX).
+//
+// The gather is turned around: one warp owns one source token, reads its
+// row once, quantises it once and stores the result at each of its K
+// destinations (16-byte stores; one lane holds 16 consecutive elements, so
+// a 32-element group is two lanes and its amax takes one shuffle).
+#include "mm_route.cuh"
+
+namespace mm {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+// Loads 16 consecutive elements of a row as fp32.
+template <int kSrc>
+__device__ __forceinline__ void load16(const char* row, int64_t col, float* v) {
+  if (kSrc == MM_DT_FLOAT32) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + col * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 u = __ldg(p + i);
+      v[4 * i] = __uint_as_float(u.x);
+      v[4 * i + 1] = __uint_as_float(u.y);
+      v[4 * i + 2] = __uint_as_float(u.z);
+      v[4 * i + 3] = __uint_as_float(u.w);
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(row + col * 2);
+    uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
+    if (kSrc == MM_DT_BFLOAT16) {
+      bf16x8_to_f32(u0, v);
+      bf16x8_to_f32(u1, v + 8);
+    } else {
+      f16x8_to_f32(u0, v);
+      f16x8_to_f32(u1, v + 8);
+    }
+  }
+}
+
+// Destination t (0 <= t < ndest) of the current row; d0 holds t = lane,
+// d1 holds t = lane + 32.  Uniform across the warp.
+__device__ __forceinline__ int32_t dest_at(int t, int32_t d0, int32_t d1) {
+  int32_t a = __shfl_sync(0xffffffffu, d0, t & 31);
+  int32_t b = __shfl_sync(0xffffffffu, d1, t & 31);
+  return t < 32 ? a : b;
+}
+
+__device__ __forceinline__ void load_dests(const PermuteArgs& a, int64_t row, int lane, int32_t& d0,
+                                           int32_t& d1, int& ndest) {
+  ndest = a.k + a.n_extra;
+  d0 = -1;
+  d1 = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = lane + 32 * h;
+    int32_t d = -1;
+    if (t < a.k) {
+      d = a.dest ? a.dest[row * a.k + t] : (int32_t)row;
+      if (d >= a.dest_limit) d = -1;
+    } else if (t < ndest) {
+      d = (int32_t)((int64_t)a.extra_base[t - a.k] * kBM + row);
+    }
+    if (h == 0) d0 = d; else d1 = d;
+  }
+  if (a.ids) {  // MegaMoE: the K experts of a token must be distinct
+    const int id = lane < a.k ? a.ids[row * a.k + lane] : (int)(0x80000000u + (unsigned)lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, id);
+    if (lane < a.k && __popc(peers) > 1) raise_err(a.dev_err, MM_DEVERR_DUPLICATE_ID);
+  }
+}
+
+template <int kSrc, int kFmt, bool kTiled>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  if (row >= a.n) return;
+  int32_t d0, d1;
+  int ndest;
+  load_dests(a, row, lane, d0, d1, ndest);
+  constexpr int esz = kSrc == MM_DT_FLOAT32 ? 4 : 2;
+  const char* src_row = static_cast<const char*>(a.src) + row * a.h * esz;
+  uint8_t* out = static_cast<uint8_t*>(a.out);
+  const int64_t groups = (a.h + 31) / 32;
+  const int64_t groups4 = a.h / 128;
+  for (int64_t c0 = 0; c0 < a.h; c0 += 512) {
+    const int64_t col = c0 + lane * 16;
+    const bool act = col < a.h;
+    float v[16];
+    if (act) {
+      load16<kSrc>(src_row, col, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    float inv;
+    const uint32_t code = mx_scale(amax, fmt_emax<kFmt>(), inv);
+    const uint2 lo = pack8_fp8<kFmt>(v, inv);
+    const uint2 hi = pack8_fp8<kFmt>(v + 8, inv);
+    const uint4 packed = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    // tile layout: lanes 8m..8m+7 hold groups 4m'..4m'+3; lane 8m packs them
+    uint32_t word = 0;
+    if (kTiled) {
+      const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 2);
+      const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 4);
+      const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 6);
+      word = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    }
+    const int64_t g = col / 32;
+    for (int t = 0; t < ndest; ++t) {
+      const int32_t d = dest_at(t, d0, d1);
+      if (d < 0 || !act) continue;
+      *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = packed;
+      if (kTiled) {
+        if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, g, groups4)) = word;
+      } else if ((lane & 1) == 0) {
+        a.scales[(int64_t)d * a.scale_cols + g] = (uint8_t)code;
+      }
+    }
+  }
+  if (!kTiled && groups < a.scale_cols) {  // zero padding columns of the row layout
+    for (int t = 0; t < ndest; ++t) {
+      const int32_t d = dest_at(t, d0, d1);
+      if (d < 0) continue;
+      for (int64_t gg = groups + lane; gg < a.scale_cols; gg += 32) a.scales[(int64_t)d * a.scale_cols + gg] = 0;
+    }
+  }
+}
+
+// Copy mode: 16-byte vectors of the row to each destination.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_copy(PermuteArgs a, int esz) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  if (row >= a.n) return;
+  int32_t d0, d1;
+  int ndest;
+  load_dests(a, row, lane, d0, d1, ndest);
+  const int64_t rb = a.h * esz;
+  const char* src = static_cast<const char*>(a.src) + row * rb;
+  char* out = static_cast<char*>(a.out);
+  for (int64_t off = (int64_t)lane * 16; off - lane * 16 < rb; off += 512) {
+    const bool act = off < rb;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (act) v = __ldg(reinterpret_cast<const uint4*>(src + off));
+    for (int t = 0; t < ndest; ++t) {
+      const int32_t d = dest_at(t, d0, d1);
+      if (d >= 0 && act) *reinterpret_cast<uint4*>(out + (int64_t)d * rb + off) = v;
+    }
+  }
+}
+
+// One thread per 4-byte word of the tile layout.
+__global__ void k_prepare_wscales(const uint8_t* __restrict__ src, int64_t experts, int64_t n_out,
+                                  int64_t k_red, int64_t nb, uint8_t* __restrict__ dst) {
+  const int64_t kc_n = k_red / 128;
+  const int64_t words = experts * nb * kc_n * 128;
+  const int64_t sc = k_red / 32;  // source row stride (2 * ceil(K/64) with K % 128 == 0)
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t wi = w & 127;
+    const int64_t chunk = w >> 7;  // (e * nb + nblk) * kc_n + kc
+    const int64_t kc = chunk % kc_n;
+    const int64_t nblk = (chunk / kc_n) % nb;
+    const int64_t e = chunk / (kc_n * nb);
+    const int64_t r = nblk * 128 + (wi & 3) * 32 + (wi >> 2);
+    uint32_t v = 0;
+    if (r < n_out) v = __ldg(reinterpret_cast<const uint32_t*>(src + (e * n_out + r) * sc + kc * 4));
+    reinterpret_cast<uint32_t*>(dst)[w] = v;
+  }
+}
+
+__global__ void k_unpad(UnpadArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t j = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  if (j >= a.rows) return;
+  const int32_t d = a.expanded_row_idx[j], p = a.pad_row[j];
+  if (d < 0 || p < 0) return;
+  for (int64_t c = lane * 16; c < a.cols; c += 512)
+    *reinterpret_cast<uint4*>(a.dst_q + (int64_t)d * a.cols + c) =
+        *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * a.cols + c);
+  const int64_t groups = a.cols / 32;
+  for (int64_t g = lane; g < groups; g += 32)
+    a.dst_sf[(int64_t)d * groups + g] = a.src_sf[sf_tile_offset(p, g, a.cols / 128)];
+}
+
+template <int kSrc, int kFmt>
+cudaError_t launch_mx_variant(const PermuteArgs& a, int blocks, cudaStream_t st) {
+  if (a.scale_cols == 0)
+    k_permute_mx<kSrc, kFmt, true><<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
+  else
+    k_permute_mx<kSrc, kFmt, false><<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int kSrc>
+cudaError_t launch_mx_src(const PermuteArgs& a, int blocks, cudaStream_t st) {
+  if (a.out_fmt == MM_DT_FP8_E5M2) return launch_mx_variant<kSrc, MM_DT_FP8_E5M2>(a, blocks, st);
+  return launch_mx_variant<kSrc, MM_DT_FP8_E4M3FN>(a, blocks, st);
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
+  if (a.n <= 0) return cudaSuccess;
+  const int64_t blocks64 = (a.n + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (blocks64 > 0x7fffffff) return cudaErrorInvalidValue;
+  const int blocks = (int)blocks64;
+  if (a.out_fmt < 0) {
+    const int esz = a.src_dtype == MM_DT_FLOAT32 ? 4 : 2;
+    k_permute_copy<<<blocks, kWarpsPerBlock * 32, 0, st>>>(a, esz);
+    return cudaGetLastError();
+  }
+  if (a.src_dtype == MM_DT_BFLOAT16) return launch_mx_src<MM_DT_BFLOAT16>(a, blocks, st);
+  if (a.src_dtype == MM_DT_FLOAT16) return launch_mx_src<MM_DT_FLOAT16>(a, blocks, st);
+  return launch_mx_src<MM_DT_FLOAT32>(a, blocks, st);
+}
+
+int64_t prepared_nblocks(int64_t n_out) { return round_up(ceil_div(n_out, 128), 2); }
+
+cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red,
+                                   uint8_t* dst, cudaStream_t st) {
+  const int64_t nb = prepared_nblocks(n_out);
+  const int64_t words = experts * nb * (k_red / 128) * 128;
+  if (words == 0) return cudaSuccess;
+  int64_t blocks = ceil_div(words, 256);
+  if (blocks > 65535 * 16) blocks = 65535 * 16;
+  k_prepare_wscales<<<(unsigned)blocks, 256, 0, st>>>(src, experts, n_out, k_red, nb, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpad(const UnpadArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  k_unpad<<<(unsigned)ceil_div(a.rows, 8), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

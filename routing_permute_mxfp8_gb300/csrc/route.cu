@@ -1,0 +1,234 @@
+// Routing: stable counting sort of the flattened expert ids.
+//
+// MoeInitRoutingV3 (moe/moe_init_routing_v3), formula steps 1-3:
+//   sortedExpertIdx, sortedRowIdx = keyValueSort(expertIdx, rowIdx)
+//   expandedRowIdx[sortedRowIdx[i]] = i
+//   expertTokensCountOrCumsum = Histogram(sortedExpertIdx)
+// The keys are expert ids in [0, E), so one counting pass replaces the two
+// sorts the permute article describes (sort, then argsort of the result):
+//   1. k_route_hist     each warp counts the ids of its contiguous chunk
+//   2. k_route_scan     one block scans the expert-major [E][units] counts:
+//                       base of (expert, chunk), per-expert offsets, counts,
+//                       and the 128-row tile table the grouped GEMMs use
+//   3. k_route_scatter  each warp walks its chunk in index order and gives
+//                       every id the next slot of its expert (warp match +
+//                       popc for ties inside a 32-wide step), which is the
+//                       stable order; it writes the inverse map and the
+//                       gather index directly.
+// No global atomics; the result is deterministic.
+#include "mm_route.cuh"
+
+namespace mm {
+
+template <typename IdT>
+__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+                             int units, int32_t* __restrict__ hist, int32_t* dev_err) {
+  extern __shared__ int32_t sh_cnt[];  // [warps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int unit = blockIdx.x * wpb + warp;
+  int32_t* cnt = sh_cnt + warp * num_experts;
+  for (int e = lane; e < num_experts; e += 32) cnt[e] = 0;
+  __syncwarp();
+  if (unit < units) {
+    const int64_t start = (int64_t)unit * chunk;
+    const int64_t end = start + chunk < rows ? start + chunk : rows;
+    bool bad = false;
+    for (int64_t j = start + lane; j < end; j += 32) {
+      const int64_t id = (int64_t)ids[j];
+      if (id >= 0 && id < num_experts)
+        atomicAdd(&cnt[id], 1);
+      else
+        bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_err(dev_err, MM_DEVERR_EXPERT_RANGE);
+    __syncwarp();
+    for (int e = lane; e < num_experts; e += 32) hist[(int64_t)e * units + unit] = cnt[e];
+  }
+}
+
+// Exclusive scan of one value per thread across a 1024-thread block.
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* sh_warp, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) sh_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < (int)(blockDim.x >> 5) ? sh_warp[lane] : 0;
+    int64_t s = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += y;
+    }
+    sh_warp[lane] = s - w;  // exclusive warp base
+    if (lane == 31) sh_warp[32] = s;
+  }
+  __syncthreads();
+  int64_t r = sh_warp[warp] + x - v;
+  total = sh_warp[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) k_route_scan(RouteScanArgs a) {
+  __shared__ int64_t sh_warp[33];
+  const int64_t entries = (int64_t)a.num_experts * a.units;
+  const int nt = blockDim.x;
+  const int64_t per = (entries + nt - 1) / nt;
+  const int64_t lo = threadIdx.x * per;
+  const int64_t hi = lo + per < entries ? lo + per : entries;
+  // 1. expert-major exclusive scan of the per-chunk counts -> per-chunk bases
+  int64_t s = 0;
+  for (int64_t i = lo; i < hi; ++i) s += a.hist[i];
+  int64_t total;
+  int64_t base = block_exclusive_scan(s, sh_warp, total);
+  for (int64_t i = lo; i < hi; ++i) {
+    const int32_t c = a.hist[i];
+    a.hist[i] = (int32_t)base;
+    if (i % a.units == 0) a.offsets[i / a.units] = (int32_t)base;
+    base += c;
+  }
+  if (threadIdx.x == 0) a.offsets[a.num_experts] = (int32_t)total;
+  // rows whose id was out of range are left out: pad the gather index
+  if (a.sorted_row_idx)
+    for (int64_t d = total + threadIdx.x; d < a.rows; d += nt) a.sorted_row_idx[d] = -1;
+  __syncthreads();
+  // 2. per-expert counts / cumsum outputs
+  for (int e = threadIdx.x; e < a.num_experts; e += nt) {
+    const int32_t c = a.offsets[e + 1] - a.offsets[e];
+    if (a.expert_tokens) a.expert_tokens[e] = a.tokens_cumsum ? (int64_t)a.offsets[e + 1] : (int64_t)c;
+    if (a.expert_token_nums) a.expert_token_nums[e] = c;
+  }
+  // 3. segment table of the grouped GEMMs: routed experts, then shared
+  //    experts (shared_rows rows each); 128-row tiles, prefix in tiles.
+  if (a.seg_mprefix) {
+    const int nseg = a.num_experts + a.n_shared;
+    const int64_t per2 = (nseg + nt - 1) / nt;
+    const int64_t l2 = threadIdx.x * per2;
+    const int64_t h2 = l2 + per2 < nseg ? l2 + per2 : nseg;
+    int64_t t = 0;
+    for (int64_t sg = l2; sg < h2; ++sg) {
+      const int64_t rows_s = sg < a.num_experts ? a.offsets[sg + 1] - a.offsets[sg] : a.shared_rows;
+      t += (rows_s + kBM - 1) / kBM;
+    }
+    int64_t tot2;
+    int64_t b2 = block_exclusive_scan(t, sh_warp, tot2);
+    for (int64_t sg = l2; sg < h2; ++sg) {
+      const int64_t rows_s = sg < a.num_experts ? a.offsets[sg + 1] - a.offsets[sg] : a.shared_rows;
+      a.seg_rows[sg] = (int32_t)rows_s;
+      a.seg_mprefix[sg] = (int32_t)b2;
+      b2 += (rows_s + kBM - 1) / kBM;
+    }
+    if (threadIdx.x == 0) a.seg_mprefix[nseg] = (int32_t)tot2;
+  }
+}
+
+template <typename IdT>
+__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+                                int units, const int32_t* __restrict__ bases,
+                                const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
+                                int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
+                                int32_t* __restrict__ pad_row) {
+  extern __shared__ int32_t sh_next[];  // [warps][E]: next free slot per expert
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int unit = blockIdx.x * wpb + warp;
+  if (unit >= units) return;
+  int32_t* next = sh_next + warp * num_experts;
+  for (int e = lane; e < num_experts; e += 32) next[e] = bases[(int64_t)e * units + unit];
+  __syncwarp();
+  const int64_t start = (int64_t)unit * chunk;
+  const int64_t end = start + chunk < rows ? start + chunk : rows;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t j0 = start; j0 < end; j0 += 32) {
+    const int64_t j = j0 + lane;
+    int key = -1;
+    if (j < end) {
+      const int64_t id = (int64_t)ids[j];
+      key = (id >= 0 && id < num_experts) ? (int)id : -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    int32_t dest = -1;
+    if (key >= 0) {
+      dest = next[key] + __popc(peers & lt);
+    }
+    __syncwarp();
+    if (key >= 0 && (peers & lt) == 0) next[key] += __popc(peers);
+    __syncwarp();
+    if (j < end) {
+      if (expanded_row_idx) expanded_row_idx[j] = dest;
+      if (key >= 0) {
+        if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
+        if (pad_row) pad_row[j] = seg_mprefix[key] * kBM + (dest - offsets[key]);
+      } else if (pad_row) {
+        pad_row[j] = -1;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+RoutePlan route_plan(int64_t rows, int num_experts) {
+  RoutePlan p;
+  p.rows = rows;
+  p.num_experts = num_experts;
+  // chunk: multiple of 32, at most ~1024 chunks
+  int64_t c = (rows + 1023) / 1024;
+  c = round_up(c < 256 ? 256 : c, 32);
+  p.chunk = (int)c;
+  p.units = (int)((rows + c - 1) / c);
+  if (p.units < 1) p.units = 1;
+  int wpb = (int)(40960 / (4 * (int64_t)num_experts));
+  p.warps_per_block = wpb < 1 ? 1 : (wpb > 8 ? 8 : wpb);
+  return p;
+}
+
+size_t route_workspace_bytes(const RoutePlan& p) {
+  return (size_t)round_up((int64_t)p.num_experts * p.units * 4, 256) +
+         (size_t)round_up(((int64_t)p.num_experts + 1) * 4, 256);
+}
+
+cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
+                         RouteOutputs o, int32_t* dev_err, cudaStream_t st) {
+  const int wpb = p.warps_per_block;
+  const int blocks = (p.units + wpb - 1) / wpb;
+  const size_t sh = (size_t)wpb * p.num_experts * sizeof(int32_t);
+  if (ids64)
+    k_route_hist<int64_t><<<blocks, wpb * 32, sh, st>>>((const int64_t*)ids, p.rows, p.num_experts, p.chunk,
+                                                         p.units, hist, dev_err);
+  else
+    k_route_hist<int32_t><<<blocks, wpb * 32, sh, st>>>((const int32_t*)ids, p.rows, p.num_experts, p.chunk,
+                                                         p.units, hist, dev_err);
+  RouteScanArgs a;
+  a.hist = hist;
+  a.num_experts = p.num_experts;
+  a.units = p.units;
+  a.rows = p.rows;
+  a.offsets = offsets;
+  a.sorted_row_idx = o.sorted_row_idx;
+  a.expert_tokens = o.expert_tokens;
+  a.tokens_cumsum = o.tokens_cumsum;
+  a.expert_token_nums = o.expert_token_nums;
+  a.seg_rows = o.seg_rows;
+  a.seg_mprefix = o.seg_mprefix;
+  a.n_shared = o.n_shared;
+  a.shared_rows = o.shared_rows;
+  k_route_scan<<<1, 1024, 0, st>>>(a);
+  if (ids64)
+    k_route_scatter<int64_t><<<blocks, wpb * 32, sh, st>>>((const int64_t*)ids, p.rows, p.num_experts,
+                                                            p.chunk, p.units, hist, offsets, o.seg_mprefix,
+                                                            o.expanded_row_idx, o.sorted_row_idx, o.pad_row);
+  else
+    k_route_scatter<int32_t><<<blocks, wpb * 32, sh, st>>>((const int32_t*)ids, p.rows, p.num_experts,
+                                                            p.chunk, p.units, hist, offsets, o.seg_mprefix,
+                                                            o.expanded_row_idx, o.sorted_row_idx, o.pad_row);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

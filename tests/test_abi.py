@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import routing_permute_mxfp8_gb300 as mm
+from routing_permute_mxfp8_gb300 import build as mmbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mm_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(mm.lib_path()):
+        mmbuild.build()
+    return mm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("mm_moe_init_routing", "mm_moe_token_permute", "mm_mega_moe", "mm_mx_quantize",
+                 "mm_prepare_weight_scales", "mm_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.mm_status_string(0) == b"ok"
+    assert lib.mm_status_string(3) == b"workspace too small"
+    assert mm.mm_version() >= 100
+
+
+def _ws(lib, fn, *args):
+    n = ctypes.c_size_t(0)
+    st = getattr(lib, fn)(*args, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_queries(lib):
+    st, n = _ws(lib, "mm_moe_init_routing_workspace_size", 16384, 8, 256)
+    assert st == 0 and n >= 16384 * 8 * 4
+    assert _ws(lib, "mm_moe_init_routing_workspace_size", 16384, 8, 0)[0] == 1
+    assert _ws(lib, "mm_moe_init_routing_workspace_size", 1 << 22, 4, 8)[0] == 1   # F >= 16777215
+    st, n = _ws(lib, "mm_mega_moe_workspace_size", 8192, 7168, 8, 256, 2048, 0, 0)
+    assert st == 0 and n > 8192 * 8 * 7168 * 3
+    assert _ws(lib, "mm_mega_moe_workspace_size", 64, 200, 2, 8, 128, 0, 0)[0] == 2   # H % 128
+    assert _ws(lib, "mm_mega_moe_workspace_size", 64, 256, 2, 8, 100, 0, 0)[0] == 2   # I % 128
+    assert _ws(lib, "mm_mega_moe_workspace_size", 64, 256, 33, 64, 128, 0, 0)[0] == 1  # topK > 32
+    assert _ws(lib, "mm_mega_moe_workspace_size", 64, 256, 2, 8, 128, 5, 0)[0] == 1   # shared > 4
+    assert lib.mm_moe_token_permute_out_rows(8, 6) == 6
+    assert lib.mm_moe_token_permute_out_rows(8, 0) == 8
+    assert lib.mm_moe_token_permute_out_rows(8, 20) == 8
+    assert lib.mm_moe_token_permute_out_rows(8, -3) == 5
+    assert lib.mm_moe_token_permute_out_rows(8, -30) == 0
+
+
+def _mega(lib, **kw):
+    a = dict(x=1, ids=1, w=1, gdt=0, w1=1, w2=1, s1=1, s2=1, wdt=24, layout=0, sw1=None, sw2=None, ss1=None,
+             ss2=None, swdt=24, s=0, bs=64, h=256, k=2, e=8, ep=1, inter=128, maxrecv=0, dqm=4, dqd=24, cqm=0,
+             act=b"swiglu", params=None, nparams=0, y=1, counts=None, exp=None, aq=None, asc=None, ws=None,
+             wsb=0, err=None, stream=None)
+    a.update(kw)
+    vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
+    return lib.mm_mega_moe(vp(a["x"]), vp(a["ids"]), vp(a["w"]), a["gdt"], vp(a["w1"]), vp(a["w2"]), vp(a["s1"]),
+                           vp(a["s2"]), a["wdt"], a["layout"], vp(a["sw1"]), vp(a["sw2"]), vp(a["ss1"]),
+                           vp(a["ss2"]), a["swdt"], a["s"], a["bs"], a["h"], a["k"], a["e"], a["ep"], a["inter"],
+                           a["maxrecv"], a["dqm"], a["dqd"], a["cqm"], a["act"], a["params"], a["nparams"],
+                           vp(a["y"]), vp(a["counts"]), vp(a["exp"]), vp(a["aq"]), vp(a["asc"]), vp(a["ws"]),
+                           a["wsb"], vp(a["err"]), a["stream"])
+
+
+def test_mega_moe_host_rejections(lib):
+    assert _mega(lib, ep=2) == 2                     # ep_world_size != 1
+    assert _mega(lib, cqm=3) == 2                    # combine quantisation
+    assert _mega(lib, dqm=0) == 2                    # pre-quantised pass-through
+    assert _mega(lib, act=b"gelu") == 2
+    assert _mega(lib, dqd=296) == 2                  # FP4 dispatch
+    assert _mega(lib, gdt=27 + 1) == 1               # gating weight dtype
+    assert _mega(lib, maxrecv=100) == 1              # below bs*k rows
+    assert _mega(lib, ws=None, wsb=0) == 3           # workspace missing
+    assert _mega(lib, bs=0) == 0                     # empty batch: nothing to do
+
+
+def test_permute_host_rejections(lib):
+    vp = lambda v: ctypes.c_void_p(16 * v)
+    call = lambda **kw: lib.mm_moe_token_permute(
+        vp(1), kw.get("dt", 27), vp(1), kw.get("idt", 3), 4, 2, kw.get("h", 128), kw.get("e", 2), 0,
+        kw.get("pad", 0), kw.get("q", -1), vp(1), vp(1), vp(1), None, 0, None, None)
+    assert call(pad=1) == 2          # padded_mode is not supported (as in the article)
+    assert call(q=9) == 2            # MXFP4
+    assert call(idt=0) == 1          # indices dtype
+    assert call(q=2, h=24) == 2      # H % 16 for MXFP8
+    assert call() == 3               # workspace missing

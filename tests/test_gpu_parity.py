@@ -1,0 +1,264 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer, index, FP8 and E8M0 outputs of routing / permute / quantisation
+must be bit-exact.  MegaMoE's Y must satisfy the BASELINE tolerance
+(relative Frobenius error <= 5e-3, max abs error <= 2e-2 * max|Y|), and the
+activation codes that follow GEMM1 may differ by one code step in at most
+0.1 % of elements (the GEMM sums in fp32 on the tensor cores, the oracle in
+double).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import routing_permute_mxfp8_gb300 as mm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+Y_REL_FROB = 5e-3
+Y_MAX_ABS = 2e-2
+ACT_FRAC = 1e-3
+
+
+def t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def bf16(bits):
+    return t(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def host(x):
+    torch.cuda.synchronize()
+    if x.dtype in (torch.bfloat16, torch.float16):
+        return x.view(torch.int16).cpu().numpy().view(np.uint16)
+    if x.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return x.view(torch.uint8).cpu().numpy()
+    return x.cpu().numpy()
+
+
+def zeros_err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+# ------------------------------------------------------------- routing + permute
+ROUTE_CASES = [
+    # n, h, e, k, quant, ids kind
+    (1000, 512, 64, 8, -1, "distinct"),
+    (1000, 512, 64, 8, 2, "distinct"),
+    (1000, 512, 64, 8, 3, "distinct"),
+    (1, 16, 1, 1, 3, "distinct"),
+    (333, 160, 300, 7, 3, "distinct"),           # ragged H (5 groups), E not a power of two
+    (2048, 48, 5, 3, 2, "any"),                  # repeated experts in a token, odd group count
+    (4096, 1024, 2048, 4, 3, "distinct"),        # many experts
+    (16384, 7168, 256, 8, -1, "distinct"),       # full routing workload, bf16 copy
+    (16384, 7168, 256, 8, 3, "distinct"),        # full routing workload, MXFP8 E4M3
+]
+
+
+def _ids(n, e, k, kind, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "distinct":
+        return np.argsort(rng.random((n, e)), axis=1)[:, :k].astype(np.int32)
+    return rng.integers(0, e, (n, k)).astype(np.int32)
+
+
+@pytest.mark.parametrize("n,h,e,k,quant,kind", ROUTE_CASES)
+def test_init_routing_bit_exact(n, h, e, k, quant, kind):
+    cfg = synth.CONFIGS["routing"].scaled(n=n, h=h, e=e, k=k)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg) if kind == "distinct" and (n, h) == (16384, 7168) else _ids(n, e, k, kind, n + e)
+    err = zeros_err()
+    for ttype in (0, 1):
+        ex, exp_idx, tok, sc, srt = mm.mm_moe_init_routing(bf16(x), t(ids), e, quant, ttype, dev_err=err)
+        r_srt, r_exp, r_cnt, bad = oracle.route(ids, e)
+        assert bad == 0 and host(err)[0] == 0
+        assert np.array_equal(host(srt), r_srt)
+        assert np.array_equal(host(exp_idx), r_exp)
+        assert np.array_equal(host(tok), np.cumsum(r_cnt) if ttype == 0 else r_cnt)
+    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    r_out, r_sc = oracle.permute(x, oracle.DT_BF16, k, r_srt, n * k, fmt=fmt)
+    assert np.array_equal(host(ex), r_out)
+    if quant != -1:
+        assert np.array_equal(host(sc), r_sc)
+
+
+@pytest.mark.parametrize("dtype,idx64,num_out,quant,one_d", [
+    (torch.bfloat16, False, 6, -1, False),
+    (torch.float16, True, 0, 2, False),
+    (torch.float16, False, -5, 3, False),
+    (torch.float32, False, 100000, -1, False),
+    (torch.bfloat16, True, None, 3, True),
+])
+def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d):
+    n, h, e, k = 700, 256, 16, 1 if one_d else 4
+    rng = np.random.default_rng(9)
+    xf = rng.standard_normal((n, h)).astype(np.float32)
+    xt = torch.from_numpy(xf).to(dtype)
+    ids = _ids(n, e, k, "distinct", 4)
+    ids_t = t(ids.reshape(-1) if one_d else ids)
+    if idx64:
+        ids_t = ids_t.long()
+    perm, sidx, sc = mm.mm_moe_token_permute(xt.to(DEV), ids_t, e, num_out_tokens=num_out, quant_mode=quant)
+    r_srt, r_exp, _, _ = oracle.route(ids, e)
+    m = n * k if not num_out else (min(num_out, n * k) if num_out > 0 else max(n * k + num_out, 0))
+    assert perm.shape[0] == m and sidx.shape[0] == n * k
+    assert np.array_equal(host(sidx), r_exp)
+    src_dt = {torch.bfloat16: oracle.DT_BF16, torch.float16: oracle.DT_F16, torch.float32: oracle.DT_F32}[dtype]
+    src = xt.view(torch.int16).numpy().view(np.uint16) if dtype != torch.float32 else xf
+    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    r_out, r_sc = oracle.permute(src, src_dt, k, r_srt, m, fmt=fmt)
+    got = host(perm)
+    assert np.array_equal(got.view(r_out.dtype) if fmt < 0 else got, r_out)
+    if quant != -1:
+        assert np.array_equal(host(sc), r_sc)
+
+
+def test_out_of_range_ids_are_left_out_and_flagged():
+    ids = np.array([[0, 5], [2, -1], [1, 0]], dtype=np.int32)
+    x = synth.f32_to_bf16_bits(np.arange(3 * 32, dtype=np.float32).reshape(3, 32))
+    err = zeros_err()
+    ex, exp_idx, tok, _, srt = mm.mm_moe_init_routing(bf16(x), t(ids), 3, -1, 1, dev_err=err)
+    r_srt, r_exp, r_cnt, bad = oracle.route(ids, 3)
+    assert bad == 2
+    assert host(err)[0] & 1
+    assert np.array_equal(host(srt), r_srt)
+    assert np.array_equal(host(exp_idx), r_exp)
+    assert np.array_equal(host(tok), r_cnt)
+    r_out, _ = oracle.permute(x, oracle.DT_BF16, 2, r_srt, 4)
+    assert np.array_equal(host(ex)[:4], r_out)
+
+
+# ---------------------------------------------------------------- MX quantiser
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("fmt", [23, 24])
+def test_mx_quantize_bit_exact(dtype, fmt):
+    rng = np.random.default_rng(fmt)
+    rows, cols = 513, 320
+    x = rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-20, 12, (rows, 1)))
+    x[0, :32] = 0.0
+    x[1, :32] = -0.0
+    x[2, 5] = 1e30 if dtype == torch.float32 else 3e4
+    x[3, :] = 1e-41 if dtype == torch.float32 else 1e-7     # fp32 subnormals / tiny values
+    x[4, 7] = -448.0 * 1.0001
+    xt = torch.from_numpy(x.astype(np.float32)).to(dtype)
+    q, s = mm.mm_mx_quantize(xt.to(DEV), fmt)
+    src_dt = {torch.bfloat16: oracle.DT_BF16, torch.float16: oracle.DT_F16, torch.float32: oracle.DT_F32}[dtype]
+    src = xt.view(torch.int16).numpy().view(np.uint16) if dtype != torch.float32 else xt.numpy()
+    rq, rs = oracle.mx_quantize(src, src_dt, fmt, s_cols=s.shape[1])
+    assert np.array_equal(host(s), rs)
+    assert np.array_equal(host(q), rq)
+
+
+# -------------------------------------------------------------------- MegaMoE
+def _weights(cfg, shared=False):
+    w1, s1 = oracle.quantized_weights(cfg, 1, shared=shared)
+    w2, s2 = oracle.quantized_weights(cfg, 2, shared=shared)
+    return w1, s1, w2, s2
+
+
+def _code_ord(c):
+    c = c.astype(np.int32)
+    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+
+def check_act(aq_gpu, as_gpu, exp_idx, aq_ref, as_ref, tokens, k):
+    """Activation codes of sampled tokens: scales equal and codes within one
+    step, except in at most ACT_FRAC of the elements."""
+    rows = exp_idx.reshape(-1, k)[tokens]                      # [T, K] sorted rows
+    g = aq_gpu[rows]                                           # [T, K, I]
+    gs = as_gpu[rows]                                          # [T, K, I/32]
+    same_scale = np.repeat(gs == as_ref, 32, axis=-1)
+    step = np.abs(_code_ord(g) - _code_ord(aq_ref))
+    bad = (~same_scale) | (step > 1)
+    diff = (step != 0) | (~same_scale)
+    assert bad.mean() <= ACT_FRAC, (bad.mean(), diff.mean())
+    assert diff.mean() <= ACT_FRAC, diff.mean()
+
+
+def check_y(y_gpu, y_ref):
+    yg = y_gpu.astype(np.float64)
+    rel = np.linalg.norm(yg - y_ref) / np.linalg.norm(y_ref)
+    mx = np.abs(yg - y_ref).max() / np.abs(y_ref).max()
+    assert rel <= Y_REL_FROB, rel
+    assert mx <= Y_MAX_ABS, mx
+    return rel, mx
+
+
+def run_mega(cfg, tokens=None, layout=0, check_acts=True):
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    sh = _weights(cfg, shared=True) if cfg.shared else None
+    gt = bf16(gate) if gate.dtype == np.uint16 else t(gate)
+    ws1, ws2 = t(s1), t(s2)
+    if layout == 1:
+        ws1 = mm.mm_prepare_weight_scales(ws1, cfg.h)
+        ws2 = mm.mm_prepare_weight_scales(ws2, cfg.inter)
+    kw = {}
+    if sh is not None:
+        sw1, ss1, sw2, ss2 = [t(a) for a in sh]
+        if layout == 1:
+            ss1 = mm.mm_prepare_weight_scales(ss1, cfg.h)
+            ss2 = mm.mm_prepare_weight_scales(ss2, cfg.inter)
+        kw = dict(shared_weight1=sw1, shared_weight2=sw2, shared_weight_scales1=ss1, shared_weight_scales2=ss2)
+    err = zeros_err()
+    y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
+        bf16(x), t(ids), gt, t(w1), t(w2), ws1, ws2, cfg.e, weight_dtype=cfg.weight_fmt, weight_scale_layout=layout,
+        dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err, want_expanded_row_idx=True, want_act=True, **kw)
+    assert host(err)[0] == 0
+    r_srt, r_exp, r_cnt, _ = oracle.route(ids, cfg.e)
+    assert np.array_equal(host(counts), r_cnt.astype(np.int32))
+    assert np.array_equal(host(exp_idx), r_exp)
+    tok = np.arange(cfg.n) if tokens is None else np.asarray(tokens)
+    y_ref, _, aq_ref, as_ref = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt,
+                                                      cfg.weight_fmt, tokens=tok, shared=sh, want_act=True)
+    yg = host(y).view(np.uint16)
+    yg = synth.bf16_bits_to_f32(yg)[tok]
+    if check_acts:
+        check_act(host(aq), host(a_s), r_exp, aq_ref, as_ref, tok, cfg.k)
+    return check_y(yg, y_ref), host(y)
+
+
+MEGA_CASES = {
+    "tiny": dict(),
+    "tiny_e5m2_zipf_bf16gate": dict(dispatch_fmt=23, routing="zipf", gate_dtype="bf16"),
+    "tiny_e5m2_weights": dict(weight_fmt=23),
+    "tiny_shared": dict(shared=1),
+    "tiny_ragged": dict(n=37, e=5, k=3),
+    "tiny_k1_e1": dict(n=200, e=1, k=1),
+    "wide": dict(n=300, h=1024, inter=384, e=16, k=4),
+}
+
+
+@pytest.mark.parametrize("case", list(MEGA_CASES))
+def test_mega_moe_small(case):
+    cfg = synth.CONFIGS["tiny"].scaled(**MEGA_CASES[case])
+    run_mega(cfg)
+
+
+def test_mega_moe_prepared_scales_identical():
+    cfg = synth.CONFIGS["tiny"].scaled(shared=1, n=96)
+    _, y0 = run_mega(cfg, layout=0)
+    _, y1 = run_mega(cfg, layout=1)
+    assert np.array_equal(y0, y1)
+
+
+def test_mega_moe_qwen3_shape_sampled():
+    cfg = synth.CONFIGS["qwen3"].scaled(n=512)
+    run_mega(cfg, tokens=np.arange(0, 512, 7))
+
+
+def test_mega_moe_duplicate_ids_flagged():
+    cfg = synth.CONFIGS["tiny"]
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    ids[3, 1] = ids[3, 0]
+    gate = synth.topk_weights(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    err = zeros_err()
+    mm.mm_mega_moe(bf16(x), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err)
+    assert host(err)[0] & 2
