@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Throughput of the MoE expert-FFN hot path on GB300 (MegaMoE at
+ep_world_size = 1: routing -> permute + MX quant -> grouped GEMM1 + swiglu +
+MX requant -> grouped GEMM2 -> top-K combine), one mm_mega_moe call per step.
+
+Workload (one GPU): DeepSeek-V3-shaped prefill, N=8192 tokens, hidden 7168,
+intermediate 2048, 256 experts, top-8 with Zipf(s=1) routing, MXFP8 E5M2
+dispatch, MXFP8 E4M3 weights with E8M0 scales (prepared once, like a load-time
+weight format), bf16 gating weights.  Inputs are seeded and synthetic and are
+resident in HBM before timing; the 11.6 GB of weights exceed L2, so no flush
+is needed between steps.
+
+Printed: one JSON line (rank 0).  Secondary measurements in the same line:
+the routing/permute workload (N=16384, H=7168, E=256, K=8; HBM GB/s of the
+permute kernel), the Qwen3-30B-A3B-shaped and the decode (N=128 + one shared
+expert) workloads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torchrun) each rank runs its own replica of the workload
+(token sharding, no collective on the data path); value = all ranks' tokens
+divided by the slowest rank's time.  --impl reference times the CPU oracle
+(the only reference implementation of this method) on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE FFN tokens/s + MXFP8 TFLOP/s (% peak); permute HBM GB/s (% peak)"
+NOMINAL_FP8_OVER_BF16 = 2.0   # 4.5 / 2.25 PFLOP/s dense
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv3_prefill")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override N (profiling on a smaller case)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling on a smaller case)")
+    return ap.parse_args()
+
+
+def workload(args):
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = cfg.scaled(n=args.tokens)
+    if args.experts:
+        cfg = cfg.scaled(e=args.experts)
+    return cfg
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [s for s, p in zip(sm, power) if p > 200.0] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_source_hash(name):
+    return hashlib.sha256(open(os.path.join(ROOT, "routing_permute_mxfp8_gb300", "csrc", name), "rb").read()
+                          ).hexdigest()[:16]
+
+
+def profiled_traffic(profile_file, kernel_src):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (its sha256 prefix is recorded there)."""
+    p = os.path.join(ROOT, "profiles", profile_file)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash(kernel_src):
+        return None
+    return float(m_tr.group(1))
+
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as tdist
+            import torch
+            torch.cuda.set_device(self.local)
+            tdist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.pg = tdist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- inputs on the GPU
+def gpu_inputs(cfg, mm, torch, seed_offset=0, weights=None):
+    """x, ids, gates from the seeded generator; fp32 N(0, 0.02) weights drawn on
+    the GPU (seeded torch generator) and MX-quantised by the library."""
+    import synth
+    dev = torch.device("cuda")
+    x = torch.from_numpy(synth.tokens_bf16(cfg).view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(synth.topk_ids(cfg)).to(dev)
+    g = synth.topk_weights(cfg)
+    gate = (torch.from_numpy(g.view(np.int16)).to(dev).view(torch.bfloat16) if g.dtype == np.uint16
+            else torch.from_numpy(g).to(dev))
+    if weights is None:
+        weights = gpu_weights(cfg, mm, torch, cfg.e, seed=1000 + seed_offset)
+    shared = None
+    if cfg.shared:
+        shared = gpu_weights(cfg, mm, torch, cfg.shared, seed=2000 + seed_offset)
+    return x, ids, gate, weights, shared
+
+
+def gpu_weights(cfg, mm, torch, n_exp, seed):
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    out = []
+    for n_out, k_red in ((2 * cfg.inter, cfg.h), (cfg.h, cfg.inter)):
+        q = torch.empty((n_exp, n_out, k_red), dtype=torch.uint8, device=dev)
+        s = torch.empty((n_exp, n_out, k_red // 32), dtype=torch.uint8, device=dev)
+        chunk = max(1, (1 << 28) // (n_out * k_red))
+        for e0 in range(0, n_exp, chunk):
+            e1 = min(n_exp, e0 + chunk)
+            w = torch.randn(((e1 - e0) * n_out, k_red), generator=gen, device=dev, dtype=torch.float32) * 0.02
+            qq, ss = mm.mm_mx_quantize(w, cfg.weight_fmt, scale_cols=k_red // 32)
+            q[e0:e1] = qq.view(e1 - e0, n_out, k_red)
+            s[e0:e1] = ss.view(e1 - e0, n_out, k_red // 32)
+            del w, qq, ss
+        out += [q, s]
+    w1, s1, w2, s2 = out
+    p1 = mm.mm_prepare_weight_scales(s1, cfg.h)
+    p2 = mm.mm_prepare_weight_scales(s2, cfg.inter)
+    return {"w1": w1, "s1": s1, "w2": w2, "s2": s2, "p1": p1, "p2": p2}
+
+
+def mega_call(mm, cfg, x, ids, gate, W, S, ws, y):
+    kw = {}
+    if S is not None:
+        kw = dict(shared_weight1=S["w1"], shared_weight2=S["w2"], shared_weight_scales1=S["p1"],
+                  shared_weight_scales2=S["p2"], shared_weight_dtype=cfg.weight_fmt)
+    return mm.mm_mega_moe(x, ids, gate, W["w1"], W["w2"], W["p1"], W["p2"], cfg.e, weight_dtype=cfg.weight_fmt,
+                          weight_scale_layout=mm.WSCALE_PREPARED, dispatch_quant_out_dtype=cfg.dispatch_fmt,
+                          workspace=ws, out=y, **kw)
+
+
+def ffn_flops(cfg, tokens=None):
+    n = cfg.n if tokens is None else tokens
+    rows = n * cfg.k + n * cfg.shared
+    return 2.0 * rows * (2 * cfg.inter) * cfg.h + 2.0 * rows * cfg.h * cfg.inter
+
+
+def time_steps(torch, fn, steps, warmup, dist, sampler_gpu=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    import routing_permute_mxfp8_gb300 as mm
+    mm.timing_read()
+    mm.timing_enable(True)
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks = None
+    if sampler_gpu is not None:
+        sampler = ClockSampler(sampler_gpu)
+        sampler.__enter__()
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    e1.synchronize()
+    if sampler_gpu is not None:
+        sampler.__exit__(None, None, None)
+        clocks = sampler.summary()
+    mm.timing_enable(False)
+    stages = mm.timing_read()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = e0.elapsed_time(e1)
+    return ms, stages, clocks
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_leg(cfg, rows_per_step, steps, warmup, max_experts=16):
+    """Times the CPU oracle as it stands on a bounded sample of the workload.
+
+    One step = the oracle's routing of the whole batch (keyValueSort, inverse,
+    histogram of all N*K ids) plus, for `rows_per_step` sampled expanded rows
+    (token i, choice k), the oracle's Q_MX of the token and its expert FFN
+    (GEMM1 + swiglu + Q_MX + GEMM2), rows spread over the host cores (ctypes
+    drops the GIL).  Rows are drawn among the experts touched first so that
+    only `max_experts` experts' weights need building.  Returns token
+    equivalents per second (rows / K per second) and details.
+    """
+    import concurrent.futures as cf
+    import oracle
+    import synth
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    chosen = []
+    for e in ids.reshape(-1):
+        if e not in chosen:
+            chosen.append(int(e))
+        if len(chosen) == max_experts:
+            break
+    cand = np.nonzero(np.isin(ids.reshape(-1), chosen))[0]
+    rng = np.random.default_rng(123)
+    total_rows = rows_per_step * (steps + warmup)
+    pick = rng.choice(cand, size=total_rows, replace=cand.size < total_rows)
+    s1c, s2c = 2 * ((cfg.h + 63) // 64), 2 * ((cfg.inter + 63) // 64)
+    W = {}
+    for e in chosen:
+        w1, s1 = oracle.mx_quantize(synth.weight_f32(cfg, 1, e), oracle.DT_F32, cfg.weight_fmt, s1c)
+        w2, s2 = oracle.mx_quantize(synth.weight_f32(cfg, 2, e), oracle.DT_F32, cfg.weight_fmt, s2c)
+        W[e] = (w1, s1, w2, s2)
+    flat = ids.reshape(-1)
+
+    def one_row(j):
+        i = j // cfg.k
+        xq, xs = oracle.mx_quantize(x[i:i + 1], oracle.DT_BF16, cfg.dispatch_fmt)
+        w1, s1, w2, s2 = W[int(flat[j])]
+        return oracle.expert_row(xq[0], xs[0], cfg.dispatch_fmt, w1, s1, w2, s2, cfg.weight_fmt, cfg.dispatch_fmt)
+
+    threads = min(rows_per_step, os.cpu_count() or 1)
+    times = []
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for st in range(steps + warmup):
+            rows = pick[st * rows_per_step:(st + 1) * rows_per_step]
+            t0 = time.perf_counter()
+            oracle.route(ids, cfg.e)
+            list(ex.map(one_row, rows))
+            dt = time.perf_counter() - t0
+            if st >= warmup:
+                times.append(dt)
+    total = sum(times)
+    tok_per_s = rows_per_step * len(times) / cfg.k / total
+    return tok_per_s, {
+        "cores": threads, "seconds": total,
+        "sample": (f"{len(times)} step(s) x [routing of all {cfg.n * cfg.k} ids of {cfg.name} + Q_MX and expert "
+                   f"FFN of {rows_per_step} sampled expanded rows]; value = rows / top-K per second; double "
+                   f"precision on {threads} host threads")}
+
+
+# ----------------------------------------------------------------------------- main arms
+def run_reference(args):
+    import synth
+    dist_rank = int(os.environ.get("RANK", "0"))
+    if dist_rank != 0:
+        return 0
+    cfg = workload(args)
+    k_eff = max(1, args.steps)
+    w_eff = max(0, args.warmup)
+    # about one row per host core per step keeps the whole run within a few minutes
+    per_step = max(1, min(os.cpu_count() or 1, 16))
+    val, info = oracle_leg(cfg, per_step, k_eff, w_eff)
+    ms_step = info["seconds"] / k_eff * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": k_eff, "warmup": w_eff, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": cfg.name, "tokens": cfg.n, "hidden": cfg.h, "intermediate": cfg.inter,
+                   "experts": cfg.e, "topk": cfg.k, "routing": cfg.routing},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": info["sample"]},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import synth
+    import routing_permute_mxfp8_gb300 as mm
+
+    dist = Dist(args.gpus)
+    torch.cuda.set_device(dist.local)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    gpu_index = vis.split(",")[dist.local].strip() if vis else str(dist.local)
+    mm.load()
+    peaks, peak_src = load_peaks()
+    hbm_peak = peaks["hbm_gbs"]
+    fp8_peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * NOMINAL_FP8_OVER_BF16
+    fp8_peak_burst = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
+
+    cfg = workload(args)
+    x, ids, gate, W, S = gpu_inputs(cfg, mm, torch, seed_offset=dist.rank)
+    need = mm.mm_mega_moe_workspace_size(cfg.n, cfg.h, cfg.k, cfg.e, cfg.inter, cfg.shared, mm.WSCALE_PREPARED)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y = torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device="cuda")
+    fn = lambda: mega_call(mm, cfg, x, ids, gate, W, S, ws, y)
+    ms, stages, clocks = time_steps(torch, fn, args.steps, args.warmup, dist, sampler_gpu=gpu_index)
+    ms = dist.max(ms)
+    ms_step = ms / args.steps
+    tokens_total = cfg.n * args.steps * dist.world
+    value = tokens_total / (ms / 1e3)
+    flops = ffn_flops(cfg)
+    launches = sum(c for _, c in stages.values())
+    g1_ms = stages["gemm1"][0] / max(1, stages["gemm1"][1])
+    g2_ms = stages["gemm2"][0] / max(1, stages["gemm2"][1])
+    g1_flops = 2.0 * (cfg.n * cfg.k + cfg.n * cfg.shared) * 2 * cfg.inter * cfg.h
+    g1_tflops = g1_flops / (g1_ms / 1e3) / 1e12
+    traffic = profiled_traffic(f"gemm1_{cfg.name}.md", "gemm.cu")
+    roofline = {"bound": "tensor", "kernel": "k_gemm_mx<1> (GEMM1 + swiglu + MX requant)",
+                "achieved": g1_tflops, "peak": fp8_peak_sus, "unit": "TFLOP/s", "frac": g1_tflops / fp8_peak_sus,
+                "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 sustained x {NOMINAL_FP8_OVER_BF16:g} (nominal FP8/bf16 ratio)",
+                "algorithmic_flops_per_launch": g1_flops, "avg_launch_ms": g1_ms}
+    stage_ms = {k: (v[0] / max(1, v[1]) if v[1] else 0.0) for k, v in stages.items() if v[1]}
+    per_step_stage_ms = {k: v[0] / args.steps for k, v in stages.items() if v[1]}
+
+    # end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        idh = ids.cpu().pin_memory()
+        gh = gate.cpu().pin_memory()
+        yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        xd, idd, gd = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(gate)
+
+        def e2e_fn():
+            xd.copy_(xh, non_blocking=True)
+            idd.copy_(idh, non_blocking=True)
+            gd.copy_(gh, non_blocking=True)
+            mega_call(mm, cfg, xd, idd, gd, W, S, ws, y)
+            yh.copy_(y, non_blocking=True)
+
+        e_steps = max(1, min(args.steps, 50))
+        ems, _, _ = time_steps(torch, e2e_fn, e_steps, min(args.warmup, 3), dist)
+        ems = dist.max(ems)
+        h2d = x.numel() * 2 + ids.numel() * 4 + gate.numel() * gate.element_size()
+        e2e = {"value": cfg.n * e_steps * dist.world / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(y.numel() * 2),
+               "ms_per_step": ems / e_steps}
+
+    secondary = {}
+    if not args.no_secondary:
+        secondary = secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak_sus, W, cfg)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded generator; random-init weights)",
+        "config": {"workload": cfg.name, "tokens": cfg.n, "hidden": cfg.h, "intermediate": cfg.inter,
+                   "experts": cfg.e, "topk": cfg.k, "routing": f"{cfg.routing}" + (" s=1.0" if cfg.routing == "zipf" else ""),
+                   "dispatch": "mxfp8_e5m2" if cfg.dispatch_fmt == 23 else "mxfp8_e4m3",
+                   "weights": "mxfp8_e4m3" if cfg.weight_fmt == 24 else "mxfp8_e5m2",
+                   "gate": cfg.gate_dtype, "shared_experts": cfg.shared,
+                   "weight_scale_layout": "prepared once (mm_prepare_weight_scales)",
+                   "l2": "inputs larger than L2 (weights streamed from HBM every step)",
+                   "parallelism": f"replica per GPU x{dist.world} (token sharding, no collective)"},
+        "tflops": flops / (ms_step / 1e3) / 1e12,
+        "tflops_frac_of_fp8_peak": flops / (ms_step / 1e3) / 1e12 / fp8_peak_sus,
+        "roofline": roofline,
+        "stage_ms_per_launch": stage_ms,
+        "stage_ms_per_step": per_step_stage_ms,
+        "gemm2_tflops": 2.0 * (cfg.n * cfg.k + cfg.n * cfg.shared) * cfg.h * cfg.inter / (g2_ms / 1e3) / 1e12,
+        "gpu_launches": launches,
+        "gpu_launches_per_step": launches / args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "peaks": {"hbm_gbs": hbm_peak, "fp8_tflops_sustained": fp8_peak_sus, "fp8_tflops_burst": fp8_peak_burst,
+                  "source": peak_src},
+    }
+    line.update(secondary)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        val, info = oracle_leg(cfg, max(1, min(os.cpu_count() or 1, 16)), 1, 0)
+        line["cpu_baseline"] = {"value": val, "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+                                "sample": info["sample"]}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_prefill, cfg_prefill):
+    out = {}
+    steps = max(10, min(args.steps, 50))
+    # routing / permute workload: HBM bandwidth of the permute kernel
+    rc = synth.CONFIGS["routing"]
+    xr = torch.from_numpy(synth.tokens_bf16(rc).view(np.int16)).cuda().view(torch.bfloat16)
+    idr = torch.from_numpy(synth.topk_ids(rc)).cuda()
+    rows = rc.n * rc.k
+    perm = {}
+    for name, q in (("mxfp8_e4m3", mm.QUANT_MXFP8_E4M3FN), ("bf16", mm.QUANT_NONE)):
+        need = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+        fn = lambda: mm.mm_moe_init_routing(xr, idr, rc.e, q, 1, workspace=need)
+        ms, st, _ = time_steps(torch, fn, steps, 3, dist)
+        d_ms = st["dispatch"][0] / max(1, st["dispatch"][1])
+        r_ms = st["route"][0] / max(1, st["route"][1])
+        out_b = rows * rc.h * (1 if q != mm.QUANT_NONE else 2) + (rows * (rc.h // 32) if q != mm.QUANT_NONE else 0)
+        dispatch_bytes = rc.n * rc.h * 2 + rows * 4 + out_b           # read x + dest idx, write rows (+scales)
+        call_bytes = dispatch_bytes + rows * 4 * 3 + rc.e * 8          # + ids read, idx writes, counts
+        perm[name] = {"dispatch_us": d_ms * 1e3, "dispatch_gbs": dispatch_bytes / (d_ms / 1e3) / 1e9,
+                      "dispatch_frac": dispatch_bytes / (d_ms / 1e3) / 1e9 / hbm_peak,
+                      "route_us": r_ms * 1e3, "call_us": ms / steps * 1e3,
+                      "call_gbs": call_bytes / (ms / steps / 1e3) / 1e9,
+                      "dispatch_bytes": dispatch_bytes}
+    out["permute"] = {"workload": "routing N=16384 H=7168 E=256 K=8 uniform", "unit": "GB/s",
+                      "peak_gbs": hbm_peak, **perm}
+    del xr
+    # Qwen3-30B-A3B-shaped FFN
+    qc = synth.CONFIGS["qwen3"]
+    x, ids, gate, W, S = gpu_inputs(qc, mm, torch, seed_offset=10 + dist.rank)
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(qc.n, qc.h, qc.k, qc.e, qc.inter, 0, 1), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty((qc.n, qc.h), dtype=torch.bfloat16, device="cuda")
+    ms, st, _ = time_steps(torch, lambda: mega_call(mm, qc, x, ids, gate, W, S, ws, y), steps, 3, dist)
+    t = ms / steps / 1e3
+    out["qwen3"] = {"tokens_per_s": qc.n / t, "ms_per_step": t * 1e3, "tflops": ffn_flops(qc) / t / 1e12,
+                    "tflops_frac": ffn_flops(qc) / t / 1e12 / fp8_peak,
+                    "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+    del x, W, ws
+    # decode: same expert weights as the prefill workload, plus one shared expert
+    dc = synth.CONFIGS["dsv3_decode"]
+    x, ids, gate, _, S = gpu_inputs(dc, mm, torch, seed_offset=20 + dist.rank, weights=W_prefill)
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(dc.n, dc.h, dc.k, dc.e, dc.inter, dc.shared, 1),
+                     dtype=torch.uint8, device="cuda")
+    y = torch.empty((dc.n, dc.h), dtype=torch.bfloat16, device="cuda")
+    ms, st, _ = time_steps(torch, lambda: mega_call(mm, dc, x, ids, gate, W_prefill, S, ws, y), steps, 3, dist)
+    t = ms / steps / 1e3
+    touched = int(torch.unique(ids).numel())
+    per_exp = 3 * dc.h * dc.inter * (1 + 1 / 32)
+    wbytes = (touched + dc.shared) * per_exp
+    out["decode"] = {"tokens_per_s": dc.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
+                     "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
+                     "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+    return out
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -244,6 +244,29 @@ mm_status mm_prepare_weight_scales(const uint8_t* src, int64_t experts, int64_t 
 mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t cols, int out_dtype,
                          uint8_t* q, uint8_t* scales, int64_t scale_cols, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Stage timing and launch counts (diagnostics; not part of the pages' API).
+ *
+ * mm_timing_enable(1) makes every following call record a CUDA event pair
+ * on its stream around each of its stages (MM_STAGE_*); mm_timing_enable(0)
+ * stops that.  mm_timing_read waits for the recorded events, writes for
+ * each stage s < n the device time summed over all recorded calls
+ * (stage_ms[s], milliseconds) and the number of kernels launched since the
+ * previous read (stage_launches[s], counted whether timing is on or not),
+ * then resets both.  Host-side state only; not thread-safe across
+ * concurrent callers on different streams.
+ * ---------------------------------------------------------------------- */
+#define MM_STAGE_WSCALE 0   /* weight-scale layout conversion */
+#define MM_STAGE_ROUTE 1    /* histogram, scan, stable scatter */
+#define MM_STAGE_DISPATCH 2 /* permute / MX quantisation */
+#define MM_STAGE_GEMM1 3    /* grouped GEMM1 + swiglu + MX requant */
+#define MM_STAGE_GEMM2 4    /* grouped GEMM2 */
+#define MM_STAGE_COMBINE 5  /* weighted top-K combine */
+#define MM_STAGE_DIAG 6     /* optional diagnostic outputs */
+#define MM_STAGE_COUNT 7
+mm_status mm_timing_enable(int on);
+mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -275,3 +275,26 @@ def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None =
     _check(L.mm_mx_quantize(_ptr(src), _dt(src), rows, cols, out_dtype, _ptr(q), _ptr(s), sc,
                             _stream(src.device)), "mm_mx_quantize")
     return q, s
+
+
+# --------------------------------------------------------------------------- diagnostics
+STAGES = ("wscale", "route", "dispatch", "gemm1", "gemm2", "combine", "diag")
+
+
+def timing_enable(on: bool = True):
+    """Record CUDA events around every stage of the following calls (mm_timing_enable)."""
+    L = load()
+    L.mm_timing_enable.argtypes, L.mm_timing_enable.restype = [ctypes.c_int], ctypes.c_int
+    _check(L.mm_timing_enable(1 if on else 0), "mm_timing_enable")
+
+
+def timing_read():
+    """{stage: (device ms summed over recorded calls, kernel launches)} since the last read."""
+    L = load()
+    n = len(STAGES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    L.mm_timing_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    L.mm_timing_read.restype = ctypes.c_int
+    _check(L.mm_timing_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p), n), "mm_timing_read")
+    return {s: (ms[i], int(cnt[i])) for i, s in enumerate(STAGES)}

@@ -4,6 +4,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
 #include "mm_route.cuh"
 
 using namespace mm;
@@ -112,6 +115,67 @@ mm_status check_mega_shapes(int64_t bs, int64_t h, int64_t k, int64_t e, int64_t
   return MM_OK;
 }
 
+// ---- stage timing (diagnostic, off by default) ----------------------------
+// While enabled, every entry point records a CUDA event pair around each of
+// its stages on the caller's stream; mm_timing_read sums the device time.
+// Launch counts are kept whether or not timing is on.
+struct StageTimer {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<cudaEvent_t> open[MM_STAGE_COUNT];  // begin, end, begin, end, ...
+  int64_t launches[MM_STAGE_COUNT] = {0};
+};
+StageTimer& timer() {
+  static StageTimer t;
+  return t;
+}
+
+cudaEvent_t take_event(StageTimer& t) {
+  if (!t.pool.empty()) {
+    cudaEvent_t ev = t.pool.back();
+    t.pool.pop_back();
+    return ev;
+  }
+  cudaEvent_t ev = nullptr;
+  cudaEventCreate(&ev);
+  return ev;
+}
+
+// One stage of one call: constructor records the begin event, finish() the
+// end event and adds the number of kernels the stage launched.
+struct StageScope {
+  int stage;
+  cudaStream_t st;
+  bool active;
+  StageScope(int s, cudaStream_t stream) : stage(s), st(stream), active(false) {
+    StageTimer& t = timer();
+    std::lock_guard<std::mutex> g(t.mu);
+    if (t.on) {
+      cudaEvent_t ev = take_event(t);
+      if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
+        t.open[stage].push_back(ev);
+        active = true;
+      }
+    }
+  }
+  void finish(int kernels) {
+    StageTimer& t = timer();
+    std::lock_guard<std::mutex> g(t.mu);
+    t.launches[stage] += kernels;
+    if (active) {
+      cudaEvent_t ev = take_event(t);
+      if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
+        t.open[stage].push_back(ev);
+      } else {
+        t.pool.push_back(t.open[stage].back());
+        t.open[stage].pop_back();
+      }
+      active = false;
+    }
+  }
+};
+
 bool activation_is_plain_swiglu(const char* act, const float* params, int64_t n) {
   if (act && strcmp(act, "swiglu") != 0) return false;
   if (n == 0) return true;
@@ -136,6 +200,38 @@ const char* mm_status_string(int status) {
 }
 
 int mm_version(void) { return 100; }
+
+mm_status mm_timing_enable(int on) {
+  StageTimer& t = timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.on = on != 0;
+  return MM_OK;
+}
+
+mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n) {
+  if (n < 0 || (n > 0 && (!stage_ms || !stage_launches))) return MM_ERR_INVALID_ARG;
+  StageTimer& t = timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  mm_status st = MM_OK;
+  for (int s = 0; s < MM_STAGE_COUNT; ++s) {
+    double ms = 0.0;
+    std::vector<cudaEvent_t>& v = t.open[s];
+    for (size_t i = 0; i + 1 < v.size(); i += 2) {
+      float f = 0.f;
+      if (cudaEventSynchronize(v[i + 1]) != cudaSuccess || cudaEventElapsedTime(&f, v[i], v[i + 1]) != cudaSuccess)
+        st = MM_ERR_CUDA;
+      ms += f;
+    }
+    for (cudaEvent_t ev : v) t.pool.push_back(ev);
+    v.clear();
+    if (s < n) {
+      stage_ms[s] = ms;
+      stage_launches[s] = t.launches[s];
+    }
+    t.launches[s] = 0;
+  }
+  return st;
+}
 
 // ------------------------------------------------------------------------
 mm_status mm_moe_init_routing_workspace_size(int64_t num_rows, int64_t k, int64_t expert_num, size_t* bytes) {
@@ -175,7 +271,9 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   o.sorted_row_idx = sorted_row_idx;
   o.expert_tokens = expert_tokens;
   o.tokens_cumsum = expert_tokens_num_type == 0;
+  StageScope sr(MM_STAGE_ROUTE, st);
   cudaError_t e = launch_route(plan, expert_idx, false, w.hist, w.offsets, o, dev_err, st);
+  sr.finish(3);
   if (e != cudaSuccess) return MM_ERR_CUDA;
   PermuteArgs a = {};
   a.src = x;
@@ -190,7 +288,10 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   a.scales = expanded_scale;
   a.scale_cols = round_up(ceil_div(h, 32), 2);
   a.dev_err = dev_err;
-  return cuda_status(launch_permute(a, st));
+  StageScope sd(MM_STAGE_DISPATCH, st);
+  e = launch_permute(a, st);
+  sd.finish(1);
+  return cuda_status(e);
 }
 
 // ------------------------------------------------------------------------
@@ -239,7 +340,9 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
   RoutingWs w = carve_routing(c, plan);
   RouteOutputs o;
   o.expanded_row_idx = sorted_indices;
+  StageScope sr(MM_STAGE_ROUTE, st);
   cudaError_t e = launch_route(plan, indices, indices_dtype == MM_DT_INT64, w.hist, w.offsets, o, dev_err, st);
+  sr.finish(3);
   if (e != cudaSuccess) return MM_ERR_CUDA;
   if (m == 0) return MM_OK;
   PermuteArgs a = {};
@@ -255,7 +358,10 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
   a.scales = expanded_scale;
   a.scale_cols = round_up(ceil_div(h, 32), 2);
   a.dev_err = dev_err;
-  return cuda_status(launch_permute(a, st));
+  StageScope sd(MM_STAGE_DISPATCH, st);
+  e = launch_permute(a, st);
+  sd.finish(1);
+  return cuda_status(e);
 }
 
 // ------------------------------------------------------------------------
@@ -325,20 +431,19 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   const uint8_t *wsf1 = weight_scales1, *wsf2 = weight_scales2;
   const uint8_t *swsf1 = shared_weight_scales1, *swsf2 = shared_weight_scales2;
   if (weight_scale_layout == MM_WSCALE_ROWS) {
-    if ((e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, w.wsf1, st)) != cudaSuccess)
-      return MM_ERR_CUDA;
-    if ((e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, w.wsf2, st)) != cudaSuccess)
-      return MM_ERR_CUDA;
+    StageScope sw(MM_STAGE_WSCALE, st);
+    e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, w.wsf1, st);
+    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, w.wsf2, st);
+    if (e == cudaSuccess && d.s > 0)
+      e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, w.swsf1, st);
+    if (e == cudaSuccess && d.s > 0)
+      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, w.swsf2, st);
+    sw.finish(d.s > 0 ? 4 : 2);
+    if (e != cudaSuccess) return MM_ERR_CUDA;
     wsf1 = w.wsf1;
     wsf2 = w.wsf2;
-    if (d.s > 0) {
-      if ((e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, w.swsf1, st)) != cudaSuccess)
-        return MM_ERR_CUDA;
-      if ((e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, w.swsf2, st)) != cudaSuccess)
-        return MM_ERR_CUDA;
-      swsf1 = w.swsf1;
-      swsf2 = w.swsf2;
-    }
+    swsf1 = w.swsf1;
+    swsf2 = w.swsf2;
   }
 
   // 1. routing: stable counting sort, inverse map, counts, GEMM segment table
@@ -350,8 +455,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   o.seg_mprefix = w.seg_mprefix;
   o.n_shared = (int)d.s;
   o.shared_rows = (int)d.bs;
-  if ((e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st)) != cudaSuccess)
-    return MM_ERR_CUDA;
+  StageScope sr(MM_STAGE_ROUTE, st);
+  e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st);
+  sr.finish(3);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 2. dispatch: MX quantisation of each token, stored at its K expert rows
   //    (and once per shared expert) in the padded grouped layout
@@ -371,7 +478,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   pa.scales = w.xsf;
   pa.scale_cols = 0;
   pa.dev_err = dev_err;
-  if ((e = launch_permute(pa, st)) != cudaSuccess) return MM_ERR_CUDA;
+  StageScope sd(MM_STAGE_DISPATCH, st);
+  e = launch_permute(pa, st);
+  sd.finish(1);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 3. GEMM1 + swiglu + MX requantisation
   GemmLaunch g1 = {};
@@ -396,7 +506,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   g1.act_q = w.aq;
   g1.act_sf = w.asf;
   g1.dev_err = dev_err;
-  if ((e = launch_gemm(g1, st)) != cudaSuccess) return MM_ERR_CUDA;
+  StageScope s1(MM_STAGE_GEMM1, st);
+  e = launch_gemm(g1, st);
+  s1.finish(1);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 4. GEMM2 -> bf16 expert rows
   GemmLaunch g2 = g1;
@@ -412,7 +525,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   g2.act_q = nullptr;
   g2.act_sf = nullptr;
   g2.out = w.o;
-  if ((e = launch_gemm(g2, st)) != cudaSuccess) return MM_ERR_CUDA;
+  StageScope s2(MM_STAGE_GEMM2, st);
+  e = launch_gemm(g2, st);
+  s2.finish(1);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 5. combine
   CombineArgs ca;
@@ -427,7 +543,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   ca.h = d.h;
   ca.k = (int)d.k;
   ca.y = static_cast<__nv_bfloat16*>(y);
-  if ((e = launch_combine(ca, st)) != cudaSuccess) return MM_ERR_CUDA;
+  StageScope sc(MM_STAGE_COMBINE, st);
+  e = launch_combine(ca, st);
+  sc.finish(1);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // optional diagnostic copy of A_hat in expert-sorted order
   if (act_q) {
@@ -440,7 +559,10 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
     ua.cols = d.inter;
     ua.dst_q = act_q;
     ua.dst_sf = act_scale;
-    if ((e = launch_unpad(ua, st)) != cudaSuccess) return MM_ERR_CUDA;
+    StageScope su(MM_STAGE_DIAG, st);
+    e = launch_unpad(ua, st);
+    su.finish(1);
+    if (e != cudaSuccess) return MM_ERR_CUDA;
   }
   return MM_OK;
 }
