@@ -245,6 +245,38 @@ mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t c
                          uint8_t* q, uint8_t* scales, int64_t scale_cols, void* stream);
 
 /* ------------------------------------------------------------------------
+ * mm_moe_init_routing_noalloc -- the same routing and permute as
+ * mm_moe_init_routing (same arguments and outputs), for callers that cannot
+ * give the library device scratch memory: for example a host program or
+ * plug-in that reaches this library only through this C interface and has
+ * no device allocator of its own, or one that must not call cudaMalloc /
+ * cudaFree while it serves requests (those calls can synchronise the device
+ * and fragment memory).  The operator pages have no counterpart of this
+ * entry point; it exists only for such callers.
+ *
+ * No allocation: the caller passes inputs and outputs only.  The scratch the
+ * kernels need lives in one fixed array of MM_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.  A problem whose scratch would not fit (about 4 bytes per
+ * expanded row, plus 4 bytes per expert for each chunk of at least 256 ids)
+ * is rejected with MM_ERR_WORKSPACE before anything is enqueued.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  A failed lookup returns MM_ERR_CUDA.
+ * Sharing: every call uses the same array and it keeps the last call's
+ * contents (nothing in it has to start at zero).  Calls whose kernels may
+ * overlap on the GPU, e.g. on different streams without ordering, race on
+ * the array; order them on one stream.
+ * ---------------------------------------------------------------------- */
+#define MM_NOALLOC_SCRATCH_BYTES (4u << 20)
+mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, const int32_t* expert_idx,
+                                      int64_t num_rows, int64_t h, int64_t k, int64_t expert_num,
+                                      int quant_mode, int expert_tokens_num_type, void* expanded_x,
+                                      uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                                      int32_t* sorted_row_idx, int64_t* expert_tokens,
+                                      int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Stage timing and launch counts (diagnostics; not part of the pages' API).
  *
  * mm_timing_enable(1) makes every following call record a CUDA event pair

@@ -298,3 +298,37 @@ def timing_read():
     L.mm_timing_read.restype = ctypes.c_int
     _check(L.mm_timing_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p), n), "mm_timing_read")
     return {s: (ms[i], int(cnt[i])) for i, s in enumerate(STAGES)}
+
+
+# --------------------------------------------------------------------------- no-allocation variant
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def mm_moe_init_routing_noalloc(x, expert_idx, expert_num: int, quant_mode: int = QUANT_NONE,
+                                expert_tokens_num_type: int = 1, *, dev_err=None):
+    """mm_moe_init_routing without a workspace: the library's fixed 4 MiB device
+    scratch array is used instead (for callers that cannot provide scratch
+    memory).  Same outputs as mm_moe_init_routing.  Calls that may overlap on
+    the GPU race on the shared array; keep them on one stream."""
+    _need_cuda(x, expert_idx)
+    L = load()
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.mm_moe_init_routing_noalloc.argtypes = [p, i32, p, i64, i64, i64, i64, i32, i32, p, p, p, p, p, p, p]
+    L.mm_moe_init_routing_noalloc.restype = i32
+    n, h = x.shape
+    k = expert_idx.shape[1] if expert_idx.dim() == 2 else 1
+    rows = n * k
+    dev = x.device
+    out_dt = x.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
+    expanded_x = torch.empty((rows, h), dtype=out_dt, device=dev)
+    scale = (torch.empty((rows, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
+             else torch.empty((0,), dtype=torch.uint8, device=dev))
+    exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    srt_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    tokens = torch.empty(expert_num, dtype=torch.int64, device=dev)
+    _check(L.mm_moe_init_routing_noalloc(_ptr(x), _dt(x), _ptr(expert_idx), n, h, k, expert_num, quant_mode,
+                                         expert_tokens_num_type, _ptr(expanded_x),
+                                         _ptr(scale) if scale.numel() else None, _ptr(exp_idx), _ptr(srt_idx),
+                                         _ptr(tokens), _dev_err(dev_err), _stream(dev)),
+           "mm_moe_init_routing_noalloc")
+    return expanded_x, exp_idx, tokens, scale, srt_idx

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmm_moe.so")
-SOURCES = ["route.cu", "permute.cu", "gemm.cu", "combine.cu", "abi.cu"]
+SOURCES = ["route.cu", "permute.cu", "gemm.cu", "combine.cu", "abi.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
