@@ -49,7 +49,7 @@ struct RoutingWs {
 RoutingWs carve_routing(Carver& c, const RoutePlan& p) {
   RoutingWs w;
   w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
-  w.offsets = c.take<int32_t>(p.num_experts + 1);
+  w.offsets = c.take<int32_t>(2 * p.num_experts + 1);
   w.exp_idx = c.take<int32_t>(p.rows);
   return w;
 }
@@ -84,7 +84,7 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   MegaWs w;
   const int64_t nseg = d.e + d.s;
   w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
-  w.offsets = c.take<int32_t>(d.e + 1);
+  w.offsets = c.take<int32_t>(2 * d.e + 1);
   w.seg_rows = c.take<int32_t>(nseg);
   w.seg_mprefix = c.take<int32_t>(nseg + 1);
   w.exp_idx = c.take<int32_t>(d.rows);

@@ -15,12 +15,12 @@
 // n-major inside an expert, so the m tiles that share a weight strip run
 // on neighbouring CTAs at the same time and the strip comes from HBM once.
 //
-// CTA = 6 warps: warp 0 issues TMA (A tile 128x128 B, B tile 256x128 B,
+// CTA = 10 warps: warp 0 issues TMA (A tile 128x128 B, B tile 256x128 B,
 // 128B swizzle) and bulk copies of the scale tiles into a 4-stage ring;
 // warp 1 copies the scales to TMEM (tcgen05.cp) and issues the MMAs
 // (M=128, N=256, K=32, four per k-block) into a 256-column fp32 TMEM
-// accumulator; warps 2-5 drain the accumulator (tcgen05.ld, one row per
-// thread) and run the epilogue:
+// accumulator; warps 2-9 drain the accumulator (tcgen05.ld, one row per
+// thread, two warps per row quarter) and run the epilogue:
 //   GEMM1: columns [0,128) are gate, [128,256) up, for the same 128
 //          intermediate columns -> swiglu -> one MX group per 32 columns,
 //          entirely within a thread; writes A_hat (FP8) and its scales
@@ -34,7 +34,8 @@ namespace mm {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // two warps per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
 constexpr uint32_t kBBytes = 256 * kBK;   // 32 KB
 constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, 32 * kEpiWarps);
     mbar_init(drain, 1);
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -240,7 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Warp w reads TMEM lanes [32*(w%4), +32) (its lane quarter); the two
+    // warps of a quarter split the columns.  Each thread loads its whole
+    // share of the accumulator first and releases TMEM before doing the
+    // math and the global stores, so the next tile's MMAs start early.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -255,29 +261,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = r < g.seg_rows[ti.seg] - ti.mt * kBM;
       const int64_t grow = (int64_t)(mpre[ti.seg] + ti.mt) * kBM + r;
       if (kMode == 1) {
+        // output columns [nt*128 + 64*half, +64): gate in accumulator
+        // columns c*32, up in 128 + c*32, for the chunks c = 2*half, 2*half+1
+        uint32_t gv[2][32], uv[2][32];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = 2 * half + i;
+          tmem_ld_32x32b_x32(trow + c * 32, gv[i]);
+          tmem_ld_32x32b_x32(trow + 128 + c * 32, uv[i]);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(acc_empty);
         uint32_t sfw = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t gv[32], uv[32];
-          tmem_ld_32x32b_x32(trow + c * 32, gv);
-          tmem_ld_32x32b_x32(trow + 128 + c * 32, uv);
-          tmem_ld_wait();
-          if (c == 3) {
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-          }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = 2 * half + i;
           float a[32];
           float amax = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float gf = __uint_as_float(gv[j]);
-            const float uf = __uint_as_float(uv[j]);
-            a[j] = gf / (1.0f + expf(-gf)) * uf;
+            const float gf = __uint_as_float(gv[i][j]);
+            const float uf = __uint_as_float(uv[i][j]);
+            // SiLU(g) * u = g * (1 / (1 + e^-g)) * u
+            a[j] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
             amax = fmaxf(amax, fabsf(a[j]));
           }
           float inv;
           const uint32_t code = mx_scale(amax, fmt_emax<kActFmt>(), inv);
-          sfw |= code << (8 * c);
+          sfw |= code << (8 * i);
           if (valid) {
             const uint2 p0 = pack8_fp8<kActFmt>(a, inv), p1 = pack8_fp8<kActFmt>(a + 8, inv);
             const uint2 p2 = pack8_fp8<kActFmt>(a + 16, inv), p3 = pack8_fp8<kActFmt>(a + 24, inv);
@@ -286,25 +298,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + 16) = make_uint4(p2.x, p2.y, p3.x, p3.y);
           }
         }
-        if (valid) *reinterpret_cast<uint32_t*>(g.act_sf + sf_tile_offset(grow, ti.nt * 4, g.inter / 128)) = sfw;
+        if (valid)
+          *reinterpret_cast<uint16_t*>(g.act_sf + sf_tile_offset(grow, ti.nt * 4 + 2 * half, g.inter / 128)) =
+              (uint16_t)sfw;
       } else {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(trow + c * 32, v);
-          tmem_ld_wait();
-          if (c == 7) {
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-          }
-          const int64_t col = (int64_t)ti.nt * 256 + c * 32;
+        // output columns [nt*256 + 128*half, +128)
+        uint32_t v[4][32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(trow + (4 * half + i) * 32, v[i]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t col = (int64_t)ti.nt * 256 + (4 * half + i) * 32;
           if (valid && col < g.N) {
             uint4* dst = reinterpret_cast<uint4*>(g.out + grow * g.N + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                                  pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pack_bf16x2(v[i][8 * u], v[i][8 * u + 1]), pack_bf16x2(v[i][8 * u + 2], v[i][8 * u + 3]),
+                                  pack_bf16x2(v[i][8 * u + 4], v[i][8 * u + 5]),
+                                  pack_bf16x2(v[i][8 * u + 6], v[i][8 * u + 7]));
           }
         }
       }

@@ -29,6 +29,7 @@ struct RouteOutputs {
 
 struct RouteScanArgs {
   int32_t* hist;
+  int32_t* totals;
   int num_experts, units;
   int64_t rows;
   int32_t* offsets;
@@ -43,7 +44,8 @@ struct RouteScanArgs {
 
 RoutePlan route_plan(int64_t rows, int num_experts);
 size_t route_workspace_bytes(const RoutePlan& p);
-// hist: [E * units] int32, offsets: [E + 1] int32 (both workspace)
+// hist: [E * units] int32, offsets: [2 * E + 1] int32 (offsets, then
+// per-expert totals; both workspace)
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st);
 

@@ -77,7 +77,7 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
   // scratch: per-chunk histograms, offsets, scatter index (unless the caller's)
   const RoutePlan plan = route_plan(rows, (int)expert_num);
   const size_t hist_b = piece((int64_t)plan.num_experts * plan.units * 4);
-  const size_t off_b = piece((expert_num + 1) * 4);
+  const size_t off_b = piece((2 * expert_num + 1) * 4);
   const size_t idx_b = expanded_row_idx ? 0 : piece(rows * 4);
   if (hist_b + off_b + idx_b > kNoallocScratchBytes) return MM_ERR_WORKSPACE;  // problem too large
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address());

@@ -7,10 +7,12 @@
 // The keys are expert ids in [0, E), so one counting pass replaces the two
 // sorts the permute article describes (sort, then argsort of the result):
 //   1. k_route_hist     each warp counts the ids of its contiguous chunk
-//   2. k_route_scan     one block scans the expert-major [E][units] counts:
-//                       base of (expert, chunk), per-expert offsets, counts,
-//                       and the 128-row tile table the grouped GEMMs use
-//   3. k_route_scatter  each warp walks its chunk in index order and gives
+//   2. k_route_scan_experts   one warp per expert scans its per-chunk counts
+//                       (exclusive prefix over chunks, in place) and totals
+//   3. k_route_scan_offsets   one block scans the totals: per-expert offsets,
+//                       counts / cumsum outputs, and the 128-row tile table
+//                       the grouped GEMMs use
+//   4. k_route_scatter  each warp walks its chunk in index order and gives
 //                       every id the next slot of its expert (warp match +
 //                       popc for ties inside a 32-wide step), which is the
 //                       stable order; it writes the inverse map and the
@@ -76,51 +78,81 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* sh_w
   return r;
 }
 
-__global__ void __launch_bounds__(1024) k_route_scan(RouteScanArgs a) {
+constexpr int kMaxUnits = 512;  // chunks per call (route_plan keeps units <= kMaxUnits)
+
+// One warp per expert: exclusive prefix of its per-chunk counts, in place,
+// and the expert's total.
+__global__ void __launch_bounds__(1024) k_route_scan_experts(int32_t* __restrict__ hist, int num_experts, int units,
+                                                             int32_t* __restrict__ totals) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= num_experts) return;
+  int32_t* row = hist + (int64_t)e * units;
+  constexpr int kPer = kMaxUnits / 32;
+  int32_t v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int u = i * 32 + lane;
+    v[i] = u < units ? row[u] : 0;
+  }
+  int32_t run = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    if (i * 32 >= units) break;
+    int32_t x = v[i];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    const int u = i * 32 + lane;
+    if (u < units) row[u] = run + x - v[i];
+    run += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) totals[e] = run;
+}
+
+__global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
   __shared__ int64_t sh_warp[33];
-  const int64_t entries = (int64_t)a.num_experts * a.units;
   const int nt = blockDim.x;
-  const int64_t per = (entries + nt - 1) / nt;
-  const int64_t lo = threadIdx.x * per;
-  const int64_t hi = lo + per < entries ? lo + per : entries;
-  // 1. expert-major exclusive scan of the per-chunk counts -> per-chunk bases
-  int64_t s = 0;
-  for (int64_t i = lo; i < hi; ++i) s += a.hist[i];
-  int64_t total;
-  int64_t base = block_exclusive_scan(s, sh_warp, total);
-  for (int64_t i = lo; i < hi; ++i) {
-    const int32_t c = a.hist[i];
-    a.hist[i] = (int32_t)base;
-    if (i % a.units == 0) a.offsets[i / a.units] = (int32_t)base;
-    base += c;
+  const int E = a.num_experts;
+  // 1. exclusive scan of the expert totals -> offsets
+  {
+    const int per = (E + nt - 1) / nt;
+    const int lo = threadIdx.x * per;
+    const int hi = lo + per < E ? lo + per : E;
+    int64_t s = 0;
+    for (int e = lo; e < hi; ++e) s += a.totals[e];
+    int64_t total;
+    int64_t base = block_exclusive_scan(s, sh_warp, total);
+    for (int e = lo; e < hi; ++e) {
+      const int32_t c = a.totals[e];
+      a.offsets[e] = (int32_t)base;
+      if (a.expert_tokens) a.expert_tokens[e] = a.tokens_cumsum ? base + c : (int64_t)c;
+      if (a.expert_token_nums) a.expert_token_nums[e] = c;
+      base += c;
+    }
+    if (threadIdx.x == 0) a.offsets[E] = (int32_t)total;
+    // rows whose id was out of range are left out: pad the gather index
+    if (a.sorted_row_idx)
+      for (int64_t d = total + threadIdx.x; d < a.rows; d += nt) a.sorted_row_idx[d] = -1;
   }
-  if (threadIdx.x == 0) a.offsets[a.num_experts] = (int32_t)total;
-  // rows whose id was out of range are left out: pad the gather index
-  if (a.sorted_row_idx)
-    for (int64_t d = total + threadIdx.x; d < a.rows; d += nt) a.sorted_row_idx[d] = -1;
-  __syncthreads();
-  // 2. per-expert counts / cumsum outputs
-  for (int e = threadIdx.x; e < a.num_experts; e += nt) {
-    const int32_t c = a.offsets[e + 1] - a.offsets[e];
-    if (a.expert_tokens) a.expert_tokens[e] = a.tokens_cumsum ? (int64_t)a.offsets[e + 1] : (int64_t)c;
-    if (a.expert_token_nums) a.expert_token_nums[e] = c;
-  }
-  // 3. segment table of the grouped GEMMs: routed experts, then shared
+  // 2. segment table of the grouped GEMMs: routed experts, then shared
   //    experts (shared_rows rows each); 128-row tiles, prefix in tiles.
   if (a.seg_mprefix) {
-    const int nseg = a.num_experts + a.n_shared;
-    const int64_t per2 = (nseg + nt - 1) / nt;
-    const int64_t l2 = threadIdx.x * per2;
-    const int64_t h2 = l2 + per2 < nseg ? l2 + per2 : nseg;
+    const int nseg = E + a.n_shared;
+    const int per = (nseg + nt - 1) / nt;
+    const int lo = threadIdx.x * per;
+    const int hi = lo + per < nseg ? lo + per : nseg;
     int64_t t = 0;
-    for (int64_t sg = l2; sg < h2; ++sg) {
-      const int64_t rows_s = sg < a.num_experts ? a.offsets[sg + 1] - a.offsets[sg] : a.shared_rows;
+    for (int sg = lo; sg < hi; ++sg) {
+      const int64_t rows_s = sg < E ? a.totals[sg] : a.shared_rows;
       t += (rows_s + kBM - 1) / kBM;
     }
     int64_t tot2;
     int64_t b2 = block_exclusive_scan(t, sh_warp, tot2);
-    for (int64_t sg = l2; sg < h2; ++sg) {
-      const int64_t rows_s = sg < a.num_experts ? a.offsets[sg + 1] - a.offsets[sg] : a.shared_rows;
+    for (int sg = lo; sg < hi; ++sg) {
+      const int64_t rows_s = sg < E ? a.totals[sg] : a.shared_rows;
       a.seg_rows[sg] = (int32_t)rows_s;
       a.seg_mprefix[sg] = (int32_t)b2;
       b2 += (rows_s + kBM - 1) / kBM;
@@ -141,7 +173,7 @@ __global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int n
   const int unit = blockIdx.x * wpb + warp;
   if (unit >= units) return;
   int32_t* next = sh_next + warp * num_experts;
-  for (int e = lane; e < num_experts; e += 32) next[e] = bases[(int64_t)e * units + unit];
+  for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
   __syncwarp();
   const int64_t start = (int64_t)unit * chunk;
   const int64_t end = start + chunk < rows ? start + chunk : rows;
@@ -178,8 +210,8 @@ RoutePlan route_plan(int64_t rows, int num_experts) {
   RoutePlan p;
   p.rows = rows;
   p.num_experts = num_experts;
-  // chunk: multiple of 32, at most ~1024 chunks
-  int64_t c = (rows + 1023) / 1024;
+  // chunk: multiple of 32, at least 256 ids, at most kMaxUnits chunks
+  int64_t c = (rows + kMaxUnits - 1) / kMaxUnits;
   c = round_up(c < 256 ? 256 : c, 32);
   p.chunk = (int)c;
   p.units = (int)((rows + c - 1) / c);
@@ -191,7 +223,7 @@ RoutePlan route_plan(int64_t rows, int num_experts) {
 
 size_t route_workspace_bytes(const RoutePlan& p) {
   return (size_t)round_up((int64_t)p.num_experts * p.units * 4, 256) +
-         (size_t)round_up(((int64_t)p.num_experts + 1) * 4, 256);
+         (size_t)round_up((2 * (int64_t)p.num_experts + 1) * 4, 256);
 }
 
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
@@ -205,8 +237,13 @@ cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_
   else
     k_route_hist<int32_t><<<blocks, wpb * 32, sh, st>>>((const int32_t*)ids, p.rows, p.num_experts, p.chunk,
                                                          p.units, hist, dev_err);
+  // per-expert totals live right after the E + 1 offsets (the offsets
+  // buffer holds 2 * E + 1 entries)
+  int32_t* totals = offsets + p.num_experts + 1;
+  k_route_scan_experts<<<(p.num_experts + 31) / 32, 1024, 0, st>>>(hist, p.num_experts, p.units, totals);
   RouteScanArgs a;
   a.hist = hist;
+  a.totals = totals;
   a.num_experts = p.num_experts;
   a.units = p.units;
   a.rows = p.rows;
@@ -219,7 +256,7 @@ cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_
   a.seg_mprefix = o.seg_mprefix;
   a.n_shared = o.n_shared;
   a.shared_rows = o.shared_rows;
-  k_route_scan<<<1, 1024, 0, st>>>(a);
+  k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
   if (ids64)
     k_route_scatter<int64_t><<<blocks, wpb * 32, sh, st>>>((const int64_t*)ids, p.rows, p.num_experts,
                                                             p.chunk, p.units, hist, offsets, o.seg_mprefix,

@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Integer, index, FP8 and E8M0 outputs of routing / permute / quantisation
-must be bit-exact.  MegaMoE's Y must satisfy the BASELINE tolerance
+must be bit-exact.  MegaMoE's Y must satisfy the stated tolerance
 (relative Frobenius error <= 5e-3, max abs error <= 2e-2 * max|Y|), and the
 activation codes that follow GEMM1 may differ by one code step in at most
 0.1 % of elements (the GEMM sums in fp32 on the tensor cores, the oracle in
