@@ -155,16 +155,25 @@ def profiled_traffic(profile_file, kernel_src):
 
 
 class Dist:
-    def __init__(self, n_gpus):
+    """One process per GPU (torchrun env).  The data path has no collective:
+    the process group only provides the barrier around the timed region and
+    the maximum of the ranks' times.  backend "nccl" on GPUs, "gloo" on CPU."""
+
+    def __init__(self, backend="nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cpu"
         if self.world > 1:
-            import torch.distributed as tdist
             import torch
-            torch.cuda.set_device(self.local)
-            tdist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            import torch.distributed as tdist
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+                tdist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+                self.device = "cuda"
+            else:
+                tdist.init_process_group(backend)
             self.pg = tdist
 
     def barrier(self):
@@ -175,7 +184,7 @@ class Dist:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -240,6 +249,11 @@ def ffn_flops(cfg, tokens=None):
     n = cfg.n if tokens is None else tokens
     rows = n * cfg.k + n * cfg.shared
     return 2.0 * rows * (2 * cfg.inter) * cfg.h + 2.0 * rows * cfg.h * cfg.inter
+
+
+def whole_job_rate(units_per_rank_step, steps, world, max_ms):
+    """Units processed by all ranks per second of the slowest rank's time."""
+    return units_per_rank_step * steps * world / (max_ms / 1e3)
 
 
 def time_steps(torch, fn, steps, warmup, dist, sampler_gpu=None):
@@ -367,7 +381,7 @@ def run_ours(args):
     import synth
     import routing_permute_mxfp8_gb300 as mm
 
-    dist = Dist(args.gpus)
+    dist = Dist("nccl")
     torch.cuda.set_device(dist.local)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     gpu_index = vis.split(",")[dist.local].strip() if vis else str(dist.local)
@@ -386,8 +400,7 @@ def run_ours(args):
     ms, stages, clocks = time_steps(torch, fn, args.steps, args.warmup, dist, sampler_gpu=gpu_index)
     ms = dist.max(ms)
     ms_step = ms / args.steps
-    tokens_total = cfg.n * args.steps * dist.world
-    value = tokens_total / (ms / 1e3)
+    value = whole_job_rate(cfg.n, args.steps, dist.world, ms)
     flops = ffn_flops(cfg)
     launches = sum(c for _, c in stages.values())
     g1_ms = stages["gemm1"][0] / max(1, stages["gemm1"][1])
@@ -423,7 +436,7 @@ def run_ours(args):
         ems, _, _ = time_steps(torch, e2e_fn, e_steps, min(args.warmup, 3), dist)
         ems = dist.max(ems)
         h2d = x.numel() * 2 + ids.numel() * 4 + gate.numel() * gate.element_size()
-        e2e = {"value": cfg.n * e_steps * dist.world / (ems / 1e3), "unit": "tokens/s",
+        e2e = {"value": whole_job_rate(cfg.n, e_steps, dist.world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(y.numel() * 2),
                "ms_per_step": ems / e_steps}
 

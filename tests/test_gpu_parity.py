@@ -187,12 +187,35 @@ def check_y(y_gpu, y_ref):
     return rel, mx
 
 
-def run_mega(cfg, tokens=None, layout=0, check_acts=True):
+def _sparse_weights(cfg, experts, shared=False):
+    """Oracle-quantised weights of the listed experts; every other expert is
+    all-zero (codes 0, scale code 127), which keeps full-size runs cheap to
+    build while every checked token sees its real weights."""
+    n_exp = cfg.shared if shared else cfg.e
+    s1c, s2c = 2 * ((cfg.h + 63) // 64), 2 * ((cfg.inter + 63) // 64)
+    w1 = np.zeros((n_exp, 2 * cfg.inter, cfg.h), np.uint8)
+    s1 = np.full((n_exp, 2 * cfg.inter, s1c), 127, np.uint8)
+    w2 = np.zeros((n_exp, cfg.h, cfg.inter), np.uint8)
+    s2 = np.full((n_exp, cfg.h, s2c), 127, np.uint8)
+    for e in experts:
+        w1[e], s1[e] = oracle.mx_quantize(synth.weight_f32(cfg, 1, int(e), shared=shared), oracle.DT_F32,
+                                          cfg.weight_fmt, s1c)
+        w2[e], s2[e] = oracle.mx_quantize(synth.weight_f32(cfg, 2, int(e), shared=shared), oracle.DT_F32,
+                                          cfg.weight_fmt, s2c)
+    return w1, s1, w2, s2
+
+
+def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
     x = synth.tokens_bf16(cfg)
     ids = synth.topk_ids(cfg)
     gate = synth.topk_weights(cfg)
-    w1, s1, w2, s2 = _weights(cfg)
-    sh = _weights(cfg, shared=True) if cfg.shared else None
+    if sparse:
+        needed = np.unique(ids[np.asarray(tokens)].reshape(-1))
+        w1, s1, w2, s2 = _sparse_weights(cfg, needed)
+        sh = _sparse_weights(cfg, range(cfg.shared), shared=True) if cfg.shared else None
+    else:
+        w1, s1, w2, s2 = _weights(cfg)
+        sh = _weights(cfg, shared=True) if cfg.shared else None
     gt = bf16(gate) if gate.dtype == np.uint16 else t(gate)
     ws1, ws2 = t(s1), t(s2)
     if layout == 1:
@@ -250,6 +273,27 @@ def test_mega_moe_prepared_scales_identical():
 def test_mega_moe_qwen3_shape_sampled():
     cfg = synth.CONFIGS["qwen3"].scaled(n=512)
     run_mega(cfg, tokens=np.arange(0, 512, 7))
+
+
+# Full-size workloads in the launch configuration the benchmark times: the
+# routing outputs are checked in full, Y and the activation codes on a token
+# sample the oracle evaluates one token at a time.
+@pytest.mark.slow
+def test_mega_moe_qwen3_full_size():
+    cfg = synth.CONFIGS["qwen3"]
+    run_mega(cfg, tokens=np.linspace(0, cfg.n - 1, 40).astype(np.int64), layout=1)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_prefill_full_size():
+    cfg = synth.CONFIGS["dsv3_prefill"]
+    run_mega(cfg, tokens=np.array([0, 1, 777, 2048, 4095, 5000, 6001, 7333, 8000, 8191]), layout=1, sparse=True)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_decode_full_size():
+    cfg = synth.CONFIGS["dsv3_decode"]
+    run_mega(cfg, tokens=np.array([0, 5, 17, 63, 64, 100, 126, 127]), layout=1, sparse=True)
 
 
 def test_mega_moe_duplicate_ids_flagged():
