@@ -230,8 +230,8 @@ def gpu_weights(cfg, mm, torch, n_exp, seed):
             del w, qq, ss
         out += [q, s]
     w1, s1, w2, s2 = out
-    p1 = mm.mm_prepare_weight_scales(s1, cfg.h)
-    p2 = mm.mm_prepare_weight_scales(s2, cfg.inter)
+    p1 = mm.mm_prepare_weight_scales(s1, cfg.h, 1)
+    p2 = mm.mm_prepare_weight_scales(s2, cfg.inter, 2)
     return {"w1": w1, "s1": s1, "w2": w2, "s2": s2, "p1": p1, "p2": p2}
 
 

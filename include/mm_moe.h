@@ -221,14 +221,16 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
  * mm_prepare_weight_scales rearranges E8M0 weight scales from the pages'
  * (E, N_out, CeilDiv(K_red, 64), 2) layout into the tile layout the grouped
  * GEMMs read (MM_WSCALE_PREPARED), the way the pages require FRACTAL_NZ
- * weight formats for some scenarios.  src and dst are device buffers;
- * dst holds mm_prepared_weight_scales_size bytes.  K_red must be a multiple
- * of 128.
+ * weight formats for some scenarios.  which = 1 for weightScales1 (N_out =
+ * 2I), 2 for weightScales2 (N_out = H); the layout groups rows by the tile
+ * width of the GEMM that reads them.  src and dst are device buffers; dst
+ * holds mm_prepared_weight_scales_size bytes.  K_red must be a multiple of
+ * 128.
  * ---------------------------------------------------------------------- */
-mm_status mm_prepared_weight_scales_size(int64_t experts, int64_t n_out, int64_t k_red,
+mm_status mm_prepared_weight_scales_size(int which, int64_t experts, int64_t n_out, int64_t k_red,
                                          size_t* bytes);
-mm_status mm_prepare_weight_scales(const uint8_t* src, int64_t experts, int64_t n_out,
-                                   int64_t k_red, uint8_t* dst, void* stream);
+mm_status mm_prepare_weight_scales(const uint8_t* src, int which, int64_t experts,
+                                   int64_t n_out, int64_t k_red, uint8_t* dst, void* stream);
 
 /* ------------------------------------------------------------------------
  * mm_mx_quantize -- Q_MX along each row (MegaMoE A8W8-FP stage 1): groups of

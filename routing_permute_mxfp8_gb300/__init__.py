@@ -64,8 +64,8 @@ def load():
     L.mm_mega_moe_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, psz]
     L.mm_mega_moe.argtypes = ([p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
                                i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, sz, p, p])
-    L.mm_prepared_weight_scales_size.argtypes = [i64, i64, i64, psz]
-    L.mm_prepare_weight_scales.argtypes = [p, i64, i64, i64, p, p]
+    L.mm_prepared_weight_scales_size.argtypes = [i32, i64, i64, i64, psz]
+    L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
     L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
     for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
                  "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
@@ -249,16 +249,17 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     return tuple(res)
 
 
-def mm_prepare_weight_scales(scales, k_red: int):
+def mm_prepare_weight_scales(scales, k_red: int, which: int):
     """Rearrange E8M0 weight scales [E, N_out, CeilDiv(K_red, 64), 2] (or [E, N_out, K_red/32])
-    into the tile layout of the grouped GEMMs (weight_scale_layout = 1)."""
+    into the tile layout of the grouped GEMMs (weight_scale_layout = 1).
+    which = 1 for weight_scales1, 2 for weight_scales2."""
     _need_cuda(scales)
     L = load()
     e, n_out = scales.shape[0], scales.shape[1]
     need = ctypes.c_size_t(0)
-    _check(L.mm_prepared_weight_scales_size(e, n_out, k_red, ctypes.byref(need)), "mm_prepare_weight_scales")
+    _check(L.mm_prepared_weight_scales_size(which, e, n_out, k_red, ctypes.byref(need)), "mm_prepare_weight_scales")
     dst = torch.empty(need.value, dtype=torch.uint8, device=scales.device)
-    _check(L.mm_prepare_weight_scales(_ptr(scales), e, n_out, k_red, _ptr(dst), _stream(scales.device)),
+    _check(L.mm_prepare_weight_scales(_ptr(scales), which, e, n_out, k_red, _ptr(dst), _stream(scales.device)),
            "mm_prepare_weight_scales")
     return dst
 

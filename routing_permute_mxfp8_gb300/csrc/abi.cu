@@ -96,11 +96,12 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   w.o = c.take<__nv_bfloat16>(d.rows_cap * d.h);
   w.wsf1 = w.wsf2 = w.swsf1 = w.swsf2 = nullptr;
   if (wscale_layout == MM_WSCALE_ROWS) {
-    w.wsf1 = c.take<uint8_t>(d.e * prepared_nblocks(2 * d.inter) * (d.h / 128) * kSfChunk);
-    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h) * (d.inter / 128) * kSfChunk);
+    const int64_t bn2 = gemm_tile_n(2, d.h);
+    w.wsf1 = c.take<uint8_t>(d.e * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
+    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h, bn2) * (d.inter / 128) * kSfChunk);
     if (d.s > 0) {
-      w.swsf1 = c.take<uint8_t>(d.s * prepared_nblocks(2 * d.inter) * (d.h / 128) * kSfChunk);
-      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h) * (d.inter / 128) * kSfChunk);
+      w.swsf1 = c.take<uint8_t>(d.s * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
+      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h, bn2) * (d.inter / 128) * kSfChunk);
     }
   }
   return w;
@@ -432,12 +433,13 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   const uint8_t *swsf1 = shared_weight_scales1, *swsf2 = shared_weight_scales2;
   if (weight_scale_layout == MM_WSCALE_ROWS) {
     StageScope sw(MM_STAGE_WSCALE, st);
-    e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, w.wsf1, st);
-    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, w.wsf2, st);
+    const int64_t bn2 = gemm_tile_n(2, d.h);
+    e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, 256, w.wsf1, st);
+    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, bn2, w.wsf2, st);
     if (e == cudaSuccess && d.s > 0)
-      e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, w.swsf1, st);
+      e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, 256, w.swsf1, st);
     if (e == cudaSuccess && d.s > 0)
-      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, w.swsf2, st);
+      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, bn2, w.swsf2, st);
     sw.finish(d.s > 0 ? 4 : 2);
     if (e != cudaSuccess) return MM_ERR_CUDA;
     wsf1 = w.wsf1;
@@ -568,20 +570,23 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
 }
 
 // ------------------------------------------------------------------------
-mm_status mm_prepared_weight_scales_size(int64_t experts, int64_t n_out, int64_t k_red, size_t* bytes) {
-  if (!bytes || experts <= 0 || n_out <= 0 || k_red <= 0 || k_red % 128 != 0) return MM_ERR_INVALID_ARG;
-  *bytes = (size_t)(experts * prepared_nblocks(n_out) * (k_red / 128) * kSfChunk);
+mm_status mm_prepared_weight_scales_size(int which, int64_t experts, int64_t n_out, int64_t k_red,
+                                         size_t* bytes) {
+  if (!bytes || (which != 1 && which != 2) || experts <= 0 || n_out <= 0 || k_red <= 0 || k_red % 128 != 0)
+    return MM_ERR_INVALID_ARG;
+  *bytes = (size_t)(experts * prepared_nblocks(n_out, gemm_tile_n(which, n_out)) * (k_red / 128) * kSfChunk);
   return MM_OK;
 }
 
-mm_status mm_prepare_weight_scales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red,
-                                   uint8_t* dst, void* stream) {
+mm_status mm_prepare_weight_scales(const uint8_t* src, int which, int64_t experts, int64_t n_out,
+                                   int64_t k_red, uint8_t* dst, void* stream) {
   size_t need;
-  mm_status s = mm_prepared_weight_scales_size(experts, n_out, k_red, &need);
+  mm_status s = mm_prepared_weight_scales_size(which, experts, n_out, k_red, &need);
   if (s != MM_OK) return s;
   if (!src || !dst || (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))
     return MM_ERR_INVALID_ARG;
-  return cuda_status(launch_prepare_wscales(src, experts, n_out, k_red, dst, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_prepare_wscales(src, experts, n_out, k_red, gemm_tile_n(which, n_out), dst,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t cols, int out_dtype, uint8_t* q,

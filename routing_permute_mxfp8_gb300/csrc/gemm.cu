@@ -37,10 +37,7 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;                 // two warps per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
-constexpr uint32_t kBBytes = 256 * kBK;   // 32 KB
-constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -104,10 +101,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int kMode, int kActFmt>
+// kBN: tile width (B rows per tile); kAcc: accumulator buffers in TMEM (2
+// lets the MMAs of the next tile run while the epilogue drains this one;
+// kBN * kAcc plus 16 scale columns per stage must fit the 512 columns).
+template <int kMode, int kActFmt, int kBN, int kAcc>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmBs, const GemmArgs g) {
+  constexpr uint32_t kBBytes = kBN * kBK;
+  constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
+  constexpr uint32_t kAccCols = kBN * kAcc;
+  static_assert(kAccCols + 16 * kStages <= kTmemCols, "TMEM columns");
+  static_assert(kMode == 2 || (kBN == 256 && kAcc == 1), "GEMM1 tiles are 128 gate + 128 up columns");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = base;
@@ -116,9 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smSFB = smSFA + kStages * 512;
   uint64_t* full = reinterpret_cast<uint64_t*>(smSFB + kStages * 1024);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + kStages;      // [kAcc]
+  uint64_t* acc_empty = acc_full + kAcc;     // [kAcc]
+  uint64_t* drain = acc_empty + kAcc;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* mpre = reinterpret_cast<int32_t*>(tmem_holder + 4);
 
@@ -130,8 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 32 * kEpiWarps);
+    for (int b = 0; b < kAcc; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 32 * kEpiWarps);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           nb0 = 2 * ti.nt;
           nb1 = 2 * ti.nt + 1;
-          bn0 = ti.nt * 256;
+          bn0 = ti.nt * kBN;
           bn1 = 0;
         }
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -198,16 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
         const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
         const uint32_t idb = ti.seg >= g.n_routed ? g.idesc_sh : g.idesc;
-        if (!wait_bounded(acc_empty, acc_phase ^ 1)) {
+        const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
+        if (!wait_bounded(&acc_empty[buf], (use & 1) ^ 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t dacc = tmem + buf * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bounded(&full[stage], phase)) {
             ok = false;
@@ -222,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(smB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 32; ++k) {
-            tc_mma_mxf8(tmem, smem_desc(a0 + 32 * k, 0, 1024, 2), smem_desc(b0 + 32 * k, 0, 1024, 2),
+            tc_mma_mxf8(dacc, smem_desc(a0 + 32 * k, 0, 1024, 2), smem_desc(b0 + 32 * k, 0, 1024, 2),
                         idesc_with_sf(idb, (uint32_t)k), sfc, sfc + 4, (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -232,8 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1;
+        tc_commit(&acc_full[buf]);
       }
       if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
       tc_commit(drain);  // all MMAs / copies of this thread complete before TMEM is freed
@@ -248,16 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
-    uint32_t acc_phase = 0;
+    uint32_t tcount = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
-      if (!wait_bounded(acc_full, acc_phase)) {
+      const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
+      if (!wait_bounded(&acc_full[buf], use & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t trow = tmem + buf * kBN + ((uint32_t)(q * 32) << 16);
       const bool valid = r < g.seg_rows[ti.seg] - ti.mt * kBM;
       const int64_t grow = (int64_t)(mpre[ti.seg] + ti.mt) * kBM + r;
       if (kMode == 1) {
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(acc_empty);
+        mbar_arrive(&acc_empty[buf]);
         uint32_t sfw = 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -302,17 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint16_t*>(g.act_sf + sf_tile_offset(grow, ti.nt * 4 + 2 * half, g.inter / 128)) =
               (uint16_t)sfw;
       } else {
-        // output columns [nt*256 + 128*half, +128)
+        // output columns [nt*kBN + 128*half, +128) (the last chunks of a
+        // tile narrower than 256 columns: half 1 has fewer)
+        constexpr int kChunks = kBN / 32;
         uint32_t v[4][32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(trow + (4 * half + i) * 32, v[i]);
+        for (int i = 0; i < 4; ++i)
+          if (4 * half + i < kChunks) tmem_ld_32x32b_x32(trow + (4 * half + i) * 32, v[i]);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(acc_empty);
+        mbar_arrive(&acc_empty[buf]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int64_t col = (int64_t)ti.nt * 256 + (4 * half + i) * 32;
-          if (valid && col < g.N) {
+          const int64_t col = (int64_t)ti.nt * kBN + (4 * half + i) * 32;
+          if (4 * half + i < kChunks && valid && col < g.N) {
             uint4* dst = reinterpret_cast<uint4*>(g.out + grow * g.N + col);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -322,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      acc_phase ^= 1;
     }
     if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
   }
@@ -377,10 +388,13 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e,
 
 int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : 0; }
 
-template <int kMode, int kActFmt>
+template <int kMode, int kActFmt, int kBN, int kAcc>
 cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbs,
-                const GemmArgs& g, int grid, size_t smem, cudaStream_t st) {
-  auto kern = k_gemm_mx<kMode, kActFmt>;
+                const GemmArgs& g, int grid, cudaStream_t st) {
+  auto kern = k_gemm_mx<kMode, kActFmt, kBN, kAcc>;
+  const size_t smem = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) + 8 * (2 * kStages + 2 * kAcc + 1) +
+                      16 + 4 * (size_t)(g.nseg + 1);
+  if (smem > 232448) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, st>>>(ma, mb, mbs, g);
@@ -388,6 +402,15 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
 }
 
 }  // namespace
+
+// Tile width of both GEMMs: 256 output columns (GEMM1: 128 gate + 128 up).
+// A 224-wide GEMM2 tile with two accumulators in tensor memory was measured
+// slower on the DeepSeek-V3 shape (more tiles re-read the activations).
+int gemm_tile_n(int mode, int64_t n_out) {
+  (void)mode;
+  (void)n_out;
+  return 256;
+}
 
 int num_sms() {
   static int n = 0;
@@ -401,7 +424,8 @@ int num_sms() {
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   const int nseg = L.n_routed + L.n_shared;
-  const uint32_t box_rows = L.mode == 1 ? 128 : 256;
+  const int bn = gemm_tile_n(L.mode, L.N);
+  const uint32_t box_rows = L.mode == 1 ? 128 : (uint32_t)bn;
   CUtensorMap ma, mb, mbs;
   if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM)) return cudaErrorInvalidValue;
   if (!map_3d(&mb, L.b, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_routed, box_rows)) return cudaErrorInvalidValue;
@@ -421,10 +445,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.n_routed = L.n_routed;
   g.K = (int)L.K;
   g.N = (int)L.N;
-  g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, 256);
-  g.nb = (int)prepared_nblocks(L.N);
-  g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, 256);
-  g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, 256);
+  g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, bn);
+  g.nb = (int)prepared_nblocks(L.N, L.mode == 1 ? 256 : bn);
+  g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, bn);
+  g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);
   g.inter = L.inter;
   g.act_q = L.act_q;
   g.act_sf = L.act_sf;
@@ -435,14 +459,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   int64_t grid = max_mtiles * g.n_tiles;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  const size_t smem = 1024 + (size_t)kStages * (kABytes + kBBytes + 512 + 1024) + 8 * (2 * kStages + 3) + 16 +
-                      4 * (size_t)(nseg + 1);
-  if (smem > 232448) return cudaErrorInvalidValue;
   if (L.mode == 1) {
-    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2>(L, ma, mb, mbs, g, (int)grid, smem, st);
-    return run<1, MM_DT_FP8_E4M3FN>(L, ma, mb, mbs, g, (int)grid, smem, st);
+    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
+    return run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
   }
-  return run<2, MM_DT_FP8_E4M3FN>(L, ma, mb, mbs, g, (int)grid, smem, st);
+  return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
 }
 
 }  // namespace mm

@@ -68,9 +68,10 @@ struct PermuteArgs {
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 
-// tile layout of E8M0 weight scales (mm_prepare_weight_scales)
-int64_t prepared_nblocks(int64_t n_out);
-cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red,
+// tile layout of E8M0 weight scales (mm_prepare_weight_scales): 128-row
+// blocks grouped by GEMM tiles of bn rows (two blocks per tile)
+int64_t prepared_nblocks(int64_t n_out, int64_t bn);
+cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red, int64_t bn,
                                    uint8_t* dst, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ----------------------------------------------
@@ -95,6 +96,8 @@ struct GemmLaunch {
   int32_t* dev_err;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+// tile width the GEMM of `mode` uses for n_out output columns
+int gemm_tile_n(int mode, int64_t n_out);
 
 // ---- combine (combine.cu) --------------------------------------------------
 struct CombineArgs {

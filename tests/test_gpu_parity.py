@@ -219,14 +219,14 @@ def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
     gt = bf16(gate) if gate.dtype == np.uint16 else t(gate)
     ws1, ws2 = t(s1), t(s2)
     if layout == 1:
-        ws1 = mm.mm_prepare_weight_scales(ws1, cfg.h)
-        ws2 = mm.mm_prepare_weight_scales(ws2, cfg.inter)
+        ws1 = mm.mm_prepare_weight_scales(ws1, cfg.h, 1)
+        ws2 = mm.mm_prepare_weight_scales(ws2, cfg.inter, 2)
     kw = {}
     if sh is not None:
         sw1, ss1, sw2, ss2 = [t(a) for a in sh]
         if layout == 1:
-            ss1 = mm.mm_prepare_weight_scales(ss1, cfg.h)
-            ss2 = mm.mm_prepare_weight_scales(ss2, cfg.inter)
+            ss1 = mm.mm_prepare_weight_scales(ss1, cfg.h, 1)
+            ss2 = mm.mm_prepare_weight_scales(ss2, cfg.inter, 2)
         kw = dict(shared_weight1=sw1, shared_weight2=sw2, shared_weight_scales1=ss1, shared_weight_scales2=ss2)
     err = zeros_err()
     y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
@@ -254,6 +254,7 @@ MEGA_CASES = {
     "tiny_ragged": dict(n=37, e=5, k=3),
     "tiny_k1_e1": dict(n=200, e=1, k=1),
     "wide": dict(n=300, h=1024, inter=384, e=16, k=4),
+    "h896_ragged_n": dict(n=256, h=896, inter=256, e=8, k=4, shared=1),   # last GEMM2 n tile half empty
 }
 
 
