@@ -11,9 +11,15 @@
 // Layout.  The expanded rows of every expert (and of each shared expert,
 // which sees all tokens) form a segment padded to a multiple of 128 rows,
 // so an M tile never straddles two experts.  One persistent kernel walks a
-// flat tile list (segment, n tile, m tile) ordered expert-major and
-// n-major inside an expert, so the m tiles that share a weight strip run
-// on neighbouring CTAs at the same time and the strip comes from HBM once.
+// flat tile list.  Segments with at least `big_mt` m tiles reuse each
+// weight strip from L2 across their m tiles (tensor-bound tiles); smaller
+// ones stream a weight strip from HBM for one tile (HBM-bound tiles).
+// Each kind forms its own list (segment, n tile, m tile), ordered
+// expert-major and n-major inside an expert, so the m tiles that share a
+// weight strip run on neighbouring CTAs at the same time and the strip
+// comes from HBM once; the two lists are then merged in proportion
+// (Bresenham), so every wave of CTAs mixes both kinds and the tensor
+// cores and HBM stay busy together instead of taking turns.
 //
 // CTA = 10 warps: warp 0 issues TMA (A tile 128x128 B, B tile 256x128 B,
 // 128B swizzle) and bulk copies of the scale tiles into a 4-stage ring;
@@ -39,6 +45,10 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+#ifndef MM_BIG_MTILES
+#define MM_BIG_MTILES 2
+#endif
+constexpr int kBigMtiles = MM_BIG_MTILES;    // m tiles from which a segment's tiles count as tensor-bound
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -65,6 +75,7 @@ struct GemmArgs {
   int nseg, n_routed;
   int K, N;
   int n_tiles;
+  int big_mt;     // segments with >= big_mt m tiles form the tensor-bound list
   int nb;         // 128-row blocks per expert in the prepared B scales
   uint32_t idesc, idesc_sh;
   int inter;
@@ -94,6 +105,19 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int32_t* mpre, int 
   ti.nt = local / mts;
   ti.mt = local - ti.nt * mts;
   return ti;
+}
+
+// Tile t of the merged order.  bpre / spre: prefixes of the m tiles of the
+// big / small segments (a segment of the other kind adds 0).  The first t
+// tiles hold floor(t * TB / T) big ones, so tile t is big when that count
+// steps at t; each list keeps its own order.
+__device__ __forceinline__ TileInfo decode_merged(int t, const int32_t* bpre, const int32_t* spre, int nseg,
+                                                  int n_tiles) {
+  const int64_t tb = (int64_t)bpre[nseg] * n_tiles;
+  const int64_t tt = tb + (int64_t)spre[nseg] * n_tiles;
+  const int cb = (int)((int64_t)t * tb / tt);
+  const int cb1 = (int)((int64_t)(t + 1) * tb / tt);
+  return cb1 > cb ? decode_tile(cb, bpre, nseg, n_tiles) : decode_tile(t - cb, spre, nseg, n_tiles);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
@@ -126,10 +150,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = acc_empty + kAcc;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* mpre = reinterpret_cast<int32_t*>(tmem_holder + 4);
+  int32_t* bpre = mpre + (g.nseg + 1);
+  int32_t* spre = bpre + (g.nseg + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = g.nseg;
   for (int i = threadIdx.x; i <= nseg; i += kThreads) mpre[i] = g.seg_mprefix[i];
+  __syncthreads();
+  if (warp == 2) {
+    // split the m-tile prefix into the big and the small segments' prefixes:
+    // lane l scans segments [l*per, (l+1)*per), then a warp scan
+    const int per = (nseg + 31) / 32;
+    const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
+    int nb = 0, ns = 0;
+    for (int sg = s0; sg < s1; ++sg) {
+      const int m = mpre[sg + 1] - mpre[sg];
+      if (m >= g.big_mt) nb += m; else ns += m;
+    }
+    int ib = nb, is = ns;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ub = __shfl_up_sync(0xffffffffu, ib, o), us = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) {
+        ib += ub;
+        is += us;
+      }
+    }
+    int pb = ib - nb, ps = is - ns;
+    for (int sg = s0; sg < s1; ++sg) {
+      bpre[sg] = pb;
+      spre[sg] = ps;
+      const int m = mpre[sg + 1] - mpre[sg];
+      if (m >= g.big_mt) pb += m; else ps += m;
+    }
+    if (lane == 31) {
+      bpre[nseg] = ib;
+      spre[nseg] = is;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -159,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, armed = 0, arm_par = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+        const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
         const bool sh = ti.seg >= g.n_routed;
         const int e = sh ? ti.seg - g.n_routed : ti.seg;
         const CUtensorMap* mb = sh ? &tmBs : &tmB;
@@ -208,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
-        const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+        const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
         const uint32_t idb = ti.seg >= g.n_routed ? g.idesc_sh : g.idesc;
         const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
         if (!wait_bounded(&acc_empty[buf], (use & 1) ^ 1)) {
@@ -259,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tcount = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-      const TileInfo ti = decode_tile(t, mpre, nseg, g.n_tiles);
+      const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
       const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
       if (!wait_bounded(&acc_full[buf], use & 1)) {
         ok = false;
@@ -393,7 +451,7 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
                 const GemmArgs& g, int grid, cudaStream_t st) {
   auto kern = k_gemm_mx<kMode, kActFmt, kBN, kAcc>;
   const size_t smem = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) + 8 * (2 * kStages + 2 * kAcc + 1) +
-                      16 + 4 * (size_t)(g.nseg + 1);
+                      16 + 12 * (size_t)(g.nseg + 1);
   if (smem > 232448) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -446,6 +504,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.K = (int)L.K;
   g.N = (int)L.N;
   g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, bn);
+  g.big_mt = kBigMtiles;
   g.nb = (int)prepared_nblocks(L.N, L.mode == 1 ? 256 : bn);
   g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, bn);
   g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);

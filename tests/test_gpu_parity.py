@@ -255,6 +255,11 @@ MEGA_CASES = {
     "tiny_k1_e1": dict(n=200, e=1, k=1),
     "wide": dict(n=300, h=1024, inter=384, e=16, k=4),
     "h896_ragged_n": dict(n=256, h=896, inter=256, e=8, k=4, shared=1),   # last GEMM2 n tile half empty
+    "zipf_shared_e5m2_h512": dict(n=300, h=512, inter=256, e=8, k=4, shared=1, routing="zipf", dispatch_fmt=23),
+    "many_mtiles": dict(n=640, h=512, inter=512, e=4, k=2),
+    # Zipf routing over 32 experts: one-tile experts beside experts with
+    # several m tiles, so the tile order interleaves the two kinds
+    "zipf_mixed_sizes": dict(n=1024, h=512, inter=256, e=32, k=4, routing="zipf"),
 }
 
 
