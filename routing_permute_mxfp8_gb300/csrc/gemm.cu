@@ -31,7 +31,11 @@
 //          intermediate columns -> swiglu -> one MX group per 32 columns,
 //          entirely within a thread; writes A_hat (FP8) and its scales
 //          directly in GEMM2's operand layouts.
-//   GEMM2: fp32 -> bf16 rows of O.
+//   GEMM2: fp32 -> bf16 rows of O.  Each warp stages a 32-row x 32-column
+//          block in shared memory (64B swizzle, conflict-free) and one TMA
+//          store writes it; blocks with padding rows, or launches whose
+//          segment table leaves no room for the staging buffers, store
+//          rows directly from registers.
 // Every wait is bounded; a timeout sets MM_DEVERR_TIMEOUT and the CTA
 // drains its own copies and MMAs, frees TMEM and returns.
 #include "mm_route.cuh"
@@ -44,6 +48,7 @@ constexpr int kEpiWarps = 8;                 // two warps per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOStageBytes = 32 * 64;  // one 32 x 32 bf16 block of O
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 #ifndef MM_BIG_MTILES
 #define MM_BIG_MTILES 2
@@ -83,6 +88,7 @@ struct GemmArgs {
   uint8_t* act_sf;
   __nv_bfloat16* out;
   int32_t* dev_err;
+  int o_stage;    // GEMM2: stage O blocks in shared memory for TMA stores
 };
 
 struct TileInfo {
@@ -131,7 +137,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
 template <int kMode, int kActFmt, int kBN, int kAcc>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmBs, const GemmArgs g) {
+              const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmO, const GemmArgs g) {
   constexpr uint32_t kBBytes = kBN * kBK;
   constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
   constexpr uint32_t kAccCols = kBN * kAcc;
@@ -143,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smB = smA + kStages * kABytes;
   uint8_t* smSFA = smB + kStages * kBBytes;
   uint8_t* smSFB = smSFA + kStages * 512;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smSFB + kStages * 1024);
+  uint8_t* smO = smSFB + kStages * 1024;  // [kEpiWarps][32 x 64 B] when g.o_stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smO + (g.o_stage ? kEpiWarps * kOStageBytes : 0));
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;      // [kAcc]
   uint64_t* acc_empty = acc_full + kAcc;     // [kAcc]
@@ -379,10 +386,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
+        // TMA store when all 32 rows of this lane quarter are real rows
+        const bool staged = g.o_stage && g.seg_rows[ti.seg] - ti.mt * kBM >= (q + 1) * 32;
+        uint8_t* stg = smO + (warp - 2) * kOStageBytes;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int64_t col = (int64_t)ti.nt * kBN + (4 * half + i) * 32;
-          if (4 * half + i < kChunks && valid && col < g.N) {
+          if (staged && 4 * half + i < kChunks && col < g.N) {
+            if (lane == 0) bulk_wait_read();  // the previous block has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(stg + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pack_bf16x2(v[i][8 * u], v[i][8 * u + 1]), pack_bf16x2(v[i][8 * u + 2], v[i][8 * u + 3]),
+                             pack_bf16x2(v[i][8 * u + 4], v[i][8 * u + 5]),
+                             pack_bf16x2(v[i][8 * u + 6], v[i][8 * u + 7]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, stg, (int)col, (int)((grow - r) + q * 32));
+              bulk_commit();
+            }
+          } else if (4 * half + i < kChunks && valid && col < g.N) {
             uint4* dst = reinterpret_cast<uint4*>(g.out + grow * g.N + col);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -393,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (kMode == 2 && g.o_stage && lane == 0) bulk_wait_all();
     if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
   }
 
@@ -444,26 +470,41 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 matrix [rows][cols] (cols contiguous), box 32 x 32, 64B swizzle: the
+// GEMM2 output blocks that the epilogue stages in shared memory.
+bool map_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  EncodeTiledFn f = encode_fn();
+  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : 0; }
 
 template <int kMode, int kActFmt, int kBN, int kAcc>
 cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbs,
-                const GemmArgs& g, int grid, cudaStream_t st) {
+                const CUtensorMap& mo, GemmArgs g, int grid, cudaStream_t st) {
   auto kern = k_gemm_mx<kMode, kActFmt, kBN, kAcc>;
-  const size_t smem = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) + 8 * (2 * kStages + 2 * kAcc + 1) +
-                      16 + 12 * (size_t)(g.nseg + 1);
-  if (smem > 232448) return cudaErrorInvalidValue;
+  const size_t base = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) +
+                      8 * (2 * kStages + 2 * kAcc + 1) + 16 + 12 * (size_t)(g.nseg + 1);
+  constexpr size_t kMaxSmem = 232448;
+  // O staging buffers only where the segment table leaves room for them
+  g.o_stage = kMode == 2 && base + kEpiWarps * kOStageBytes <= kMaxSmem ? 1 : 0;
+  const size_t smem = base + (g.o_stage ? kEpiWarps * kOStageBytes : 0);
+  if (smem > kMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(ma, mb, mbs, g);
+  kern<<<grid, kThreads, smem, st>>>(ma, mb, mbs, mo, g);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // Tile width of both GEMMs: 256 output columns (GEMM1: 128 gate + 128 up).
-// A 224-wide GEMM2 tile with two accumulators in tensor memory was measured
-// slower on the DeepSeek-V3 shape (more tiles re-read the activations).
 int gemm_tile_n(int mode, int64_t n_out) {
   (void)mode;
   (void)n_out;
@@ -493,6 +534,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   } else {
     mbs = mb;
   }
+  CUtensorMap mo = ma;  // GEMM1 stores no O
+  if (L.mode == 2) {
+    if (!map_out(&mo, L.out, (uint64_t)L.N, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
+  }
   GemmArgs g;
   g.sfa = L.sfa;
   g.sfb = L.sfb;
@@ -519,10 +564,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
   if (L.mode == 1) {
-    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
-    return run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
+    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
+    return run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
   }
-  return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, g, (int)grid, st);
+  return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
 }
 
 }  // namespace mm

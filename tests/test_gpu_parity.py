@@ -260,6 +260,9 @@ MEGA_CASES = {
     # Zipf routing over 32 experts: one-tile experts beside experts with
     # several m tiles, so the tile order interleaves the two kinds
     "zipf_mixed_sizes": dict(n=1024, h=512, inter=256, e=32, k=4, routing="zipf"),
+    # 1024 routed + 1 shared segments: the segment table leaves no shared
+    # memory for GEMM2's output staging, so O rows are stored directly
+    "many_experts": dict(n=256, h=256, inter=128, e=1024, k=8, shared=1),
 }
 
 
