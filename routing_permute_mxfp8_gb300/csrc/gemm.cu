@@ -31,11 +31,12 @@
 //          intermediate columns -> swiglu -> one MX group per 32 columns,
 //          entirely within a thread; writes A_hat (FP8) and its scales
 //          directly in GEMM2's operand layouts.
-//   GEMM2: fp32 -> bf16 rows of O.  Each warp stages a 32-row x 32-column
-//          block in shared memory (64B swizzle, conflict-free) and one TMA
-//          store writes it; blocks with padding rows, or launches whose
-//          segment table leaves no room for the staging buffers, store
-//          rows directly from registers.
+//   GEMM2: fp32 -> bf16 rows of O.
+// Output stores: each warp stages a 32-row x 64-byte block (GEMM1: 64
+// A_hat codes, GEMM2: 32 bf16) in shared memory (64B swizzle, no bank
+// conflicts) and one TMA store writes it; blocks with padding rows, and
+// launches whose segment table leaves no room for the staging buffers,
+// store rows directly from registers.
 // Every wait is bounded; a timeout sets MM_DEVERR_TIMEOUT and the CTA
 // drains its own copies and MMAs, frees TMEM and returns.
 #include "mm_route.cuh"
@@ -88,7 +89,7 @@ struct GemmArgs {
   uint8_t* act_sf;
   __nv_bfloat16* out;
   int32_t* dev_err;
-  int o_stage;    // GEMM2: stage O blocks in shared memory for TMA stores
+  int o_stage;    // stage output blocks (A_hat / O) in shared memory for TMA stores
 };
 
 struct TileInfo {
@@ -218,6 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = mpre[nseg] * g.n_tiles;
   const int kblocks = g.K / kBK;
 
+  // E8M0 scale tiles of a stage -> its 16 TMEM columns (A, B rows 0-127, B rows 128-255)
+  auto copy_sf = [&](uint32_t s) {
+    const uint32_t c = tmem + kAccCols + s * 16;
+    tc_cp_32x128b_warpx4(c, smem_desc(smem_u32(smSFA + s * 512), 0, 128, 0));
+    tc_cp_32x128b_warpx4(c + 4, smem_desc(smem_u32(smSFB + s * 1024), 0, 128, 0));
+    tc_cp_32x128b_warpx4(c + 8, smem_desc(smem_u32(smSFB + s * 1024 + 512), 0, 128, 0));
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -288,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // the scale copies serialise with the MMAs in the tensor pipe
+          // (one copy instruction costs about a sixth of this k-block's MMAs)
+          copy_sf(stage);
           const uint32_t sfc = tmem + kAccCols + stage * 16;
-          tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(smSFA + stage * 512), 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(smSFB + stage * 1024), 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfc + 8, smem_desc(smem_u32(smSFB + stage * 1024 + 512), 0, 128, 0));
           const uint32_t a0 = smem_u32(smA + stage * kABytes);
           const uint32_t b0 = smem_u32(smB + stage * kBBytes);
 #pragma unroll
@@ -347,6 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
+        // TMA store of the warp's 32 x 64 FP8 block when all its rows are real
+        const bool staged = g.o_stage && g.seg_rows[ti.seg] - ti.mt * kBM >= (q + 1) * 32;
+        uint8_t* stg = smO + (warp - 2) * kOStageBytes;
+        if (staged) {
+          if (lane == 0) bulk_wait_read();  // the previous block has left the buffer
+          __syncwarp();
+        }
         uint32_t sfw = 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -364,12 +380,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           float inv;
           const uint32_t code = mx_scale(amax, fmt_emax<kActFmt>(), inv);
           sfw |= code << (8 * i);
-          if (valid) {
+          if (staged || valid) {
             const uint2 p0 = pack8_fp8<kActFmt>(a, inv), p1 = pack8_fp8<kActFmt>(a + 8, inv);
             const uint2 p2 = pack8_fp8<kActFmt>(a + 16, inv), p3 = pack8_fp8<kActFmt>(a + 24, inv);
-            uint8_t* dst = g.act_q + grow * g.inter + ti.nt * 128 + c * 32;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(p0.x, p0.y, p1.x, p1.y);
-            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(p2.x, p2.y, p3.x, p3.y);
+            const uint4 lo = make_uint4(p0.x, p0.y, p1.x, p1.y), hi = make_uint4(p2.x, p2.y, p3.x, p3.y);
+            if (staged) {
+              const int sw = (lane >> 1) & 3;  // 64B swizzle of row `lane`
+              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * i) ^ sw) << 4)) = lo;
+              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * i + 1) ^ sw) << 4)) = hi;
+            } else {
+              uint8_t* dst = g.act_q + grow * g.inter + ti.nt * 128 + c * 32;
+              *reinterpret_cast<uint4*>(dst) = lo;
+              *reinterpret_cast<uint4*>(dst + 16) = hi;
+            }
+          }
+        }
+        if (staged) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, stg, ti.nt * 128 + 64 * half, (int)((grow - r) + q * 32));
+            bulk_commit();
           }
         }
         if (valid)
@@ -418,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (kMode == 2 && g.o_stage && lane == 0) bulk_wait_all();
+    if (g.o_stage && lane == 0) bulk_wait_all();
     if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
   }
 
@@ -470,15 +501,18 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 matrix [rows][cols] (cols contiguous), box 32 x 32, 64B swizzle: the
-// GEMM2 output blocks that the epilogue stages in shared memory.
-bool map_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+// Output matrix [rows][cols] (cols contiguous) of bf16 (GEMM2's O) or FP8
+// bytes (GEMM1's A_hat), box 64 bytes x 32 rows, 64B swizzle: the blocks
+// that the epilogue stages in shared memory.
+bool map_out(CUtensorMap* m, const void* ptr, bool bf16, uint64_t cols, uint64_t rows) {
+  const uint64_t esz = bf16 ? 2 : 1;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {32, 32};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32};
   cuuint32_t es[2] = {1, 1};
   EncodeTiledFn f = encode_fn();
-  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+  return f && f(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr),
+                dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -492,8 +526,8 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
   const size_t base = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) +
                       8 * (2 * kStages + 2 * kAcc + 1) + 16 + 12 * (size_t)(g.nseg + 1);
   constexpr size_t kMaxSmem = 232448;
-  // O staging buffers only where the segment table leaves room for them
-  g.o_stage = kMode == 2 && base + kEpiWarps * kOStageBytes <= kMaxSmem ? 1 : 0;
+  // output staging buffers only where the segment table leaves room for them
+  g.o_stage = base + kEpiWarps * kOStageBytes <= kMaxSmem ? 1 : 0;
   const size_t smem = base + (g.o_stage ? kEpiWarps * kOStageBytes : 0);
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -534,9 +568,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   } else {
     mbs = mb;
   }
-  CUtensorMap mo = ma;  // GEMM1 stores no O
+  CUtensorMap mo;
   if (L.mode == 2) {
-    if (!map_out(&mo, L.out, (uint64_t)L.N, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
+    if (!map_out(&mo, L.out, true, (uint64_t)L.N, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
+  } else {
+    if (!map_out(&mo, L.act_q, false, (uint64_t)L.inter, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
   }
   GemmArgs g;
   g.sfa = L.sfa;
