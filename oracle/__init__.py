@@ -24,6 +24,7 @@ _lib = None
 
 E5M2 = 23
 E4M3 = 24
+E2M1 = 296   # FLOAT4_E2M1; the oracle keeps one 4-bit code per byte (bits 0-3)
 DT_F32, DT_F16, DT_BF16 = 0, 1, 27
 
 
@@ -73,7 +74,8 @@ def num_threads() -> int:
 
 
 def fp8_value(code: int, fmt: int) -> float:
-    """Value of one FP8 code (format definition of FLOAT8_E4M3FN / FLOAT8_E5M2)."""
+    """Value of one FP8 code (format definition of FLOAT8_E4M3FN / FLOAT8_E5M2), or of
+    one FLOAT4_E2M1 code (bits 0-3)."""
     return float(_load().orc_fp8_value(code, fmt))
 
 

@@ -15,7 +15,9 @@
  *   MegaMoE README (gitcode.com/azyuli/ops-transformer, mc2/mega_moe),
  *     "A8W8-FP quantization scenario" stages 1-4 and the swiglu formula in
  *     "Activation function formulas"  -> orc_mx_block, orc_expert_row,
- *     orc_mega_moe_tokens
+ *     orc_mega_moe_tokens;  "A8W4-FP quantization scenario" (FLOAT4_E2M1
+ *     weights with E8M0 scales, FP8 E4M3 activations) -> the same functions
+ *     with the E2M1 element format
  *
  * Floating point is carried in double.  Readings of what the pages leave
  * open (shared-exponent rule, rounding, saturation, sign of zero, flatten
@@ -31,6 +33,7 @@
 
 #define ORC_E5M2 23
 #define ORC_E4M3 24
+#define ORC_E2M1 296  /* FLOAT4_E2M1: one 4-bit code per byte here (bits 0-3) */
 
 int orc_num_threads(void) {
 #ifdef _OPENMP
@@ -49,8 +52,13 @@ int orc_num_threads(void) {
  * FLOAT8_E5M2: 1 sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent
  * field 31 holds inf / NaN; largest finite 1.75 * 2^15 = 57344; smallest
  * normal 2^-14; subnormals m * 2^-16.
+ * FLOAT4_E2M1 (OCP MX v1.0 FP4): 1 sign, 2 exponent bits (bias 1), 1
+ * mantissa bit, no infinities or NaN; values 0, 0.5 (subnormal), 1, 1.5, 2,
+ * 3, 4, 6; largest finite 6 = 1.5 * 2^2; smallest normal 2^0.  The sign is
+ * bit 3 of the code.
  * ------------------------------------------------------------------------- */
 typedef struct {
+  int nbits;    /* bits of a code (8, or 4 for E2M1) */
   int mbits;    /* explicit mantissa bits */
   int bias;
   int emin;     /* exponent of the smallest normal */
@@ -61,20 +69,22 @@ typedef struct {
 static orc_fmt fmt_of(int code) {
   orc_fmt f;
   if (code == ORC_E5M2) {
-    f.mbits = 2; f.bias = 15; f.emin = -14; f.emax = 15; f.maxv = 57344.0;
+    f.nbits = 8; f.mbits = 2; f.bias = 15; f.emin = -14; f.emax = 15; f.maxv = 57344.0;
+  } else if (code == ORC_E2M1) {
+    f.nbits = 4; f.mbits = 1; f.bias = 1; f.emin = 0; f.emax = 2; f.maxv = 6.0;
   } else {
-    f.mbits = 3; f.bias = 7; f.emin = -6; f.emax = 8; f.maxv = 448.0;
+    f.nbits = 8; f.mbits = 3; f.bias = 7; f.emin = -6; f.emax = 8; f.maxv = 448.0;
   }
   return f;
 }
 
-/* Value of an FP8 code (NaN / inf as such). */
+/* Value of an FP8 (or FP4 E2M1) code (NaN / inf as such). */
 double orc_fp8_value(uint8_t c, int code) {
   orc_fmt f = fmt_of(code);
-  int sign = c >> 7;
-  int ebits = (c >> f.mbits) & ((1 << (7 - f.mbits)) - 1);
+  int sign = (c >> (f.nbits - 1)) & 1;
+  int ebits = (c >> f.mbits) & ((1 << (f.nbits - 1 - f.mbits)) - 1);
   int m = c & ((1 << f.mbits) - 1);
-  int etop = (1 << (7 - f.mbits)) - 1;
+  int etop = (1 << (f.nbits - 1 - f.mbits)) - 1;
   double v;
   if (code == ORC_E4M3 && ebits == etop && m == (1 << f.mbits) - 1) return NAN;
   if (code == ORC_E5M2 && ebits == etop) return m == 0 ? (sign ? -INFINITY : INFINITY) : NAN;
@@ -98,11 +108,12 @@ static double round_to_grid(double a, int mbits, int emin) {
   return nearbyint(a / q) * q;          /* a / q and r * q are exact; nearbyint is ties-to-even */
 }
 
-/* FP8 code of a finite double: saturate the magnitude to the largest finite
- * value, round to nearest with ties to even, keep the sign (also for zero). */
+/* FP8 (or FP4 E2M1) code of a finite double: saturate the magnitude to the
+ * largest finite value, round to nearest with ties to even, keep the sign
+ * (also for zero). */
 uint8_t orc_fp8_round(double t, int code) {
   orc_fmt f = fmt_of(code);
-  uint8_t sign = signbit(t) ? 0x80 : 0x00;
+  uint8_t sign = signbit(t) ? (uint8_t)(1u << (f.nbits - 1)) : 0x00;
   double a = fabs(t);
   if (a > f.maxv) a = f.maxv;
   double v = round_to_grid(a, f.mbits, f.emin);

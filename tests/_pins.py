@@ -1,7 +1,8 @@
 """Test-side reference helpers that are independent of the oracle.
 
-FP8 code values come from PyTorch's float8 dtypes (a library decode);
-rounding is an exhaustive search over all codes.  Nothing here imports the
+FP8 code values come from PyTorch's float8 dtypes (a library decode), FP4
+E2M1 values from the value list of the OCP MX v1.0 specification; rounding
+is an exhaustive search over all codes.  Nothing here imports the
 oracle or the CUDA library.
 """
 from __future__ import annotations
@@ -9,15 +10,24 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-E5M2, E4M3 = 23, 24
-MAXV = {E4M3: 448.0, E5M2: 57344.0}
-EMAX = {E4M3: 8, E5M2: 15}
+E5M2, E4M3, E2M1 = 23, 24, 296
+MAXV = {E4M3: 448.0, E5M2: 57344.0, E2M1: 6.0}
+EMAX = {E4M3: 8, E5M2: 15, E2M1: 2}
+# FLOAT4_E2M1 magnitudes of the codes 0..7 as the OCP MX v1.0 spec lists them;
+# codes 8..15 are their negatives (sign bit 3)
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 _TORCH = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 _tables = {}
 
 
 def fp8_table(fmt: int) -> np.ndarray:
-    """float64 value of each of the 256 codes, decoded by torch."""
+    """float64 value of each of the 256 codes, decoded by torch (FP8), or of
+    the 16 E2M1 codes from the spec's list (codes 16..255 are NaN)."""
+    if fmt == E2M1 and fmt not in _tables:
+        tab = np.full(256, np.nan)
+        tab[:8] = E2M1_MAGNITUDES
+        tab[8:16] = [-v for v in E2M1_MAGNITUDES]
+        _tables[fmt] = tab
     if fmt not in _tables:
         codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
         _tables[fmt] = codes.view(_TORCH[fmt]).to(torch.float64).numpy().copy()
@@ -31,7 +41,7 @@ def brute_round(t: np.ndarray, fmt: int) -> np.ndarray:
     tab = fp8_table(fmt)
     t = np.asarray(t, dtype=np.float64).ravel()
     a = np.minimum(np.abs(t), MAXV[fmt])
-    pos = np.arange(128)
+    pos = np.arange(8 if fmt == E2M1 else 128)
     pos = pos[np.isfinite(tab[pos])]
     vals = tab[pos]
     out = np.empty(t.size, dtype=np.uint8)
@@ -45,7 +55,7 @@ def brute_round(t: np.ndarray, fmt: int) -> np.ndarray:
         pick = np.where(even.any(axis=1), even.argmax(axis=1), tie.argmax(axis=1))
         out[i:i + step] = pos[pick]
     neg = np.signbit(t)
-    out[neg] |= 0x80
+    out[neg] |= 0x08 if fmt == E2M1 else 0x80
     return out
 
 

@@ -19,6 +19,7 @@ from tests import _pins as P
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 FMTS = [P.E4M3, P.E5M2]
+FMTS_ALL = FMTS + [P.E2M1]   # with FLOAT4_E2M1 (A8W4-FP weights)
 
 
 # ---------------------------------------------------------------- FP8 codes
@@ -31,6 +32,18 @@ def test_fp8_decode_matches_torch(fmt):
             assert np.isnan(v), c
         else:
             assert v == tab[c], (c, v, tab[c])
+
+
+def test_fp4_decode_matches_spec_list():
+    """FLOAT4_E2M1: the 16 codes against the OCP MX v1.0 value list."""
+    tab = P.fp8_table(P.E2M1)
+    for c in range(16):
+        v = oracle.fp8_value(c, P.E2M1)
+        assert v == tab[c] and np.signbit(v) == (c >= 8), (c, v)
+    # largest finite value, the subnormal, one
+    assert oracle.fp8_value(0x7, P.E2M1) == 6.0
+    assert oracle.fp8_value(0x1, P.E2M1) == 0.5
+    assert oracle.fp8_value(0x2, P.E2M1) == 1.0
 
 
 def test_fp8_closed_forms():
@@ -61,7 +74,7 @@ def _hard_values(fmt, n, seed):
     return allv
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS_ALL)
 def test_fp8_round_brute_force(fmt):
     t = _hard_values(fmt, 1_000_000, 1 + fmt)
     got = oracle.fp8_round_array(t, fmt)
@@ -103,7 +116,7 @@ def test_mx_hand_blocks(block):
     assert list(q[: len(codes)]) == codes
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS_ALL)
 def test_mx_scale_puts_amax_in_top_binade(fmt):
     """With s = code - 127, amax * 2^-s lies in [2^emax, 2^(emax+1)) unless the
     scale is clamped: the group's largest element uses the format's top binade."""
@@ -112,11 +125,11 @@ def test_mx_scale_puts_amax_in_top_binade(fmt):
     for r in range(x.shape[0]):
         _, s = oracle.mx_block(x[r], fmt)
         t = np.abs(x[r]).max() * 2.0 ** -(s - 127)
-        top = {P.E4M3: 256.0, P.E5M2: 32768.0}[fmt]
+        top = {P.E4M3: 256.0, P.E5M2: 32768.0, P.E2M1: 4.0}[fmt]
         assert top <= t < 2 * top
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS_ALL)
 def test_mx_roundtrip_bound(fmt):
     """|DQ(Q(v)) - v| <= half the local FP8 spacing times 2^s for unsaturated
     elements; saturated ones decode to the largest finite value."""
@@ -139,7 +152,7 @@ def test_mx_roundtrip_bound(fmt):
             assert abs(bi - ti) <= (hi - lo) / 2 + 1e-300
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS_ALL)
 def test_mx_rows_match_brute_force(fmt):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((64, 256)) * np.exp2(rng.integers(-6, 6, (64, 1)))
@@ -293,6 +306,9 @@ def _weights(cfg, shared=False):
     ("tiny", dict(dispatch_fmt=P.E5M2, gate_dtype="bf16", routing="zipf")),
     ("tiny", dict(n=16, shared=1)),
     ("tiny", dict(n=24, e=1, k=1)),     # K = 1, one expert: a dense two-layer FFN
+    # A8W4-FP: FLOAT4_E2M1 weights, MXFP8 E4M3 activations
+    ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E4M3)),
+    ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E4M3, n=16, shared=1, routing="zipf")),
 ])
 def test_mega_moe_matches_numpy_grouped(name, kw):
     cfg = synth.CONFIGS[name].scaled(**kw)
