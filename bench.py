@@ -218,14 +218,15 @@ def gpu_weights(cfg, mm, torch, n_exp, seed):
     gen.manual_seed(seed)
     out = []
     for n_out, k_red in ((2 * cfg.inter, cfg.h), (cfg.h, cfg.inter)):
-        q = torch.empty((n_exp, n_out, k_red), dtype=torch.uint8, device=dev)
+        kq = k_red // 2 if cfg.weight_fmt == mm.DT_FP4_E2M1 else k_red   # FP4: two codes per byte
+        q = torch.empty((n_exp, n_out, kq), dtype=torch.uint8, device=dev)
         s = torch.empty((n_exp, n_out, k_red // 32), dtype=torch.uint8, device=dev)
         chunk = max(1, (1 << 28) // (n_out * k_red))
         for e0 in range(0, n_exp, chunk):
             e1 = min(n_exp, e0 + chunk)
             w = torch.randn(((e1 - e0) * n_out, k_red), generator=gen, device=dev, dtype=torch.float32) * 0.02
             qq, ss = mm.mm_mx_quantize(w, cfg.weight_fmt, scale_cols=k_red // 32)
-            q[e0:e1] = qq.view(e1 - e0, n_out, k_red)
+            q[e0:e1] = qq.view(e1 - e0, n_out, kq)
             s[e0:e1] = ss.view(e1 - e0, n_out, k_red // 32)
             del w, qq, ss
         out += [q, s]
@@ -532,6 +533,37 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
     out["decode"] = {"tokens_per_s": dc.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
                      "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
                      "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+    del x, ws, S
+    # A8W4-FP: the same prefill and decode shapes with MXFP4 E2M1 weights (packed,
+    # half the weight bytes) and MXFP8 E4M3 activations
+    a8w4 = {}
+    pc4 = cfg_prefill.scaled(weight_fmt=mm.DT_FP4_E2M1, dispatch_fmt=mm.DT_FP8_E4M3FN)
+    x, ids, gate, W4, _ = gpu_inputs(pc4, mm, torch, seed_offset=30 + dist.rank)
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(pc4.n, pc4.h, pc4.k, pc4.e, pc4.inter, pc4.shared, 1),
+                     dtype=torch.uint8, device="cuda")
+    y = torch.empty((pc4.n, pc4.h), dtype=torch.bfloat16, device="cuda")
+    ms, st, _ = time_steps(torch, lambda: mega_call(mm, pc4, x, ids, gate, W4, None, ws, y), steps, 3, dist)
+    t = ms / steps / 1e3
+    a8w4["prefill"] = {"workload": f"{pc4.name} N={pc4.n} H={pc4.h} I={pc4.inter} E={pc4.e} K={pc4.k}",
+                       "tokens_per_s": pc4.n / t, "ms_per_step": t * 1e3, "tflops": ffn_flops(pc4) / t / 1e12,
+                       "tflops_frac": ffn_flops(pc4) / t / 1e12 / fp8_peak,
+                       "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+    del x, ws
+    dc4 = dc.scaled(weight_fmt=mm.DT_FP4_E2M1, dispatch_fmt=mm.DT_FP8_E4M3FN)
+    x, ids, gate, _, S4 = gpu_inputs(dc4, mm, torch, seed_offset=40 + dist.rank, weights=W4)
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(dc4.n, dc4.h, dc4.k, dc4.e, dc4.inter, dc4.shared, 1),
+                     dtype=torch.uint8, device="cuda")
+    y = torch.empty((dc4.n, dc4.h), dtype=torch.bfloat16, device="cuda")
+    ms, st, _ = time_steps(torch, lambda: mega_call(mm, dc4, x, ids, gate, W4, S4, ws, y), steps, 3, dist)
+    t = ms / steps / 1e3
+    touched = int(torch.unique(ids).numel())
+    wbytes = (touched + dc4.shared) * 3 * dc4.h * dc4.inter * (0.5 + 1 / 32)
+    a8w4["decode"] = {"tokens_per_s": dc4.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
+                      "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9,
+                      "hbm_frac": wbytes / t / 1e9 / hbm_peak,
+                      "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+    out["a8w4"] = a8w4
+    del x, ws, W4, S4
     return out
 
 

@@ -63,8 +63,12 @@ typedef enum {
 #define MM_DEVERR_DUPLICATE_ID 2 /* a token lists one expert twice (MegaMoE forbids it) */
 #define MM_DEVERR_TIMEOUT 4      /* a bounded wait inside a kernel gave up */
 
-/* Element type codes.  The FP8 codes are the MegaMoE dtype codes
- * (dispatchQuantOutDtype: 23 = FLOAT8_E5M2, 24 = FLOAT8_E4M3FN). */
+/* Element type codes.  The FP8 / FP4 codes are the MegaMoE dtype codes
+ * (dispatchQuantOutDtype: 23 = FLOAT8_E5M2, 24 = FLOAT8_E4M3FN,
+ * 296 = FLOAT4_E2M1).  FLOAT4_E2M1 arrays here are packed two codes per
+ * byte along the contiguous dimension, element 2i in bits 0-3 and element
+ * 2i+1 in bits 4-7 (the pages store them in Ascend's FRACTAL_NZ_C0_32
+ * format instead). */
 #define MM_DT_FLOAT32 0
 #define MM_DT_FLOAT16 1
 #define MM_DT_INT32 3
@@ -72,6 +76,7 @@ typedef enum {
 #define MM_DT_FP8_E5M2 23
 #define MM_DT_FP8_E4M3FN 24
 #define MM_DT_BFLOAT16 27
+#define MM_DT_FP4_E2M1 296
 
 /* Quant-mode codes of moe_token_permute and MoeInitRoutingV3:
  * -1 none, 2 MXFP8 E5M2, 3 MXFP8 E4M3FN (9, MXFP4, is not implemented). */
@@ -174,18 +179,21 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  * x                  [bs, h] bf16.
  * topk_ids           [bs, k] int32, distinct per token, in [0, moe_expert_num).
  * topk_weights       [bs, k], topk_weights_dtype MM_DT_FLOAT32 or MM_DT_BFLOAT16.
- * weight1            [E, 2*intermediate, h] FP8 (weight_dtype 23 / 24); rows
- *                    [0, I) are the gate (SiLU) branch, [I, 2I) the up branch.
- * weight2            [E, h, intermediate] FP8 of the same type.
+ * weight1            [E, 2*intermediate, h] FP8 (weight_dtype 23 / 24), or
+ *                    FLOAT4_E2M1 (weight_dtype 296, the A8W4-FP scenario:
+ *                    [E, 2*intermediate, h/2] packed bytes); rows [0, I) are
+ *                    the gate (SiLU) branch, [I, 2I) the up branch.
+ * weight2            [E, h, intermediate] of the same type (FP4: [E, h, I/2]).
  * weight_scales1/2   E8M0, MM_WSCALE_ROWS: [E, 2I, CeilDiv(h,64), 2] and
  *                    [E, h, CeilDiv(I,64), 2]; MM_WSCALE_PREPARED: the
  *                    outputs of mm_prepare_weight_scales for those arrays.
  * shared_weight*     same layouts with leading dimension shared_expert_num
- *                    (0..4; NULL when 0); shared_weight_dtype 23 / 24.
+ *                    (0..4; NULL when 0); shared_weight_dtype 23 / 24 / 296.
  * ep_world_size      must be 1.
  * max_recv_token_num 0, or >= bs*k (the rows this rank receives at ep = 1).
  * dispatch_quant_mode must be 4 (MX quantisation inside the operator);
- * dispatch_quant_out_dtype 23 / 24 is also the type of A_hat.
+ * dispatch_quant_out_dtype 23 / 24 is also the type of A_hat (FP8 with either
+ *                    weight type: A8W8-FP, A8W4-FP).
  * combine_quant_mode must be 0; activation must be "swiglu" (or NULL) with
  *                    no parameters (clamp disabled).
  * y                  [bs, h] bf16 output.
@@ -233,13 +241,16 @@ mm_status mm_prepare_weight_scales(const uint8_t* src, int which, int64_t expert
                                    int64_t n_out, int64_t k_red, uint8_t* dst, void* stream);
 
 /* ------------------------------------------------------------------------
- * mm_mx_quantize -- Q_MX along each row (MegaMoE A8W8-FP stage 1): groups of
+ * mm_mx_quantize -- Q_MX along each row (MegaMoE A8W8-FP stage 1; with
+ * out_dtype 296 the MXFP4 E2M1 weights of the A8W4-FP scenario): groups of
  * 32 consecutive elements share one E8M0 exponent s = floor(log2 amax) -
- * emax (8 for E4M3FN, 15 for E5M2), clamped to [-127, 127]; elements are
- * FP8(v * 2^-s), nearest-even, saturated to the largest finite value.
+ * emax (8 for E4M3FN, 15 for E5M2, 2 for E2M1), clamped to [-127, 127];
+ * elements are FP8 / FP4(v * 2^-s), nearest-even, saturated to the largest
+ * finite value.
  *
  * src     [rows, cols] of src_dtype (fp32 / bf16 / fp16); cols a multiple of 16.
- * q       [rows, cols] FP8 output of out_dtype (23 / 24).
+ * q       [rows, cols] FP8 output of out_dtype (23 / 24), or [rows, cols/2]
+ *         packed FP4 bytes (296).
  * scales  [rows, scale_cols] E8M0 output, scale_cols >= CeilDiv(cols, 32);
  *         columns past CeilDiv(cols, 32) are written as 0.
  * ---------------------------------------------------------------------- */

@@ -26,6 +26,7 @@ _lib = None
 
 DT_F32, DT_F16, DT_I32, DT_I64, DT_BF16 = 0, 1, 3, 9, 27
 DT_FP8_E5M2, DT_FP8_E4M3FN = 23, 24
+DT_FP4_E2M1 = 296   # packed two codes per byte, element 2i in bits 0-3
 QUANT_NONE, QUANT_MXFP8_E5M2, QUANT_MXFP8_E4M3FN = -1, 2, 3
 WSCALE_ROWS, WSCALE_PREPARED = 0, 1
 
@@ -204,11 +205,12 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 dispatch_quant_mode: int = 4, dispatch_quant_out_dtype: int = DT_FP8_E4M3FN,
                 combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
                 out=None, workspace=None, dev_err=None, want_expanded_row_idx=False, want_act=False):
-    """MegaMoE forward, A8W8-FP, ep_world_size = 1.
+    """MegaMoE forward, A8W8-FP or A8W4-FP, ep_world_size = 1.
 
     x [BS, H] bf16; topk_ids [BS, K] int32; topk_weights [BS, K] fp32 / bf16;
     weight1 [E, 2I, H] and weight2 [E, H, I] FP8 (torch float8 or uint8 with
-    weight_dtype); weight_scales1 / 2 uint8 E8M0 in the pages' layout
+    weight_dtype), or with weight_dtype=DT_FP4_E2M1 packed FP4 bytes
+    [E, 2I, H/2] and [E, H, I/2]; weight_scales1 / 2 uint8 E8M0 in the pages' layout
     (weight_scale_layout=0) or prepared by mm_prepare_weight_scales (1).
     Returns (y [BS, H] bf16, expert_token_nums [E] int32) and, on request,
     expanded_row_idx [BS*K] int32 and A_hat codes / scales in sorted order.
@@ -217,10 +219,10 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     L = load()
     bs, h = x.shape
     k = topk_ids.shape[1]
-    inter = weight2.shape[2]
+    wdt = _fp8_code(weight1, weight_dtype)
+    inter = weight2.shape[2] * (2 if wdt == DT_FP4_E2M1 else 1)
     s_num = 0 if shared_weight1 is None else shared_weight1.shape[0]
     dev = x.device
-    wdt = _fp8_code(weight1, weight_dtype)
     swdt = wdt if shared_weight1 is None else _fp8_code(shared_weight1, wdt if shared_weight_dtype is None
                                                          else shared_weight_dtype)
     y = out if out is not None else torch.empty((bs, h), dtype=torch.bfloat16, device=dev)
@@ -266,12 +268,13 @@ def mm_prepare_weight_scales(scales, k_red: int, which: int):
 
 def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None = None):
     """Q_MX along the last dimension of a 2-D fp32 / bf16 / fp16 tensor.
-    Returns (codes [rows, cols] uint8, scales [rows, scale_cols] uint8 E8M0)."""
+    Returns (codes [rows, cols] uint8 -- [rows, cols / 2] packed for DT_FP4_E2M1 --,
+    scales [rows, scale_cols] uint8 E8M0)."""
     _need_cuda(src)
     L = load()
     rows, cols = src.shape
     sc = _scale_cols(cols) if scale_cols is None else scale_cols
-    q = torch.empty((rows, cols), dtype=torch.uint8, device=src.device)
+    q = torch.empty((rows, cols // 2 if out_dtype == DT_FP4_E2M1 else cols), dtype=torch.uint8, device=src.device)
     s = torch.empty((rows, sc), dtype=torch.uint8, device=src.device)
     _check(L.mm_mx_quantize(_ptr(src), _dt(src), rows, cols, out_dtype, _ptr(q), _ptr(s), sc,
                             _stream(src.device)), "mm_mx_quantize")

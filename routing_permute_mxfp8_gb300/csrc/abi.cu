@@ -32,6 +32,8 @@ struct Carver {
 bool is_src_dtype(int dt) { return dt == MM_DT_BFLOAT16 || dt == MM_DT_FLOAT16 || dt == MM_DT_FLOAT32; }
 int dt_size(int dt) { return dt == MM_DT_FLOAT32 ? 4 : 2; }
 bool is_fp8(int64_t dt) { return dt == MM_DT_FP8_E4M3FN || dt == MM_DT_FP8_E5M2; }
+// expert weight types: FP8 (A8W8-FP) or FP4 E2M1 (A8W4-FP)
+bool is_mx_weight(int64_t dt) { return is_fp8(dt) || dt == MM_DT_FP4_E2M1; }
 int quant_fmt(int quant_mode) {
   return quant_mode == MM_QUANT_MXFP8_E5M2 ? MM_DT_FP8_E5M2
                                            : (quant_mode == MM_QUANT_MXFP8_E4M3FN ? MM_DT_FP8_E4M3FN : -1);
@@ -400,8 +402,8 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   if (ep_world_size != 1) return MM_ERR_UNSUPPORTED;
   if (combine_quant_mode != 0) return MM_ERR_UNSUPPORTED;
   if (dispatch_quant_mode != 4) return MM_ERR_UNSUPPORTED;
-  if (!is_fp8(dispatch_quant_out_dtype) || !is_fp8(weight_dtype)) return MM_ERR_UNSUPPORTED;
-  if (shared_expert_num > 0 && !is_fp8(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
+  if (!is_fp8(dispatch_quant_out_dtype) || !is_mx_weight(weight_dtype)) return MM_ERR_UNSUPPORTED;
+  if (shared_expert_num > 0 && !is_mx_weight(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
   if (!activation_is_plain_swiglu(activation, activation_params, n_activation_params)) return MM_ERR_UNSUPPORTED;
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
   const int64_t rows = bs * k;
@@ -591,7 +593,7 @@ mm_status mm_prepare_weight_scales(const uint8_t* src, int which, int64_t expert
 
 mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t cols, int out_dtype, uint8_t* q,
                          uint8_t* scales, int64_t scale_cols, void* stream) {
-  if (rows < 0 || cols <= 0 || !is_src_dtype(src_dtype) || !is_fp8(out_dtype)) return MM_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || !is_src_dtype(src_dtype) || !is_mx_weight(out_dtype)) return MM_ERR_INVALID_ARG;
   if (cols % 16 != 0) return MM_ERR_UNSUPPORTED;
   if (scale_cols < ceil_div(cols, 32)) return MM_ERR_INVALID_ARG;
   if (rows == 0) return MM_OK;

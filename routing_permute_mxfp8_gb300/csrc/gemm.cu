@@ -90,6 +90,7 @@ struct GemmArgs {
   __nv_bfloat16* out;
   int32_t* dev_err;
   int o_stage;    // stage output blocks (A_hat / O) in shared memory for TMA stores
+  int b_fp4, b_fp4_sh;  // routed / shared weights are packed FP4 E2M1
 };
 
 struct TileInfo {
@@ -256,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kStageTx);
+          // packed FP4 weights count their global (packed) bytes
+          mbar_arrive_expect_tx(&full[stage], kStageTx - ((sh ? g.b_fp4_sh : g.b_fp4) ? kBBytes / 2 : 0));
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], kb * kBK, am * kBM);
@@ -489,14 +491,20 @@ bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uin
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Stacked weights [E][N][K] FP8.
-bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e, uint32_t box_rows) {
+// Stacked weights [E][N][K]: FP8 bytes, or FP4 E2M1 packed two per byte,
+// which TMA expands into the 16-byte-aligned groups of 16 codes that the
+// kind::mxf8f6f4 MMA reads (a box row of 128 codes fills 128 smem bytes,
+// like FP8, so the stage layout does not change).
+bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e, uint32_t box_rows,
+            bool fp4 = false) {
   cuuint64_t dims[3] = {k, n, e};
-  cuuint64_t strides[2] = {k, n * k};
+  const uint64_t row_bytes = fp4 ? k / 2 : k;
+  cuuint64_t strides[2] = {row_bytes, n * row_bytes};
   cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   EncodeTiledFn f = encode_fn();
-  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+  return f && f(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                const_cast<void*>(ptr), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -517,7 +525,8 @@ bool map_out(CUtensorMap* m, const void* ptr, bool bf16, uint64_t cols, uint64_t
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : 0; }
+// instruction-descriptor format code (kind::mxf8f6f4): E4M3 0, E5M2 1, E2M1 5
+int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : (dt == MM_DT_FP4_E2M1 ? 5 : 0); }
 
 template <int kMode, int kActFmt, int kBN, int kAcc>
 cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbs,
@@ -561,9 +570,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   const uint32_t box_rows = L.mode == 1 ? 128 : (uint32_t)bn;
   CUtensorMap ma, mb, mbs;
   if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM)) return cudaErrorInvalidValue;
-  if (!map_3d(&mb, L.b, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_routed, box_rows)) return cudaErrorInvalidValue;
+  if (!map_3d(&mb, L.b, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_routed, box_rows, L.b_fmt == MM_DT_FP4_E2M1))
+    return cudaErrorInvalidValue;
   if (L.n_shared > 0) {
-    if (!map_3d(&mbs, L.b_sh, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_shared, box_rows))
+    if (!map_3d(&mbs, L.b_sh, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_shared, box_rows,
+                L.b_fmt_sh == MM_DT_FP4_E2M1))
       return cudaErrorInvalidValue;
   } else {
     mbs = mb;
@@ -587,6 +598,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, bn);
   g.big_mt = kBigMtiles;
   g.nb = (int)prepared_nblocks(L.N, L.mode == 1 ? 256 : bn);
+  g.b_fp4 = L.b_fmt == MM_DT_FP4_E2M1;
+  g.b_fp4_sh = (L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt) == MM_DT_FP4_E2M1;
   g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, bn);
   g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);
   g.inter = L.inter;

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -51,7 +52,20 @@ __device__ __forceinline__ uint16_t cvt_fp8x2(float lo, float hi) {
 
 template <int kFmt>
 __host__ __device__ constexpr int fmt_emax() {
-  return kFmt == MM_DT_FP8_E5M2 ? 15 : 8;
+  return kFmt == MM_DT_FP8_E5M2 ? 15 : (kFmt == MM_DT_FP4_E2M1 ? 2 : 8);
+}
+
+// Sixteen fp32 values scaled by inv -> 16 E2M1 codes, two per byte (element
+// 2i in bits 0-3), nearest-even, saturated to +-6 (8 bytes in a uint2).
+__device__ __forceinline__ uint2 pack16_fp4(const float* v, float inv) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t b = (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv),
+                                                          __NV_E2M1, cudaRoundNearest);
+    w[i >> 2] |= (b & 0xFFu) << (8 * (i & 3));
+  }
+  return make_uint2(w[0], w[1]);
 }
 
 // Eight fp32 values scaled by inv -> 8 FP8 bytes (little-endian in a uint2).

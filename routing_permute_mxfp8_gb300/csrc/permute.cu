@@ -105,9 +105,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs 
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     float inv;
     const uint32_t code = mx_scale(amax, fmt_emax<kFmt>(), inv);
-    const uint2 lo = pack8_fp8<kFmt>(v, inv);
-    const uint2 hi = pack8_fp8<kFmt>(v + 8, inv);
-    const uint4 packed = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    // 16 codes of this lane: 16 FP8 bytes, or 8 bytes of packed FP4
+    uint4 packed;
+    if (kFmt == MM_DT_FP4_E2M1) {
+      const uint2 p4 = pack16_fp4(v, inv);
+      packed = make_uint4(p4.x, p4.y, 0u, 0u);
+    } else {
+      const uint2 lo = pack8_fp8<kFmt>(v, inv);
+      const uint2 hi = pack8_fp8<kFmt>(v + 8, inv);
+      packed = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
     // tile layout: lanes 8m..8m+7 hold groups 4m'..4m'+3; lane 8m packs them
     uint32_t word = 0;
     if (kTiled) {
@@ -120,7 +127,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs 
     for (int t = 0; t < ndest; ++t) {
       const int32_t d = dest_at(t, d0, d1);
       if (d < 0 || !act) continue;
-      *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = packed;
+      if (kFmt == MM_DT_FP4_E2M1)
+        *reinterpret_cast<uint2*>(out + (int64_t)d * (a.h / 2) + col / 2) = make_uint2(packed.x, packed.y);
+      else
+        *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = packed;
       if (kTiled) {
         if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, g, groups4)) = word;
       } else if ((lane & 1) == 0) {
@@ -210,6 +220,7 @@ cudaError_t launch_mx_variant(const PermuteArgs& a, int blocks, cudaStream_t st)
 template <int kSrc>
 cudaError_t launch_mx_src(const PermuteArgs& a, int blocks, cudaStream_t st) {
   if (a.out_fmt == MM_DT_FP8_E5M2) return launch_mx_variant<kSrc, MM_DT_FP8_E5M2>(a, blocks, st);
+  if (a.out_fmt == MM_DT_FP4_E2M1) return launch_mx_variant<kSrc, MM_DT_FP4_E2M1>(a, blocks, st);
   return launch_mx_variant<kSrc, MM_DT_FP8_E4M3FN>(a, blocks, st);
 }
 

@@ -132,8 +132,19 @@ def test_out_of_range_ids_are_left_out_and_flagged():
 
 
 # ---------------------------------------------------------------- MX quantiser
+def pack_fp4(codes):
+    """Oracle FP4 codes (one per byte) -> the library's packed bytes (element
+    2i in bits 0-3, 2i+1 in bits 4-7)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def gpu_codes(codes, fmt):
+    return t(pack_fp4(codes) if fmt == 296 else codes)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("fmt", [23, 24])
+@pytest.mark.parametrize("fmt", [23, 24, 296])
 def test_mx_quantize_bit_exact(dtype, fmt):
     rng = np.random.default_rng(fmt)
     rows, cols = 513, 320
@@ -149,7 +160,7 @@ def test_mx_quantize_bit_exact(dtype, fmt):
     src = xt.view(torch.int16).numpy().view(np.uint16) if dtype != torch.float32 else xt.numpy()
     rq, rs = oracle.mx_quantize(src, src_dt, fmt, s_cols=s.shape[1])
     assert np.array_equal(host(s), rs)
-    assert np.array_equal(host(q), rq)
+    assert np.array_equal(host(q), pack_fp4(rq) if fmt == 296 else rq)
 
 
 # -------------------------------------------------------------------- MegaMoE
@@ -223,14 +234,15 @@ def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
         ws2 = mm.mm_prepare_weight_scales(ws2, cfg.inter, 2)
     kw = {}
     if sh is not None:
-        sw1, ss1, sw2, ss2 = [t(a) for a in sh]
+        sw1, ss1, sw2, ss2 = gpu_codes(sh[0], cfg.weight_fmt), t(sh[1]), gpu_codes(sh[2], cfg.weight_fmt), t(sh[3])
         if layout == 1:
             ss1 = mm.mm_prepare_weight_scales(ss1, cfg.h, 1)
             ss2 = mm.mm_prepare_weight_scales(ss2, cfg.inter, 2)
         kw = dict(shared_weight1=sw1, shared_weight2=sw2, shared_weight_scales1=ss1, shared_weight_scales2=ss2)
     err = zeros_err()
     y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
-        bf16(x), t(ids), gt, t(w1), t(w2), ws1, ws2, cfg.e, weight_dtype=cfg.weight_fmt, weight_scale_layout=layout,
+        bf16(x), t(ids), gt, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt), ws1, ws2, cfg.e,
+        weight_dtype=cfg.weight_fmt, weight_scale_layout=layout,
         dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err, want_expanded_row_idx=True, want_act=True, **kw)
     assert host(err)[0] == 0
     r_srt, r_exp, r_cnt, _ = oracle.route(ids, cfg.e)
@@ -260,6 +272,11 @@ MEGA_CASES = {
     # Zipf routing over 32 experts: one-tile experts beside experts with
     # several m tiles, so the tile order interleaves the two kinds
     "zipf_mixed_sizes": dict(n=1024, h=512, inter=256, e=32, k=4, routing="zipf"),
+    # A8W4-FP: MXFP4 E2M1 weights (packed), MXFP8 E4M3 activations
+    "a8w4_tiny": dict(weight_fmt=296, dispatch_fmt=24),
+    "a8w4_shared_zipf": dict(n=300, h=512, inter=256, e=8, k=4, shared=1, routing="zipf", weight_fmt=296,
+                             dispatch_fmt=24),
+    "a8w4_e5m2_tokens": dict(n=256, h=896, inter=384, e=8, k=4, weight_fmt=296, dispatch_fmt=23),
     # 1024 routed + 1 shared segments: the segment table leaves no shared
     # memory for GEMM2's output staging, so O rows are stored directly
     "many_experts": dict(n=256, h=256, inter=128, e=1024, k=8, shared=1),
