@@ -56,10 +56,10 @@ def _load():
     L.orc_mx_quantize_src.argtypes, L.orc_mx_quantize_src.restype = [p, i32, i64, i64, i32, p, p, i64], None
     L.orc_route.argtypes, L.orc_route.restype = [p, i32, i64, i64, i64, p, p, p], i64
     L.orc_permute.argtypes, L.orc_permute.restype = [p, i32, i64, i64, p, i64, i32, p, p, i64], None
-    L.orc_expert_row.argtypes = [p, p, i32, p, p, p, p, i32, i64, i64, i32, p, p, p]
+    L.orc_expert_row.argtypes = [p, p, i32, p, p, p, p, i32, i64, i64, i32, i32, p, p, p, p]
     L.orc_expert_row.restype = None
     L.orc_mega_moe_tokens.argtypes = [p, p, p, i32, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
-                                      i32, i32, i32, p, i64, p, p, p, p]
+                                      i32, i32, i32, p, i64, p, p, p, p, p, p, i32, p]
     L.orc_mega_moe_tokens.restype = None
     _lib = L
     return L
@@ -165,27 +165,58 @@ def permute(x: np.ndarray, dtype: int, k: int, sorted_row_idx: np.ndarray, m_out
     return out, sc
 
 
-def expert_row(xq, xs, x_fmt, w1, s1, w2, s2, w_fmt, a_fmt):
-    """One expanded row through one expert (A8W8-FP stages 2-3, swiglu).
+# Activations of the MegaMoE README ("Activation function formulas") and the
+# defaults its activation_params description gives.
+ACTIVATIONS = {"swiglu": 0, "swiglustep": 1, "swigluoai": 2, "situglu": 3, "gelu": 4}
+
+
+def activation_spec(name="swiglu", params=()):
+    """(kind, [c, alpha, beta, beta_lin]) for an activation name and its
+    activation_params list: clamp c (absent or 0: not enabled, +inf) for
+    swiglu / swiglustep / swigluoai; swigluoai alpha 1.702 and beta 1.0 by
+    default; situglu [beta] or [beta, beta_lin] (beta 1.0 when the list is
+    empty; beta_lin 0 = not configured); gelu takes a placeholder only."""
+    kind = ACTIVATIONS[name]
+    params = [float(v) for v in params]
+    c, alpha, beta, beta_lin = np.inf, 1.702, 1.0, 0.0
+    if kind in (0, 1, 2) and params:
+        c = params[0] if params[0] != 0.0 else np.inf
+        if kind == 2 and len(params) == 3:
+            alpha, beta = params[1], params[2]
+    if kind == 3:
+        beta = params[0] if params else 1.0
+        beta_lin = params[1] if len(params) > 1 else 0.0
+    return kind, np.array([c, alpha, beta, beta_lin], dtype=np.float64)
+
+
+def expert_row(xq, xs, x_fmt, w1, s1, w2, s2, w_fmt, a_fmt, activation="swiglu", act_params=()):
+    """One expanded row through one expert (A8W8-FP / A8W4-FP stages 2-3).
 
     xq uint8[H], xs uint8[H/32]; w1 [2I, H], s1 [2I, 2*ceil(H/64)];
-    w2 [H, I], s2 [H, 2*ceil(I/64)].  Returns (aq uint8[I], as uint8[I/32], o float64[H]).
+    w2 [H, W], s2 [H, 2*ceil(W/64)] with W = I (gated) or 2I (gelu).
+    Returns (aq uint8[W], as uint8[W/32], o float64[H]).
     """
+    kind, p = activation_spec(activation, act_params)
     h = xq.size
-    inter = w2.shape[1]
-    aq = np.zeros(inter, dtype=np.uint8)
-    a_s = np.zeros((inter + 31) // 32, dtype=np.uint8)
+    inter = w1.shape[0] // 2
+    aw = w2.shape[1]
+    aq = np.zeros(aw, dtype=np.uint8)
+    a_s = np.zeros((aw + 31) // 32, dtype=np.uint8)
     o = np.zeros(h, dtype=np.float64)
     arrs = [np.ascontiguousarray(a) for a in (xq, xs, w1, s1, w2, s2)]
     _load().orc_expert_row(_ptr(arrs[0]), _ptr(arrs[1]), x_fmt, _ptr(arrs[2]), _ptr(arrs[3]),
-                           _ptr(arrs[4]), _ptr(arrs[5]), w_fmt, h, inter, a_fmt, _ptr(aq), _ptr(a_s),
-                           _ptr(o))
+                           _ptr(arrs[4]), _ptr(arrs[5]), w_fmt, h, inter, a_fmt, kind, _ptr(p), _ptr(aq),
+                           _ptr(a_s), _ptr(o))
     return aq, a_s, o
 
 
 def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None,
-                    shared=None, shared_w_fmt=None, want_act=False):
-    """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP stages 1-4).
+                    shared=None, shared_w_fmt=None, want_act=False, activation="swiglu", act_params=(),
+                    x_prequant=None):
+    """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP / A8W4-FP
+    stages 1-4).  x_prequant = (codes uint8[N, H], scales uint8[N, ceil(H/32)]):
+    pre-quantised pass-through (dispatchQuantMode = 0): X_hat and S_X are the given
+    ones and x_bf16 is not read.
 
     x_bf16 uint16[N, H]; ids int32[N, K]; gate float32[N, K] or bf16 bits uint16[N, K];
     w1 uint8[E, 2I, H], s1 uint8[E, 2I, 2*ceil(H/64)], w2 uint8[E, H, I],
@@ -194,10 +225,12 @@ def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None
     Returns (y float64[T, H], y_bf16 uint16[T, H]) and, with want_act, the
     activation codes uint8[T, K, I] and scales uint8[T, K, I/32].
     """
-    n, h = x_bf16.shape
+    kind, p = activation_spec(activation, act_params)
+    n, h = x_bf16.shape if x_prequant is None else x_prequant[0].shape
     k = ids.shape[1]
     e, two_i, _ = w1.shape
     inter = two_i // 2
+    aw = two_i if kind == ACTIVATIONS["gelu"] else inter
     tokens = np.arange(n, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
     t = tokens.size
     y = np.zeros((t, h), dtype=np.float64)
@@ -212,13 +245,19 @@ def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None
         sw = [np.ascontiguousarray(a) for a in shared]
         n_sh = sw[0].shape[0]
         shared_w_fmt = w_fmt if shared_w_fmt is None else shared_w_fmt
-    aq = np.zeros((t, k, inter), dtype=np.uint8) if want_act else None
-    a_s = np.zeros((t, k, (inter + 31) // 32), dtype=np.uint8) if want_act else None
-    arrs = [np.ascontiguousarray(a) for a in (x_bf16, ids.astype(np.int32, copy=False), w1, s1, w2, s2)]
+    aq = np.zeros((t, k, aw), dtype=np.uint8) if want_act else None
+    a_s = np.zeros((t, k, (aw + 31) // 32), dtype=np.uint8) if want_act else None
+    xq = xs = None
+    if x_prequant is not None:
+        xq, xs = (np.ascontiguousarray(a, dtype=np.uint8) for a in x_prequant)
+        x_bf16 = None
+    arrs = [None if a is None else np.ascontiguousarray(a)
+            for a in (x_bf16, ids.astype(np.int32, copy=False), w1, s1, w2, s2)]
     _load().orc_mega_moe_tokens(
         _ptr(arrs[0]), _ptr(arrs[1]), _ptr(gate), gate_is_bf16, _ptr(arrs[2]), _ptr(arrs[3]),
         _ptr(arrs[4]), _ptr(arrs[5]), _ptr(sw[0]), _ptr(sw[1]), _ptr(sw[2]), _ptr(sw[3]), n_sh, h, k,
-        e, inter, x_fmt, w_fmt, shared_w_fmt, _ptr(tokens), t, _ptr(y), _ptr(yb), _ptr(aq), _ptr(a_s))
+        e, inter, x_fmt, w_fmt, shared_w_fmt, _ptr(tokens), t, _ptr(y), _ptr(yb), _ptr(aq), _ptr(a_s),
+        _ptr(xq), _ptr(xs), kind, _ptr(p))
     if want_act:
         return y, yb, aq, a_s
     return y, yb
@@ -234,7 +273,7 @@ def quantized_weights(cfg, which: int, shared: bool = False, fmt: int | None = N
     if which == 1:
         n_out, k_red = 2 * cfg.inter, cfg.h
     else:
-        n_out, k_red = cfg.h, cfg.inter
+        n_out, k_red = cfg.h, cfg.act_width
     s_cols = 2 * ((k_red + 63) // 64)
     q = np.empty((n_exp, n_out, k_red), dtype=np.uint8)
     s = np.empty((n_exp, n_out, s_cols), dtype=np.uint8)

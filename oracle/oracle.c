@@ -312,25 +312,74 @@ static void dequant_row(const uint8_t* q, const uint8_t* s, int64_t n, int code,
 }
 
 /* ---------------------------------------------------------------------------
- * One expanded row through one expert (MegaMoE A8W8-FP stages 2-3, gated
- * swiglu with clamp disabled, c = +inf):
+ * Activation (MegaMoE README, "Activation function formulas").
+ * sigma(z) = 1 / (1 + e^-z), SiLU(z) = z sigma(z); clamp c (+inf when not
+ * enabled), G_c = min(G, c), U_c = clip(U, -c, c):
+ *   0 swiglu      A = SiLU(G_c) U_c
+ *   1 swiglustep  A = min(SiLU(G), c) U_c
+ *   2 swigluoai   A = G_c sigma(alpha G_c) (U_c + beta)
+ *   3 situglu     A = beta tanh(G / beta) sigma(G) L(U),
+ *                 L(U) = U, or beta_lin tanh(U / beta_lin) when configured
+ *   4 gelu        A = Z sigma(sqrt(8/pi) (Z + 0.044715 Z^3)), element-wise
+ *                 on the whole Linear1 output Z (no gate / up split)
+ * p = {c, alpha, beta, beta_lin} (beta_lin 0: not configured).
+ * ------------------------------------------------------------------------- */
+#define ORC_SWIGLU 0
+#define ORC_SWIGLUSTEP 1
+#define ORC_SWIGLUOAI 2
+#define ORC_SITUGLU 3
+#define ORC_GELU 4
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+static double act_gated(int kind, double g, double u, const double* p) {
+  double c = p[0];
+  double gc = g < c ? g : c;
+  double uc = u < -c ? -c : (u > c ? c : u);
+  switch (kind) {
+    case ORC_SWIGLUSTEP: {
+      double s = g * sigmoid(g);
+      return (s < c ? s : c) * uc;
+    }
+    case ORC_SWIGLUOAI:
+      return gc * sigmoid(p[1] * gc) * (uc + p[2]);
+    case ORC_SITUGLU: {
+      double l = p[3] > 0.0 ? p[3] * tanh(u / p[3]) : u;
+      return p[2] * tanh(g / p[2]) * sigmoid(g) * l;
+    }
+    default:
+      return gc * sigmoid(gc) * uc;
+  }
+}
+
+static double act_gelu(double z) {
+  return z * sigmoid(sqrt(8.0 / acos(-1.0)) * (z + 0.044715 * z * z * z));
+}
+
+/* Activation output width for a Linear1 output width of 2I. */
+static int64_t act_width(int kind, int64_t inter) { return kind == ORC_GELU ? 2 * inter : inter; }
+
+/* ---------------------------------------------------------------------------
+ * One expanded row through one expert (MegaMoE A8W8-FP / A8W4-FP stages 2-3):
  *   h[n] = sum_c DQ(x)[c] * DQ(W1)[n][c]      n in [0, 2I)   (sequential double sum)
- *   G = h[0:I] (gate, SiLU applied), U = h[I:2I] (up)
- *   A[n] = SiLU(G[n]) * U[n],  SiLU(z) = z / (1 + e^-z),  rounded to fp32
- *   Ahat, S_A = Q_MX(A) in the dispatch format
- *   o[c] = sum_n DQ(Ahat)[n] * DQ(W2)[c][n]   c in [0, H)
+ *   gated: G = h[0:I] (gate), U = h[I:2I] (up), A[n] = Activation(G[n], U[n]);
+ *   gelu:  A[n] = GELU(h[n]) for n in [0, 2I);  A rounded to fp32
+ *   Ahat, S_A = Q_MX(A) in the dispatch format   (width W = I, or 2I for gelu)
+ *   o[c] = sum_n DQ(Ahat)[n] * DQ(W2)[c][n]   c in [0, H), W2 [H, W]
  * Weights are in the storage layout [N_out, K_red] with E8M0 scales
  * [N_out, w_s_cols] (the pages' (., N_out, CeilDiv(K_red, 64), 2) flattened).
  * ------------------------------------------------------------------------- */
 void orc_expert_row(const uint8_t* xq, const uint8_t* xs, int x_code, const uint8_t* w1,
                     const uint8_t* s1, const uint8_t* w2, const uint8_t* s2, int w_code,
-                    int64_t h, int64_t inter, int a_code, uint8_t* aq, uint8_t* as, double* o) {
-  int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((inter + 63) / 64);
+                    int64_t h, int64_t inter, int a_code, int act, const double* act_p, uint8_t* aq,
+                    uint8_t* as, double* o) {
+  int64_t aw = act_width(act, inter);
+  int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((aw + 63) / 64);
   double* xd = (double*)malloc(sizeof(double) * (size_t)h);
-  double* wd = (double*)malloc(sizeof(double) * (size_t)(h > inter ? h : inter));
+  double* wd = (double*)malloc(sizeof(double) * (size_t)(h > aw ? h : aw));
   double* hv = (double*)malloc(sizeof(double) * (size_t)(2 * inter));
-  double* a = (double*)malloc(sizeof(double) * (size_t)inter);
-  double* ad = (double*)malloc(sizeof(double) * (size_t)inter);
+  double* a = (double*)malloc(sizeof(double) * (size_t)aw);
+  double* ad = (double*)malloc(sizeof(double) * (size_t)aw);
   dequant_row(xq, xs, h, x_code, xd);
   for (int64_t n = 0; n < 2 * inter; ++n) {
     dequant_row(w1 + n * h, s1 + n * s1_cols, h, w_code, wd);
@@ -338,16 +387,17 @@ void orc_expert_row(const uint8_t* xq, const uint8_t* xs, int x_code, const uint
     for (int64_t c = 0; c < h; ++c) acc += xd[c] * wd[c];
     hv[n] = acc;
   }
-  for (int64_t n = 0; n < inter; ++n) {
-    double g = hv[n], u = hv[inter + n];
-    a[n] = (double)(float)(g / (1.0 + exp(-g)) * u);
+  if (act == ORC_GELU) {
+    for (int64_t n = 0; n < aw; ++n) a[n] = (double)(float)act_gelu(hv[n]);
+  } else {
+    for (int64_t n = 0; n < inter; ++n) a[n] = (double)(float)act_gated(act, hv[n], hv[inter + n], act_p);
   }
-  orc_mx_quantize_rows(a, 1, inter, a_code, aq, as, (inter + 31) / 32);
-  dequant_row(aq, as, inter, a_code, ad);
+  orc_mx_quantize_rows(a, 1, aw, a_code, aq, as, (aw + 31) / 32);
+  dequant_row(aq, as, aw, a_code, ad);
   for (int64_t c = 0; c < h; ++c) {
-    dequant_row(w2 + c * inter, s2 + c * s2_cols, inter, w_code, wd);
+    dequant_row(w2 + c * aw, s2 + c * s2_cols, aw, w_code, wd);
     double acc = 0.0;
-    for (int64_t n = 0; n < inter; ++n) acc += ad[n] * wd[n];
+    for (int64_t n = 0; n < aw; ++n) acc += ad[n] * wd[n];
     o[c] = acc;
   }
   free(xd); free(wd); free(hv); free(a); free(ad);
@@ -370,36 +420,43 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
                          const uint8_t* ss2, int64_t n_shared, int64_t h, int64_t k,
                          int64_t num_experts, int64_t inter, int x_code, int w_code,
                          int shared_w_code, const int64_t* tokens, int64_t n_tok, double* y,
-                         uint16_t* y_bf16, uint8_t* aq_out, uint8_t* as_out) {
-  int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((inter + 63) / 64);
-  int64_t w1_sz = 2 * inter * h, w2_sz = h * inter;
-  int64_t i_groups = (inter + 31) / 32;
+                         uint16_t* y_bf16, uint8_t* aq_out, uint8_t* as_out, const uint8_t* xq_in,
+                         const uint8_t* xs_in, int act, const double* act_p) {
+  int64_t aw = act_width(act, inter);
+  int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((aw + 63) / 64);
+  int64_t w1_sz = 2 * inter * h, w2_sz = h * aw;
+  int64_t i_groups = (aw + 31) / 32;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t t = 0; t < n_tok; ++t) {
     int64_t i = tokens[t];
     uint8_t* xq = (uint8_t*)malloc((size_t)h);
     uint8_t* xs = (uint8_t*)malloc((size_t)((h + 31) / 32));
-    uint8_t* aq = (uint8_t*)malloc((size_t)inter);
+    uint8_t* aq = (uint8_t*)malloc((size_t)aw);
     uint8_t* as = (uint8_t*)malloc((size_t)i_groups);
     double* o = (double*)malloc(sizeof(double) * (size_t)h);
     double* acc = y + t * h;
     for (int64_t c = 0; c < h; ++c) acc[c] = 0.0;
-    orc_mx_quantize_src(x + i * h, 27, 1, h, x_code, xq, xs, (h + 31) / 32);
+    if (xq_in) { /* pre-quantised pass-through: X_hat and S_X as given */
+      memcpy(xq, xq_in + i * h, (size_t)h);
+      memcpy(xs, xs_in + i * ((h + 31) / 32), (size_t)((h + 31) / 32));
+    } else {
+      orc_mx_quantize_src(x + i * h, 27, 1, h, x_code, xq, xs, (h + 31) / 32);
+    }
     for (int64_t kk = 0; kk < k; ++kk) {
       int32_t e = ids[i * k + kk];
       if (e < 0 || e >= num_experts) continue;
       double w = gate_is_bf16 ? orc_bf16_value(((const uint16_t*)gate)[i * k + kk])
                               : (double)((const float*)gate)[i * k + kk];
       orc_expert_row(xq, xs, x_code, w1 + e * w1_sz, s1 + e * 2 * inter * s1_cols,
-                     w2 + e * w2_sz, s2 + e * h * s2_cols, w_code, h, inter, x_code, aq, as, o);
-      if (aq_out) memcpy(aq_out + (t * k + kk) * inter, aq, (size_t)inter);
+                     w2 + e * w2_sz, s2 + e * h * s2_cols, w_code, h, inter, x_code, act, act_p, aq, as, o);
+      if (aq_out) memcpy(aq_out + (t * k + kk) * aw, aq, (size_t)aw);
       if (as_out) memcpy(as_out + (t * k + kk) * i_groups, as, (size_t)i_groups);
       for (int64_t c = 0; c < h; ++c) acc[c] += w * o[c];
     }
     for (int64_t s = 0; s < n_shared; ++s) {
       orc_expert_row(xq, xs, x_code, sw1 + s * w1_sz, ss1 + s * 2 * inter * s1_cols,
-                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, x_code, aq,
-                     as, o);
+                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, x_code, act, act_p,
+                     aq, as, o);
       for (int64_t c = 0; c < h; ++c) acc[c] += o[c];
     }
     for (int64_t c = 0; c < h; ++c) y_bf16[t * h + c] = orc_bf16_round(acc[c]);

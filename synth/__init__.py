@@ -117,10 +117,17 @@ class MoeConfig:
     shared: int = 0            # shared experts
     seed: int = 0
     zipf_s: float = 1.0
+    activation: str = "swiglu"  # MegaMoE activation; "gelu" keeps the whole 2I-wide Linear1 output
+    act_params: tuple = ()
 
     @property
     def rows(self) -> int:
         return self.n * self.k
+
+    @property
+    def act_width(self) -> int:
+        """Width of the activation output = reduction length of weight2."""
+        return 2 * self.inter if self.activation == "gelu" else self.inter
 
     def scaled(self, **kw) -> "MoeConfig":
         d = dict(self.__dict__)
@@ -175,10 +182,10 @@ def weight_f32(cfg: MoeConfig, which: int, expert: int, shared: bool = False) ->
     """fp32 N(0, 0.02) source weights of one expert, storage layout [N_out, K_red].
 
     which = 1: weight1, [2I, H] (rows [0, I) gate, [I, 2I) up);
-    which = 2: weight2, [H, I].
+    which = 2: weight2, [H, I] ([H, 2I] under gelu).
     """
     if which == 1:
         shape, stream = (2 * cfg.inter, cfg.h), (S_SW1 if shared else S_W1)
     else:
-        shape, stream = (cfg.h, cfg.inter), (S_SW2 if shared else S_W2)
+        shape, stream = (cfg.h, cfg.act_width), (S_SW2 if shared else S_W2)
     return normal_f32(cfg.seed, stream | expert, shape, scale=0.02)

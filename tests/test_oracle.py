@@ -367,3 +367,104 @@ def test_swiglu_special_values():
     deq = P.fp8_table(P.E4M3)[aq[0]] * 2.0 ** (int(a_s[0]) - 127)
     assert abs(deq - a0) <= a0 * 2 ** -3
     assert np.allclose(o, deq)
+
+
+# ------------------------------------------------- activations, pass-through
+def _one_expert(cfg):
+    """Quantised x row of token 0 and expert 0's quantised weights."""
+    x = synth.tokens_bf16(cfg)
+    xq, xs = oracle.mx_quantize(x[:1], oracle.DT_BF16, cfg.dispatch_fmt)
+    w1, s1 = oracle.quantized_weights(cfg, 1)
+    w2, s2 = oracle.quantized_weights(cfg, 2)
+    return xq[0], xs[0], w1[0], s1[0], w2[0], s2[0]
+
+
+def _row(cfg, act, params=()):
+    xq, xs, w1, s1, w2, s2 = _one_expert(cfg)
+    return oracle.expert_row(xq, xs, cfg.dispatch_fmt, w1, s1, w2, s2, cfg.weight_fmt, cfg.dispatch_fmt,
+                             activation=act, act_params=params)
+
+
+def test_activation_special_cases_reduce_to_swiglu():
+    """MegaMoE "Activation function formulas": with the clamp disabled
+    (absent, 0 or FLT_MAX) every gated form below is SwiGLU exactly or in
+    the limit: swiglustep with c = inf; swigluoai with alpha = 1, beta = 0;
+    situglu with beta -> inf (beta tanh(G/beta) -> G) and linear_beta -> inf."""
+    cfg = synth.CONFIGS["tiny"]
+    aq0, as0, o0 = _row(cfg, "swiglu")
+    for act, params in (("swiglu", (0.0,)), ("swiglu", (np.finfo(np.float32).max,)), ("swiglustep", ()),
+                        ("swigluoai", (0.0, 1.0, 0.0))):
+        aq, a_s, o = _row(cfg, act, params)
+        assert np.array_equal(aq, aq0) and np.array_equal(a_s, as0), act
+        assert np.array_equal(o, o0), act
+    aq, a_s, o = _row(cfg, "situglu", (1e7, 1e7))
+    assert np.array_equal(a_s, as0)
+    assert np.abs(_code_steps(aq, aq0, cfg.dispatch_fmt)).max() <= 1
+    assert np.abs(o - o0).max() <= 1e-3 * np.abs(o0).max()
+
+
+def _code_steps(a, b, fmt):
+    """Signed code distance of two FP8 code arrays (codes ordered by value)."""
+    def ordv(c):
+        c = c.astype(np.int64)
+        return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+    return ordv(a) - ordv(b)
+
+
+def test_activation_clamp_cases():
+    """Clamp c: G_c = min(G, c), U_c = clip(U, -c, c).  For a c below every |G|
+    and |U| the gated products reduce to constants times the signs of U:
+    swiglu A = SiLU(c) * c * sign(U) where G > c; swiglustep A = min(SiLU(G), c)
+    U_c; a clamp far above the data changes nothing."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=1)
+    aq0, _, o0 = _row(cfg, "swiglu")
+    aq1, _, o1 = _row(cfg, "swiglu", (1e30,))
+    assert np.array_equal(aq0, aq1) and np.array_equal(o0, o1)
+    # pin through the A8W8 formulas written with a tiny clamp: A = SiLU(min(G, c)) clip(U)
+    c = 1e-3
+    xq, xs, w1, s1, w2, s2 = _one_expert(cfg)
+    xd = P.dequant_rows(xq[None], xs[None], cfg.dispatch_fmt)[0]
+    hv = P.dequant_rows(w1, s1, cfg.weight_fmt) @ xd
+    g, u = hv[:cfg.inter], hv[cfg.inter:]
+    assert np.mean(np.abs(u) > c) > 0.9             # nearly every U clips to +-c
+    gc = np.minimum(g, c)
+    want = (gc * expit(gc) * np.clip(u, -c, c)).astype(np.float32).astype(np.float64)
+    wq, ws = P.brute_mx_rows(want[None], cfg.dispatch_fmt)
+    aq, a_s, _ = _row(cfg, "swiglu", (c,))
+    assert np.array_equal(aq, wq[0]) and np.array_equal(a_s, ws[0])
+
+
+def test_gelu_matches_tanh_form():
+    """gelu: the README prints GELU(Z) = Z/2 (1 + tanh(sqrt(2/pi) (Z + 0.044715 Z^3)))
+    = Z sigma(sqrt(8/pi) (...)).  The oracle evaluates the sigma form; the tanh
+    form (numpy) must give the same quantised activation of the full 2I-wide
+    Linear1 output, and GELU_tanh(1) = 0.84119199 (the approximation's value)."""
+    cfg = synth.CONFIGS["tiny"].scaled(activation="gelu", act_params=(float(np.finfo(np.float32).max),))
+    xq, xs, w1, s1, w2, s2 = _one_expert(cfg)
+    assert w2.shape[1] == 2 * cfg.inter
+    xd = P.dequant_rows(xq[None], xs[None], cfg.dispatch_fmt)[0]
+    z = P.dequant_rows(w1, s1, cfg.weight_fmt) @ xd
+    tanh_form = 0.5 * z * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (z + 0.044715 * z ** 3)))
+    want = tanh_form.astype(np.float32).astype(np.float64)
+    wq, ws = P.brute_mx_rows(want[None], cfg.dispatch_fmt)
+    aq, a_s, o = oracle.expert_row(xq, xs, cfg.dispatch_fmt, w1, s1, w2, s2, cfg.weight_fmt, cfg.dispatch_fmt,
+                                   activation="gelu", act_params=cfg.act_params)
+    assert np.array_equal(a_s, ws[0])
+    assert np.abs(_code_steps(aq, wq[0], cfg.dispatch_fmt)).max() <= 1
+    assert abs(0.5 * (1 + np.tanh(np.sqrt(2 / np.pi) * 1.044715)) - 0.8411919906) < 1e-9
+
+
+def test_prequant_passthrough_equals_internal_quantisation():
+    """dispatchQuantMode = 0: X_hat, S_X given by the caller.  Passing the
+    oracle's own Q_MX(x) must reproduce the internal-quantisation result."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=1)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    w = _weights(cfg)
+    sh = _weights(cfg, shared=True)
+    y0, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh)
+    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, cfg.dispatch_fmt)
+    y1, _ = oracle.mega_moe_tokens(None, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
+                                   x_prequant=(xq, xs))
+    assert np.array_equal(y0, y1)
