@@ -176,7 +176,11 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *   O_e = DQ(A_hat_e) DQ(W2_e)^T                                  stage 3
  *   Y[i] = sum_k W[i,k] O[pi(i,k)] + sum_s O_s^shared[i]          stage 4
  *
- * x                  [bs, h] bf16.
+ * x                  [bs, h] bf16 (dispatch_quant_mode 4), or FP8 codes of
+ *                    dispatch_quant_out_dtype (dispatch_quant_mode 0).
+ * x_scales           dispatch_quant_mode 0: E8M0 scales of x, [bs, h/32]
+ *                    (the pages' scales input, (BS, CeilDiv(H, 32))); NULL
+ *                    otherwise.
  * topk_ids           [bs, k] int32, distinct per token, in [0, moe_expert_num).
  * topk_weights       [bs, k], topk_weights_dtype MM_DT_FLOAT32 or MM_DT_BFLOAT16.
  * weight1            [E, 2*intermediate, h] FP8 (weight_dtype 23 / 24), or
@@ -191,25 +195,38 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    (0..4; NULL when 0); shared_weight_dtype 23 / 24 / 296.
  * ep_world_size      must be 1.
  * max_recv_token_num 0, or >= bs*k (the rows this rank receives at ep = 1).
- * dispatch_quant_mode must be 4 (MX quantisation inside the operator);
+ * dispatch_quant_mode 4 (MX quantisation inside the operator) or 0
+ *                    (pre-quantised pass-through: x and x_scales are X_hat, S_X);
  * dispatch_quant_out_dtype 23 / 24 is also the type of A_hat (FP8 with either
  *                    weight type: A8W8-FP, A8W4-FP).
- * combine_quant_mode must be 0; activation must be "swiglu" (or NULL) with
- *                    no parameters (clamp disabled).
+ * combine_quant_mode must be 0.
+ * activation         "swiglu" (or NULL), "swiglustep", "swigluoai", "situglu" or
+ *                    "gelu", with activation_params as the README's parameter
+ *                    table gives them: swiglu / swiglustep [] or [clamp];
+ *                    swigluoai [] or [clamp, alpha, beta] (defaults: clamp off,
+ *                    alpha 1.702, beta 1.0); situglu [], [beta] or [beta,
+ *                    linear_beta] (beta 1.0 when empty); gelu [FLT_MAX] only.
+ *                    A clamp of 0 or FLT_MAX is "not enabled".  Formulas:
+ *                    "Activation function formulas".  Under gelu the whole
+ *                    2*intermediate-wide Linear1 output is activated, so
+ *                    weight2 is [E, h, 2*intermediate] (scales likewise) and
+ *                    A_hat has 2*intermediate columns.  Bad parameter lists
+ *                    give MM_ERR_INVALID_ARG, other names MM_ERR_UNSUPPORTED.
  * y                  [bs, h] bf16 output.
  * expert_token_nums  [E] int32 output (rows per expert), or NULL.
  * expanded_row_idx   [bs*k] int32 output pi(i, k) (position of row j = i*k+k'
  *                    in expert-sorted order), or NULL.
  * act_q, act_scale   optional diagnostic outputs of A_hat in expert-sorted
- *                    row order: [bs*k, I] FP8 and [bs*k, I/32] E8M0; NULL to skip.
+ *                    row order: [bs*k, W] FP8 and [bs*k, W/32] E8M0 with W = I
+ *                    (2I under gelu); NULL to skip.
  * Shape limits: h and intermediate multiples of 128; k <= 32;
  * moe_expert_num <= 2048.
  * ---------------------------------------------------------------------- */
 mm_status mm_mega_moe_workspace_size(int64_t bs, int64_t h, int64_t k, int64_t moe_expert_num,
                                      int64_t intermediate, int64_t shared_expert_num,
                                      int weight_scale_layout, size_t* bytes);
-mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_weights,
-                      int topk_weights_dtype, const uint8_t* weight1, const uint8_t* weight2,
+mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* topk_ids,
+                      const void* topk_weights, int topk_weights_dtype, const uint8_t* weight1, const uint8_t* weight2,
                       const uint8_t* weight_scales1, const uint8_t* weight_scales2,
                       int weight_dtype, int weight_scale_layout, const uint8_t* shared_weight1,
                       const uint8_t* shared_weight2, const uint8_t* shared_weight_scales1,

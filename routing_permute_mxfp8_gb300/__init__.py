@@ -63,7 +63,7 @@ def load():
     L.mm_moe_token_permute_workspace_size.argtypes = [i64, i64, psz]
     L.mm_moe_token_permute.argtypes = [p, i32, p, i32, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, sz, p, p]
     L.mm_mega_moe_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, psz]
-    L.mm_mega_moe.argtypes = ([p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
+    L.mm_mega_moe.argtypes = ([p, p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
                                i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, sz, p, p])
     L.mm_prepared_weight_scales_size.argtypes = [i32, i64, i64, i64, psz]
     L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
@@ -204,23 +204,28 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 shared_weight_dtype: int | None = None, ep_world_size: int = 1, max_recv_token_num: int = 0,
                 dispatch_quant_mode: int = 4, dispatch_quant_out_dtype: int = DT_FP8_E4M3FN,
                 combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
-                out=None, workspace=None, dev_err=None, want_expanded_row_idx=False, want_act=False):
+                x_scales=None, out=None, workspace=None, dev_err=None, want_expanded_row_idx=False,
+                want_act=False):
     """MegaMoE forward, A8W8-FP or A8W4-FP, ep_world_size = 1.
 
     x [BS, H] bf16; topk_ids [BS, K] int32; topk_weights [BS, K] fp32 / bf16;
     weight1 [E, 2I, H] and weight2 [E, H, I] FP8 (torch float8 or uint8 with
     weight_dtype), or with weight_dtype=DT_FP4_E2M1 packed FP4 bytes
     [E, 2I, H/2] and [E, H, I/2]; weight_scales1 / 2 uint8 E8M0 in the pages' layout
-    (weight_scale_layout=0) or prepared by mm_prepare_weight_scales (1).
+    (weight_scale_layout=0) or prepared by mm_prepare_weight_scales (1).  Under
+    activation="gelu", weight2 is [E, H, 2I] and A_hat 2I wide.
     Returns (y [BS, H] bf16, expert_token_nums [E] int32) and, on request,
     expanded_row_idx [BS*K] int32 and A_hat codes / scales in sorted order.
+    With dispatch_quant_mode=0, x holds FP8 codes (uint8 [BS, H]) and x_scales their
+    E8M0 scales [BS, H/32] (pre-quantised pass-through).
     """
     _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
     L = load()
     bs, h = x.shape
     k = topk_ids.shape[1]
     wdt = _fp8_code(weight1, weight_dtype)
-    inter = weight2.shape[2] * (2 if wdt == DT_FP4_E2M1 else 1)
+    inter = weight1.shape[1] // 2
+    aw = 2 * inter if activation == "gelu" else inter   # width of A_hat
     s_num = 0 if shared_weight1 is None else shared_weight1.shape[0]
     dev = x.device
     swdt = wdt if shared_weight1 is None else _fp8_code(shared_weight1, wdt if shared_weight_dtype is None
@@ -228,15 +233,15 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     y = out if out is not None else torch.empty((bs, h), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(moe_expert_num, dtype=torch.int32, device=dev)
     exp_idx = torch.empty(bs * k, dtype=torch.int32, device=dev) if want_expanded_row_idx else None
-    act_q = torch.empty((bs * k, inter), dtype=torch.uint8, device=dev) if want_act else None
-    act_s = torch.empty((bs * k, inter // 32), dtype=torch.uint8, device=dev) if want_act else None
+    act_q = torch.empty((bs * k, aw), dtype=torch.uint8, device=dev) if want_act else None
+    act_s = torch.empty((bs * k, aw // 32), dtype=torch.uint8, device=dev) if want_act else None
     need = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, inter, s_num, weight_scale_layout)
     ws = _workspace(need, dev, workspace)
     params = list(activation_params)
     parr = (ctypes.c_float * max(len(params), 1))(*params) if params else None
     gdt = _dt(topk_weights)
     _check(L.mm_mega_moe(
-        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), gdt, _ptr(weight1), _ptr(weight2), _ptr(weight_scales1),
+        _ptr(x), _ptr(x_scales), _ptr(topk_ids), _ptr(topk_weights), gdt, _ptr(weight1), _ptr(weight2), _ptr(weight_scales1),
         _ptr(weight_scales2), wdt, weight_scale_layout, _ptr(shared_weight1), _ptr(shared_weight2),
         _ptr(shared_weight_scales1), _ptr(shared_weight_scales2), swdt, s_num, bs, h, k, moe_expert_num,
         ep_world_size, inter, max_recv_token_num, dispatch_quant_mode, dispatch_quant_out_dtype,

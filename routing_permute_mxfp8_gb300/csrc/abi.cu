@@ -59,6 +59,7 @@ RoutingWs carve_routing(Carver& c, const RoutePlan& p) {
 // ---- mm_mega_moe ----
 struct MegaDims {
   int64_t bs, h, k, e, inter, s, rows, rows_cap;
+  int64_t aw_max;  // widest A_hat: 2I (gelu keeps the whole Linear1 output)
 };
 
 struct MegaWs {
@@ -77,6 +78,7 @@ MegaDims mega_dims(int64_t bs, int64_t h, int64_t k, int64_t e, int64_t inter, i
   d.inter = inter;
   d.s = s;
   d.rows = bs * k;
+  d.aw_max = 2 * inter;
   // each segment pads to whole 128-row tiles
   d.rows_cap = kBM * (ceil_div(d.rows, kBM) + e) + s * round_up(bs, kBM);
   return d;
@@ -93,17 +95,17 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   w.pad_row = c.take<int32_t>(d.rows);
   w.xq = c.take<uint8_t>(d.rows_cap * d.h);
   w.xsf = c.take<uint8_t>(d.rows_cap / kBM * (d.h / 128) * kSfChunk);
-  w.aq = c.take<uint8_t>(d.rows_cap * d.inter);
-  w.asf = c.take<uint8_t>(d.rows_cap / kBM * (d.inter / 128) * kSfChunk);
+  w.aq = c.take<uint8_t>(d.rows_cap * d.aw_max);
+  w.asf = c.take<uint8_t>(d.rows_cap / kBM * (d.aw_max / 128) * kSfChunk);
   w.o = c.take<__nv_bfloat16>(d.rows_cap * d.h);
   w.wsf1 = w.wsf2 = w.swsf1 = w.swsf2 = nullptr;
   if (wscale_layout == MM_WSCALE_ROWS) {
     const int64_t bn2 = gemm_tile_n(2, d.h);
     w.wsf1 = c.take<uint8_t>(d.e * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
-    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h, bn2) * (d.inter / 128) * kSfChunk);
+    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h, bn2) * (d.aw_max / 128) * kSfChunk);
     if (d.s > 0) {
       w.swsf1 = c.take<uint8_t>(d.s * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
-      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h, bn2) * (d.inter / 128) * kSfChunk);
+      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h, bn2) * (d.aw_max / 128) * kSfChunk);
     }
   }
   return w;
@@ -179,12 +181,54 @@ struct StageScope {
   }
 };
 
-bool activation_is_plain_swiglu(const char* act, const float* params, int64_t n) {
-  if (act && strcmp(act, "swiglu") != 0) return false;
-  if (n == 0) return true;
-  if (n != 1 || !params) return false;
-  const float c = params[0];  // clamp 0 or the float maximum disables clamping
-  return c == 0.0f || c >= FLT_MAX;
+// The activation and its activation_params (MegaMoE parameter table,
+// "activation_params"): swiglu / swiglustep [] or [clamp]; swigluoai [] or
+// [clamp, alpha, beta] (alpha 1.702, beta 1.0 by default); situglu [],
+// [beta] or [beta, linear_beta] (beta 1.0 by default); gelu exactly [FLT_MAX]
+// (a placeholder).  A clamp of 0 or the float maximum disables clamping;
+// a clamp must be >= 0 and not NaN, alpha and beta finite, the situglu
+// betas finite and > 0.
+struct ActSpec {
+  int kind = MM_ACT_SWIGLU;
+  float c = INFINITY, alpha = 1.702f, beta = 1.0f, beta_lin = 0.0f;
+};
+
+mm_status parse_activation(const char* act, const float* p, int64_t n, ActSpec* out) {
+  ActSpec a;
+  if (n < 0 || (n > 0 && !p)) return MM_ERR_INVALID_ARG;
+  const char* name = act ? act : "swiglu";
+  auto clamp_of = [](float c, float* dst) {
+    if (!(c >= 0.0f)) return false;  // negative or NaN
+    *dst = (c == 0.0f || c >= FLT_MAX) ? INFINITY : c;
+    return true;
+  };
+  if (strcmp(name, "swiglu") == 0 || strcmp(name, "swiglustep") == 0) {
+    a.kind = name[6] == 0 ? MM_ACT_SWIGLU : MM_ACT_SWIGLUSTEP;
+    if (n > 1) return MM_ERR_INVALID_ARG;
+    if (n == 1 && !clamp_of(p[0], &a.c)) return MM_ERR_INVALID_ARG;
+  } else if (strcmp(name, "swigluoai") == 0) {
+    a.kind = MM_ACT_SWIGLUOAI;
+    if (n != 0 && n != 3) return MM_ERR_INVALID_ARG;
+    if (n == 3) {
+      if (!clamp_of(p[0], &a.c) || !isfinite(p[1]) || !isfinite(p[2])) return MM_ERR_INVALID_ARG;
+      a.alpha = p[1];
+      a.beta = p[2];
+    }
+  } else if (strcmp(name, "situglu") == 0) {
+    a.kind = MM_ACT_SITUGLU;
+    if (n > 2) return MM_ERR_INVALID_ARG;
+    if (n >= 1) a.beta = p[0];
+    if (n == 2) a.beta_lin = p[1];
+    if (!(isfinite(a.beta) && a.beta > 0.0f)) return MM_ERR_INVALID_ARG;
+    if (n == 2 && !(isfinite(a.beta_lin) && a.beta_lin > 0.0f)) return MM_ERR_INVALID_ARG;
+  } else if (strcmp(name, "gelu") == 0) {
+    a.kind = MM_ACT_GELU;
+    if (n != 1 || p[0] != FLT_MAX) return MM_ERR_INVALID_ARG;
+  } else {
+    return MM_ERR_UNSUPPORTED;
+  }
+  *out = a;
+  return MM_OK;
 }
 
 }  // namespace
@@ -383,7 +427,8 @@ mm_status mm_mega_moe_workspace_size(int64_t bs, int64_t h, int64_t k, int64_t m
   return MM_OK;
 }
 
-mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_weights, int topk_weights_dtype,
+mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* topk_ids, const void* topk_weights,
+                      int topk_weights_dtype,
                       const uint8_t* weight1, const uint8_t* weight2, const uint8_t* weight_scales1,
                       const uint8_t* weight_scales2, int weight_dtype, int weight_scale_layout,
                       const uint8_t* shared_weight1, const uint8_t* shared_weight2,
@@ -401,10 +446,16 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   if (s != MM_OK) return s;
   if (ep_world_size != 1) return MM_ERR_UNSUPPORTED;
   if (combine_quant_mode != 0) return MM_ERR_UNSUPPORTED;
-  if (dispatch_quant_mode != 4) return MM_ERR_UNSUPPORTED;
+  // 4: MX quantisation inside the operator; 0: pre-quantised pass-through
+  // (x holds FP8 codes of dispatch_quant_out_dtype, x_scales its E8M0 scales)
+  if (dispatch_quant_mode != 4 && dispatch_quant_mode != 0) return MM_ERR_UNSUPPORTED;
   if (!is_fp8(dispatch_quant_out_dtype) || !is_mx_weight(weight_dtype)) return MM_ERR_UNSUPPORTED;
   if (shared_expert_num > 0 && !is_mx_weight(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
-  if (!activation_is_plain_swiglu(activation, activation_params, n_activation_params)) return MM_ERR_UNSUPPORTED;
+  if ((dispatch_quant_mode == 0) != (x_scales != nullptr)) return MM_ERR_INVALID_ARG;
+  ActSpec act;
+  s = parse_activation(activation, activation_params, n_activation_params, &act);
+  if (s != MM_OK) return s;
+  const int64_t aw = act.kind == MM_ACT_GELU ? 2 * intermediate : intermediate;
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
   const int64_t rows = bs * k;
   if (max_recv_token_num != 0 && max_recv_token_num < rows) return MM_ERR_INVALID_ARG;
@@ -437,11 +488,11 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
     StageScope sw(MM_STAGE_WSCALE, st);
     const int64_t bn2 = gemm_tile_n(2, d.h);
     e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, 256, w.wsf1, st);
-    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, d.inter, bn2, w.wsf2, st);
+    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, aw, bn2, w.wsf2, st);
     if (e == cudaSuccess && d.s > 0)
       e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, 256, w.swsf1, st);
     if (e == cudaSuccess && d.s > 0)
-      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, d.inter, bn2, w.swsf2, st);
+      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, aw, bn2, w.swsf2, st);
     sw.finish(d.s > 0 ? 4 : 2);
     if (e != cudaSuccess) return MM_ERR_CUDA;
     wsf1 = w.wsf1;
@@ -468,7 +519,8 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   //    (and once per shared expert) in the padded grouped layout
   PermuteArgs pa = {};
   pa.src = x;
-  pa.src_dtype = MM_DT_BFLOAT16;
+  pa.src_dtype = dispatch_quant_mode == 0 ? (int)dispatch_quant_out_dtype : MM_DT_BFLOAT16;
+  pa.src_scales = x_scales;
   pa.n = d.bs;
   pa.h = d.h;
   pa.k = (int)d.k;
@@ -507,6 +559,11 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   g1.b_fmt = weight_dtype;
   g1.b_fmt_sh = shared_weight_dtype;
   g1.inter = (int)d.inter;
+  g1.act = act.kind;
+  g1.act_c = act.c;
+  g1.act_alpha = act.alpha;
+  g1.act_beta = act.beta;
+  g1.act_beta_lin = act.beta_lin;
   g1.act_q = w.aq;
   g1.act_sf = w.asf;
   g1.dev_err = dev_err;
@@ -524,7 +581,7 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
   g2.sfb = wsf2;
   g2.b_sh = shared_weight2;
   g2.sfb_sh = swsf2;
-  g2.K = d.inter;
+  g2.K = aw;
   g2.N = d.h;
   g2.act_q = nullptr;
   g2.act_sf = nullptr;
@@ -560,7 +617,7 @@ mm_status mm_mega_moe(const void* x, const int32_t* topk_ids, const void* topk_w
     ua.pad_row = w.pad_row;
     ua.expanded_row_idx = o.expanded_row_idx;
     ua.rows = d.rows;
-    ua.cols = d.inter;
+    ua.cols = aw;
     ua.dst_q = act_q;
     ua.dst_sf = act_scale;
     StageScope su(MM_STAGE_DIAG, st);

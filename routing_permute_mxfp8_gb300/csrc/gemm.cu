@@ -91,6 +91,10 @@ struct GemmArgs {
   int32_t* dev_err;
   int o_stage;    // stage output blocks (A_hat / O) in shared memory for TMA stores
   int b_fp4, b_fp4_sh;  // routed / shared weights are packed FP4 E2M1
+  // mode 1: activation (MM_ACT_*), its parameters, and the width of A_hat
+  int act;
+  float act_c, act_alpha, act_beta, act_rbeta, act_beta_lin, act_rbeta_lin, act_gelu_k;
+  int aw;
 };
 
 struct TileInfo {
@@ -126,6 +130,59 @@ __device__ __forceinline__ TileInfo decode_merged(int t, const int32_t* bpre, co
   const int cb = (int)((int64_t)t * tb / tt);
   const int cb1 = (int)((int64_t)(t + 1) * tb / tt);
   return cb1 > cb ? decode_tile(cb, bpre, nseg, n_tiles) : decode_tile(t - cb, spre, nseg, n_tiles);
+}
+
+// The MegaMoE activations ("Activation function formulas") on one 32-column
+// chunk: sigma(z) = 1 / (1 + e^-z); clamp c (+inf when disabled), G_c =
+// min(G, c), U_c = clip(U, -c, c).
+//   swiglu      SiLU(G_c) U_c              swiglustep  min(SiLU(G), c) U_c
+//   swigluoai   G_c sigma(alpha G_c) (U_c + beta)
+//   situglu     beta tanh(G / beta) sigma(G) L(U), L(U) = U or beta_lin tanh(U / beta_lin)
+//   gelu        Z sigma(sqrt(8/pi) (Z + 0.044715 Z^3)), element-wise (gv = Z)
+__device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void act_chunk(const GemmArgs& g, const uint32_t* gv, const uint32_t* uv, bool gelu,
+                                          float* a) {
+  const float c = g.act_c;
+  if (gelu) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float z = __uint_as_float(gv[j]);
+      a[j] = z * sigmoid_f(g.act_gelu_k * (z + 0.044715f * z * z * z));
+    }
+    return;
+  }
+  switch (g.act) {
+    case MM_ACT_SWIGLUSTEP:
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float gf = __uint_as_float(gv[j]), uf = __uint_as_float(uv[j]);
+        a[j] = fminf(gf * sigmoid_f(gf), c) * fminf(fmaxf(uf, -c), c);
+      }
+      break;
+    case MM_ACT_SWIGLUOAI:
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float gc = fminf(__uint_as_float(gv[j]), c), uf = __uint_as_float(uv[j]);
+        a[j] = gc * sigmoid_f(g.act_alpha * gc) * (fminf(fmaxf(uf, -c), c) + g.act_beta);
+      }
+      break;
+    case MM_ACT_SITUGLU:
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float gf = __uint_as_float(gv[j]), uf = __uint_as_float(uv[j]);
+        const float l = g.act_beta_lin > 0.f ? g.act_beta_lin * tanhf(uf * g.act_rbeta_lin) : uf;
+        a[j] = g.act_beta * tanhf(gf * g.act_rbeta) * sigmoid_f(gf) * l;
+      }
+      break;
+    default:  // swiglu
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float gc = fminf(__uint_as_float(gv[j]), c), uf = __uint_as_float(uv[j]);
+        // SiLU(G_c) U_c = G_c * (1 / (1 + e^-G_c)) * U_c
+        a[j] = gc * sigmoid_f(gc) * fminf(fmaxf(uf, -c), c);
+      }
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
@@ -241,11 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sfb = (sh ? g.sfb_sh : g.sfb) + (int64_t)e * g.nb * kblocks * 512;
         const int am = mpre[ti.seg] + ti.mt;
         int nb0, nb1, bn0, bn1;
-        if (kMode == 1) {
-          nb0 = ti.nt;
+        if (kMode == 1 && g.act != MM_ACT_GELU) {
+          nb0 = ti.nt;  // gate rows nt*128.., up rows I + nt*128..
           nb1 = g.inter / 128 + ti.nt;
           bn0 = ti.nt * 128;
           bn1 = g.inter + ti.nt * 128;
+        } else if (kMode == 1) {
+          nb0 = 2 * ti.nt;  // gelu: 256 consecutive rows of W1
+          nb1 = 2 * ti.nt + 1;
+          bn0 = ti.nt * 256;
+          bn1 = bn0 + 128;
         } else {
           nb0 = 2 * ti.nt;
           nb1 = 2 * ti.nt + 1;
@@ -346,39 +408,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = r < g.seg_rows[ti.seg] - ti.mt * kBM;
       const int64_t grow = (int64_t)(mpre[ti.seg] + ti.mt) * kBM + r;
       if (kMode == 1) {
-        // output columns [nt*128 + 64*half, +64): gate in accumulator
-        // columns c*32, up in 128 + c*32, for the chunks c = 2*half, 2*half+1
-        uint32_t gv[2][32], uv[2][32];
+        // gated activations: output columns [nt*128 + 64*half, +64) from the
+        //   gate accumulator columns c*32 and the up columns 128 + c*32 for
+        //   the chunks c = 2*half, 2*half+1 (v[0..1] gate, v[2..3] up);
+        // gelu: output columns [nt*256 + 128*half, +128) from the accumulator
+        //   chunks 4*half .. 4*half+3 (v[0..3]), element-wise
+        const bool gelu = g.act == MM_ACT_GELU;
+        uint32_t v[4][32];
+        if (gelu) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 2 * half + i;
-          tmem_ld_32x32b_x32(trow + c * 32, gv[i]);
-          tmem_ld_32x32b_x32(trow + 128 + c * 32, uv[i]);
+          for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(trow + (4 * half + i) * 32, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 2 * half + i;
+            tmem_ld_32x32b_x32(trow + c * 32, v[i]);
+            tmem_ld_32x32b_x32(trow + 128 + c * 32, v[2 + i]);
+          }
         }
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
-        // TMA store of the warp's 32 x 64 FP8 block when all its rows are real
+        const int nout = gelu ? 4 : 2;  // 32-column output chunks of this thread
+        const int ocol0 = gelu ? ti.nt * 256 + 128 * half : ti.nt * 128 + 64 * half;
+        // TMA stores of the warp's 32 x 64 FP8 blocks when all its rows are real
         const bool staged = g.o_stage && g.seg_rows[ti.seg] - ti.mt * kBM >= (q + 1) * 32;
         uint8_t* stg = smO + (warp - 2) * kOStageBytes;
-        if (staged) {
-          if (lane == 0) bulk_wait_read();  // the previous block has left the buffer
-          __syncwarp();
-        }
         uint32_t sfw = 0;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 2 * half + i;
+        for (int i = 0; i < 4; ++i) {
+          if (i >= nout) break;
+          if (staged && (i & 1) == 0) {
+            if (lane == 0) bulk_wait_read();  // the previous block has left the buffer
+            __syncwarp();
+          }
           float a[32];
+          act_chunk(g, v[i], v[(2 + i) & 3], gelu, a);  // up chunk unused under gelu
           float amax = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float gf = __uint_as_float(gv[i][j]);
-            const float uf = __uint_as_float(uv[i][j]);
-            // SiLU(g) * u = g * (1 / (1 + e^-g)) * u
-            a[j] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
-            amax = fmaxf(amax, fabsf(a[j]));
-          }
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(a[j]));
           float inv;
           const uint32_t code = mx_scale(amax, fmt_emax<kActFmt>(), inv);
           sfw |= code << (8 * i);
@@ -388,26 +456,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 lo = make_uint4(p0.x, p0.y, p1.x, p1.y), hi = make_uint4(p2.x, p2.y, p3.x, p3.y);
             if (staged) {
               const int sw = (lane >> 1) & 3;  // 64B swizzle of row `lane`
-              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * i) ^ sw) << 4)) = lo;
-              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * i + 1) ^ sw) << 4)) = hi;
+              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * (i & 1)) ^ sw) << 4)) = lo;
+              *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * (i & 1) + 1) ^ sw) << 4)) = hi;
             } else {
-              uint8_t* dst = g.act_q + grow * g.inter + ti.nt * 128 + c * 32;
+              uint8_t* dst = g.act_q + grow * g.aw + ocol0 + i * 32;
               *reinterpret_cast<uint4*>(dst) = lo;
               *reinterpret_cast<uint4*>(dst + 16) = hi;
             }
           }
-        }
-        if (staged) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmO, stg, ti.nt * 128 + 64 * half, (int)((grow - r) + q * 32));
-            bulk_commit();
+          if (staged && (i & 1) == 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, stg, ocol0 + (i - 1) * 32, (int)((grow - r) + q * 32));
+              bulk_commit();
+            }
           }
         }
-        if (valid)
-          *reinterpret_cast<uint16_t*>(g.act_sf + sf_tile_offset(grow, ti.nt * 4 + 2 * half, g.inter / 128)) =
-              (uint16_t)sfw;
+        if (valid) {
+          uint8_t* sfp = g.act_sf + sf_tile_offset(grow, ocol0 / 32, g.aw / 128);
+          if (gelu)
+            *reinterpret_cast<uint32_t*>(sfp) = sfw;
+          else
+            *reinterpret_cast<uint16_t*>(sfp) = (uint16_t)sfw;
+        }
       } else {
         // output columns [nt*kBN + 128*half, +128) (the last chunks of a
         // tile narrower than 256 columns: half 1 has fewer)
@@ -583,7 +655,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   if (L.mode == 2) {
     if (!map_out(&mo, L.out, true, (uint64_t)L.N, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
   } else {
-    if (!map_out(&mo, L.act_q, false, (uint64_t)L.inter, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
+    const int64_t aw = L.act == MM_ACT_GELU ? 2 * L.inter : L.inter;
+    if (!map_out(&mo, L.act_q, false, (uint64_t)aw, (uint64_t)L.rows_cap)) return cudaErrorInvalidValue;
   }
   GemmArgs g;
   g.sfa = L.sfa;
@@ -595,10 +668,19 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.n_routed = L.n_routed;
   g.K = (int)L.K;
   g.N = (int)L.N;
-  g.n_tiles = L.mode == 1 ? (int)(L.inter / 128) : (int)ceil_div(L.N, bn);
+  g.n_tiles = L.mode == 1 ? (int)(L.act == MM_ACT_GELU ? L.N / 256 : L.inter / 128) : (int)ceil_div(L.N, bn);
   g.big_mt = kBigMtiles;
   g.nb = (int)prepared_nblocks(L.N, L.mode == 1 ? 256 : bn);
   g.b_fp4 = L.b_fmt == MM_DT_FP4_E2M1;
+  g.act = L.act;
+  g.act_c = L.act_c;
+  g.act_alpha = L.act_alpha;
+  g.act_beta = L.act_beta;
+  g.act_rbeta = L.act_beta != 0.f ? 1.0f / L.act_beta : 0.f;
+  g.act_beta_lin = L.act_beta_lin;
+  g.act_rbeta_lin = L.act_beta_lin > 0.f ? 1.0f / L.act_beta_lin : 0.f;
+  g.act_gelu_k = (float)sqrt(8.0 / acos(-1.0));
+  g.aw = L.mode == 1 ? (L.act == MM_ACT_GELU ? 2 * L.inter : L.inter) : 0;
   g.b_fp4_sh = (L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt) == MM_DT_FP4_E2M1;
   g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, bn);
   g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);

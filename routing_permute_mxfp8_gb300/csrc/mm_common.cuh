@@ -20,6 +20,13 @@ constexpr int kBM = 128;              // GEMM tile rows (expanded rows)
 constexpr int kBK = 128;              // GEMM k-block (FP8 bytes = one 128B swizzle row)
 constexpr int kSfChunk = 512;         // E8M0 bytes of one (128 rows x 128 k) scale tile
 
+// MegaMoE activations (the ABI takes their names)
+constexpr int MM_ACT_SWIGLU = 0;
+constexpr int MM_ACT_SWIGLUSTEP = 1;
+constexpr int MM_ACT_SWIGLUOAI = 2;
+constexpr int MM_ACT_SITUGLU = 3;
+constexpr int MM_ACT_GELU = 4;
+
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 

@@ -52,7 +52,8 @@ cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_
 // ---- permute / quantise (permute.cu) -------------------------------------
 struct PermuteArgs {
   const void* src;          // [n, h] source rows
-  int src_dtype;            // MM_DT_BFLOAT16 / FLOAT16 / FLOAT32
+  int src_dtype;            // MM_DT_BFLOAT16 / FLOAT16 / FLOAT32, or FP8 with src_scales
+  const uint8_t* src_scales;  // pre-quantised source: E8M0 [n, h/32] (tile-layout output only)
   int64_t n, h;             // rows, row length (elements)
   int k;                    // destinations per row from dest[] (row i -> dest[i*k + t])
   const int32_t* dest;      // [n*k] destination rows (< 0: skipped; null: identity, k must be 1)
@@ -90,6 +91,9 @@ struct GemmLaunch {
   int64_t K, N;
   int a_fmt, b_fmt, b_fmt_sh; // 23 / 24
   int inter;                  // mode 1: I (= N / 2)
+  int act;                    // mode 1: MM_ACT_* (A_hat width I, or 2I for gelu)
+  float act_c, act_alpha, act_beta, act_beta_lin;  // clamp (+inf: off), swigluoai alpha / beta,
+                                                   // situglu beta / linear beta (0: off)
   uint8_t* act_q;             // mode 1 outputs
   uint8_t* act_sf;
   __nv_bfloat16* out;         // mode 2 output [rows_cap, N]

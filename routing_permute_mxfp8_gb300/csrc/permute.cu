@@ -208,6 +208,34 @@ __global__ void k_unpad(UnpadArgs a) {
     a.dst_sf[(int64_t)d * groups + g] = a.src_sf[sf_tile_offset(p, g, a.cols / 128)];
 }
 
+// Pre-quantised pass-through (MegaMoE dispatchQuantMode = 0): the source
+// rows already hold FP8 codes and src_scales their E8M0 scales, [n, h/32];
+// each row is copied to its destinations and its scales rewritten in the
+// GEMM tile layout.  Warp per row, 16 bytes per lane, one 4-group scale
+// word per lane and step.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(PermuteArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  if (row >= a.n) return;
+  int32_t d0, d1;
+  int ndest;
+  load_dests(a, row, lane, d0, d1, ndest);
+  const uint8_t* src_row = static_cast<const uint8_t*>(a.src) + row * a.h;
+  const uint8_t* src_sf = a.src_scales + row * (a.h / 32);
+  uint8_t* out = static_cast<uint8_t*>(a.out);
+  const int64_t groups4 = a.h / 128;
+  // destinations are read by warp shuffles: every lane runs the t loop
+  for (int t = 0; t < ndest; ++t) {
+    const int32_t d = dest_at(t, d0, d1);
+    if (d < 0) continue;  // uniform across the warp
+    for (int64_t col = lane * 16; col < a.h; col += 512)
+      *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = *reinterpret_cast<const uint4*>(src_row + col);
+    for (int64_t w = lane; w < groups4; w += 32)
+      *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, 4 * w, groups4)) =
+          *reinterpret_cast<const uint32_t*>(src_sf + 4 * w);
+  }
+}
+
 template <int kSrc, int kFmt>
 cudaError_t launch_mx_variant(const PermuteArgs& a, int blocks, cudaStream_t st) {
   if (a.scale_cols == 0)
@@ -231,6 +259,11 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
   const int64_t blocks64 = (a.n + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks64 > 0x7fffffff) return cudaErrorInvalidValue;
   const int blocks = (int)blocks64;
+  if (a.src_scales) {  // pre-quantised rows into the tile layout
+    if (a.scale_cols != 0 || a.h % 128 != 0) return cudaErrorInvalidValue;
+    k_permute_prequant<<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
+    return cudaGetLastError();
+  }
   if (a.out_fmt < 0) {
     const int esz = a.src_dtype == MM_DT_FLOAT32 ? 4 : 2;
     k_permute_copy<<<blocks, kWarpsPerBlock * 32, 0, st>>>(a, esz);

@@ -69,13 +69,13 @@ def test_workspace_queries(lib):
 
 
 def _mega(lib, **kw):
-    a = dict(x=1, ids=1, w=1, gdt=0, w1=1, w2=1, s1=1, s2=1, wdt=24, layout=0, sw1=None, sw2=None, ss1=None,
+    a = dict(x=1, xs=None, ids=1, w=1, gdt=0, w1=1, w2=1, s1=1, s2=1, wdt=24, layout=0, sw1=None, sw2=None, ss1=None,
              ss2=None, swdt=24, s=0, bs=64, h=256, k=2, e=8, ep=1, inter=128, maxrecv=0, dqm=4, dqd=24, cqm=0,
              act=b"swiglu", params=None, nparams=0, y=1, counts=None, exp=None, aq=None, asc=None, ws=None,
              wsb=0, err=None, stream=None)
     a.update(kw)
     vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
-    return lib.mm_mega_moe(vp(a["x"]), vp(a["ids"]), vp(a["w"]), a["gdt"], vp(a["w1"]), vp(a["w2"]), vp(a["s1"]),
+    return lib.mm_mega_moe(vp(a["x"]), vp(a["xs"]), vp(a["ids"]), vp(a["w"]), a["gdt"], vp(a["w1"]), vp(a["w2"]), vp(a["s1"]),
                            vp(a["s2"]), a["wdt"], a["layout"], vp(a["sw1"]), vp(a["sw2"]), vp(a["ss1"]),
                            vp(a["ss2"]), a["swdt"], a["s"], a["bs"], a["h"], a["k"], a["e"], a["ep"], a["inter"],
                            a["maxrecv"], a["dqm"], a["dqd"], a["cqm"], a["act"], a["params"], a["nparams"],
@@ -86,13 +86,27 @@ def _mega(lib, **kw):
 def test_mega_moe_host_rejections(lib):
     assert _mega(lib, ep=2) == 2                     # ep_world_size != 1
     assert _mega(lib, cqm=3) == 2                    # combine quantisation
-    assert _mega(lib, dqm=0) == 2                    # pre-quantised pass-through
-    assert _mega(lib, act=b"gelu") == 2
-    assert _mega(lib, dqd=296) == 2                  # FP4 dispatch
+    assert _mega(lib, dqm=0) == 1                    # pass-through without x_scales
+    assert _mega(lib, xs=1) == 1                     # x_scales with internal quantisation
+    assert _mega(lib, dqm=3) == 2                    # other dispatch quant modes
+    assert _mega(lib, act=b"relu") == 2              # unknown activation
+    assert _mega(lib, act=b"gelu") == 1              # gelu needs its [FLT_MAX] placeholder
+    assert _mega(lib, dqd=296) == 2                  # FP4 dispatch (A4W4-FP)
     assert _mega(lib, gdt=27 + 1) == 1               # gating weight dtype
     assert _mega(lib, maxrecv=100) == 1              # below bs*k rows
     assert _mega(lib, ws=None, wsb=0) == 3           # workspace missing
     assert _mega(lib, bs=0) == 0                     # empty batch: nothing to do
+    f = lambda *v: (ctypes.c_float * len(v))(*v)
+    for act, params in ((b"swiglu", (2.0, 1.0)), (b"swiglu", (-1.0,)), (b"swiglu", (float("nan"),)),
+                        (b"swigluoai", (1.0,)), (b"swigluoai", (0.0, float("inf"), 1.0)), (b"situglu", (0.0,)),
+                        (b"situglu", (1.0, -2.0)), (b"situglu", (1.0, 2.0, 3.0)), (b"gelu", (1.0,))):
+        assert _mega(lib, act=act, params=f(*params), nparams=len(params)) == 1, (act, params)
+    # valid lists pass the activation check (and stop at the missing workspace)
+    fmax = 3.4028234663852886e38
+    for act, params in ((b"swiglu", (0.0,)), (b"swiglustep", (7.0,)), (b"swigluoai", ()),
+                        (b"swigluoai", (7.0, 1.702, 1.0)), (b"situglu", ()), (b"situglu", (2.0, 3.0)),
+                        (b"gelu", (fmax,))):
+        assert _mega(lib, act=act, params=f(*params) if params else None, nparams=len(params)) == 3, act
 
 
 def test_permute_host_rejections(lib):

@@ -203,10 +203,10 @@ def _sparse_weights(cfg, experts, shared=False):
     all-zero (codes 0, scale code 127), which keeps full-size runs cheap to
     build while every checked token sees its real weights."""
     n_exp = cfg.shared if shared else cfg.e
-    s1c, s2c = 2 * ((cfg.h + 63) // 64), 2 * ((cfg.inter + 63) // 64)
+    s1c, s2c = 2 * ((cfg.h + 63) // 64), 2 * ((cfg.act_width + 63) // 64)
     w1 = np.zeros((n_exp, 2 * cfg.inter, cfg.h), np.uint8)
     s1 = np.full((n_exp, 2 * cfg.inter, s1c), 127, np.uint8)
-    w2 = np.zeros((n_exp, cfg.h, cfg.inter), np.uint8)
+    w2 = np.zeros((n_exp, cfg.h, cfg.act_width), np.uint8)
     s2 = np.full((n_exp, cfg.h, s2c), 127, np.uint8)
     for e in experts:
         w1[e], s1[e] = oracle.mx_quantize(synth.weight_f32(cfg, 1, int(e), shared=shared), oracle.DT_F32,
@@ -242,15 +242,17 @@ def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
     err = zeros_err()
     y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
         bf16(x), t(ids), gt, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt), ws1, ws2, cfg.e,
-        weight_dtype=cfg.weight_fmt, weight_scale_layout=layout,
-        dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err, want_expanded_row_idx=True, want_act=True, **kw)
+        weight_dtype=cfg.weight_fmt, weight_scale_layout=layout, activation=cfg.activation,
+        activation_params=cfg.act_params, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err,
+        want_expanded_row_idx=True, want_act=True, **kw)
     assert host(err)[0] == 0
     r_srt, r_exp, r_cnt, _ = oracle.route(ids, cfg.e)
     assert np.array_equal(host(counts), r_cnt.astype(np.int32))
     assert np.array_equal(host(exp_idx), r_exp)
     tok = np.arange(cfg.n) if tokens is None else np.asarray(tokens)
     y_ref, _, aq_ref, as_ref = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt,
-                                                      cfg.weight_fmt, tokens=tok, shared=sh, want_act=True)
+                                                      cfg.weight_fmt, tokens=tok, shared=sh, want_act=True,
+                                                      activation=cfg.activation, act_params=cfg.act_params)
     yg = host(y).view(np.uint16)
     yg = synth.bf16_bits_to_f32(yg)[tok]
     if check_acts:
@@ -277,6 +279,16 @@ MEGA_CASES = {
     "a8w4_shared_zipf": dict(n=300, h=512, inter=256, e=8, k=4, shared=1, routing="zipf", weight_fmt=296,
                              dispatch_fmt=24),
     "a8w4_e5m2_tokens": dict(n=256, h=896, inter=384, e=8, k=4, weight_fmt=296, dispatch_fmt=23),
+    # the README's other activations ("Activation function formulas") and clamps
+    "swiglu_clamp": dict(n=128, e=8, k=4, act_params=(0.05,)),
+    "swiglustep_clamp": dict(n=128, e=8, k=4, activation="swiglustep", act_params=(0.002,)),
+    "swigluoai_default": dict(n=128, e=8, k=4, activation="swigluoai"),
+    "swigluoai_params": dict(n=128, e=8, k=4, shared=1, activation="swigluoai", act_params=(0.05, 1.5, 0.25)),
+    "situglu_beta": dict(n=128, e=8, k=4, activation="situglu", act_params=(0.5,)),
+    "situglu_linear": dict(n=128, e=8, k=4, activation="situglu", act_params=(0.5, 0.3)),
+    "gelu": dict(n=128, e=8, k=4, shared=1, activation="gelu", act_params=(float(np.finfo(np.float32).max),)),
+    "gelu_a8w4": dict(n=200, h=512, inter=256, e=8, k=4, activation="gelu", weight_fmt=296,
+                      act_params=(float(np.finfo(np.float32).max),)),
     # 1024 routed + 1 shared segments: the segment table leaves no shared
     # memory for GEMM2's output staging, so O rows are stored directly
     "many_experts": dict(n=256, h=256, inter=128, e=1024, k=8, shared=1),
@@ -287,6 +299,30 @@ MEGA_CASES = {
 def test_mega_moe_small(case):
     cfg = synth.CONFIGS["tiny"].scaled(**MEGA_CASES[case])
     run_mega(cfg)
+
+
+def test_mega_moe_prequant_passthrough():
+    """dispatch_quant_mode 0: the caller's FP8 codes and E8M0 scales are used as
+    X_hat, S_X.  Feeding Q_MX(x) (oracle) gives the internal-quantisation result
+    bit for bit, and matches the oracle's pass-through run."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1, routing="zipf")
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    sh = _weights(cfg, shared=True)
+    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, cfg.dispatch_fmt)
+    kw = dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]), shared_weight2=t(sh[2]),
+              shared_weight_scales2=t(sh[3]), dispatch_quant_out_dtype=cfg.dispatch_fmt)
+    err = zeros_err()
+    y0 = mm.mm_mega_moe(bf16(x), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err, **kw)[0]
+    y1 = mm.mm_mega_moe(t(xq), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err,
+                        dispatch_quant_mode=0, x_scales=t(xs), **kw)[0]
+    assert host(err)[0] == 0
+    assert np.array_equal(host(y0).view(np.uint16), host(y1).view(np.uint16))
+    y_ref, _ = oracle.mega_moe_tokens(None, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt,
+                                      shared=sh, x_prequant=(xq, xs))
+    check_y(synth.bf16_bits_to_f32(host(y1).view(np.uint16)), y_ref)
 
 
 def test_mega_moe_prepared_scales_identical():
