@@ -79,10 +79,11 @@ typedef enum {
 #define MM_DT_FP4_E2M1 296
 
 /* Quant-mode codes of moe_token_permute and MoeInitRoutingV3:
- * -1 none, 2 MXFP8 E5M2, 3 MXFP8 E4M3FN (9, MXFP4, is not implemented). */
+ * -1 none, 2 MXFP8 E5M2, 3 MXFP8 E4M3FN; 9 MXFP4 E2M1 (moe_token_permute only). */
 #define MM_QUANT_NONE (-1)
 #define MM_QUANT_MXFP8_E5M2 2
 #define MM_QUANT_MXFP8_E4M3FN 3
+#define MM_QUANT_MXFP4_E2M1 9
 
 /* Layouts of the E8M0 weight scales passed to mm_mega_moe. */
 #define MM_WSCALE_ROWS 0     /* the pages' (E, N_out, CeilDiv(K_red, 64), 2) */
@@ -151,9 +152,12 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
  * num_out_tokens  0: M = F = n*topk; > 0: M = min(num_out_tokens, F);
  *                 < 0: M = max(F + num_out_tokens, 0).
  * padded_mode     must be 0 (MM_ERR_UNSUPPORTED otherwise, as in the article).
- * quant_mode      MM_QUANT_NONE, MM_QUANT_MXFP8_E5M2, MM_QUANT_MXFP8_E4M3FN.
- * permuted_tokens [M, h] output (tokens' type, or FP8).
- * expanded_scale  [M, AlignUp(CeilDiv(h, 32), 2)] E8M0 output (MXFP8 modes).
+ * quant_mode      MM_QUANT_NONE, MM_QUANT_MXFP8_E5M2, MM_QUANT_MXFP8_E4M3FN, or
+ *                 MM_QUANT_MXFP4_E2M1 (the article's quant_mode 9: 32-element
+ *                 groups, emax 2, two codes per byte, element 2i in bits 0-3).
+ * permuted_tokens [M, h] output (tokens' type, or FP8); MXFP4: [M, h/2] bytes.
+ * expanded_scale  [M, AlignUp(CeilDiv(h, 32), 2)] E8M0 output (MXFP8 modes);
+ *                 MXFP4: [M, CeilDiv(h, 64), 2], the same number of columns.
  * sorted_indices  [F] int32 output, never truncated.
  * Limits: F < 16777215.
  * ---------------------------------------------------------------------- */

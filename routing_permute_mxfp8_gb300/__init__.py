@@ -28,6 +28,7 @@ DT_F32, DT_F16, DT_I32, DT_I64, DT_BF16 = 0, 1, 3, 9, 27
 DT_FP8_E5M2, DT_FP8_E4M3FN = 23, 24
 DT_FP4_E2M1 = 296   # packed two codes per byte, element 2i in bits 0-3
 QUANT_NONE, QUANT_MXFP8_E5M2, QUANT_MXFP8_E4M3FN = -1, 2, 3
+QUANT_MXFP4_E2M1 = 9   # moe_token_permute: packed [M, H/2] codes, scales [M, CeilDiv(H, 64), 2]
 WSCALE_ROWS, WSCALE_PREPARED = 0, 1
 
 _TORCH_DT = {torch.float32: DT_F32, torch.float16: DT_F16, torch.bfloat16: DT_BF16,
@@ -157,7 +158,9 @@ def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_
 def mm_moe_token_permute(tokens, indices, num_experts: int, num_out_tokens=None, padded_mode: bool = False,
                          quant_mode: int = QUANT_NONE, *, workspace=None, dev_err=None):
     """moe_token_permute: returns (permuted_tokens [M, H], sorted_indices [F] int32,
-    expanded_scale [M, AlignUp(H/32, 2)] uint8 E8M0 or an empty tensor)."""
+    expanded_scale [M, AlignUp(H/32, 2)] uint8 E8M0 or an empty tensor).  With
+    QUANT_MXFP4_E2M1: permuted_tokens [M, H/2] packed uint8, expanded_scale
+    [M, CeilDiv(H, 64), 2]."""
     _need_cuda(tokens, indices)
     L = load()
     n, h = tokens.shape
@@ -167,9 +170,11 @@ def mm_moe_token_permute(tokens, indices, num_experts: int, num_out_tokens=None,
     m = int(L.mm_moe_token_permute_out_rows(f, nout))
     dev = tokens.device
     out_dt = tokens.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
-    permuted = torch.empty((m, h), dtype=out_dt, device=dev)
+    permuted = torch.empty((m, h // 2 if quant_mode == QUANT_MXFP4_E2M1 else h), dtype=out_dt, device=dev)
     scale = (torch.empty((m, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
              else torch.empty((0,), dtype=torch.float32, device=dev))
+    if quant_mode == QUANT_MXFP4_E2M1:
+        scale = scale.view(m, (h + 63) // 64, 2)
     sorted_indices = torch.empty(f, dtype=torch.int32, device=dev)
     need = ctypes.c_size_t(0)
     _check(L.mm_moe_token_permute_workspace_size(f, num_experts, ctypes.byref(need)), "mm_moe_token_permute")

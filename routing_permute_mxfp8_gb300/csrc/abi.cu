@@ -35,6 +35,7 @@ bool is_fp8(int64_t dt) { return dt == MM_DT_FP8_E4M3FN || dt == MM_DT_FP8_E5M2;
 // expert weight types: FP8 (A8W8-FP) or FP4 E2M1 (A8W4-FP)
 bool is_mx_weight(int64_t dt) { return is_fp8(dt) || dt == MM_DT_FP4_E2M1; }
 int quant_fmt(int quant_mode) {
+  if (quant_mode == MM_QUANT_MXFP4_E2M1) return MM_DT_FP4_E2M1;
   return quant_mode == MM_QUANT_MXFP8_E5M2 ? MM_DT_FP8_E5M2
                                            : (quant_mode == MM_QUANT_MXFP8_E4M3FN ? MM_DT_FP8_E4M3FN : -1);
 }
@@ -370,7 +371,8 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
   mm_status s = mm_moe_token_permute_workspace_size(f, num_experts, &need);
   if (s != MM_OK) return s;
   if (padded_mode != 0) return MM_ERR_UNSUPPORTED;
-  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
+  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN &&
+      quant_mode != MM_QUANT_MXFP4_E2M1)
     return MM_ERR_UNSUPPORTED;
   const bool quant = quant_mode != MM_QUANT_NONE;
   if (quant && tokens_dtype == MM_DT_FLOAT32) return MM_ERR_UNSUPPORTED;  // the article: fp16 / bf16

@@ -115,7 +115,9 @@ def test_permute_host_rejections(lib):
         vp(1), kw.get("dt", 27), vp(1), kw.get("idt", 3), 4, 2, kw.get("h", 128), kw.get("e", 2), 0,
         kw.get("pad", 0), kw.get("q", -1), vp(1), vp(1), vp(1), None, 0, None, None)
     assert call(pad=1) == 2          # padded_mode is not supported (as in the article)
-    assert call(q=9) == 2            # MXFP4
+    assert call(q=4) == 2            # not a quant mode of the article
+    assert call(q=9, dt=0) == 2      # MXFP4 takes fp16 / bf16 tokens
+    assert call(q=9) == 3            # MXFP4 accepted (stops at the missing workspace)
     assert call(idt=0) == 1          # indices dtype
     assert call(q=2, h=24) == 2      # H % 16 for MXFP8
     assert call() == 3               # workspace missing

@@ -91,6 +91,8 @@ def test_init_routing_bit_exact(n, h, e, k, quant, kind):
     (torch.float16, False, -5, 3, False),
     (torch.float32, False, 100000, -1, False),
     (torch.bfloat16, True, None, 3, True),
+    (torch.bfloat16, False, 0, 9, False),      # MXFP4 E2M1 (the article's quant_mode 9)
+    (torch.float16, True, -7, 9, False),
 ])
 def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d):
     n, h, e, k = 700, 256, 16, 1 if one_d else 4
@@ -108,12 +110,15 @@ def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d):
     assert np.array_equal(host(sidx), r_exp)
     src_dt = {torch.bfloat16: oracle.DT_BF16, torch.float16: oracle.DT_F16, torch.float32: oracle.DT_F32}[dtype]
     src = xt.view(torch.int16).numpy().view(np.uint16) if dtype != torch.float32 else xf
-    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    fmt = {-1: -1, 2: 23, 3: 24, 9: 296}[quant]
     r_out, r_sc = oracle.permute(src, src_dt, k, r_srt, m, fmt=fmt)
     got = host(perm)
+    if fmt == 296:
+        assert got.shape == (m, h // 2) and tuple(sc.shape) == (m, (h + 63) // 64, 2)
+        r_out = pack_fp4(r_out)
     assert np.array_equal(got.view(r_out.dtype) if fmt < 0 else got, r_out)
     if quant != -1:
-        assert np.array_equal(host(sc), r_sc)
+        assert np.array_equal(host(sc).reshape(m, -1), r_sc)
 
 
 def test_out_of_range_ids_are_left_out_and_flagged():

@@ -229,7 +229,7 @@ def test_route_int64_and_invalid_ids():
 
 
 # ------------------------------------------------------------------ permute
-@pytest.mark.parametrize("fmt", [-1, P.E4M3, P.E5M2])
+@pytest.mark.parametrize("fmt", [-1, P.E4M3, P.E5M2, P.E2M1])
 def test_permute_matches_gather(fmt):
     cfg = synth.CONFIGS["tiny"].scaled(n=96, h=160)
     x = synth.tokens_bf16(cfg)
