@@ -236,13 +236,13 @@ def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
     ws1, ws2 = t(s1), t(s2)
     if layout == 1:
         ws1 = mm.mm_prepare_weight_scales(ws1, cfg.h, 1)
-        ws2 = mm.mm_prepare_weight_scales(ws2, cfg.inter, 2)
+        ws2 = mm.mm_prepare_weight_scales(ws2, cfg.act_width, 2)
     kw = {}
     if sh is not None:
         sw1, ss1, sw2, ss2 = gpu_codes(sh[0], cfg.weight_fmt), t(sh[1]), gpu_codes(sh[2], cfg.weight_fmt), t(sh[3])
         if layout == 1:
             ss1 = mm.mm_prepare_weight_scales(ss1, cfg.h, 1)
-            ss2 = mm.mm_prepare_weight_scales(ss2, cfg.inter, 2)
+            ss2 = mm.mm_prepare_weight_scales(ss2, cfg.act_width, 2)
         kw = dict(shared_weight1=sw1, shared_weight2=sw2, shared_weight_scales1=ss1, shared_weight_scales2=ss2)
     err = zeros_err()
     y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
@@ -361,6 +361,20 @@ def test_mega_moe_dsv3_prefill_full_size():
 def test_mega_moe_dsv3_decode_full_size():
     cfg = synth.CONFIGS["dsv3_decode"]
     run_mega(cfg, tokens=np.array([0, 5, 17, 63, 64, 100, 126, 127]), layout=1, sparse=True)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_prefill_a8w4_full_size():
+    """A8W4-FP (MXFP4 weights, MXFP8 E4M3 activations) at the DeepSeek-V3 prefill shape."""
+    cfg = synth.CONFIGS["dsv3_prefill"].scaled(weight_fmt=296, dispatch_fmt=24)
+    run_mega(cfg, tokens=np.array([0, 3, 1500, 4096, 7000, 8191]), layout=1, sparse=True)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_decode_gelu_full_size():
+    """gelu (whole 2I-wide Linear1 output) with a shared expert at the decode shape."""
+    cfg = synth.CONFIGS["dsv3_decode"].scaled(activation="gelu", act_params=(float(np.finfo(np.float32).max),))
+    run_mega(cfg, tokens=np.array([0, 31, 64, 127]), layout=1, sparse=True)
 
 
 def test_mega_moe_duplicate_ids_flagged():
