@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling on a smaller case)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling on a smaller case)")
+    ap.add_argument("--weights", choices=["fp8", "fp4"], default="fp8",
+                    help="fp4: the A8W4-FP variant of the workload (MXFP4 weights, MXFP8 E4M3 activations)")
     return ap.parse_args()
 
 
@@ -67,6 +69,8 @@ def workload(args):
         cfg = cfg.scaled(n=args.tokens)
     if args.experts:
         cfg = cfg.scaled(e=args.experts)
+    if args.weights == "fp4":
+        cfg = cfg.scaled(name=cfg.name + "_a8w4", weight_fmt=296, dispatch_fmt=24)
     return cfg
 
 
@@ -452,7 +456,7 @@ def run_ours(args):
         "config": {"workload": cfg.name, "tokens": cfg.n, "hidden": cfg.h, "intermediate": cfg.inter,
                    "experts": cfg.e, "topk": cfg.k, "routing": f"{cfg.routing}" + (" s=1.0" if cfg.routing == "zipf" else ""),
                    "dispatch": "mxfp8_e5m2" if cfg.dispatch_fmt == 23 else "mxfp8_e4m3",
-                   "weights": "mxfp8_e4m3" if cfg.weight_fmt == 24 else "mxfp8_e5m2",
+                   "weights": {24: "mxfp8_e4m3", 23: "mxfp8_e5m2", 296: "mxfp4_e2m1"}[cfg.weight_fmt],
                    "gate": cfg.gate_dtype, "shared_experts": cfg.shared,
                    "weight_scale_layout": "prepared once (mm_prepare_weight_scales)",
                    "l2": "inputs larger than L2 (weights streamed from HBM every step)",
@@ -520,7 +524,8 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
                     "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
     del x, W, ws
     # decode: same expert weights as the prefill workload, plus one shared expert
-    dc = synth.CONFIGS["dsv3_decode"]
+    # (same weight type as the prefill weights it reuses)
+    dc = synth.CONFIGS["dsv3_decode"].scaled(weight_fmt=cfg_prefill.weight_fmt)
     x, ids, gate, _, S = gpu_inputs(dc, mm, torch, seed_offset=20 + dist.rank, weights=W_prefill)
     ws = torch.empty(mm.mm_mega_moe_workspace_size(dc.n, dc.h, dc.k, dc.e, dc.inter, dc.shared, 1),
                      dtype=torch.uint8, device="cuda")
@@ -528,12 +533,14 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
     ms, st, _ = time_steps(torch, lambda: mega_call(mm, dc, x, ids, gate, W_prefill, S, ws, y), steps, 3, dist)
     t = ms / steps / 1e3
     touched = int(torch.unique(ids).numel())
-    per_exp = 3 * dc.h * dc.inter * (1 + 1 / 32)
+    per_exp = 3 * dc.h * dc.inter * ((0.5 if dc.weight_fmt == mm.DT_FP4_E2M1 else 1.0) + 1 / 32)
     wbytes = (touched + dc.shared) * per_exp
     out["decode"] = {"tokens_per_s": dc.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
                      "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
                      "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
     del x, ws, S
+    if cfg_prefill.weight_fmt == mm.DT_FP4_E2M1:
+        return out
     # A8W4-FP: the same prefill and decode shapes with MXFP4 E2M1 weights (packed,
     # half the weight bytes) and MXFP8 E4M3 activations
     a8w4 = {}
