@@ -251,10 +251,14 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
  * (E, N_out, CeilDiv(K_red, 64), 2) layout into the tile layout the grouped
  * GEMMs read (MM_WSCALE_PREPARED), the way the pages require FRACTAL_NZ
  * weight formats for some scenarios.  which = 1 for weightScales1 (N_out =
- * 2I), 2 for weightScales2 (N_out = H); the layout groups rows by the tile
- * width of the GEMM that reads them.  src and dst are device buffers; dst
- * holds mm_prepared_weight_scales_size bytes.  K_red must be a multiple of
- * 128.
+ * 2I), 2 for weightScales2 (N_out = H).  The layout is [E][pair][K_red/128]
+ * [2][512 B]: each 512-byte tile holds the scales of 128 rows x 128 k in the
+ * order the tensor-core scale copy reads them, and the two tiles of one GEMM
+ * n tile sit side by side (which = 1: gate rows 128p.. with up rows
+ * I + 128p..; which = 2: rows 256p..; rows past N_out read as zero).  src and
+ * dst are device buffers; dst holds mm_prepared_weight_scales_size bytes.
+ * K_red must be a multiple of 128, and with which = 1 N_out a multiple of
+ * 256; other sizes give MM_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */
 mm_status mm_prepared_weight_scales_size(int which, int64_t experts, int64_t n_out, int64_t k_red,
                                          size_t* bytes);

@@ -101,12 +101,11 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   w.o = c.take<__nv_bfloat16>(d.rows_cap * d.h);
   w.wsf1 = w.wsf2 = w.swsf1 = w.swsf2 = nullptr;
   if (wscale_layout == MM_WSCALE_ROWS) {
-    const int64_t bn2 = gemm_tile_n(2, d.h);
-    w.wsf1 = c.take<uint8_t>(d.e * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
-    w.wsf2 = c.take<uint8_t>(d.e * prepared_nblocks(d.h, bn2) * (d.aw_max / 128) * kSfChunk);
+    w.wsf1 = c.take<uint8_t>(d.e * 2 * prepared_npairs(2 * d.inter, 1) * (d.h / 128) * kSfChunk);
+    w.wsf2 = c.take<uint8_t>(d.e * 2 * prepared_npairs(d.h, 2) * (d.aw_max / 128) * kSfChunk);
     if (d.s > 0) {
-      w.swsf1 = c.take<uint8_t>(d.s * prepared_nblocks(2 * d.inter, 256) * (d.h / 128) * kSfChunk);
-      w.swsf2 = c.take<uint8_t>(d.s * prepared_nblocks(d.h, bn2) * (d.aw_max / 128) * kSfChunk);
+      w.swsf1 = c.take<uint8_t>(d.s * 2 * prepared_npairs(2 * d.inter, 1) * (d.h / 128) * kSfChunk);
+      w.swsf2 = c.take<uint8_t>(d.s * 2 * prepared_npairs(d.h, 2) * (d.aw_max / 128) * kSfChunk);
     }
   }
   return w;
@@ -488,13 +487,12 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   const uint8_t *swsf1 = shared_weight_scales1, *swsf2 = shared_weight_scales2;
   if (weight_scale_layout == MM_WSCALE_ROWS) {
     StageScope sw(MM_STAGE_WSCALE, st);
-    const int64_t bn2 = gemm_tile_n(2, d.h);
-    e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, 256, w.wsf1, st);
-    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, aw, bn2, w.wsf2, st);
+    e = launch_prepare_wscales(weight_scales1, d.e, 2 * d.inter, d.h, 1, w.wsf1, st);
+    if (e == cudaSuccess) e = launch_prepare_wscales(weight_scales2, d.e, d.h, aw, 2, w.wsf2, st);
     if (e == cudaSuccess && d.s > 0)
-      e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, 256, w.swsf1, st);
+      e = launch_prepare_wscales(shared_weight_scales1, d.s, 2 * d.inter, d.h, 1, w.swsf1, st);
     if (e == cudaSuccess && d.s > 0)
-      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, aw, bn2, w.swsf2, st);
+      e = launch_prepare_wscales(shared_weight_scales2, d.s, d.h, aw, 2, w.swsf2, st);
     sw.finish(d.s > 0 ? 4 : 2);
     if (e != cudaSuccess) return MM_ERR_CUDA;
     wsf1 = w.wsf1;
@@ -635,7 +633,8 @@ mm_status mm_prepared_weight_scales_size(int which, int64_t experts, int64_t n_o
                                          size_t* bytes) {
   if (!bytes || (which != 1 && which != 2) || experts <= 0 || n_out <= 0 || k_red <= 0 || k_red % 128 != 0)
     return MM_ERR_INVALID_ARG;
-  *bytes = (size_t)(experts * prepared_nblocks(n_out, gemm_tile_n(which, n_out)) * (k_red / 128) * kSfChunk);
+  if (which == 1 && n_out % 256 != 0) return MM_ERR_INVALID_ARG;  // 2I with I a multiple of 128
+  *bytes = (size_t)(experts * 2 * prepared_npairs(n_out, which) * (k_red / 128) * kSfChunk);
   return MM_OK;
 }
 
@@ -646,7 +645,7 @@ mm_status mm_prepare_weight_scales(const uint8_t* src, int which, int64_t expert
   if (s != MM_OK) return s;
   if (!src || !dst || (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))
     return MM_ERR_INVALID_ARG;
-  return cuda_status(launch_prepare_wscales(src, experts, n_out, k_red, gemm_tile_n(which, n_out), dst,
+  return cuda_status(launch_prepare_wscales(src, experts, n_out, k_red, which, dst,
                                             static_cast<cudaStream_t>(stream)));
 }
 

@@ -82,7 +82,7 @@ struct GemmArgs {
   int K, N;
   int n_tiles;
   int big_mt;     // segments with >= big_mt m tiles form the tensor-bound list
-  int nb;         // 128-row blocks per expert in the prepared B scales
+  int npairs;     // 1 KB scale-tile pairs per expert and k-block in the prepared B scales
   uint32_t idesc, idesc_sh;
   int inter;
   uint8_t* act_q;
@@ -295,25 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool sh = ti.seg >= g.n_routed;
         const int e = sh ? ti.seg - g.n_routed : ti.seg;
         const CUtensorMap* mb = sh ? &tmBs : &tmB;
-        const uint8_t* sfb = (sh ? g.sfb_sh : g.sfb) + (int64_t)e * g.nb * kblocks * 512;
+        const uint8_t* sfb = (sh ? g.sfb_sh : g.sfb) + (int64_t)e * g.npairs * kblocks * 1024;
         const int am = mpre[ti.seg] + ti.mt;
-        int nb0, nb1, bn0, bn1;
-        if (kMode == 1 && g.act != MM_ACT_GELU) {
-          nb0 = ti.nt;  // gate rows nt*128.., up rows I + nt*128..
-          nb1 = g.inter / 128 + ti.nt;
-          bn0 = ti.nt * 128;
-          bn1 = g.inter + ti.nt * 128;
-        } else if (kMode == 1) {
-          nb0 = 2 * ti.nt;  // gelu: 256 consecutive rows of W1
-          nb1 = 2 * ti.nt + 1;
-          bn0 = ti.nt * 256;
-          bn1 = bn0 + 128;
-        } else {
-          nb0 = 2 * ti.nt;
-          nb1 = 2 * ti.nt + 1;
-          bn0 = ti.nt * kBN;
-          bn1 = 0;
-        }
+        // gated GEMM1: one 4-D box = gate rows nt*128.. and up rows I + nt*128..,
+        // whose scale tiles are prepared as one pair; otherwise 256 consecutive
+        // rows.  Under gelu, W1's scales are paired gate/up all the same, so the
+        // two 128-row blocks 2nt, 2nt+1 come from two pairs.
+        const bool gelu1 = kMode == 1 && g.act == MM_ACT_GELU;
+        const int p0 = gelu1 ? (2 * ti.nt) % g.npairs : ti.nt;
+        const int h0 = gelu1 ? (2 * ti.nt) / g.npairs : 0;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bounded(&empty[stage], phase ^ 1)) {
             ok = false;
@@ -324,11 +314,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], kb * kBK, am * kBM);
-          tma_load_3d(smB + stage * kBBytes, mb, &full[stage], kb * kBK, bn0, e);
-          if (kMode == 1) tma_load_3d(smB + stage * kBBytes + kABytes, mb, &full[stage], kb * kBK, bn1, e);
+          if (kMode == 1 && !gelu1)
+            tma_load_4d(smB + stage * kBBytes, mb, &full[stage], kb * kBK, ti.nt * 128, 0, e);
+          else
+            tma_load_3d(smB + stage * kBBytes, mb, &full[stage], kb * kBK, ti.nt * 256, e);
           bulk_load(smSFA + stage * 512, g.sfa + ((int64_t)am * kblocks + kb) * 512, 512, &full[stage]);
-          bulk_load(smSFB + stage * 1024, sfb + ((int64_t)nb0 * kblocks + kb) * 512, 512, &full[stage]);
-          bulk_load(smSFB + stage * 1024 + 512, sfb + ((int64_t)nb1 * kblocks + kb) * 512, 512, &full[stage]);
+          if (!gelu1) {
+            bulk_load(smSFB + stage * 1024, sfb + ((int64_t)ti.nt * kblocks + kb) * 1024, 1024, &full[stage]);
+          } else {
+            // blocks 2nt and 2nt+1 are in consecutive pairs (same half), or
+            // straddle from the last gate pair into the first up pair
+            const int p1 = (2 * ti.nt + 1) % g.npairs, h1 = (2 * ti.nt + 1) / g.npairs;
+            bulk_load(smSFB + stage * 1024, sfb + (((int64_t)p0 * kblocks + kb) * 2 + h0) * 512, 512, &full[stage]);
+            bulk_load(smSFB + stage * 1024 + 512, sfb + (((int64_t)p1 * kblocks + kb) * 2 + h1) * 512, 512,
+                      &full[stage]);
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -581,6 +581,22 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t n, uint64_t e,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Gated weight1 [E][2I][K] viewed as {K, I, 2, E}: one box of 2 x 128 rows
+// brings a tile's gate rows and the matching up rows (I further down) to
+// consecutive 16 KB halves of the stage.
+bool map_4d_pair(CUtensorMap* m, const void* ptr, uint64_t k, uint64_t inter, uint64_t e, bool fp4) {
+  cuuint64_t dims[4] = {k, inter, 2, e};
+  const uint64_t row_bytes = fp4 ? k / 2 : k;
+  cuuint64_t strides[3] = {row_bytes, inter * row_bytes, 2 * inter * row_bytes};
+  cuuint32_t box[4] = {(cuuint32_t)kBK, 128, 2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  EncodeTiledFn f = encode_fn();
+  return f && f(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                const_cast<void*>(ptr), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output matrix [rows][cols] (cols contiguous) of bf16 (GEMM2's O) or FP8
 // bytes (GEMM1's A_hat), box 64 bytes x 32 rows, 64B swizzle: the blocks
 // that the epilogue stages in shared memory.
@@ -639,15 +655,17 @@ int num_sms() {
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   const int nseg = L.n_routed + L.n_shared;
   const int bn = gemm_tile_n(L.mode, L.N);
-  const uint32_t box_rows = L.mode == 1 ? 128 : (uint32_t)bn;
+  const bool pair_map = L.mode == 1 && L.act != MM_ACT_GELU;
+  auto map_b = [&](CUtensorMap* m, const void* p, int64_t experts, int fmt) {
+    const bool fp4 = fmt == MM_DT_FP4_E2M1;
+    return pair_map ? map_4d_pair(m, p, (uint64_t)L.K, (uint64_t)L.inter, (uint64_t)experts, fp4)
+                    : map_3d(m, p, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)experts, (uint32_t)bn, fp4);
+  };
   CUtensorMap ma, mb, mbs;
   if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM)) return cudaErrorInvalidValue;
-  if (!map_3d(&mb, L.b, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_routed, box_rows, L.b_fmt == MM_DT_FP4_E2M1))
-    return cudaErrorInvalidValue;
+  if (!map_b(&mb, L.b, L.n_routed, L.b_fmt)) return cudaErrorInvalidValue;
   if (L.n_shared > 0) {
-    if (!map_3d(&mbs, L.b_sh, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)L.n_shared, box_rows,
-                L.b_fmt_sh == MM_DT_FP4_E2M1))
-      return cudaErrorInvalidValue;
+    if (!map_b(&mbs, L.b_sh, L.n_shared, L.b_fmt_sh)) return cudaErrorInvalidValue;
   } else {
     mbs = mb;
   }
@@ -670,7 +688,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.N = (int)L.N;
   g.n_tiles = L.mode == 1 ? (int)(L.act == MM_ACT_GELU ? L.N / 256 : L.inter / 128) : (int)ceil_div(L.N, bn);
   g.big_mt = kBigMtiles;
-  g.nb = (int)prepared_nblocks(L.N, L.mode == 1 ? 256 : bn);
+  g.npairs = (int)prepared_npairs(L.N, L.mode);
   g.b_fp4 = L.b_fmt == MM_DT_FP4_E2M1;
   g.act = L.act;
   g.act_c = L.act_c;

@@ -69,10 +69,13 @@ struct PermuteArgs {
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 
-// tile layout of E8M0 weight scales (mm_prepare_weight_scales): 128-row
-// blocks grouped by GEMM tiles of bn rows (two blocks per tile)
-int64_t prepared_nblocks(int64_t n_out, int64_t bn);
-cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red, int64_t bn,
+// Tile layout of E8M0 weight scales (mm_prepare_weight_scales): 512-byte
+// tiles of 128 rows x 128 k, two per GEMM n tile and k-block side by side
+// ([E][pair][k-block][2][512 B]) so one 1 KB copy brings a stage's B scales.
+// which = 1 (weight1, n_out = 2I): pair p = gate rows [128p, +128) and up
+// rows [I + 128p, +128); which = 2: rows [256p, +256).
+int64_t prepared_npairs(int64_t n_out, int which);
+cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red, int which,
                                    uint8_t* dst, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm.cu) ----------------------------------------------

@@ -169,27 +169,28 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_copy(PermuteArg
   }
 }
 
-// One thread per 4-byte word of the tile layout.  Rows are grouped by GEMM
-// tile (bn rows): 128-row block 2t + c holds rows [128c, 128c + 128) of
-// tile t (rows past the tile or past n_out read as 0).  For bn = 256 this
-// is simply 128-row blocks of consecutive rows.
+// One thread per 4-byte word of the tile layout [E][pair][k-block][2][128
+// words]: word wi of a tile holds the 4 scales (k 0-127) of row
+// (wi % 4) * 32 + wi / 4 of its 128-row block, the order in which the
+// 32x128b scale copy spreads them over TMEM lanes.  Rows past n_out read 0.
 __global__ void k_prepare_wscales(const uint8_t* __restrict__ src, int64_t experts, int64_t n_out,
-                                  int64_t k_red, int64_t nb, int64_t bn, uint8_t* __restrict__ dst) {
+                                  int64_t k_red, int64_t npairs, int which, uint8_t* __restrict__ dst) {
   const int64_t kc_n = k_red / 128;
-  const int64_t words = experts * nb * kc_n * 128;
+  const int64_t words = experts * npairs * kc_n * 2 * 128;
   const int64_t sc = k_red / 32;  // source row stride (2 * ceil(K/64) with K % 128 == 0)
   for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words;
        w += (int64_t)gridDim.x * blockDim.x) {
     const int64_t wi = w & 127;
-    const int64_t chunk = w >> 7;  // (e * nb + nblk) * kc_n + kc
-    const int64_t kc = chunk % kc_n;
-    const int64_t nblk = (chunk / kc_n) % nb;
-    const int64_t e = chunk / (kc_n * nb);
-    const int64_t n_in_tile = (nblk & 1) * 128 + (wi & 3) * 32 + (wi >> 2);
-    const int64_t r = (nblk >> 1) * bn + n_in_tile;
+    const int64_t tile = w >> 7;  // ((e * npairs + pair) * kc_n + kc) * 2 + half
+    const int64_t half = tile & 1;
+    const int64_t kc = (tile >> 1) % kc_n;
+    const int64_t pair = ((tile >> 1) / kc_n) % npairs;
+    const int64_t e = (tile >> 1) / (kc_n * npairs);
+    // GEMM1 pairs gate block p with up block I/128 + p; GEMM2 pairs 2p, 2p+1
+    const int64_t blk = which == 1 ? half * npairs + pair : 2 * pair + half;
+    const int64_t r = blk * 128 + (wi & 3) * 32 + (wi >> 2);
     uint32_t v = 0;
-    if (n_in_tile < bn && r < n_out)
-      v = __ldg(reinterpret_cast<const uint32_t*>(src + (e * n_out + r) * sc + kc * 4));
+    if (r < n_out) v = __ldg(reinterpret_cast<const uint32_t*>(src + (e * n_out + r) * sc + kc * 4));
     reinterpret_cast<uint32_t*>(dst)[w] = v;
   }
 }
@@ -274,16 +275,16 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
   return launch_mx_src<MM_DT_FLOAT32>(a, blocks, st);
 }
 
-int64_t prepared_nblocks(int64_t n_out, int64_t bn) { return 2 * ceil_div(n_out, bn); }
+int64_t prepared_npairs(int64_t n_out, int which) { return which == 1 ? n_out / 256 : ceil_div(n_out, 256); }
 
-cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red, int64_t bn,
+cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t n_out, int64_t k_red, int which,
                                    uint8_t* dst, cudaStream_t st) {
-  const int64_t nb = prepared_nblocks(n_out, bn);
-  const int64_t words = experts * nb * (k_red / 128) * 128;
+  const int64_t npairs = prepared_npairs(n_out, which);
+  const int64_t words = experts * npairs * (k_red / 128) * 2 * 128;
   if (words == 0) return cudaSuccess;
   int64_t blocks = ceil_div(words, 256);
   if (blocks > 65535 * 16) blocks = 65535 * 16;
-  k_prepare_wscales<<<(unsigned)blocks, 256, 0, st>>>(src, experts, n_out, k_red, nb, bn, dst);
+  k_prepare_wscales<<<(unsigned)blocks, 256, 0, st>>>(src, experts, n_out, k_red, npairs, which, dst);
   return cudaGetLastError();
 }
 
