@@ -119,7 +119,8 @@ int mm_version(void);
  *                   MXFP8 modes (padding column 0); ignored otherwise.
  * expanded_row_idx  [num_rows*k] int32 scatter index (rowIdxType 1), or NULL.
  * sorted_row_idx    [num_rows*k] int32 gather index (rowIdxType 0), or NULL.
- * expert_tokens     [expert_num] int64, or NULL.
+ * expert_tokens     [expert_num] int64, or NULL.  With num_rows = 0 only
+ *                   expert_tokens is written (all zeros).
  * Rows whose id is out of range are left out: their expanded_row_idx is -1,
  * the tail of sorted_row_idx is -1, the matching tail rows of expanded_x are
  * not written, and MM_DEVERR_EXPERT_RANGE is raised.
@@ -217,7 +218,8 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    A_hat has 2*intermediate columns.  Bad parameter lists
  *                    give MM_ERR_INVALID_ARG, other names MM_ERR_UNSUPPORTED.
  * y                  [bs, h] bf16 output.
- * expert_token_nums  [E] int32 output (rows per expert), or NULL.
+ * expert_token_nums  [E] int32 output (rows per expert), or NULL.  With
+ *                    bs = 0 only this is written (all zeros).
  * expanded_row_idx   [bs*k] int32 output pi(i, k) (position of row j = i*k+k'
  *                    in expert-sorted order), or NULL.
  * act_q, act_scale   optional diagnostic outputs of A_hat in expert-sorted

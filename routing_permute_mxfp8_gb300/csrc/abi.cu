@@ -305,7 +305,10 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   const bool quant = quant_mode != MM_QUANT_NONE;
   if (quant ? (h % 16 != 0) : ((h * dt_size(x_dtype)) % 16 != 0)) return MM_ERR_UNSUPPORTED;
   const int64_t rows = num_rows * k;
-  if (rows == 0) return MM_OK;
+  if (rows == 0)  // no rows: every expert's count (and the cumsum) is 0
+    return expert_tokens ? cuda_status(cudaMemsetAsync(expert_tokens, 0, (size_t)expert_num * sizeof(int64_t),
+                                                       static_cast<cudaStream_t>(stream)))
+                         : MM_OK;
   if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(expanded_x)) return MM_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
@@ -460,7 +463,11 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
   const int64_t rows = bs * k;
   if (max_recv_token_num != 0 && max_recv_token_num < rows) return MM_ERR_INVALID_ARG;
-  if (bs == 0) return MM_OK;
+  if (bs == 0)  // no tokens: Y is empty and every expert received 0 rows
+    return expert_token_nums ? cuda_status(cudaMemsetAsync(expert_token_nums, 0,
+                                                           (size_t)moe_expert_num * sizeof(int32_t),
+                                                           static_cast<cudaStream_t>(stream)))
+                             : MM_OK;
   if (!x || !topk_ids || !topk_weights || !weight1 || !weight2 || !weight_scales1 || !weight_scales2 || !y)
     return MM_ERR_INVALID_ARG;
   if (shared_expert_num > 0 &&

@@ -69,7 +69,13 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
   const int esz = x_dtype == MM_DT_FLOAT32 ? 4 : 2;
   if (quant ? (h % 16 != 0) : ((h * esz) % 16 != 0)) return MM_ERR_UNSUPPORTED;
   const int64_t rows = num_rows * k;
-  if (rows == 0) return MM_OK;
+  if (rows == 0) {  // no rows: every expert's count (and the cumsum) is 0
+    if (expert_tokens &&
+        cudaMemsetAsync(expert_tokens, 0, (size_t)expert_num * sizeof(int64_t), static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+      return MM_ERR_CUDA;
+    return MM_OK;
+  }
   if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(expanded_x) & 15))
     return MM_ERR_INVALID_ARG;

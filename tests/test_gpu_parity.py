@@ -7,6 +7,8 @@ activation codes that follow GEMM1 may differ by one code step in at most
 0.1 % of elements (the GEMM sums in fp32 on the tensor cores, the oracle in
 double).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -134,6 +136,29 @@ def test_out_of_range_ids_are_left_out_and_flagged():
     assert np.array_equal(host(tok), r_cnt)
     r_out, _ = oracle.permute(x, oracle.DT_BF16, 2, r_srt, 4)
     assert np.array_equal(host(ex)[:4], r_out)
+
+
+@pytest.mark.parametrize("ttype", [0, 1])
+def test_empty_batch_writes_zero_counts(ttype):
+    """No rows (num_rows = 0, bs = 0): every expert's count, and the cumsum,
+    is 0 (the histogram of an empty id list), so the count outputs are
+    written even though nothing else is.  Called through the C ABI on
+    buffers that hold junk beforehand."""
+    L = mm.load()
+    e = 16
+    vp = lambda a: ctypes.c_void_p(a.data_ptr())
+    dummy = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    tok = torch.full((e,), -7, dtype=torch.int64, device=DEV)
+    st = L.mm_moe_init_routing(vp(dummy), 27, vp(dummy), 0, 64, 4, e, 3, ttype, vp(dummy), vp(dummy), vp(dummy),
+                               vp(dummy), vp(tok), vp(dummy), 64, None, None)
+    assert st == 0
+    assert np.array_equal(host(tok), np.zeros(e, np.int64))
+    cnt = torch.full((e,), -7, dtype=torch.int32, device=DEV)
+    st = L.mm_mega_moe(vp(dummy), None, vp(dummy), vp(dummy), 0, vp(dummy), vp(dummy), vp(dummy), vp(dummy), 24, 0,
+                       None, None, None, None, 24, 0, 0, 256, 2, e, 1, 128, 0, 4, 24, 0, b"swiglu", None, 0,
+                       vp(dummy), vp(cnt), None, None, None, vp(dummy), 64, None, None)
+    assert st == 0
+    assert np.array_equal(host(cnt), np.zeros(e, np.int32))
 
 
 # ---------------------------------------------------------------- MX quantiser

@@ -86,3 +86,19 @@ def test_noalloc_rejects_a_problem_larger_than_its_scratch():
     st = f(ctypes.c_void_p(16), 27, ctypes.c_void_p(16), 1 << 17, 128, 8, 256, -1, 1, ctypes.c_void_p(16), None,
            None, None, None, None, None)
     assert st == 3
+
+
+@pytest.mark.parametrize("ttype", [0, 1])
+def test_noalloc_empty_batch_writes_zero_counts(ttype):
+    """num_rows = 0: the counts (or cumsum) output is all zeros, as from the
+    workspace-based entry point; nothing else is written."""
+    f = _abi()
+    e = 32
+    tok = torch.full((e,), -7, dtype=torch.int64, device=DEV)
+    dummy = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = f(vp(dummy), 27, vp(dummy), 0, 64, 4, e, 3, ttype, vp(dummy), vp(dummy), vp(dummy), vp(dummy), vp(tok),
+           None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(tok.cpu(), torch.zeros(e, dtype=torch.int64))
