@@ -18,29 +18,39 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-// Loads 16 consecutive elements of a row as fp32.
+// The raw 16-byte vectors of 16 consecutive elements (zeros past the row),
+// and their conversion to fp32: split so that a slice's loads can be issued
+// before the previous slice is quantised and stored.
 template <int kSrc>
-__device__ __forceinline__ void load16(const char* row, int64_t col, float* v) {
+struct Raw16 {
+  static constexpr int kN = kSrc == MM_DT_FLOAT32 ? 4 : 2;
+  uint4 u[kN];
+};
+
+template <int kSrc>
+__device__ __forceinline__ void load_raw16(const char* row, int64_t col, int64_t h, Raw16<kSrc>& r) {
+  constexpr int esz = kSrc == MM_DT_FLOAT32 ? 4 : 2;
+  const uint4* p = reinterpret_cast<const uint4*>(row + col * esz);
+#pragma unroll
+  for (int i = 0; i < Raw16<kSrc>::kN; ++i) r.u[i] = col < h ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int kSrc>
+__device__ __forceinline__ void raw16_to_f32(const Raw16<kSrc>& r, float* v) {
   if (kSrc == MM_DT_FLOAT32) {
-    const uint4* p = reinterpret_cast<const uint4*>(row + col * 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint4 u = __ldg(p + i);
-      v[4 * i] = __uint_as_float(u.x);
-      v[4 * i + 1] = __uint_as_float(u.y);
-      v[4 * i + 2] = __uint_as_float(u.z);
-      v[4 * i + 3] = __uint_as_float(u.w);
+      v[4 * i] = __uint_as_float(r.u[i].x);
+      v[4 * i + 1] = __uint_as_float(r.u[i].y);
+      v[4 * i + 2] = __uint_as_float(r.u[i].z);
+      v[4 * i + 3] = __uint_as_float(r.u[i].w);
     }
+  } else if (kSrc == MM_DT_BFLOAT16) {
+    bf16x8_to_f32(r.u[0], v);
+    bf16x8_to_f32(r.u[1], v + 8);
   } else {
-    const uint4* p = reinterpret_cast<const uint4*>(row + col * 2);
-    uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
-    if (kSrc == MM_DT_BFLOAT16) {
-      bf16x8_to_f32(u0, v);
-      bf16x8_to_f32(u1, v + 8);
-    } else {
-      f16x8_to_f32(u0, v);
-      f16x8_to_f32(u1, v + 8);
-    }
+    f16x8_to_f32(r.u[0], v);
+    f16x8_to_f32(r.u[1], v + 8);
   }
 }
 
@@ -89,16 +99,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs 
   uint8_t* out = static_cast<uint8_t*>(a.out);
   const int64_t groups = (a.h + 31) / 32;
   const int64_t groups4 = a.h / 128;
+  // slice c0 = 512 columns (16 per lane); the next slice's loads are in
+  // flight while this one is quantised and written to the K destinations
+  Raw16<kSrc> cur;
+  load_raw16<kSrc>(src_row, lane * 16, a.h, cur);
+  Raw16<kSrc> nxt = cur;
   for (int64_t c0 = 0; c0 < a.h; c0 += 512) {
     const int64_t col = c0 + lane * 16;
     const bool act = col < a.h;
+    if (c0 + 512 < a.h) load_raw16<kSrc>(src_row, col + 512, a.h, nxt);
     float v[16];
-    if (act) {
-      load16<kSrc>(src_row, col, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    }
+    raw16_to_f32<kSrc>(cur, v);
+    cur = nxt;
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
