@@ -1,8 +1,9 @@
 // Combine (MegaMoE README, A8W8-FP stage 4 at epWorldSize = 1):
 //   Y[i] = sum_k W[i,k] * O[pi(i,k)] + sum_s O_s^shared[i]
-// One block per token.  The expert rows are gathered with 16-byte loads,
-// accumulated in fp32 in the order k = 0..K-1 then the shared experts, and
-// rounded to bf16 once.  No atomics, so the result is deterministic.
+// One block per token.  The expert rows are gathered with 16-byte loads
+// (eight rows in flight per thread), accumulated in fp32 in the order
+// k = 0..K-1 then the shared experts, and rounded to bf16 once.  No atomics,
+// so the result is deterministic.
 #include "mm_route.cuh"
 
 namespace mm {
@@ -10,6 +11,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kMaxTerms = 36;  // top-K <= 32 plus up to 4 shared experts
+constexpr int kBatch = 8;      // expert rows gathered per round
 
 __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
   __shared__ int32_t rows[kMaxTerms];
@@ -31,15 +33,24 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
     float acc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-    for (int t = 0; t < nterm; ++t) {
-      const int32_t r = rows[t];
-      if (r < 0) continue;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.o + (int64_t)r * a.h + c));
-      float f[8];
-      bf16x8_to_f32(v, f);
-      const float wt = w[t];
+    // gather up to kBatch rows before accumulating any (all their loads in
+    // flight at once), then add them in term order
+    for (int t0 = 0; t0 < nterm; t0 += kBatch) {
+      uint4 v[kBatch];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
+      for (int b = 0; b < kBatch; ++b) {
+        const int32_t r = t0 + b < nterm ? rows[t0 + b] : -1;
+        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.o + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (t0 + b >= nterm || rows[t0 + b] < 0) continue;
+        float f[8];
+        bf16x8_to_f32(v[b], f);
+        const float wt = w[t0 + b];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
+      }
     }
     uint4 o;
     __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[0], acc[1]);
