@@ -529,7 +529,8 @@ def run_ours(args):
     }
     line.update(secondary)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        val, info = oracle_leg(cfg, max(1, min(os.cpu_count() or 1, 16)), 1, 0)
+        # about 10 s of host time: two steps of 12 sampled rows per host thread
+        val, info = oracle_leg(cfg, 12 * max(1, min(os.cpu_count() or 1, 16)), 2, 0)
         line["cpu_baseline"] = {"value": val, "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
                                 "sample": info["sample"]}
     if dist.rank == 0:
