@@ -55,6 +55,8 @@ def test_workspace_queries(lib):
     assert st == 0 and n >= 16384 * 8 * 4
     assert _ws(lib, "mm_moe_init_routing_workspace_size", 16384, 8, 0)[0] == 1
     assert _ws(lib, "mm_moe_init_routing_workspace_size", 1 << 22, 4, 8)[0] == 1   # F >= 16777215
+    assert _ws(lib, "mm_moe_init_routing_workspace_size", 16777215, 1, 8)[0] == 1  # F = the sort limit
+    assert _ws(lib, "mm_moe_init_routing_workspace_size", 16777214, 1, 8)[0] == 0  # largest F allowed
     st, n = _ws(lib, "mm_mega_moe_workspace_size", 8192, 7168, 8, 256, 2048, 0, 0)
     assert st == 0 and n > 8192 * 8 * 7168 * 3
     assert _ws(lib, "mm_mega_moe_workspace_size", 64, 200, 2, 8, 128, 0, 0)[0] == 2   # H % 128

@@ -57,6 +57,7 @@ ROUTE_CASES = [
     (4096, 1024, 2048, 4, 3, "distinct"),        # many experts
     (16384, 7168, 256, 8, -1, "distinct"),       # full routing workload, bf16 copy
     (16384, 7168, 256, 8, 3, "distinct"),        # full routing workload, MXFP8 E4M3
+    (8388607, 16, 256, 2, 3, "any"),             # N*K = 16777214, the largest the sort limit allows
 ]
 
 
@@ -322,6 +323,10 @@ MEGA_CASES = {
     # 1024 routed + 1 shared segments: the segment table leaves no shared
     # memory for GEMM2's output staging, so O rows are stored directly
     "many_experts": dict(n=256, h=256, inter=128, e=1024, k=8, shared=1),
+    # the limits: top-K 32 with 4 shared experts (36 destinations and combine
+    # terms per token), and 2048 routed experts + 4 shared segments
+    "topk32_shared4": dict(n=96, h=256, inter=128, e=64, k=32, shared=4),
+    "max_experts": dict(n=256, h=256, inter=128, e=2048, k=8, shared=4),
 }
 
 
