@@ -86,10 +86,17 @@ __device__ __forceinline__ void load_dests(const PermuteArgs& a, int64_t row, in
   }
 }
 
+// wpt warps share a row when rows are few: warp `part` covers columns
+// [part * span, +span) (span a multiple of 512).
 template <int kSrc, int kFmt, bool kTiled>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs a) {
+// (6 blocks per SM for 2-byte sources: 40 registers; fp32 sources hold
+// twice the raw vectors and are left at 5)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5 : 6)
+    k_permute_mx(PermuteArgs a, int wpt, int64_t span) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  const int gw = (int)blockIdx.x * kWarpsPerBlock + warp;  // n * wpt < 2^31 (checked at launch)
+  const int row = wpt == 1 ? gw : gw / wpt;
+  const int part = gw - row * wpt;
   if (row >= a.n) return;
   int32_t d0, d1;
   int ndest;
@@ -101,13 +108,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs 
   const int64_t groups4 = a.h / 128;
   // slice c0 = 512 columns (16 per lane); the next slice's loads are in
   // flight while this one is quantised and written to the K destinations
+  const int64_t cbeg = (int64_t)part * span;
+  const int64_t cend = cbeg + span < a.h ? cbeg + span : a.h;
   Raw16<kSrc> cur;
-  load_raw16<kSrc>(src_row, lane * 16, a.h, cur);
+  load_raw16<kSrc>(src_row, cbeg + lane * 16, a.h, cur);
   Raw16<kSrc> nxt = cur;
-  for (int64_t c0 = 0; c0 < a.h; c0 += 512) {
+  for (int64_t c0 = cbeg; c0 < cend; c0 += 512) {
     const int64_t col = c0 + lane * 16;
     const bool act = col < a.h;
-    if (c0 + 512 < a.h) load_raw16<kSrc>(src_row, col + 512, a.h, nxt);
+    if (c0 + 512 < cend) load_raw16<kSrc>(src_row, col + 512, a.h, nxt);
     float v[16];
     raw16_to_f32<kSrc>(cur, v);
     cur = nxt;
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_mx(PermuteArgs 
       }
     }
   }
-  if (!kTiled && groups < a.scale_cols) {  // zero padding columns of the row layout
+  if (!kTiled && groups < a.scale_cols && part == wpt - 1) {  // zero padding columns of the row layout
     for (int t = 0; t < ndest; ++t) {
       const int32_t d = dest_at(t, d0, d1);
       if (d < 0) continue;
@@ -250,11 +259,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
 }
 
 template <int kSrc, int kFmt>
-cudaError_t launch_mx_variant(const PermuteArgs& a, int blocks, cudaStream_t st) {
+cudaError_t launch_mx_variant(const PermuteArgs& a, int, cudaStream_t st) {
+  // few rows: split each row's 512-column slices over several warps so that
+  // about 64 warps per SM are busy
+  const int64_t slices = (a.h + 511) / 512;
+  int64_t wpt = (int64_t)num_sms() * 64 / a.n;
+  if (wpt < 1) wpt = 1;
+  if (wpt > slices) wpt = slices;
+  const int64_t span = ceil_div(slices, wpt) * 512;
+  wpt = ceil_div(a.h, span);
+  if (a.n * wpt > 0x7fffffff - kWarpsPerBlock) return cudaErrorInvalidValue;
+  const int64_t blocks = ceil_div(a.n * wpt, kWarpsPerBlock);
   if (a.scale_cols == 0)
-    k_permute_mx<kSrc, kFmt, true><<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
+    k_permute_mx<kSrc, kFmt, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, st>>>(a, (int)wpt, span);
   else
-    k_permute_mx<kSrc, kFmt, false><<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
+    k_permute_mx<kSrc, kFmt, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, st>>>(a, (int)wpt, span);
   return cudaGetLastError();
 }
 
