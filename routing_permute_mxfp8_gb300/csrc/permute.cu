@@ -260,10 +260,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
 
 template <int kSrc, int kFmt>
 cudaError_t launch_mx_variant(const PermuteArgs& a, int, cudaStream_t st) {
-  // few rows: split each row's 512-column slices over several warps so that
-  // about 64 warps per SM are busy
+  // split each row's 512-column slices over several warps until there are
+  // about 288 warps per SM (several waves of short warps balance better
+  // than one wave of whole rows)
   const int64_t slices = (a.h + 511) / 512;
-  int64_t wpt = (int64_t)num_sms() * 64 / a.n;
+  int64_t wpt = (int64_t)num_sms() * 288 / a.n;
   if (wpt < 1) wpt = 1;
   if (wpt > slices) wpt = slices;
   const int64_t span = ceil_div(slices, wpt) * 512;
