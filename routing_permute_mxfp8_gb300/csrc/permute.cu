@@ -168,10 +168,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5
   }
 }
 
-// Copy mode: 16-byte vectors of the row to each destination.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_copy(PermuteArgs a, int esz) {
+// Copy mode: 16-byte vectors of the row to each destination; like
+// k_permute_mx, wpt warps may share a row (bytes [part * span, +span)) and
+// the next 512-byte slice is loaded before the current one is stored.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    k_permute_copy(PermuteArgs a, int esz, int wpt, int64_t span) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  const int gw = (int)blockIdx.x * kWarpsPerBlock + warp;  // n * wpt < 2^31 (checked at launch)
+  const int row = wpt == 1 ? gw : gw / wpt;
+  const int part = gw - row * wpt;
   if (row >= a.n) return;
   int32_t d0, d1;
   int ndest;
@@ -179,14 +184,20 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_copy(PermuteArg
   const int64_t rb = a.h * esz;
   const char* src = static_cast<const char*>(a.src) + row * rb;
   char* out = static_cast<char*>(a.out);
-  for (int64_t off = (int64_t)lane * 16; off - lane * 16 < rb; off += 512) {
+  const int64_t bbeg = (int64_t)part * span;
+  const int64_t bend = bbeg + span < rb ? bbeg + span : rb;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 cur = bbeg + lane * 16 < rb ? __ldg(reinterpret_cast<const uint4*>(src + bbeg + lane * 16)) : zero;
+  uint4 nxt = cur;
+  for (int64_t off0 = bbeg; off0 < bend; off0 += 512) {
+    const int64_t off = off0 + lane * 16;
     const bool act = off < rb;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (act) v = __ldg(reinterpret_cast<const uint4*>(src + off));
+    if (off0 + 512 < bend) nxt = off + 512 < rb ? __ldg(reinterpret_cast<const uint4*>(src + off + 512)) : zero;
     for (int t = 0; t < ndest; ++t) {
       const int32_t d = dest_at(t, d0, d1);
-      if (d >= 0 && act) *reinterpret_cast<uint4*>(out + (int64_t)d * rb + off) = v;
+      if (d >= 0 && act) *reinterpret_cast<uint4*>(out + (int64_t)d * rb + off) = cur;
     }
+    cur = nxt;
   }
 }
 
@@ -299,7 +310,15 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
   }
   if (a.out_fmt < 0) {
     const int esz = a.src_dtype == MM_DT_FLOAT32 ? 4 : 2;
-    k_permute_copy<<<blocks, kWarpsPerBlock * 32, 0, st>>>(a, esz);
+    const int64_t rb = a.h * esz, slices = (rb + 511) / 512;
+    int64_t wpt = (int64_t)num_sms() * 288 / a.n;  // as in launch_mx_variant
+    if (wpt < 1) wpt = 1;
+    if (wpt > slices) wpt = slices;
+    const int64_t span = ceil_div(slices, wpt) * 512;
+    wpt = ceil_div(rb, span);
+    if (a.n * wpt > 0x7fffffff - kWarpsPerBlock) return cudaErrorInvalidValue;
+    k_permute_copy<<<(unsigned)ceil_div(a.n * wpt, kWarpsPerBlock), kWarpsPerBlock * 32, 0, st>>>(a, esz, (int)wpt,
+                                                                                               span);
     return cudaGetLastError();
   }
   if (a.src_dtype == MM_DT_BFLOAT16) return launch_mx_src<MM_DT_BFLOAT16>(a, blocks, st);
