@@ -18,18 +18,21 @@
 //                       stable order; it writes the inverse map and the
 //                       gather index directly.
 // No global atomics; the result is deterministic.
+#include <cooperative_groups.h>
+
 #include "mm_route.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace mm {
 
+// Phase 1, one warp per chunk: counts of each expert in chunk `unit`
+// (cnt: this warp's [E] shared-memory counters).
 template <typename IdT>
-__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
-                             int units, int32_t* __restrict__ hist, int32_t* dev_err) {
-  extern __shared__ int32_t sh_cnt[];  // [warps][E]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  const int unit = blockIdx.x * wpb + warp;
-  int32_t* cnt = sh_cnt + warp * num_experts;
+__device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                int chunk, int units, int unit, int32_t* cnt,
+                                                int32_t* __restrict__ hist, int32_t* dev_err) {
+  const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) cnt[e] = 0;
   __syncwarp();
   if (unit < units) {
@@ -49,7 +52,16 @@ __global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_
   }
 }
 
-// Exclusive scan of one value per thread across a 1024-thread block.
+template <typename IdT>
+__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+                             int units, int32_t* __restrict__ hist, int32_t* dev_err) {
+  extern __shared__ int32_t sh_cnt[];  // [warps][E]
+  const int warp = threadIdx.x >> 5;
+  route_hist_warp(ids, rows, num_experts, chunk, units, blockIdx.x * (blockDim.x >> 5) + warp,
+                  sh_cnt + warp * num_experts, hist, dev_err);
+}
+
+// Exclusive scan of one value per thread across the block (<= 1024 threads).
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* sh_warp, int64_t& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t x = v;
@@ -80,13 +92,11 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* sh_w
 
 constexpr int kMaxUnits = 512;  // chunks per call (route_plan keeps units <= kMaxUnits)
 
-// One warp per expert: exclusive prefix of its per-chunk counts, in place,
-// and the expert's total.
-__global__ void __launch_bounds__(1024) k_route_scan_experts(int32_t* __restrict__ hist, int num_experts, int units,
-                                                             int32_t* __restrict__ totals) {
+// Phase 2, one warp per expert: exclusive prefix of its per-chunk counts,
+// in place, and the expert's total.
+__device__ __forceinline__ void route_scan_expert_warp(int32_t* __restrict__ hist, int units, int e,
+                                                       int32_t* __restrict__ totals) {
   const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= num_experts) return;
   int32_t* row = hist + (int64_t)e * units;
   constexpr int kPer = kMaxUnits / 32;
   int32_t v[kPer];
@@ -112,8 +122,32 @@ __global__ void __launch_bounds__(1024) k_route_scan_experts(int32_t* __restrict
   if (lane == 0) totals[e] = run;
 }
 
-__global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
-  __shared__ int64_t sh_warp[33];
+// The same with one thread per expert, for few chunks (units <= 32).
+__device__ __forceinline__ void route_scan_expert_thread(int32_t* __restrict__ hist, int units, int e,
+                                                         int32_t* __restrict__ totals) {
+  int32_t* row = hist + (int64_t)e * units;
+  int32_t v[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) v[u] = u < units ? row[u] : 0;
+  int32_t run = 0;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    if (u >= units) break;
+    row[u] = run;
+    run += v[u];
+  }
+  totals[e] = run;
+}
+
+__global__ void __launch_bounds__(1024) k_route_scan_experts(int32_t* __restrict__ hist, int num_experts, int units,
+                                                             int32_t* __restrict__ totals) {
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e < num_experts) route_scan_expert_warp(hist, units, e, totals);
+}
+
+// Phase 3, one block: expert offsets, count / cumsum outputs, GEMM segment
+// table.
+__device__ __forceinline__ void route_scan_offsets_block(const RouteScanArgs& a, int64_t* sh_warp) {
   const int nt = blockDim.x;
   const int E = a.num_experts;
   // 1. exclusive scan of the expert totals -> offsets
@@ -161,18 +195,22 @@ __global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
+  __shared__ int64_t sh_warp[33];
+  route_scan_offsets_block(a, sh_warp);
+}
+
+// Phase 4, one warp per chunk, in index order (next: this warp's [E]
+// shared-memory slots).
 template <typename IdT>
-__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
-                                int units, const int32_t* __restrict__ bases,
-                                const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
-                                int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
-                                int32_t* __restrict__ pad_row) {
-  extern __shared__ int32_t sh_next[];  // [warps][E]: next free slot per expert
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  const int unit = blockIdx.x * wpb + warp;
-  if (unit >= units) return;
-  int32_t* next = sh_next + warp * num_experts;
+__device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                   int chunk, int units, int unit, int32_t* next,
+                                                   const int32_t* __restrict__ bases,
+                                                   const int32_t* __restrict__ offsets,
+                                                   const int32_t* __restrict__ seg_mprefix,
+                                                   int32_t* __restrict__ expanded_row_idx,
+                                                   int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row) {
+  const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
   __syncwarp();
   const int64_t start = (int64_t)unit * chunk;
@@ -205,6 +243,48 @@ __global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int n
   }
 }
 
+template <typename IdT>
+__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+                                int units, const int32_t* __restrict__ bases,
+                                const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
+                                int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
+                                int32_t* __restrict__ pad_row) {
+  extern __shared__ int32_t sh_next[];  // [warps][E]: next free slot per expert
+  const int warp = threadIdx.x >> 5;
+  const int unit = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (unit >= units) return;
+  route_scatter_warp(ids, rows, num_experts, chunk, units, unit, sh_next + warp * num_experts, bases, offsets,
+                     seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row);
+}
+
+// All four phases in one cooperative launch (every block resident), with
+// grid-wide barriers between them: one launch instead of four.
+template <typename IdT>
+__global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk, int units,
+                              int32_t* __restrict__ hist, RouteScanArgs sa, int32_t* __restrict__ expanded_row_idx,
+                              int32_t* __restrict__ pad_row, int32_t* dev_err) {
+  extern __shared__ int32_t sh_route[];  // [warps][E]
+  __shared__ int64_t sh_warp[33];
+  cg::grid_group grid = cg::this_grid();
+  const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  const int unit = blockIdx.x * wpb + warp;
+  int32_t* mine = sh_route + warp * num_experts;
+  if (unit < units) route_hist_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, dev_err);
+  grid.sync();
+  if (units <= 32) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < num_experts; e += gridDim.x * blockDim.x)
+      route_scan_expert_thread(hist, units, e, sa.totals);
+  } else {
+    for (int e = unit; e < num_experts; e += gridDim.x * wpb) route_scan_expert_warp(hist, units, e, sa.totals);
+  }
+  grid.sync();
+  if (blockIdx.x == 0) route_scan_offsets_block(sa, sh_warp);
+  grid.sync();
+  if (unit < units)
+    route_scatter_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
+                       expanded_row_idx, sa.sorted_row_idx, pad_row);
+}
+
 // ---------------------------------------------------------------------------
 RoutePlan route_plan(int64_t rows, int num_experts) {
   RoutePlan p;
@@ -226,24 +306,64 @@ size_t route_workspace_bytes(const RoutePlan& p) {
          (size_t)round_up((2 * (int64_t)p.num_experts + 1) * 4, 256);
 }
 
-cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
-                         RouteOutputs o, int32_t* dev_err, cudaStream_t st) {
+namespace {
+
+// Blocks of k_route_fused with `wpb` warps that can be resident at once
+// (0: no cooperative launch).  Queried once per block size with the largest
+// shared-memory table route_plan allows (40 KB), so it never overestimates.
+template <typename IdT>
+int fused_capacity(int wpb) {
+  static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (wpb < 1 || wpb > 8) return 0;
+  if (cap[wpb] < 0) {
+    int dev = 0, coop = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) coop = 0;
+    int c = 0;
+    if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused<IdT>, wpb * 32, 40960) ==
+                    cudaSuccess)
+      c = per_sm * num_sms();
+    cudaGetLastError();
+    cap[wpb] = c;
+  }
+  return cap[wpb];
+}
+
+template <typename IdT>
+cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist, RouteScanArgs a,
+                               const RouteOutputs& o, int32_t* dev_err, cudaStream_t st) {
   const int wpb = p.warps_per_block;
   const int blocks = (p.units + wpb - 1) / wpb;
   const size_t sh = (size_t)wpb * p.num_experts * sizeof(int32_t);
-  if (ids64)
-    k_route_hist<int64_t><<<blocks, wpb * 32, sh, st>>>((const int64_t*)ids, p.rows, p.num_experts, p.chunk,
-                                                         p.units, hist, dev_err);
-  else
-    k_route_hist<int32_t><<<blocks, wpb * 32, sh, st>>>((const int32_t*)ids, p.rows, p.num_experts, p.chunk,
-                                                         p.units, hist, dev_err);
-  // per-expert totals live right after the E + 1 offsets (the offsets
-  // buffer holds 2 * E + 1 entries)
-  int32_t* totals = offsets + p.num_experts + 1;
-  k_route_scan_experts<<<(p.num_experts + 31) / 32, 1024, 0, st>>>(hist, p.num_experts, p.units, totals);
+  if (blocks <= fused_capacity<IdT>(wpb)) {
+    int64_t rows = p.rows;
+    int ne = p.num_experts, chunk = p.chunk, units = p.units;
+    int32_t* exp_idx = o.expanded_row_idx;
+    int32_t* pad = o.pad_row;
+    void* args[] = {(void*)&ids, &rows, &ne, &chunk, &units, &hist, &a, &exp_idx, &pad, &dev_err};
+    if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
+        cudaSuccess)
+      return cudaSuccess;
+    cudaGetLastError();  // not launched (e.g. no cooperative launch here): the four kernels below
+  }
+  k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, dev_err);
+  k_route_scan_experts<<<(p.num_experts + 31) / 32, 1024, 0, st>>>(hist, p.num_experts, p.units, a.totals);
+  k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
+  k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, a.offsets,
+                                                     o.seg_mprefix, o.expanded_row_idx, o.sorted_row_idx,
+                                                     o.pad_row);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
+                         RouteOutputs o, int32_t* dev_err, cudaStream_t st) {
   RouteScanArgs a;
   a.hist = hist;
-  a.totals = totals;
+  // per-expert totals live right after the E + 1 offsets (the offsets
+  // buffer holds 2 * E + 1 entries)
+  a.totals = offsets + p.num_experts + 1;
   a.num_experts = p.num_experts;
   a.units = p.units;
   a.rows = p.rows;
@@ -256,16 +376,8 @@ cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_
   a.seg_mprefix = o.seg_mprefix;
   a.n_shared = o.n_shared;
   a.shared_rows = o.shared_rows;
-  k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
-  if (ids64)
-    k_route_scatter<int64_t><<<blocks, wpb * 32, sh, st>>>((const int64_t*)ids, p.rows, p.num_experts,
-                                                            p.chunk, p.units, hist, offsets, o.seg_mprefix,
-                                                            o.expanded_row_idx, o.sorted_row_idx, o.pad_row);
-  else
-    k_route_scatter<int32_t><<<blocks, wpb * 32, sh, st>>>((const int32_t*)ids, p.rows, p.num_experts,
-                                                            p.chunk, p.units, hist, offsets, o.seg_mprefix,
-                                                            o.expanded_row_idx, o.sorted_row_idx, o.pad_row);
-  return cudaGetLastError();
+  if (ids64) return launch_route_typed(p, static_cast<const int64_t*>(ids), hist, a, o, dev_err, st);
+  return launch_route_typed(p, static_cast<const int32_t*>(ids), hist, a, o, dev_err, st);
 }
 
 }  // namespace mm
