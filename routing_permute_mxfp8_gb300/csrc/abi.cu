@@ -322,8 +322,9 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   o.expert_tokens = expert_tokens;
   o.tokens_cumsum = expert_tokens_num_type == 0;
   StageScope sr(MM_STAGE_ROUTE, st);
-  cudaError_t e = launch_route(plan, expert_idx, false, w.hist, w.offsets, o, dev_err, st);
-  sr.finish(3);
+  int nl = 0;
+  cudaError_t e = launch_route(plan, expert_idx, false, w.hist, w.offsets, o, dev_err, st, &nl);
+  sr.finish(nl);
   if (e != cudaSuccess) return MM_ERR_CUDA;
   PermuteArgs a = {};
   a.src = x;
@@ -392,8 +393,10 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
   RouteOutputs o;
   o.expanded_row_idx = sorted_indices;
   StageScope sr(MM_STAGE_ROUTE, st);
-  cudaError_t e = launch_route(plan, indices, indices_dtype == MM_DT_INT64, w.hist, w.offsets, o, dev_err, st);
-  sr.finish(3);
+  int nl = 0;
+  cudaError_t e =
+      launch_route(plan, indices, indices_dtype == MM_DT_INT64, w.hist, w.offsets, o, dev_err, st, &nl);
+  sr.finish(nl);
   if (e != cudaSuccess) return MM_ERR_CUDA;
   if (m == 0) return MM_OK;
   PermuteArgs a = {};
@@ -518,8 +521,9 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   o.n_shared = (int)d.s;
   o.shared_rows = (int)d.bs;
   StageScope sr(MM_STAGE_ROUTE, st);
-  e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st);
-  sr.finish(3);
+  int nl = 0;
+  e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st, &nl);
+  sr.finish(nl);
   if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 2. dispatch: MX quantisation of each token, stored at its K expert rows

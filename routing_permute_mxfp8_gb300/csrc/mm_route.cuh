@@ -46,8 +46,10 @@ RoutePlan route_plan(int64_t rows, int num_experts);
 size_t route_workspace_bytes(const RoutePlan& p);
 // hist: [E * units] int32, offsets: [2 * E + 1] int32 (offsets, then
 // per-expert totals; both workspace)
+// *launches (optional) receives the number of kernels launched: 1 (one
+// cooperative launch) or 4.
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
-                         RouteOutputs o, int32_t* dev_err, cudaStream_t st);
+                         RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches = nullptr);
 
 // ---- permute / quantise (permute.cu) -------------------------------------
 struct PermuteArgs {

@@ -331,7 +331,7 @@ int fused_capacity(int wpb) {
 
 template <typename IdT>
 cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist, RouteScanArgs a,
-                               const RouteOutputs& o, int32_t* dev_err, cudaStream_t st) {
+                               const RouteOutputs& o, int32_t* dev_err, cudaStream_t st, int& launches) {
   const int wpb = p.warps_per_block;
   const int blocks = (p.units + wpb - 1) / wpb;
   const size_t sh = (size_t)wpb * p.num_experts * sizeof(int32_t);
@@ -342,8 +342,10 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     int32_t* pad = o.pad_row;
     void* args[] = {(void*)&ids, &rows, &ne, &chunk, &units, &hist, &a, &exp_idx, &pad, &dev_err};
     if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
-        cudaSuccess)
+        cudaSuccess) {
+      launches = 1;
       return cudaSuccess;
+    }
     cudaGetLastError();  // not launched (e.g. no cooperative launch here): the four kernels below
   }
   k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, dev_err);
@@ -352,13 +354,15 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
   k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, a.offsets,
                                                      o.seg_mprefix, o.expanded_row_idx, o.sorted_row_idx,
                                                      o.pad_row);
+  launches = 4;
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
-                         RouteOutputs o, int32_t* dev_err, cudaStream_t st) {
+                         RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches) {
+  int n = 0;
   RouteScanArgs a;
   a.hist = hist;
   // per-expert totals live right after the E + 1 offsets (the offsets
@@ -376,8 +380,10 @@ cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_
   a.seg_mprefix = o.seg_mprefix;
   a.n_shared = o.n_shared;
   a.shared_rows = o.shared_rows;
-  if (ids64) return launch_route_typed(p, static_cast<const int64_t*>(ids), hist, a, o, dev_err, st);
-  return launch_route_typed(p, static_cast<const int32_t*>(ids), hist, a, o, dev_err, st);
+  const cudaError_t e = ids64 ? launch_route_typed(p, static_cast<const int64_t*>(ids), hist, a, o, dev_err, st, n)
+                              : launch_route_typed(p, static_cast<const int32_t*>(ids), hist, a, o, dev_err, st, n);
+  if (launches) *launches = n;
+  return e;
 }
 
 }  // namespace mm
