@@ -17,6 +17,9 @@
 //                       popc for ties inside a 32-wide step), which is the
 //                       stable order; it writes the inverse map and the
 //                       gather index directly.
+// k_route_fused runs the four phases in one cooperative launch, with a
+// grid-wide barrier between phases; the four kernels remain for when its
+// blocks cannot all be resident.
 // No global atomics; the result is deterministic.
 #include <cooperative_groups.h>
 
