@@ -68,6 +68,18 @@ def _ids(n, e, k, kind, seed):
     return rng.integers(0, e, (n, k)).astype(np.int32)
 
 
+def _random_route_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    e = int(rng.integers(1, 600))
+    return (int(rng.integers(1, 5000)), 16 * int(rng.integers(1, 80)), e, int(rng.integers(1, min(e, 16) + 1)),
+            int(rng.choice([-1, 2, 3])), str(rng.choice(["distinct", "any"])))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_init_routing_random_shapes(seed):
+    test_init_routing_bit_exact(*_random_route_case(seed))
+
+
 @pytest.mark.parametrize("n,h,e,k,quant,kind", ROUTE_CASES)
 def test_init_routing_bit_exact(n, h, e, k, quant, kind):
     cfg = synth.CONFIGS["routing"].scaled(n=n, h=h, e=e, k=k)
@@ -328,6 +340,31 @@ MEGA_CASES = {
     "topk32_shared4": dict(n=96, h=256, inter=128, e=64, k=32, shared=4),
     "max_experts": dict(n=256, h=256, inter=128, e=2048, k=8, shared=4),
 }
+
+
+def _random_mega_cfg(seed):
+    """A seeded random MegaMoE problem: shapes, routing, formats, shared
+    experts and activation drawn independently (sizes small enough for the
+    oracle to finish in seconds, large enough for several tiles)."""
+    rng = np.random.default_rng(1000 + seed)
+    e = int(rng.choice([1, 3, 8, 17, 40, 64]))
+    k = int(rng.integers(1, min(e, 8) + 1))
+    act = str(rng.choice(["swiglu", "swiglu", "swigluoai", "situglu", "swiglustep", "gelu"]))
+    params = {"swiglu": (), "swigluoai": (), "situglu": (0.7,), "swiglustep": (0.5,),
+              "gelu": (float(np.finfo(np.float32).max),)}[act]
+    return synth.CONFIGS["tiny"].scaled(
+        n=int(rng.integers(1, 400)), h=128 * int(rng.integers(1, 9)), inter=128 * int(rng.integers(1, 5)), e=e, k=k,
+        routing=str(rng.choice(["uniform", "zipf"])), dispatch_fmt=int(rng.choice([23, 24])),
+        weight_fmt=int(rng.choice([23, 24, 296])), gate_dtype=str(rng.choice(["fp32", "bf16"])),
+        shared=int(rng.integers(0, 3)), activation=act, act_params=params, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_mega_moe_random_shapes(seed):
+    cfg = _random_mega_cfg(seed)
+    if cfg.weight_fmt == 296:
+        cfg = cfg.scaled(dispatch_fmt=24 if seed % 2 else 23)
+    run_mega(cfg)
 
 
 @pytest.mark.parametrize("case", list(MEGA_CASES))
