@@ -109,8 +109,8 @@ def test_init_routing_bit_exact(n, h, e, k, quant, kind):
     (torch.bfloat16, False, 0, 9, False),      # MXFP4 E2M1 (the article's quant_mode 9)
     (torch.float16, True, -7, 9, False),
 ])
-def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d):
-    n, h, e, k = 700, 256, 16, 1 if one_d else 4
+def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d, shape=None):
+    n, h, e, k = shape if shape else (700, 256, 16, 1 if one_d else 4)
     rng = np.random.default_rng(9)
     xf = rng.standard_normal((n, h)).astype(np.float32)
     xt = torch.from_numpy(xf).to(dtype)
@@ -134,6 +134,20 @@ def test_token_permute_bit_exact(dtype, idx64, num_out, quant, one_d):
     assert np.array_equal(got.view(r_out.dtype) if fmt < 0 else got, r_out)
     if quant != -1:
         assert np.array_equal(host(sc).reshape(m, -1), r_sc)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_token_permute_random_shapes(seed):
+    rng = np.random.default_rng(3000 + seed)
+    one_d = bool(rng.integers(0, 2))
+    e = int(rng.integers(1, 300))
+    k = 1 if one_d else int(rng.integers(1, min(e, 12) + 1))
+    n = int(rng.integers(1, 3000))
+    quant = int(rng.choice([-1, 2, 3, 9]))
+    dtype = [torch.bfloat16, torch.float16, torch.float32][int(rng.integers(0, 2 if quant != -1 else 3))]
+    h = 32 * int(rng.integers(1, 40)) if quant == 9 else 16 * int(rng.integers(1, 80))
+    num_out = [None, 0, int(rng.integers(1, 2 * n * k)), -int(rng.integers(0, n * k + 5))][int(rng.integers(0, 4))]
+    test_token_permute_bit_exact(dtype, bool(rng.integers(0, 2)), num_out, quant, one_d, shape=(n, h, e, k))
 
 
 def test_out_of_range_ids_are_left_out_and_flagged():
