@@ -285,6 +285,20 @@ mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t c
                          uint8_t* q, uint8_t* scales, int64_t scale_cols, void* stream);
 
 /* ------------------------------------------------------------------------
+ * mm_selftest_wait_timeout -- exercises the failure path of the kernels'
+ * bounded waits.  The operator pages have no counterpart; it exists so that
+ * a caller (and the tests) can check, without any fault, that a wait which
+ * never completes ends: one CTA waits on an mbarrier that nothing arrives at,
+ * gives up after limit_ns nanoseconds of %globaltimer time (the GEMM kernels
+ * use the same wait with a 2 s limit), OR-s MM_DEVERR_TIMEOUT into *dev_err
+ * and returns; the context stays usable.
+ *
+ * limit_ns   in (0, 10 s]; dev_err: device int32, required.  Asynchronous on
+ * stream; MM_ERR_INVALID_ARG for a bad limit or a null dev_err.
+ * ---------------------------------------------------------------------- */
+mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * mm_moe_init_routing_noalloc -- the same routing and permute as
  * mm_moe_init_routing (same arguments and outputs), for callers that cannot
  * give the library device scratch memory: for example a host program or

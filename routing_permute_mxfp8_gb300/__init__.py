@@ -69,9 +69,11 @@ def load():
     L.mm_prepared_weight_scales_size.argtypes = [i32, i64, i64, i64, psz]
     L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
     L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
+    L.mm_selftest_wait_timeout.argtypes = [i64, p, p]
     for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
                  "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
-                 "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize"):
+                 "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize",
+                 "mm_selftest_wait_timeout"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -274,6 +276,15 @@ def mm_prepare_weight_scales(scales, k_red: int, which: int):
     _check(L.mm_prepare_weight_scales(_ptr(scales), which, e, n_out, k_red, _ptr(dst), _stream(scales.device)),
            "mm_prepare_weight_scales")
     return dst
+
+
+def mm_selftest_wait_timeout(limit_ns: int, dev_err):
+    """One CTA waits, with a limit of limit_ns, on an mbarrier that nothing
+    completes (the kernels' bounded-wait failure path): MM_DEVERR_TIMEOUT is
+    OR-ed into dev_err (a device int32 tensor) and the context stays usable."""
+    _need_cuda(dev_err)
+    _check(load().mm_selftest_wait_timeout(int(limit_ns), _ptr(dev_err), _stream(dev_err.device)),
+           "mm_selftest_wait_timeout")
 
 
 def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None = None):

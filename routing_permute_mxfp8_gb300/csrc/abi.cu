@@ -640,6 +640,12 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
 }
 
 // ------------------------------------------------------------------------
+mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 10000000000ll || !dev_err) return MM_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait_timeout((uint64_t)limit_ns, dev_err, static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------------
 mm_status mm_prepared_weight_scales_size(int which, int64_t experts, int64_t n_out, int64_t k_red,
                                          size_t* bytes) {
   if (!bytes || (which != 1 && which != 2) || experts <= 0 || n_out <= 0 || k_red <= 0 || k_red % 128 != 0)

@@ -62,14 +62,26 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with `parity` of an mbarrier, giving up after
+// limit_ns of %globaltimer time (false: the caller raises MM_DEVERR_TIMEOUT).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
+}
+
+// Self-test of the failure path: one thread waits on a barrier that nothing
+// arrives at, with the same bounded wait as the GEMM's pipeline.
+__global__ void k_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!wait_bounded(&bar, 0, limit_ns)) raise_err(dev_err, MM_DEVERR_TIMEOUT);
 }
 
 struct GemmArgs {
@@ -640,6 +652,11 @@ int gemm_tile_n(int mode, int64_t n_out) {
   (void)mode;
   (void)n_out;
   return 256;
+}
+
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, cudaStream_t st) {
+  k_selftest_wait_timeout<<<1, 32, 0, st>>>(limit_ns, dev_err);
+  return cudaGetLastError();
 }
 
 int num_sms() {

@@ -136,5 +136,8 @@ struct UnpadArgs {
 cudaError_t launch_unpad(const UnpadArgs& a, cudaStream_t st);
 
 int num_sms();
+// one CTA waits on an mbarrier that nothing completes, gives up after
+// limit_ns and raises MM_DEVERR_TIMEOUT (the bounded-wait failure path)
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, cudaStream_t st);
 
 }  // namespace mm

@@ -85,6 +85,12 @@ def _mega(lib, **kw):
                            a["wsb"], vp(a["err"]), a["stream"])
 
 
+def test_selftest_wait_timeout_host_validation(lib):
+    assert lib.mm_selftest_wait_timeout(0, ctypes.c_void_p(16), None) == 1             # limit must be > 0
+    assert lib.mm_selftest_wait_timeout(20_000_000_000, ctypes.c_void_p(16), None) == 1  # at most 10 s
+    assert lib.mm_selftest_wait_timeout(1_000_000, None, None) == 1                    # dev_err required
+
+
 def test_mega_moe_host_rejections(lib):
     assert _mega(lib, ep=2) == 2                     # ep_world_size != 1
     assert _mega(lib, cqm=3) == 2                    # combine quantisation

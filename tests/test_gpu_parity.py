@@ -188,6 +188,21 @@ def test_empty_batch_writes_zero_counts(ttype):
     assert np.array_equal(host(cnt), np.zeros(e, np.int32))
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """A wait that nothing completes ends after its limit with
+    MM_DEVERR_TIMEOUT set, without a fault; the next MegaMoE call is exact."""
+    err = zeros_err()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    mm.mm_selftest_wait_timeout(20_000_000, err)  # 20 ms
+    e1.record()
+    torch.cuda.synchronize()
+    assert host(err)[0] & 4
+    assert 19.0 <= e0.elapsed_time(e1) < 1000.0
+    run_mega(synth.CONFIGS["tiny"])
+
+
 # ---------------------------------------------------------------- MX quantiser
 def pack_fp4(codes):
     """Oracle FP4 codes (one per byte) -> the library's packed bytes (element
