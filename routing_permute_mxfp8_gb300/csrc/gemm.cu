@@ -2,11 +2,13 @@
 //
 // MegaMoE README, A8W8-FP scenario:
 //   stage 2  G_e, U_e = DQ_MX(X_hat_e) . DQ_MX(W1_e^(G|U))   then
-//            A_e = SiLU(G_e) * U_e (swiglu, "Activation function formulas"),
+//            A_e = SiLU(G_e) * U_e (swiglu, or another activation of
+//            "Activation function formulas"; gelu acts on all 2I columns),
 //            A_hat_e, S_A,e = Q_MX(A_e) in the dispatch FP8 type
 //   stage 3  O_e = DQ_MX(A_hat_e) . DQ_MX(W2_e)
 // DQ_MX happens inside the MMA: tcgen05.mma kind::mxf8f6f4 with one E8M0
-// scale per 32 k for every row of A and of B (scale_vec::1X).
+// scale per 32 k for every row of A and of B (scale_vec::1X).  Weights are
+// FP8 (A8W8-FP) or packed FP4 E2M1 (A8W4-FP), which TMA expands on load.
 //
 // Layout.  The expanded rows of every expert (and of each shared expert,
 // which sees all tokens) form a segment padded to a multiple of 128 rows,
@@ -50,6 +52,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOStageBytes = 32 * 64;  // one 32 x 32 bf16 block of O
+constexpr int kTileN = 256;                  // output columns per tile (GEMM1: 128 gate + 128 up)
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 #ifndef MM_BIG_MTILES
 #define MM_BIG_MTILES 2
@@ -647,12 +650,6 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
 
 }  // namespace
 
-// Tile width of both GEMMs: 256 output columns (GEMM1: 128 gate + 128 up).
-int gemm_tile_n(int mode, int64_t n_out) {
-  (void)mode;
-  (void)n_out;
-  return 256;
-}
 
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, cudaStream_t st) {
   k_selftest_wait_timeout<<<1, 32, 0, st>>>(limit_ns, dev_err);
@@ -671,7 +668,7 @@ int num_sms() {
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   const int nseg = L.n_routed + L.n_shared;
-  const int bn = gemm_tile_n(L.mode, L.N);
+  const int bn = kTileN;
   const bool pair_map = L.mode == 1 && L.act != MM_ACT_GELU;
   auto map_b = [&](CUtensorMap* m, const void* p, int64_t experts, int fmt) {
     const bool fp4 = fmt == MM_DT_FP4_E2M1;

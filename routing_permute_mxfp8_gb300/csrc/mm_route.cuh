@@ -105,8 +105,6 @@ struct GemmLaunch {
   int32_t* dev_err;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
-// tile width the GEMM of `mode` uses for n_out output columns
-int gemm_tile_n(int mode, int64_t n_out);
 
 // ---- combine (combine.cu) --------------------------------------------------
 struct CombineArgs {
