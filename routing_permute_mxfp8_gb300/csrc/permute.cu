@@ -6,8 +6,9 @@
 // MXFP8 modes every group of 32 consecutive elements shares one E8M0
 // exponent (MegaMoE README, A8W8-FP stage 1, Q_MX).
 //
-// The gather is turned around: one warp owns one source token, reads its
-// row once, quantises it once and stores the result at each of its K
+// The gather is turned around: one warp owns one source token (or a span of
+// its 512-column slices, when tokens are too few to fill the GPU), reads
+// its row once, quantises it once and stores the result at each of its K
 // destinations (16-byte stores; one lane holds 16 consecutive elements, so
 // a 32-element group is two lanes and its amax takes one shuffle).
 #include "mm_route.cuh"
