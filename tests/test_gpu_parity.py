@@ -393,7 +393,7 @@ def test_mega_moe_random_shapes(seed):
     cfg = _random_mega_cfg(seed)
     if cfg.weight_fmt == 296:
         cfg = cfg.scaled(dispatch_fmt=24 if seed % 2 else 23)
-    run_mega(cfg)
+    run_mega(cfg, layout=seed % 2)  # odd seeds: weight scales prepared once (mm_prepare_weight_scales)
 
 
 @pytest.mark.parametrize("case", list(MEGA_CASES))
@@ -426,8 +426,16 @@ def test_mega_moe_prequant_passthrough():
     check_y(synth.bf16_bits_to_f32(host(y1).view(np.uint16)), y_ref)
 
 
-def test_mega_moe_prepared_scales_identical():
-    cfg = synth.CONFIGS["tiny"].scaled(shared=1, n=96)
+@pytest.mark.parametrize("kw", [
+    dict(shared=1, n=96),
+    # gelu reads W1's scale tiles block by block; with I / 128 odd, one GEMM1
+    # tile's two blocks straddle the last gate pair and the first up pair
+    dict(shared=1, n=96, inter=384, activation="gelu", act_params=(float(np.finfo(np.float32).max),)),
+    dict(n=128, inter=384, activation="gelu", act_params=(float(np.finfo(np.float32).max),), weight_fmt=296,
+         dispatch_fmt=24),
+], ids=["swiglu", "gelu_odd_pairs", "gelu_a8w4_odd_pairs"])
+def test_mega_moe_prepared_scales_identical(kw):
+    cfg = synth.CONFIGS["tiny"].scaled(**kw)
     _, y0 = run_mega(cfg, layout=0)
     _, y1 = run_mega(cfg, layout=1)
     assert np.array_equal(y0, y1)
