@@ -426,6 +426,27 @@ def test_mega_moe_prequant_passthrough():
     check_y(synth.bf16_bits_to_f32(host(y1).view(np.uint16)), y_ref)
 
 
+@pytest.mark.parametrize("routed_fmt,shared_fmt", [(296, 24), (24, 296), (23, 24)])
+def test_mega_moe_shared_weight_type_differs(routed_fmt, shared_fmt):
+    """Routed and shared experts with different weight types (the shared
+    expert's own MMA format), e.g. FP4 routed experts beside an FP8 shared one."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=128, e=8, k=4, shared=2, weight_fmt=routed_fmt, dispatch_fmt=24)
+    cfg_sh = cfg.scaled(weight_fmt=shared_fmt)
+    x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    sh = _weights(cfg_sh, shared=True)
+    err = zeros_err()
+    y, counts = mm.mm_mega_moe(
+        bf16(x), t(ids), t(gate), gpu_codes(w1, routed_fmt), gpu_codes(w2, routed_fmt), t(s1), t(s2), cfg.e,
+        weight_dtype=routed_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err,
+        shared_weight1=gpu_codes(sh[0], shared_fmt), shared_weight_scales1=t(sh[1]),
+        shared_weight2=gpu_codes(sh[2], shared_fmt), shared_weight_scales2=t(sh[3]), shared_weight_dtype=shared_fmt)
+    assert host(err)[0] == 0
+    y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, routed_fmt, shared=sh,
+                                      shared_w_fmt=shared_fmt)
+    check_y(synth.bf16_bits_to_f32(host(y).view(np.uint16)), y_ref)
+
+
 @pytest.mark.parametrize("kw", [
     dict(shared=1, n=96),
     # gelu reads W1's scale tiles block by block; with I / 128 odd, one GEMM1
