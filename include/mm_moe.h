@@ -187,6 +187,9 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    (the pages' scales input, (BS, CeilDiv(H, 32))); NULL
  *                    otherwise.
  * topk_ids           [bs, k] int32, distinct per token, in [0, moe_expert_num).
+ *                    An id outside that range raises MM_DEVERR_EXPERT_RANGE and
+ *                    its (token, k) term is left out of Y (and of the counts);
+ *                    a repeated id raises MM_DEVERR_DUPLICATE_ID.
  * topk_weights       [bs, k], topk_weights_dtype MM_DT_FLOAT32 or MM_DT_BFLOAT16.
  * weight1            [E, 2*intermediate, h] FP8 (weight_dtype 23 / 24), or
  *                    FLOAT4_E2M1 (weight_dtype 296, the A8W4-FP scenario:

@@ -502,6 +502,33 @@ def test_mega_moe_dsv3_decode_gelu_full_size():
     run_mega(cfg, tokens=np.array([0, 31, 64, 127]), layout=1, sparse=True)
 
 
+def test_mega_moe_out_of_range_ids_left_out():
+    """An id outside [0, E) is flagged and its term leaves Y: the reference
+    gives that term weight 0 (on a valid, unused expert) in the oracle."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1)
+    x, gate = synth.tokens_bf16(cfg), synth.topk_weights(cfg)
+    ids = synth.topk_ids(cfg)
+    bad = [(5, 1, cfg.e), (7, 0, -1), (40, 1, 1 << 20)]
+    ids_ref, gate_ref = ids.copy(), gate.copy()
+    for i, kk, v in bad:
+        ids[i, kk] = v
+        ids_ref[i, kk] = next(e for e in range(cfg.e) if e not in ids_ref[i])
+        gate_ref[i, kk] = 0.0
+    w1, s1, w2, s2 = _weights(cfg)
+    sh = _weights(cfg, shared=True)
+    err = zeros_err()
+    y, counts = mm.mm_mega_moe(bf16(x), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err,
+                               shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]), shared_weight2=t(sh[2]),
+                               shared_weight_scales2=t(sh[3]))
+    assert host(err)[0] & 1
+    _, _, r_cnt, n_bad = oracle.route(ids, cfg.e)
+    assert n_bad == len(bad)
+    assert np.array_equal(host(counts), r_cnt.astype(np.int32))
+    y_ref, _ = oracle.mega_moe_tokens(x, ids_ref, gate_ref, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt,
+                                      shared=sh)
+    check_y(synth.bf16_bits_to_f32(host(y).view(np.uint16)), y_ref)
+
+
 def test_mega_moe_duplicate_ids_flagged():
     cfg = synth.CONFIGS["tiny"]
     x = synth.tokens_bf16(cfg)
