@@ -250,7 +250,7 @@ def test_permute_matches_gather(fmt):
 
 
 # ---------------------------------------------------------------- expert FFN
-def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None):
+def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
     """Grouped-by-expert FFN with numpy matmuls on dequantised operands, from
     the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort."""
     (w1, s1, w2, s2) = w
@@ -290,7 +290,8 @@ def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None):
         y += gw[:, kk:kk + 1] * o_all[pos.reshape(n, k)[:, kk]]
     if shared is not None:
         for s in range(shared[0].shape[0]):
-            _, o = ffn(xq, xs, shared[0][s], shared[1][s], shared[2][s], shared[3][s], cfg.weight_fmt)
+            _, o = ffn(xq, xs, shared[0][s], shared[1][s], shared[2][s], shared[3][s],
+                       cfg.weight_fmt if shared_fmt is None else shared_fmt)
             y += o
     return y, aq_all[pos.reshape(n, k)]
 
@@ -328,6 +329,19 @@ def test_mega_moe_matches_numpy_grouped(name, kw):
     want_b = torch.from_numpy(y_ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
     got_b = P.bf16_bits_to_f64(yb)
     assert np.max(np.abs(got_b - want_b)) <= 2.0 ** -8 * np.abs(want_b).max()
+
+
+@pytest.mark.parametrize("routed,shared_fmt", [(P.E2M1, P.E4M3), (P.E4M3, P.E2M1), (P.E5M2, P.E4M3)])
+def test_mega_moe_shared_weight_type_matches_numpy(routed, shared_fmt):
+    """Shared experts whose weight type differs from the routed experts'."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=2, weight_fmt=routed, dispatch_fmt=P.E4M3)
+    x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
+    w = _weights(cfg)
+    sh = _weights(cfg.scaled(weight_fmt=shared_fmt), shared=True)
+    y, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
+                                  shared_w_fmt=shared_fmt)
+    y_ref, _ = _numpy_grouped_moe(cfg, x, ids, gate, w, shared=sh, shared_fmt=shared_fmt)
+    assert np.max(np.abs(y - y_ref)) <= 1e-11 * np.abs(y_ref).max()
 
 
 def test_mega_moe_metamorphic():
