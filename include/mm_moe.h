@@ -221,6 +221,9 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    A_hat has 2*intermediate columns.  Bad parameter lists
  *                    give MM_ERR_INVALID_ARG, other names MM_ERR_UNSUPPORTED.
  * y                  [bs, h] bf16 output.
+ * The call may be captured in a CUDA graph on `stream` (its kernels are
+ * ordinary launches while the stream is capturing); the workspace and the
+ * outputs then belong to the graph's replays.
  * expert_token_nums  [E] int32 output (rows per expert), or NULL.  With
  *                    bs = 0 only this is written (all zeros).
  * expanded_row_idx   [bs*k] int32 output pi(i, k) (position of row j = i*k+k'

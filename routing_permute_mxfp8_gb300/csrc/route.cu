@@ -338,7 +338,14 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
   const int wpb = p.warps_per_block;
   const int blocks = (p.units + wpb - 1) / wpb;
   const size_t sh = (size_t)wpb * p.num_experts * sizeof(int32_t);
-  if (blocks <= fused_capacity<IdT>(wpb)) {
+  // under stream capture the four ordinary launches are used: a refused
+  // cooperative launch there would invalidate the caller's capture
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;
+  }
+  if (cap == cudaStreamCaptureStatusNone && blocks <= fused_capacity<IdT>(wpb)) {
     int64_t rows = p.rows;
     int ne = p.num_experts, chunk = p.chunk, units = p.units;
     int32_t* exp_idx = o.expanded_row_idx;

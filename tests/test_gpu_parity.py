@@ -502,6 +502,34 @@ def test_mega_moe_dsv3_decode_gelu_full_size():
     run_mega(cfg, tokens=np.array([0, 31, 64, 127]), layout=1, sparse=True)
 
 
+def test_mega_moe_in_cuda_graph():
+    """The whole call captured in a CUDA graph (caller's workspace and
+    output; routing then takes its ordinary launches) replays to the same Y
+    bits as a direct call, and matches the oracle."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1)
+    x, ids, gate = bf16(synth.tokens_bf16(cfg)), t(synth.topk_ids(cfg)), t(synth.topk_weights(cfg))
+    w1, s1, w2, s2 = (t(a) for a in _weights(cfg))
+    sh = [t(a) for a in _weights(cfg, shared=True)]
+    kw = dict(shared_weight1=sh[0], shared_weight_scales1=sh[1], shared_weight2=sh[2], shared_weight_scales2=sh[3])
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(cfg.n, cfg.h, cfg.k, cfg.e, cfg.inter, cfg.shared, 0),
+                     dtype=torch.uint8, device=DEV)
+    y = torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device=DEV)
+    y0 = mm.mm_mega_moe(x, ids, gate, w1, w2, s1, s2, cfg.e, workspace=ws, **kw)[0].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        mm.mm_mega_moe(x, ids, gate, w1, w2, s1, s2, cfg.e, workspace=ws, out=y, **kw)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    y.zero_()
+    with torch.cuda.graph(graph):
+        mm.mm_mega_moe(x, ids, gate, w1, w2, s1, s2, cfg.e, workspace=ws, out=y, **kw)
+    y.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host(y), host(y0))
+
+
 def test_mega_moe_out_of_range_ids_left_out():
     """An id outside [0, E) is flagged and its term leaves Y: the reference
     gives that term weight 0 (on a valid, unused expert) in the oracle."""
