@@ -321,6 +321,33 @@ def mega_call(mm, cfg, x, ids, gate, W, S, ws, y):
                           workspace=ws, out=y, **kw)
 
 
+def stage_rooflines(cfg, ms, hbm_peak, fp8_peak):
+    """Each stage of the step against the roofline that bounds it, from its
+    algorithmic work (inputs read once, outputs written once; FLOPs without
+    the padding rows) and its device time per step."""
+    rows = cfg.n * cfg.k + cfg.n * cfg.shared          # expanded rows, shared experts included
+    gate_b = 2 if cfg.gate_dtype == "bf16" else 4
+    out = {}
+
+    def hbm(name, nbytes):
+        if ms.get(name):
+            gbs = nbytes / (ms[name] / 1e3) / 1e9
+            out[name] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "algorithmic_bytes": nbytes, "ms": ms[name]}
+
+    # dispatch: x and the row indices read; FP8 rows and E8M0 scales written
+    hbm("dispatch", cfg.n * cfg.h * 2 + cfg.n * cfg.k * 4 + rows * cfg.h + rows * (cfg.h // 32))
+    # combine: O rows, gating weights and indices read; Y written
+    hbm("combine", rows * cfg.h * 2 + cfg.n * cfg.k * (gate_b + 4) + cfg.n * cfg.h * 2)
+    if ms.get("gemm2"):
+        tf = 2.0 * rows * cfg.h * cfg.act_width / (ms["gemm2"] / 1e3) / 1e12
+        out["gemm2"] = {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s",
+                        "frac": tf / fp8_peak, "ms": ms["gemm2"]}
+    if ms.get("route"):
+        out["route"] = {"bound": "latency", "us": ms["route"] * 1e3}
+    return out
+
+
 def ffn_flops(cfg, tokens=None):
     n = cfg.n if tokens is None else tokens
     rows = n * cfg.k + n * cfg.shared
@@ -493,6 +520,7 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": g1_flops, "avg_launch_ms": g1_ms}
     stage_ms = {k: (v[0] / max(1, v[1]) if v[1] else 0.0) for k, v in stages.items() if v[1]}
     per_step_stage_ms = {k: v[0] / args.steps for k, v in stages.items() if v[1]}
+    stage_roofline = stage_rooflines(cfg, per_step_stage_ms, hbm_peak, fp8_peak_sus)
 
     # end to end through the public call with host buffers
     e2e = None
@@ -518,6 +546,7 @@ def run_ours(args):
         "tflops": flops / (ms_step / 1e3) / 1e12,
         "tflops_frac_of_fp8_peak": flops / (ms_step / 1e3) / 1e12 / fp8_peak_sus,
         "roofline": roofline,
+        "stage_roofline": stage_roofline,
         "stage_ms_per_launch": stage_ms,
         "stage_ms_per_step": per_step_stage_ms,
         "gemm2_tflops": 2.0 * (cfg.n * cfg.k + cfg.n * cfg.shared) * cfg.h * cfg.inter / (g2_ms / 1e3) / 1e12,
