@@ -129,3 +129,23 @@ def test_permute_host_rejections(lib):
     assert call(idt=0) == 1          # indices dtype
     assert call(q=2, h=24) == 2      # H % 16 for MXFP8
     assert call() == 3               # workspace missing
+
+
+def test_binding_fails_loudly_without_its_library(monkeypatch, tmp_path):
+    """No fallback path: with the CUDA library absent the binding raises."""
+    monkeypatch.setattr(mm, "_LIB_PATH", str(tmp_path / "absent" / "libmm_moe.so"))
+    monkeypatch.setattr(mm, "_lib", None)
+    with pytest.raises(mm.MMError):
+        mm.load()
+
+
+def test_binding_refuses_host_tensors():
+    """The operations run only in the CUDA kernels: host (CPU) tensors are
+    rejected, never computed on the CPU."""
+    import torch
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    ids = torch.zeros((4, 2), dtype=torch.int32)
+    with pytest.raises(mm.MMError):
+        mm.mm_moe_init_routing(x, ids, 8)
+    with pytest.raises(mm.MMError):
+        mm.mm_moe_token_permute(x, ids, 8)
