@@ -482,3 +482,84 @@ def test_prequant_passthrough_equals_internal_quantisation():
     y1, _ = oracle.mega_moe_tokens(None, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
                                    x_prequant=(xq, xs))
     assert np.array_equal(y0, y1)
+
+
+# ------------------------------------------- gated activations, every branch
+def _gated_reference(g, u, act, params):
+    """The MegaMoE README's "Activation function formulas", written out in
+    numpy from the page (not from the oracle): sigma(z) = 1 / (1 + e^-z),
+    SiLU(z) = z sigma(z), G_c = min(G, c), U_c = clip(U, -c, c), the clamp c
+    +inf when not configured or 0; defaults from the activation_params row of
+    the parameter table: alpha 1.702 and beta 1.0 for swigluoai, beta 1.0 for
+    situglu, linear_beta not enabled."""
+    p = list(params)
+    c = np.inf
+    if act in ("swiglu", "swiglustep", "swigluoai") and p and p[0] != 0.0:
+        c = p[0]
+    gc, uc = np.minimum(g, c), np.clip(u, -c, c)
+    if act == "swiglu":
+        return gc * expit(gc) * uc
+    if act == "swiglustep":
+        return np.minimum(g * expit(g), c) * uc
+    if act == "swigluoai":
+        alpha, beta = (p[1], p[2]) if len(p) == 3 else (1.702, 1.0)
+        return gc * expit(alpha * gc) * (uc + beta)
+    assert act == "situglu"
+    beta = p[0] if p else 1.0
+    lin = u if len(p) < 2 else p[1] * np.tanh(u / p[1])
+    return beta * np.tanh(g / beta) * expit(g) * lin
+
+
+# parameter sets chosen so that each branch's terms matter at the data's
+# scale (|G|, |U| about 0.3 at scale shift 0 and about 2.5 at shift 3): the
+# clamp cuts inside the data, alpha and beta are away from 1 and 0 (and
+# negative), the situglu betas are small enough that tanh bends
+GATED_PIN_CASES = [
+    ("swiglustep", (0.3,)), ("swiglustep", (1.5,)), ("swiglustep", ()),
+    ("swigluoai", ()), ("swigluoai", (0.0, 0.5, -0.5)), ("swigluoai", (0.4, 1.702, 1.0)),
+    ("swigluoai", (2.0, 3.0, -0.5)), ("swigluoai", (0.0, 1.702, 1.0)),
+    ("situglu", ()), ("situglu", (0.5,)), ("situglu", (2.0,)), ("situglu", (0.5, 0.3)), ("situglu", (2.0, 4.0)),
+    ("swiglu", (0.3,)),
+]
+
+
+@pytest.mark.parametrize("shift", [0, 3])
+@pytest.mark.parametrize("act,params", GATED_PIN_CASES)
+def test_gated_activation_branches_match_the_formulas(act, params, shift):
+    """Every gated branch of the oracle against the page's formula evaluated
+    independently in numpy on the dequantised Linear1 output, for several
+    tokens of one expert: A rounded to fp32, then MX-quantised by the
+    brute-force quantiser; codes and scales must be identical.  The token
+    scales are raised by 2^shift (exact: E8M0 codes + shift) so both the small
+    and the saturating regimes of tanh, sigma and the clamp are reached."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=6)
+    x = synth.tokens_bf16(cfg)
+    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, cfg.dispatch_fmt)
+    xs = (xs.astype(np.int32) + shift).astype(np.uint8)
+    w1, s1 = oracle.quantized_weights(cfg, 1)
+    w2, s2 = oracle.quantized_weights(cfg, 2)
+    w1d = P.dequant_rows(w1[0], s1[0], cfg.weight_fmt)
+    mism = 0
+    for t in range(cfg.n):
+        xd = P.dequant_rows(xq[t][None], xs[t][None], cfg.dispatch_fmt)[0]
+        hv = w1d @ xd
+        g, u = hv[:cfg.inter], hv[cfg.inter:]
+        want = _gated_reference(g, u, act, params).astype(np.float32).astype(np.float64)
+        wq, ws = P.brute_mx_rows(want[None], cfg.dispatch_fmt)
+        aq, a_s, _ = oracle.expert_row(xq[t], xs[t], cfg.dispatch_fmt, w1[0], s1[0], w2[0], s2[0],
+                                       cfg.weight_fmt, cfg.dispatch_fmt, activation=act, act_params=params)
+        assert np.array_equal(a_s, ws[0]), (act, params, t)
+        mism += int(np.count_nonzero(aq != wq[0]))
+    assert mism == 0, (act, params, mism)
+
+
+def test_gated_activation_defaults_are_the_parameter_table_values():
+    """activation_params = [] means: no clamp, swigluoai alpha 1.702 and beta
+    1.0, situglu beta 1.0 without linear_beta (parameter table).  The empty
+    list must equal the explicit list of those values."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=1)
+    fmax = float(np.finfo(np.float32).max)
+    for act, explicit in (("swigluoai", (fmax, 1.702, 1.0)), ("situglu", (1.0,)), ("swiglustep", (fmax,))):
+        aq0, as0, o0 = _row(cfg, act, ())
+        aq1, as1, o1 = _row(cfg, act, explicit)
+        assert np.array_equal(aq0, aq1) and np.array_equal(as0, as1) and np.array_equal(o0, o1), act
