@@ -231,6 +231,10 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  * act_q, act_scale   optional diagnostic outputs of A_hat in expert-sorted
  *                    row order: [bs*k, W] FP8 and [bs*k, W/32] E8M0 with W = I
  *                    (2I under gelu); NULL to skip.
+ * dispatch_q, dispatch_scale  optional diagnostic outputs of the dispatched
+ *                    X_hat (stage 1) in expert-sorted row order: [bs*k, h]
+ *                    FP8 codes of dispatch_quant_out_dtype and [bs*k, h/32]
+ *                    E8M0; NULL to skip (both or neither).
  * Shape limits: h and intermediate multiples of 128; k <= 32;
  * moe_expert_num <= 2048.
  * ---------------------------------------------------------------------- */
@@ -250,6 +254,7 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
                       const char* activation, const float* activation_params,
                       int64_t n_activation_params, void* y, int32_t* expert_token_nums,
                       int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale,
+                      uint8_t* dispatch_q, uint8_t* dispatch_scale,
                       void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -317,16 +322,23 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  * No allocation: the caller passes inputs and outputs only.  The scratch the
  * kernels need lives in one fixed array of MM_NOALLOC_SCRATCH_BYTES inside
  * the library, which every GPU that loads the library holds until the
- * process exits.  A problem whose scratch would not fit (about 4 bytes per
- * expanded row, plus 4 bytes per expert for each chunk of at least 256 ids)
- * is rejected with MM_ERR_WORKSPACE before anything is enqueued.
+ * process exits.  With R = num_rows * k expanded rows and E = expert_num
+ * the scratch is 4 * E * min(CeilDiv(R, 256), 512) bytes of histograms,
+ * about 8 * E bytes of offsets, and 4 * R bytes of scatter index only when
+ * expanded_row_idx is NULL (each piece rounded up to 256 bytes).  At
+ * E = 256 every R below the sort limit fits when the caller passes
+ * expanded_row_idx, and R up to 916,928 without it; from E = 2041 up, no
+ * problem of 131,072 rows or more fits.  A problem that does not fit is
+ * rejected with MM_ERR_WORKSPACE before anything is enqueued.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  A failed lookup returns MM_ERR_CUDA.
  * Sharing: every call uses the same array and it keeps the last call's
- * contents (nothing in it has to start at zero).  Calls whose kernels may
- * overlap on the GPU, e.g. on different streams without ordering, race on
- * the array; order them on one stream.
+ * contents; the one word that must start at zero (a grid-barrier counter)
+ * is cleared on the stream by each call.  Calls whose kernels may overlap
+ * on the GPU, e.g. on different streams without ordering, race on the
+ * array; order them on one stream.  Launches are counted and timed by
+ * mm_timing_read like those of mm_moe_init_routing.
  * ---------------------------------------------------------------------- */
 #define MM_NOALLOC_SCRATCH_BYTES (4u << 20)
 mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, const int32_t* expert_idx,

@@ -65,7 +65,8 @@ def load():
     L.mm_moe_token_permute.argtypes = [p, i32, p, i32, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, sz, p, p]
     L.mm_mega_moe_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, psz]
     L.mm_mega_moe.argtypes = ([p, p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
-                               i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, sz, p, p])
+                               i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, p, p, sz, p,
+                               p])
     L.mm_prepared_weight_scales_size.argtypes = [i32, i64, i64, i64, psz]
     L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
     L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
@@ -113,6 +114,19 @@ def _need_cuda(*ts):
             raise MMError("inputs must be contiguous CUDA tensors")
 
 
+_SRC_DTYPES = (torch.bfloat16, torch.float16, torch.float32)
+_BYTE_DTYPES = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+
+
+def _need_dtype(t, allowed, what):
+    """The C ABI reads raw memory: a tensor of another dtype would be
+    reinterpreted silently (an int64 index tensor read as pairs of int32
+    words), so it is refused here."""
+    if t is not None and t.dtype not in allowed:
+        names = " or ".join(str(d).replace("torch.", "") for d in allowed)
+        raise MMError(f"{what} must be {names}, got {str(t.dtype).replace('torch.', '')}")
+
+
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
         if workspace.numel() < nbytes:
@@ -134,6 +148,8 @@ def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_
     expert_tokens [E] int64 (count or cumsum), expanded_scale [N*K, AlignUp(H/32, 2)]
     uint8 E8M0 (empty without quantisation), sorted_row_idx [N*K] int32 (gather)).
     """
+    _need_dtype(x, _SRC_DTYPES, "x")
+    _need_dtype(expert_idx, (torch.int32,), "expert_idx")
     _need_cuda(x, expert_idx)
     L = load()
     n, h = x.shape
@@ -163,6 +179,8 @@ def mm_moe_token_permute(tokens, indices, num_experts: int, num_out_tokens=None,
     expanded_scale [M, AlignUp(H/32, 2)] uint8 E8M0 or an empty tensor).  With
     QUANT_MXFP4_E2M1: permuted_tokens [M, H/2] packed uint8, expanded_scale
     [M, CeilDiv(H, 64), 2]."""
+    _need_dtype(tokens, _SRC_DTYPES, "tokens")
+    _need_dtype(indices, (torch.int32, torch.int64), "indices")
     _need_cuda(tokens, indices)
     L = load()
     n, h = tokens.shape
@@ -212,7 +230,7 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 dispatch_quant_mode: int = 4, dispatch_quant_out_dtype: int = DT_FP8_E4M3FN,
                 combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
                 x_scales=None, out=None, workspace=None, dev_err=None, want_expanded_row_idx=False,
-                want_act=False):
+                want_act=False, want_dispatch=False):
     """MegaMoE forward, A8W8-FP or A8W4-FP, ep_world_size = 1.
 
     x [BS, H] bf16; topk_ids [BS, K] int32; topk_weights [BS, K] fp32 / bf16;
@@ -222,10 +240,23 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     (weight_scale_layout=0) or prepared by mm_prepare_weight_scales (1).  Under
     activation="gelu", weight2 is [E, H, 2I] and A_hat 2I wide.
     Returns (y [BS, H] bf16, expert_token_nums [E] int32) and, on request,
-    expanded_row_idx [BS*K] int32 and A_hat codes / scales in sorted order.
+    expanded_row_idx [BS*K] int32, A_hat codes / scales and the dispatched
+    X_hat codes [BS*K, H] / scales [BS*K, H/32], in sorted order.
     With dispatch_quant_mode=0, x holds FP8 codes (uint8 [BS, H]) and x_scales their
     E8M0 scales [BS, H/32] (pre-quantised pass-through).
     """
+    _need_dtype(x, (torch.bfloat16,) if dispatch_quant_mode != 0 else _BYTE_DTYPES, "x")
+    _need_dtype(topk_ids, (torch.int32,), "topk_ids")
+    _need_dtype(topk_weights, (torch.float32, torch.bfloat16), "topk_weights")
+    for name, t in (("weight1", weight1), ("weight2", weight2), ("shared_weight1", shared_weight1),
+                    ("shared_weight2", shared_weight2)):
+        _need_dtype(t, _BYTE_DTYPES, name)
+    for name, t in (("weight_scales1", weight_scales1), ("weight_scales2", weight_scales2), ("x_scales", x_scales),
+                    ("shared_weight_scales1", shared_weight_scales1),
+                    ("shared_weight_scales2", shared_weight_scales2)):
+        _need_dtype(t, (torch.uint8,), name)
+    if topk_ids.dim() != 2 or tuple(topk_weights.shape) != tuple(topk_ids.shape) or topk_ids.shape[0] != x.shape[0]:
+        raise MMError("topk_ids and topk_weights must both be [BS, K] with BS = x.shape[0]")
     _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
     L = load()
     bs, h = x.shape
@@ -242,6 +273,8 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     exp_idx = torch.empty(bs * k, dtype=torch.int32, device=dev) if want_expanded_row_idx else None
     act_q = torch.empty((bs * k, aw), dtype=torch.uint8, device=dev) if want_act else None
     act_s = torch.empty((bs * k, aw // 32), dtype=torch.uint8, device=dev) if want_act else None
+    dsp_q = torch.empty((bs * k, h), dtype=torch.uint8, device=dev) if want_dispatch else None
+    dsp_s = torch.empty((bs * k, h // 32), dtype=torch.uint8, device=dev) if want_dispatch else None
     need = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, inter, s_num, weight_scale_layout)
     ws = _workspace(need, dev, workspace)
     params = list(activation_params)
@@ -253,13 +286,16 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
         _ptr(shared_weight_scales1), _ptr(shared_weight_scales2), swdt, s_num, bs, h, k, moe_expert_num,
         ep_world_size, inter, max_recv_token_num, dispatch_quant_mode, dispatch_quant_out_dtype,
         combine_quant_mode, activation.encode() if activation else None, parr, len(params), _ptr(y), _ptr(counts),
-        _ptr(exp_idx), _ptr(act_q), _ptr(act_s), _ptr(ws), ws.numel(), _dev_err(dev_err), _stream(dev)),
+        _ptr(exp_idx), _ptr(act_q), _ptr(act_s), _ptr(dsp_q), _ptr(dsp_s), _ptr(ws), ws.numel(), _dev_err(dev_err),
+        _stream(dev)),
         "mm_mega_moe")
     res = [y, counts]
     if want_expanded_row_idx:
         res.append(exp_idx)
     if want_act:
         res += [act_q, act_s]
+    if want_dispatch:
+        res += [dsp_q, dsp_s]
     return tuple(res)
 
 
@@ -267,6 +303,7 @@ def mm_prepare_weight_scales(scales, k_red: int, which: int):
     """Rearrange E8M0 weight scales [E, N_out, CeilDiv(K_red, 64), 2] (or [E, N_out, K_red/32])
     into the tile layout of the grouped GEMMs (weight_scale_layout = 1).
     which = 1 for weight_scales1, 2 for weight_scales2."""
+    _need_dtype(scales, (torch.uint8,), "scales")
     _need_cuda(scales)
     L = load()
     e, n_out = scales.shape[0], scales.shape[1]
@@ -291,6 +328,7 @@ def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None =
     """Q_MX along the last dimension of a 2-D fp32 / bf16 / fp16 tensor.
     Returns (codes [rows, cols] uint8 -- [rows, cols / 2] packed for DT_FP4_E2M1 --,
     scales [rows, scale_cols] uint8 E8M0)."""
+    _need_dtype(src, _SRC_DTYPES, "src")
     _need_cuda(src)
     L = load()
     rows, cols = src.shape
@@ -335,6 +373,8 @@ def mm_moe_init_routing_noalloc(x, expert_idx, expert_num: int, quant_mode: int 
     scratch array is used instead (for callers that cannot provide scratch
     memory).  Same outputs as mm_moe_init_routing.  Calls that may overlap on
     the GPU race on the shared array; keep them on one stream."""
+    _need_dtype(x, _SRC_DTYPES, "x")
+    _need_dtype(expert_idx, (torch.int32,), "expert_idx")
     _need_cuda(x, expert_idx)
     L = load()
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int

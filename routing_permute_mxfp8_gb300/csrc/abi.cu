@@ -52,7 +52,7 @@ struct RoutingWs {
 RoutingWs carve_routing(Carver& c, const RoutePlan& p) {
   RoutingWs w;
   w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
-  w.offsets = c.take<int32_t>(2 * p.num_experts + 1);
+  w.offsets = c.take<int32_t>(route_offsets_words(p.num_experts));
   w.exp_idx = c.take<int32_t>(p.rows);
   return w;
 }
@@ -89,7 +89,7 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   MegaWs w;
   const int64_t nseg = d.e + d.s;
   w.hist = c.take<int32_t>((int64_t)p.num_experts * p.units);
-  w.offsets = c.take<int32_t>(2 * d.e + 1);
+  w.offsets = c.take<int32_t>(route_offsets_words((int)d.e));
   w.seg_rows = c.take<int32_t>(nseg);
   w.seg_mprefix = c.take<int32_t>(nseg + 1);
   w.exp_idx = c.take<int32_t>(d.rows);
@@ -120,6 +120,10 @@ mm_status check_mega_shapes(int64_t bs, int64_t h, int64_t k, int64_t e, int64_t
   return MM_OK;
 }
 
+}  // namespace
+
+namespace mm {
+
 // ---- stage timing (diagnostic, off by default) ----------------------------
 // While enabled, every entry point records a CUDA event pair around each of
 // its stages on the caller's stream; mm_timing_read sums the device time.
@@ -136,7 +140,7 @@ StageTimer& timer() {
   return t;
 }
 
-cudaEvent_t take_event(StageTimer& t) {
+static cudaEvent_t take_event(StageTimer& t) {
   if (!t.pool.empty()) {
     cudaEvent_t ev = t.pool.back();
     t.pool.pop_back();
@@ -147,39 +151,56 @@ cudaEvent_t take_event(StageTimer& t) {
   return ev;
 }
 
-// One stage of one call: constructor records the begin event, finish() the
-// end event and adds the number of kernels the stage launched.
-struct StageScope {
-  int stage;
-  cudaStream_t st;
-  bool active;
-  StageScope(int s, cudaStream_t stream) : stage(s), st(stream), active(false) {
-    StageTimer& t = timer();
-    std::lock_guard<std::mutex> g(t.mu);
-    if (t.on) {
-      cudaEvent_t ev = take_event(t);
-      if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
-        t.open[stage].push_back(ev);
-        active = true;
-      }
+StageScope::StageScope(int s, cudaStream_t stream) : stage(s), st(stream), active(false) {
+  StageTimer& t = timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  if (t.on) {
+    cudaEvent_t ev = take_event(t);
+    if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
+      t.open[stage].push_back(ev);
+      active = true;
     }
   }
-  void finish(int kernels) {
-    StageTimer& t = timer();
-    std::lock_guard<std::mutex> g(t.mu);
-    t.launches[stage] += kernels;
-    if (active) {
-      cudaEvent_t ev = take_event(t);
-      if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
-        t.open[stage].push_back(ev);
-      } else {
-        t.pool.push_back(t.open[stage].back());
-        t.open[stage].pop_back();
-      }
-      active = false;
+}
+
+void StageScope::finish(int kernels) {
+  StageTimer& t = timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.launches[stage] += kernels;
+  if (active) {
+    cudaEvent_t ev = take_event(t);
+    if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
+      t.open[stage].push_back(ev);
+    } else {
+      t.pool.push_back(t.open[stage].back());
+      t.open[stage].pop_back();
     }
+    active = false;
   }
-};
+}
+
+mm_status validate_init_routing(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows,
+                                int64_t h, int64_t k, int64_t expert_num, int quant_mode, int expert_tokens_num_type,
+                                const void* expanded_x, const uint8_t* expanded_scale) {
+  if (num_rows < 0 || k <= 0 || expert_num <= 0 || expert_num > 10240) return MM_ERR_INVALID_ARG;
+  if (num_rows * k >= kSortLimit) return MM_ERR_INVALID_ARG;
+  if (h <= 0 || !is_src_dtype(x_dtype)) return MM_ERR_INVALID_ARG;
+  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
+    return MM_ERR_UNSUPPORTED;
+  if (expert_tokens_num_type != 0 && expert_tokens_num_type != 1) return MM_ERR_UNSUPPORTED;
+  const bool quant = quant_mode != MM_QUANT_NONE;
+  if (quant ? (h % 16 != 0) : ((h * dt_size(x_dtype)) % 16 != 0)) return MM_ERR_UNSUPPORTED;
+  if (num_rows * k == 0) return MM_OK;  // nothing is read or written but the counts
+  if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(expanded_x)) return MM_ERR_INVALID_ARG;
+  return MM_OK;
+}
+
+int init_routing_out_fmt(int quant_mode) { return quant_fmt(quant_mode); }
+
+}  // namespace mm
+
+namespace {
 
 // The activation and its activation_params (MegaMoE parameter table,
 // "activation_params"): swiglu / swiglustep [] or [clamp]; swigluoai [] or
@@ -298,19 +319,14 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   size_t need = 0;
   mm_status s = mm_moe_init_routing_workspace_size(num_rows, k, expert_num, &need);
   if (s != MM_OK) return s;
-  if (h <= 0 || !is_src_dtype(x_dtype)) return MM_ERR_INVALID_ARG;
-  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
-    return MM_ERR_UNSUPPORTED;
-  if (expert_tokens_num_type != 0 && expert_tokens_num_type != 1) return MM_ERR_UNSUPPORTED;
-  const bool quant = quant_mode != MM_QUANT_NONE;
-  if (quant ? (h % 16 != 0) : ((h * dt_size(x_dtype)) % 16 != 0)) return MM_ERR_UNSUPPORTED;
+  s = validate_init_routing(x, x_dtype, expert_idx, num_rows, h, k, expert_num, quant_mode, expert_tokens_num_type,
+                            expanded_x, expanded_scale);
+  if (s != MM_OK) return s;
   const int64_t rows = num_rows * k;
   if (rows == 0)  // no rows: every expert's count (and the cumsum) is 0
     return expert_tokens ? cuda_status(cudaMemsetAsync(expert_tokens, 0, (size_t)expert_num * sizeof(int64_t),
                                                        static_cast<cudaStream_t>(stream)))
                          : MM_OK;
-  if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(expanded_x)) return MM_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const RoutePlan plan = route_plan(rows, (int)expert_num);
@@ -445,8 +461,9 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
                       int64_t max_recv_token_num, int64_t dispatch_quant_mode, int64_t dispatch_quant_out_dtype,
                       int64_t combine_quant_mode, const char* activation, const float* activation_params,
                       int64_t n_activation_params, void* y, int32_t* expert_token_nums,
-                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_err, void* stream) {
+                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, uint8_t* dispatch_q,
+                      uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                      void* stream) {
   size_t need = 0;
   mm_status s = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, intermediate, shared_expert_num,
                                            weight_scale_layout, &need);
@@ -477,8 +494,10 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
       (!shared_weight1 || !shared_weight2 || !shared_weight_scales1 || !shared_weight_scales2))
     return MM_ERR_INVALID_ARG;
   if ((act_q == nullptr) != (act_scale == nullptr)) return MM_ERR_INVALID_ARG;
+  if ((dispatch_q == nullptr) != (dispatch_scale == nullptr)) return MM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y) || !aligned16(weight1) || !aligned16(weight2) ||
-      !aligned16(weight_scales1) || !aligned16(weight_scales2) || (act_q && !aligned16(act_q)))
+      !aligned16(weight_scales1) || !aligned16(weight_scales2) || (act_q && !aligned16(act_q)) ||
+      (dispatch_q && !aligned16(dispatch_q)))
     return MM_ERR_INVALID_ARG;
   if (shared_expert_num > 0 && (!aligned16(shared_weight1) || !aligned16(shared_weight2) ||
                                 !aligned16(shared_weight_scales1) || !aligned16(shared_weight_scales2)))
@@ -620,7 +639,22 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   sc.finish(1);
   if (e != cudaSuccess) return MM_ERR_CUDA;
 
-  // optional diagnostic copy of A_hat in expert-sorted order
+  // optional diagnostic copies of X_hat and A_hat in expert-sorted order
+  if (dispatch_q) {
+    UnpadArgs ua;
+    ua.src_q = w.xq;
+    ua.src_sf = w.xsf;
+    ua.pad_row = w.pad_row;
+    ua.expanded_row_idx = o.expanded_row_idx;
+    ua.rows = d.rows;
+    ua.cols = d.h;
+    ua.dst_q = dispatch_q;
+    ua.dst_sf = dispatch_scale;
+    StageScope su(MM_STAGE_DIAG, st);
+    e = launch_unpad(ua, st);
+    su.finish(1);
+    if (e != cudaSuccess) return MM_ERR_CUDA;
+  }
   if (act_q) {
     UnpadArgs ua;
     ua.src_q = w.aq;

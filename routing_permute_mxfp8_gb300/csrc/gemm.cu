@@ -41,6 +41,8 @@
 // store rows directly from registers.
 // Every wait is bounded; a timeout sets MM_DEVERR_TIMEOUT and the CTA
 // drains its own copies and MMAs, frees TMEM and returns.
+#include <mutex>
+
 #include "mm_route.cuh"
 
 namespace mm {
@@ -53,17 +55,10 @@ constexpr uint32_t kABytes = kBM * kBK;   // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOStageBytes = 32 * 64;  // one 32 x 32 bf16 block of O
 constexpr int kTileN = 256;                  // output columns per tile (GEMM1: 128 gate + 128 up)
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 #ifndef MM_BIG_MTILES
 #define MM_BIG_MTILES 2
 #endif
 constexpr int kBigMtiles = MM_BIG_MTILES;    // m tiles from which a segment's tiles count as tensor-bound
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Waits for the phase with `parity` of an mbarrier, giving up after
 // limit_ns of %globaltimer time (false: the caller raises MM_DEVERR_TIMEOUT).
@@ -657,13 +652,18 @@ cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, cu
 }
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int n[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> g(mu);
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    n[dev] = v;
   }
-  return n;
+  return n[dev];
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {

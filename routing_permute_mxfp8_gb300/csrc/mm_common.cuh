@@ -109,6 +109,22 @@ __device__ __forceinline__ void raise_err(int32_t* dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
 }
 
+// Limit of every wait inside a kernel (a mbarrier phase, a grid barrier):
+// past it the kernel raises MM_DEVERR_TIMEOUT and stops instead of hanging.
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers, TMA (inline PTX).
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -44,8 +44,11 @@ struct RouteScanArgs {
 
 RoutePlan route_plan(int64_t rows, int num_experts);
 size_t route_workspace_bytes(const RoutePlan& p);
-// hist: [E * units] int32, offsets: [2 * E + 1] int32 (offsets, then
-// per-expert totals; both workspace)
+// int32 words of the offsets workspace: offsets [E + 1], totals [E] and the
+// fused launch's grid-barrier counter
+int64_t route_offsets_words(int num_experts);
+// hist: [E * units] int32, offsets: [route_offsets_words(E)] int32 (both
+// workspace)
 // *launches (optional) receives the number of kernels launched: 1 (one
 // cooperative launch) or 4.
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
@@ -133,9 +136,30 @@ struct UnpadArgs {
 };
 cudaError_t launch_unpad(const UnpadArgs& a, cudaStream_t st);
 
+// SMs of the current device (queried once per device)
 int num_sms();
 // one CTA waits on an mbarrier that nothing completes, gives up after
 // limit_ns and raises MM_DEVERR_TIMEOUT (the bounded-wait failure path)
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, cudaStream_t st);
+
+// ---- C-ABI helpers shared by the entry points (abi.cu) -------------------
+// One stage of one call for mm_timing_read: the constructor records the
+// begin event on the stream (while timing is enabled), finish() the end
+// event and adds the number of kernels the stage launched.
+struct StageScope {
+  int stage;
+  cudaStream_t st;
+  bool active;
+  StageScope(int s, cudaStream_t stream);
+  void finish(int kernels);
+};
+
+// Argument checks of mm_moe_init_routing that do not involve the workspace
+// (also used by mm_moe_init_routing_noalloc).
+mm_status validate_init_routing(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows,
+                                int64_t h, int64_t k, int64_t expert_num, int quant_mode, int expert_tokens_num_type,
+                                const void* expanded_x, const uint8_t* expanded_scale);
+// element format of expanded_x for a quant mode (-1: copy)
+int init_routing_out_fmt(int quant_mode);
 
 }  // namespace mm

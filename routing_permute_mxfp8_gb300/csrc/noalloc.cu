@@ -17,9 +17,17 @@
 // that device is current and keeps it; that first call should therefore come
 // before any stream capture.  All calls share the one array, and it keeps
 // whatever the last call left in it: two calls whose kernels overlap on the
-// GPU (different streams, no ordering between them) race on it.  No part of
-// it has to start at zero, because every word the kernels read is written
-// earlier in the same call.
+// GPU (different streams, no ordering between them) race on it.  The one
+// word that has to start at zero, the routing launch's grid-barrier counter,
+// is cleared on the stream by every call before its routing kernel runs;
+// every other word the kernels read is written earlier in the same call.
+// Capacity: the histogram takes 4 * E * min(ceil(R / 256), 512) bytes, the
+// offsets about 8 * E bytes, and the scatter index 4 * R bytes only when the
+// caller passes no expanded_row_idx (each piece rounded up to 256 bytes).
+// At E = 256 that leaves room for any R < 16777215 with a caller index, and
+// for R up to 916,928 without one; from E = 2041 up, problems of 131,072 ids
+// or more do not fit either way.
+// The calls are counted and timed by mm_timing_read like mm_moe_init_routing.
 #include <mutex>
 
 #include "mm_route.cuh"
@@ -59,15 +67,10 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
                                                  int32_t* sorted_row_idx, int64_t* expert_tokens,
                                                  int32_t* dev_err, void* stream) {
   using namespace mm;
-  if (num_rows < 0 || k <= 0 || expert_num <= 0 || expert_num > 10240 || h <= 0) return MM_ERR_INVALID_ARG;
-  if (num_rows * k >= 16777215) return MM_ERR_INVALID_ARG;
-  if (x_dtype != MM_DT_BFLOAT16 && x_dtype != MM_DT_FLOAT16 && x_dtype != MM_DT_FLOAT32) return MM_ERR_INVALID_ARG;
-  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
-    return MM_ERR_UNSUPPORTED;
-  if (expert_tokens_num_type != 0 && expert_tokens_num_type != 1) return MM_ERR_UNSUPPORTED;
-  const bool quant = quant_mode != MM_QUANT_NONE;
-  const int esz = x_dtype == MM_DT_FLOAT32 ? 4 : 2;
-  if (quant ? (h % 16 != 0) : ((h * esz) % 16 != 0)) return MM_ERR_UNSUPPORTED;
+  // the same argument checks as mm_moe_init_routing
+  mm_status s = validate_init_routing(x, x_dtype, expert_idx, num_rows, h, k, expert_num, quant_mode,
+                                      expert_tokens_num_type, expanded_x, expanded_scale);
+  if (s != MM_OK) return s;
   const int64_t rows = num_rows * k;
   if (rows == 0) {  // no rows: every expert's count (and the cumsum) is 0
     if (expert_tokens &&
@@ -76,14 +79,12 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
       return MM_ERR_CUDA;
     return MM_OK;
   }
-  if (!x || !expert_idx || !expanded_x || (quant && !expanded_scale)) return MM_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(expanded_x) & 15))
-    return MM_ERR_INVALID_ARG;
 
-  // scratch: per-chunk histograms, offsets, scatter index (unless the caller's)
+  // scratch: per-chunk histograms, offsets (with the grid-barrier counter),
+  // and the scatter index unless the caller passes expanded_row_idx
   const RoutePlan plan = route_plan(rows, (int)expert_num);
   const size_t hist_b = piece((int64_t)plan.num_experts * plan.units * 4);
-  const size_t off_b = piece((2 * expert_num + 1) * 4);
+  const size_t off_b = piece(route_offsets_words(plan.num_experts) * 4);
   const size_t idx_b = expanded_row_idx ? 0 : piece(rows * 4);
   if (hist_b + off_b + idx_b > kNoallocScratchBytes) return MM_ERR_WORKSPACE;  // problem too large
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address());
@@ -98,7 +99,11 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
   o.sorted_row_idx = sorted_row_idx;
   o.expert_tokens = expert_tokens;
   o.tokens_cumsum = expert_tokens_num_type == 0;
-  if (launch_route(plan, expert_idx, false, hist, offsets, o, dev_err, st) != cudaSuccess) return MM_ERR_CUDA;
+  StageScope sr(MM_STAGE_ROUTE, st);
+  int nl = 0;
+  cudaError_t e = launch_route(plan, expert_idx, false, hist, offsets, o, dev_err, st, &nl);
+  sr.finish(nl);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
   PermuteArgs a = {};
   a.src = x;
   a.src_dtype = x_dtype;
@@ -107,10 +112,13 @@ extern "C" mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, con
   a.k = (int)k;
   a.dest = exp_idx;
   a.dest_limit = rows;
-  a.out_fmt = quant_mode == MM_QUANT_MXFP8_E5M2 ? MM_DT_FP8_E5M2 : (quant ? MM_DT_FP8_E4M3FN : -1);
+  a.out_fmt = init_routing_out_fmt(quant_mode);
   a.out = expanded_x;
   a.scales = expanded_scale;
   a.scale_cols = round_up(ceil_div(h, 32), 2);
   a.dev_err = dev_err;
-  return launch_permute(a, st) == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+  StageScope sd(MM_STAGE_DISPATCH, st);
+  e = launch_permute(a, st);
+  sd.finish(1);
+  return e == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }

@@ -20,12 +20,10 @@
 // k_route_fused runs the four phases in one cooperative launch, with a
 // grid-wide barrier between phases; the four kernels remain for when its
 // blocks cannot all be resident.
-// No global atomics; the result is deterministic.
-#include <cooperative_groups.h>
+// No global atomics on the data; the result is deterministic.
+#include <mutex>
 
 #include "mm_route.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace mm {
 
@@ -260,29 +258,58 @@ __global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int n
                      seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row);
 }
 
+// Grid-wide barrier of a cooperative launch (every block is resident) on a
+// counter that is zero when the launch starts: barrier number b (1, 2, ...)
+// opens when the counter reaches b * gridDim.x.  The wait is bounded: after
+// kWaitNs the block raises MM_DEVERR_TIMEOUT and the caller stops (the
+// other blocks then time out at their next barrier, so the launch ends).
+__device__ __forceinline__ bool grid_barrier_bounded(uint32_t* count, uint32_t b, int32_t* dev_err, int* sh_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this block's writes before its arrival
+    atomicAdd(count, 1u);
+    const uint32_t target = b * gridDim.x;
+    int ok = 1;
+    if (ld_acquire_u32(count) < target) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_u32(count) < target) {
+        if (globaltimer() - t0 > kWaitNs) {
+          ok = 0;
+          raise_err(dev_err, MM_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *sh_ok = ok;
+  }
+  __syncthreads();
+  return *sh_ok != 0;
+}
+
 // All four phases in one cooperative launch (every block resident), with
 // grid-wide barriers between them: one launch instead of four.
 template <typename IdT>
 __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk, int units,
                               int32_t* __restrict__ hist, RouteScanArgs sa, int32_t* __restrict__ expanded_row_idx,
-                              int32_t* __restrict__ pad_row, int32_t* dev_err) {
+                              int32_t* __restrict__ pad_row, uint32_t* __restrict__ barrier, int32_t* dev_err) {
   extern __shared__ int32_t sh_route[];  // [warps][E]
   __shared__ int64_t sh_warp[33];
-  cg::grid_group grid = cg::this_grid();
+  __shared__ int sh_ok;
   const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int unit = blockIdx.x * wpb + warp;
   int32_t* mine = sh_route + warp * num_experts;
   if (unit < units) route_hist_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, dev_err);
-  grid.sync();
+  if (!grid_barrier_bounded(barrier, 1, dev_err, &sh_ok)) return;
   if (units <= 32) {
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < num_experts; e += gridDim.x * blockDim.x)
       route_scan_expert_thread(hist, units, e, sa.totals);
   } else {
     for (int e = unit; e < num_experts; e += gridDim.x * wpb) route_scan_expert_warp(hist, units, e, sa.totals);
   }
-  grid.sync();
+  if (!grid_barrier_bounded(barrier, 2, dev_err, &sh_ok)) return;
   if (blockIdx.x == 0) route_scan_offsets_block(sa, sh_warp);
-  grid.sync();
+  if (!grid_barrier_bounded(barrier, 3, dev_err, &sh_ok)) return;
   if (unit < units)
     route_scatter_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
                        expanded_row_idx, sa.sorted_row_idx, pad_row);
@@ -304,32 +331,48 @@ RoutePlan route_plan(int64_t rows, int num_experts) {
   return p;
 }
 
+int64_t route_offsets_words(int num_experts) {
+  // offsets [E + 1], totals [E], then the grid-barrier counter on its own
+  // 8-byte boundary
+  return round_up(2 * (int64_t)num_experts + 1, 2) + 2;
+}
+
 size_t route_workspace_bytes(const RoutePlan& p) {
   return (size_t)round_up((int64_t)p.num_experts * p.units * 4, 256) +
-         (size_t)round_up((2 * (int64_t)p.num_experts + 1) * 4, 256);
+         (size_t)round_up(route_offsets_words(p.num_experts) * 4, 256);
 }
 
 namespace {
 
-// Blocks of k_route_fused with `wpb` warps that can be resident at once
-// (0: no cooperative launch).  Queried once per block size with the largest
-// shared-memory table route_plan allows (40 KB), so it never overestimates.
+// Blocks of k_route_fused with `wpb` warps that can be resident at once on
+// the current device (0: no cooperative launch).  Queried once per device
+// and block size with the largest shared-memory table route_plan allows
+// (40 KB), so it never overestimates.
+constexpr int kMaxDevices = 64;
+
 template <typename IdT>
 int fused_capacity(int wpb) {
-  static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
-  if (wpb < 1 || wpb > 8) return 0;
-  if (cap[wpb] < 0) {
-    int dev = 0, coop = 0, per_sm = 0;
-    cudaGetDevice(&dev);
+  static std::mutex mu;
+  static int cap[kMaxDevices][9];
+  static bool init[kMaxDevices] = {false};
+  int dev = 0;
+  if (wpb < 1 || wpb > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (!init[dev]) {
+    for (int w = 0; w < 9; ++w) cap[dev][w] = -1;
+    init[dev] = true;
+  }
+  if (cap[dev][wpb] < 0) {
+    int coop = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) coop = 0;
     int c = 0;
     if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused<IdT>, wpb * 32, 40960) ==
                     cudaSuccess)
       c = per_sm * num_sms();
     cudaGetLastError();
-    cap[wpb] = c;
+    cap[dev][wpb] = c;
   }
-  return cap[wpb];
+  return cap[dev][wpb];
 }
 
 template <typename IdT>
@@ -350,7 +393,10 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     int ne = p.num_experts, chunk = p.chunk, units = p.units;
     int32_t* exp_idx = o.expanded_row_idx;
     int32_t* pad = o.pad_row;
-    void* args[] = {(void*)&ids, &rows, &ne, &chunk, &units, &hist, &a, &exp_idx, &pad, &dev_err};
+    // the barrier counter (workspace, after the offsets and totals) starts at 0
+    uint32_t* barrier = reinterpret_cast<uint32_t*>(a.offsets + route_offsets_words(p.num_experts) - 2);
+    void* args[] = {(void*)&ids, &rows, &ne, &chunk, &units, &hist, &a, &exp_idx, &pad, &barrier, &dev_err};
+    if (cudaMemsetAsync(barrier, 0, sizeof(uint32_t), st) != cudaSuccess) return cudaGetLastError();
     if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
         cudaSuccess) {
       launches = 1;

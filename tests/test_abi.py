@@ -73,7 +73,8 @@ def test_workspace_queries(lib):
 def _mega(lib, **kw):
     a = dict(x=1, xs=None, ids=1, w=1, gdt=0, w1=1, w2=1, s1=1, s2=1, wdt=24, layout=0, sw1=None, sw2=None, ss1=None,
              ss2=None, swdt=24, s=0, bs=64, h=256, k=2, e=8, ep=1, inter=128, maxrecv=0, dqm=4, dqd=24, cqm=0,
-             act=b"swiglu", params=None, nparams=0, y=1, counts=None, exp=None, aq=None, asc=None, ws=None,
+             act=b"swiglu", params=None, nparams=0, y=1, counts=None, exp=None, aq=None, asc=None, dq=None, dsc=None,
+             ws=None,
              wsb=0, err=None, stream=None)
     a.update(kw)
     vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
@@ -81,7 +82,8 @@ def _mega(lib, **kw):
                            vp(a["s2"]), a["wdt"], a["layout"], vp(a["sw1"]), vp(a["sw2"]), vp(a["ss1"]),
                            vp(a["ss2"]), a["swdt"], a["s"], a["bs"], a["h"], a["k"], a["e"], a["ep"], a["inter"],
                            a["maxrecv"], a["dqm"], a["dqd"], a["cqm"], a["act"], a["params"], a["nparams"],
-                           vp(a["y"]), vp(a["counts"]), vp(a["exp"]), vp(a["aq"]), vp(a["asc"]), vp(a["ws"]),
+                           vp(a["y"]), vp(a["counts"]), vp(a["exp"]), vp(a["aq"]), vp(a["asc"]), vp(a["dq"]),
+                           vp(a["dsc"]), vp(a["ws"]),
                            a["wsb"], vp(a["err"]), a["stream"])
 
 
@@ -104,6 +106,8 @@ def test_mega_moe_host_rejections(lib):
     assert _mega(lib, maxrecv=100) == 1              # below bs*k rows
     assert _mega(lib, ws=None, wsb=0) == 3           # workspace missing
     assert _mega(lib, bs=0) == 0                     # empty batch: nothing to do
+    assert _mega(lib, dq=1) == 1                     # dispatch diagnostic codes without their scales
+    assert _mega(lib, aq=1) == 1                     # activation diagnostic codes without their scales
     f = lambda *v: (ctypes.c_float * len(v))(*v)
     for act, params in ((b"swiglu", (2.0, 1.0)), (b"swiglu", (-1.0,)), (b"swiglu", (float("nan"),)),
                         (b"swigluoai", (1.0,)), (b"swigluoai", (0.0, float("inf"), 1.0)), (b"situglu", (0.0,)),
@@ -149,3 +153,39 @@ def test_binding_refuses_host_tensors():
         mm.mm_moe_init_routing(x, ids, 8)
     with pytest.raises(mm.MMError):
         mm.mm_moe_token_permute(x, ids, 8)
+
+
+def test_binding_refuses_index_and_data_types_the_abi_would_misread():
+    """The C entry points read expert ids as int32 (MoeInitRoutingV3 parameter
+    table: expertIdx INT32) and x / weights as the stated codes.  Tensors of
+    another dtype (torch's default int64 for ids, most of all) are refused with
+    MMError before any pointer reaches the library, on any device."""
+    import torch
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    ids64 = torch.zeros((4, 2), dtype=torch.int64)
+    ids32 = ids64.to(torch.int32)
+    for call in (lambda: mm.mm_moe_init_routing(x, ids64, 8),
+                 lambda: mm.mm_moe_init_routing_noalloc(x, ids64, 8)):
+        with pytest.raises(mm.MMError, match="expert_idx must be int32"):
+            call()
+    with pytest.raises(mm.MMError, match="x must be"):
+        mm.mm_moe_init_routing(x.to(torch.int16), ids32, 8)
+    with pytest.raises(mm.MMError, match="indices must be"):
+        mm.mm_moe_token_permute(x, ids32.to(torch.int16), 8)
+    w1 = torch.zeros((8, 256, 256), dtype=torch.uint8)
+    w2 = torch.zeros((8, 256, 128), dtype=torch.uint8)
+    s1 = torch.zeros((8, 256, 8), dtype=torch.uint8)
+    s2 = torch.zeros((8, 256, 4), dtype=torch.uint8)
+    gate = torch.zeros((4, 2), dtype=torch.float32)
+    with pytest.raises(mm.MMError, match="topk_ids must be int32"):
+        mm.mm_mega_moe(x, ids64, gate, w1, w2, s1, s2, 8)
+    with pytest.raises(mm.MMError, match="topk_weights must be"):
+        mm.mm_mega_moe(x, ids32, gate.to(torch.float16), w1, w2, s1, s2, 8)
+    with pytest.raises(mm.MMError, match="x must be bfloat16"):
+        mm.mm_mega_moe(x.float(), ids32, gate, w1, w2, s1, s2, 8)
+    with pytest.raises(mm.MMError, match="weight1 must be"):
+        mm.mm_mega_moe(x, ids32, gate, w1.to(torch.int8), w2, s1, s2, 8)
+    with pytest.raises(mm.MMError, match="weight_scales2 must be uint8"):
+        mm.mm_mega_moe(x, ids32, gate, w1, w2, s1, s2.to(torch.int32), 8)
+    with pytest.raises(mm.MMError, match="BS = x.shape"):
+        mm.mm_mega_moe(x, ids32[:3], gate[:3], w1, w2, s1, s2, 8)

@@ -183,7 +183,7 @@ def test_empty_batch_writes_zero_counts(ttype):
     cnt = torch.full((e,), -7, dtype=torch.int32, device=DEV)
     st = L.mm_mega_moe(vp(dummy), None, vp(dummy), vp(dummy), 0, vp(dummy), vp(dummy), vp(dummy), vp(dummy), 24, 0,
                        None, None, None, None, 24, 0, 0, 256, 2, e, 1, 128, 0, 4, 24, 0, b"swiglu", None, 0,
-                       vp(dummy), vp(cnt), None, None, None, vp(dummy), 64, None, None)
+                       vp(dummy), vp(cnt), None, None, None, None, None, vp(dummy), 64, None, None)
     assert st == 0
     assert np.array_equal(host(cnt), np.zeros(e, np.int32))
 
@@ -261,6 +261,17 @@ def check_act(aq_gpu, as_gpu, exp_idx, aq_ref, as_ref, tokens, k):
     assert diff.mean() <= ACT_FRAC, diff.mean()
 
 
+def check_dispatch(xq_gpu, xs_gpu, x, cfg, r_srt, tokens=None):
+    """Dispatched rows of a MegaMoE call (expert-sorted order) against
+    oracle.permute with the dispatch format: codes and E8M0 scales identical.
+    With sampled tokens only the rows of those tokens are compared (the
+    oracle quantises every row; that part is cheap)."""
+    q_ref, s_ref = oracle.permute(x, oracle.DT_BF16, cfg.k, r_srt, r_srt.size, cfg.dispatch_fmt)
+    rows = np.arange(r_srt.size) if tokens is None else np.nonzero(np.isin(r_srt // cfg.k, tokens))[0]
+    assert np.array_equal(xq_gpu[rows], q_ref[rows])
+    assert np.array_equal(xs_gpu[rows], s_ref[rows, :xs_gpu.shape[1]])
+
+
 def check_y(y_gpu, y_ref):
     yg = y_gpu.astype(np.float64)
     rel = np.linalg.norm(yg - y_ref) / np.linalg.norm(y_ref)
@@ -312,15 +323,18 @@ def run_mega(cfg, tokens=None, layout=0, check_acts=True, sparse=False):
             ss2 = mm.mm_prepare_weight_scales(ss2, cfg.act_width, 2)
         kw = dict(shared_weight1=sw1, shared_weight2=sw2, shared_weight_scales1=ss1, shared_weight_scales2=ss2)
     err = zeros_err()
-    y, counts, exp_idx, aq, a_s = mm.mm_mega_moe(
+    y, counts, exp_idx, aq, a_s, xq, xs = mm.mm_mega_moe(
         bf16(x), t(ids), gt, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt), ws1, ws2, cfg.e,
         weight_dtype=cfg.weight_fmt, weight_scale_layout=layout, activation=cfg.activation,
         activation_params=cfg.act_params, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err,
-        want_expanded_row_idx=True, want_act=True, **kw)
+        want_expanded_row_idx=True, want_act=True, want_dispatch=True, **kw)
     assert host(err)[0] == 0
     r_srt, r_exp, r_cnt, _ = oracle.route(ids, cfg.e)
     assert np.array_equal(host(counts), r_cnt.astype(np.int32))
     assert np.array_equal(host(exp_idx), r_exp)
+    # stage 1 (dispatch): the X_hat rows and scales inside the step, bit-exact
+    # against the oracle's permute + Q_MX in the dispatch format
+    check_dispatch(host(xq), host(xs), x, cfg, r_srt, tokens)
     tok = np.arange(cfg.n) if tokens is None else np.asarray(tokens)
     y_ref, _, aq_ref, as_ref = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt,
                                                       cfg.weight_fmt, tokens=tok, shared=sh, want_act=True,
