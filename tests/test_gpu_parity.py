@@ -382,6 +382,22 @@ MEGA_CASES = {
     # terms per token), and 2048 routed experts + 4 shared segments
     "topk32_shared4": dict(n=96, h=256, inter=128, e=64, k=32, shared=4),
     "max_experts": dict(n=256, h=256, inter=128, e=2048, k=8, shared=4),
+    # segments of 1 to 128 rows (one padded m tile) next to segments of two and
+    # more tiles: every row count up to 128 and the step to two m tiles, FP8 and
+    # FP4 weights, shared experts, gelu, both dispatch formats
+    "small_seg_zipf_mixed": dict(n=400, h=512, inter=256, e=48, k=3, routing="zipf"),
+    "small_seg_single_rows": dict(n=5, h=256, inter=128, e=8, k=1),
+    "small_seg_128_rows": dict(n=128, h=384, inter=128, e=1, k=1, shared=1),
+    "small_seg_129_rows": dict(n=129, h=384, inter=128, e=1, k=1, shared=1),
+    "small_seg_112_rows_e5m2": dict(n=112, h=256, inter=256, e=1, k=1, dispatch_fmt=23),
+    "small_seg_fp4_shared": dict(n=100, h=512, inter=256, e=16, k=4, shared=1, weight_fmt=296, dispatch_fmt=24),
+    "small_seg_fp4_e5m2_zipf": dict(n=300, h=256, inter=384, e=32, k=2, routing="zipf", weight_fmt=296, dispatch_fmt=23),
+    "small_seg_gelu_shared": dict(n=90, h=512, inter=256, e=8, k=3, shared=1, activation="gelu",
+                             act_params=(float(np.finfo(np.float32).max),)),
+    "small_seg_gelu_fp4_zipf": dict(n=200, h=256, inter=128, e=16, k=4, routing="zipf", weight_fmt=296, dispatch_fmt=24,
+                               activation="gelu", act_params=(float(np.finfo(np.float32).max),)),
+    "small_seg_swigluoai_h896": dict(n=70, h=896, inter=256, e=4, k=2, shared=2, activation="swigluoai",
+                                act_params=(0.4, 1.702, 1.0)),
 }
 
 
