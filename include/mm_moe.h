@@ -310,6 +310,54 @@ mm_status mm_mx_quantize(const void* src, int src_dtype, int64_t rows, int64_t c
 mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Expert parallelism: dispatch to ranks and combine (MegaMoE README, A8W8-FP
+ * scenario stage 1 "dispatch the quantised tokens to the ranks holding
+ * their experts" and stage 4 "GMM2 rows written back to the source rank,
+ * weighted and summed", with epWorldSize > 1; parameter table
+ * epWorldSize / moeExpertNum).  Rank r holds experts [r*E/W, (r+1)*E/W).
+ * The exchange between ranks is the caller's collective (an all-to-all with
+ * the counts below as split sizes); each rank runs mm_mega_moe on the rows
+ * it receives (pass-through quantisation, top-K 1, weight 1, its local
+ * experts) and sends the resulting rows back in the order received.
+ *
+ * mm_moe_ep_dispatch -- on the source rank: the flattened ids j = i*K + k
+ *   are sorted by destination rank id / (E/W), stably (rows of one rank in
+ *   ascending j); every token is MX-quantised once (group 32, E8M0 shared
+ *   exponent, dispatch_quant_out_dtype 23 / 24) and its row stored at its K
+ *   positions.
+ * x                 [num_rows, h] bf16 / fp16 (x_dtype), h a multiple of 128.
+ * topk_ids          [num_rows, k] int32 in [0, moe_expert_num); k <= 32.
+ * moe_expert_num    E, a multiple of ep_world_size W.
+ * send_x            [num_rows*k, h] FP8 codes, rank-sorted (output).
+ * send_scales       [num_rows*k, h/32] E8M0 (output).
+ * send_expert       [num_rows*k] int32: the row's expert on its destination
+ *                   rank, id % (E/W) (output).
+ * rank_counts       [W] int64: rows for each rank, the send split sizes.
+ * expanded_row_idx  [num_rows*k] int32: position of row j in the send
+ *                   order; -1 for an id out of range (row left out,
+ *                   MM_DEVERR_EXPERT_RANGE set).
+ * workspace         mm_moe_ep_dispatch_workspace_size bytes.
+ * num_rows = 0 only zeroes rank_counts.
+ *
+ * mm_moe_combine -- Y[i] = sum_k W[i,k] * expert_rows[row_idx[i*k + k']]
+ *   accumulated in fp32 in the order k' = 0..k-1, rounded to bf16 once;
+ *   row_idx < 0 leaves the term out (MegaMoE stage 4).  On the source rank:
+ *   expert_rows = the returned rows in send order, row_idx =
+ *   expanded_row_idx of mm_moe_ep_dispatch.
+ * expert_rows       [*, h] bf16, h a multiple of 8.
+ * topk_weights      [num_rows, k] fp32 or bf16 (topk_weights_dtype); k <= 36.
+ * y                 [num_rows, h] bf16 output.
+ * ---------------------------------------------------------------------- */
+mm_status mm_moe_ep_dispatch_workspace_size(int64_t num_rows, int64_t k, int64_t ep_world_size, size_t* bytes);
+mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids, int64_t num_rows, int64_t h,
+                             int64_t k, int64_t moe_expert_num, int64_t ep_world_size,
+                             int64_t dispatch_quant_out_dtype, uint8_t* send_x, uint8_t* send_scales,
+                             int32_t* send_expert, int64_t* rank_counts, int32_t* expanded_row_idx,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
+                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, void* y, void* stream);
+
+/* ------------------------------------------------------------------------
  * mm_moe_init_routing_noalloc -- the same routing and permute as
  * mm_moe_init_routing (same arguments and outputs), for callers that cannot
  * give the library device scratch memory: for example a host program or

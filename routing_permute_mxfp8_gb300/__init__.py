@@ -18,6 +18,7 @@ __all__ = [
     "MMError", "lib_path", "load", "mm_version", "mm_moe_init_routing", "mm_moe_token_permute",
     "mm_mega_moe", "mm_mega_moe_workspace_size", "mm_prepare_weight_scales", "mm_mx_quantize",
     "DT_FP8_E5M2", "DT_FP8_E4M3FN", "QUANT_NONE", "QUANT_MXFP8_E5M2", "QUANT_MXFP8_E4M3FN",
+    "mm_moe_ep_dispatch", "mm_moe_combine",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -71,10 +72,14 @@ def load():
     L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
     L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
     L.mm_selftest_wait_timeout.argtypes = [i64, p, p]
+    L.mm_moe_ep_dispatch_workspace_size.argtypes = [i64, i64, i64, psz]
+    L.mm_moe_ep_dispatch.argtypes = [p, i32, p, i64, i64, i64, i64, i64, i64, p, p, p, p, p, p, sz, p, p]
+    L.mm_moe_combine.argtypes = [p, p, p, i32, i64, i64, i64, p, p]
     for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
                  "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
                  "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize",
-                 "mm_selftest_wait_timeout"):
+                 "mm_selftest_wait_timeout", "mm_moe_ep_dispatch_workspace_size", "mm_moe_ep_dispatch",
+                 "mm_moe_combine"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -338,6 +343,56 @@ def mm_mx_quantize(src, out_dtype: int = DT_FP8_E4M3FN, scale_cols: int | None =
     _check(L.mm_mx_quantize(_ptr(src), _dt(src), rows, cols, out_dtype, _ptr(q), _ptr(s), sc,
                             _stream(src.device)), "mm_mx_quantize")
     return q, s
+
+
+# --------------------------------------------------------------------------- expert parallelism
+def mm_moe_ep_dispatch(x, topk_ids, moe_expert_num: int, ep_world_size: int,
+                       dispatch_quant_out_dtype: int = DT_FP8_E4M3FN, *, workspace=None, dev_err=None):
+    """Source side of the expert-parallel dispatch (MegaMoE stage 1 with
+    epWorldSize > 1): rows j = i*K + k sorted stably by destination rank
+    id // (E / W), each token MX-quantised once.  Returns (send_x [N*K, H] uint8
+    FP8 codes, send_scales [N*K, H/32] uint8 E8M0, send_expert [N*K] int32 local
+    expert on the destination rank, rank_counts [W] int64, expanded_row_idx
+    [N*K] int32 position of row j in the send order)."""
+    _need_dtype(x, (torch.bfloat16, torch.float16), "x")
+    _need_dtype(topk_ids, (torch.int32,), "topk_ids")
+    _need_cuda(x, topk_ids)
+    L = load()
+    n, h = x.shape
+    k = topk_ids.shape[1]
+    rows = n * k
+    dev = x.device
+    send_x = torch.empty((rows, h), dtype=torch.uint8, device=dev)
+    send_s = torch.empty((rows, h // 32), dtype=torch.uint8, device=dev)
+    send_e = torch.empty(rows, dtype=torch.int32, device=dev)
+    counts = torch.empty(ep_world_size, dtype=torch.int64, device=dev)
+    exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+    need = ctypes.c_size_t(0)
+    _check(L.mm_moe_ep_dispatch_workspace_size(n, k, ep_world_size, ctypes.byref(need)), "mm_moe_ep_dispatch")
+    ws = _workspace(need.value, dev, workspace)
+    _check(L.mm_moe_ep_dispatch(_ptr(x), _dt(x), _ptr(topk_ids), n, h, k, moe_expert_num, ep_world_size,
+                                dispatch_quant_out_dtype, _ptr(send_x), _ptr(send_s), _ptr(send_e), _ptr(counts),
+                                _ptr(exp_idx), _ptr(ws), ws.numel(), _dev_err(dev_err), _stream(dev)),
+           "mm_moe_ep_dispatch")
+    return send_x, send_s, send_e, counts, exp_idx
+
+
+def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None):
+    """Y[i] = sum_k W[i,k] * expert_rows[row_idx[i*K + k]] in fp32, k in order, one
+    bf16 rounding (MegaMoE stage 4); row_idx < 0 leaves a term out.
+    expert_rows [*, H] bf16, row_idx [N*K] int32, topk_weights [N, K] fp32 / bf16."""
+    _need_dtype(expert_rows, (torch.bfloat16,), "expert_rows")
+    _need_dtype(row_idx, (torch.int32,), "row_idx")
+    _need_dtype(topk_weights, (torch.float32, torch.bfloat16), "topk_weights")
+    _need_cuda(expert_rows, row_idx, topk_weights)
+    n, k = topk_weights.shape
+    h = expert_rows.shape[1]
+    if row_idx.numel() != n * k:
+        raise MMError("row_idx must hold N*K entries")
+    y = out if out is not None else torch.empty((n, h), dtype=torch.bfloat16, device=expert_rows.device)
+    _check(load().mm_moe_combine(_ptr(expert_rows), _ptr(row_idx), _ptr(topk_weights), _dt(topk_weights), n, h, k,
+                                 _ptr(y), _stream(expert_rows.device)), "mm_moe_combine")
+    return y
 
 
 # --------------------------------------------------------------------------- diagnostics

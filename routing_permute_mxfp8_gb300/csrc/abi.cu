@@ -674,6 +674,95 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
 }
 
 // ------------------------------------------------------------------------
+// Expert parallelism (MegaMoE README, A8W8-FP stage 1 / stage 4 with
+// epWorldSize > 1): the source-side dispatch and the combine; the exchange
+// between ranks is the caller's collective.
+mm_status mm_moe_ep_dispatch_workspace_size(int64_t num_rows, int64_t k, int64_t ep_world_size, size_t* bytes) {
+  if (!bytes || num_rows < 0 || k <= 0 || k > 32 || ep_world_size <= 0 || ep_world_size > 10240)
+    return MM_ERR_INVALID_ARG;
+  if (num_rows * k >= kSortLimit) return MM_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_routing(c, route_plan(num_rows * k, (int)ep_world_size));
+  *bytes = c.off;
+  return MM_OK;
+}
+
+mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids, int64_t num_rows, int64_t h,
+                             int64_t k, int64_t moe_expert_num, int64_t ep_world_size,
+                             int64_t dispatch_quant_out_dtype, uint8_t* send_x, uint8_t* send_scales,
+                             int32_t* send_expert, int64_t* rank_counts, int32_t* expanded_row_idx, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  size_t need = 0;
+  mm_status s = mm_moe_ep_dispatch_workspace_size(num_rows, k, ep_world_size, &need);
+  if (s != MM_OK) return s;
+  if (moe_expert_num <= 0 || moe_expert_num % ep_world_size != 0 || k > moe_expert_num) return MM_ERR_INVALID_ARG;
+  if (x_dtype != MM_DT_BFLOAT16 && x_dtype != MM_DT_FLOAT16) return MM_ERR_INVALID_ARG;
+  if (!is_fp8(dispatch_quant_out_dtype)) return MM_ERR_UNSUPPORTED;
+  if (h <= 0 || h % 128 != 0) return MM_ERR_UNSUPPORTED;
+  const int64_t rows = num_rows * k;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0)  // nothing to send: every rank receives 0 rows
+    return rank_counts ? cuda_status(cudaMemsetAsync(rank_counts, 0, (size_t)ep_world_size * sizeof(int64_t), st))
+                       : MM_OK;
+  if (!x || !topk_ids || !send_x || !send_scales || !send_expert || !rank_counts || !expanded_row_idx)
+    return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(send_x)) return MM_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
+  // stable sort of the flattened ids by destination rank = id / (E / W);
+  // within a rank the rows stay in (token, choice) order
+  const RoutePlan plan = route_plan(rows, (int)ep_world_size);
+  Carver c(workspace);
+  RoutingWs w = carve_routing(c, plan);
+  RouteOutputs o;
+  o.expanded_row_idx = expanded_row_idx;
+  o.expert_tokens = rank_counts;
+  o.tokens_cumsum = 0;
+  o.key_div = (int)(moe_expert_num / ep_world_size);
+  o.sorted_rem = send_expert;
+  StageScope sr(MM_STAGE_ROUTE, st);
+  int nl = 0;
+  cudaError_t e = launch_route(plan, topk_ids, false, w.hist, w.offsets, o, dev_err, st, &nl);
+  sr.finish(nl);
+  if (e != cudaSuccess) return MM_ERR_CUDA;
+  // Q_MX of each token once, stored at its K positions of the send buffer
+  PermuteArgs a = {};
+  a.src = x;
+  a.src_dtype = x_dtype;
+  a.n = num_rows;
+  a.h = h;
+  a.k = (int)k;
+  a.dest = expanded_row_idx;
+  a.dest_limit = rows;
+  a.ids = topk_ids;
+  a.out_fmt = (int)dispatch_quant_out_dtype;
+  a.out = send_x;
+  a.scales = send_scales;
+  a.scale_cols = h / 32;
+  a.dev_err = dev_err;
+  StageScope sd(MM_STAGE_DISPATCH, st);
+  e = launch_permute(a, st);
+  sd.finish(1);
+  return cuda_status(e);
+}
+
+mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
+                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, void* y, void* stream) {
+  if (num_rows < 0 || h <= 0 || k <= 0 || k > 36) return MM_ERR_INVALID_ARG;
+  if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
+  if (h % 8 != 0) return MM_ERR_UNSUPPORTED;
+  if (num_rows == 0) return MM_OK;
+  if (!expert_rows || !row_idx || !topk_weights || !y || !aligned16(expert_rows) || !aligned16(y))
+    return MM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StageScope sc(MM_STAGE_COMBINE, st);
+  const cudaError_t e =
+      launch_combine_rows(static_cast<const __nv_bfloat16*>(expert_rows), row_idx, topk_weights,
+                          topk_weights_dtype == MM_DT_BFLOAT16, num_rows, h, (int)k, static_cast<__nv_bfloat16*>(y), st);
+  sc.finish(1);
+  return cuda_status(e);
+}
+
+// ------------------------------------------------------------------------
 mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* stream) {
   if (limit_ns <= 0 || limit_ns > 10000000000ll || !dev_err) return MM_ERR_INVALID_ARG;
   return cuda_status(launch_selftest_wait_timeout((uint64_t)limit_ns, dev_err, static_cast<cudaStream_t>(stream)));

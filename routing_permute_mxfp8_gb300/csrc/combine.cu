@@ -67,6 +67,23 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
 
 }  // namespace
 
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
+                                int64_t n, int64_t h, int k, __nv_bfloat16* y, cudaStream_t st) {
+  CombineArgs a;
+  a.o = rows;
+  a.pad_row = row_idx;
+  a.gate = gate;
+  a.gate_bf16 = gate_bf16;
+  a.n_shared = 0;
+  a.seg_mprefix = nullptr;
+  a.n_routed = 0;
+  a.n = n;
+  a.h = h;
+  a.k = k;
+  a.y = y;
+  return launch_combine(a, st);
+}
+
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
   k_combine<<<(unsigned)a.n, kThreads, 0, st>>>(a);

@@ -25,6 +25,8 @@ struct RouteOutputs {
   int32_t* seg_mprefix = nullptr;        // [E + S + 1] prefix of 128-row tiles (or null)
   int n_shared = 0;                      // S shared segments ...
   int shared_rows = 0;                   // ... of this many rows each
+  int key_div = 1;                       // sort key = id / key_div (ids < num_experts * key_div)
+  int32_t* sorted_rem = nullptr;         // [R] id % key_div at each sorted position (or null)
 };
 
 struct RouteScanArgs {
@@ -53,6 +55,12 @@ int64_t route_offsets_words(int num_experts);
 // cooperative launch) or 4.
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches = nullptr);
+
+// ---- combine of rows given by an index (combine.cu) ------------------------
+// Y[i] = sum_k W[i,k] * rows[row_idx[i*K + k]] (row_idx < 0: term left out),
+// fp32 in k order, one bf16 rounding (MegaMoE stage 4 / EP combine).
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
+                                int64_t n, int64_t h, int k, __nv_bfloat16* y, cudaStream_t st);
 
 // ---- permute / quantise (permute.cu) -------------------------------------
 struct PermuteArgs {

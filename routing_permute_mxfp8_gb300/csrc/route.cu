@@ -29,9 +29,12 @@ namespace mm {
 
 // Phase 1, one warp per chunk: counts of each expert in chunk `unit`
 // (cnt: this warp's [E] shared-memory counters).
+// Keys: the sort key of id is id / key_div (1: the expert itself; the number
+// of experts per rank: the destination rank of expert parallelism); ids
+// outside [0, num_experts * key_div) are out of range.
 template <typename IdT>
 __device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                int chunk, int units, int unit, int32_t* cnt,
+                                                int key_div, int chunk, int units, int unit, int32_t* cnt,
                                                 int32_t* __restrict__ hist, int32_t* dev_err) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) cnt[e] = 0;
@@ -40,10 +43,11 @@ __device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int
     const int64_t start = (int64_t)unit * chunk;
     const int64_t end = start + chunk < rows ? start + chunk : rows;
     bool bad = false;
+    const int64_t id_end = (int64_t)num_experts * key_div;
     for (int64_t j = start + lane; j < end; j += 32) {
       const int64_t id = (int64_t)ids[j];
-      if (id >= 0 && id < num_experts)
-        atomicAdd(&cnt[id], 1);
+      if (id >= 0 && id < id_end)
+        atomicAdd(&cnt[key_div == 1 ? id : id / key_div], 1);
       else
         bad = true;
     }
@@ -54,11 +58,11 @@ __device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int
 }
 
 template <typename IdT>
-__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
                              int units, int32_t* __restrict__ hist, int32_t* dev_err) {
   extern __shared__ int32_t sh_cnt[];  // [warps][E]
   const int warp = threadIdx.x >> 5;
-  route_hist_warp(ids, rows, num_experts, chunk, units, blockIdx.x * (blockDim.x >> 5) + warp,
+  route_hist_warp(ids, rows, num_experts, key_div, chunk, units, blockIdx.x * (blockDim.x >> 5) + warp,
                   sh_cnt + warp * num_experts, hist, dev_err);
 }
 
@@ -205,12 +209,13 @@ __global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
 // shared-memory slots).
 template <typename IdT>
 __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                   int chunk, int units, int unit, int32_t* next,
+                                                   int key_div, int chunk, int units, int unit, int32_t* next,
                                                    const int32_t* __restrict__ bases,
                                                    const int32_t* __restrict__ offsets,
                                                    const int32_t* __restrict__ seg_mprefix,
                                                    int32_t* __restrict__ expanded_row_idx,
-                                                   int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row) {
+                                                   int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
+                                                   int32_t* __restrict__ sorted_rem) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
   __syncwarp();
@@ -219,10 +224,13 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
   const unsigned lt = (1u << lane) - 1u;
   for (int64_t j0 = start; j0 < end; j0 += 32) {
     const int64_t j = j0 + lane;
-    int key = -1;
+    int key = -1, rem = 0;
     if (j < end) {
       const int64_t id = (int64_t)ids[j];
-      key = (id >= 0 && id < num_experts) ? (int)id : -1;
+      if (id >= 0 && id < (int64_t)num_experts * key_div) {
+        key = key_div == 1 ? (int)id : (int)(id / key_div);
+        rem = (int)(id - (int64_t)key * key_div);
+      }
     }
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     int32_t dest = -1;
@@ -236,6 +244,7 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
       if (expanded_row_idx) expanded_row_idx[j] = dest;
       if (key >= 0) {
         if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
+        if (sorted_rem) sorted_rem[dest] = rem;
         if (pad_row) pad_row[j] = seg_mprefix[key] * kBM + (dest - offsets[key]);
       } else if (pad_row) {
         pad_row[j] = -1;
@@ -245,17 +254,17 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
 }
 
 template <typename IdT>
-__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk,
+__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
                                 int units, const int32_t* __restrict__ bases,
                                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
                                 int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
-                                int32_t* __restrict__ pad_row) {
+                                int32_t* __restrict__ pad_row, int32_t* __restrict__ sorted_rem) {
   extern __shared__ int32_t sh_next[];  // [warps][E]: next free slot per expert
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x * (blockDim.x >> 5) + warp;
   if (unit >= units) return;
-  route_scatter_warp(ids, rows, num_experts, chunk, units, unit, sh_next + warp * num_experts, bases, offsets,
-                     seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row);
+  route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, sh_next + warp * num_experts, bases,
+                     offsets, seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row, sorted_rem);
 }
 
 // Grid-wide barrier of a cooperative launch (every block is resident) on a
@@ -290,16 +299,17 @@ __device__ __forceinline__ bool grid_barrier_bounded(uint32_t* count, uint32_t b
 // All four phases in one cooperative launch (every block resident), with
 // grid-wide barriers between them: one launch instead of four.
 template <typename IdT>
-__global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int chunk, int units,
-                              int32_t* __restrict__ hist, RouteScanArgs sa, int32_t* __restrict__ expanded_row_idx,
-                              int32_t* __restrict__ pad_row, uint32_t* __restrict__ barrier, int32_t* dev_err) {
+__global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
+                              int units, int32_t* __restrict__ hist, RouteScanArgs sa,
+                              int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ pad_row,
+                              int32_t* __restrict__ sorted_rem, uint32_t* __restrict__ barrier, int32_t* dev_err) {
   extern __shared__ int32_t sh_route[];  // [warps][E]
   __shared__ int64_t sh_warp[33];
   __shared__ int sh_ok;
   const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int unit = blockIdx.x * wpb + warp;
   int32_t* mine = sh_route + warp * num_experts;
-  if (unit < units) route_hist_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, dev_err);
+  if (unit < units) route_hist_warp(ids, rows, num_experts, key_div, chunk, units, unit, mine, hist, dev_err);
   if (!grid_barrier_bounded(barrier, 1, dev_err, &sh_ok)) return;
   if (units <= 32) {
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < num_experts; e += gridDim.x * blockDim.x)
@@ -311,8 +321,8 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
   if (blockIdx.x == 0) route_scan_offsets_block(sa, sh_warp);
   if (!grid_barrier_bounded(barrier, 3, dev_err, &sh_ok)) return;
   if (unit < units)
-    route_scatter_warp(ids, rows, num_experts, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
-                       expanded_row_idx, sa.sorted_row_idx, pad_row);
+    route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
+                       expanded_row_idx, sa.sorted_row_idx, pad_row, sorted_rem);
 }
 
 // ---------------------------------------------------------------------------
@@ -390,12 +400,13 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
   }
   if (cap == cudaStreamCaptureStatusNone && blocks <= fused_capacity<IdT>(wpb)) {
     int64_t rows = p.rows;
-    int ne = p.num_experts, chunk = p.chunk, units = p.units;
+    int ne = p.num_experts, kdiv = o.key_div, chunk = p.chunk, units = p.units;
     int32_t* exp_idx = o.expanded_row_idx;
     int32_t* pad = o.pad_row;
+    int32_t* rem = o.sorted_rem;
     // the barrier counter (workspace, after the offsets and totals) starts at 0
     uint32_t* barrier = reinterpret_cast<uint32_t*>(a.offsets + route_offsets_words(p.num_experts) - 2);
-    void* args[] = {(void*)&ids, &rows, &ne, &chunk, &units, &hist, &a, &exp_idx, &pad, &barrier, &dev_err};
+    void* args[] = {(void*)&ids, &rows, &ne, &kdiv, &chunk, &units, &hist, &a, &exp_idx, &pad, &rem, &barrier, &dev_err};
     if (cudaMemsetAsync(barrier, 0, sizeof(uint32_t), st) != cudaSuccess) return cudaGetLastError();
     if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
         cudaSuccess) {
@@ -404,12 +415,13 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     }
     cudaGetLastError();  // not launched (e.g. no cooperative launch here): the four kernels below
   }
-  k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, dev_err);
+  k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, o.key_div, p.chunk, p.units, hist,
+                                                  dev_err);
   k_route_scan_experts<<<(p.num_experts + 31) / 32, 1024, 0, st>>>(hist, p.num_experts, p.units, a.totals);
   k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
-  k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, p.chunk, p.units, hist, a.offsets,
-                                                     o.seg_mprefix, o.expanded_row_idx, o.sorted_row_idx,
-                                                     o.pad_row);
+  k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, o.key_div, p.chunk, p.units, hist,
+                                                     a.offsets, o.seg_mprefix, o.expanded_row_idx,
+                                                     o.sorted_row_idx, o.pad_row, o.sorted_rem);
   launches = 4;
   return cudaGetLastError();
 }

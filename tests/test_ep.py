@@ -1,0 +1,188 @@
+"""Expert parallelism (MegaMoE README, A8W8-FP stages 1-4 with epWorldSize > 1):
+the exchange plan of routing_permute_mxfp8_gb300.ep with two ranks.
+
+CPU (gloo, two processes): the three kernel entry points the EP path calls
+are replaced, inside the test only, by CPU versions built from the oracle, so
+the collectives, split sizes, row orders and the combine indices are checked
+on the host: the two-rank result must equal, bit for bit, the same fakes run
+on one rank without any exchange, and the oracle's MegaMoE within tolerance.
+
+GPU (two processes on the one GPU, gloo with the buffers staged through host
+memory): the library's kernels on each rank; Y must equal the single-process
+mm_mega_moe bit for bit (each row's GEMMs, its bf16 O and the k-ordered
+combine are the same arithmetic), and the oracle within tolerance.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+W = 2
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _cfg():
+    import synth
+    # 2 ranks x 4 experts; Zipf routing so the two ranks receive unequal row counts
+    return synth.CONFIGS["tiny"].scaled(n=96, e=8, k=3, routing="zipf", dispatch_fmt=23, gate_dtype="bf16")
+
+
+def _problem():
+    import oracle
+    import synth
+    cfg = _cfg()
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    gate = synth.topk_weights(cfg)
+    w1, s1 = oracle.quantized_weights(cfg, 1)
+    w2, s2 = oracle.quantized_weights(cfg, 2)
+    return cfg, x, ids, gate, (w1, s1, w2, s2)
+
+
+def _oracle_fakes(mm, cfg):
+    """CPU stand-ins for mm_moe_ep_dispatch / mm_mega_moe / mm_moe_combine,
+    computed by the oracle (test infrastructure only)."""
+    import oracle
+
+    def dispatch(x, ids, moe_expert_num, world, fmt, workspace=None, dev_err=None):
+        e_local = moe_expert_num // world
+        idn = ids.numpy()
+        n, k = idn.shape
+        h = x.shape[1]
+        srt, exp, cnt, bad = oracle.route((idn // e_local).astype(np.int32), world)
+        assert bad == 0
+        q, sc = oracle.permute(x.view(torch.int16).numpy().view(np.uint16), oracle.DT_BF16, k, srt, n * k, fmt)
+        send_e = (idn.reshape(-1)[srt] % e_local).astype(np.int32)
+        return (torch.from_numpy(q), torch.from_numpy(np.ascontiguousarray(sc[:, :h // 32])), torch.from_numpy(send_e),
+                torch.from_numpy(cnt.astype(np.int64)), torch.from_numpy(exp.astype(np.int32)))
+
+    def mega(xq, ids, gate, w1, w2, s1, s2, e, *, x_scales=None, dispatch_quant_out_dtype=None, **kw):
+        assert kw.get("dispatch_quant_mode") == 0
+        _, yb = oracle.mega_moe_tokens(None, ids.numpy(), gate.numpy(), w1.numpy(), s1.numpy(), w2.numpy(), s2.numpy(),
+                                       dispatch_quant_out_dtype, cfg.weight_fmt,
+                                       x_prequant=(xq.numpy(), x_scales.numpy()))
+        return (torch.from_numpy(yb.view(np.int16)).view(torch.bfloat16),)
+
+    def combine(rows, idx, gate, out=None):
+        r = rows.float().numpy()
+        g = gate.float().numpy()
+        n, k = g.shape
+        acc = np.zeros((n, rows.shape[1]), np.float32)
+        ix = idx.numpy().reshape(n, k)
+        for kk in range(k):
+            ok = ix[:, kk] >= 0
+            acc[ok] += g[ok, kk:kk + 1] * r[ix[ok, kk]]
+        return torch.from_numpy(acc).to(torch.bfloat16)
+
+    mm.mm_moe_ep_dispatch = dispatch
+    mm.mm_mega_moe = mega
+    mm.mm_moe_combine = combine
+
+
+def _slices(cfg, rank):
+    per = cfg.n // W
+    return slice(rank * per, (rank + 1) * per)
+
+
+def _cpu_rank(rank, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    import routing_permute_mxfp8_gb300 as mm
+    from routing_permute_mxfp8_gb300 import ep
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem()
+    _oracle_fakes(mm, cfg)
+    dist.init_process_group("gloo", rank=rank, world_size=W)
+    sl = _slices(cfg, rank)
+    el = cfg.e // W
+    mine = slice(rank * el, (rank + 1) * el)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    xt = t(x[sl].view(np.int16)).view(torch.bfloat16)
+    gt = t(gate[sl].view(np.int16)).view(torch.bfloat16)
+    y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt)
+    # the same fakes on one rank, no exchange: every expert local
+    sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(xt, t(ids[sl]), cfg.e, 1, cfg.dispatch_fmt)
+    o = mm.mm_mega_moe(sx, se.view(-1, 1), torch.ones((sx.shape[0], 1)), t(w1), t(w2), t(s1), t(s2), cfg.e,
+                       x_scales=ss, dispatch_quant_mode=0, dispatch_quant_out_dtype=cfg.dispatch_fmt)[0]
+    y1 = mm.mm_moe_combine(o, ei, gt)
+    out[rank] = (y.view(torch.int16).numpy().copy(), y1.view(torch.int16).numpy().copy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def _check_against_oracle(cfg, x, ids, gate, w, y_bits):
+    import oracle
+    import synth
+    w1, s1, w2, s2 = w
+    y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt)
+    yg = synth.bf16_bits_to_f32(y_bits.view(np.uint16)).astype(np.float64)
+    rel = np.linalg.norm(yg - y_ref) / np.linalg.norm(y_ref)
+    mx = np.abs(yg - y_ref).max() / np.abs(y_ref).max()
+    assert rel <= 5e-3 and mx <= 2e-2, (rel, mx)
+
+
+def test_ep_exchange_two_gloo_ranks_cpu():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_cpu_rank, args=(port, out), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem()
+    ys = []
+    for r in range(W):
+        y, y1 = out[r]
+        assert np.array_equal(y, y1), r          # exchange changes nothing in the result
+        ys.append(y)
+    _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))
+
+
+def _gpu_rank(rank, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    import routing_permute_mxfp8_gb300 as mm
+    from routing_permute_mxfp8_gb300 import ep
+    torch.cuda.set_device(0)
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem()
+    dist.init_process_group("gloo", rank=rank, world_size=W)
+    sl = _slices(cfg, rank)
+    el = cfg.e // W
+    mine = slice(rank * el, (rank + 1) * el)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    xt = t(x[sl].view(np.int16)).view(torch.bfloat16)
+    gt = t(gate[sl].view(np.int16)).view(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err)
+    # single process, all experts on this GPU (ep_world_size = 1)
+    y1 = mm.mm_mega_moe(xt, t(ids[sl]), gt, t(w1), t(w2), t(s1), t(s2), cfg.e, weight_dtype=cfg.weight_fmt,
+                        dispatch_quant_out_dtype=cfg.dispatch_fmt)[0]
+    torch.cuda.synchronize()
+    out[rank] = (y.view(torch.int16).cpu().numpy(), y1.view(torch.int16).cpu().numpy(), int(err.item()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+def test_ep_two_ranks_on_one_gpu_matches_single_process():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_gpu_rank, args=(port, out), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem()
+    ys = []
+    for r in range(W):
+        y, y1, err = out[r]
+        assert err == 0
+        assert np.array_equal(y, y1), r
+        ys.append(y)
+    _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))

@@ -597,3 +597,52 @@ def test_mega_moe_duplicate_ids_flagged():
     err = zeros_err()
     mm.mm_mega_moe(bf16(x), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err)
     assert host(err)[0] & 2
+
+
+# ------------------------------------------------------- expert parallelism
+@pytest.mark.parametrize("w,fmt", [(1, 24), (2, 23), (4, 24), (16, 23)])
+def test_ep_dispatch_bit_exact(w, fmt):
+    """mm_moe_ep_dispatch against the oracle: the stable sort by destination
+    rank id // (E/W) (the routing of MoeInitRoutingV3 on rank keys), Q_MX of
+    every token in the send order, the local expert ids, the per-rank counts
+    and the scatter index."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=300, h=512, e=16, k=4, routing="zipf")
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    el = cfg.e // w
+    err = zeros_err()
+    sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(bf16(x), t(ids), cfg.e, w, fmt, dev_err=err)
+    assert host(err)[0] == 0
+    srt, exp, ocnt, bad = oracle.route((ids // el).astype(np.int32), w)
+    q, sc = oracle.permute(x, oracle.DT_BF16, cfg.k, srt, srt.size, fmt)
+    assert np.array_equal(host(cnt), ocnt)
+    assert np.array_equal(host(ei), exp)
+    assert np.array_equal(host(se), ids.reshape(-1)[srt] % el)
+    assert np.array_equal(host(sx), q)
+    assert np.array_equal(host(ss), sc[:, :cfg.h // 32])
+
+
+@pytest.mark.parametrize("gate_bf16", [False, True])
+def test_moe_combine_rows(gate_bf16):
+    """mm_moe_combine: fp32 sum in k order of weighted rows chosen by an index
+    (negative: left out), one bf16 rounding -- MegaMoE stage 4."""
+    rng = np.random.default_rng(5)
+    n, k, h, nrows = 200, 6, 384, 900
+    rows = rng.standard_normal((nrows, h)).astype(np.float32)
+    rows_b = torch.from_numpy(rows).to(torch.bfloat16)
+    idx = rng.integers(-1, nrows, size=n * k).astype(np.int32)
+    g = rng.random((n, k)).astype(np.float32)
+    gt = torch.from_numpy(g)
+    if gate_bf16:
+        gt = gt.to(torch.bfloat16)
+    y = mm.mm_moe_combine(rows_b.to(DEV), torch.from_numpy(idx).to(DEV), gt.to(DEV))
+    r = rows_b.float().numpy()
+    gw = gt.float().numpy()
+    acc = np.zeros((n, h), np.float32)
+    ix = idx.reshape(n, k)
+    for kk in range(k):
+        ok = ix[:, kk] >= 0
+        # a fused multiply-add: the fp32 product is exact in float64, one rounding to fp32
+        acc[ok] = (gw[ok, kk:kk + 1].astype(np.float64) * r[ix[ok, kk]] + acc[ok]).astype(np.float32)
+    want = torch.from_numpy(acc).to(torch.bfloat16)
+    assert torch.equal(y.cpu(), want)
