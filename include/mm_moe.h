@@ -419,6 +419,30 @@ mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, const int32_t*
 mm_status mm_timing_enable(int on);
 mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n);
 
+/* ------------------------------------------------------------------------
+ * Routing implementation (diagnostics; not part of the pages' API).  Every
+ * routing path computes the same stable counting sort (MoeInitRoutingV3,
+ * formula steps 1-3) bit for bit; this selects which one the following
+ * calls of every entry point use, process-wide:
+ *   MM_ROUTE_AUTO      one thread-block cluster of up to 16 CTAs
+ *                      (distributed shared memory, two cluster barriers)
+ *                      for up to 131072 ids and 4096 keys; otherwise one
+ *                      cooperative grid launch; under
+ *                      stream capture, or where the grid does not fit,
+ *                      four ordinary kernels
+ *   MM_ROUTE_CLUSTER   the cluster kernel whenever the key count allows it
+ *   MM_ROUTE_GRID      the cooperative grid launch (not under capture)
+ *   MM_ROUTE_KERNELS   the four kernels
+ * A path that cannot run for a problem falls through to the next one in
+ * that order.  Returns MM_ERR_INVALID_ARG for any other value.  Host-side
+ * state only.
+ * ---------------------------------------------------------------------- */
+#define MM_ROUTE_AUTO 0
+#define MM_ROUTE_CLUSTER 1
+#define MM_ROUTE_GRID 2
+#define MM_ROUTE_KERNELS 3
+mm_status mm_set_routing_path(int path);
+
 #ifdef __cplusplus
 }
 #endif

@@ -418,6 +418,17 @@ def timing_read():
     return {s: (ms[i], int(cnt[i])) for i, s in enumerate(STAGES)}
 
 
+ROUTE_AUTO, ROUTE_CLUSTER, ROUTE_GRID, ROUTE_KERNELS = 0, 1, 2, 3
+
+
+def set_routing_path(path: int):
+    """Routing implementation for the following calls, process-wide (mm_set_routing_path):
+    ROUTE_AUTO, ROUTE_CLUSTER, ROUTE_GRID or ROUTE_KERNELS.  All give identical results."""
+    L = load()
+    L.mm_set_routing_path.argtypes, L.mm_set_routing_path.restype = [ctypes.c_int], ctypes.c_int
+    _check(L.mm_set_routing_path(int(path)), "mm_set_routing_path")
+
+
 # --------------------------------------------------------------------------- no-allocation variant
 NOALLOC_SCRATCH_BYTES = 4 << 20
 

@@ -276,6 +276,12 @@ mm_status mm_timing_enable(int on) {
   return MM_OK;
 }
 
+mm_status mm_set_routing_path(int path) {
+  if (path < MM_ROUTE_AUTO || path > MM_ROUTE_KERNELS) return MM_ERR_INVALID_ARG;
+  set_route_path(path);
+  return MM_OK;
+}
+
 mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n) {
   if (n < 0 || (n > 0 && (!stage_ms || !stage_launches))) return MM_ERR_INVALID_ARG;
   StageTimer& t = timer();

@@ -52,9 +52,14 @@ int64_t route_offsets_words(int num_experts);
 // hist: [E * units] int32, offsets: [route_offsets_words(E)] int32 (both
 // workspace)
 // *launches (optional) receives the number of kernels launched: 1 (one
-// cooperative launch) or 4.
+// cluster launch or one cooperative launch) or 4.
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches = nullptr);
+// Routing implementation used from now on, process-wide: 0 automatic (one
+// cluster of up to 16 CTAs up to 131072 ids and 4096 keys, else the cooperative grid launch,
+// else four kernels), 1 cluster, 2 cooperative grid, 3 four kernels (a path
+// that cannot run falls through to the next).
+void set_route_path(int path);
 
 // ---- combine of rows given by an index (combine.cu) ------------------------
 // Y[i] = sum_k W[i,k] * rows[row_idx[i*K + k]] (row_idx < 0: term left out),

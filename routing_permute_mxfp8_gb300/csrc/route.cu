@@ -13,19 +13,33 @@
 //                       counts / cumsum outputs, and the 128-row tile table
 //                       the grouped GEMMs use
 //   4. k_route_scatter  each warp walks its chunk in index order and gives
-//                       every id the next slot of its expert (warp match +
-//                       popc for ties inside a 32-wide step), which is the
+//                       every id the next slot of its expert (warp ballots
+//                       + popc for ties inside a 32-wide step), which is the
 //                       stable order; it writes the inverse map and the
 //                       gather index directly.
 // k_route_fused runs the four phases in one cooperative launch, with a
 // grid-wide barrier between phases; the four kernels remain for when its
 // blocks cannot all be resident.
 // No global atomics on the data; the result is deterministic.
+#include <atomic>
 #include <mutex>
 
 #include "mm_route.cuh"
 
 namespace mm {
+
+constexpr int kIdBatch = 8;  // 32-id steps whose loads a warp issues together
+
+// ids j0 + 32 b + lane (b < kIdBatch) of [.., end) into v (0 past the end)
+template <typename IdT>
+__device__ __forceinline__ void route_load_ids(const IdT* __restrict__ ids, int64_t j0, int64_t end, IdT* v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int b = 0; b < kIdBatch; ++b) {
+    const int64_t j = j0 + 32 * b + lane;
+    v[b] = j < end ? ids[j] : IdT(0);
+  }
+}
 
 // Phase 1, one warp per chunk: counts of each expert in chunk `unit`
 // (cnt: this warp's [E] shared-memory counters).
@@ -33,28 +47,44 @@ namespace mm {
 // of experts per rank: the destination rank of expert parallelism); ids
 // outside [0, num_experts * key_div) are out of range.
 template <typename IdT>
-__device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                int key_div, int chunk, int units, int unit, int32_t* cnt,
-                                                int32_t* __restrict__ hist, int32_t* dev_err) {
+__device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                 int key_div, int chunk, int unit, int32_t* cnt, int32_t* dev_err,
+                                                 IdT* v, bool preloaded = false) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) cnt[e] = 0;
   __syncwarp();
-  if (unit < units) {
-    const int64_t start = (int64_t)unit * chunk;
-    const int64_t end = start + chunk < rows ? start + chunk : rows;
-    bool bad = false;
-    const int64_t id_end = (int64_t)num_experts * key_div;
-    for (int64_t j = start + lane; j < end; j += 32) {
-      const int64_t id = (int64_t)ids[j];
+  const int64_t start = (int64_t)unit * chunk;
+  const int64_t end = start + chunk < rows ? start + chunk : rows;
+  bool bad = false;
+  const int64_t id_end = (int64_t)num_experts * key_div;
+  // kIdBatch 32-id steps per round: their loads are all in flight before
+  // the first is counted (preloaded: the caller has loaded the first round)
+  for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
+    if (!(preloaded && j0 == start)) route_load_ids(ids, j0, end, v);
+#pragma unroll
+    for (int b = 0; b < kIdBatch; ++b) {
+      if (j0 + 32 * b + lane >= end) break;
+      const int64_t id = (int64_t)v[b];
       if (id >= 0 && id < id_end)
         atomicAdd(&cnt[key_div == 1 ? id : id / key_div], 1);
       else
         bad = true;
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_err(dev_err, MM_DEVERR_EXPERT_RANGE);
-    __syncwarp();
-    for (int e = lane; e < num_experts; e += 32) hist[(int64_t)e * units + unit] = cnt[e];
   }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) raise_err(dev_err, MM_DEVERR_EXPERT_RANGE);
+  __syncwarp();
+}
+
+// ... and the counts stored to the global [E][units] table
+template <typename IdT>
+__device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                int key_div, int chunk, int units, int unit, int32_t* cnt,
+                                                int32_t* __restrict__ hist, int32_t* dev_err) {
+  const int lane = threadIdx.x & 31;
+  if (unit >= units) return;
+  IdT v[kIdBatch];
+  route_count_warp(ids, rows, num_experts, key_div, chunk, unit, cnt, dev_err, v);
+  for (int e = lane; e < num_experts; e += 32) hist[(int64_t)e * units + unit] = cnt[e];
 }
 
 template <typename IdT>
@@ -205,34 +235,48 @@ __global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
   route_scan_offsets_block(a, sh_warp);
 }
 
-// Phase 4, one warp per chunk, in index order (next: this warp's [E]
-// shared-memory slots).
+// Phase 4, one warp per chunk, in index order: every id of [start, end)
+// takes the next slot of its key (next: this warp's [E] shared-memory slots,
+// initialised to the chunk's first slot of each key); ties inside a 32-id
+// step are ranked by lane (the lanes with an equal key from ballots of the
+// key's bits, then popc), so the order is stable.
+// offsets / seg_mprefix: per-key first slot and GEMM tile prefix (pad_row).
 template <typename IdT>
-__device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                   int key_div, int chunk, int units, int unit, int32_t* next,
-                                                   const int32_t* __restrict__ bases,
-                                                   const int32_t* __restrict__ offsets,
-                                                   const int32_t* __restrict__ seg_mprefix,
+__device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, int64_t start, int64_t end,
+                                                   int num_experts, int key_div, int32_t* next,
+                                                   const int32_t* offsets, const int32_t* seg_mprefix,
                                                    int32_t* __restrict__ expanded_row_idx,
                                                    int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
-                                                   int32_t* __restrict__ sorted_rem) {
+                                                   int32_t* __restrict__ sorted_rem, IdT* v, bool preloaded = false) {
   const int lane = threadIdx.x & 31;
-  for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
-  __syncwarp();
-  const int64_t start = (int64_t)unit * chunk;
-  const int64_t end = start + chunk < rows ? start + chunk : rows;
   const unsigned lt = (1u << lane) - 1u;
+  const int key_bits = 32 - __clz(num_experts);  // bits of the largest key + 1
   for (int64_t j0 = start; j0 < end; j0 += 32) {
+    const int b = (int)(((j0 - start) >> 5) % kIdBatch);
+    // the next kIdBatch steps' ids, loaded together (preloaded: the caller
+    // has loaded the first round)
+    if (b == 0 && !(preloaded && j0 == start)) route_load_ids(ids, j0, end, v);
+    IdT idv = v[0];
+#pragma unroll
+    for (int i = 1; i < kIdBatch; ++i)
+      if (b == i) idv = v[i];
     const int64_t j = j0 + lane;
     int key = -1, rem = 0;
     if (j < end) {
-      const int64_t id = (int64_t)ids[j];
+      const int64_t id = (int64_t)idv;
       if (id >= 0 && id < (int64_t)num_experts * key_div) {
         key = key_div == 1 ? (int)id : (int)(id / key_div);
         rem = (int)(id - (int64_t)key * key_div);
       }
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    // lanes holding the same key: one ballot per bit of key + 1 (the
+    // invalid key -1 becomes 0), all bits equal
+    const uint32_t kk = (uint32_t)(key + 1);
+    unsigned peers = 0xffffffffu;
+    for (int bit = 0; bit < key_bits; ++bit) {
+      const unsigned m = __ballot_sync(0xffffffffu, (kk >> bit) & 1u);
+      peers &= ((kk >> bit) & 1u) ? m : ~m;
+    }
     int32_t dest = -1;
     if (key >= 0) {
       dest = next[key] + __popc(peers & lt);
@@ -251,6 +295,25 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
       }
     }
   }
+}
+
+template <typename IdT>
+__device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                   int key_div, int chunk, int units, int unit, int32_t* next,
+                                                   const int32_t* __restrict__ bases,
+                                                   const int32_t* __restrict__ offsets,
+                                                   const int32_t* __restrict__ seg_mprefix,
+                                                   int32_t* __restrict__ expanded_row_idx,
+                                                   int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
+                                                   int32_t* __restrict__ sorted_rem) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
+  __syncwarp();
+  const int64_t start = (int64_t)unit * chunk;
+  const int64_t end = start + chunk < rows ? start + chunk : rows;
+  IdT v[kIdBatch];
+  route_scatter_walk(ids, start, end, num_experts, key_div, next, offsets, seg_mprefix, expanded_row_idx,
+                     sorted_row_idx, pad_row, sorted_rem, v);
 }
 
 template <typename IdT>
@@ -326,6 +389,177 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
 }
 
 // ---------------------------------------------------------------------------
+// Problems of up to kClusterMaxRows ids: the whole routing in one
+// thread-block cluster of up to 16 CTAs (one per 4096 ids), which exchange
+// their per-expert counts through distributed shared memory, with two
+// hardware cluster barriers instead of three grid-wide barriers on global
+// memory.
+//   1. each warp counts its chunk (CTA c owns the chunks c*W .. c*W+W-1, in
+//      index order; chunks of up to kIdBatch 32-id steps stay in registers
+//      for step 3), then each CTA scans its warps' counts per expert
+//      (exclusive, in place) and keeps its own per-expert total;
+//   -- cluster barrier: every CTA's totals are visible --
+//   2. every CTA reads all CTAs' totals (the prefix over the CTAs before it,
+//      and the expert totals) and scans the totals into the expert offsets
+//      and the GEMM segment table in shared memory (CTA 0 also writes the
+//      outputs);
+//   -- arrival: this CTA no longer reads the others' shared memory --
+//   3. each warp walks its chunk as in k_route_scatter;
+//   -- wait: no CTA leaves while another may still read its totals --
+// The cluster's CTAs are co-scheduled by the hardware, so the barriers have
+// the standing of __syncthreads: every thread reaches both.
+constexpr int kClusterMaxCtas = 16;
+constexpr int64_t kClusterRowsPerCta = 4096;
+constexpr int64_t kClusterMinWarpIds = 128;
+constexpr int64_t kClusterMaxRows = 131072;
+constexpr int kClusterMaxExperts = 4096;
+constexpr int kClusterCntWords = 32768;  // per-warp counters: warps * E <= this
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the int32 at the same shared-memory offset in CTA `cta` of the cluster
+__device__ __forceinline__ int32_t ld_cluster_peer(const int32_t* local, uint32_t cta) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(cta));
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+template <typename IdT>
+__global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ ids, int64_t rows, int num_experts,
+                                                        int key_div, int chunk, RouteScanArgs sa,
+                                                        int32_t* __restrict__ expanded_row_idx,
+                                                        int32_t* __restrict__ pad_row,
+                                                        int32_t* __restrict__ sorted_rem, int32_t* dev_err) {
+  extern __shared__ int32_t sh_cl[];
+  __shared__ int64_t sh_warp[33];
+  const int E = num_experts, nt = blockDim.x, W = nt >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t c = cluster_ctarank(), ncta = cluster_nctarank();
+  const int nseg = E + sa.n_shared;
+  int32_t* cnt = sh_cl;           // [W][E] counts, then each warp's next slots
+  int32_t* ctot = cnt + W * E;    // [E] this CTA's per-expert total (read by the others)
+  int32_t* cpre = ctot + E;       // [E] the CTAs before this one: their per-expert total
+  int32_t* etot = cpre + E;       // [E] expert totals
+  int32_t* eoff = etot + E;       // [E + 1] expert offsets
+  int32_t* mpre = eoff + E + 1;   // [nseg + 1] tile prefix of the GEMM segments
+  const int unit = (int)c * W + warp;
+  int32_t* mine = cnt + warp * E;
+  const int64_t start = (int64_t)unit * chunk;
+  const int64_t end = start + chunk < rows ? start + chunk : rows;
+  const bool resident = chunk <= 32 * kIdBatch;  // the whole chunk fits one round of loads
+  IdT v[kIdBatch];
+  route_load_ids(ids, start, end, v);
+
+  route_count_warp(ids, rows, E, key_div, chunk, unit, mine, dev_err, v, true);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += nt) {
+    int32_t run = 0;
+    for (int w = 0; w < W; ++w) {
+      const int32_t x = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += x;
+    }
+    ctot[e] = run;
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  for (int e = threadIdx.x; e < E; e += nt) {
+    int32_t pre = 0, tot = 0;
+    for (uint32_t q0 = 0; q0 < ncta; q0 += 4) {
+      int32_t x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = q0 + u < ncta ? ld_cluster_peer(ctot + e, q0 + u) : 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (q0 + u < c) pre += x[u];
+        tot += x[u];
+      }
+    }
+    cpre[e] = pre;
+    etot[e] = tot;
+  }
+  cluster_arrive_release();
+  __syncthreads();
+
+  // expert offsets, counts / cumsum, gather-index tail and the GEMM segment
+  // table from one scan over the segments (routed experts, then the shared
+  // ones): an entry packs its rows counted in the expert offsets (high word)
+  // and its 128-row tiles (low word); neither sum reaches 2^32
+  {
+    const int nsc = sa.seg_mprefix ? nseg : E;
+    const int per = (nsc + nt - 1) / nt;
+    const int lo = min(nsc, (int)threadIdx.x * per), hi = min(nsc, lo + per);
+    auto pack = [&](int sg) -> int64_t {
+      const int64_t r = sg < E ? etot[sg] : sa.shared_rows;
+      return ((sg < E ? r : 0) << 32) | ((r + kBM - 1) / kBM);
+    };
+    int64_t sum = 0;
+    for (int sg = lo; sg < hi; ++sg) sum += pack(sg);
+    int64_t total;
+    int64_t base = block_exclusive_scan(sum, sh_warp, total);
+    for (int sg = lo; sg < hi; ++sg) {
+      const int32_t off = (int32_t)(base >> 32), tiles = (int32_t)(base & 0xffffffff);
+      if (sg < E) {
+        const int32_t ce = etot[sg];
+        eoff[sg] = off;
+        if (c == 0) {
+          sa.offsets[sg] = off;
+          sa.totals[sg] = ce;
+          if (sa.expert_tokens) sa.expert_tokens[sg] = sa.tokens_cumsum ? (int64_t)off + ce : (int64_t)ce;
+          if (sa.expert_token_nums) sa.expert_token_nums[sg] = ce;
+        }
+      }
+      if (sa.seg_mprefix) {
+        mpre[sg] = tiles;
+        if (c == 0) {
+          sa.seg_rows[sg] = sg < E ? etot[sg] : sa.shared_rows;
+          sa.seg_mprefix[sg] = tiles;
+        }
+      }
+      base += pack(sg);
+    }
+    const int64_t routed = total >> 32;
+    if (threadIdx.x == 0) {
+      eoff[E] = (int32_t)routed;
+      if (c == 0) sa.offsets[E] = (int32_t)routed;
+      if (sa.seg_mprefix) {
+        mpre[nseg] = (int32_t)(total & 0xffffffff);
+        if (c == 0) sa.seg_mprefix[nseg] = (int32_t)(total & 0xffffffff);
+      }
+    }
+    // rows whose id was out of range are left out: pad the gather index
+    if (sa.sorted_row_idx)
+      for (int64_t d = routed + (int64_t)c * nt + threadIdx.x; d < rows; d += (int64_t)ncta * nt)
+        sa.sorted_row_idx[d] = -1;
+  }
+  __syncthreads();
+
+  for (int e = lane; e < E; e += 32) mine[e] += eoff[e] + cpre[e];
+  __syncwarp();
+  route_scatter_walk(ids, start, end, E, key_div, mine, eoff, mpre, expanded_row_idx, sa.sorted_row_idx, pad_row,
+                     sorted_rem, v, resident);
+  cluster_wait_acquire();
+}
+
+// ---------------------------------------------------------------------------
 RoutePlan route_plan(int64_t rows, int num_experts) {
   RoutePlan p;
   p.rows = rows;
@@ -385,9 +619,116 @@ int fused_capacity(int wpb) {
   return cap[dev][wpb];
 }
 
+// Path selection for tests and measurements (mm_set_routing_path):
+// 0 automatic, 1 cluster, 2 cooperative grid, 3 four kernels.
+std::atomic<int> g_route_path{0};
+
+// Warps per CTA of k_route_cluster for E experts, and its shared memory.
+int cluster_warps(int num_experts) {
+  const int w = kClusterCntWords / (num_experts < 1 ? 1 : num_experts);
+  return w < 1 ? 1 : (w > 32 ? 32 : w);
+}
+size_t cluster_smem(int wpb, int num_experts, int nseg) {
+  return 4 * ((size_t)wpb * num_experts + 4 * (size_t)num_experts + 1 + (size_t)nseg + 1);
+}
+// the largest cluster_smem of any accepted problem (E <= kClusterMaxExperts,
+// at most 4 shared segments)
+constexpr size_t kClusterMaxSmem = 4 * ((size_t)kClusterCntWords + 5 * (size_t)kClusterMaxExperts + 8);
+
+cudaLaunchConfig_t cluster_config(int ncta, int wpb, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ncta);
+  cfg.blockDim = dim3(wpb * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// The largest cluster (16, else 8 CTAs; 0: none) of k_route_cluster with
+// `wpb` warps per CTA and the largest shared-memory size that fits on the
+// current device (queried once per device and block size).
+template <typename IdT>
+int cluster_max_ctas(int wpb) {
+  static std::mutex mu;
+  static int fits[kMaxDevices][33];
+  static bool init[kMaxDevices] = {false};
+  int dev = 0;
+  if (wpb < 1 || wpb > 32 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (!init[dev]) {
+    for (int w = 0; w < 33; ++w) fits[dev][w] = -1;
+    init[dev] = true;
+  }
+  if (fits[dev][wpb] < 0) {
+    int best = 0;
+    if (cudaFuncSetAttribute(k_route_cluster<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClusterMaxSmem) == cudaSuccess) {
+      const bool big = cudaFuncSetAttribute(k_route_cluster<IdT>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                            1) == cudaSuccess;
+      for (int n : {kClusterMaxCtas, 8}) {
+        if (n > 8 && !big) continue;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = cluster_config(n, wpb, kClusterMaxSmem, nullptr, attr);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, k_route_cluster<IdT>, &cfg) == cudaSuccess && active >= 1) {
+          best = n;
+          break;
+        }
+      }
+    }
+    cudaGetLastError();
+    fits[dev][wpb] = best;
+  }
+  return fits[dev][wpb];
+}
+
+template <typename IdT>
+bool launch_route_cluster(const RoutePlan& p, const IdT* ids, RouteScanArgs a, const RouteOutputs& o,
+                          int32_t* dev_err, cudaStream_t st) {
+  if (p.num_experts > kClusterMaxExperts || a.n_shared > 4 || (o.pad_row && !o.seg_mprefix)) return false;
+  // one CTA per kClusterRowsPerCta ids (at most 16); warps of at least
+  // kClusterMinWarpIds ids (at least 4, at most what the counters allow)
+  int64_t ncta = (p.rows + kClusterRowsPerCta - 1) / kClusterRowsPerCta;
+  ncta = ncta < 1 ? 1 : (ncta > kClusterMaxCtas ? kClusterMaxCtas : ncta);
+  const int64_t per_cta = (p.rows + ncta - 1) / ncta;
+  int64_t w = (per_cta + kClusterMinWarpIds - 1) / kClusterMinWarpIds;
+  const int wmax = cluster_warps(p.num_experts);
+  w = w < 4 ? 4 : w;
+  const int wpb = (int)(w > wmax ? wmax : w);
+  const int max_ctas = cluster_max_ctas<IdT>(wpb);
+  if (max_ctas < 1) return false;
+  if (ncta > max_ctas) ncta = max_ctas;
+  int64_t per = (p.rows + ncta * wpb - 1) / (ncta * wpb);
+  per = round_up(per < 32 ? 32 : per, 32);
+  if (per > INT32_MAX) return false;
+  const int64_t rows = p.rows;
+  const int ne = p.num_experts, kdiv = o.key_div, chunk = (int)per;
+  int32_t* exp_idx = o.expanded_row_idx;
+  int32_t* pad = o.pad_row;
+  int32_t* rem = o.sorted_rem;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config((int)ncta, wpb, cluster_smem(wpb, ne, ne + a.n_shared), st, attr);
+  if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, kdiv, chunk, a, exp_idx, pad, rem, dev_err) ==
+      cudaSuccess)
+    return true;
+  cudaGetLastError();
+  return false;
+}
+
 template <typename IdT>
 cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist, RouteScanArgs a,
                                const RouteOutputs& o, int32_t* dev_err, cudaStream_t st, int& launches) {
+  const int path = g_route_path.load();
+  if ((path == 1 || (path == 0 && p.rows <= kClusterMaxRows)) && launch_route_cluster(p, ids, a, o, dev_err, st)) {
+    launches = 1;
+    return cudaSuccess;
+  }
   const int wpb = p.warps_per_block;
   const int blocks = (p.units + wpb - 1) / wpb;
   const size_t sh = (size_t)wpb * p.num_experts * sizeof(int32_t);
@@ -398,7 +739,7 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     cudaGetLastError();
     cap = cudaStreamCaptureStatusActive;
   }
-  if (cap == cudaStreamCaptureStatusNone && blocks <= fused_capacity<IdT>(wpb)) {
+  if (path != 3 && cap == cudaStreamCaptureStatusNone && blocks <= fused_capacity<IdT>(wpb)) {
     int64_t rows = p.rows;
     int ne = p.num_experts, kdiv = o.key_div, chunk = p.chunk, units = p.units;
     int32_t* exp_idx = o.expanded_row_idx;
@@ -427,6 +768,8 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
 }
 
 }  // namespace
+
+void set_route_path(int path) { g_route_path.store(path); }
 
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches) {

@@ -93,6 +93,13 @@ def test_selftest_wait_timeout_host_validation(lib):
     assert lib.mm_selftest_wait_timeout(1_000_000, None, None) == 1                    # dev_err required
 
 
+def test_routing_path_selector(lib):
+    for path in (1, 2, 3, 0):
+        assert lib.mm_set_routing_path(path) == 0
+    assert lib.mm_set_routing_path(-1) == 1
+    assert lib.mm_set_routing_path(4) == 1
+
+
 def test_mega_moe_host_rejections(lib):
     assert _mega(lib, ep=2) == 2                     # ep_world_size != 1
     assert _mega(lib, cqm=3) == 2                    # combine quantisation

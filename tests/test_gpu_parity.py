@@ -100,6 +100,38 @@ def test_init_routing_bit_exact(n, h, e, k, quant, kind):
         assert np.array_equal(host(sc), r_sc)
 
 
+ROUTE_PATHS = {"cluster": mm.ROUTE_CLUSTER, "grid": mm.ROUTE_GRID, "kernels": mm.ROUTE_KERNELS}
+
+
+@pytest.fixture
+def route_path(request):
+    """Runs the test with one routing implementation forced, then restores the automatic choice."""
+    mm.set_routing_path(ROUTE_PATHS[request.param])
+    yield request.param
+    mm.set_routing_path(mm.ROUTE_AUTO)
+
+
+@pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
+@pytest.mark.parametrize("case", [ROUTE_CASES[i] for i in (1, 3, 4, 5, 6, 8)])
+def test_init_routing_every_path(route_path, case):
+    """The cluster kernel, the cooperative grid launch and the four kernels
+    give the oracle's bits (E up to 2048, ragged chunks, repeated ids)."""
+    test_init_routing_bit_exact(*case)
+
+
+@pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
+def test_routing_paths_out_of_range_and_empty(route_path):
+    test_out_of_range_ids_are_left_out_and_flagged()
+    test_empty_batch_writes_zero_counts(0)
+    test_empty_batch_writes_zero_counts(1)
+
+
+@pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
+@pytest.mark.parametrize("case", ["zipf_shared_e5m2_h512", "max_experts", "topk32_shared4"])
+def test_mega_moe_every_routing_path(route_path, case):
+    run_mega(synth.CONFIGS["tiny"].scaled(**MEGA_CASES[case]))
+
+
 @pytest.mark.parametrize("dtype,idx64,num_out,quant,one_d", [
     (torch.bfloat16, False, 6, -1, False),
     (torch.float16, True, 0, 2, False),
@@ -532,10 +564,11 @@ def test_mega_moe_dsv3_decode_gelu_full_size():
     run_mega(cfg, tokens=np.array([0, 31, 64, 127]), layout=1, sparse=True)
 
 
-def test_mega_moe_in_cuda_graph():
+@pytest.mark.parametrize("route_path", ["cluster", "kernels"], indirect=True)
+def test_mega_moe_in_cuda_graph(route_path):
     """The whole call captured in a CUDA graph (caller's workspace and
-    output; routing then takes its ordinary launches) replays to the same Y
-    bits as a direct call, and matches the oracle."""
+    output; routing as one cluster launch, or as its four ordinary kernels)
+    replays to the same Y bits as a direct call."""
     cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1)
     x, ids, gate = bf16(synth.tokens_bf16(cfg)), t(synth.topk_ids(cfg)), t(synth.topk_weights(cfg))
     w1, s1, w2, s2 = (t(a) for a in _weights(cfg))
@@ -600,6 +633,11 @@ def test_mega_moe_duplicate_ids_flagged():
 
 
 # ------------------------------------------------------- expert parallelism
+@pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
+def test_ep_dispatch_every_routing_path(route_path):
+    test_ep_dispatch_bit_exact(4, 24)
+
+
 @pytest.mark.parametrize("w,fmt", [(1, 24), (2, 23), (4, 24), (16, 23)])
 def test_ep_dispatch_bit_exact(w, fmt):
     """mm_moe_ep_dispatch against the oracle: the stable sort by destination
