@@ -62,6 +62,9 @@ typedef enum {
 #define MM_DEVERR_EXPERT_RANGE 1 /* an expert id outside [0, expert_num): row left out */
 #define MM_DEVERR_DUPLICATE_ID 2 /* a token lists one expert twice (MegaMoE forbids it) */
 #define MM_DEVERR_TIMEOUT 4      /* a bounded wait inside a kernel gave up */
+#define MM_DEVERR_BOUNDS 8       /* checked build only (mm_checked_build): an index computed on
+                                    the GPU fell outside the buffer it addresses; that access
+                                    was skipped */
 
 /* Element type codes.  The FP8 / FP4 codes are the MegaMoE dtype codes
  * (dispatchQuantOutDtype: 23 = FLOAT8_E5M2, 24 = FLOAT8_E4M3FN,
@@ -442,6 +445,20 @@ mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n);
 #define MM_ROUTE_GRID 2
 #define MM_ROUTE_KERNELS 3
 mm_status mm_set_routing_path(int path);
+
+/* ------------------------------------------------------------------------
+ * Checked build (a debug aid; not part of the pages' API).  The same
+ * sources compiled with MM_CHECK give libmm_moe_check.so, whose kernels
+ * test every index they compute on the GPU (a routed row's slot against
+ * the expanded-row count, a padded row against the grouped-layout
+ * capacity, a GEMM tile against the tile count of its segment and of the
+ * buffers, a combine term's row against the expert-row buffer) before the
+ * access it guards; a failed test skips the access and ORs
+ * MM_DEVERR_BOUNDS into *dev_err, so an internal inconsistency shows up as
+ * a status bit instead of a memory fault.  The ABI is identical.
+ * mm_checked_build returns 1 in that library and 0 in libmm_moe.so.
+ * ---------------------------------------------------------------------- */
+int mm_checked_build(void);
 
 #ifdef __cplusplus
 }

@@ -22,8 +22,11 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libmm_moe.so")
-_lib = None
+_LIB_PATHS = {False: os.path.join(_HERE, "libmm_moe.so"), True: os.path.join(_HERE, "libmm_moe_check.so")}
+_libs = {}
+# the checked build (device index checks, MM_DEVERR_BOUNDS) instead of the
+# normal one: use_checked_library(True), or MM_MOE_CHECKED=1 in the environment
+_checked = os.environ.get("MM_MOE_CHECKED", "0") == "1"
 
 DT_F32, DT_F16, DT_I32, DT_I64, DT_BF16 = 0, 1, 3, 9, 27
 DT_FP8_E5M2, DT_FP8_E4M3FN = 23, 24
@@ -44,17 +47,27 @@ class MMError(RuntimeError):
 
 
 def lib_path() -> str:
-    return _LIB_PATH
+    return _LIB_PATHS[_checked]
+
+
+def use_checked_library(on: bool = True):
+    """Route the following calls to libmm_moe_check.so (the checked build,
+    whose kernels report MM_DEVERR_BOUNDS for an index outside its buffer)
+    or back to libmm_moe.so.  Each library keeps its own host-side state
+    (timing, routing path, no-allocation scratch)."""
+    global _checked
+    _checked = bool(on)
 
 
 def load():
-    """Load libmm_moe.so; raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(_LIB_PATH):
-        raise MMError(f"{_LIB_PATH} is missing: build it with `python -m routing_permute_mxfp8_gb300.build`")
-    L = ctypes.CDLL(_LIB_PATH)
+    """Load the selected library (libmm_moe.so, or libmm_moe_check.so after
+    use_checked_library(True)); raises if it has not been built."""
+    path = _LIB_PATHS[_checked]
+    if path in _libs:
+        return _libs[path]
+    if not os.path.exists(path):
+        raise MMError(f"{path} is missing: build it with `python -m routing_permute_mxfp8_gb300.build`")
+    L = ctypes.CDLL(path)
     p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     psz = ctypes.POINTER(ctypes.c_size_t)
     L.mm_status_string.argtypes, L.mm_status_string.restype = [i32], ctypes.c_char_p
@@ -81,7 +94,7 @@ def load():
                  "mm_selftest_wait_timeout", "mm_moe_ep_dispatch_workspace_size", "mm_moe_ep_dispatch",
                  "mm_moe_combine"):
         getattr(L, name).restype = i32
-    _lib = L
+    _libs[path] = L
     return L
 
 

@@ -276,6 +276,8 @@ mm_status mm_timing_enable(int on) {
   return MM_OK;
 }
 
+int mm_checked_build(void) { return kChecked ? 1 : 0; }
+
 mm_status mm_set_routing_path(int path) {
   if (path < MM_ROUTE_AUTO || path > MM_ROUTE_KERNELS) return MM_ERR_INVALID_ARG;
   set_route_path(path);
@@ -540,6 +542,7 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   RouteOutputs o;
   o.expanded_row_idx = expanded_row_idx ? expanded_row_idx : w.exp_idx;
   o.pad_row = w.pad_row;
+  o.pad_limit = d.rows_cap;
   o.expert_token_nums = expert_token_nums;
   o.seg_rows = w.seg_rows;
   o.seg_mprefix = w.seg_mprefix;
@@ -640,6 +643,8 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   ca.h = d.h;
   ca.k = (int)d.k;
   ca.y = static_cast<__nv_bfloat16*>(y);
+  ca.rows_cap = d.rows_cap;
+  ca.dev_err = dev_err;
   StageScope sc(MM_STAGE_COMBINE, st);
   e = launch_combine(ca, st);
   sc.finish(1);
@@ -656,6 +661,8 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
     ua.cols = d.h;
     ua.dst_q = dispatch_q;
     ua.dst_sf = dispatch_scale;
+    ua.rows_cap = d.rows_cap;
+    ua.dev_err = dev_err;
     StageScope su(MM_STAGE_DIAG, st);
     e = launch_unpad(ua, st);
     su.finish(1);
@@ -671,6 +678,8 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
     ua.cols = aw;
     ua.dst_q = act_q;
     ua.dst_sf = act_scale;
+    ua.rows_cap = d.rows_cap;
+    ua.dev_err = dev_err;
     StageScope su(MM_STAGE_DIAG, st);
     e = launch_unpad(ua, st);
     su.finish(1);

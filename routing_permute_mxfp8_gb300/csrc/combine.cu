@@ -20,12 +20,14 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
   const int nterm = a.k + a.n_shared;
   if (threadIdx.x < a.k) {
     const int64_t j = i * a.k + threadIdx.x;
-    rows[threadIdx.x] = a.pad_row[j];
+    const int32_t r = a.pad_row[j];
+    rows[threadIdx.x] = in_bounds(r < a.rows_cap, a.dev_err) ? r : -1;
     w[threadIdx.x] = a.gate_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.gate)[j])
                                  : static_cast<const float*>(a.gate)[j];
   } else if (threadIdx.x < nterm) {
     const int s = threadIdx.x - a.k;
-    rows[threadIdx.x] = a.seg_mprefix[a.n_routed + s] * kBM + (int32_t)i;
+    const int64_t r = (int64_t)a.seg_mprefix[a.n_routed + s] * kBM + i;
+    rows[threadIdx.x] = in_bounds(r >= 0 && r < a.rows_cap, a.dev_err) ? (int32_t)r : -1;
     w[threadIdx.x] = 1.0f;
   }
   __syncthreads();
@@ -81,6 +83,8 @@ cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_id
   a.h = h;
   a.k = k;
   a.y = y;
+  a.rows_cap = INT64_MAX;  // the caller's row buffer: its size is not known here
+  a.dev_err = nullptr;
   return launch_combine(a, st);
 }
 

@@ -105,11 +105,22 @@ struct GemmArgs {
   int act;
   float act_c, act_alpha, act_beta, act_rbeta, act_beta_lin, act_rbeta_lin, act_gelu_k;
   int aw;
+  int mtiles_cap;  // 128-row tiles of the A / output buffers (checked build)
 };
 
 struct TileInfo {
   int seg, mt, nt;
 };
+
+// Checked build: the tile's rows lie inside its segment and inside the
+// buffers (every role skips a tile that fails; the producer reports it).
+__device__ __forceinline__ bool tile_fits(const GemmArgs& g, const int32_t* mpre, const TileInfo& ti) {
+  if (!kChecked) return true;
+  const int am = mpre[ti.seg] + ti.mt;
+  const int rows_s = g.seg_rows[ti.seg];
+  return ti.seg >= 0 && ti.seg < g.nseg && am >= 0 && am < g.mtiles_cap && rows_s >= 0 &&
+         rows_s <= (mpre[ti.seg + 1] - mpre[ti.seg]) * kBM;
+}
 
 __device__ __forceinline__ TileInfo decode_tile(int t, const int32_t* mpre, int nseg, int n_tiles) {
   int lo = 0, hi = nseg;
@@ -302,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
+        if (!in_bounds(tile_fits(g, mpre, ti), g.dev_err)) continue;
         const bool sh = ti.seg >= g.n_routed;
         const int e = sh ? ti.seg - g.n_routed : ti.seg;
         const CUtensorMap* mb = sh ? &tmBs : &tmB;
@@ -355,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
+        if (!tile_fits(g, mpre, ti)) continue;
         const uint32_t idb = ti.seg >= g.n_routed ? g.idesc_sh : g.idesc;
         const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
         if (!wait_bounded(&acc_empty[buf], (use & 1) ^ 1)) {
@@ -390,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(&acc_full[buf]);
+        ++tcount;
       }
       if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
       tc_commit(drain);  // all MMAs / copies of this thread complete before TMEM is freed
@@ -406,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     uint32_t tcount = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_merged(t, bpre, spre, nseg, g.n_tiles);
+      if (!tile_fits(g, mpre, ti)) continue;
       const uint32_t buf = tcount % kAcc, use = tcount / kAcc;
       if (!wait_bounded(&acc_full[buf], use & 1)) {
         ok = false;
@@ -532,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ++tcount;
     }
     if (g.o_stage && lane == 0) bulk_wait_all();
     if (!ok) raise_err(g.dev_err, MM_DEVERR_TIMEOUT);
@@ -721,6 +737,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.act_sf = L.act_sf;
   g.out = L.out;
   g.dev_err = L.dev_err;
+  g.mtiles_cap = (int)(L.rows_cap / kBM);
   // upper bound of the tile count decides how many persistent CTAs to start
   const int64_t max_mtiles = L.rows_cap / kBM;
   int64_t grid = max_mtiles * g.n_tiles;

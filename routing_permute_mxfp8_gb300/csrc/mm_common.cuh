@@ -109,6 +109,20 @@ __device__ __forceinline__ void raise_err(int32_t* dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
 }
 
+// Checked build (compiled with MM_CHECK): in_bounds(ok, dev_err) reports a
+// failed index test as MM_DEVERR_BOUNDS and returns it, so the caller skips
+// the access; in the normal build it is `true` and the test compiles away.
+#ifdef MM_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* dev_err) {
+  if (!kChecked) return true;
+  if (!ok) raise_err(dev_err, MM_DEVERR_BOUNDS);
+  return ok;
+}
+
 // Limit of every wait inside a kernel (a mbarrier phase, a grid barrier):
 // past it the kernel raises MM_DEVERR_TIMEOUT and stops instead of hanging.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s

@@ -27,6 +27,7 @@ struct RouteOutputs {
   int shared_rows = 0;                   // ... of this many rows each
   int key_div = 1;                       // sort key = id / key_div (ids < num_experts * key_div)
   int32_t* sorted_rem = nullptr;         // [R] id % key_div at each sorted position (or null)
+  int64_t pad_limit = 0;                 // rows of the padded layout pad_row addresses (checked build)
 };
 
 struct RouteScanArgs {
@@ -134,6 +135,8 @@ struct CombineArgs {
   int64_t n, h;
   int k;
   __nv_bfloat16* y;           // [n, h]
+  int64_t rows_cap;           // rows of o (checked build)
+  int32_t* dev_err;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
@@ -146,6 +149,8 @@ struct UnpadArgs {
   int64_t rows, cols;
   uint8_t* dst_q;             // [rows, cols]
   uint8_t* dst_sf;            // [rows, cols/32]
+  int64_t rows_cap;           // rows of src_q (checked build)
+  int32_t* dev_err;
 };
 cudaError_t launch_unpad(const UnpadArgs& a, cudaStream_t st);
 

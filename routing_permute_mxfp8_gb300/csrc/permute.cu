@@ -76,7 +76,8 @@ __device__ __forceinline__ void load_dests(const PermuteArgs& a, int64_t row, in
       d = a.dest ? a.dest[row * a.k + t] : (int32_t)row;
       if (d >= a.dest_limit) d = -1;
     } else if (t < ndest) {
-      d = (int32_t)((int64_t)a.extra_base[t - a.k] * kBM + row);
+      const int64_t de = (int64_t)a.extra_base[t - a.k] * kBM + row;
+      d = in_bounds(de >= 0 && de < a.dest_limit, a.dev_err) ? (int32_t)de : -1;
     }
     if (h == 0) d0 = d; else d1 = d;
   }
@@ -233,7 +234,7 @@ __global__ void k_unpad(UnpadArgs a) {
   const int64_t j = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
   if (j >= a.rows) return;
   const int32_t d = a.expanded_row_idx[j], p = a.pad_row[j];
-  if (d < 0 || p < 0) return;
+  if (d < 0 || p < 0 || !in_bounds(d < a.rows && p < a.rows_cap, a.dev_err)) return;
   for (int64_t c = lane * 16; c < a.cols; c += 512)
     *reinterpret_cast<uint4*>(a.dst_q + (int64_t)d * a.cols + c) =
         *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * a.cols + c);

@@ -247,7 +247,9 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
                                                    const int32_t* offsets, const int32_t* seg_mprefix,
                                                    int32_t* __restrict__ expanded_row_idx,
                                                    int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
-                                                   int32_t* __restrict__ sorted_rem, IdT* v, bool preloaded = false) {
+                                                   int32_t* __restrict__ sorted_rem, int64_t rows_total,
+                                                   int64_t pad_limit, int32_t* dev_err, IdT* v,
+                                                   bool preloaded = false) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   const int key_bits = 32 - __clz(num_experts);  // bits of the largest key + 1
@@ -287,9 +289,14 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
     if (j < end) {
       if (expanded_row_idx) expanded_row_idx[j] = dest;
       if (key >= 0) {
-        if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
-        if (sorted_rem) sorted_rem[dest] = rem;
-        if (pad_row) pad_row[j] = seg_mprefix[key] * kBM + (dest - offsets[key]);
+        if (in_bounds(dest < rows_total, dev_err)) {
+          if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
+          if (sorted_rem) sorted_rem[dest] = rem;
+        }
+        if (pad_row) {
+          const int32_t pr = seg_mprefix[key] * kBM + (dest - offsets[key]);
+          pad_row[j] = in_bounds(pr >= 0 && pr < pad_limit, dev_err) ? pr : -1;
+        }
       } else if (pad_row) {
         pad_row[j] = -1;
       }
@@ -305,7 +312,8 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
                                                    const int32_t* __restrict__ seg_mprefix,
                                                    int32_t* __restrict__ expanded_row_idx,
                                                    int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
-                                                   int32_t* __restrict__ sorted_rem) {
+                                                   int32_t* __restrict__ sorted_rem, int64_t pad_limit,
+                                                   int32_t* dev_err) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) next[e] = offsets[e] + bases[(int64_t)e * units + unit];
   __syncwarp();
@@ -313,7 +321,7 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
   const int64_t end = start + chunk < rows ? start + chunk : rows;
   IdT v[kIdBatch];
   route_scatter_walk(ids, start, end, num_experts, key_div, next, offsets, seg_mprefix, expanded_row_idx,
-                     sorted_row_idx, pad_row, sorted_rem, v);
+                     sorted_row_idx, pad_row, sorted_rem, rows, pad_limit, dev_err, v);
 }
 
 template <typename IdT>
@@ -321,13 +329,14 @@ __global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int n
                                 int units, const int32_t* __restrict__ bases,
                                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
                                 int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
-                                int32_t* __restrict__ pad_row, int32_t* __restrict__ sorted_rem) {
+                                int32_t* __restrict__ pad_row, int32_t* __restrict__ sorted_rem, int64_t pad_limit,
+                                int32_t* dev_err) {
   extern __shared__ int32_t sh_next[];  // [warps][E]: next free slot per expert
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x * (blockDim.x >> 5) + warp;
   if (unit >= units) return;
   route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, sh_next + warp * num_experts, bases,
-                     offsets, seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row, sorted_rem);
+                     offsets, seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row, sorted_rem, pad_limit, dev_err);
 }
 
 // Grid-wide barrier of a cooperative launch (every block is resident) on a
@@ -365,7 +374,8 @@ template <typename IdT>
 __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
                               int units, int32_t* __restrict__ hist, RouteScanArgs sa,
                               int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ pad_row,
-                              int32_t* __restrict__ sorted_rem, uint32_t* __restrict__ barrier, int32_t* dev_err) {
+                              int32_t* __restrict__ sorted_rem, int64_t pad_limit, uint32_t* __restrict__ barrier,
+                              int32_t* dev_err) {
   extern __shared__ int32_t sh_route[];  // [warps][E]
   __shared__ int64_t sh_warp[33];
   __shared__ int sh_ok;
@@ -385,7 +395,7 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
   if (!grid_barrier_bounded(barrier, 3, dev_err, &sh_ok)) return;
   if (unit < units)
     route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
-                       expanded_row_idx, sa.sorted_row_idx, pad_row, sorted_rem);
+                       expanded_row_idx, sa.sorted_row_idx, pad_row, sorted_rem, pad_limit, dev_err);
 }
 
 // ---------------------------------------------------------------------------
@@ -446,7 +456,8 @@ __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ 
                                                         int key_div, int chunk, RouteScanArgs sa,
                                                         int32_t* __restrict__ expanded_row_idx,
                                                         int32_t* __restrict__ pad_row,
-                                                        int32_t* __restrict__ sorted_rem, int32_t* dev_err) {
+                                                        int32_t* __restrict__ sorted_rem, int64_t pad_limit,
+                                                        int32_t* dev_err) {
   extern __shared__ int32_t sh_cl[];
   __shared__ int64_t sh_warp[33];
   const int E = num_experts, nt = blockDim.x, W = nt >> 5;
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ 
   for (int e = lane; e < E; e += 32) mine[e] += eoff[e] + cpre[e];
   __syncwarp();
   route_scatter_walk(ids, start, end, E, key_div, mine, eoff, mpre, expanded_row_idx, sa.sorted_row_idx, pad_row,
-                     sorted_rem, v, resident);
+                     sorted_rem, rows, pad_limit, dev_err, v, resident);
   cluster_wait_acquire();
 }
 
@@ -714,7 +725,8 @@ bool launch_route_cluster(const RoutePlan& p, const IdT* ids, RouteScanArgs a, c
   int32_t* rem = o.sorted_rem;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config((int)ncta, wpb, cluster_smem(wpb, ne, ne + a.n_shared), st, attr);
-  if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, kdiv, chunk, a, exp_idx, pad, rem, dev_err) ==
+  const int64_t plim = o.pad_limit;
+  if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, kdiv, chunk, a, exp_idx, pad, rem, plim, dev_err) ==
       cudaSuccess)
     return true;
   cudaGetLastError();
@@ -745,9 +757,11 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     int32_t* exp_idx = o.expanded_row_idx;
     int32_t* pad = o.pad_row;
     int32_t* rem = o.sorted_rem;
+    int64_t plim = o.pad_limit;
     // the barrier counter (workspace, after the offsets and totals) starts at 0
     uint32_t* barrier = reinterpret_cast<uint32_t*>(a.offsets + route_offsets_words(p.num_experts) - 2);
-    void* args[] = {(void*)&ids, &rows, &ne, &kdiv, &chunk, &units, &hist, &a, &exp_idx, &pad, &rem, &barrier, &dev_err};
+    void* args[] = {(void*)&ids, &rows, &ne, &kdiv, &chunk, &units, &hist, &a, &exp_idx, &pad, &rem, &plim, &barrier,
+                    &dev_err};
     if (cudaMemsetAsync(barrier, 0, sizeof(uint32_t), st) != cudaSuccess) return cudaGetLastError();
     if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
         cudaSuccess) {
@@ -762,7 +776,7 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
   k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
   k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, o.key_div, p.chunk, p.units, hist,
                                                      a.offsets, o.seg_mprefix, o.expanded_row_idx,
-                                                     o.sorted_row_idx, o.pad_row, o.sorted_rem);
+                                                     o.sorted_row_idx, o.pad_row, o.sorted_rem, o.pad_limit, dev_err);
   launches = 4;
   return cudaGetLastError();
 }

@@ -38,6 +38,22 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    """libmm_moe_check.so (MM_CHECK: device index checks) has the same ABI
+    and says which build it is."""
+    checked = ctypes.CDLL(os.path.join(os.path.dirname(mm.lib_path()), "libmm_moe_check.so"))
+    missing = [n for n in declared_functions() if not hasattr(checked, n)]
+    assert not missing, missing
+    assert checked.mm_checked_build() == 1
+    assert lib.mm_checked_build() == 0
+    mm.use_checked_library(True)
+    try:
+        assert mm.lib_path().endswith("libmm_moe_check.so") and mm.load().mm_checked_build() == 1
+    finally:
+        mm.use_checked_library(False)
+    assert mm.load().mm_checked_build() == 0
+
+
 def test_status_strings(lib):
     assert lib.mm_status_string(0) == b"ok"
     assert lib.mm_status_string(3) == b"workspace too small"
@@ -144,8 +160,9 @@ def test_permute_host_rejections(lib):
 
 def test_binding_fails_loudly_without_its_library(monkeypatch, tmp_path):
     """No fallback path: with the CUDA library absent the binding raises."""
-    monkeypatch.setattr(mm, "_LIB_PATH", str(tmp_path / "absent" / "libmm_moe.so"))
-    monkeypatch.setattr(mm, "_lib", None)
+    absent = str(tmp_path / "absent" / "libmm_moe.so")
+    monkeypatch.setattr(mm, "_LIB_PATHS", {False: absent, True: absent})
+    monkeypatch.setattr(mm, "_libs", {})
     with pytest.raises(mm.MMError):
         mm.load()
 
