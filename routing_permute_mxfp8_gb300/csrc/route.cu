@@ -17,10 +17,16 @@
 //                       + popc for ties inside a 32-wide step), which is the
 //                       stable order; it writes the inverse map and the
 //                       gather index directly.
-// k_route_fused runs the four phases in one cooperative launch, with a
-// grid-wide barrier between phases; the four kernels remain for when its
-// blocks cannot all be resident.
-// No global atomics on the data; the result is deterministic.
+// Three implementations of the same sort, chosen per call:
+//   k_route_cluster  up to 131072 ids: the phases inside one thread-block
+//                    cluster (per-CTA counts exchanged through distributed
+//                    shared memory, two hardware cluster barriers);
+//   k_route_fused    larger problems: the four phases in one cooperative
+//                    launch with a grid-wide barrier between phases;
+//   the four kernels when the cooperative grid cannot be resident, or under
+//                    stream capture.
+// No global atomics on the data; the result is deterministic and identical
+// on every path.
 #include <atomic>
 #include <mutex>
 
