@@ -160,7 +160,10 @@ __device__ __forceinline__ TileInfo decode_merged(int t, const int32_t* bpre, co
 //   swigluoai   G_c sigma(alpha G_c) (U_c + beta)
 //   situglu     beta tanh(G / beta) sigma(G) L(U), L(U) = U or beta_lin tanh(U / beta_lin)
 //   gelu        Z sigma(sqrt(8/pi) (Z + 0.044715 Z^3)), element-wise (gv = Z)
-__device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+// (CUDA's fast intrinsics __expf and __fdividef; the epilogue's arithmetic
+// competes with the MMA issue and the loads for the SM's issue slots, so
+// its instruction count shows in the GEMM's time on short-K shapes)
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void act_chunk(const GemmArgs& g, const uint32_t* gv, const uint32_t* uv, bool gelu,
                                           float* a) {
@@ -197,6 +200,14 @@ __device__ __forceinline__ void act_chunk(const GemmArgs& g, const uint32_t* gv,
       }
       break;
     default:  // swiglu
+      if (c == INFINITY) {  // no clamp: SiLU(G) U = G / (1 + e^-G) * U
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float gf = __uint_as_float(gv[j]), uf = __uint_as_float(uv[j]);
+          a[j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+        }
+        break;
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float gc = fminf(__uint_as_float(gv[j]), c), uf = __uint_as_float(uv[j]);
