@@ -343,9 +343,23 @@ def stage_rooflines(cfg, ms, hbm_peak, fp8_peak):
     # combine: O rows, gating weights and indices read; Y written
     hbm("combine", rows * cfg.h * 2 + cfg.n * cfg.k * (gate_b + 4) + cfg.n * cfg.h * 2)
     if ms.get("gemm2"):
-        tf = 2.0 * rows * cfg.h * cfg.act_width / (ms["gemm2"] / 1e3) / 1e12
-        out["gemm2"] = {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s",
-                        "frac": tf / fp8_peak, "ms": ms["gemm2"]}
+        # the bound by arithmetic intensity against the ridge, as for GEMM1;
+        # compulsory bytes: W2 and its scales of every expert, A_hat and its
+        # scales read, bf16 O written
+        sec = ms["gemm2"] / 1e3
+        flops = 2.0 * rows * cfg.h * cfg.act_width
+        wb = 0.5 if cfg.weight_fmt == 296 else 1.0
+        nbytes = ((cfg.e + cfg.shared) * cfg.h * cfg.act_width * (wb + 1 / 32) +
+                  rows * cfg.act_width * (1 + 1 / 32) + rows * cfg.h * 2)
+        tf, gbs = flops / sec / 1e12, nbytes / sec / 1e9
+        hbm_bound = flops / nbytes < fp8_peak * 1e12 / (hbm_peak * 1e9)
+        out["gemm2"] = {"bound": "hbm" if hbm_bound else "tensor",
+                        "achieved": gbs if hbm_bound else tf, "peak": hbm_peak if hbm_bound else fp8_peak,
+                        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                        "frac": gbs / hbm_peak if hbm_bound else tf / fp8_peak,
+                        "frac_hbm": gbs / hbm_peak, "frac_tensor": tf / fp8_peak, "achieved_tflops": tf,
+                        "achieved_gbs": gbs, "algorithmic_bytes": nbytes,
+                        "arithmetic_intensity_flop_per_byte": flops / nbytes, "ms": ms["gemm2"]}
     if ms.get("route"):
         out["route"] = {"bound": "latency", "us": ms["route"] * 1e3}
     return out
