@@ -421,6 +421,12 @@ mm_status mm_moe_init_routing_noalloc(const void* x, int x_dtype, const int32_t*
 #define MM_STAGE_COUNT 7
 mm_status mm_timing_enable(int on);
 mm_status mm_timing_read(double* stage_ms, int64_t* stage_launches, int n);
+/* mm_timing_select: which stages record their event pair while timing is on
+ * (bit s = stage s; all stages by default).  Each event record between two
+ * kernels costs the stream a few microseconds, so a measurement of the whole
+ * call can keep the pair of one stage only.  MM_ERR_INVALID_ARG for bits at
+ * or above MM_STAGE_COUNT. */
+mm_status mm_timing_select(uint32_t stage_mask);
 
 /* ------------------------------------------------------------------------
  * Routing implementation (diagnostics; not part of the pages' API).  Every

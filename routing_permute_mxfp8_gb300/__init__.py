@@ -419,6 +419,14 @@ def timing_enable(on: bool = True):
     _check(L.mm_timing_enable(1 if on else 0), "mm_timing_enable")
 
 
+def timing_select(stages=None):
+    """Record events only around the named stages (all when None) while timing is on (mm_timing_select)."""
+    L = load()
+    mask = (1 << len(STAGES)) - 1 if stages is None else sum(1 << STAGES.index(s) for s in stages)
+    L.mm_timing_select.argtypes, L.mm_timing_select.restype = [ctypes.c_uint32], ctypes.c_int
+    _check(L.mm_timing_select(mask), "mm_timing_select")
+
+
 def timing_read():
     """{stage: (device ms summed over recorded calls, kernel launches)} since the last read."""
     L = load()

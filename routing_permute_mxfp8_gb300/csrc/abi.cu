@@ -131,6 +131,7 @@ namespace mm {
 struct StageTimer {
   std::mutex mu;
   bool on = false;
+  uint32_t mask = (1u << MM_STAGE_COUNT) - 1;  // stages that record events
   std::vector<cudaEvent_t> pool;
   std::vector<cudaEvent_t> open[MM_STAGE_COUNT];  // begin, end, begin, end, ...
   int64_t launches[MM_STAGE_COUNT] = {0};
@@ -154,7 +155,7 @@ static cudaEvent_t take_event(StageTimer& t) {
 StageScope::StageScope(int s, cudaStream_t stream) : stage(s), st(stream), active(false) {
   StageTimer& t = timer();
   std::lock_guard<std::mutex> g(t.mu);
-  if (t.on) {
+  if (t.on && ((t.mask >> stage) & 1u)) {
     cudaEvent_t ev = take_event(t);
     if (ev && cudaEventRecord(ev, st) == cudaSuccess) {
       t.open[stage].push_back(ev);
@@ -281,6 +282,14 @@ int mm_checked_build(void) { return kChecked ? 1 : 0; }
 mm_status mm_set_routing_path(int path) {
   if (path < MM_ROUTE_AUTO || path > MM_ROUTE_KERNELS) return MM_ERR_INVALID_ARG;
   set_route_path(path);
+  return MM_OK;
+}
+
+mm_status mm_timing_select(uint32_t stage_mask) {
+  if (stage_mask >> MM_STAGE_COUNT) return MM_ERR_INVALID_ARG;
+  StageTimer& t = timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.mask = stage_mask;
   return MM_OK;
 }
 

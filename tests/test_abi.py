@@ -109,6 +109,13 @@ def test_selftest_wait_timeout_host_validation(lib):
     assert lib.mm_selftest_wait_timeout(1_000_000, None, None) == 1                    # dev_err required
 
 
+def test_timing_stage_selector(lib):
+    lib.mm_timing_select.argtypes = [ctypes.c_uint32]
+    assert lib.mm_timing_select(1 << 3) == 0        # GEMM1 only
+    assert lib.mm_timing_select(1 << 7) == 1        # no such stage
+    assert lib.mm_timing_select((1 << 7) - 1) == 0  # every stage (the default)
+
+
 def test_routing_path_selector(lib):
     for path in (1, 2, 3, 0):
         assert lib.mm_set_routing_path(path) == 0
