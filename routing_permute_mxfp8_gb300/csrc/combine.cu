@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
   __shared__ float w[kMaxTerms];
   const int64_t i = blockIdx.x;
   const int nterm = a.k + a.n_shared;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < a.k) {
     const int64_t j = i * a.k + threadIdx.x;
     const int32_t r = a.pad_row[j];
@@ -90,8 +92,7 @@ cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_id
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
-  k_combine<<<(unsigned)a.n, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace mm

@@ -253,6 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = g.nseg;
+  // set-up that reads nothing an earlier kernel wrote, before the wait for it
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kAcc; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 32 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (nseg > g.n_routed) prefetch_tensormap(&tmBs);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i <= nseg; i += kThreads) mpre[i] = g.seg_mprefix[i];
   __syncthreads();
   if (warp == 2) {
@@ -286,22 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       spre[nseg] = is;
     }
   }
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < kAcc; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 32 * kEpiWarps);
-    }
-    mbar_init(drain, 1);
-    fence_barrier_init();
-    prefetch_tensormap(&tmA);
-    prefetch_tensormap(&tmB);
-    if (nseg > g.n_routed) prefetch_tensormap(&tmBs);
-  }
-  if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -666,8 +669,7 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(ma, mb, mbs, mo, g);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, ma, mb, mbs, mo, g);
 }
 
 }  // namespace

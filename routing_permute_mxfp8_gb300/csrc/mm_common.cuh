@@ -123,6 +123,33 @@ __device__ __forceinline__ bool in_bounds(bool ok, int32_t* dev_err) {
   return ok;
 }
 
+// Programmatic dependent launch.  A kernel started by launch_pdl may begin
+// while the kernel before it on the stream is still finishing; it calls
+// pdl_wait() before it reads anything an earlier kernel wrote (the wait
+// returns once the previous grid has completed and its writes are visible;
+// it is a no-op in a kernel launched without the attribute), and
+// pdl_trigger() lets the next kernel begin launching once every CTA of this
+// one has called it.  What a kernel does before pdl_wait() touches only its
+// own shared memory, barriers and tensor memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Limit of every wait inside a kernel (a mbarrier phase, a grid barrier):
 // past it the kernel raises MM_DEVERR_TIMEOUT and stops instead of hanging.
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s

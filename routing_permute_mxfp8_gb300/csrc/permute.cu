@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5
   const int gw = (int)blockIdx.x * kWarpsPerBlock + warp;  // n * wpt < 2^31 (checked at launch)
   const int row = wpt == 1 ? gw : gw / wpt;
   const int part = gw - row * wpt;
+  pdl_wait();
+  pdl_trigger();
   if (row >= a.n) return;
   int32_t d0, d1;
   int ndest;
@@ -179,6 +181,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int gw = (int)blockIdx.x * kWarpsPerBlock + warp;  // n * wpt < 2^31 (checked at launch)
   const int row = wpt == 1 ? gw : gw / wpt;
   const int part = gw - row * wpt;
+  pdl_wait();
+  pdl_trigger();
   if (row >= a.n) return;
   int32_t d0, d1;
   int ndest;
@@ -251,6 +255,8 @@ __global__ void k_unpad(UnpadArgs a) {
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(PermuteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+  pdl_wait();
+  pdl_trigger();
   if (row >= a.n) return;
   int32_t d0, d1;
   int ndest;
@@ -285,10 +291,10 @@ cudaError_t launch_mx_variant(const PermuteArgs& a, int, cudaStream_t st) {
   if (a.n * wpt > 0x7fffffff - kWarpsPerBlock) return cudaErrorInvalidValue;
   const int64_t blocks = ceil_div(a.n * wpt, kWarpsPerBlock);
   if (a.scale_cols == 0)
-    k_permute_mx<kSrc, kFmt, true><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, st>>>(a, (int)wpt, span);
-  else
-    k_permute_mx<kSrc, kFmt, false><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, st>>>(a, (int)wpt, span);
-  return cudaGetLastError();
+    return launch_pdl(k_permute_mx<kSrc, kFmt, true>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st, a,
+                      (int)wpt, span);
+  return launch_pdl(k_permute_mx<kSrc, kFmt, false>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st, a,
+                    (int)wpt, span);
 }
 
 template <int kSrc>
@@ -307,8 +313,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
   const int blocks = (int)blocks64;
   if (a.src_scales) {  // pre-quantised rows into the tile layout
     if (a.scale_cols != 0 || a.h % 128 != 0) return cudaErrorInvalidValue;
-    k_permute_prequant<<<blocks, kWarpsPerBlock * 32, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_permute_prequant, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, st, a);
   }
   if (a.out_fmt < 0) {
     const int esz = a.src_dtype == MM_DT_FLOAT32 ? 4 : 2;
@@ -319,9 +324,8 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
     const int64_t span = ceil_div(slices, wpt) * 512;
     wpt = ceil_div(rb, span);
     if (a.n * wpt > 0x7fffffff - kWarpsPerBlock) return cudaErrorInvalidValue;
-    k_permute_copy<<<(unsigned)ceil_div(a.n * wpt, kWarpsPerBlock), kWarpsPerBlock * 32, 0, st>>>(a, esz, (int)wpt,
-                                                                                               span);
-    return cudaGetLastError();
+    return launch_pdl(k_permute_copy, dim3((unsigned)ceil_div(a.n * wpt, kWarpsPerBlock)), dim3(kWarpsPerBlock * 32),
+                      0, st, a, esz, (int)wpt, span);
   }
   if (a.src_dtype == MM_DT_BFLOAT16) return launch_mx_src<MM_DT_BFLOAT16>(a, blocks, st);
   if (a.src_dtype == MM_DT_FLOAT16) return launch_mx_src<MM_DT_FLOAT16>(a, blocks, st);

@@ -478,6 +478,8 @@ __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ 
   int32_t* mpre = eoff + E + 1;   // [nseg + 1] tile prefix of the GEMM segments
   const int unit = (int)c * W + warp;
   int32_t* mine = cnt + warp * E;
+  pdl_wait();
+  pdl_trigger();
   const int64_t start = (int64_t)unit * chunk;
   const int64_t end = start + chunk < rows ? start + chunk : rows;
   const bool resident = chunk <= 32 * kIdBatch;  // the whole chunk fits one round of loads
@@ -652,18 +654,23 @@ size_t cluster_smem(int wpb, int num_experts, int nseg) {
 // at most 4 shared segments)
 constexpr size_t kClusterMaxSmem = 4 * ((size_t)kClusterCntWords + 5 * (size_t)kClusterMaxExperts + 8);
 
-cudaLaunchConfig_t cluster_config(int ncta, int wpb, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+// launch configuration of one cluster of k_route_cluster (attr: room for
+// two attributes; pdl adds the programmatic dependent launch)
+cudaLaunchConfig_t cluster_config(int ncta, int wpb, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr,
+                                  bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ncta;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(ncta);
   cfg.blockDim = dim3(wpb * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cfg;
 }
 
@@ -690,7 +697,7 @@ int cluster_max_ctas(int wpb) {
                                             1) == cudaSuccess;
       for (int n : {kClusterMaxCtas, 8}) {
         if (n > 8 && !big) continue;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = cluster_config(n, wpb, kClusterMaxSmem, nullptr, attr);
         int active = 0;
         if (cudaOccupancyMaxActiveClusters(&active, k_route_cluster<IdT>, &cfg) == cudaSuccess && active >= 1) {
@@ -729,8 +736,8 @@ bool launch_route_cluster(const RoutePlan& p, const IdT* ids, RouteScanArgs a, c
   int32_t* exp_idx = o.expanded_row_idx;
   int32_t* pad = o.pad_row;
   int32_t* rem = o.sorted_rem;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config((int)ncta, wpb, cluster_smem(wpb, ne, ne + a.n_shared), st, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config((int)ncta, wpb, cluster_smem(wpb, ne, ne + a.n_shared), st, attr, true);
   const int64_t plim = o.pad_limit;
   if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, kdiv, chunk, a, exp_idx, pad, rem, plim, dev_err) ==
       cudaSuccess)
