@@ -58,6 +58,13 @@ ROUTE_CASES = [
     (16384, 7168, 256, 8, -1, "distinct"),       # full routing workload, bf16 copy
     (16384, 7168, 256, 8, 3, "distinct"),        # full routing workload, MXFP8 E4M3
     (8388607, 16, 256, 2, 3, "any"),             # N*K = 16777214, the largest the sort limit allows
+    # the automatic choice's boundaries: 131072 ids (one 16-CTA cluster) and
+    # 131080 (the cooperative grid); 4096 keys (cluster, 8 warps per CTA)
+    # and 4097 (grid)
+    (16384, 32, 256, 8, 2, "any"),
+    (16385, 32, 256, 8, 2, "any"),
+    (300, 32, 4096, 12, -1, "distinct"),
+    (300, 32, 4097, 12, 3, "distinct"),
 ]
 
 
@@ -112,7 +119,7 @@ def route_path(request):
 
 
 @pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
-@pytest.mark.parametrize("case", [ROUTE_CASES[i] for i in (1, 3, 4, 5, 6, 8)])
+@pytest.mark.parametrize("case", [ROUTE_CASES[i] for i in (1, 3, 4, 5, 6, 8, 10, 12)])
 def test_init_routing_every_path(route_path, case):
     """The cluster kernel, the cooperative grid launch and the four kernels
     give the oracle's bits (E up to 2048, ragged chunks, repeated ids)."""
