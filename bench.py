@@ -688,6 +688,11 @@ def run_ours(args):
     ridge = fp8_peak * 1e12 / (hbm_peak * 1e9)          # FLOP per byte where the two roofs meet
     intensity = g1_flops / g1_bytes
     bound = "tensor" if intensity > ridge else "hbm"
+    # the tensor cores work on 128-row tiles: rows the MMAs compute, padding
+    # of every expert's (and shared expert's) rows to a multiple of 128 included
+    counts = np.bincount(ids.reshape(-1).cpu().numpy(), minlength=cfg.e)
+    padded_rows = 128 * (int(np.sum((counts + 127) // 128)) + cfg.shared * ((cfg.n + 127) // 128))
+    g1_exec_tflops = 2.0 * padded_rows * 2 * cfg.inter * cfg.h / (g1_ms / 1e3) / 1e12
     roofline = {"bound": bound, "kernel": "k_gemm_mx<1> (GEMM1 + swiglu + MX requant)",
                 "achieved": g1_tflops if bound == "tensor" else g1_gbs,
                 "peak": fp8_peak if bound == "tensor" else hbm_peak,
@@ -699,6 +704,8 @@ def run_ours(args):
                 "arithmetic_intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
                 "algorithmic_flops_per_launch": g1_flops, "algorithmic_bytes_per_launch": g1_bytes,
                 "avg_launch_ms": g1_ms,
+                "mma_rows": padded_rows, "padding_frac": 1.0 - rows / padded_rows,
+                "frac_tensor_mma_rows": g1_exec_tflops / fp8_peak,
                 "peak_source": (f"hbm: {peak_src} copy bandwidth; tensor: {'burst' if burst else 'sustained'} dense "
                                 f"MXFP8 rate measured in this run at 8192^3, the higher of cuBLASLt's block-scaled "
                                 f"GEMM and k_gemm_mx; the timed region being {ms / 1e3:.2f} s"),
