@@ -28,6 +28,7 @@
 // No global atomics on the data; the result is deterministic and identical
 // on every path.
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "mm_route.cuh"
@@ -70,11 +71,19 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
 #pragma unroll
     for (int b = 0; b < kIdBatch; ++b) {
       if (j0 + 32 * b + lane >= end) break;
-      const int64_t id = (int64_t)v[b];
-      if (id >= 0 && id < id_end)
-        atomicAdd(&cnt[key_div == 1 ? id : id / key_div], 1);
-      else
-        bad = true;
+      if (key_div == 1) {
+        using UIdT = typename std::make_unsigned<IdT>::type;
+        if ((UIdT)v[b] < (UIdT)num_experts)
+          atomicAdd(&cnt[(int)v[b]], 1);
+        else
+          bad = true;
+      } else {
+        const int64_t id = (int64_t)v[b];
+        if (id >= 0 && id < id_end)
+          atomicAdd(&cnt[id / key_div], 1);
+        else
+          bad = true;
+      }
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_err(dev_err, MM_DEVERR_EXPERT_RANGE);
@@ -259,52 +268,58 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   const int key_bits = 32 - __clz(num_experts);  // bits of the largest key + 1
-  for (int64_t j0 = start; j0 < end; j0 += 32) {
-    const int b = (int)(((j0 - start) >> 5) % kIdBatch);
+  using UIdT = typename std::make_unsigned<IdT>::type;
+  const int64_t id_end = (int64_t)num_experts * key_div;
+  for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
     // the next kIdBatch steps' ids, loaded together (preloaded: the caller
     // has loaded the first round)
-    if (b == 0 && !(preloaded && j0 == start)) route_load_ids(ids, j0, end, v);
-    IdT idv = v[0];
+    if (!(preloaded && j0 == start)) route_load_ids(ids, j0, end, v);
 #pragma unroll
-    for (int i = 1; i < kIdBatch; ++i)
-      if (b == i) idv = v[i];
-    const int64_t j = j0 + lane;
-    int key = -1, rem = 0;
-    if (j < end) {
-      const int64_t id = (int64_t)idv;
-      if (id >= 0 && id < (int64_t)num_experts * key_div) {
-        key = key_div == 1 ? (int)id : (int)(id / key_div);
-        rem = (int)(id - (int64_t)key * key_div);
+    for (int b = 0; b < kIdBatch; ++b) {
+      const int64_t jb = j0 + 32 * b;
+      if (jb >= end) break;  // uniform across the warp
+      const int64_t j = jb + lane;
+      const bool in = j < end;
+      int key = -1, rem = 0;
+      if (in) {
+        if (key_div == 1) {
+          if ((UIdT)v[b] < (UIdT)num_experts) key = (int)v[b];
+        } else {
+          const int64_t id = (int64_t)v[b];
+          if (id >= 0 && id < id_end) {
+            key = (int)(id / key_div);
+            rem = (int)(id - (int64_t)key * key_div);
+          }
+        }
       }
-    }
-    // lanes holding the same key: one ballot per bit of key + 1 (the
-    // invalid key -1 becomes 0), all bits equal
-    const uint32_t kk = (uint32_t)(key + 1);
-    unsigned peers = 0xffffffffu;
-    for (int bit = 0; bit < key_bits; ++bit) {
-      const unsigned m = __ballot_sync(0xffffffffu, (kk >> bit) & 1u);
-      peers &= ((kk >> bit) & 1u) ? m : ~m;
-    }
-    int32_t dest = -1;
-    if (key >= 0) {
-      dest = next[key] + __popc(peers & lt);
-    }
-    __syncwarp();
-    if (key >= 0 && (peers & lt) == 0) next[key] += __popc(peers);
-    __syncwarp();
-    if (j < end) {
-      if (expanded_row_idx) expanded_row_idx[j] = dest;
-      if (key >= 0) {
-        if (in_bounds(dest < rows_total, dev_err)) {
-          if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
-          if (sorted_rem) sorted_rem[dest] = rem;
+      // lanes holding the same key: one ballot per bit of key + 1 (the
+      // invalid key -1 becomes 0), all bits equal
+      const uint32_t kk = (uint32_t)(key + 1);
+      unsigned peers = 0xffffffffu;
+      for (int bit = 0; bit < key_bits; ++bit) {
+        const unsigned m = __ballot_sync(0xffffffffu, (kk >> bit) & 1u);
+        peers &= ((kk >> bit) & 1u) ? m : ~m;
+      }
+      const unsigned below = peers & lt;
+      int32_t dest = -1;
+      if (key >= 0) dest = next[key] + __popc(below);
+      __syncwarp();
+      if (key >= 0 && below == 0) next[key] += __popc(peers);
+      __syncwarp();
+      if (in) {
+        if (expanded_row_idx) expanded_row_idx[j] = dest;
+        if (key >= 0) {
+          if (in_bounds(dest < rows_total, dev_err)) {
+            if (sorted_row_idx) sorted_row_idx[dest] = (int32_t)j;
+            if (sorted_rem) sorted_rem[dest] = rem;
+          }
+          if (pad_row) {
+            const int32_t pr = seg_mprefix[key] * kBM + (dest - offsets[key]);
+            pad_row[j] = in_bounds(pr >= 0 && pr < pad_limit, dev_err) ? pr : -1;
+          }
+        } else if (pad_row) {
+          pad_row[j] = -1;
         }
-        if (pad_row) {
-          const int32_t pr = seg_mprefix[key] * kBM + (dest - offsets[key]);
-          pad_row[j] = in_bounds(pr >= 0 && pr < pad_limit, dev_err) ? pr : -1;
-        }
-      } else if (pad_row) {
-        pad_row[j] = -1;
       }
     }
   }
