@@ -828,6 +828,7 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
                      "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / hbm_peak,
                      "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
     del x, ws, S
+    out["ep8"] = ep_local_measurements(mm, torch, synth, dist, hbm_peak, W_prefill, cfg_prefill, steps)
     if cfg_prefill.weight_fmt == mm.DT_FP4_E2M1:
         return out
     # A8W4-FP: the same prefill and decode shapes with MXFP4 E2M1 weights (packed,
@@ -861,6 +862,59 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
     out["a8w4"] = a8w4
     del x, ws, W4, S4
     return out
+
+
+def ep_local_measurements(mm, torch, synth, dist, hbm_peak, W, cfg, steps, world=8):
+    """Expert parallelism over `world` ranks (MegaMoE stages 1-4 with
+    epWorldSize > 1), the kernels one rank runs, on this GPU: the source
+    side's dispatch (rows sorted by destination rank, each token MX-quantised
+    once), the expert side of the busiest rank (its E/W experts on the rows
+    it receives when every source rank routes like this batch: the rows this
+    batch sends it, `world` times), and the source side's combine of the
+    returned rows.  The all-to-all exchanges are not measured: one GPU."""
+    e_loc = cfg.e // world
+    x, ids, gate, _, _ = gpu_inputs(cfg, mm, torch, seed_offset=50 + dist.rank, weights=W)
+    sx, ss, se, counts, exp_idx = mm.mm_moe_ep_dispatch(x, ids, cfg.e, world, cfg.dispatch_fmt)
+    ms_d, st_d, _ = time_steps(torch, lambda: mm.mm_moe_ep_dispatch(x, ids, cfg.e, world, cfg.dispatch_fmt),
+                               steps, 3, dist)
+    cnt = counts.cpu().tolist()
+    r = int(np.argmax(cnt))
+    off = int(sum(cnt[:r]))
+    m = world * cnt[r]
+    rx = sx[off:off + cnt[r]].repeat(world, 1)
+    rs = ss[off:off + cnt[r]].repeat(world, 1)
+    re = se[off:off + cnt[r]].repeat(world).view(m, 1).contiguous()
+    ones = torch.ones((m, 1), dtype=torch.float32, device="cuda")
+    pe1, pe2 = W["p1"].numel() // cfg.e, W["p2"].numel() // cfg.e
+    w1, w2 = W["w1"][r * e_loc:(r + 1) * e_loc], W["w2"][r * e_loc:(r + 1) * e_loc]
+    p1 = W["p1"][r * e_loc * pe1:(r + 1) * e_loc * pe1]
+    p2 = W["p2"][r * e_loc * pe2:(r + 1) * e_loc * pe2]
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(m, cfg.h, 1, e_loc, cfg.inter, 0, mm.WSCALE_PREPARED),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty((m, cfg.h), dtype=torch.bfloat16, device="cuda")
+    expert = lambda: mm.mm_mega_moe(rx, re, ones, w1, w2, p1, p2, e_loc, weight_dtype=cfg.weight_fmt,
+                                    weight_scale_layout=mm.WSCALE_PREPARED, dispatch_quant_mode=0,
+                                    dispatch_quant_out_dtype=cfg.dispatch_fmt, x_scales=rs, workspace=ws, out=o)
+    ms_e, st_e, _ = time_steps(torch, expert, steps, 3, dist)
+    del rx, rs, re, ones, ws, o
+    back = torch.randn((cfg.n * cfg.k, cfg.h), device="cuda").to(torch.bfloat16)
+    y = torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device="cuda")
+    ms_c, st_c, _ = time_steps(torch, lambda: mm.mm_moe_combine(back, exp_idx, gate, out=y), steps, 3, dist)
+    rows = cfg.n * cfg.k
+    d_ms = (st_d["route"][0] + st_d["dispatch"][0]) / steps
+    c_ms = st_c["combine"][0] / steps
+    d_bytes = cfg.n * cfg.h * 2 + rows * (4 + 4 + 4 + cfg.h + cfg.h // 32)
+    c_bytes = rows * cfg.h * 2 + rows * (4 + gate.element_size()) + cfg.n * cfg.h * 2
+    del x, ids, gate, sx, ss, se, back, y
+    return {"workload": f"{cfg.name}, ep_world_size {world}, {e_loc} experts per rank",
+            "exchange": "not measured (one GPU)",
+            "dispatch_ms": d_ms, "dispatch_gbs": d_bytes / (d_ms / 1e3) / 1e9,
+            "dispatch_frac": d_bytes / (d_ms / 1e3) / 1e9 / hbm_peak,
+            "expert_rank": r, "expert_rows": m, "expert_ms": ms_e / steps,
+            "expert_stage_ms": {k: v[0] / steps for k, v in st_e.items() if v[1]},
+            "combine_ms": c_ms, "combine_gbs": c_bytes / (c_ms / 1e3) / 1e9,
+            "combine_frac": c_bytes / (c_ms / 1e3) / 1e9 / hbm_peak,
+            "rank_rows_sent": cnt}
 
 
 def main():
