@@ -883,8 +883,7 @@ def ep_local_measurements(mm, torch, synth, dist, hbm_peak, W, cfg, steps, world
     m = world * cnt[r]
     rx = sx[off:off + cnt[r]].repeat(world, 1)
     rs = ss[off:off + cnt[r]].repeat(world, 1)
-    re = se[off:off + cnt[r]].repeat(world).view(m, 1).contiguous()
-    ones = torch.ones((m, 1), dtype=torch.float32, device="cuda")
+    re = se[off:off + cnt[r]].repeat(world).contiguous()
     pe1, pe2 = W["p1"].numel() // cfg.e, W["p2"].numel() // cfg.e
     w1, w2 = W["w1"][r * e_loc:(r + 1) * e_loc], W["w2"][r * e_loc:(r + 1) * e_loc]
     p1 = W["p1"][r * e_loc * pe1:(r + 1) * e_loc * pe1]
@@ -892,11 +891,11 @@ def ep_local_measurements(mm, torch, synth, dist, hbm_peak, W, cfg, steps, world
     ws = torch.empty(mm.mm_mega_moe_workspace_size(m, cfg.h, 1, e_loc, cfg.inter, 0, mm.WSCALE_PREPARED),
                      dtype=torch.uint8, device="cuda")
     o = torch.empty((m, cfg.h), dtype=torch.bfloat16, device="cuda")
-    expert = lambda: mm.mm_mega_moe(rx, re, ones, w1, w2, p1, p2, e_loc, weight_dtype=cfg.weight_fmt,
-                                    weight_scale_layout=mm.WSCALE_PREPARED, dispatch_quant_mode=0,
-                                    dispatch_quant_out_dtype=cfg.dispatch_fmt, x_scales=rs, workspace=ws, out=o)
+    expert = lambda: mm.mm_moe_expert_ffn(rx, rs, re, w1, w2, p1, p2, e_loc, x_dtype=cfg.dispatch_fmt,
+                                          weight_dtype=cfg.weight_fmt, weight_scale_layout=mm.WSCALE_PREPARED,
+                                          workspace=ws, out=o)
     ms_e, st_e, _ = time_steps(torch, expert, steps, 3, dist)
-    del rx, rs, re, ones, ws, o
+    del rx, rs, re, ws, o
     back = torch.randn((cfg.n * cfg.k, cfg.h), device="cuda").to(torch.bfloat16)
     y = torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device="cuda")
     ms_c, st_c, _ = time_steps(torch, lambda: mm.mm_moe_combine(back, exp_idx, gate, out=y), steps, 3, dist)

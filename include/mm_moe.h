@@ -361,6 +361,36 @@ mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const 
                          int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, void* y, void* stream);
 
 /* ------------------------------------------------------------------------
+ * mm_moe_expert_ffn -- the expert side of expert parallelism (MegaMoE README,
+ * A8W8-FP scenario stages 2-3 on the rows a rank receives): for every
+ * received row r, out[r] = GMM2(act(GMM1(DQ_MX(x[r]))), Q_MX between them)
+ * with the weights of its local expert expert_ids[r], the bf16 result
+ * written at row r itself (the order in which the rows go back to their
+ * source ranks).  The same arithmetic as mm_mega_moe with top-K 1, gating
+ * weight 1, pass-through quantisation and no shared experts, bit for bit,
+ * without its combine pass.
+ * x                 [rows, h] FP8 codes of x_dtype (23 | 24); x_scales
+ *                   [rows, h/32] E8M0 (required when rows > 0).
+ * expert_ids        [rows] int32 local expert ids in [0, local_experts); an
+ *                   id outside the range leaves its row of out unwritten and
+ *                   raises MM_DEVERR_EXPERT_RANGE.
+ * weights, scales, weight_dtype, weight_scale_layout, activation: as for
+ *                   mm_mega_moe, with E = local_experts.
+ * out               [rows, h] bf16.  expert_token_nums [local_experts] int32
+ *                   rows per expert (may be NULL).
+ * Workspace from mm_moe_expert_ffn_workspace_size; errors as mm_mega_moe.
+ * ---------------------------------------------------------------------- */
+mm_status mm_moe_expert_ffn_workspace_size(int64_t rows, int64_t h, int64_t local_experts, int64_t intermediate,
+                                           int weight_scale_layout, size_t* bytes);
+mm_status mm_moe_expert_ffn(const uint8_t* x, const uint8_t* x_scales, int x_dtype, const int32_t* expert_ids,
+                            int64_t rows, int64_t h, const uint8_t* weight1, const uint8_t* weight2,
+                            const uint8_t* weight_scales1, const uint8_t* weight_scales2, int weight_dtype,
+                            int weight_scale_layout, int64_t local_experts, int64_t intermediate,
+                            const char* activation, const float* activation_params, int64_t n_activation_params,
+                            void* out, int32_t* expert_token_nums, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * mm_moe_init_routing_noalloc -- the same routing and permute as
  * mm_moe_init_routing (same arguments and outputs), for callers that cannot
  * give the library device scratch memory: for example a host program or

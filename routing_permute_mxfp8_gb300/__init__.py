@@ -18,7 +18,7 @@ __all__ = [
     "MMError", "lib_path", "load", "mm_version", "mm_moe_init_routing", "mm_moe_token_permute",
     "mm_mega_moe", "mm_mega_moe_workspace_size", "mm_prepare_weight_scales", "mm_mx_quantize",
     "DT_FP8_E5M2", "DT_FP8_E4M3FN", "QUANT_NONE", "QUANT_MXFP8_E5M2", "QUANT_MXFP8_E4M3FN",
-    "mm_moe_ep_dispatch", "mm_moe_combine",
+    "mm_moe_ep_dispatch", "mm_moe_combine", "mm_moe_expert_ffn",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,13 +86,16 @@ def load():
     L.mm_mx_quantize.argtypes = [p, i32, i64, i64, i32, p, p, i64, p]
     L.mm_selftest_wait_timeout.argtypes = [i64, p, p]
     L.mm_moe_ep_dispatch_workspace_size.argtypes = [i64, i64, i64, psz]
+    L.mm_moe_expert_ffn_workspace_size.argtypes = [i64, i64, i64, i64, i32, psz]
+    L.mm_moe_expert_ffn.argtypes = [p, p, i32, p, i64, i64, p, p, p, p, i32, i32, i64, i64, ctypes.c_char_p, p, i64,
+                                    p, p, p, sz, p, p]
     L.mm_moe_ep_dispatch.argtypes = [p, i32, p, i64, i64, i64, i64, i64, i64, p, p, p, p, p, p, sz, p, p]
     L.mm_moe_combine.argtypes = [p, p, p, i32, i64, i64, i64, p, p]
     for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
                  "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
                  "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize",
                  "mm_selftest_wait_timeout", "mm_moe_ep_dispatch_workspace_size", "mm_moe_ep_dispatch",
-                 "mm_moe_combine"):
+                 "mm_moe_combine", "mm_moe_expert_ffn_workspace_size", "mm_moe_expert_ffn"):
         getattr(L, name).restype = i32
     _libs[path] = L
     return L
@@ -406,6 +409,46 @@ def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None):
     _check(load().mm_moe_combine(_ptr(expert_rows), _ptr(row_idx), _ptr(topk_weights), _dt(topk_weights), n, h, k,
                                  _ptr(y), _stream(expert_rows.device)), "mm_moe_combine")
     return y
+
+
+def mm_moe_expert_ffn(x, x_scales, expert_ids, weight1, weight2, weight_scales1, weight_scales2, local_experts: int, *,
+                      x_dtype: int = DT_FP8_E4M3FN, weight_dtype: int = DT_FP8_E4M3FN,
+                      weight_scale_layout: int = WSCALE_ROWS, activation: str = "swiglu", activation_params=(),
+                      out=None, workspace=None, dev_err=None):
+    """The expert side of expert parallelism (MegaMoE stages 2-3 on the rows a
+    rank receives): out[r] = the FFN of local expert expert_ids[r] on row r.
+    x [M, H] FP8 codes (uint8 or torch float8, type x_dtype), x_scales [M, H/32]
+    uint8 E8M0, expert_ids [M] int32; weights as for mm_mega_moe with E =
+    local_experts.  Returns (out [M, H] bf16, expert_token_nums [local_experts]
+    int32)."""
+    _need_dtype(x, _BYTE_DTYPES, "x")
+    _need_dtype(x_scales, (torch.uint8,), "x_scales")
+    _need_dtype(expert_ids, (torch.int32,), "expert_ids")
+    for name, t in (("weight1", weight1), ("weight2", weight2)):
+        _need_dtype(t, _BYTE_DTYPES, name)
+    for name, t in (("weight_scales1", weight_scales1), ("weight_scales2", weight_scales2)):
+        _need_dtype(t, (torch.uint8,), name)
+    _need_cuda(x, x_scales, expert_ids, weight1, weight2, weight_scales1, weight_scales2)
+    m, h = x.shape
+    if expert_ids.numel() != m or x_scales.shape[0] != m:
+        raise MMError("expert_ids and x_scales must hold one entry / row per row of x")
+    L = load()
+    dev = x.device
+    inter = weight1.shape[1] // 2
+    y = out if out is not None else torch.empty((m, h), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(local_experts, dtype=torch.int32, device=dev)
+    need = ctypes.c_size_t(0)
+    _check(L.mm_moe_expert_ffn_workspace_size(m, h, local_experts, inter, weight_scale_layout, ctypes.byref(need)),
+           "mm_moe_expert_ffn_workspace_size")
+    ws = _workspace(need.value, dev, workspace)
+    params = list(activation_params)
+    parr = (ctypes.c_float * max(len(params), 1))(*params) if params else None
+    _check(L.mm_moe_expert_ffn(_ptr(x), _ptr(x_scales), _fp8_code(x, x_dtype), _ptr(expert_ids), m, h, _ptr(weight1),
+                               _ptr(weight2), _ptr(weight_scales1), _ptr(weight_scales2),
+                               _fp8_code(weight1, weight_dtype), weight_scale_layout, local_experts, inter,
+                               activation.encode(), parr, len(params), _ptr(y), _ptr(counts), _ptr(ws), ws.numel(),
+                               _dev_err(dev_err), _stream(dev)), "mm_moe_expert_ffn")
+    return y, counts
 
 
 # --------------------------------------------------------------------------- diagnostics

@@ -64,7 +64,7 @@ struct MegaDims {
 };
 
 struct MegaWs {
-  int32_t *hist, *offsets, *seg_rows, *seg_mprefix, *exp_idx, *pad_row;
+  int32_t *hist, *offsets, *seg_rows, *seg_mprefix, *exp_idx, *pad_row, *pad_inv;
   uint8_t *xq, *xsf, *aq, *asf;
   __nv_bfloat16* o;
   uint8_t *wsf1, *wsf2, *swsf1, *swsf2;
@@ -94,6 +94,7 @@ MegaWs carve_mega(Carver& c, const MegaDims& d, const RoutePlan& p, int wscale_l
   w.seg_mprefix = c.take<int32_t>(nseg + 1);
   w.exp_idx = c.take<int32_t>(d.rows);
   w.pad_row = c.take<int32_t>(d.rows);
+  w.pad_inv = c.take<int32_t>(d.rows_cap);
   w.xq = c.take<uint8_t>(d.rows_cap * d.h);
   w.xsf = c.take<uint8_t>(d.rows_cap / kBM * (d.h / 128) * kSfChunk);
   w.aq = c.take<uint8_t>(d.rows_cap * d.aw_max);
@@ -467,8 +468,11 @@ mm_status mm_mega_moe_workspace_size(int64_t bs, int64_t h, int64_t k, int64_t m
   return MM_OK;
 }
 
-mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* topk_ids, const void* topk_weights,
-                      int topk_weights_dtype,
+// The MegaMoE step; rows_out: the expert side of expert parallelism
+// (top-K 1, no gating weights, no shared experts): GEMM2 writes each input
+// row's expert output to y at that row's position and there is no combine.
+static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_scales, const int32_t* topk_ids,
+                               const void* topk_weights, int topk_weights_dtype,
                       const uint8_t* weight1, const uint8_t* weight2, const uint8_t* weight_scales1,
                       const uint8_t* weight_scales2, int weight_dtype, int weight_scale_layout,
                       const uint8_t* shared_weight1, const uint8_t* shared_weight2,
@@ -492,12 +496,13 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   if (dispatch_quant_mode != 4 && dispatch_quant_mode != 0) return MM_ERR_UNSUPPORTED;
   if (!is_fp8(dispatch_quant_out_dtype) || !is_mx_weight(weight_dtype)) return MM_ERR_UNSUPPORTED;
   if (shared_expert_num > 0 && !is_mx_weight(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
-  if ((dispatch_quant_mode == 0) != (x_scales != nullptr)) return MM_ERR_INVALID_ARG;
+  if (bs > 0 && (dispatch_quant_mode == 0) != (x_scales != nullptr)) return MM_ERR_INVALID_ARG;
   ActSpec act;
   s = parse_activation(activation, activation_params, n_activation_params, &act);
   if (s != MM_OK) return s;
   const int64_t aw = act.kind == MM_ACT_GELU ? 2 * intermediate : intermediate;
-  if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
+  if (!rows_out && topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16)
+    return MM_ERR_INVALID_ARG;
   const int64_t rows = bs * k;
   if (max_recv_token_num != 0 && max_recv_token_num < rows) return MM_ERR_INVALID_ARG;
   if (bs == 0)  // no tokens: Y is empty and every expert received 0 rows
@@ -505,7 +510,8 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
                                                            (size_t)moe_expert_num * sizeof(int32_t),
                                                            static_cast<cudaStream_t>(stream)))
                              : MM_OK;
-  if (!x || !topk_ids || !topk_weights || !weight1 || !weight2 || !weight_scales1 || !weight_scales2 || !y)
+  if (!x || !topk_ids || (!topk_weights && !rows_out) || !weight1 || !weight2 || !weight_scales1 ||
+      !weight_scales2 || !y)
     return MM_ERR_INVALID_ARG;
   if (shared_expert_num > 0 &&
       (!shared_weight1 || !shared_weight2 || !shared_weight_scales1 || !shared_weight_scales2))
@@ -582,6 +588,7 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   pa.scales = w.xsf;
   pa.scale_cols = 0;
   pa.dev_err = dev_err;
+  pa.dest_inv = rows_out ? w.pad_inv : nullptr;
   StageScope sd(MM_STAGE_DISPATCH, st);
   e = launch_permute(pa, st);
   sd.finish(1);
@@ -633,31 +640,36 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
   g2.N = d.h;
   g2.act_q = nullptr;
   g2.act_sf = nullptr;
-  g2.out = w.o;
+  g2.out = rows_out ? static_cast<__nv_bfloat16*>(y) : w.o;
+  g2.out_row = rows_out ? w.pad_inv : nullptr;
+  g2.out_rows = d.rows;
   StageScope s2(MM_STAGE_GEMM2, st);
   e = launch_gemm(g2, st);
   s2.finish(1);
   if (e != cudaSuccess) return MM_ERR_CUDA;
 
-  // 5. combine
-  CombineArgs ca;
-  ca.o = w.o;
-  ca.pad_row = w.pad_row;
-  ca.gate = topk_weights;
-  ca.gate_bf16 = topk_weights_dtype == MM_DT_BFLOAT16;
-  ca.n_shared = (int)d.s;
-  ca.seg_mprefix = w.seg_mprefix;
-  ca.n_routed = (int)d.e;
-  ca.n = d.bs;
-  ca.h = d.h;
-  ca.k = (int)d.k;
-  ca.y = static_cast<__nv_bfloat16*>(y);
-  ca.rows_cap = d.rows_cap;
-  ca.dev_err = dev_err;
-  StageScope sc(MM_STAGE_COMBINE, st);
-  e = launch_combine(ca, st);
-  sc.finish(1);
-  if (e != cudaSuccess) return MM_ERR_CUDA;
+  // 5. combine (the expert side of expert parallelism has none: its rows
+  //    go back to their source ranks)
+  if (!rows_out) {
+    CombineArgs ca;
+    ca.o = w.o;
+    ca.pad_row = w.pad_row;
+    ca.gate = topk_weights;
+    ca.gate_bf16 = topk_weights_dtype == MM_DT_BFLOAT16;
+    ca.n_shared = (int)d.s;
+    ca.seg_mprefix = w.seg_mprefix;
+    ca.n_routed = (int)d.e;
+    ca.n = d.bs;
+    ca.h = d.h;
+    ca.k = (int)d.k;
+    ca.y = static_cast<__nv_bfloat16*>(y);
+    ca.rows_cap = d.rows_cap;
+    ca.dev_err = dev_err;
+    StageScope sc(MM_STAGE_COMBINE, st);
+    e = launch_combine(ca, st);
+    sc.finish(1);
+    if (e != cudaSuccess) return MM_ERR_CUDA;
+  }
 
   // optional diagnostic copies of X_hat and A_hat in expert-sorted order
   if (dispatch_q) {
@@ -695,6 +707,51 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
     if (e != cudaSuccess) return MM_ERR_CUDA;
   }
   return MM_OK;
+}
+
+mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* topk_ids, const void* topk_weights,
+                      int topk_weights_dtype, const uint8_t* weight1, const uint8_t* weight2,
+                      const uint8_t* weight_scales1, const uint8_t* weight_scales2, int weight_dtype,
+                      int weight_scale_layout, const uint8_t* shared_weight1, const uint8_t* shared_weight2,
+                      const uint8_t* shared_weight_scales1, const uint8_t* shared_weight_scales2,
+                      int shared_weight_dtype, int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
+                      int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
+                      int64_t max_recv_token_num, int64_t dispatch_quant_mode, int64_t dispatch_quant_out_dtype,
+                      int64_t combine_quant_mode, const char* activation, const float* activation_params,
+                      int64_t n_activation_params, void* y, int32_t* expert_token_nums,
+                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, uint8_t* dispatch_q,
+                      uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                      void* stream) {
+  return mega_moe_impl(false, x, x_scales, topk_ids, topk_weights, topk_weights_dtype, weight1, weight2,
+                       weight_scales1, weight_scales2, weight_dtype, weight_scale_layout, shared_weight1,
+                       shared_weight2, shared_weight_scales1, shared_weight_scales2, shared_weight_dtype,
+                       shared_expert_num, bs, h, k, moe_expert_num, ep_world_size, intermediate, max_recv_token_num,
+                       dispatch_quant_mode, dispatch_quant_out_dtype, combine_quant_mode, activation,
+                       activation_params, n_activation_params, y, expert_token_nums, expanded_row_idx, act_q,
+                       act_scale, dispatch_q, dispatch_scale, workspace, workspace_bytes, dev_err, stream);
+}
+
+// ------------------------------------------------------------------------
+// The expert side of expert parallelism (MegaMoE README, A8W8-FP stages 2-3
+// on the rows a rank receives): GEMM1 + activation + GEMM2 of each row's
+// local expert, the result written at the row's own position.
+mm_status mm_moe_expert_ffn_workspace_size(int64_t rows, int64_t h, int64_t local_experts, int64_t intermediate,
+                                           int weight_scale_layout, size_t* bytes) {
+  return mm_mega_moe_workspace_size(rows, h, 1, local_experts, intermediate, 0, weight_scale_layout, bytes);
+}
+
+mm_status mm_moe_expert_ffn(const uint8_t* x, const uint8_t* x_scales, int x_dtype, const int32_t* expert_ids,
+                            int64_t rows, int64_t h, const uint8_t* weight1, const uint8_t* weight2,
+                            const uint8_t* weight_scales1, const uint8_t* weight_scales2, int weight_dtype,
+                            int weight_scale_layout, int64_t local_experts, int64_t intermediate,
+                            const char* activation, const float* activation_params, int64_t n_activation_params,
+                            void* out, int32_t* expert_token_nums, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_err, void* stream) {
+  return mega_moe_impl(true, x, x_scales, expert_ids, nullptr, 0,
+                       weight1, weight2, weight_scales1, weight_scales2, weight_dtype, weight_scale_layout, nullptr,
+                       nullptr, nullptr, nullptr, 0, 0, rows, h, 1, local_experts, 1, intermediate, 0, 0, x_dtype, 0,
+                       activation, activation_params, n_activation_params, out, expert_token_nums, nullptr, nullptr,
+                       nullptr, nullptr, nullptr, workspace, workspace_bytes, dev_err, stream);
 }
 
 // ------------------------------------------------------------------------

@@ -106,6 +106,10 @@ struct GemmArgs {
   float act_c, act_alpha, act_beta, act_rbeta, act_beta_lin, act_rbeta_lin, act_gelu_k;
   int aw;
   int mtiles_cap;  // 128-row tiles of the A / output buffers (checked build)
+  // mode 2, optional: padded row r goes to output row out_row[r] (rows of the
+  // output: out_rows), stored from registers
+  const int32_t* out_row;
+  int64_t out_rows;
 };
 
 struct TileInfo {
@@ -532,6 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&acc_empty[buf]);
         // TMA store when all 32 rows of this lane quarter are real rows
         const bool staged = g.o_stage && g.seg_rows[ti.seg] - ti.mt * kBM >= (q + 1) * 32;
+        int64_t orow = grow;
+        if (g.out_row && valid) {
+          const int64_t m = g.out_row[grow];
+          orow = in_bounds(m >= 0 && m < g.out_rows, g.dev_err) ? m : -1;
+        }
         uint8_t* stg = smO + (warp - 2) * kOStageBytes;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -551,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_2d(&tmO, stg, (int)col, (int)((grow - r) + q * 32));
               bulk_commit();
             }
-          } else if (4 * half + i < kChunks && valid && col < g.N) {
-            uint4* dst = reinterpret_cast<uint4*>(g.out + grow * g.N + col);
+          } else if (4 * half + i < kChunks && valid && col < g.N && orow >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(g.out + orow * g.N + col);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               dst[u] = make_uint4(pack_bf16x2(v[i][8 * u], v[i][8 * u + 1]), pack_bf16x2(v[i][8 * u + 2], v[i][8 * u + 3]),
@@ -664,7 +673,7 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
                       8 * (2 * kStages + 2 * kAcc + 1) + 16 + 12 * (size_t)(g.nseg + 1);
   constexpr size_t kMaxSmem = 232448;
   // output staging buffers only where the segment table leaves room for them
-  g.o_stage = base + kEpiWarps * kOStageBytes <= kMaxSmem ? 1 : 0;
+  g.o_stage = (base + kEpiWarps * kOStageBytes <= kMaxSmem && !g.out_row) ? 1 : 0;
   const size_t smem = base + (g.o_stage ? kEpiWarps * kOStageBytes : 0);
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -751,6 +760,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.out = L.out;
   g.dev_err = L.dev_err;
   g.mtiles_cap = (int)(L.rows_cap / kBM);
+  g.out_row = L.mode == 2 ? L.out_row : nullptr;
+  g.out_rows = L.out_rows;
   // upper bound of the tile count decides how many persistent CTAs to start
   const int64_t max_mtiles = L.rows_cap / kBM;
   int64_t grid = max_mtiles * g.n_tiles;

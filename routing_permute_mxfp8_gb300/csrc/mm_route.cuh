@@ -85,6 +85,7 @@ struct PermuteArgs {
   uint8_t* scales;          // E8M0 output
   int64_t scale_cols;       // row layout: scale row stride; 0 = GEMM tile layout
   int32_t* dev_err;
+  int32_t* dest_inv;        // optional [dest_limit]: dest_inv[dest[i*k + t]] = i*k + t (routed destinations)
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st);
 
@@ -118,7 +119,9 @@ struct GemmLaunch {
                                                    // situglu beta / linear beta (0: off)
   uint8_t* act_q;             // mode 1 outputs
   uint8_t* act_sf;
-  __nv_bfloat16* out;         // mode 2 output [rows_cap, N]
+  __nv_bfloat16* out;         // mode 2 output [rows_cap, N], or [rows of out_row, N]
+  const int32_t* out_row;     // mode 2, optional: padded row r is written to output row out_row[r]
+  int64_t out_rows;           // rows of out when out_row is set (checked build)
   int32_t* dev_err;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);

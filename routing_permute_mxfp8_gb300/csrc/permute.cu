@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5
   int32_t d0, d1;
   int ndest;
   load_dests(a, row, lane, d0, d1, ndest);
+  if (a.dest_inv && part == 0 && lane < a.k && d0 >= 0) a.dest_inv[d0] = (int32_t)((int64_t)row * a.k + lane);
   constexpr int esz = kSrc == MM_DT_FLOAT32 ? 4 : 2;
   const char* src_row = static_cast<const char*>(a.src) + row * a.h * esz;
   uint8_t* out = static_cast<uint8_t*>(a.out);
@@ -261,6 +262,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
   int32_t d0, d1;
   int ndest;
   load_dests(a, row, lane, d0, d1, ndest);
+  if (a.dest_inv && lane < a.k && d0 >= 0) a.dest_inv[d0] = (int32_t)(row * a.k + lane);
   const uint8_t* src_row = static_cast<const uint8_t*>(a.src) + row * a.h;
   const uint8_t* src_sf = a.src_scales + row * (a.h / 32);
   uint8_t* out = static_cast<uint8_t*>(a.out);

@@ -7,8 +7,9 @@ the experts [r*E/W, (r+1)*E/W):
            then an all-to-all of the per-rank counts and of the rows, their
            E8M0 scales and their local expert ids);
   stage 2-3 each rank runs its experts' GEMM1 + activation + GEMM2 on the rows
-           it received (mm_mega_moe with the received FP8 rows passed through,
-           top-K 1 and weight 1, so its output rows are the expert rows O);
+           it received (mm_moe_expert_ffn: the received FP8 rows and scales
+           passed through, each row's result written at its own position, the
+           order in which the rows go back);
   stage 4  the O rows go back to their source ranks in the order they came
            (the reverse all-to-all), where mm_moe_combine forms
            Y[i] = sum_k W[i,k] O[pi(i,k)] in fp32 and rounds once to bf16.
@@ -74,12 +75,11 @@ def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     # stages 2-3 on this rank's experts: one choice per received row, weight 1,
     # the received FP8 rows and scales passed through
     if m > 0:
-        ones = torch.ones((m, 1), dtype=torch.float32, device=x.device)
-        o_rows = _mm.mm_mega_moe(recv_x, recv_e.reshape(m, 1).contiguous(), ones, weight1, weight2, weight_scales1,
-                                 weight_scales2, e_local, weight_dtype=weight_dtype,
-                                 weight_scale_layout=weight_scale_layout, dispatch_quant_mode=0,
-                                 dispatch_quant_out_dtype=dispatch_quant_out_dtype, x_scales=recv_s,
-                                 activation=activation, activation_params=activation_params, dev_err=dev_err)[0]
+        o_rows = _mm.mm_moe_expert_ffn(recv_x, recv_s, recv_e.reshape(m).contiguous(), weight1, weight2,
+                                       weight_scales1, weight_scales2, e_local, x_dtype=dispatch_quant_out_dtype,
+                                       weight_dtype=weight_dtype, weight_scale_layout=weight_scale_layout,
+                                       activation=activation, activation_params=activation_params,
+                                       dev_err=dev_err)[0]
     else:
         o_rows = torch.empty((0, h), dtype=torch.bfloat16, device=x.device)
     # stage 4: rows back to their source ranks in send order, then the weighted sum

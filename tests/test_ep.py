@@ -49,7 +49,7 @@ def _problem():
 
 
 def _oracle_fakes(mm, cfg):
-    """CPU stand-ins for mm_moe_ep_dispatch / mm_mega_moe / mm_moe_combine,
+    """CPU stand-ins for mm_moe_ep_dispatch / mm_mega_moe / mm_moe_expert_ffn / mm_moe_combine,
     computed by the oracle (test infrastructure only)."""
     import oracle
 
@@ -72,6 +72,11 @@ def _oracle_fakes(mm, cfg):
                                        x_prequant=(xq.numpy(), x_scales.numpy()))
         return (torch.from_numpy(yb.view(np.int16)).view(torch.bfloat16),)
 
+    def expert_ffn(xq, xs, eids, w1, w2, s1, s2, e, *, x_dtype=None, **kw):
+        m = xq.shape[0]
+        return mega(xq, eids.view(m, 1), torch.ones((m, 1)), w1, w2, s1, s2, e, x_scales=xs,
+                    dispatch_quant_out_dtype=x_dtype, dispatch_quant_mode=0)[0], None
+
     def combine(rows, idx, gate, out=None):
         r = rows.float().numpy()
         g = gate.float().numpy()
@@ -85,6 +90,7 @@ def _oracle_fakes(mm, cfg):
 
     mm.mm_moe_ep_dispatch = dispatch
     mm.mm_mega_moe = mega
+    mm.mm_moe_expert_ffn = expert_ffn
     mm.mm_moe_combine = combine
 
 

@@ -667,6 +667,42 @@ def test_ep_dispatch_bit_exact(w, fmt):
     assert np.array_equal(host(ss), sc[:, :cfg.h // 32])
 
 
+@pytest.mark.parametrize("case", [
+    dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"),
+    dict(n=300, h=896, inter=384, e=5, k=1, weight_fmt=296, dispatch_fmt=23),
+    dict(n=200, h=512, inter=256, e=16, k=1, activation="gelu", act_params=(float(np.finfo(np.float32).max),)),
+])
+def test_expert_ffn_equals_mega_moe_top1(case):
+    """mm_moe_expert_ffn (the expert side of expert parallelism: GEMM2 writes
+    each received row's result at the row's own position, no combine pass)
+    gives mm_mega_moe's bits for the same rows at top-K 1 with weight 1 and
+    pass-through quantisation, and the oracle's Y within tolerance."""
+    cfg = synth.CONFIGS["tiny"].scaled(**case)
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    fmt = cfg.dispatch_fmt
+    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, fmt)   # the received rows: FP8 codes + E8M0 scales
+    xq, xs = t(xq), t(xs)
+    ids1 = t(ids.reshape(cfg.n))
+    err = zeros_err()
+    out, cnt = mm.mm_moe_expert_ffn(xq, xs, ids1, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt), t(s1),
+                                    t(s2), cfg.e, x_dtype=fmt, weight_dtype=cfg.weight_fmt,
+                                    activation=cfg.activation, activation_params=cfg.act_params, dev_err=err)
+    ones = torch.ones((cfg.n, 1), dtype=torch.float32, device=DEV)
+    y, cnt2 = mm.mm_mega_moe(xq, ids1.view(cfg.n, 1), ones, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt),
+                             t(s1), t(s2), cfg.e, weight_dtype=cfg.weight_fmt, dispatch_quant_mode=0,
+                             dispatch_quant_out_dtype=fmt, x_scales=xs, activation=cfg.activation,
+                             activation_params=cfg.act_params)
+    assert host(err)[0] == 0
+    assert np.array_equal(host(out), host(y))
+    assert np.array_equal(host(cnt), host(cnt2))
+    assert np.array_equal(host(cnt), np.bincount(ids.reshape(-1), minlength=cfg.e))
+    y_ref, _ = oracle.mega_moe_tokens(x, ids, np.ones((cfg.n, 1), np.float32), w1, s1, w2, s2, fmt, cfg.weight_fmt,
+                                      activation=cfg.activation, act_params=cfg.act_params)
+    check_y(synth.bf16_bits_to_f32(host(out).view(np.uint16)), y_ref)
+
+
 @pytest.mark.parametrize("gate_bf16", [False, True])
 def test_moe_combine_rows(gate_bf16):
     """mm_moe_combine: fp32 sum in k order of weighted rows chosen by an index
