@@ -319,9 +319,9 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  * weighted and summed", with epWorldSize > 1; parameter table
  * epWorldSize / moeExpertNum).  Rank r holds experts [r*E/W, (r+1)*E/W).
  * The exchange between ranks is the caller's collective (an all-to-all with
- * the counts below as split sizes); each rank runs mm_mega_moe on the rows
- * it receives (pass-through quantisation, top-K 1, weight 1, its local
- * experts) and sends the resulting rows back in the order received.
+ * the counts below as split sizes); each rank runs mm_moe_expert_ffn on the
+ * rows it receives (its local experts) and sends the resulting rows back in
+ * the order received.
  *
  * mm_moe_ep_dispatch -- on the source rank: the flattened ids j = i*K + k
  *   are sorted by destination rank id / (E/W), stably (rows of one rank in
