@@ -571,6 +571,36 @@ def test_mega_moe_dsv3_decode_gelu_full_size():
     run_mega(cfg, tokens=np.array([0, 31, 64, 127]), layout=1, sparse=True)
 
 
+def test_mega_moe_back_to_back_calls_share_a_workspace():
+    """Calls enqueued back to back on one stream, one workspace, no host
+    synchronisation between them: each kernel starts early (programmatic
+    dependent launch) but reads an earlier kernel's output only after that
+    kernel has finished, so every call gives the bits it gives alone."""
+    cfgs = [synth.CONFIGS["tiny"].scaled(**MEGA_CASES[c]) for c in ("zipf_shared_e5m2_h512", "wide", "tiny_shared")]
+    h, inter = 1024, 512
+    cfgs = [c.scaled(h=h, inter=inter, dispatch_fmt=24, weight_fmt=24) for c in cfgs]
+    inputs = []
+    for c in cfgs:
+        x, ids, gate = bf16(synth.tokens_bf16(c)), t(synth.topk_ids(c)), t(synth.topk_weights(c))
+        w = [t(a) for a in _weights(c)]
+        sh = [t(a) for a in _weights(c, shared=True)] if c.shared else None
+        kw = dict(shared_weight1=sh[0], shared_weight_scales1=sh[1], shared_weight2=sh[2],
+                  shared_weight_scales2=sh[3]) if sh else {}
+        inputs.append((c, x, ids, gate, w, kw))
+    need = max(mm.mm_mega_moe_workspace_size(c.n, c.h, c.k, c.e, c.inter, c.shared, 0) for c in cfgs)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    alone = []
+    for c, x, ids, gate, w, kw in inputs:
+        alone.append(host(mm.mm_mega_moe(x, ids, gate, w[0], w[2], w[1], w[3], c.e, workspace=ws, **kw)[0]).copy())
+    ys = [torch.empty((c.n, c.h), dtype=torch.bfloat16, device=DEV) for c in cfgs]
+    for rep in range(3):
+        for (c, x, ids, gate, w, kw), y in zip(inputs, ys):
+            mm.mm_mega_moe(x, ids, gate, w[0], w[2], w[1], w[3], c.e, workspace=ws, out=y, **kw)
+    torch.cuda.synchronize()
+    for y, a in zip(ys, alone):
+        assert np.array_equal(host(y), a)
+
+
 @pytest.mark.parametrize("route_path", ["cluster", "kernels"], indirect=True)
 def test_mega_moe_in_cuda_graph(route_path):
     """The whole call captured in a CUDA graph (caller's workspace and
