@@ -733,6 +733,39 @@ def test_expert_ffn_equals_mega_moe_top1(case):
     check_y(synth.bf16_bits_to_f32(host(out).view(np.uint16)), y_ref)
 
 
+@pytest.mark.slow
+def test_expert_ffn_full_size_equals_mega_moe_top1():
+    """The expert side of expert parallelism at the size one rank of an
+    8-way DeepSeek-V3 prefill receives (16384 rows, hidden 7168,
+    intermediate 2048, 32 local experts with Zipf-skewed loads, E5M2 rows,
+    prepared weight scales): bit-identical to mm_mega_moe at top-K 1.
+    Weights are drawn on the GPU (any values serve for bit-identity; the
+    oracle comparison runs at the small sizes above)."""
+    m, h, inter, e = 16384, 7168, 2048, 32
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(5)
+    w = []
+    for n_out, k_red in ((2 * inter, h), (h, inter)):
+        q, sc = mm.mm_mx_quantize(torch.randn((e * n_out, k_red), generator=gen, device=DEV) * 0.02, 24,
+                                  scale_cols=k_red // 32)
+        w += [q.view(e, n_out, k_red), sc.view(e, n_out, k_red // 32)]
+    p1 = mm.mm_prepare_weight_scales(w[1], h, 1)
+    p2 = mm.mm_prepare_weight_scales(w[3], inter, 2)
+    xq, xs = mm.mm_mx_quantize(torch.randn((m, h), generator=gen, device=DEV), 23, scale_cols=h // 32)
+    rng = np.random.default_rng(11)
+    pz = 1.0 / np.arange(1, e + 1)
+    ids = t(rng.permutation(e)[rng.choice(e, m, p=pz / pz.sum())].astype(np.int32))
+    err = zeros_err()
+    out, cnt = mm.mm_moe_expert_ffn(xq, xs, ids, w[0], w[2], p1, p2, e, x_dtype=23,
+                                    weight_scale_layout=mm.WSCALE_PREPARED, dev_err=err)
+    ones = torch.ones((m, 1), dtype=torch.float32, device=DEV)
+    y, cnt2 = mm.mm_mega_moe(xq, ids.view(m, 1), ones, w[0], w[2], p1, p2, e, weight_scale_layout=mm.WSCALE_PREPARED,
+                             dispatch_quant_mode=0, dispatch_quant_out_dtype=23, x_scales=xs)
+    assert host(err)[0] == 0
+    assert np.array_equal(host(cnt), host(cnt2))
+    assert np.array_equal(host(out), host(y))
+
+
 @pytest.mark.parametrize("gate_bf16", [False, True])
 def test_moe_combine_rows(gate_bf16):
     """mm_moe_combine: fp32 sum in k order of weighted rows chosen by an index
