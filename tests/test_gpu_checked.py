@@ -60,3 +60,4 @@ def test_permute_expert_parallel_and_combine_checked():
     P.test_ep_dispatch_bit_exact(4, 24)
     P.test_moe_combine_rows(True)
     P.test_out_of_range_ids_are_left_out_and_flagged()
+    P.test_expert_ffn_equals_mega_moe_top1(dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"))
