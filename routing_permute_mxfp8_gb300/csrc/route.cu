@@ -421,7 +421,7 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
 
 // ---------------------------------------------------------------------------
 // Problems of up to kClusterMaxRows ids: the whole routing in one
-// thread-block cluster of up to 16 CTAs (one per 4096 ids), which exchange
+// thread-block cluster of up to 16 CTAs (one per 2048 ids), which exchange
 // their per-expert counts through distributed shared memory, with two
 // hardware cluster barriers instead of three grid-wide barriers on global
 // memory.
@@ -440,7 +440,7 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
 // The cluster's CTAs are co-scheduled by the hardware, so the barriers have
 // the standing of __syncthreads: every thread reaches both.
 constexpr int kClusterMaxCtas = 16;
-constexpr int64_t kClusterRowsPerCta = 4096;
+constexpr int64_t kClusterRowsPerCta = 2048;
 constexpr int64_t kClusterMinWarpIds = 128;
 constexpr int64_t kClusterMaxRows = 131072;
 constexpr int kClusterMaxExperts = 4096;
