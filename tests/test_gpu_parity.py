@@ -601,6 +601,42 @@ def test_mega_moe_back_to_back_calls_share_a_workspace():
         assert np.array_equal(host(y), a)
 
 
+@pytest.mark.slow
+def test_mega_moe_full_size_repeatable_back_to_back():
+    """The DeepSeek-V3-shaped prefill step (Zipf routing, E5M2 dispatch) run
+    24 times back to back on one stream and one workspace, into three
+    rotating outputs, without host synchronisation: every run gives the same
+    bits (deterministic kernels, no race between a kernel's early launch and
+    its predecessor's writes)."""
+    cfg = synth.CONFIGS["dsv3_prefill"]
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(3)
+    w = []
+    for n_out, k_red in ((2 * cfg.inter, cfg.h), (cfg.h, cfg.inter)):
+        q, sc = mm.mm_mx_quantize(torch.randn((cfg.e * n_out, k_red), generator=gen, device=DEV) * 0.02, 24,
+                                  scale_cols=k_red // 32)
+        w += [q.view(cfg.e, n_out, k_red), mm.mm_prepare_weight_scales(sc.view(cfg.e, n_out, k_red // 32), k_red,
+                                                                       1 if n_out == 2 * cfg.inter else 2)]
+    x, ids = bf16(synth.tokens_bf16(cfg)), t(synth.topk_ids(cfg))
+    gate = bf16(synth.topk_weights(cfg))
+    ws = torch.empty(mm.mm_mega_moe_workspace_size(cfg.n, cfg.h, cfg.k, cfg.e, cfg.inter, 0, mm.WSCALE_PREPARED),
+                     dtype=torch.uint8, device=DEV)
+    ys = [torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    err = zeros_err()
+    ref = None
+    for rnd in range(8):
+        for y in ys:
+            mm.mm_mega_moe(x, ids, gate, w[0], w[2], w[1], w[3], cfg.e, weight_scale_layout=mm.WSCALE_PREPARED,
+                           dispatch_quant_out_dtype=23, workspace=ws, out=y, dev_err=err)
+        torch.cuda.synchronize()
+        for y in ys:
+            h = host(y)
+            if ref is None:
+                ref = h.copy()
+            assert np.array_equal(h, ref), rnd
+    assert host(err)[0] == 0
+
+
 @pytest.mark.parametrize("route_path", ["cluster", "kernels"], indirect=True)
 def test_mega_moe_in_cuda_graph(route_path):
     """The whole call captured in a CUDA graph (caller's workspace and
