@@ -140,7 +140,7 @@ def _check_against_oracle(cfg, x, ids, gate, w, y_bits):
 
 def test_ep_exchange_two_gloo_ranks_cpu():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
     mp.spawn(_cpu_rank, args=(port, out), nprocs=W, join=True)
     cfg, x, ids, gate, w = _problem()
     ys = []
@@ -182,7 +182,7 @@ def _gpu_rank(rank, port, out):
 @pytest.mark.gpu
 def test_ep_two_ranks_on_one_gpu_matches_single_process():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
     mp.spawn(_gpu_rank, args=(port, out), nprocs=W, join=True)
     cfg, x, ids, gate, w = _problem()
     ys = []

@@ -36,7 +36,7 @@ def _rank_main(rank, world, port, out):
 @pytest.mark.parametrize("world", [2])
 def test_two_gloo_ranks_time_and_throughput(world):
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork after CUDA is initialised
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     for r in range(world):
