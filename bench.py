@@ -445,7 +445,7 @@ def library_mxfp8_peak(torch, sustain_s=2.0):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-    except Exception as ex:  # no block-scaled path in this build
+    except Exception as ex:  # this PyTorch has no block-scaled _scaled_mm
         return {"error": str(ex)[:200]}
     best = 1e9
     for _ in range(20):
