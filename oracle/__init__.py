@@ -61,6 +61,7 @@ def _load():
     L.orc_mega_moe_tokens.argtypes = [p, p, p, i32, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                       i32, i32, i32, p, i64, p, p, p, p, p, p, i32, p]
     L.orc_mega_moe_tokens.restype = None
+    L.orc_act_code.argtypes, L.orc_act_code.restype = [i32], i32
     _lib = L
     return L
 
@@ -210,11 +211,17 @@ def expert_row(xq, xs, x_fmt, w1, s1, w2, s2, w_fmt, a_fmt, activation="swiglu",
     return aq, a_s, o
 
 
+def act_format(x_fmt: int) -> int:
+    """Format of A_hat for dispatch format x_fmt: x_fmt itself (A8W8-FP, A8W4-FP),
+    MXFP8 E4M3 under an FP4 E2M1 dispatch (A4W4-FP stage 2, so that GEMM2 is A8W4)."""
+    return int(_load().orc_act_code(int(x_fmt)))
+
+
 def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None,
                     shared=None, shared_w_fmt=None, want_act=False, activation="swiglu", act_params=(),
                     x_prequant=None):
-    """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP / A8W4-FP
-    stages 1-4).  x_prequant = (codes uint8[N, H], scales uint8[N, ceil(H/32)]):
+    """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP / A8W4-FP /
+    A4W4-FP stages 1-4; x_fmt 296 dispatches MXFP4 E2M1 codes, one per byte).  x_prequant = (codes uint8[N, H], scales uint8[N, ceil(H/32)]):
     pre-quantised pass-through (dispatchQuantMode = 0): X_hat and S_X are the given
     ones and x_bf16 is not read.
 
@@ -223,7 +230,7 @@ def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None
     s2 uint8[E, H, 2*ceil(I/64)]; shared = (sw1, ss1, sw2, ss2) with a leading
     shared-expert dimension, or None.
     Returns (y float64[T, H], y_bf16 uint16[T, H]) and, with want_act, the
-    activation codes uint8[T, K, I] and scales uint8[T, K, I/32].
+    activation codes uint8[T, K, I] (format act_format(x_fmt)) and scales uint8[T, K, I/32].
     """
     kind, p = activation_spec(activation, act_params)
     n, h = x_bf16.shape if x_prequant is None else x_prequant[0].shape

@@ -17,7 +17,10 @@
  *     "Activation function formulas"  -> orc_mx_block, orc_expert_row,
  *     orc_mega_moe_tokens;  "A8W4-FP quantization scenario" (FLOAT4_E2M1
  *     weights with E8M0 scales, FP8 E4M3 activations) -> the same functions
- *     with the E2M1 element format
+ *     with the E2M1 element format;  "A4W4-FP quantization scenario" (tokens
+ *     dispatched as MXFP4 E2M1, FLOAT4_E2M1 weights, the activation
+ *     re-quantised to MXFP8 E4M3 for the A8W4 second layer) -> the same
+ *     functions, with the activation format of orc_act_code
  *
  * Floating point is carried in double.  Readings of what the pages leave
  * open (shared-exponent rule, rounding, saturation, sign of zero, flatten
@@ -364,7 +367,7 @@ static int64_t act_width(int kind, int64_t inter) { return kind == ORC_GELU ? 2 
  *   h[n] = sum_c DQ(x)[c] * DQ(W1)[n][c]      n in [0, 2I)   (sequential double sum)
  *   gated: G = h[0:I] (gate), U = h[I:2I] (up), A[n] = Activation(G[n], U[n]);
  *   gelu:  A[n] = GELU(h[n]) for n in [0, 2I);  A rounded to fp32
- *   Ahat, S_A = Q_MX(A) in the dispatch format   (width W = I, or 2I for gelu)
+ *   Ahat, S_A = Q_MX(A) in the format a_code     (width W = I, or 2I for gelu)
  *   o[c] = sum_n DQ(Ahat)[n] * DQ(W2)[c][n]   c in [0, H), W2 [H, W]
  * Weights are in the storage layout [N_out, K_red] with E8M0 scales
  * [N_out, w_s_cols] (the pages' (., N_out, CeilDiv(K_red, 64), 2) flattened).
@@ -403,6 +406,13 @@ void orc_expert_row(const uint8_t* xq, const uint8_t* xs, int x_code, const uint
   free(xd); free(wd); free(hv); free(a); free(ad);
 }
 
+/* Format of A_hat for a dispatch format: the dispatch format itself in the
+ * A8W8-FP and A8W4-FP scenarios (their stage 2 re-quantises the activation
+ * into the dispatch type); MXFP8 E4M3 in the A4W4-FP scenario, whose stage 2
+ * re-quantises the activation into MXFP8 E4M3 so that the second layer is
+ * A8W4 (MegaMoE README, "A4W4-FP quantization scenario", stages 2-3). */
+int orc_act_code(int x_code) { return x_code == ORC_E2M1 ? ORC_E4M3 : x_code; }
+
 /* ---------------------------------------------------------------------------
  * MegaMoE at ep_world_size = 1, for a list of tokens (stage 4, combine):
  *   Y[i] = sum_k W[i,k] * O[pi(i,k)] + sum_s O_s^shared[i]
@@ -412,7 +422,7 @@ void orc_expert_row(const uint8_t* xq, const uint8_t* xs, int x_code, const uint
  * then the shared experts; Y is reported in double and rounded once to bf16.
  * Gating weights are fp32 (gate_is_bf16 = 0) or bf16 (1), widened exactly.
  * Optionally also returns the activation codes of every (token, k) pair:
- * aq_out [n_tok, K, I], as_out [n_tok, K, I/32].
+ * aq_out [n_tok, K, I], as_out [n_tok, K, I/32] (format orc_act_code(x_code)).
  * ------------------------------------------------------------------------- */
 void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate, int gate_is_bf16,
                          const uint8_t* w1, const uint8_t* s1, const uint8_t* w2, const uint8_t* s2,
@@ -426,6 +436,7 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
   int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((aw + 63) / 64);
   int64_t w1_sz = 2 * inter * h, w2_sz = h * aw;
   int64_t i_groups = (aw + 31) / 32;
+  int a_code = orc_act_code(x_code);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t t = 0; t < n_tok; ++t) {
     int64_t i = tokens[t];
@@ -448,14 +459,14 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
       double w = gate_is_bf16 ? orc_bf16_value(((const uint16_t*)gate)[i * k + kk])
                               : (double)((const float*)gate)[i * k + kk];
       orc_expert_row(xq, xs, x_code, w1 + e * w1_sz, s1 + e * 2 * inter * s1_cols,
-                     w2 + e * w2_sz, s2 + e * h * s2_cols, w_code, h, inter, x_code, act, act_p, aq, as, o);
+                     w2 + e * w2_sz, s2 + e * h * s2_cols, w_code, h, inter, a_code, act, act_p, aq, as, o);
       if (aq_out) memcpy(aq_out + (t * k + kk) * aw, aq, (size_t)aw);
       if (as_out) memcpy(as_out + (t * k + kk) * i_groups, as, (size_t)i_groups);
       for (int64_t c = 0; c < h; ++c) acc[c] += w * o[c];
     }
     for (int64_t s = 0; s < n_shared; ++s) {
       orc_expert_row(xq, xs, x_code, sw1 + s * w1_sz, ss1 + s * 2 * inter * s1_cols,
-                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, x_code, act, act_p,
+                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, a_code, act, act_p,
                      aq, as, o);
       for (int64_t c = 0; c < h; ++c) acc[c] += o[c];
     }

@@ -252,9 +252,12 @@ def test_permute_matches_gather(fmt):
 # ---------------------------------------------------------------- expert FFN
 def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
     """Grouped-by-expert FFN with numpy matmuls on dequantised operands, from
-    the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort."""
+    the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort.  The
+    activation is re-quantised in the dispatch type, except in the A4W4-FP
+    scenario (FP4 E2M1 dispatch), whose stage 2 re-quantises it to MXFP8 E4M3."""
     (w1, s1, w2, s2) = w
     fx = cfg.dispatch_fmt
+    fa = P.E4M3 if fx == P.E2M1 else fx
     xq, xs = P.brute_mx_rows(P.bf16_bits_to_f64(x), fx)
     n, h = x.shape
     k = ids.shape[1]
@@ -272,8 +275,8 @@ def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
         hv = xd @ w1d.T
         g, u = hv[:, :inter], hv[:, inter:]
         a = (g * expit(g) * u).astype(np.float32).astype(np.float64)
-        aq, a_s = P.brute_mx_rows(a, fx)
-        o = P.dequant_rows(aq, a_s, fx) @ P.dequant_rows(W2, S2, wfmt).T
+        aq, a_s = P.brute_mx_rows(a, fa)
+        o = P.dequant_rows(aq, a_s, fa) @ P.dequant_rows(W2, S2, wfmt).T
         return aq, o
 
     flat = ids.reshape(-1)[order]
@@ -310,6 +313,9 @@ def _weights(cfg, shared=False):
     # A8W4-FP: FLOAT4_E2M1 weights, MXFP8 E4M3 activations
     ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E4M3)),
     ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E4M3, n=16, shared=1, routing="zipf")),
+    # A4W4-FP: MXFP4 E2M1 tokens and weights, the activation re-quantised to MXFP8 E4M3
+    ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1)),
+    ("tiny", dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1, n=16, shared=1, routing="zipf", gate_dtype="bf16")),
 ])
 def test_mega_moe_matches_numpy_grouped(name, kw):
     cfg = synth.CONFIGS[name].scaled(**kw)
@@ -331,10 +337,12 @@ def test_mega_moe_matches_numpy_grouped(name, kw):
     assert np.max(np.abs(got_b - want_b)) <= 2.0 ** -8 * np.abs(want_b).max()
 
 
-@pytest.mark.parametrize("routed,shared_fmt", [(P.E2M1, P.E4M3), (P.E4M3, P.E2M1), (P.E5M2, P.E4M3)])
-def test_mega_moe_shared_weight_type_matches_numpy(routed, shared_fmt):
-    """Shared experts whose weight type differs from the routed experts'."""
-    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=2, weight_fmt=routed, dispatch_fmt=P.E4M3)
+@pytest.mark.parametrize("routed,shared_fmt,dispatch", [(P.E2M1, P.E4M3, P.E4M3), (P.E4M3, P.E2M1, P.E4M3),
+                                                       (P.E5M2, P.E4M3, P.E4M3), (P.E2M1, P.E4M3, P.E2M1)])
+def test_mega_moe_shared_weight_type_matches_numpy(routed, shared_fmt, dispatch):
+    """Shared experts whose weight type differs from the routed experts' (the
+    last case: FP4 tokens through FP8 shared weights under A4W4-FP)."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=2, weight_fmt=routed, dispatch_fmt=dispatch)
     x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
     w = _weights(cfg)
     sh = _weights(cfg.scaled(weight_fmt=shared_fmt), shared=True)
@@ -468,10 +476,11 @@ def test_gelu_matches_tanh_form():
     assert abs(0.5 * (1 + np.tanh(np.sqrt(2 / np.pi) * 1.044715)) - 0.8411919906) < 1e-9
 
 
-def test_prequant_passthrough_equals_internal_quantisation():
+@pytest.mark.parametrize("kw", [{}, dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1)])
+def test_prequant_passthrough_equals_internal_quantisation(kw):
     """dispatchQuantMode = 0: X_hat, S_X given by the caller.  Passing the
     oracle's own Q_MX(x) must reproduce the internal-quantisation result."""
-    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=1)
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=1, **kw)
     x = synth.tokens_bf16(cfg)
     ids = synth.topk_ids(cfg)
     gate = synth.topk_weights(cfg)
