@@ -252,7 +252,7 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
                 x_scales=None, out=None, workspace=None, dev_err=None, want_expanded_row_idx=False,
                 want_act=False, want_dispatch=False):
-    """MegaMoE forward, A8W8-FP or A8W4-FP, ep_world_size = 1.
+    """MegaMoE forward, A8W8-FP, A8W4-FP or A4W4-FP, ep_world_size = 1.
 
     x [BS, H] bf16; topk_ids [BS, K] int32; topk_weights [BS, K] fp32 / bf16;
     weight1 [E, 2I, H] and weight2 [E, H, I] FP8 (torch float8 or uint8 with
@@ -265,6 +265,9 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     X_hat codes [BS*K, H] / scales [BS*K, H/32], in sorted order.
     With dispatch_quant_mode=0, x holds FP8 codes (uint8 [BS, H]) and x_scales their
     E8M0 scales [BS, H/32] (pre-quantised pass-through).
+    A4W4-FP: dispatch_quant_out_dtype=DT_FP4_E2M1 with FP4 weights; the dispatched
+    X_hat is packed FP4 ([BS*K, H/2] when returned; x [BS, H/2] in pass-through) and
+    A_hat is MXFP8 E4M3.
     """
     _need_dtype(x, (torch.bfloat16,) if dispatch_quant_mode != 0 else _BYTE_DTYPES, "x")
     _need_dtype(topk_ids, (torch.int32,), "topk_ids")
@@ -280,7 +283,9 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
         raise MMError("topk_ids and topk_weights must both be [BS, K] with BS = x.shape[0]")
     _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
     L = load()
-    bs, h = x.shape
+    fp4_x = dispatch_quant_out_dtype == DT_FP4_E2M1
+    bs = x.shape[0]
+    h = x.shape[1] * 2 if fp4_x and dispatch_quant_mode == 0 else x.shape[1]   # packed FP4 pass-through
     k = topk_ids.shape[1]
     wdt = _fp8_code(weight1, weight_dtype)
     inter = weight1.shape[1] // 2
@@ -294,7 +299,7 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     exp_idx = torch.empty(bs * k, dtype=torch.int32, device=dev) if want_expanded_row_idx else None
     act_q = torch.empty((bs * k, aw), dtype=torch.uint8, device=dev) if want_act else None
     act_s = torch.empty((bs * k, aw // 32), dtype=torch.uint8, device=dev) if want_act else None
-    dsp_q = torch.empty((bs * k, h), dtype=torch.uint8, device=dev) if want_dispatch else None
+    dsp_q = torch.empty((bs * k, h // 2 if fp4_x else h), dtype=torch.uint8, device=dev) if want_dispatch else None
     dsp_s = torch.empty((bs * k, h // 32), dtype=torch.uint8, device=dev) if want_dispatch else None
     need = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, inter, s_num, weight_scale_layout)
     ws = _workspace(need, dev, workspace)
@@ -367,7 +372,8 @@ def mm_moe_ep_dispatch(x, topk_ids, moe_expert_num: int, ep_world_size: int,
     """Source side of the expert-parallel dispatch (MegaMoE stage 1 with
     epWorldSize > 1): rows j = i*K + k sorted stably by destination rank
     id // (E / W), each token MX-quantised once.  Returns (send_x [N*K, H] uint8
-    FP8 codes, send_scales [N*K, H/32] uint8 E8M0, send_expert [N*K] int32 local
+    FP8 codes ([N*K, H/2] packed for DT_FP4_E2M1), send_scales [N*K, H/32] uint8 E8M0,
+    send_expert [N*K] int32 local
     expert on the destination rank, rank_counts [W] int64, expanded_row_idx
     [N*K] int32 position of row j in the send order)."""
     _need_dtype(x, (torch.bfloat16, torch.float16), "x")
@@ -378,7 +384,8 @@ def mm_moe_ep_dispatch(x, topk_ids, moe_expert_num: int, ep_world_size: int,
     k = topk_ids.shape[1]
     rows = n * k
     dev = x.device
-    send_x = torch.empty((rows, h), dtype=torch.uint8, device=dev)
+    send_x = torch.empty((rows, h // 2 if dispatch_quant_out_dtype == DT_FP4_E2M1 else h), dtype=torch.uint8,
+                         device=dev)
     send_s = torch.empty((rows, h // 32), dtype=torch.uint8, device=dev)
     send_e = torch.empty(rows, dtype=torch.int32, device=dev)
     counts = torch.empty(ep_world_size, dtype=torch.int64, device=dev)
@@ -417,8 +424,9 @@ def mm_moe_expert_ffn(x, x_scales, expert_ids, weight1, weight2, weight_scales1,
                       out=None, workspace=None, dev_err=None):
     """The expert side of expert parallelism (MegaMoE stages 2-3 on the rows a
     rank receives): out[r] = the FFN of local expert expert_ids[r] on row r.
-    x [M, H] FP8 codes (uint8 or torch float8, type x_dtype), x_scales [M, H/32]
-    uint8 E8M0, expert_ids [M] int32; weights as for mm_mega_moe with E =
+    x [M, H] FP8 codes (uint8 or torch float8, type x_dtype; [M, H/2] packed for
+    DT_FP4_E2M1), x_scales [M, H/32] uint8 E8M0, expert_ids [M] int32; weights as
+    for mm_mega_moe with E =
     local_experts.  Returns (out [M, H] bf16, expert_token_nums [local_experts]
     int32)."""
     _need_dtype(x, _BYTE_DTYPES, "x")
@@ -429,7 +437,8 @@ def mm_moe_expert_ffn(x, x_scales, expert_ids, weight1, weight2, weight_scales1,
     for name, t in (("weight_scales1", weight_scales1), ("weight_scales2", weight_scales2)):
         _need_dtype(t, (torch.uint8,), name)
     _need_cuda(x, x_scales, expert_ids, weight1, weight2, weight_scales1, weight_scales2)
-    m, h = x.shape
+    m = x.shape[0]
+    h = x.shape[1] * 2 if x_dtype == DT_FP4_E2M1 else x.shape[1]
     if expert_ids.numel() != m or x_scales.shape[0] != m:
         raise MMError("expert_ids and x_scales must hold one entry / row per row of x")
     L = load()

@@ -492,9 +492,14 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   if (ep_world_size != 1) return MM_ERR_UNSUPPORTED;
   if (combine_quant_mode != 0) return MM_ERR_UNSUPPORTED;
   // 4: MX quantisation inside the operator; 0: pre-quantised pass-through
-  // (x holds FP8 codes of dispatch_quant_out_dtype, x_scales its E8M0 scales)
+  // (x holds codes of dispatch_quant_out_dtype, x_scales its E8M0 scales).
+  // An FP4 E2M1 dispatch is the A4W4-FP scenario: FP4 routed weights, and
+  // A_hat re-quantised to MXFP8 E4M3 so that GEMM2 is A8W4.
   if (dispatch_quant_mode != 4 && dispatch_quant_mode != 0) return MM_ERR_UNSUPPORTED;
-  if (!is_fp8(dispatch_quant_out_dtype) || !is_mx_weight(weight_dtype)) return MM_ERR_UNSUPPORTED;
+  if (!is_mx_weight(dispatch_quant_out_dtype) || !is_mx_weight(weight_dtype)) return MM_ERR_UNSUPPORTED;
+  const bool a4w4 = dispatch_quant_out_dtype == MM_DT_FP4_E2M1;
+  if (a4w4 && weight_dtype != MM_DT_FP4_E2M1) return MM_ERR_UNSUPPORTED;
+  const int act_fmt = a4w4 ? MM_DT_FP8_E4M3FN : (int)dispatch_quant_out_dtype;
   if (shared_expert_num > 0 && !is_mx_weight(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
   if (bs > 0 && (dispatch_quant_mode == 0) != (x_scales != nullptr)) return MM_ERR_INVALID_ARG;
   ActSpec act;
@@ -611,6 +616,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   g1.K = d.h;
   g1.N = 2 * d.inter;
   g1.a_fmt = (int)dispatch_quant_out_dtype;
+  g1.act_fmt = act_fmt;
   g1.b_fmt = weight_dtype;
   g1.b_fmt_sh = shared_weight_dtype;
   g1.inter = (int)d.inter;
@@ -631,6 +637,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   GemmLaunch g2 = g1;
   g2.mode = 2;
   g2.a = w.aq;
+  g2.a_fmt = act_fmt;
   g2.sfa = w.asf;
   g2.b = weight2;
   g2.sfb = wsf2;
@@ -680,6 +687,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
     ua.expanded_row_idx = o.expanded_row_idx;
     ua.rows = d.rows;
     ua.cols = d.h;
+    ua.qbytes = a4w4 ? d.h / 2 : d.h;
     ua.dst_q = dispatch_q;
     ua.dst_sf = dispatch_scale;
     ua.rows_cap = d.rows_cap;
@@ -697,6 +705,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
     ua.expanded_row_idx = o.expanded_row_idx;
     ua.rows = d.rows;
     ua.cols = aw;
+    ua.qbytes = aw;
     ua.dst_q = act_q;
     ua.dst_sf = act_scale;
     ua.rows_cap = d.rows_cap;
@@ -778,7 +787,7 @@ mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids
   if (s != MM_OK) return s;
   if (moe_expert_num <= 0 || moe_expert_num % ep_world_size != 0 || k > moe_expert_num) return MM_ERR_INVALID_ARG;
   if (x_dtype != MM_DT_BFLOAT16 && x_dtype != MM_DT_FLOAT16) return MM_ERR_INVALID_ARG;
-  if (!is_fp8(dispatch_quant_out_dtype)) return MM_ERR_UNSUPPORTED;
+  if (!is_mx_weight(dispatch_quant_out_dtype)) return MM_ERR_UNSUPPORTED;  // FP8, or FP4 (A4W4-FP)
   if (h <= 0 || h % 128 != 0) return MM_ERR_UNSUPPORTED;
   const int64_t rows = num_rows * k;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

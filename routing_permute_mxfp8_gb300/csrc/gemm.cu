@@ -101,6 +101,7 @@ struct GemmArgs {
   int32_t* dev_err;
   int o_stage;    // stage output blocks (A_hat / O) in shared memory for TMA stores
   int b_fp4, b_fp4_sh;  // routed / shared weights are packed FP4 E2M1
+  int a_fp4;           // A is packed FP4 E2M1 (GEMM1 of A4W4-FP)
   // mode 1: activation (MM_ACT_*), its parameters, and the width of A_hat
   int act;
   float act_c, act_alpha, act_beta, act_rbeta, act_beta_lin, act_rbeta_lin, act_gelu_k;
@@ -349,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // packed FP4 weights count their global (packed) bytes
-          mbar_arrive_expect_tx(&full[stage], kStageTx - ((sh ? g.b_fp4_sh : g.b_fp4) ? kBBytes / 2 : 0));
+          // packed FP4 operands count their global (packed) bytes
+          mbar_arrive_expect_tx(&full[stage], kStageTx - ((sh ? g.b_fp4_sh : g.b_fp4) ? kBBytes / 2 : 0) -
+                                                  (g.a_fp4 ? kABytes / 2 : 0));
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], kb * kBK, am * kBM);
@@ -600,14 +602,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// FP8 byte matrix [outer][inner] (inner contiguous), box inner 128 B, 128B swizzle.
-bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// FP8 byte matrix [outer][inner] (inner contiguous), box inner 128 codes,
+// 128B swizzle; or packed FP4 E2M1 (inner / 2 bytes a row), expanded by TMA
+// like the FP4 weights below.
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer, bool fp4 = false) {
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner};
+  cuuint64_t strides[1] = {fp4 ? inner / 2 : inner};
   cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
   cuuint32_t es[2] = {1, 1};
   EncodeTiledFn f = encode_fn();
-  return f && f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+  return f && f(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                const_cast<void*>(ptr), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -714,7 +719,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
                     : map_3d(m, p, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)experts, (uint32_t)bn, fp4);
   };
   CUtensorMap ma, mb, mbs;
-  if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM)) return cudaErrorInvalidValue;
+  if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM, L.a_fmt == MM_DT_FP4_E2M1))
+    return cudaErrorInvalidValue;
   if (!map_b(&mb, L.b, L.n_routed, L.b_fmt)) return cudaErrorInvalidValue;
   if (L.n_shared > 0) {
     if (!map_b(&mbs, L.b_sh, L.n_shared, L.b_fmt_sh)) return cudaErrorInvalidValue;
@@ -742,6 +748,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.big_mt = kBigMtiles;
   g.npairs = (int)prepared_npairs(L.N, L.mode);
   g.b_fp4 = L.b_fmt == MM_DT_FP4_E2M1;
+  g.a_fp4 = L.a_fmt == MM_DT_FP4_E2M1;
   g.act = L.act;
   g.act_c = L.act_c;
   g.act_alpha = L.act_alpha;
@@ -767,8 +774,9 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   int64_t grid = max_mtiles * g.n_tiles;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  if (L.mode == 1) {
-    if (L.a_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
+  if (L.mode == 1) {  // the template argument is A_hat's type
+    if (L.act_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
+    if (L.act_fmt != MM_DT_FP8_E4M3FN) return cudaErrorInvalidValue;
     return run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
   }
   return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);

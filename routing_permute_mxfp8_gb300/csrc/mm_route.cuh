@@ -101,7 +101,7 @@ cudaError_t launch_prepare_wscales(const uint8_t* src, int64_t experts, int64_t 
 // ---- grouped GEMMs (gemm.cu) ----------------------------------------------
 struct GemmLaunch {
   int mode;                   // 1: GEMM1 + swiglu + MX requant; 2: GEMM2 -> bf16
-  const uint8_t* a;           // [rows_cap, K] FP8 A (padded grouped layout)
+  const uint8_t* a;           // [rows_cap, K] FP8 A (padded grouped layout), or packed FP4 [rows_cap, K/2]
   int64_t rows_cap;
   const uint8_t* sfa;         // A scales, tile layout
   const uint8_t* b;           // routed weights [E, N, K] FP8
@@ -112,7 +112,8 @@ struct GemmLaunch {
   const int32_t* seg_rows;    // [n_routed + n_shared]
   const int32_t* seg_mprefix; // [n_routed + n_shared + 1]
   int64_t K, N;
-  int a_fmt, b_fmt, b_fmt_sh; // 23 / 24
+  int a_fmt, b_fmt, b_fmt_sh; // 23 / 24, or 296 (packed FP4 E2M1)
+  int act_fmt;                // mode 1: type of A_hat (23 / 24)
   int inter;                  // mode 1: I (= N / 2)
   int act;                    // mode 1: MM_ACT_* (A_hat width I, or 2I for gelu)
   float act_c, act_alpha, act_beta, act_beta_lin;  // clamp (+inf: off), swigluoai alpha / beta,
@@ -145,12 +146,13 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
 // diagnostic: padded grouped rows -> expert-sorted dense rows
 struct UnpadArgs {
-  const uint8_t* src_q;       // [rows_cap, cols]
+  const uint8_t* src_q;       // [rows_cap, qbytes]
   const uint8_t* src_sf;      // tile layout, cols/128 groups4
   const int32_t* pad_row;     // [rows]
   const int32_t* expanded_row_idx;  // [rows]
-  int64_t rows, cols;
-  uint8_t* dst_q;             // [rows, cols]
+  int64_t rows, cols;         // cols: elements of a row (cols / 32 scale groups)
+  int64_t qbytes;             // bytes of a row of codes: cols, or cols / 2 for packed FP4
+  uint8_t* dst_q;             // [rows, qbytes]
   uint8_t* dst_sf;            // [rows, cols/32]
   int64_t rows_cap;           // rows of src_q (checked build)
   int32_t* dev_err;

@@ -240,19 +240,19 @@ __global__ void k_unpad(UnpadArgs a) {
   if (j >= a.rows) return;
   const int32_t d = a.expanded_row_idx[j], p = a.pad_row[j];
   if (d < 0 || p < 0 || !in_bounds(d < a.rows && p < a.rows_cap, a.dev_err)) return;
-  for (int64_t c = lane * 16; c < a.cols; c += 512)
-    *reinterpret_cast<uint4*>(a.dst_q + (int64_t)d * a.cols + c) =
-        *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * a.cols + c);
+  for (int64_t c = lane * 16; c < a.qbytes; c += 512)
+    *reinterpret_cast<uint4*>(a.dst_q + (int64_t)d * a.qbytes + c) =
+        *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * a.qbytes + c);
   const int64_t groups = a.cols / 32;
   for (int64_t g = lane; g < groups; g += 32)
     a.dst_sf[(int64_t)d * groups + g] = a.src_sf[sf_tile_offset(p, g, a.cols / 128)];
 }
 
 // Pre-quantised pass-through (MegaMoE dispatchQuantMode = 0): the source
-// rows already hold FP8 codes and src_scales their E8M0 scales, [n, h/32];
-// each row is copied to its destinations and its scales rewritten in the
-// GEMM tile layout.  Warp per row, 16 bytes per lane, one 4-group scale
-// word per lane and step.
+// rows already hold FP8 codes (h bytes) or packed FP4 E2M1 codes (h / 2
+// bytes) and src_scales their E8M0 scales, [n, h/32]; each row is copied to
+// its destinations and its scales rewritten in the GEMM tile layout.  Warp
+// per row, 16 bytes per lane, one 4-group scale word per lane and step.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(PermuteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
   int ndest;
   load_dests(a, row, lane, d0, d1, ndest);
   if (a.dest_inv && lane < a.k && d0 >= 0) a.dest_inv[d0] = (int32_t)(row * a.k + lane);
-  const uint8_t* src_row = static_cast<const uint8_t*>(a.src) + row * a.h;
+  const int64_t rb = a.out_fmt == MM_DT_FP4_E2M1 ? a.h / 2 : a.h;
+  const uint8_t* src_row = static_cast<const uint8_t*>(a.src) + row * rb;
   const uint8_t* src_sf = a.src_scales + row * (a.h / 32);
   uint8_t* out = static_cast<uint8_t*>(a.out);
   const int64_t groups4 = a.h / 128;
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
   for (int t = 0; t < ndest; ++t) {
     const int32_t d = dest_at(t, d0, d1);
     if (d < 0) continue;  // uniform across the warp
-    for (int64_t col = lane * 16; col < a.h; col += 512)
-      *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = *reinterpret_cast<const uint4*>(src_row + col);
+    for (int64_t col = lane * 16; col < rb; col += 512)
+      *reinterpret_cast<uint4*>(out + (int64_t)d * rb + col) = *reinterpret_cast<const uint4*>(src_row + col);
     for (int64_t w = lane; w < groups4; w += 32)
       *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, 4 * w, groups4)) =
           *reinterpret_cast<const uint32_t*>(src_sf + 4 * w);

@@ -30,16 +30,23 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _cfg():
+def _cfg(a4w4=False):
     import synth
     # 2 ranks x 4 experts; Zipf routing so the two ranks receive unequal row counts
-    return synth.CONFIGS["tiny"].scaled(n=96, e=8, k=3, routing="zipf", dispatch_fmt=23, gate_dtype="bf16")
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, e=8, k=3, routing="zipf", dispatch_fmt=23, gate_dtype="bf16")
+    # A4W4-FP: MXFP4 rows exchanged (packed, H/2 bytes a row), FP4 weights
+    return cfg.scaled(weight_fmt=296, dispatch_fmt=296) if a4w4 else cfg
 
 
-def _problem():
+def _pack_fp4(c):
+    """One FP4 code per byte -> the library's packed bytes (element 2i in bits 0-3)."""
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def _problem(a4w4=False):
     import oracle
     import synth
-    cfg = _cfg()
+    cfg = _cfg(a4w4)
     x = synth.tokens_bf16(cfg)
     ids = synth.topk_ids(cfg)
     gate = synth.topk_weights(cfg)
@@ -151,7 +158,7 @@ def test_ep_exchange_two_gloo_ranks_cpu():
     _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))
 
 
-def _gpu_rank(rank, port, out):
+def _gpu_rank(rank, port, out, a4w4):
     import sys
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -159,7 +166,9 @@ def _gpu_rank(rank, port, out):
     import routing_permute_mxfp8_gb300 as mm
     from routing_permute_mxfp8_gb300 import ep
     torch.cuda.set_device(0)
-    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem()
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem(a4w4)
+    if cfg.weight_fmt == 296:
+        w1, w2 = _pack_fp4(w1), _pack_fp4(w2)
     dist.init_process_group("gloo", rank=rank, world_size=W)
     sl = _slices(cfg, rank)
     el = cfg.e // W
@@ -180,11 +189,12 @@ def _gpu_rank(rank, port, out):
 
 
 @pytest.mark.gpu
-def test_ep_two_ranks_on_one_gpu_matches_single_process():
+@pytest.mark.parametrize("a4w4", [False, True], ids=["a8w8", "a4w4"])
+def test_ep_two_ranks_on_one_gpu_matches_single_process(a4w4):
     port = _free_port()
     out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
-    mp.spawn(_gpu_rank, args=(port, out), nprocs=W, join=True)
-    cfg, x, ids, gate, w = _problem()
+    mp.spawn(_gpu_rank, args=(port, out, a4w4), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem(a4w4)
     ys = []
     for r in range(W):
         y, y1, err = out[r]

@@ -37,8 +37,9 @@ def test_routing_checked(path, case):
     P.test_init_routing_bit_exact(*case)
 
 
-@pytest.mark.parametrize("case", ["tiny_shared", "zipf_mixed_sizes", "a8w4_shared_zipf", "gelu", "max_experts",
-                                  "topk32_shared4", "small_seg_zipf_mixed", "h896_ragged_n", "many_experts"])
+@pytest.mark.parametrize("case", ["tiny_shared", "zipf_mixed_sizes", "a8w4_shared_zipf", "a4w4_shared_zipf_bf16gate",
+                                  "gelu", "max_experts", "topk32_shared4", "small_seg_zipf_mixed", "h896_ragged_n",
+                                  "many_experts"])
 def test_mega_moe_checked(case):
     P.run_mega(synth.CONFIGS["tiny"].scaled(**P.MEGA_CASES[case]))
 
@@ -58,6 +59,7 @@ def test_permute_expert_parallel_and_combine_checked():
     P.test_token_permute_bit_exact(torch.bfloat16, False, 6, -1, False)
     P.test_token_permute_bit_exact(torch.float16, True, -7, 9, False)
     P.test_ep_dispatch_bit_exact(4, 24)
+    P.test_ep_dispatch_bit_exact(4, 296)
     P.test_moe_combine_rows(True)
     P.test_out_of_range_ids_are_left_out_and_flagged()
     P.test_expert_ffn_equals_mega_moe_top1(dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"))

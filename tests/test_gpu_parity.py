@@ -306,6 +306,8 @@ def check_dispatch(xq_gpu, xs_gpu, x, cfg, r_srt, tokens=None):
     With sampled tokens only the rows of those tokens are compared (the
     oracle quantises every row; that part is cheap)."""
     q_ref, s_ref = oracle.permute(x, oracle.DT_BF16, cfg.k, r_srt, r_srt.size, cfg.dispatch_fmt)
+    if cfg.dispatch_fmt == 296:   # A4W4-FP: the library's X_hat is packed FP4
+        q_ref = pack_fp4(q_ref)
     rows = np.arange(r_srt.size) if tokens is None else np.nonzero(np.isin(r_srt // cfg.k, tokens))[0]
     assert np.array_equal(xq_gpu[rows], q_ref[rows])
     assert np.array_equal(xs_gpu[rows], s_ref[rows, :xs_gpu.shape[1]])
@@ -404,6 +406,16 @@ MEGA_CASES = {
     "a8w4_shared_zipf": dict(n=300, h=512, inter=256, e=8, k=4, shared=1, routing="zipf", weight_fmt=296,
                              dispatch_fmt=24),
     "a8w4_e5m2_tokens": dict(n=256, h=896, inter=384, e=8, k=4, weight_fmt=296, dispatch_fmt=23),
+    # A4W4-FP: MXFP4 E2M1 tokens and weights, A_hat MXFP8 E4M3 (GEMM2 A8W4)
+    "a4w4_tiny": dict(weight_fmt=296, dispatch_fmt=296),
+    "a4w4_shared_zipf_bf16gate": dict(n=300, h=512, inter=256, e=8, k=4, shared=1, routing="zipf", weight_fmt=296,
+                                      dispatch_fmt=296, gate_dtype="bf16"),
+    "a4w4_h896_ragged": dict(n=257, h=896, inter=384, e=8, k=4, weight_fmt=296, dispatch_fmt=296),
+    "a4w4_gelu": dict(n=200, h=512, inter=256, e=8, k=4, activation="gelu", weight_fmt=296, dispatch_fmt=296,
+                      act_params=(float(np.finfo(np.float32).max),)),
+    "a4w4_swigluoai": dict(n=128, e=8, k=4, activation="swigluoai", act_params=(0.05, 1.5, 0.25), weight_fmt=296,
+                           dispatch_fmt=296),
+    "a4w4_small_seg_zipf": dict(n=300, h=256, inter=384, e=32, k=2, routing="zipf", weight_fmt=296, dispatch_fmt=296),
     # the README's other activations ("Activation function formulas") and clamps
     "swiglu_clamp": dict(n=128, e=8, k=4, act_params=(0.05,)),
     "swiglustep_clamp": dict(n=128, e=8, k=4, activation="swiglustep", act_params=(0.002,)),
@@ -457,11 +469,11 @@ def _random_mega_cfg(seed):
         shared=int(rng.integers(0, 3)), activation=act, act_params=params, seed=seed)
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(10))
 def test_mega_moe_random_shapes(seed):
     cfg = _random_mega_cfg(seed)
-    if cfg.weight_fmt == 296:
-        cfg = cfg.scaled(dispatch_fmt=24 if seed % 2 else 23)
+    if cfg.weight_fmt == 296:   # FP4 weights: A8W4-FP with either FP8 dispatch, or A4W4-FP
+        cfg = cfg.scaled(dispatch_fmt=(23, 24, 296)[seed % 3])
     run_mega(cfg, layout=seed % 2)  # odd seeds: weight scales prepared once (mm_prepare_weight_scales)
 
 
@@ -471,22 +483,27 @@ def test_mega_moe_small(case):
     run_mega(cfg)
 
 
-def test_mega_moe_prequant_passthrough():
-    """dispatch_quant_mode 0: the caller's FP8 codes and E8M0 scales are used as
-    X_hat, S_X.  Feeding Q_MX(x) (oracle) gives the internal-quantisation result
-    bit for bit, and matches the oracle's pass-through run."""
-    cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1, routing="zipf")
+@pytest.mark.parametrize("fmts", [(24, 24), (296, 296)], ids=["a8w8", "a4w4"])
+def test_mega_moe_prequant_passthrough(fmts):
+    """dispatch_quant_mode 0: the caller's FP8 (or packed FP4) codes and E8M0
+    scales are used as X_hat, S_X.  Feeding Q_MX(x) (oracle) gives the
+    internal-quantisation result bit for bit, and matches the oracle's
+    pass-through run."""
+    wf, df = fmts
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, shared=1, routing="zipf", weight_fmt=wf, dispatch_fmt=df)
     x = synth.tokens_bf16(cfg)
     ids = synth.topk_ids(cfg)
     gate = synth.topk_weights(cfg)
     w1, s1, w2, s2 = _weights(cfg)
     sh = _weights(cfg, shared=True)
     xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, cfg.dispatch_fmt)
-    kw = dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]), shared_weight2=t(sh[2]),
-              shared_weight_scales2=t(sh[3]), dispatch_quant_out_dtype=cfg.dispatch_fmt)
+    kw = dict(shared_weight1=gpu_codes(sh[0], wf), shared_weight_scales1=t(sh[1]),
+              shared_weight2=gpu_codes(sh[2], wf), shared_weight_scales2=t(sh[3]),
+              dispatch_quant_out_dtype=cfg.dispatch_fmt, weight_dtype=wf)
     err = zeros_err()
-    y0 = mm.mm_mega_moe(bf16(x), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err, **kw)[0]
-    y1 = mm.mm_mega_moe(t(xq), t(ids), t(gate), t(w1), t(w2), t(s1), t(s2), cfg.e, dev_err=err,
+    g1, g2 = gpu_codes(w1, wf), gpu_codes(w2, wf)
+    y0 = mm.mm_mega_moe(bf16(x), t(ids), t(gate), g1, g2, t(s1), t(s2), cfg.e, dev_err=err, **kw)[0]
+    y1 = mm.mm_mega_moe(gpu_codes(xq, df), t(ids), t(gate), g1, g2, t(s1), t(s2), cfg.e, dev_err=err,
                         dispatch_quant_mode=0, x_scales=t(xs), **kw)[0]
     assert host(err)[0] == 0
     assert np.array_equal(host(y0).view(np.uint16), host(y1).view(np.uint16))
@@ -495,11 +512,13 @@ def test_mega_moe_prequant_passthrough():
     check_y(synth.bf16_bits_to_f32(host(y1).view(np.uint16)), y_ref)
 
 
-@pytest.mark.parametrize("routed_fmt,shared_fmt", [(296, 24), (24, 296), (23, 24)])
-def test_mega_moe_shared_weight_type_differs(routed_fmt, shared_fmt):
+@pytest.mark.parametrize("routed_fmt,shared_fmt,dispatch", [(296, 24, 24), (24, 296, 24), (23, 24, 24),
+                                                            (296, 24, 296)])
+def test_mega_moe_shared_weight_type_differs(routed_fmt, shared_fmt, dispatch):
     """Routed and shared experts with different weight types (the shared
-    expert's own MMA format), e.g. FP4 routed experts beside an FP8 shared one."""
-    cfg = synth.CONFIGS["tiny"].scaled(n=128, e=8, k=4, shared=2, weight_fmt=routed_fmt, dispatch_fmt=24)
+    expert's own MMA format), e.g. FP4 routed experts beside an FP8 shared one;
+    the last case dispatches FP4 tokens (A4W4-FP) into FP8 shared weights."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=128, e=8, k=4, shared=2, weight_fmt=routed_fmt, dispatch_fmt=dispatch)
     cfg_sh = cfg.scaled(weight_fmt=shared_fmt)
     x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
     w1, s1, w2, s2 = _weights(cfg)
@@ -562,6 +581,20 @@ def test_mega_moe_dsv3_prefill_a8w4_full_size():
     """A8W4-FP (MXFP4 weights, MXFP8 E4M3 activations) at the DeepSeek-V3 prefill shape."""
     cfg = synth.CONFIGS["dsv3_prefill"].scaled(weight_fmt=296, dispatch_fmt=24)
     run_mega(cfg, tokens=np.array([0, 3, 1500, 4096, 7000, 8191]), layout=1, sparse=True)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_prefill_a4w4_full_size():
+    """A4W4-FP (MXFP4 tokens and weights, MXFP8 E4M3 activation) at the DeepSeek-V3 prefill shape."""
+    cfg = synth.CONFIGS["dsv3_prefill"].scaled(weight_fmt=296, dispatch_fmt=296)
+    run_mega(cfg, tokens=np.array([0, 2, 1501, 4097, 7001, 8191]), layout=1, sparse=True)
+
+
+@pytest.mark.slow
+def test_mega_moe_dsv3_decode_a4w4_full_size():
+    """A4W4-FP at the decode shape, with its shared expert."""
+    cfg = synth.CONFIGS["dsv3_decode"].scaled(weight_fmt=296, dispatch_fmt=296)
+    run_mega(cfg, tokens=np.array([0, 9, 64, 127]), layout=1, sparse=True)
 
 
 @pytest.mark.slow
@@ -711,7 +744,7 @@ def test_ep_dispatch_every_routing_path(route_path):
     test_ep_dispatch_bit_exact(4, 24)
 
 
-@pytest.mark.parametrize("w,fmt", [(1, 24), (2, 23), (4, 24), (16, 23)])
+@pytest.mark.parametrize("w,fmt", [(1, 24), (2, 23), (4, 24), (16, 23), (4, 296)])
 def test_ep_dispatch_bit_exact(w, fmt):
     """mm_moe_ep_dispatch against the oracle: the stable sort by destination
     rank id // (E/W) (the routing of MoeInitRoutingV3 on rank keys), Q_MX of
@@ -729,7 +762,7 @@ def test_ep_dispatch_bit_exact(w, fmt):
     assert np.array_equal(host(cnt), ocnt)
     assert np.array_equal(host(ei), exp)
     assert np.array_equal(host(se), ids.reshape(-1)[srt] % el)
-    assert np.array_equal(host(sx), q)
+    assert np.array_equal(host(sx), pack_fp4(q) if fmt == 296 else q)
     assert np.array_equal(host(ss), sc[:, :cfg.h // 32])
 
 
@@ -737,6 +770,7 @@ def test_ep_dispatch_bit_exact(w, fmt):
     dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"),
     dict(n=300, h=896, inter=384, e=5, k=1, weight_fmt=296, dispatch_fmt=23),
     dict(n=200, h=512, inter=256, e=16, k=1, activation="gelu", act_params=(float(np.finfo(np.float32).max),)),
+    dict(n=300, h=512, inter=256, e=8, k=1, routing="zipf", weight_fmt=296, dispatch_fmt=296),   # A4W4-FP rows
 ])
 def test_expert_ffn_equals_mega_moe_top1(case):
     """mm_moe_expert_ffn (the expert side of expert parallelism: GEMM2 writes
@@ -748,8 +782,8 @@ def test_expert_ffn_equals_mega_moe_top1(case):
     ids = synth.topk_ids(cfg)
     w1, s1, w2, s2 = _weights(cfg)
     fmt = cfg.dispatch_fmt
-    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, fmt)   # the received rows: FP8 codes + E8M0 scales
-    xq, xs = t(xq), t(xs)
+    xq, xs = oracle.mx_quantize(x, oracle.DT_BF16, fmt)   # the received rows: FP8 (FP4) codes + E8M0 scales
+    xq, xs = gpu_codes(xq, fmt), t(xs)
     ids1 = t(ids.reshape(cfg.n))
     err = zeros_err()
     out, cnt = mm.mm_moe_expert_ffn(xq, xs, ids1, gpu_codes(w1, cfg.weight_fmt), gpu_codes(w2, cfg.weight_fmt), t(s1),
