@@ -60,8 +60,9 @@ def parse_args():
                          "FP8/bf16 ratio times the measured bf16 peak")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling on a smaller case)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling on a smaller case)")
-    ap.add_argument("--weights", choices=["fp8", "fp4"], default="fp8",
-                    help="fp4: the A8W4-FP variant of the workload (MXFP4 weights, MXFP8 E4M3 activations)")
+    ap.add_argument("--weights", choices=["fp8", "fp4", "a4w4"], default="fp8",
+                    help="fp4: the A8W4-FP variant of the workload (MXFP4 weights, MXFP8 E4M3 activations); "
+                         "a4w4: the A4W4-FP variant (MXFP4 tokens and weights, MXFP8 E4M3 activation for GEMM2)")
     return ap.parse_args()
 
 
@@ -74,6 +75,8 @@ def workload(args):
         cfg = cfg.scaled(e=args.experts)
     if args.weights == "fp4":
         cfg = cfg.scaled(name=cfg.name + "_a8w4", weight_fmt=296, dispatch_fmt=24)
+    if args.weights == "a4w4":
+        cfg = cfg.scaled(name=cfg.name + "_a4w4", weight_fmt=296, dispatch_fmt=296)
     return cfg
 
 
@@ -201,9 +204,10 @@ class Dist:
 
 
 # ----------------------------------------------------------------------------- inputs on the GPU
-def gpu_inputs(cfg, mm, torch, seed_offset=0, weights=None):
+def gpu_inputs(cfg, mm, torch, seed_offset=0, weights=None, shared=None):
     """x, ids, gates from the seeded generator; fp32 N(0, 0.02) weights drawn on
-    the GPU (seeded torch generator) and MX-quantised by the library."""
+    the GPU (seeded torch generator) and MX-quantised by the library (or the
+    given routed / shared weights, reused)."""
     import synth
     dev = torch.device("cuda")
     x = torch.from_numpy(synth.tokens_bf16(cfg).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -213,10 +217,9 @@ def gpu_inputs(cfg, mm, torch, seed_offset=0, weights=None):
             else torch.from_numpy(g).to(dev))
     if weights is None:
         weights = gpu_weights(cfg, mm, torch, cfg.e, seed=1000 + seed_offset)
-    shared = None
-    if cfg.shared:
+    if cfg.shared and shared is None:
         shared = gpu_weights(cfg, mm, torch, cfg.shared, seed=2000 + seed_offset)
-    return x, ids, gate, weights, shared
+    return x, ids, gate, weights, shared if cfg.shared else None
 
 
 def gpu_weights(cfg, mm, torch, n_exp, seed):
@@ -343,8 +346,9 @@ def stage_rooflines(cfg, ms, hbm_peak, fp8_peak):
             out[name] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                          "algorithmic_bytes": nbytes, "ms": ms[name]}
 
-    # dispatch: x and the row indices read; FP8 rows and E8M0 scales written
-    hbm("dispatch", cfg.n * cfg.h * 2 + cfg.n * cfg.k * 4 + rows * cfg.h + rows * (cfg.h // 32))
+    # dispatch: x and the row indices read; FP8 (packed FP4) rows and E8M0 scales written
+    xb = 0.5 if cfg.dispatch_fmt == 296 else 1.0
+    hbm("dispatch", cfg.n * cfg.h * 2 + cfg.n * cfg.k * 4 + rows * cfg.h * xb + rows * (cfg.h // 32))
     # combine: O rows, gating weights and indices read; Y written
     hbm("combine", rows * cfg.h * 2 + cfg.n * cfg.k * (gate_b + 4) + cfg.n * cfg.h * 2)
     if ms.get("gemm2"):
@@ -477,11 +481,13 @@ def library_mxfp8_peak(torch, sustain_s=2.0):
 def gemm1_algorithmic_bytes(cfg, rows):
     """Compulsory bytes of one GEMM1 launch: the weights of the experts that
     receive rows (FP8 1 byte or FP4 half a byte per element, plus one E8M0
-    byte per 32), X_hat and its scales read, A_hat and its scales written."""
+    byte per 32), X_hat (FP8, or packed FP4 under A4W4-FP) and its scales
+    read, A_hat (FP8) and its scales written."""
     wb = 0.5 if cfg.weight_fmt == 296 else 1.0
+    xb = 0.5 if cfg.dispatch_fmt == 296 else 1.0
     per_expert = 2 * cfg.inter * cfg.h * (wb + 1 / 32)
     experts = cfg.e + cfg.shared
-    return experts * per_expert + rows * cfg.h * (1 + 1 / 32) + rows * cfg.act_width * (1 + 1 / 32)
+    return experts * per_expert + rows * cfg.h * (xb + 1 / 32) + rows * cfg.act_width * (1 + 1 / 32)
 
 
 def ffn_flops(cfg, tokens=None):
@@ -731,10 +737,12 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded generator; random-init weights)",
+        "vs_baseline": None,
+        "dtype": {"fp8": "mxfp8", "fp4": "mxfp8 x mxfp4", "a4w4": "mxfp4 (GEMM1), mxfp8 x mxfp4 (GEMM2)"}[args.weights],
+        "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": cfg.name, "tokens": cfg.n, "hidden": cfg.h, "intermediate": cfg.inter,
                    "experts": cfg.e, "topk": cfg.k, "routing": f"{cfg.routing}" + (" s=1.0" if cfg.routing == "zipf" else ""),
-                   "dispatch": "mxfp8_e5m2" if cfg.dispatch_fmt == 23 else "mxfp8_e4m3",
+                   "dispatch": {23: "mxfp8_e5m2", 24: "mxfp8_e4m3", 296: "mxfp4_e2m1"}[cfg.dispatch_fmt],
                    "weights": {24: "mxfp8_e4m3", 23: "mxfp8_e5m2", 296: "mxfp4_e2m1"}[cfg.weight_fmt],
                    "gate": cfg.gate_dtype, "shared_experts": cfg.shared,
                    "weight_scale_layout": "prepared once (mm_prepare_weight_scales)",
@@ -832,35 +840,43 @@ def secondary_measurements(args, mm, torch, synth, dist, hbm_peak, fp8_peak, W_p
     if cfg_prefill.weight_fmt == mm.DT_FP4_E2M1:
         return out
     # A8W4-FP: the same prefill and decode shapes with MXFP4 E2M1 weights (packed,
-    # half the weight bytes) and MXFP8 E4M3 activations
-    a8w4 = {}
+    # half the weight bytes) and MXFP8 E4M3 activations; A4W4-FP: the same FP4
+    # weights with the tokens dispatched as MXFP4 too (GEMM2 stays A8W4)
     pc4 = cfg_prefill.scaled(weight_fmt=mm.DT_FP4_E2M1, dispatch_fmt=mm.DT_FP8_E4M3FN)
-    x, ids, gate, W4, _ = gpu_inputs(pc4, mm, torch, seed_offset=30 + dist.rank)
-    ws = torch.empty(mm.mm_mega_moe_workspace_size(pc4.n, pc4.h, pc4.k, pc4.e, pc4.inter, pc4.shared, 1),
-                     dtype=torch.uint8, device="cuda")
-    y = torch.empty((pc4.n, pc4.h), dtype=torch.bfloat16, device="cuda")
-    ms, st, _ = time_steps(torch, lambda: mega_call(mm, pc4, x, ids, gate, W4, None, ws, y), steps, 3, dist)
-    t = ms / steps / 1e3
-    a8w4["prefill"] = {"workload": f"{pc4.name} N={pc4.n} H={pc4.h} I={pc4.inter} E={pc4.e} K={pc4.k}",
-                       "tokens_per_s": pc4.n / t, "ms_per_step": t * 1e3, "tflops": ffn_flops(pc4) / t / 1e12,
-                       "tflops_frac": ffn_flops(pc4) / t / 1e12 / fp8_peak,
-                       "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
-    del x, ws
-    dc4 = dc.scaled(weight_fmt=mm.DT_FP4_E2M1, dispatch_fmt=mm.DT_FP8_E4M3FN)
-    x, ids, gate, _, S4 = gpu_inputs(dc4, mm, torch, seed_offset=40 + dist.rank, weights=W4)
-    ws = torch.empty(mm.mm_mega_moe_workspace_size(dc4.n, dc4.h, dc4.k, dc4.e, dc4.inter, dc4.shared, 1),
-                     dtype=torch.uint8, device="cuda")
-    y = torch.empty((dc4.n, dc4.h), dtype=torch.bfloat16, device="cuda")
-    ms, st, _ = time_steps(torch, lambda: mega_call(mm, dc4, x, ids, gate, W4, S4, ws, y), steps, 3, dist)
-    t = ms / steps / 1e3
-    touched = int(torch.unique(ids).numel())
-    wbytes = (touched + dc4.shared) * 3 * dc4.h * dc4.inter * (0.5 + 1 / 32)
-    a8w4["decode"] = {"tokens_per_s": dc4.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
-                      "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9,
-                      "hbm_frac": wbytes / t / 1e9 / hbm_peak,
-                      "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
-    out["a8w4"] = a8w4
-    del x, ws, W4, S4
+    W4 = None
+    S4 = None
+    for key, dfmt in (("a8w4", mm.DT_FP8_E4M3FN), ("a4w4", mm.DT_FP4_E2M1)):
+        res = {}
+        pc = pc4.scaled(dispatch_fmt=dfmt)
+        x, ids, gate, W4g, _ = gpu_inputs(pc, mm, torch, seed_offset=30 + dist.rank, weights=W4)
+        W4 = W4g if W4 is None else W4
+        ws = torch.empty(mm.mm_mega_moe_workspace_size(pc.n, pc.h, pc.k, pc.e, pc.inter, pc.shared, 1),
+                         dtype=torch.uint8, device="cuda")
+        y = torch.empty((pc.n, pc.h), dtype=torch.bfloat16, device="cuda")
+        ms, st, _ = time_steps(torch, lambda: mega_call(mm, pc, x, ids, gate, W4, None, ws, y), steps, 3, dist)
+        t = ms / steps / 1e3
+        res["prefill"] = {"workload": f"{pc.name} N={pc.n} H={pc.h} I={pc.inter} E={pc.e} K={pc.k}",
+                          "tokens_per_s": pc.n / t, "ms_per_step": t * 1e3, "tflops": ffn_flops(pc) / t / 1e12,
+                          "tflops_frac": ffn_flops(pc) / t / 1e12 / fp8_peak,
+                          "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+        del x, ws
+        dcf = dc.scaled(weight_fmt=mm.DT_FP4_E2M1, dispatch_fmt=dfmt)
+        x, ids, gate, _, S4g = gpu_inputs(dcf, mm, torch, seed_offset=40 + dist.rank, weights=W4, shared=S4)
+        S4 = S4g if S4 is None else S4
+        ws = torch.empty(mm.mm_mega_moe_workspace_size(dcf.n, dcf.h, dcf.k, dcf.e, dcf.inter, dcf.shared, 1),
+                         dtype=torch.uint8, device="cuda")
+        y = torch.empty((dcf.n, dcf.h), dtype=torch.bfloat16, device="cuda")
+        ms, st, _ = time_steps(torch, lambda: mega_call(mm, dcf, x, ids, gate, W4, S4, ws, y), steps, 3, dist)
+        t = ms / steps / 1e3
+        touched = int(torch.unique(ids).numel())
+        wbytes = (touched + dcf.shared) * 3 * dcf.h * dcf.inter * (0.5 + 1 / 32)
+        res["decode"] = {"tokens_per_s": dcf.n / t, "ms_per_step": t * 1e3, "experts_touched": touched,
+                         "weight_bytes": wbytes, "weight_gbs": wbytes / t / 1e9,
+                         "hbm_frac": wbytes / t / 1e9 / hbm_peak,
+                         "stage_ms_per_step": {k: v[0] / steps for k, v in st.items() if v[1]}}
+        out[key] = res
+        del x, ws
+    del W4, S4
     return out
 
 

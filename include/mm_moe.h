@@ -176,7 +176,7 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
                                int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
- * mm_mega_moe -- MegaMoE, A8W8-FP scenario, epWorldSize = 1:
+ * mm_mega_moe -- MegaMoE, A8W8-FP / A8W4-FP / A4W4-FP scenarios, epWorldSize = 1:
  *
  *   X_hat_e, S_X,e = Q_MX(x[T_e])                                 stage 1
  *   G_e = DQ(X_hat_e) DQ(W1_e^(G))^T, U_e = DQ(X_hat_e) DQ(W1_e^(U))^T
@@ -185,7 +185,8 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *   Y[i] = sum_k W[i,k] O[pi(i,k)] + sum_s O_s^shared[i]          stage 4
  *
  * x                  [bs, h] bf16 (dispatch_quant_mode 4), or FP8 codes of
- *                    dispatch_quant_out_dtype (dispatch_quant_mode 0).
+ *                    dispatch_quant_out_dtype (dispatch_quant_mode 0; packed
+ *                    FP4 [bs, h/2] when that type is 296).
  * x_scales           dispatch_quant_mode 0: E8M0 scales of x, [bs, h/32]
  *                    (the pages' scales input, (BS, CeilDiv(H, 32))); NULL
  *                    otherwise.
@@ -209,7 +210,13 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  * dispatch_quant_mode 4 (MX quantisation inside the operator) or 0
  *                    (pre-quantised pass-through: x and x_scales are X_hat, S_X);
  * dispatch_quant_out_dtype 23 / 24 is also the type of A_hat (FP8 with either
- *                    weight type: A8W8-FP, A8W4-FP).
+ *                    weight type: A8W8-FP, A8W4-FP).  296 (FLOAT4_E2M1) is
+ *                    the A4W4-FP scenario ("A4W4-FP quantization scenario"):
+ *                    the routed weights must be FP4 too (else
+ *                    MM_ERR_UNSUPPORTED); X_hat is packed MXFP4, GEMM1 multiplies
+ *                    FP4 by FP4, and A_hat is re-quantised to MXFP8 E4M3, so
+ *                    GEMM2 is A8W4.  Shared experts see the same FP4 X_hat
+ *                    whatever their own weight type.
  * combine_quant_mode must be 0.
  * activation         "swiglu" (or NULL), "swiglustep", "swigluoai", "situglu" or
  *                    "gelu", with activation_params as the README's parameter
@@ -217,7 +224,7 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    swigluoai [] or [clamp, alpha, beta] (defaults: clamp off,
  *                    alpha 1.702, beta 1.0); situglu [], [beta] or [beta,
  *                    linear_beta] (beta 1.0 when empty); gelu [FLT_MAX] only.
- *                    A clamp of 0 or FLT_MAX is "not enabled".  Formulas:
+ *                    A clamp of 0 or FLT_MAX means no clamp.  Formulas:
  *                    "Activation function formulas".  Under gelu the whole
  *                    2*intermediate-wide Linear1 output is activated, so
  *                    weight2 is [E, h, 2*intermediate] (scales likewise) and
@@ -236,8 +243,9 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    (2I under gelu); NULL to skip.
  * dispatch_q, dispatch_scale  optional diagnostic outputs of the dispatched
  *                    X_hat (stage 1) in expert-sorted row order: [bs*k, h]
- *                    FP8 codes of dispatch_quant_out_dtype and [bs*k, h/32]
- *                    E8M0; NULL to skip (both or neither).
+ *                    FP8 codes of dispatch_quant_out_dtype ([bs*k, h/2] packed
+ *                    FP4 under A4W4-FP) and [bs*k, h/32] E8M0; NULL to skip
+ *                    (both or neither).
  * Shape limits: h and intermediate multiples of 128; k <= 32;
  * moe_expert_num <= 2048.
  * ---------------------------------------------------------------------- */
@@ -314,10 +322,10 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
 
 /* ------------------------------------------------------------------------
  * Expert parallelism: dispatch to ranks and combine (MegaMoE README, A8W8-FP
- * scenario stage 1 "dispatch the quantised tokens to the ranks holding
- * their experts" and stage 4 "GMM2 rows written back to the source rank,
- * weighted and summed", with epWorldSize > 1; parameter table
- * epWorldSize / moeExpertNum).  Rank r holds experts [r*E/W, (r+1)*E/W).
+ * scenario stage 1, where the quantised tokens travel to the ranks that hold
+ * their experts, and stage 4, where the GMM2 rows go back to their source
+ * rank to be weighted and summed, with epWorldSize > 1; parameter table
+ * epWorldSize / moeExpertNum; the A4W4-FP scenario sends MXFP4 rows).  Rank r holds experts [r*E/W, (r+1)*E/W).
  * The exchange between ranks is the caller's collective (an all-to-all with
  * the counts below as split sizes); each rank runs mm_moe_expert_ffn on the
  * rows it receives (its local experts) and sends the resulting rows back in
@@ -326,12 +334,13 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  * mm_moe_ep_dispatch -- on the source rank: the flattened ids j = i*K + k
  *   are sorted by destination rank id / (E/W), stably (rows of one rank in
  *   ascending j); every token is MX-quantised once (group 32, E8M0 shared
- *   exponent, dispatch_quant_out_dtype 23 / 24) and its row stored at its K
- *   positions.
+ *   exponent, dispatch_quant_out_dtype 23 / 24, or 296 for packed FP4 E2M1)
+ *   and its row stored at its K positions.
  * x                 [num_rows, h] bf16 / fp16 (x_dtype), h a multiple of 128.
  * topk_ids          [num_rows, k] int32 in [0, moe_expert_num); k <= 32.
  * moe_expert_num    E, a multiple of ep_world_size W.
- * send_x            [num_rows*k, h] FP8 codes, rank-sorted (output).
+ * send_x            [num_rows*k, h] FP8 codes ([num_rows*k, h/2] packed FP4),
+ *                   rank-sorted (output).
  * send_scales       [num_rows*k, h/32] E8M0 (output).
  * send_expert       [num_rows*k] int32: the row's expert on its destination
  *                   rank, id % (E/W) (output).
@@ -369,8 +378,10 @@ mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const 
  * source ranks).  The same arithmetic as mm_mega_moe with top-K 1, gating
  * weight 1, pass-through quantisation and no shared experts, bit for bit,
  * without its combine pass.
- * x                 [rows, h] FP8 codes of x_dtype (23 | 24); x_scales
- *                   [rows, h/32] E8M0 (required when rows > 0).
+ * x                 [rows, h] FP8 codes of x_dtype (23 | 24), or [rows, h/2]
+ *                   packed FP4 codes (x_dtype 296, A4W4-FP: FP4 weights
+ *                   required); x_scales [rows, h/32] E8M0 (required when
+ *                   rows > 0).
  * expert_ids        [rows] int32 local expert ids in [0, local_experts); an
  *                   id outside the range leaves its row of out unwritten and
  *                   raises MM_DEVERR_EXPERT_RANGE.

@@ -131,7 +131,10 @@ def test_mega_moe_host_rejections(lib):
     assert _mega(lib, dqm=3) == 2                    # other dispatch quant modes
     assert _mega(lib, act=b"relu") == 2              # unknown activation
     assert _mega(lib, act=b"gelu") == 1              # gelu needs its [FLT_MAX] placeholder
-    assert _mega(lib, dqd=296) == 2                  # FP4 dispatch (A4W4-FP)
+    assert _mega(lib, dqd=296) == 2                  # FP4 dispatch (A4W4-FP) needs FP4 routed weights
+    assert _mega(lib, dqd=296, wdt=296) == 3         # A4W4-FP passes the checks (stops at the workspace)
+    assert _mega(lib, dqd=296, wdt=296, s=1, sw1=1, sw2=1, ss1=1, ss2=1, swdt=24) == 3  # FP8 shared experts
+    assert _mega(lib, dqd=1) == 2                    # INT8 dispatch (not an MX scenario)
     assert _mega(lib, gdt=27 + 1) == 1               # gating weight dtype
     assert _mega(lib, maxrecv=100) == 1              # below bs*k rows
     assert _mega(lib, ws=None, wsb=0) == 3           # workspace missing
