@@ -423,6 +423,9 @@ int orc_act_code(int x_code) { return x_code == ORC_E2M1 ? ORC_E4M3 : x_code; }
  * Gating weights are fp32 (gate_is_bf16 = 0) or bf16 (1), widened exactly.
  * Optionally also returns the activation codes of every (token, k) pair:
  * aq_out [n_tok, K, I], as_out [n_tok, K, I/32] (format orc_act_code(x_code)).
+ * Shared experts quantise their input in shared_x_code (the parameter
+ * table's shared-expert quantisation type; < 0: the dispatch type), with
+ * their activation in orc_act_code(shared_x_code).
  * ------------------------------------------------------------------------- */
 void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate, int gate_is_bf16,
                          const uint8_t* w1, const uint8_t* s1, const uint8_t* w2, const uint8_t* s2,
@@ -431,17 +434,21 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
                          int64_t num_experts, int64_t inter, int x_code, int w_code,
                          int shared_w_code, const int64_t* tokens, int64_t n_tok, double* y,
                          uint16_t* y_bf16, uint8_t* aq_out, uint8_t* as_out, const uint8_t* xq_in,
-                         const uint8_t* xs_in, int act, const double* act_p) {
+                         const uint8_t* xs_in, int act, const double* act_p, int shared_x_code) {
   int64_t aw = act_width(act, inter);
   int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((aw + 63) / 64);
   int64_t w1_sz = 2 * inter * h, w2_sz = h * aw;
   int64_t i_groups = (aw + 31) / 32;
   int a_code = orc_act_code(x_code);
+  int sx_code = shared_x_code < 0 ? x_code : shared_x_code;
+  int sa_code = orc_act_code(sx_code);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t t = 0; t < n_tok; ++t) {
     int64_t i = tokens[t];
     uint8_t* xq = (uint8_t*)malloc((size_t)h);
     uint8_t* xs = (uint8_t*)malloc((size_t)((h + 31) / 32));
+    uint8_t* sxq = (uint8_t*)malloc((size_t)h);
+    uint8_t* sxs = (uint8_t*)malloc((size_t)((h + 31) / 32));
     uint8_t* aq = (uint8_t*)malloc((size_t)aw);
     uint8_t* as = (uint8_t*)malloc((size_t)i_groups);
     double* o = (double*)malloc(sizeof(double) * (size_t)h);
@@ -464,13 +471,21 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
       if (as_out) memcpy(as_out + (t * k + kk) * i_groups, as, (size_t)i_groups);
       for (int64_t c = 0; c < h; ++c) acc[c] += w * o[c];
     }
+    if (n_shared > 0) {
+      if (sx_code == x_code) {
+        memcpy(sxq, xq, (size_t)h);
+        memcpy(sxs, xs, (size_t)((h + 31) / 32));
+      } else {
+        orc_mx_quantize_src(x + i * h, 27, 1, h, sx_code, sxq, sxs, (h + 31) / 32);
+      }
+    }
     for (int64_t s = 0; s < n_shared; ++s) {
-      orc_expert_row(xq, xs, x_code, sw1 + s * w1_sz, ss1 + s * 2 * inter * s1_cols,
-                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, a_code, act, act_p,
+      orc_expert_row(sxq, sxs, sx_code, sw1 + s * w1_sz, ss1 + s * 2 * inter * s1_cols,
+                     sw2 + s * w2_sz, ss2 + s * h * s2_cols, shared_w_code, h, inter, sa_code, act, act_p,
                      aq, as, o);
       for (int64_t c = 0; c < h; ++c) acc[c] += o[c];
     }
     for (int64_t c = 0; c < h; ++c) y_bf16[t * h + c] = orc_bf16_round(acc[c]);
-    free(xq); free(xs); free(aq); free(as); free(o);
+    free(xq); free(xs); free(sxq); free(sxs); free(aq); free(as); free(o);
   }
 }

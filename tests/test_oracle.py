@@ -250,14 +250,16 @@ def test_permute_matches_gather(fmt):
 
 
 # ---------------------------------------------------------------- expert FFN
-def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
+def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None, shared_xfmt=None):
     """Grouped-by-expert FFN with numpy matmuls on dequantised operands, from
     the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort.  The
     activation is re-quantised in the dispatch type, except in the A4W4-FP
-    scenario (FP4 E2M1 dispatch), whose stage 2 re-quantises it to MXFP8 E4M3."""
+    scenario (FP4 E2M1 dispatch), whose stage 2 re-quantises it to MXFP8 E4M3.
+    Shared experts quantise their input in shared_xfmt when given (the
+    parameter table's sharedExpertQuantOutDtype), with the same rule for
+    their activation."""
     (w1, s1, w2, s2) = w
     fx = cfg.dispatch_fmt
-    fa = P.E4M3 if fx == P.E2M1 else fx
     xq, xs = P.brute_mx_rows(P.bf16_bits_to_f64(x), fx)
     n, h = x.shape
     k = ids.shape[1]
@@ -269,7 +271,8 @@ def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
     o_all = np.zeros((order.size, h))
     aq_all = np.zeros((order.size, inter), dtype=np.uint8)
 
-    def ffn(rows_q, rows_s, W1, S1, W2, S2, wfmt):
+    def ffn(rows_q, rows_s, W1, S1, W2, S2, wfmt, fx=fx):
+        fa = P.E4M3 if fx == P.E2M1 else fx
         xd = P.dequant_rows(rows_q, rows_s, fx)
         w1d = P.dequant_rows(W1, S1, wfmt)
         hv = xd @ w1d.T
@@ -292,9 +295,11 @@ def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None):
     for kk in range(k):
         y += gw[:, kk:kk + 1] * o_all[pos.reshape(n, k)[:, kk]]
     if shared is not None:
+        sfx = fx if shared_xfmt is None else shared_xfmt
+        sq, ss = (xq, xs) if sfx == fx else P.brute_mx_rows(P.bf16_bits_to_f64(x), sfx)
         for s in range(shared[0].shape[0]):
-            _, o = ffn(xq, xs, shared[0][s], shared[1][s], shared[2][s], shared[3][s],
-                       cfg.weight_fmt if shared_fmt is None else shared_fmt)
+            _, o = ffn(sq, ss, shared[0][s], shared[1][s], shared[2][s], shared[3][s],
+                       cfg.weight_fmt if shared_fmt is None else shared_fmt, fx=sfx)
             y += o
     return y, aq_all[pos.reshape(n, k)]
 
@@ -474,6 +479,29 @@ def test_gelu_matches_tanh_form():
     assert np.array_equal(a_s, ws[0])
     assert np.abs(_code_steps(aq, wq[0], cfg.dispatch_fmt)).max() <= 1
     assert abs(0.5 * (1 + np.tanh(np.sqrt(2 / np.pi) * 1.044715)) - 0.8411919906) < 1e-9
+
+
+@pytest.mark.parametrize("routed,dispatch,shared_w,shared_x", [
+    (P.E2M1, P.E2M1, P.E4M3, P.E4M3),    # A4W4-FP routed experts, A8W8-FP shared experts
+    (P.E4M3, P.E4M3, P.E2M1, P.E2M1),    # A8W8-FP routed, A4W4-FP shared
+    (P.E5M2, P.E5M2, P.E4M3, P.E4M3),    # E5M2 routed, E4M3 shared (activations differ too)
+    (P.E2M1, P.E4M3, P.E2M1, P.E2M1),    # A8W4-FP routed, A4W4-FP shared
+])
+def test_mega_moe_shared_quant_type_matches_numpy(routed, dispatch, shared_w, shared_x):
+    """Shared experts with their own input quantisation type (the MegaMoE
+    parameter table's sharedExpertQuantOutDtype) and weight type."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, shared=2, weight_fmt=routed, dispatch_fmt=dispatch)
+    x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
+    w = _weights(cfg)
+    sh = _weights(cfg.scaled(weight_fmt=shared_w), shared=True)
+    y, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
+                                  shared_w_fmt=shared_w, shared_x_fmt=shared_x)
+    y_ref, _ = _numpy_grouped_moe(cfg, x, ids, gate, w, shared=sh, shared_fmt=shared_w, shared_xfmt=shared_x)
+    assert np.max(np.abs(y - y_ref)) <= 1e-11 * np.abs(y_ref).max()
+    # the shared experts' type matters: the routed type instead gives another Y
+    y_same, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
+                                       shared_w_fmt=shared_w)
+    assert np.max(np.abs(y_same - y_ref)) > 1e-6 * np.abs(y_ref).max()
 
 
 @pytest.mark.parametrize("kw", [{}, dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1)])
