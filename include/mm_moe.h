@@ -215,8 +215,14 @@ mm_status mm_moe_token_permute(const void* tokens, int tokens_dtype, const void*
  *                    the routed weights must be FP4 too (else
  *                    MM_ERR_UNSUPPORTED); X_hat is packed MXFP4, GEMM1 multiplies
  *                    FP4 by FP4, and A_hat is re-quantised to MXFP8 E4M3, so
- *                    GEMM2 is A8W4.  Shared experts see the same FP4 X_hat
- *                    whatever their own weight type.
+ *                    GEMM2 is A8W4.
+ * shared_quant_out_dtype  the shared experts' own input quantisation type (the
+ *                    parameter table's sharedExpertQuantOutDtype): 0 for the
+ *                    dispatch type, or 23 / 24 / 296 (any shared weight type;
+ *                    with 296 their A_hat is E4M3, as in A4W4-FP).  The
+ *                    shared rows are quantised in a pass of their own; with
+ *                    dispatch_quant_mode 0 only 0 or the dispatch type is
+ *                    accepted (MM_ERR_INVALID_ARG otherwise).
  * combine_quant_mode must be 0.
  * activation         "swiglu" (or NULL), "swiglustep", "swigluoai", "situglu" or
  *                    "gelu", with activation_params as the README's parameter
@@ -261,8 +267,8 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
                       int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
                       int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
                       int64_t max_recv_token_num, int64_t dispatch_quant_mode,
-                      int64_t dispatch_quant_out_dtype, int64_t combine_quant_mode,
-                      const char* activation, const float* activation_params,
+                      int64_t dispatch_quant_out_dtype, int64_t shared_quant_out_dtype,
+                      int64_t combine_quant_mode, const char* activation, const float* activation_params,
                       int64_t n_activation_params, void* y, int32_t* expert_token_nums,
                       int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale,
                       uint8_t* dispatch_q, uint8_t* dispatch_scale,

@@ -79,7 +79,7 @@ def load():
     L.mm_moe_token_permute.argtypes = [p, i32, p, i32, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, sz, p, p]
     L.mm_mega_moe_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i32, psz]
     L.mm_mega_moe.argtypes = ([p, p, p, p, i32, p, p, p, p, i32, i32, p, p, p, p, i32, i64, i64, i64, i64, i64, i64,
-                               i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, p, p, sz, p,
+                               i64, i64, i64, i64, i64, i64, ctypes.c_char_p, p, i64, p, p, p, p, p, p, p, p, sz, p,
                                p])
     L.mm_prepared_weight_scales_size.argtypes = [i32, i64, i64, i64, psz]
     L.mm_prepare_weight_scales.argtypes = [p, i32, i64, i64, i64, p, p]
@@ -249,6 +249,7 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 shared_weight1=None, shared_weight2=None, shared_weight_scales1=None, shared_weight_scales2=None,
                 shared_weight_dtype: int | None = None, ep_world_size: int = 1, max_recv_token_num: int = 0,
                 dispatch_quant_mode: int = 4, dispatch_quant_out_dtype: int = DT_FP8_E4M3FN,
+                shared_expert_quant_out_dtype: int | None = None,
                 combine_quant_mode: int = 0, activation: str = "swiglu", activation_params=(),
                 x_scales=None, out=None, workspace=None, dev_err=None, want_expanded_row_idx=False,
                 want_act=False, want_dispatch=False):
@@ -267,7 +268,8 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     E8M0 scales [BS, H/32] (pre-quantised pass-through).
     A4W4-FP: dispatch_quant_out_dtype=DT_FP4_E2M1 with FP4 weights; the dispatched
     X_hat is packed FP4 ([BS*K, H/2] when returned; x [BS, H/2] in pass-through) and
-    A_hat is MXFP8 E4M3.
+    A_hat is MXFP8 E4M3.  shared_expert_quant_out_dtype: the shared experts' own input
+    type (sharedExpertQuantOutDtype; None: the dispatch type).
     """
     _need_dtype(x, (torch.bfloat16,) if dispatch_quant_mode != 0 else _BYTE_DTYPES, "x")
     _need_dtype(topk_ids, (torch.int32,), "topk_ids")
@@ -311,7 +313,8 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
         _ptr(weight_scales2), wdt, weight_scale_layout, _ptr(shared_weight1), _ptr(shared_weight2),
         _ptr(shared_weight_scales1), _ptr(shared_weight_scales2), swdt, s_num, bs, h, k, moe_expert_num,
         ep_world_size, inter, max_recv_token_num, dispatch_quant_mode, dispatch_quant_out_dtype,
-        combine_quant_mode, activation.encode() if activation else None, parr, len(params), _ptr(y), _ptr(counts),
+        shared_expert_quant_out_dtype or 0, combine_quant_mode, activation.encode() if activation else None, parr,
+        len(params), _ptr(y), _ptr(counts),
         _ptr(exp_idx), _ptr(act_q), _ptr(act_s), _ptr(dsp_q), _ptr(dsp_s), _ptr(ws), ws.numel(), _dev_err(dev_err),
         _stream(dev)),
         "mm_mega_moe")

@@ -480,11 +480,11 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
                       int shared_weight_dtype, int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
                       int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
                       int64_t max_recv_token_num, int64_t dispatch_quant_mode, int64_t dispatch_quant_out_dtype,
-                      int64_t combine_quant_mode, const char* activation, const float* activation_params,
-                      int64_t n_activation_params, void* y, int32_t* expert_token_nums,
-                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, uint8_t* dispatch_q,
-                      uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                      void* stream) {
+                      int64_t shared_quant_out_dtype, int64_t combine_quant_mode, const char* activation,
+                      const float* activation_params, int64_t n_activation_params, void* y,
+                      int32_t* expert_token_nums, int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale,
+                      uint8_t* dispatch_q, uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_err, void* stream) {
   size_t need = 0;
   mm_status s = mm_mega_moe_workspace_size(bs, h, k, moe_expert_num, intermediate, shared_expert_num,
                                            weight_scale_layout, &need);
@@ -500,6 +500,17 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   const bool a4w4 = dispatch_quant_out_dtype == MM_DT_FP4_E2M1;
   if (a4w4 && weight_dtype != MM_DT_FP4_E2M1) return MM_ERR_UNSUPPORTED;
   const int act_fmt = a4w4 ? MM_DT_FP8_E4M3FN : (int)dispatch_quant_out_dtype;
+  // the shared experts' own input type (the parameter table's
+  // sharedExpertQuantOutDtype; 0: the dispatch type), with the same rules
+  if (shared_quant_out_dtype != 0 && !is_mx_weight(shared_quant_out_dtype)) return MM_ERR_UNSUPPORTED;
+  const int sx_fmt = shared_expert_num > 0 && shared_quant_out_dtype != 0 ? (int)shared_quant_out_dtype
+                                                                          : (int)dispatch_quant_out_dtype;
+  if (dispatch_quant_mode == 0 && sx_fmt != dispatch_quant_out_dtype) return MM_ERR_INVALID_ARG;
+  const int act_fmt_sh = sx_fmt == MM_DT_FP4_E2M1 ? MM_DT_FP8_E4M3FN : sx_fmt;
+  // X_hat rows: FP8 (h bytes) or packed FP4 (h / 2); an FP8 stride for both
+  // when routed and shared rows differ in width
+  const int64_t xw = a4w4 ? h / 2 : h;
+  const int64_t xstride = (sx_fmt == MM_DT_FP4_E2M1) == a4w4 ? xw : h;
   if (shared_expert_num > 0 && !is_mx_weight(shared_weight_dtype)) return MM_ERR_UNSUPPORTED;
   if (bs > 0 && (dispatch_quant_mode == 0) != (x_scales != nullptr)) return MM_ERR_INVALID_ARG;
   ActSpec act;
@@ -590,13 +601,26 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   pa.extra_base = w.seg_mprefix + d.e;
   pa.out_fmt = (int)dispatch_quant_out_dtype;
   pa.out = w.xq;
+  pa.out_stride = xstride;
   pa.scales = w.xsf;
   pa.scale_cols = 0;
   pa.dev_err = dev_err;
   pa.dest_inv = rows_out ? w.pad_inv : nullptr;
+  const bool split = sx_fmt != dispatch_quant_out_dtype;  // the shared rows in their own type
+  if (split) pa.n_extra = 0;
   StageScope sd(MM_STAGE_DISPATCH, st);
   e = launch_permute(pa, st);
-  sd.finish(1);
+  if (e == cudaSuccess && split) {
+    PermuteArgs ps = pa;
+    ps.k = 0;
+    ps.dest = nullptr;
+    ps.ids = nullptr;
+    ps.dest_inv = nullptr;
+    ps.n_extra = (int)d.s;
+    ps.out_fmt = sx_fmt;
+    e = launch_permute(ps, st);
+  }
+  sd.finish(split ? 2 : 1);
   if (e != cudaSuccess) return MM_ERR_CUDA;
 
   // 3. GEMM1 + swiglu + MX requantisation
@@ -616,7 +640,10 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   g1.K = d.h;
   g1.N = 2 * d.inter;
   g1.a_fmt = (int)dispatch_quant_out_dtype;
+  g1.a_fmt_sh = sx_fmt;
+  g1.a_stride = xstride;
   g1.act_fmt = act_fmt;
+  g1.act_fmt_sh = act_fmt_sh;
   g1.b_fmt = weight_dtype;
   g1.b_fmt_sh = shared_weight_dtype;
   g1.inter = (int)d.inter;
@@ -638,6 +665,8 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   g2.mode = 2;
   g2.a = w.aq;
   g2.a_fmt = act_fmt;
+  g2.a_fmt_sh = act_fmt_sh;
+  g2.a_stride = 0;
   g2.sfa = w.asf;
   g2.b = weight2;
   g2.sfb = wsf2;
@@ -680,14 +709,15 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
 
   // optional diagnostic copies of X_hat and A_hat in expert-sorted order
   if (dispatch_q) {
-    UnpadArgs ua;
+    UnpadArgs ua = {};
     ua.src_q = w.xq;
     ua.src_sf = w.xsf;
     ua.pad_row = w.pad_row;
     ua.expanded_row_idx = o.expanded_row_idx;
     ua.rows = d.rows;
     ua.cols = d.h;
-    ua.qbytes = a4w4 ? d.h / 2 : d.h;
+    ua.qbytes = xw;
+    ua.src_stride = xstride;
     ua.dst_q = dispatch_q;
     ua.dst_sf = dispatch_scale;
     ua.rows_cap = d.rows_cap;
@@ -698,7 +728,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
     if (e != cudaSuccess) return MM_ERR_CUDA;
   }
   if (act_q) {
-    UnpadArgs ua;
+    UnpadArgs ua = {};
     ua.src_q = w.aq;
     ua.src_sf = w.asf;
     ua.pad_row = w.pad_row;
@@ -726,16 +756,17 @@ mm_status mm_mega_moe(const void* x, const uint8_t* x_scales, const int32_t* top
                       int shared_weight_dtype, int64_t shared_expert_num, int64_t bs, int64_t h, int64_t k,
                       int64_t moe_expert_num, int64_t ep_world_size, int64_t intermediate,
                       int64_t max_recv_token_num, int64_t dispatch_quant_mode, int64_t dispatch_quant_out_dtype,
-                      int64_t combine_quant_mode, const char* activation, const float* activation_params,
-                      int64_t n_activation_params, void* y, int32_t* expert_token_nums,
-                      int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale, uint8_t* dispatch_q,
-                      uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                      void* stream) {
+                      int64_t shared_quant_out_dtype, int64_t combine_quant_mode, const char* activation,
+                      const float* activation_params, int64_t n_activation_params, void* y,
+                      int32_t* expert_token_nums, int32_t* expanded_row_idx, uint8_t* act_q, uint8_t* act_scale,
+                      uint8_t* dispatch_q, uint8_t* dispatch_scale, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_err, void* stream) {
   return mega_moe_impl(false, x, x_scales, topk_ids, topk_weights, topk_weights_dtype, weight1, weight2,
                        weight_scales1, weight_scales2, weight_dtype, weight_scale_layout, shared_weight1,
                        shared_weight2, shared_weight_scales1, shared_weight_scales2, shared_weight_dtype,
                        shared_expert_num, bs, h, k, moe_expert_num, ep_world_size, intermediate, max_recv_token_num,
-                       dispatch_quant_mode, dispatch_quant_out_dtype, combine_quant_mode, activation,
+                       dispatch_quant_mode, dispatch_quant_out_dtype, shared_quant_out_dtype, combine_quant_mode,
+                       activation,
                        activation_params, n_activation_params, y, expert_token_nums, expanded_row_idx, act_q,
                        act_scale, dispatch_q, dispatch_scale, workspace, workspace_bytes, dev_err, stream);
 }
@@ -758,7 +789,7 @@ mm_status mm_moe_expert_ffn(const uint8_t* x, const uint8_t* x_scales, int x_dty
                             int32_t* dev_err, void* stream) {
   return mega_moe_impl(true, x, x_scales, expert_ids, nullptr, 0,
                        weight1, weight2, weight_scales1, weight_scales2, weight_dtype, weight_scale_layout, nullptr,
-                       nullptr, nullptr, nullptr, 0, 0, rows, h, 1, local_experts, 1, intermediate, 0, 0, x_dtype, 0,
+                       nullptr, nullptr, nullptr, 0, 0, rows, h, 1, local_experts, 1, intermediate, 0, 0, x_dtype, 0, 0,
                        activation, activation_params, n_activation_params, out, expert_token_nums, nullptr, nullptr,
                        nullptr, nullptr, nullptr, workspace, workspace_bytes, dev_err, stream);
 }

@@ -101,7 +101,7 @@ struct GemmArgs {
   int32_t* dev_err;
   int o_stage;    // stage output blocks (A_hat / O) in shared memory for TMA stores
   int b_fp4, b_fp4_sh;  // routed / shared weights are packed FP4 E2M1
-  int a_fp4;           // A is packed FP4 E2M1 (GEMM1 of A4W4-FP)
+  int a_fp4, a_fp4_sh;  // routed / shared rows of A are packed FP4 E2M1 (GEMM1 of A4W4-FP)
   // mode 1: activation (MM_ACT_*), its parameters, and the width of A_hat
   int act;
   float act_c, act_alpha, act_beta, act_rbeta, act_beta_lin, act_rbeta_lin, act_gelu_k;
@@ -230,10 +230,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
 // kBN: tile width (B rows per tile); kAcc: accumulator buffers in TMEM (2
 // lets the MMAs of the next tile run while the epilogue drains this one;
 // kBN * kAcc plus 16 scale columns per stage must fit the 512 columns).
-template <int kMode, int kActFmt, int kBN, int kAcc>
+// The 32 codes of one MX group in FP8 type kF (inv = 2^-scale) as two 16-byte vectors.
+template <int kF>
+__device__ __forceinline__ void q_pack32(const float* a, float inv, uint4& lo, uint4& hi) {
+  const uint2 p0 = pack8_fp8<kF>(a, inv), p1 = pack8_fp8<kF>(a + 8, inv);
+  const uint2 p2 = pack8_fp8<kF>(a + 16, inv), p3 = pack8_fp8<kF>(a + 24, inv);
+  lo = make_uint4(p0.x, p0.y, p1.x, p1.y);
+  hi = make_uint4(p2.x, p2.y, p3.x, p3.y);
+}
+
+// kAlt: the shared segments' A_hat takes the other FP8 type (a separate
+// instantiation, so the usual kernels carry no second quantiser)
+template <int kMode, int kActFmt, int kBN, int kAcc, bool kAlt = false>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmO, const GemmArgs g) {
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+              const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+              const __grid_constant__ CUtensorMap tmO, const GemmArgs g) {
+  constexpr int kAltFmt = kActFmt == MM_DT_FP8_E5M2 ? MM_DT_FP8_E4M3FN : MM_DT_FP8_E5M2;
   constexpr uint32_t kBBytes = kBN * kBK;
   constexpr uint32_t kStageTx = kABytes + kBBytes + 512 + 1024;
   constexpr uint32_t kAccCols = kBN * kAcc;
@@ -272,7 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
-    if (nseg > g.n_routed) prefetch_tensormap(&tmBs);
+    if (nseg > g.n_routed) {
+      prefetch_tensormap(&tmAs);
+      prefetch_tensormap(&tmBs);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
   pdl_wait();
@@ -352,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // packed FP4 operands count their global (packed) bytes
           mbar_arrive_expect_tx(&full[stage], kStageTx - ((sh ? g.b_fp4_sh : g.b_fp4) ? kBBytes / 2 : 0) -
-                                                  (g.a_fp4 ? kABytes / 2 : 0));
+                                                  ((sh ? g.a_fp4_sh : g.a_fp4) ? kABytes / 2 : 0));
           armed |= 1u << stage;
           arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-          tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], kb * kBK, am * kBM);
+          tma_load_2d(smA + stage * kABytes, sh ? &tmAs : &tmA, &full[stage], kb * kBK, am * kBM);
           if (kMode == 1 && !gelu1)
             tma_load_4d(smB + stage * kBBytes, mb, &full[stage], kb * kBK, ti.nt * 128, 0, e);
           else
@@ -475,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
         const int nout = gelu ? 4 : 2;  // 32-column output chunks of this thread
+        // A_hat of a shared segment in the shared experts' activation type when it differs
+        const bool alt = kAlt && ti.seg >= g.n_routed;
         const int ocol0 = gelu ? ti.nt * 256 + 128 * half : ti.nt * 128 + 64 * half;
         // TMA stores of the warp's 32 x 64 FP8 blocks when all its rows are real
         const bool staged = g.o_stage && g.seg_rows[ti.seg] - ti.mt * kBM >= (q + 1) * 32;
@@ -493,12 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(a[j]));
           float inv;
-          const uint32_t code = mx_scale(amax, fmt_emax<kActFmt>(), inv);
+          const uint32_t code = alt ? mx_scale(amax, fmt_emax<kAltFmt>(), inv) : mx_scale(amax, fmt_emax<kActFmt>(), inv);
           sfw |= code << (8 * i);
           if (staged || valid) {
-            const uint2 p0 = pack8_fp8<kActFmt>(a, inv), p1 = pack8_fp8<kActFmt>(a + 8, inv);
-            const uint2 p2 = pack8_fp8<kActFmt>(a + 16, inv), p3 = pack8_fp8<kActFmt>(a + 24, inv);
-            const uint4 lo = make_uint4(p0.x, p0.y, p1.x, p1.y), hi = make_uint4(p2.x, p2.y, p3.x, p3.y);
+            uint4 lo, hi;
+            if (alt)
+              q_pack32<kAltFmt>(a, inv, lo, hi);
+            else
+              q_pack32<kActFmt>(a, inv, lo, hi);
             if (staged) {
               const int sw = (lane >> 1) & 3;  // 64B swizzle of row `lane`
               *reinterpret_cast<uint4*>(stg + lane * 64 + (((2 * (i & 1)) ^ sw) << 4)) = lo;
@@ -605,9 +625,10 @@ EncodeTiledFn encode_fn() {
 // FP8 byte matrix [outer][inner] (inner contiguous), box inner 128 codes,
 // 128B swizzle; or packed FP4 E2M1 (inner / 2 bytes a row), expanded by TMA
 // like the FP4 weights below.
-bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer, bool fp4 = false) {
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer, bool fp4 = false,
+            uint64_t stride = 0) {
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {fp4 ? inner / 2 : inner};
+  cuuint64_t strides[1] = {stride ? stride : (fp4 ? inner / 2 : inner)};
   cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
   cuuint32_t es[2] = {1, 1};
   EncodeTiledFn f = encode_fn();
@@ -670,10 +691,10 @@ bool map_out(CUtensorMap* m, const void* ptr, bool bf16, uint64_t cols, uint64_t
 // instruction-descriptor format code (kind::mxf8f6f4): E4M3 0, E5M2 1, E2M1 5
 int fmt_code(int dt) { return dt == MM_DT_FP8_E5M2 ? 1 : (dt == MM_DT_FP4_E2M1 ? 5 : 0); }
 
-template <int kMode, int kActFmt, int kBN, int kAcc>
-cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbs,
-                const CUtensorMap& mo, GemmArgs g, int grid, cudaStream_t st) {
-  auto kern = k_gemm_mx<kMode, kActFmt, kBN, kAcc>;
+template <int kMode, int kActFmt, int kBN, int kAcc, bool kAlt = false>
+cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& mas, const CUtensorMap& mb,
+                const CUtensorMap& mbs, const CUtensorMap& mo, GemmArgs g, int grid, cudaStream_t st) {
+  auto kern = k_gemm_mx<kMode, kActFmt, kBN, kAcc, kAlt>;
   const size_t base = 1024 + (size_t)kStages * (kABytes + kBN * kBK + 512 + 1024) +
                       8 * (2 * kStages + 2 * kAcc + 1) + 16 + 12 * (size_t)(g.nseg + 1);
   constexpr size_t kMaxSmem = 232448;
@@ -683,7 +704,7 @@ cudaError_t run(const GemmLaunch& L, const CUtensorMap& ma, const CUtensorMap& m
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, ma, mb, mbs, mo, g);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, ma, mas, mb, mbs, mo, g);
 }
 
 }  // namespace
@@ -718,9 +739,16 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
     return pair_map ? map_4d_pair(m, p, (uint64_t)L.K, (uint64_t)L.inter, (uint64_t)experts, fp4)
                     : map_3d(m, p, (uint64_t)L.K, (uint64_t)L.N, (uint64_t)experts, (uint32_t)bn, fp4);
   };
-  CUtensorMap ma, mb, mbs;
-  if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM, L.a_fmt == MM_DT_FP4_E2M1))
+  CUtensorMap ma, mas, mb, mbs;
+  if (!map_2d(&ma, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM, L.a_fmt == MM_DT_FP4_E2M1, (uint64_t)L.a_stride))
     return cudaErrorInvalidValue;
+  if (L.n_shared > 0 && L.a_fmt_sh != L.a_fmt) {
+    if (!map_2d(&mas, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, kBM, L.a_fmt_sh == MM_DT_FP4_E2M1,
+                (uint64_t)L.a_stride))
+      return cudaErrorInvalidValue;
+  } else {
+    mas = ma;
+  }
   if (!map_b(&mb, L.b, L.n_routed, L.b_fmt)) return cudaErrorInvalidValue;
   if (L.n_shared > 0) {
     if (!map_b(&mbs, L.b_sh, L.n_shared, L.b_fmt_sh)) return cudaErrorInvalidValue;
@@ -749,6 +777,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.npairs = (int)prepared_npairs(L.N, L.mode);
   g.b_fp4 = L.b_fmt == MM_DT_FP4_E2M1;
   g.a_fp4 = L.a_fmt == MM_DT_FP4_E2M1;
+  g.a_fp4_sh = (L.n_shared > 0 ? L.a_fmt_sh : L.a_fmt) == MM_DT_FP4_E2M1;
+  const bool alt = L.mode == 1 && L.n_shared > 0 && L.act_fmt_sh != L.act_fmt;
   g.act = L.act;
   g.act_c = L.act_c;
   g.act_alpha = L.act_alpha;
@@ -760,7 +790,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   g.aw = L.mode == 1 ? (L.act == MM_ACT_GELU ? 2 * L.inter : L.inter) : 0;
   g.b_fp4_sh = (L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt) == MM_DT_FP4_E2M1;
   g.idesc = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.b_fmt), kBM, bn);
-  g.idesc_sh = idesc_mxf8(fmt_code(L.a_fmt), fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);
+  g.idesc_sh = idesc_mxf8(fmt_code(L.n_shared > 0 ? L.a_fmt_sh : L.a_fmt),
+                          fmt_code(L.n_shared > 0 ? L.b_fmt_sh : L.b_fmt), kBM, bn);
   g.inter = L.inter;
   g.act_q = L.act_q;
   g.act_sf = L.act_sf;
@@ -775,11 +806,15 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
   if (L.mode == 1) {  // the template argument is A_hat's type
-    if (L.act_fmt == MM_DT_FP8_E5M2) return run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
-    if (L.act_fmt != MM_DT_FP8_E4M3FN) return cudaErrorInvalidValue;
-    return run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
+    if (L.act_fmt != MM_DT_FP8_E5M2 && L.act_fmt != MM_DT_FP8_E4M3FN) return cudaErrorInvalidValue;
+    if (alt && L.act_fmt_sh != MM_DT_FP8_E5M2 && L.act_fmt_sh != MM_DT_FP8_E4M3FN) return cudaErrorInvalidValue;
+    if (L.act_fmt == MM_DT_FP8_E5M2)
+      return alt ? run<1, MM_DT_FP8_E5M2, 256, 1, true>(L, ma, mas, mb, mbs, mo, g, (int)grid, st)
+                 : run<1, MM_DT_FP8_E5M2, 256, 1>(L, ma, mas, mb, mbs, mo, g, (int)grid, st);
+    return alt ? run<1, MM_DT_FP8_E4M3FN, 256, 1, true>(L, ma, mas, mb, mbs, mo, g, (int)grid, st)
+               : run<1, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mas, mb, mbs, mo, g, (int)grid, st);
   }
-  return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mb, mbs, mo, g, (int)grid, st);
+  return run<2, MM_DT_FP8_E4M3FN, 256, 1>(L, ma, mas, mb, mbs, mo, g, (int)grid, st);
 }
 
 }  // namespace mm

@@ -82,6 +82,7 @@ struct PermuteArgs {
   const int32_t* extra_base;  // [n_extra] tile index of each extra segment (device)
   int out_fmt;              // -1 copy, 23 / 24 FP8
   void* out;                // [*, h] output rows
+  int64_t out_stride;       // bytes between output rows (0: the row's own size, h or h / 2 for packed FP4)
   uint8_t* scales;          // E8M0 output
   int64_t scale_cols;       // row layout: scale row stride; 0 = GEMM tile layout
   int32_t* dev_err;
@@ -113,7 +114,10 @@ struct GemmLaunch {
   const int32_t* seg_mprefix; // [n_routed + n_shared + 1]
   int64_t K, N;
   int a_fmt, b_fmt, b_fmt_sh; // 23 / 24, or 296 (packed FP4 E2M1)
+  int a_fmt_sh;               // A type of the shared segments (their own input quantisation)
+  int64_t a_stride;           // bytes between rows of a (0: K, or K / 2 for packed FP4)
   int act_fmt;                // mode 1: type of A_hat (23 / 24)
+  int act_fmt_sh;             // mode 1: type of the shared segments' A_hat
   int inter;                  // mode 1: I (= N / 2)
   int act;                    // mode 1: MM_ACT_* (A_hat width I, or 2I for gelu)
   float act_c, act_alpha, act_beta, act_beta_lin;  // clamp (+inf: off), swigluoai alpha / beta,
@@ -152,6 +156,7 @@ struct UnpadArgs {
   const int32_t* expanded_row_idx;  // [rows]
   int64_t rows, cols;         // cols: elements of a row (cols / 32 scale groups)
   int64_t qbytes;             // bytes of a row of codes: cols, or cols / 2 for packed FP4
+  int64_t src_stride;         // bytes between rows of src_q (0: qbytes)
   uint8_t* dst_q;             // [rows, qbytes]
   uint8_t* dst_sf;            // [rows, cols/32]
   int64_t rows_cap;           // rows of src_q (checked build)

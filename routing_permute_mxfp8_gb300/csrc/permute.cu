@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5
   uint8_t* out = static_cast<uint8_t*>(a.out);
   const int64_t groups = (a.h + 31) / 32;
   const int64_t groups4 = a.h / 128;
+  const int64_t ostride = a.out_stride ? a.out_stride : (kFmt == MM_DT_FP4_E2M1 ? a.h / 2 : a.h);
   // slice c0 = 512 columns (16 per lane); the next slice's loads are in
   // flight while this one is quantised and written to the K destinations
   const int64_t cbeg = (int64_t)part * span;
@@ -154,9 +155,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kSrc == MM_DT_FLOAT32 ? 5
       const int32_t d = dest_at(t, d0, d1);
       if (d < 0 || !act) continue;
       if (kFmt == MM_DT_FP4_E2M1)
-        *reinterpret_cast<uint2*>(out + (int64_t)d * (a.h / 2) + col / 2) = make_uint2(packed.x, packed.y);
+        *reinterpret_cast<uint2*>(out + (int64_t)d * ostride + col / 2) = make_uint2(packed.x, packed.y);
       else
-        *reinterpret_cast<uint4*>(out + (int64_t)d * a.h + col) = packed;
+        *reinterpret_cast<uint4*>(out + (int64_t)d * ostride + col) = packed;
       if (kTiled) {
         if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, g, groups4)) = word;
       } else if ((lane & 1) == 0) {
@@ -240,9 +241,10 @@ __global__ void k_unpad(UnpadArgs a) {
   if (j >= a.rows) return;
   const int32_t d = a.expanded_row_idx[j], p = a.pad_row[j];
   if (d < 0 || p < 0 || !in_bounds(d < a.rows && p < a.rows_cap, a.dev_err)) return;
+  const int64_t ss = a.src_stride ? a.src_stride : a.qbytes;
   for (int64_t c = lane * 16; c < a.qbytes; c += 512)
     *reinterpret_cast<uint4*>(a.dst_q + (int64_t)d * a.qbytes + c) =
-        *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * a.qbytes + c);
+        *reinterpret_cast<const uint4*>(a.src_q + (int64_t)p * ss + c);
   const int64_t groups = a.cols / 32;
   for (int64_t g = lane; g < groups; g += 32)
     a.dst_sf[(int64_t)d * groups + g] = a.src_sf[sf_tile_offset(p, g, a.cols / 128)];
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
   load_dests(a, row, lane, d0, d1, ndest);
   if (a.dest_inv && lane < a.k && d0 >= 0) a.dest_inv[d0] = (int32_t)(row * a.k + lane);
   const int64_t rb = a.out_fmt == MM_DT_FP4_E2M1 ? a.h / 2 : a.h;
+  const int64_t ostride = a.out_stride ? a.out_stride : rb;
   const uint8_t* src_row = static_cast<const uint8_t*>(a.src) + row * rb;
   const uint8_t* src_sf = a.src_scales + row * (a.h / 32);
   uint8_t* out = static_cast<uint8_t*>(a.out);
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
     const int32_t d = dest_at(t, d0, d1);
     if (d < 0) continue;  // uniform across the warp
     for (int64_t col = lane * 16; col < rb; col += 512)
-      *reinterpret_cast<uint4*>(out + (int64_t)d * rb + col) = *reinterpret_cast<const uint4*>(src_row + col);
+      *reinterpret_cast<uint4*>(out + (int64_t)d * ostride + col) = *reinterpret_cast<const uint4*>(src_row + col);
     for (int64_t w = lane; w < groups4; w += 32)
       *reinterpret_cast<uint32_t*>(a.scales + sf_tile_offset(d, 4 * w, groups4)) =
           *reinterpret_cast<const uint32_t*>(src_sf + 4 * w);

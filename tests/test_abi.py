@@ -88,7 +88,7 @@ def test_workspace_queries(lib):
 
 def _mega(lib, **kw):
     a = dict(x=1, xs=None, ids=1, w=1, gdt=0, w1=1, w2=1, s1=1, s2=1, wdt=24, layout=0, sw1=None, sw2=None, ss1=None,
-             ss2=None, swdt=24, s=0, bs=64, h=256, k=2, e=8, ep=1, inter=128, maxrecv=0, dqm=4, dqd=24, cqm=0,
+             ss2=None, swdt=24, s=0, bs=64, h=256, k=2, e=8, ep=1, inter=128, maxrecv=0, dqm=4, dqd=24, sqd=0, cqm=0,
              act=b"swiglu", params=None, nparams=0, y=1, counts=None, exp=None, aq=None, asc=None, dq=None, dsc=None,
              ws=None,
              wsb=0, err=None, stream=None)
@@ -97,7 +97,7 @@ def _mega(lib, **kw):
     return lib.mm_mega_moe(vp(a["x"]), vp(a["xs"]), vp(a["ids"]), vp(a["w"]), a["gdt"], vp(a["w1"]), vp(a["w2"]), vp(a["s1"]),
                            vp(a["s2"]), a["wdt"], a["layout"], vp(a["sw1"]), vp(a["sw2"]), vp(a["ss1"]),
                            vp(a["ss2"]), a["swdt"], a["s"], a["bs"], a["h"], a["k"], a["e"], a["ep"], a["inter"],
-                           a["maxrecv"], a["dqm"], a["dqd"], a["cqm"], a["act"], a["params"], a["nparams"],
+                           a["maxrecv"], a["dqm"], a["dqd"], a["sqd"], a["cqm"], a["act"], a["params"], a["nparams"],
                            vp(a["y"]), vp(a["counts"]), vp(a["exp"]), vp(a["aq"]), vp(a["asc"]), vp(a["dq"]),
                            vp(a["dsc"]), vp(a["ws"]),
                            a["wsb"], vp(a["err"]), a["stream"])
@@ -135,6 +135,12 @@ def test_mega_moe_host_rejections(lib):
     assert _mega(lib, dqd=296, wdt=296) == 3         # A4W4-FP passes the checks (stops at the workspace)
     assert _mega(lib, dqd=296, wdt=296, s=1, sw1=1, sw2=1, ss1=1, ss2=1, swdt=24) == 3  # FP8 shared experts
     assert _mega(lib, dqd=1) == 2                    # INT8 dispatch (not an MX scenario)
+    sh = dict(s=1, sw1=1, sw2=1, ss1=1, ss2=1)
+    assert _mega(lib, sqd=23, **sh) == 3             # shared experts in their own type: accepted
+    assert _mega(lib, sqd=296, swdt=24, **sh) == 3   # FP4 shared input, FP8 shared weights
+    assert _mega(lib, sqd=296, swdt=296, **sh) == 3
+    assert _mega(lib, sqd=1, **sh) == 2              # INT8
+    assert _mega(lib, sqd=23, dqm=0, xs=1, **sh) == 1  # pass-through: the shared experts take the dispatch type
     assert _mega(lib, gdt=27 + 1) == 1               # gating weight dtype
     assert _mega(lib, maxrecv=100) == 1              # below bs*k rows
     assert _mega(lib, ws=None, wsb=0) == 3           # workspace missing

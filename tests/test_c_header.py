@@ -33,7 +33,7 @@ int main(void) {
   /* ep_world_size 2 is rejected before anything is enqueued */
   if (mm_mega_moe((void*)16, NULL, (void*)16, (void*)16, MM_DT_FLOAT32, (void*)16, (void*)16, (void*)16,
                   (void*)16, MM_DT_FP8_E4M3FN, MM_WSCALE_ROWS, NULL, NULL, NULL, NULL, MM_DT_FP8_E4M3FN, 0,
-                  64, 256, 2, 8, 2, 128, 0, 4, MM_DT_FP8_E4M3FN, 0, "swiglu", NULL, 0, (void*)16, NULL, NULL,
+                  64, 256, 2, 8, 2, 128, 0, 4, MM_DT_FP8_E4M3FN, 0, 0, "swiglu", NULL, 0, (void*)16, NULL, NULL,
                   NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL) != MM_ERR_UNSUPPORTED)
     bad |= 64;
   printf("%d\n", bad);

@@ -221,7 +221,7 @@ def test_empty_batch_writes_zero_counts(ttype):
     assert np.array_equal(host(tok), np.zeros(e, np.int64))
     cnt = torch.full((e,), -7, dtype=torch.int32, device=DEV)
     st = L.mm_mega_moe(vp(dummy), None, vp(dummy), vp(dummy), 0, vp(dummy), vp(dummy), vp(dummy), vp(dummy), 24, 0,
-                       None, None, None, None, 24, 0, 0, 256, 2, e, 1, 128, 0, 4, 24, 0, b"swiglu", None, 0,
+                       None, None, None, None, 24, 0, 0, 256, 2, e, 1, 128, 0, 4, 24, 0, 0, b"swiglu", None, 0,
                        vp(dummy), vp(cnt), None, None, None, None, None, vp(dummy), 64, None, None)
     assert st == 0
     assert np.array_equal(host(cnt), np.zeros(e, np.int32))
@@ -532,6 +532,42 @@ def test_mega_moe_shared_weight_type_differs(routed_fmt, shared_fmt, dispatch):
     assert host(err)[0] == 0
     y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, routed_fmt, shared=sh,
                                       shared_w_fmt=shared_fmt)
+    check_y(synth.bf16_bits_to_f32(host(y).view(np.uint16)), y_ref)
+
+
+@pytest.mark.parametrize("routed,dispatch,shared_w,shared_x,act", [
+    (296, 296, 24, 24, "swiglu"),     # A4W4-FP routed experts, A8W8-FP E4M3 shared experts
+    (24, 24, 296, 296, "swiglu"),     # A8W8-FP routed, A4W4-FP shared
+    (23, 23, 24, 24, "swiglu"),       # E5M2 routed, E4M3 shared: A_hat types differ too
+    (24, 24, 24, 23, "gelu"),         # E4M3 routed, E5M2 shared, gelu
+    (296, 24, 296, 296, "swigluoai"),  # A8W4-FP routed, A4W4-FP shared
+])
+def test_mega_moe_shared_quant_type(routed, dispatch, shared_w, shared_x, act):
+    """Shared experts with their own input quantisation type (the MegaMoE
+    parameter table's sharedExpertQuantOutDtype): the routed rows' X_hat
+    bit-exact, routed A_hat codes within one step, Y against the oracle."""
+    params = (float(np.finfo(np.float32).max),) if act == "gelu" else ()
+    cfg = synth.CONFIGS["tiny"].scaled(n=160, h=512, inter=256, e=8, k=3, shared=2, routing="zipf",
+                                       weight_fmt=routed, dispatch_fmt=dispatch, activation=act, act_params=params)
+    x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
+    w1, s1, w2, s2 = _weights(cfg)
+    sh = _weights(cfg.scaled(weight_fmt=shared_w), shared=True)
+    err = zeros_err()
+    y, counts, exp_idx, aq, a_s, xq, xs = mm.mm_mega_moe(
+        bf16(x), t(ids), t(gate), gpu_codes(w1, routed), gpu_codes(w2, routed), t(s1), t(s2), cfg.e,
+        weight_dtype=routed, dispatch_quant_out_dtype=dispatch, shared_expert_quant_out_dtype=shared_x,
+        shared_weight1=gpu_codes(sh[0], shared_w), shared_weight_scales1=t(sh[1]),
+        shared_weight2=gpu_codes(sh[2], shared_w), shared_weight_scales2=t(sh[3]), shared_weight_dtype=shared_w,
+        activation=act, activation_params=params, dev_err=err, want_expanded_row_idx=True, want_act=True,
+        want_dispatch=True)
+    assert host(err)[0] == 0
+    r_srt, r_exp, r_cnt, _ = oracle.route(ids, cfg.e)
+    assert np.array_equal(host(counts), r_cnt.astype(np.int32))
+    check_dispatch(host(xq), host(xs), x, cfg, r_srt)
+    y_ref, _, aq_ref, as_ref = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, dispatch, routed, shared=sh,
+                                                      shared_w_fmt=shared_w, shared_x_fmt=shared_x, want_act=True,
+                                                      activation=act, act_params=params)
+    check_act(host(aq), host(a_s), r_exp, aq_ref, as_ref, np.arange(cfg.n), cfg.k)
     check_y(synth.bf16_bits_to_f32(host(y).view(np.uint16)), y_ref)
 
 
