@@ -55,6 +55,7 @@ def _load():
     L.orc_mx_quantize_rows.argtypes, L.orc_mx_quantize_rows.restype = [p, i64, i64, i32, p, p, i64], None
     L.orc_mx_quantize_src.argtypes, L.orc_mx_quantize_src.restype = [p, i32, i64, i64, i32, p, p, i64], None
     L.orc_route.argtypes, L.orc_route.restype = [p, i32, i64, i64, i64, p, p, p], i64
+    L.orc_route_range.argtypes, L.orc_route_range.restype = [p, i32, i64, i64, i64, i64, i64, p, p, p], i64
     L.orc_permute.argtypes, L.orc_permute.restype = [p, i32, i64, i64, p, i64, i32, p, p, i64], None
     L.orc_expert_row.argtypes = [p, p, i32, p, p, p, p, i32, i64, i64, i32, i32, p, p, p, p]
     L.orc_expert_row.restype = None
@@ -145,6 +146,38 @@ def route(ids: np.ndarray, num_experts: int):
     cnt = np.empty(num_experts, dtype=np.int64)
     bad = _load().orc_route(_ptr(ids), is64, n, k, num_experts, _ptr(srt), _ptr(exp), _ptr(cnt))
     return srt, exp, cnt, int(bad)
+
+
+def route_range(ids: np.ndarray, num_experts: int, start: int, end: int):
+    """route() with MoeInitRoutingV3's active expert range [start, end)
+    (activeExpertRangeOptional): only ids in the range are sorted (step 6:
+    availableIdxNum of them); counts int64[end - start]; the fourth value is the
+    number of ids outside [0, num_experts) (ids outside the range are no error)."""
+    ids = np.ascontiguousarray(ids)
+    is64 = 1 if ids.dtype == np.int64 else 0
+    if not is64:
+        ids = ids.astype(np.int32, copy=False)
+    n = ids.shape[0]
+    k = ids.shape[1] if ids.ndim == 2 else 1
+    rows = n * k
+    srt = np.empty(rows, dtype=np.int32)
+    exp = np.empty(rows, dtype=np.int32)
+    cnt = np.empty(max(end - start, 0), dtype=np.int64)
+    bad = _load().orc_route_range(_ptr(ids), is64, n, k, num_experts, start, end, _ptr(srt), _ptr(exp), _ptr(cnt))
+    return srt, exp, cnt, int(bad)
+
+
+def key_value_counts(counts: np.ndarray, start: int, num_experts: int) -> np.ndarray:
+    """MoeInitRoutingV3 expertTokensNumType 2 (key_value): [num_experts, 2] int64
+    holding (expert id, token count) for each expert of the active range with a
+    non-zero count, in ascending expert order; the rows after them are 0."""
+    out = np.zeros((num_experts, 2), dtype=np.int64)
+    m = 0
+    for e, c in enumerate(counts):
+        if c != 0:
+            out[m] = (start + e, c)
+            m += 1
+    return out
 
 
 def permute(x: np.ndarray, dtype: int, k: int, sorted_row_idx: np.ndarray, m_out: int, fmt: int = -1):

@@ -263,19 +263,30 @@ static int cmp_kv(const void* a, const void* b) {
   return x->j < y->j ? -1 : (x->j > y->j ? 1 : 0);
 }
 
-int64_t orc_route(const void* ids, int ids_is_int64, int64_t n, int64_t k, int64_t num_experts,
-                  int32_t* sorted_row_idx, int32_t* expanded_row_idx, int64_t* counts) {
-  int64_t rows = n * k, valid = 0;
+/* With an active expert range [start, end) (MoeInitRoutingV3,
+ * activeExpertRangeOptional; step 6: availableIdxNum counts the ids in
+ * the range): only ids in the range are sorted, counts[e - start] for the
+ * experts of the range; ids in [0, num_experts) but outside the range are
+ * left out like the out-of-range ones but are not errors.  Returns the
+ * number of ids outside [0, num_experts). */
+int64_t orc_route_range(const void* ids, int ids_is_int64, int64_t n, int64_t k, int64_t num_experts,
+                        int64_t start, int64_t end, int32_t* sorted_row_idx, int32_t* expanded_row_idx,
+                        int64_t* counts) {
+  int64_t rows = n * k, valid = 0, bad = 0;
   orc_kv* kv = (orc_kv*)malloc(sizeof(orc_kv) * (size_t)(rows > 0 ? rows : 1));
-  for (int64_t e = 0; e < num_experts; ++e) counts[e] = 0;
+  for (int64_t e = start; e < end; ++e) counts[e - start] = 0;
   for (int64_t j = 0; j < rows; ++j) {
     int64_t id = ids_is_int64 ? ((const int64_t*)ids)[j] : (int64_t)((const int32_t*)ids)[j];
     expanded_row_idx[j] = -1;
-    if (id < 0 || id >= num_experts) continue;
+    if (id < 0 || id >= num_experts) {
+      ++bad;
+      continue;
+    }
+    if (id < start || id >= end) continue;
     kv[valid].key = id;
     kv[valid].j = j;
     ++valid;
-    counts[id] += 1;
+    counts[id - start] += 1;
   }
   qsort(kv, (size_t)valid, sizeof(orc_kv), cmp_kv);
   for (int64_t d = 0; d < rows; ++d) sorted_row_idx[d] = -1;
@@ -284,7 +295,13 @@ int64_t orc_route(const void* ids, int ids_is_int64, int64_t n, int64_t k, int64
     expanded_row_idx[kv[d].j] = (int32_t)d;
   }
   free(kv);
-  return rows - valid;
+  return bad;
+}
+
+int64_t orc_route(const void* ids, int ids_is_int64, int64_t n, int64_t k, int64_t num_experts,
+                  int32_t* sorted_row_idx, int32_t* expanded_row_idx, int64_t* counts) {
+  return orc_route_range(ids, ids_is_int64, n, k, num_experts, 0, num_experts, sorted_row_idx, expanded_row_idx,
+                         counts);
 }
 
 /* ---------------------------------------------------------------------------

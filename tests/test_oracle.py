@@ -228,6 +228,40 @@ def test_route_int64_and_invalid_ids():
     assert cnt.tolist() == [2, 1, 1]
 
 
+@pytest.mark.parametrize("n,k,e,start,end", [(300, 4, 16, 0, 16), (300, 4, 16, 4, 12), (257, 8, 64, 63, 64),
+                                             (64, 2, 8, 3, 3), (500, 6, 40, 0, 7)])
+def test_route_active_range_matches_numpy(n, k, e, start, end):
+    """MoeInitRoutingV3 with activeExpertRangeOptional = [start, end): the ids of
+    the range sorted stably (numpy argsort), availableIdxNum = their number
+    (step 6), counts of the range's experts; other ids (and out-of-range
+    ones, counted as errors) get no row."""
+    rng = np.random.default_rng(7 * n + start)
+    ids = rng.integers(-1, e + 1, (n, k)).astype(np.int32)
+    srt, exp, cnt, bad = oracle.route_range(ids, e, start, end)
+    flat = ids.reshape(-1)
+    act = (flat >= start) & (flat < end)
+    order = np.nonzero(act)[0][np.argsort(flat[act], kind="stable")]
+    avail = int(act.sum())
+    assert avail == len(order)
+    assert np.array_equal(srt[:avail], order)
+    assert np.all(srt[avail:] == -1)
+    want_exp = np.full(flat.size, -1, np.int32)
+    want_exp[order] = np.arange(avail)
+    assert np.array_equal(exp, want_exp)
+    assert np.array_equal(cnt, np.bincount(flat[act] - start, minlength=end - start)[: end - start])
+    assert bad == int(((flat < 0) | (flat >= e)).sum())
+    if start == 0 and end == e:   # the full range is route()
+        r = oracle.route(ids, e)
+        assert all(np.array_equal(a, b) for a, b in zip(r[:3], (srt, exp, cnt))) and r[3] == bad
+
+
+def test_key_value_counts_hand_example():
+    """expertTokensNumType 2: (expert, count) of the range's non-zero experts in
+    ascending order, [expertNum, 2]; rows after them 0."""
+    kv = oracle.key_value_counts(np.array([0, 3, 0, 2]), 4, 6)
+    assert kv.tolist() == [[5, 3], [7, 2], [0, 0], [0, 0], [0, 0], [0, 0]]
+
+
 # ------------------------------------------------------------------ permute
 @pytest.mark.parametrize("fmt", [-1, P.E4M3, P.E5M2, P.E2M1])
 def test_permute_matches_gather(fmt):
