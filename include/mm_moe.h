@@ -100,7 +100,8 @@ int mm_version(void);
 
 /* ------------------------------------------------------------------------
  * mm_moe_init_routing -- MoeInitRoutingV3, Dropless, active expert range
- * [0, expert_num), quantMode -1 / 2 / 3.
+ * [0, expert_num), quantMode -1 / 2 / 3 (another range, and the key_value
+ * count type: mm_moe_init_routing_v3 below).
  *
  *   sortedRowIdx          = keyValueSort(expertIdx, rowIdx)      (step 1)
  *   expandedRowIdx[sortedRowIdx[d]] = d                           (step 2)
@@ -138,6 +139,36 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
                               uint8_t* expanded_scale, int32_t* expanded_row_idx,
                               int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
                               size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mm_moe_init_routing_v3 -- MoeInitRoutingV3, Dropless, with the active
+ * expert range (activeExpertRangeOptional = [active_expert_start,
+ * active_expert_end), computation step 6) and the three count types.
+ *
+ * Only ids in the range are sorted: they fill the first availableIdxNum =
+ * |{ids in the range}| rows of expanded_x / expanded_scale and of
+ * sorted_row_idx (whose tail is -1); the other ids get expanded_row_idx -1
+ * and no row.  Ids in [0, expert_num) but outside the range are not errors;
+ * ids outside [0, expert_num) raise MM_DEVERR_EXPERT_RANGE.
+ * 0 <= active_expert_start < active_expert_end <= expert_num, else
+ * MM_ERR_INVALID_ARG.
+ * expert_tokens_num_type  0: expert_tokens [end - start] inclusive cumsum;
+ *                   1: [end - start] counts; 2 (key_value): [expert_num, 2]
+ *                   int64 pairs (expert id, count) of the range's experts with
+ *                   a non-zero count, in ascending id, the rows after them 0
+ *                   (expert_num <= 5120 in this mode).
+ * Other arguments as mm_moe_init_routing; the workspace is sized by
+ * mm_moe_init_routing_v3_workspace_size.
+ * ---------------------------------------------------------------------- */
+mm_status mm_moe_init_routing_v3_workspace_size(int64_t num_rows, int64_t k, int64_t expert_num,
+                                                size_t* bytes);
+mm_status mm_moe_init_routing_v3(const void* x, int x_dtype, const int32_t* expert_idx,
+                                 int64_t num_rows, int64_t h, int64_t k, int64_t expert_num,
+                                 int64_t active_expert_start, int64_t active_expert_end,
+                                 int quant_mode, int expert_tokens_num_type, void* expanded_x,
+                                 uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                                 int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * mm_moe_token_permute -- moe_token_permute with padded_mode = false.

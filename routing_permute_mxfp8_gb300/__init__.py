@@ -74,6 +74,9 @@ def load():
     L.mm_version.restype = i32
     L.mm_moe_init_routing_workspace_size.argtypes = [i64, i64, i64, psz]
     L.mm_moe_init_routing.argtypes = [p, i32, p, i64, i64, i64, i64, i32, i32, p, p, p, p, p, p, sz, p, p]
+    L.mm_moe_init_routing_v3_workspace_size.argtypes = [i64, i64, i64, psz]
+    L.mm_moe_init_routing_v3.argtypes = [p, i32, p, i64, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, p, p, sz,
+                                         p, p]
     L.mm_moe_token_permute_out_rows.argtypes, L.mm_moe_token_permute_out_rows.restype = [i64, i64], i64
     L.mm_moe_token_permute_workspace_size.argtypes = [i64, i64, psz]
     L.mm_moe_token_permute.argtypes = [p, i32, p, i32, i64, i64, i64, i64, i64, i32, i32, p, p, p, p, sz, p, p]
@@ -162,12 +165,17 @@ def _dev_err(dev_err):
 
 # --------------------------------------------------------------------------- routing / permute
 def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_NONE,
-                        expert_tokens_num_type: int = 1, *, workspace=None, dev_err=None):
-    """MoeInitRoutingV3 (Dropless, full expert range).
+                        expert_tokens_num_type: int = 1, *, active_expert_range=None, workspace=None,
+                        dev_err=None):
+    """MoeInitRoutingV3 (Dropless).
 
     Returns (expanded_x [N*K, H], expanded_row_idx [N*K] int32 (scatter),
-    expert_tokens [E] int64 (count or cumsum), expanded_scale [N*K, AlignUp(H/32, 2)]
-    uint8 E8M0 (empty without quantisation), sorted_row_idx [N*K] int32 (gather)).
+    expert_tokens (count or cumsum [E'] int64, or key_value [E, 2] int64 with
+    expert_tokens_num_type 2), expanded_scale [N*K, AlignUp(H/32, 2)] uint8 E8M0
+    (empty without quantisation), sorted_row_idx [N*K] int32 (gather)).
+    active_expert_range = (start, end): only ids in [start, end) are routed
+    (E' = end - start; the first availableIdxNum rows of the outputs are valid);
+    None: the full range (mm_moe_init_routing), else mm_moe_init_routing_v3.
     """
     _need_dtype(x, _SRC_DTYPES, "x")
     _need_dtype(expert_idx, (torch.int32,), "expert_idx")
@@ -183,14 +191,28 @@ def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_
              else torch.empty((0,), dtype=torch.uint8, device=dev))
     exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)
     srt_idx = torch.empty(rows, dtype=torch.int32, device=dev)
-    tokens = torch.empty(expert_num, dtype=torch.int64, device=dev)
+    v3 = active_expert_range is not None or expert_tokens_num_type == 2
+    start, end = (0, expert_num) if active_expert_range is None else (int(active_expert_range[0]),
+                                                                      int(active_expert_range[1]))
+    tokens = (torch.empty((expert_num, 2), dtype=torch.int64, device=dev) if expert_tokens_num_type == 2
+              else torch.empty(max(end - start, 0), dtype=torch.int64, device=dev))
     need = ctypes.c_size_t(0)
-    _check(L.mm_moe_init_routing_workspace_size(n, k, expert_num, ctypes.byref(need)), "mm_moe_init_routing")
+    if v3:
+        _check(L.mm_moe_init_routing_v3_workspace_size(n, k, expert_num, ctypes.byref(need)), "mm_moe_init_routing_v3")
+    else:
+        _check(L.mm_moe_init_routing_workspace_size(n, k, expert_num, ctypes.byref(need)), "mm_moe_init_routing")
     ws = _workspace(need.value, dev, workspace)
-    _check(L.mm_moe_init_routing(_ptr(x), _dt(x), _ptr(expert_idx), n, h, k, expert_num, quant_mode,
-                                 expert_tokens_num_type, _ptr(expanded_x), _ptr(scale) if scale.numel() else None,
-                                 _ptr(exp_idx), _ptr(srt_idx), _ptr(tokens), _ptr(ws), ws.numel(),
-                                 _dev_err(dev_err), _stream(dev)), "mm_moe_init_routing")
+    sc = _ptr(scale) if scale.numel() else None
+    if v3:
+        _check(L.mm_moe_init_routing_v3(_ptr(x), _dt(x), _ptr(expert_idx), n, h, k, expert_num, start, end,
+                                        quant_mode, expert_tokens_num_type, _ptr(expanded_x), sc, _ptr(exp_idx),
+                                        _ptr(srt_idx), _ptr(tokens), _ptr(ws), ws.numel(), _dev_err(dev_err),
+                                        _stream(dev)), "mm_moe_init_routing_v3")
+    else:
+        _check(L.mm_moe_init_routing(_ptr(x), _dt(x), _ptr(expert_idx), n, h, k, expert_num, quant_mode,
+                                     expert_tokens_num_type, _ptr(expanded_x), sc, _ptr(exp_idx), _ptr(srt_idx),
+                                     _ptr(tokens), _ptr(ws), ws.numel(), _dev_err(dev_err), _stream(dev)),
+               "mm_moe_init_routing")
     return expanded_x, exp_idx, tokens, scale, srt_idx
 
 

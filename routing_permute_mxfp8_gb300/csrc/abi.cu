@@ -329,35 +329,58 @@ mm_status mm_moe_init_routing_workspace_size(int64_t num_rows, int64_t k, int64_
   return MM_OK;
 }
 
-mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows, int64_t h,
-                              int64_t k, int64_t expert_num, int quant_mode, int expert_tokens_num_type,
-                              void* expanded_x, uint8_t* expanded_scale, int32_t* expanded_row_idx,
-                              int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_err, void* stream) {
+mm_status mm_moe_init_routing_v3_workspace_size(int64_t num_rows, int64_t k, int64_t expert_num, size_t* bytes) {
+  mm_status s = mm_moe_init_routing_workspace_size(num_rows, k, expert_num, bytes);
+  if (s == MM_OK) *bytes += (size_t)round_up(expert_num * (int64_t)sizeof(int64_t), 256);  // key_value counts
+  return s;
+}
+
+// MoeInitRoutingV3, Dropless, with the active expert range [start, end)
+// (activeExpertRangeOptional; computation step 6) and the three count
+// types; mm_moe_init_routing is the full range with types 0 / 1.
+static mm_status init_routing_impl(bool v3, const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows,
+                                   int64_t h, int64_t k, int64_t expert_num, int64_t start, int64_t end,
+                                   int quant_mode, int expert_tokens_num_type, void* expanded_x,
+                                   uint8_t* expanded_scale, int32_t* expanded_row_idx, int32_t* sorted_row_idx,
+                                   int64_t* expert_tokens, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_err, void* stream) {
   size_t need = 0;
-  mm_status s = mm_moe_init_routing_workspace_size(num_rows, k, expert_num, &need);
+  mm_status s = v3 ? mm_moe_init_routing_v3_workspace_size(num_rows, k, expert_num, &need)
+                   : mm_moe_init_routing_workspace_size(num_rows, k, expert_num, &need);
   if (s != MM_OK) return s;
-  s = validate_init_routing(x, x_dtype, expert_idx, num_rows, h, k, expert_num, quant_mode, expert_tokens_num_type,
-                            expanded_x, expanded_scale);
+  if (start < 0 || end <= start || end > expert_num) return MM_ERR_INVALID_ARG;
+  const bool key_value = expert_tokens_num_type == 2;
+  if (key_value && !v3) return MM_ERR_UNSUPPORTED;
+  if (key_value && expert_num > 5120) return MM_ERR_INVALID_ARG;
+  s = validate_init_routing(x, x_dtype, expert_idx, num_rows, h, k, expert_num, quant_mode,
+                            key_value ? 1 : expert_tokens_num_type, expanded_x, expanded_scale);
   if (s != MM_OK) return s;
   const int64_t rows = num_rows * k;
+  const int64_t ne = end - start;  // experts of the active range
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows == 0)  // no rows: every expert's count (and the cumsum) is 0
-    return expert_tokens ? cuda_status(cudaMemsetAsync(expert_tokens, 0, (size_t)expert_num * sizeof(int64_t),
-                                                       static_cast<cudaStream_t>(stream)))
+    return expert_tokens ? cuda_status(cudaMemsetAsync(
+                               expert_tokens, 0, (size_t)(key_value ? 2 * expert_num : ne) * sizeof(int64_t), st))
                          : MM_OK;
   if (!workspace || workspace_bytes < need) return MM_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const RoutePlan plan = route_plan(rows, (int)expert_num);
+  const RoutePlan plan = route_plan(rows, (int)ne);
   Carver c(workspace);
   RoutingWs w = carve_routing(c, plan);
+  int64_t* kv_counts = key_value ? c.take<int64_t>(expert_num) : nullptr;
   RouteOutputs o;
   o.expanded_row_idx = expanded_row_idx ? expanded_row_idx : w.exp_idx;
   o.sorted_row_idx = sorted_row_idx;
-  o.expert_tokens = expert_tokens;
+  o.expert_tokens = key_value ? (expert_tokens ? kv_counts : nullptr) : expert_tokens;
   o.tokens_cumsum = expert_tokens_num_type == 0;
+  o.key_off = (int)start;
+  o.id_limit = expert_num;
   StageScope sr(MM_STAGE_ROUTE, st);
   int nl = 0;
   cudaError_t e = launch_route(plan, expert_idx, false, w.hist, w.offsets, o, dev_err, st, &nl);
+  if (e == cudaSuccess && key_value && expert_tokens) {
+    e = launch_key_value_counts(kv_counts, (int)ne, start, expert_num, expert_tokens, st);
+    ++nl;
+  }
   sr.finish(nl);
   if (e != cudaSuccess) return MM_ERR_CUDA;
   PermuteArgs a = {};
@@ -377,6 +400,29 @@ mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_
   e = launch_permute(a, st);
   sd.finish(1);
   return cuda_status(e);
+}
+
+mm_status mm_moe_init_routing(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows, int64_t h,
+                              int64_t k, int64_t expert_num, int quant_mode, int expert_tokens_num_type,
+                              void* expanded_x, uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                              int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (expert_num <= 0 || expert_num > 10240) return MM_ERR_INVALID_ARG;
+  return init_routing_impl(false, x, x_dtype, expert_idx, num_rows, h, k, expert_num, 0, expert_num, quant_mode,
+                           expert_tokens_num_type, expanded_x, expanded_scale, expanded_row_idx, sorted_row_idx,
+                           expert_tokens, workspace, workspace_bytes, dev_err, stream);
+}
+
+mm_status mm_moe_init_routing_v3(const void* x, int x_dtype, const int32_t* expert_idx, int64_t num_rows, int64_t h,
+                                 int64_t k, int64_t expert_num, int64_t active_expert_start,
+                                 int64_t active_expert_end, int quant_mode, int expert_tokens_num_type,
+                                 void* expanded_x, uint8_t* expanded_scale, int32_t* expanded_row_idx,
+                                 int32_t* sorted_row_idx, int64_t* expert_tokens, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  return init_routing_impl(true, x, x_dtype, expert_idx, num_rows, h, k, expert_num, active_expert_start,
+                           active_expert_end, quant_mode, expert_tokens_num_type, expanded_x, expanded_scale,
+                           expanded_row_idx, sorted_row_idx, expert_tokens, workspace, workspace_bytes, dev_err,
+                           stream);
 }
 
 // ------------------------------------------------------------------------

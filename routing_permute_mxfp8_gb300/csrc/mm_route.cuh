@@ -14,6 +14,14 @@ struct RoutePlan {
   int warps_per_block;  // chunks per block (smem: warps * E * 4 bytes)
 };
 
+// Sort keys of the routing: key = (id - off) / div for the ids with a key in
+// [0, num_experts); ids outside [0, limit) raise MM_DEVERR_EXPERT_RANGE.
+struct KeyMap {
+  int div;
+  int off;
+  int64_t limit;
+};
+
 struct RouteOutputs {
   int32_t* expanded_row_idx = nullptr;   // [R] scatter index (or null)
   int32_t* sorted_row_idx = nullptr;     // [R] gather index (or null)
@@ -27,6 +35,9 @@ struct RouteOutputs {
   int shared_rows = 0;                   // ... of this many rows each
   int key_div = 1;                       // sort key = id / key_div (ids < num_experts * key_div)
   int32_t* sorted_rem = nullptr;         // [R] id % key_div at each sorted position (or null)
+  int key_off = 0;                       // key_div 1: sort key = id - key_off (an active expert range)
+  int64_t id_limit = 0;                  // ids outside [0, id_limit) are errors (0: num_experts * key_div);
+                                         // other ids without a key are left out silently
   int64_t pad_limit = 0;                 // rows of the padded layout pad_row addresses (checked build)
 };
 
@@ -54,6 +65,11 @@ int64_t route_offsets_words(int num_experts);
 // workspace)
 // *launches (optional) receives the number of kernels launched: 1 (one
 // cluster launch or one cooperative launch) or 4.
+// MoeInitRoutingV3 expertTokensNumType 2 (key_value): out [out_rows, 2] int64
+// = (first + e, counts[e]) for each e < n with counts[e] != 0, in ascending e,
+// then zeros.
+cudaError_t launch_key_value_counts(const int64_t* counts, int n, int64_t first, int64_t out_rows, int64_t* out,
+                                    cudaStream_t st);
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches = nullptr);
 // Routing implementation used from now on, process-wide: 0 automatic (one

@@ -50,12 +50,14 @@ __device__ __forceinline__ void route_load_ids(const IdT* __restrict__ ids, int6
 
 // Phase 1, one warp per chunk: counts of each expert in chunk `unit`
 // (cnt: this warp's [E] shared-memory counters).
-// Keys: the sort key of id is id / key_div (1: the expert itself; the number
-// of experts per rank: the destination rank of expert parallelism); ids
-// outside [0, num_experts * key_div) are out of range.
+// Keys (KeyMap): the sort key of id is (id - off) / div (div 1: the expert
+// itself, or its place in an active expert range starting at off; div = the
+// experts per rank: the destination rank of expert parallelism); ids without
+// a key in [0, num_experts) are left out, and those outside [0, limit) are
+// errors.
 template <typename IdT>
 __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                 int key_div, int chunk, int unit, int32_t* cnt, int32_t* dev_err,
+                                                 KeyMap km, int chunk, int unit, int32_t* cnt, int32_t* dev_err,
                                                  IdT* v, bool preloaded = false) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < num_experts; e += 32) cnt[e] = 0;
@@ -63,7 +65,7 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
   const int64_t start = (int64_t)unit * chunk;
   const int64_t end = start + chunk < rows ? start + chunk : rows;
   bool bad = false;
-  const int64_t id_end = (int64_t)num_experts * key_div;
+  const int64_t id_end = (int64_t)num_experts * km.div;
   // kIdBatch 32-id steps per round: their loads are all in flight before
   // the first is counted (preloaded: the caller has loaded the first round)
   for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
@@ -71,16 +73,17 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
 #pragma unroll
     for (int b = 0; b < kIdBatch; ++b) {
       if (j0 + 32 * b + lane >= end) break;
-      if (key_div == 1) {
+      if (km.div == 1) {
         using UIdT = typename std::make_unsigned<IdT>::type;
-        if ((UIdT)v[b] < (UIdT)num_experts)
-          atomicAdd(&cnt[(int)v[b]], 1);
-        else
+        const UIdT kv = (UIdT)v[b] - (UIdT)km.off;
+        if (kv < (UIdT)num_experts)
+          atomicAdd(&cnt[(int)kv], 1);
+        else if ((UIdT)v[b] >= (UIdT)km.limit)
           bad = true;
       } else {
         const int64_t id = (int64_t)v[b];
         if (id >= 0 && id < id_end)
-          atomicAdd(&cnt[id / key_div], 1);
+          atomicAdd(&cnt[id / km.div], 1);
         else
           bad = true;
       }
@@ -93,21 +96,21 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
 // ... and the counts stored to the global [E][units] table
 template <typename IdT>
 __device__ __forceinline__ void route_hist_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                int key_div, int chunk, int units, int unit, int32_t* cnt,
+                                                KeyMap km, int chunk, int units, int unit, int32_t* cnt,
                                                 int32_t* __restrict__ hist, int32_t* dev_err) {
   const int lane = threadIdx.x & 31;
   if (unit >= units) return;
   IdT v[kIdBatch];
-  route_count_warp(ids, rows, num_experts, key_div, chunk, unit, cnt, dev_err, v);
+  route_count_warp(ids, rows, num_experts, km, chunk, unit, cnt, dev_err, v);
   for (int e = lane; e < num_experts; e += 32) hist[(int64_t)e * units + unit] = cnt[e];
 }
 
 template <typename IdT>
-__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
+__global__ void k_route_hist(const IdT* __restrict__ ids, int64_t rows, int num_experts, KeyMap km, int chunk,
                              int units, int32_t* __restrict__ hist, int32_t* dev_err) {
   extern __shared__ int32_t sh_cnt[];  // [warps][E]
   const int warp = threadIdx.x >> 5;
-  route_hist_warp(ids, rows, num_experts, key_div, chunk, units, blockIdx.x * (blockDim.x >> 5) + warp,
+  route_hist_warp(ids, rows, num_experts, km, chunk, units, blockIdx.x * (blockDim.x >> 5) + warp,
                   sh_cnt + warp * num_experts, hist, dev_err);
 }
 
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(1024) k_route_scan_offsets(RouteScanArgs a) {
 // offsets / seg_mprefix: per-key first slot and GEMM tile prefix (pad_row).
 template <typename IdT>
 __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, int64_t start, int64_t end,
-                                                   int num_experts, int key_div, int32_t* next,
+                                                   int num_experts, KeyMap km, int32_t* next,
                                                    const int32_t* offsets, const int32_t* seg_mprefix,
                                                    int32_t* __restrict__ expanded_row_idx,
                                                    int32_t* __restrict__ sorted_row_idx, int32_t* __restrict__ pad_row,
@@ -269,7 +272,7 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
   const unsigned lt = (1u << lane) - 1u;
   const int key_bits = 32 - __clz(num_experts);  // bits of the largest key + 1
   using UIdT = typename std::make_unsigned<IdT>::type;
-  const int64_t id_end = (int64_t)num_experts * key_div;
+  const int64_t id_end = (int64_t)num_experts * km.div;
   for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
     // the next kIdBatch steps' ids, loaded together (preloaded: the caller
     // has loaded the first round)
@@ -282,13 +285,14 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
       const bool in = j < end;
       int key = -1, rem = 0;
       if (in) {
-        if (key_div == 1) {
-          if ((UIdT)v[b] < (UIdT)num_experts) key = (int)v[b];
+        if (km.div == 1) {
+          const UIdT kv = (UIdT)v[b] - (UIdT)km.off;
+          if (kv < (UIdT)num_experts) key = (int)kv;
         } else {
           const int64_t id = (int64_t)v[b];
           if (id >= 0 && id < id_end) {
-            key = (int)(id / key_div);
-            rem = (int)(id - (int64_t)key * key_div);
+            key = (int)(id / km.div);
+            rem = (int)(id - (int64_t)key * km.div);
           }
         }
       }
@@ -327,7 +331,7 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
 
 template <typename IdT>
 __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                   int key_div, int chunk, int units, int unit, int32_t* next,
+                                                   KeyMap km, int chunk, int units, int unit, int32_t* next,
                                                    const int32_t* __restrict__ bases,
                                                    const int32_t* __restrict__ offsets,
                                                    const int32_t* __restrict__ seg_mprefix,
@@ -341,12 +345,12 @@ __device__ __forceinline__ void route_scatter_warp(const IdT* __restrict__ ids, 
   const int64_t start = (int64_t)unit * chunk;
   const int64_t end = start + chunk < rows ? start + chunk : rows;
   IdT v[kIdBatch];
-  route_scatter_walk(ids, start, end, num_experts, key_div, next, offsets, seg_mprefix, expanded_row_idx,
+  route_scatter_walk(ids, start, end, num_experts, km, next, offsets, seg_mprefix, expanded_row_idx,
                      sorted_row_idx, pad_row, sorted_rem, rows, pad_limit, dev_err, v);
 }
 
 template <typename IdT>
-__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
+__global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int num_experts, KeyMap km, int chunk,
                                 int units, const int32_t* __restrict__ bases,
                                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ seg_mprefix,
                                 int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ sorted_row_idx,
@@ -356,7 +360,7 @@ __global__ void k_route_scatter(const IdT* __restrict__ ids, int64_t rows, int n
   const int warp = threadIdx.x >> 5;
   const int unit = blockIdx.x * (blockDim.x >> 5) + warp;
   if (unit >= units) return;
-  route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, sh_next + warp * num_experts, bases,
+  route_scatter_warp(ids, rows, num_experts, km, chunk, units, unit, sh_next + warp * num_experts, bases,
                      offsets, seg_mprefix, expanded_row_idx, sorted_row_idx, pad_row, sorted_rem, pad_limit, dev_err);
 }
 
@@ -392,7 +396,7 @@ __device__ __forceinline__ bool grid_barrier_bounded(uint32_t* count, uint32_t b
 // All four phases in one cooperative launch (every block resident), with
 // grid-wide barriers between them: one launch instead of four.
 template <typename IdT>
-__global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, int key_div, int chunk,
+__global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num_experts, KeyMap km, int chunk,
                               int units, int32_t* __restrict__ hist, RouteScanArgs sa,
                               int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ pad_row,
                               int32_t* __restrict__ sorted_rem, int64_t pad_limit, uint32_t* __restrict__ barrier,
@@ -403,7 +407,7 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
   const int warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int unit = blockIdx.x * wpb + warp;
   int32_t* mine = sh_route + warp * num_experts;
-  if (unit < units) route_hist_warp(ids, rows, num_experts, key_div, chunk, units, unit, mine, hist, dev_err);
+  if (unit < units) route_hist_warp(ids, rows, num_experts, km, chunk, units, unit, mine, hist, dev_err);
   if (!grid_barrier_bounded(barrier, 1, dev_err, &sh_ok)) return;
   if (units <= 32) {
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < num_experts; e += gridDim.x * blockDim.x)
@@ -415,7 +419,7 @@ __global__ void k_route_fused(const IdT* __restrict__ ids, int64_t rows, int num
   if (blockIdx.x == 0) route_scan_offsets_block(sa, sh_warp);
   if (!grid_barrier_bounded(barrier, 3, dev_err, &sh_ok)) return;
   if (unit < units)
-    route_scatter_warp(ids, rows, num_experts, key_div, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
+    route_scatter_warp(ids, rows, num_experts, km, chunk, units, unit, mine, hist, sa.offsets, sa.seg_mprefix,
                        expanded_row_idx, sa.sorted_row_idx, pad_row, sorted_rem, pad_limit, dev_err);
 }
 
@@ -474,7 +478,7 @@ __device__ __forceinline__ int32_t ld_cluster_peer(const int32_t* local, uint32_
 
 template <typename IdT>
 __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ ids, int64_t rows, int num_experts,
-                                                        int key_div, int chunk, RouteScanArgs sa,
+                                                        KeyMap km, int chunk, RouteScanArgs sa,
                                                         int32_t* __restrict__ expanded_row_idx,
                                                         int32_t* __restrict__ pad_row,
                                                         int32_t* __restrict__ sorted_rem, int64_t pad_limit,
@@ -501,7 +505,7 @@ __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ 
   IdT v[kIdBatch];
   route_load_ids(ids, start, end, v);
 
-  route_count_warp(ids, rows, E, key_div, chunk, unit, mine, dev_err, v, true);
+  route_count_warp(ids, rows, E, km, chunk, unit, mine, dev_err, v, true);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += nt) {
     int32_t run = 0;
@@ -588,12 +592,42 @@ __global__ void __launch_bounds__(1024) k_route_cluster(const IdT* __restrict__ 
 
   for (int e = lane; e < E; e += 32) mine[e] += eoff[e] + cpre[e];
   __syncwarp();
-  route_scatter_walk(ids, start, end, E, key_div, mine, eoff, mpre, expanded_row_idx, sa.sorted_row_idx, pad_row,
+  route_scatter_walk(ids, start, end, E, km, mine, eoff, mpre, expanded_row_idx, sa.sorted_row_idx, pad_row,
                      sorted_rem, rows, pad_limit, dev_err, v, resident);
   cluster_wait_acquire();
 }
 
 // ---------------------------------------------------------------------------
+// key_value counts: one block; the non-zero counts are compacted in
+// ascending expert order by a block-wide scan of their flags, 1024 experts
+// at a time, after the output has been zeroed.
+__global__ void __launch_bounds__(1024) k_key_value_counts(const int64_t* __restrict__ counts, int n, int64_t first,
+                                                           int64_t out_rows, int64_t* __restrict__ out) {
+  __shared__ int warp_tot[32];
+  __shared__ int base;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int64_t i = threadIdx.x; i < 2 * out_rows; i += blockDim.x) out[i] = 0;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int e0 = 0; e0 < n; e0 += blockDim.x) {
+    const int e = e0 + (int)threadIdx.x;
+    const int64_t c = e < n ? counts[e] : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+    if (lane == 0) warp_tot[w] = __popc(m);
+    __syncthreads();
+    int before = base;
+    for (int i = 0; i < w; ++i) before += warp_tot[i];
+    const int pos = before + __popc(m & ((1u << lane) - 1u));
+    if (c != 0 && pos < out_rows) {
+      out[2 * (int64_t)pos] = first + e;
+      out[2 * (int64_t)pos + 1] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) base = pos + (c != 0 ? 1 : 0);
+    __syncthreads();
+  }
+}
+
 RoutePlan route_plan(int64_t rows, int num_experts) {
   RoutePlan p;
   p.rows = rows;
@@ -727,6 +761,14 @@ int cluster_max_ctas(int wpb) {
   return fits[dev][wpb];
 }
 
+KeyMap key_map(const RouteOutputs& o, int num_experts) {
+  KeyMap k;
+  k.div = o.key_div;
+  k.off = o.key_off;
+  k.limit = o.id_limit > 0 ? o.id_limit : (int64_t)num_experts * o.key_div;
+  return k;
+}
+
 template <typename IdT>
 bool launch_route_cluster(const RoutePlan& p, const IdT* ids, RouteScanArgs a, const RouteOutputs& o,
                           int32_t* dev_err, cudaStream_t st) {
@@ -747,14 +789,15 @@ bool launch_route_cluster(const RoutePlan& p, const IdT* ids, RouteScanArgs a, c
   per = round_up(per < 32 ? 32 : per, 32);
   if (per > INT32_MAX) return false;
   const int64_t rows = p.rows;
-  const int ne = p.num_experts, kdiv = o.key_div, chunk = (int)per;
+  const int ne = p.num_experts, chunk = (int)per;
+  const KeyMap km = key_map(o, ne);
   int32_t* exp_idx = o.expanded_row_idx;
   int32_t* pad = o.pad_row;
   int32_t* rem = o.sorted_rem;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config((int)ncta, wpb, cluster_smem(wpb, ne, ne + a.n_shared), st, attr, true);
   const int64_t plim = o.pad_limit;
-  if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, kdiv, chunk, a, exp_idx, pad, rem, plim, dev_err) ==
+  if (cudaLaunchKernelEx(&cfg, k_route_cluster<IdT>, ids, rows, ne, km, chunk, a, exp_idx, pad, rem, plim, dev_err) ==
       cudaSuccess)
     return true;
   cudaGetLastError();
@@ -781,14 +824,15 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
   }
   if (path != 3 && cap == cudaStreamCaptureStatusNone && blocks <= fused_capacity<IdT>(wpb)) {
     int64_t rows = p.rows;
-    int ne = p.num_experts, kdiv = o.key_div, chunk = p.chunk, units = p.units;
+    int ne = p.num_experts, chunk = p.chunk, units = p.units;
+    KeyMap km = key_map(o, ne);
     int32_t* exp_idx = o.expanded_row_idx;
     int32_t* pad = o.pad_row;
     int32_t* rem = o.sorted_rem;
     int64_t plim = o.pad_limit;
     // the barrier counter (workspace, after the offsets and totals) starts at 0
     uint32_t* barrier = reinterpret_cast<uint32_t*>(a.offsets + route_offsets_words(p.num_experts) - 2);
-    void* args[] = {(void*)&ids, &rows, &ne, &kdiv, &chunk, &units, &hist, &a, &exp_idx, &pad, &rem, &plim, &barrier,
+    void* args[] = {(void*)&ids, &rows, &ne, &km, &chunk, &units, &hist, &a, &exp_idx, &pad, &rem, &plim, &barrier,
                     &dev_err};
     if (cudaMemsetAsync(barrier, 0, sizeof(uint32_t), st) != cudaSuccess) return cudaGetLastError();
     if (cudaLaunchCooperativeKernel((const void*)k_route_fused<IdT>, dim3(blocks), dim3(wpb * 32), args, sh, st) ==
@@ -798,11 +842,13 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
     }
     cudaGetLastError();  // not launched (e.g. no cooperative launch here): the four kernels below
   }
-  k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, o.key_div, p.chunk, p.units, hist,
+  k_route_hist<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, key_map(o, p.num_experts), p.chunk,
+                                                  p.units, hist,
                                                   dev_err);
   k_route_scan_experts<<<(p.num_experts + 31) / 32, 1024, 0, st>>>(hist, p.num_experts, p.units, a.totals);
   k_route_scan_offsets<<<1, 1024, 0, st>>>(a);
-  k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, o.key_div, p.chunk, p.units, hist,
+  k_route_scatter<IdT><<<blocks, wpb * 32, sh, st>>>(ids, p.rows, p.num_experts, key_map(o, p.num_experts), p.chunk,
+                                                     p.units, hist,
                                                      a.offsets, o.seg_mprefix, o.expanded_row_idx,
                                                      o.sorted_row_idx, o.pad_row, o.sorted_rem, o.pad_limit, dev_err);
   launches = 4;
@@ -812,6 +858,12 @@ cudaError_t launch_route_typed(const RoutePlan& p, const IdT* ids, int32_t* hist
 }  // namespace
 
 void set_route_path(int path) { g_route_path.store(path); }
+
+cudaError_t launch_key_value_counts(const int64_t* counts, int n, int64_t first, int64_t out_rows, int64_t* out,
+                                    cudaStream_t st) {
+  k_key_value_counts<<<1, 1024, 0, st>>>(counts, n, first, out_rows, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(const RoutePlan& p, const void* ids, bool ids64, int32_t* hist, int32_t* offsets,
                          RouteOutputs o, int32_t* dev_err, cudaStream_t st, int* launches) {

@@ -160,6 +160,31 @@ def test_mega_moe_host_rejections(lib):
         assert _mega(lib, act=act, params=f(*params) if params else None, nparams=len(params)) == 3, act
 
 
+def test_init_routing_v3_host_rejections(lib):
+    """Active expert range and count-type checks, before anything is enqueued."""
+    vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
+
+    def call(start, end, ttype=1, e=8, ws=None, wsb=0):
+        return lib.mm_moe_init_routing_v3(vp(1), 27, vp(1), 64, 256, 2, e, start, end, -1, ttype, vp(1), None, vp(1),
+                                          None, vp(1), vp(ws), wsb, None, None)
+    assert call(0, 8) == 3           # valid: stops at the missing workspace
+    assert call(3, 4) == 3
+    assert call(-1, 4) == 1          # start < 0
+    assert call(4, 4) == 1           # empty range
+    assert call(5, 4) == 1
+    assert call(0, 9) == 1           # end > expert_num
+    assert call(0, 8, ttype=2) == 3  # key_value counts
+    assert call(0, 8, ttype=3) == 2
+    assert call(0, 6000, ttype=2, e=6000) == 1   # key_value: expert_num <= 5120
+    n_v3, n_base = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.mm_moe_init_routing_v3_workspace_size(64, 2, 8, ctypes.byref(n_v3)) == 0
+    assert lib.mm_moe_init_routing_workspace_size(64, 2, 8, ctypes.byref(n_base)) == 0
+    assert n_v3.value >= n_base.value + 8 * 8
+    # mm_moe_init_routing itself keeps types 0 / 1
+    assert lib.mm_moe_init_routing(vp(1), 27, vp(1), 64, 256, 2, 8, -1, 2, vp(1), None, vp(1), None, vp(1), None, 0,
+                                   None, None) == 2
+
+
 def test_permute_host_rejections(lib):
     vp = lambda v: ctypes.c_void_p(16 * v)
     call = lambda **kw: lib.mm_moe_token_permute(

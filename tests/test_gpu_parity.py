@@ -109,6 +109,49 @@ def test_init_routing_bit_exact(n, h, e, k, quant, kind):
 
 ROUTE_PATHS = {"cluster": mm.ROUTE_CLUSTER, "grid": mm.ROUTE_GRID, "kernels": mm.ROUTE_KERNELS}
 
+# MoeInitRoutingV3 with activeExpertRangeOptional: (n, h, e, k, start, end, quant, bad ids)
+RANGE_CASES = [
+    (300, 256, 16, 4, 4, 12, 3, False),
+    (1000, 512, 64, 8, 63, 64, -1, False),      # one expert at the end of the ids
+    (4096, 256, 256, 8, 32, 64, 2, True),       # an eighth of the experts; ids -1 and E mixed in
+    (70000, 128, 512, 2, 0, 300, 3, False),     # above the cluster kernel's range
+    (513, 384, 8, 8, 0, 8, -1, True),           # the full range through the v3 entry point
+]
+
+
+@pytest.mark.parametrize("n,h,e,k,start,end,quant,bad", RANGE_CASES)
+def test_init_routing_active_range(n, h, e, k, start, end, quant, bad):
+    """Only ids in [start, end) are routed (computation step 6: availableIdxNum of
+    them, in the first rows); counts / cumsum of the range's experts and the
+    key_value form; ids outside [0, E) flagged, other ids left out silently."""
+    cfg = synth.CONFIGS["routing"].scaled(n=n, h=h, e=e, k=k)
+    x = synth.tokens_bf16(cfg)
+    ids = _ids(n, e, k, "any", n + e + start)
+    if bad:
+        ids[1, 0], ids[n // 2, k - 1] = -1, e
+    r_srt, r_exp, r_cnt, r_bad = oracle.route_range(ids, e, start, end)
+    avail = int(((ids >= start) & (ids < end)).sum())
+    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    r_out, r_sc = oracle.permute(x, oracle.DT_BF16, k, r_srt, avail, fmt=fmt)
+    for ttype in (0, 1, 2):
+        err = zeros_err()
+        ex, exp_idx, tok, sc, srt = mm.mm_moe_init_routing(bf16(x), t(ids), e, quant, ttype,
+                                                           active_expert_range=(start, end), dev_err=err)
+        assert (host(err)[0] & 1) == (1 if r_bad else 0)
+        assert np.array_equal(host(srt), r_srt)
+        assert np.array_equal(host(exp_idx), r_exp)
+        want = {0: np.cumsum(r_cnt), 1: r_cnt, 2: oracle.key_value_counts(r_cnt, start, e)}[ttype]
+        assert np.array_equal(host(tok), want), ttype
+        assert np.array_equal(host(ex)[:avail], r_out)
+        if quant != -1:
+            assert np.array_equal(host(sc)[:avail], r_sc)
+
+
+@pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
+@pytest.mark.parametrize("case", [RANGE_CASES[i] for i in (0, 2, 4)])
+def test_init_routing_active_range_every_path(route_path, case):
+    test_init_routing_active_range(*case)
+
 
 @pytest.fixture
 def route_path(request):
