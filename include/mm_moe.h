@@ -389,12 +389,16 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  * num_rows = 0 only zeroes rank_counts.
  *
  * mm_moe_combine -- Y[i] = sum_k W[i,k] * expert_rows[row_idx[i*k + k']]
- *   accumulated in fp32 in the order k' = 0..k-1, rounded to bf16 once;
- *   row_idx < 0 leaves the term out (MegaMoE stage 4).  On the source rank:
- *   expert_rows = the returned rows in send order, row_idx =
- *   expanded_row_idx of mm_moe_ep_dispatch.
+ *   + sum_s shared_rows[s][i], accumulated in fp32 in the order k' = 0..k-1
+ *   then s, rounded to bf16 once; row_idx < 0 leaves the term out (MegaMoE
+ *   stage 4).  On the source rank: expert_rows = the returned rows in send
+ *   order, row_idx = expanded_row_idx of mm_moe_ep_dispatch, shared_rows =
+ *   the rank's own shared experts' outputs for its tokens (they take part in
+ *   no exchange).
  * expert_rows       [*, h] bf16, h a multiple of 8.
- * topk_weights      [num_rows, k] fp32 or bf16 (topk_weights_dtype); k <= 36.
+ * topk_weights      [num_rows, k] fp32 or bf16 (topk_weights_dtype).
+ * shared_rows       [n_shared, num_rows, h] bf16, n_shared 0..4 (NULL when 0);
+ *                   k + n_shared <= 36.
  * y                 [num_rows, h] bf16 output.
  * ---------------------------------------------------------------------- */
 mm_status mm_moe_ep_dispatch_workspace_size(int64_t num_rows, int64_t k, int64_t ep_world_size, size_t* bytes);
@@ -404,7 +408,8 @@ mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids
                              int32_t* send_expert, int64_t* rank_counts, int32_t* expanded_row_idx,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
 mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
-                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, void* y, void* stream);
+                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, const void* shared_rows,
+                         int64_t n_shared, void* y, void* stream);
 
 /* ------------------------------------------------------------------------
  * mm_moe_expert_ffn -- the expert side of expert parallelism (MegaMoE README,

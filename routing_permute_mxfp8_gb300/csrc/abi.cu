@@ -733,7 +733,7 @@ static mm_status mega_moe_impl(bool rows_out, const void* x, const uint8_t* x_sc
   // 5. combine (the expert side of expert parallelism has none: its rows
   //    go back to their source ranks)
   if (!rows_out) {
-    CombineArgs ca;
+    CombineArgs ca = {};
     ca.o = w.o;
     ca.pad_row = w.pad_row;
     ca.gate = topk_weights;
@@ -913,18 +913,22 @@ mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids
 }
 
 mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
-                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, void* y, void* stream) {
-  if (num_rows < 0 || h <= 0 || k <= 0 || k > 36) return MM_ERR_INVALID_ARG;
+                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, const void* shared_rows,
+                         int64_t n_shared, void* y, void* stream) {
+  if (num_rows < 0 || h <= 0 || k <= 0 || n_shared < 0 || n_shared > 4 || k + n_shared > 36)
+    return MM_ERR_INVALID_ARG;
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
   if (h % 8 != 0) return MM_ERR_UNSUPPORTED;
   if (num_rows == 0) return MM_OK;
   if (!expert_rows || !row_idx || !topk_weights || !y || !aligned16(expert_rows) || !aligned16(y))
     return MM_ERR_INVALID_ARG;
+  if (n_shared > 0 && (!shared_rows || !aligned16(shared_rows))) return MM_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   StageScope sc(MM_STAGE_COMBINE, st);
-  const cudaError_t e =
-      launch_combine_rows(static_cast<const __nv_bfloat16*>(expert_rows), row_idx, topk_weights,
-                          topk_weights_dtype == MM_DT_BFLOAT16, num_rows, h, (int)k, static_cast<__nv_bfloat16*>(y), st);
+  const cudaError_t e = launch_combine_rows(
+      static_cast<const __nv_bfloat16*>(expert_rows), row_idx, topk_weights, topk_weights_dtype == MM_DT_BFLOAT16,
+      num_rows, h, (int)k, static_cast<const __nv_bfloat16*>(shared_rows), (int)n_shared,
+      static_cast<__nv_bfloat16*>(y), st);
   sc.finish(1);
   return cuda_status(e);
 }

@@ -28,8 +28,12 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
                                  : static_cast<const float*>(a.gate)[j];
   } else if (threadIdx.x < nterm) {
     const int s = threadIdx.x - a.k;
-    const int64_t r = (int64_t)a.seg_mprefix[a.n_routed + s] * kBM + i;
-    rows[threadIdx.x] = in_bounds(r >= 0 && r < a.rows_cap, a.dev_err) ? (int32_t)r : -1;
+    if (a.o_sh) {
+      rows[threadIdx.x] = (int32_t)((int64_t)s * a.n + i);  // the caller's [n_shared, n, h] rows
+    } else {
+      const int64_t r = (int64_t)a.seg_mprefix[a.n_routed + s] * kBM + i;
+      rows[threadIdx.x] = in_bounds(r >= 0 && r < a.rows_cap, a.dev_err) ? (int32_t)r : -1;
+    }
     w[threadIdx.x] = 1.0f;
   }
   __syncthreads();
@@ -44,7 +48,8 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int32_t r = t0 + b < nterm ? rows[t0 + b] : -1;
-        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.o + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
+        const __nv_bfloat16* src = (t0 + b >= a.k && a.o_sh) ? a.o_sh : a.o;
+        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
@@ -72,13 +77,15 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
 }  // namespace
 
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
-                                int64_t n, int64_t h, int k, __nv_bfloat16* y, cudaStream_t st) {
+                                int64_t n, int64_t h, int k, const __nv_bfloat16* shared_rows, int n_shared,
+                                __nv_bfloat16* y, cudaStream_t st) {
   CombineArgs a;
   a.o = rows;
+  a.o_sh = n_shared > 0 ? shared_rows : nullptr;
   a.pad_row = row_idx;
   a.gate = gate;
   a.gate_bf16 = gate_bf16;
-  a.n_shared = 0;
+  a.n_shared = n_shared;
   a.seg_mprefix = nullptr;
   a.n_routed = 0;
   a.n = n;

@@ -82,7 +82,8 @@ void set_route_path(int path);
 // Y[i] = sum_k W[i,k] * rows[row_idx[i*K + k]] (row_idx < 0: term left out),
 // fp32 in k order, one bf16 rounding (MegaMoE stage 4 / EP combine).
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
-                                int64_t n, int64_t h, int k, __nv_bfloat16* y, cudaStream_t st);
+                                int64_t n, int64_t h, int k, const __nv_bfloat16* shared_rows, int n_shared,
+                                __nv_bfloat16* y, cudaStream_t st);
 
 // ---- permute / quantise (permute.cu) -------------------------------------
 struct PermuteArgs {
@@ -150,6 +151,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
 // ---- combine (combine.cu) --------------------------------------------------
 struct CombineArgs {
   const __nv_bfloat16* o;     // [rows_cap, h] expert outputs (padded grouped layout)
+  const __nv_bfloat16* o_sh;  // optional [n_shared, n, h] shared-expert rows (else in o at their segments)
   const int32_t* pad_row;     // [n*k]
   const void* gate;           // [n, k] fp32 or bf16
   int gate_bf16;

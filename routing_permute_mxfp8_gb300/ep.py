@@ -13,11 +13,14 @@ the experts [r*E/W, (r+1)*E/W):
   stage 4  the O rows go back to their source ranks in the order they came
            (the reverse all-to-all), where mm_moe_combine forms
            Y[i] = sum_k W[i,k] O[pi(i,k)] in fp32 and rounds once to bf16.
+Shared experts take part in no exchange: each rank runs them on its own
+tokens (quantised in the shared experts' input type, through the expert-side
+entry point with one local expert) and the combine adds their rows after the
+K routed terms, as the single-GPU step does.
 Every step on the data runs in the library's kernels; this module only
 allocates buffers and calls the collectives.  With the NCCL backend the
 exchanges run on device memory; with gloo (which exchanges host memory) the
-buffers are staged through the host.  Shared experts are not part of this
-path (each rank would run them on its own tokens with mm_mega_moe).
+buffers are staged through the host.
 """
 from __future__ import annotations
 
@@ -45,13 +48,16 @@ def _a2a_rows(send, send_counts, recv_counts, group):
 def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2, moe_expert_num: int, *,
                 group=None, weight_dtype: int = _mm.DT_FP8_E4M3FN, weight_scale_layout: int = _mm.WSCALE_ROWS,
                 dispatch_quant_out_dtype: int = _mm.DT_FP8_E4M3FN, activation: str = "swiglu",
-                activation_params=(), dev_err=None):
+                activation_params=(), dev_err=None, shared_weight1=None, shared_weight2=None,
+                shared_weight_scales1=None, shared_weight_scales2=None, shared_weight_dtype=None,
+                shared_expert_quant_out_dtype=None):
     """MegaMoE forward of this rank's tokens with expert parallelism.
 
     x [N, H] bf16, topk_ids [N, K] int32 (global expert ids), topk_weights [N, K]
     fp32 / bf16 of this rank; weight1 / weight2 / their scales hold this rank's
-    E/W local experts in the layouts of mm_mega_moe.  Collective: every rank of
-    `group` calls it.  Returns y [N, H] bf16.
+    E/W local experts in the layouts of mm_mega_moe; shared_weight* hold the
+    shared experts (every rank holds all of them, [S, ...] as in mm_mega_moe).
+    Collective: every rank of `group` calls it.  Returns y [N, H] bf16.
     """
     world = dist.get_world_size(group)
     if moe_expert_num % world != 0:
@@ -86,4 +92,30 @@ def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
     back = _a2a_rows(o_rows, recv_counts, send_counts, group)
     if n == 0:
         return torch.empty((0, h), dtype=torch.bfloat16, device=x.device)
-    return _mm.mm_moe_combine(back, exp_idx, topk_weights)
+    shared = None
+    if shared_weight1 is not None and shared_weight1.shape[0] > 0:
+        shared = _shared_rows(x, shared_weight1, shared_weight2, shared_weight_scales1, shared_weight_scales2,
+                              weight_dtype if shared_weight_dtype is None else shared_weight_dtype,
+                              dispatch_quant_out_dtype if shared_expert_quant_out_dtype is None
+                              else shared_expert_quant_out_dtype,
+                              weight_scale_layout, activation, activation_params, dev_err)
+    return _mm.mm_moe_combine(back, exp_idx, topk_weights, shared_rows=shared)
+
+
+def _shared_rows(x, w1, w2, s1, s2, w_dtype, x_dtype, layout, activation, activation_params, dev_err):
+    """[S, N, H] bf16: every shared expert's output for this rank's tokens (the
+    tokens MX-quantised in the shared experts' input type, then the expert side
+    with one local expert)."""
+    n, h = x.shape
+    xq, xs = _mm.mm_mx_quantize(x, x_dtype, scale_cols=h // 32)
+    ids = torch.zeros(n, dtype=torch.int32, device=x.device)
+    out = torch.empty((w1.shape[0], n, h), dtype=torch.bfloat16, device=x.device)
+    S = w1.shape[0]
+    # one expert's scales: a [1, ...] slice of the pages' layout, or one
+    # expert's equal share of a prepared buffer
+    one = (lambda t, s: t[s:s + 1]) if layout == _mm.WSCALE_ROWS else (lambda t, s: t.reshape(S, -1)[s])
+    for s in range(S):
+        _mm.mm_moe_expert_ffn(xq, xs, ids, w1[s:s + 1], w2[s:s + 1], one(s1, s), one(s2, s), 1, x_dtype=x_dtype,
+                              weight_dtype=w_dtype, weight_scale_layout=layout, activation=activation,
+                              activation_params=activation_params, out=out[s], dev_err=dev_err)
+    return out

@@ -30,10 +30,11 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _cfg(a4w4=False):
+def _cfg(a4w4=False, shared=0):
     import synth
     # 2 ranks x 4 experts; Zipf routing so the two ranks receive unequal row counts
-    cfg = synth.CONFIGS["tiny"].scaled(n=96, e=8, k=3, routing="zipf", dispatch_fmt=23, gate_dtype="bf16")
+    cfg = synth.CONFIGS["tiny"].scaled(n=96, e=8, k=3, routing="zipf", dispatch_fmt=23, gate_dtype="bf16",
+                                       shared=shared)
     # A4W4-FP: MXFP4 rows exchanged (packed, H/2 bytes a row), FP4 weights
     return cfg.scaled(weight_fmt=296, dispatch_fmt=296) if a4w4 else cfg
 
@@ -43,16 +44,25 @@ def _pack_fp4(c):
     return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
 
 
-def _problem(a4w4=False):
+def _problem(a4w4=False, shared=0):
     import oracle
     import synth
-    cfg = _cfg(a4w4)
+    cfg = _cfg(a4w4, shared)
     x = synth.tokens_bf16(cfg)
     ids = synth.topk_ids(cfg)
     gate = synth.topk_weights(cfg)
     w1, s1 = oracle.quantized_weights(cfg, 1)
     w2, s2 = oracle.quantized_weights(cfg, 2)
     return cfg, x, ids, gate, (w1, s1, w2, s2)
+
+
+def _shared(cfg):
+    import oracle
+    if not cfg.shared:
+        return None
+    sw1, ss1 = oracle.quantized_weights(cfg, 1, shared=True)
+    sw2, ss2 = oracle.quantized_weights(cfg, 2, shared=True)
+    return sw1, ss1, sw2, ss2
 
 
 def _oracle_fakes(mm, cfg):
@@ -79,12 +89,20 @@ def _oracle_fakes(mm, cfg):
                                        x_prequant=(xq.numpy(), x_scales.numpy()))
         return (torch.from_numpy(yb.view(np.int16)).view(torch.bfloat16),)
 
-    def expert_ffn(xq, xs, eids, w1, w2, s1, s2, e, *, x_dtype=None, **kw):
+    def expert_ffn(xq, xs, eids, w1, w2, s1, s2, e, *, x_dtype=None, out=None, **kw):
         m = xq.shape[0]
-        return mega(xq, eids.view(m, 1), torch.ones((m, 1)), w1, w2, s1, s2, e, x_scales=xs,
-                    dispatch_quant_out_dtype=x_dtype, dispatch_quant_mode=0)[0], None
+        y = mega(xq, eids.view(m, 1), torch.ones((m, 1)), w1, w2, s1, s2, e, x_scales=xs,
+                 dispatch_quant_out_dtype=x_dtype, dispatch_quant_mode=0)[0]
+        if out is not None:
+            out.copy_(y)
+        return y, None
 
-    def combine(rows, idx, gate, out=None):
+    def mx_quantize(src, out_dtype, scale_cols=None):
+        q, sc = oracle.mx_quantize(src.view(torch.int16).numpy().view(np.uint16), oracle.DT_BF16, out_dtype,
+                                   s_cols=scale_cols)
+        return torch.from_numpy(q), torch.from_numpy(np.ascontiguousarray(sc))
+
+    def combine(rows, idx, gate, out=None, shared_rows=None):
         r = rows.float().numpy()
         g = gate.float().numpy()
         n, k = g.shape
@@ -93,11 +111,15 @@ def _oracle_fakes(mm, cfg):
         for kk in range(k):
             ok = ix[:, kk] >= 0
             acc[ok] += g[ok, kk:kk + 1] * r[ix[ok, kk]]
+        if shared_rows is not None:
+            for s in range(shared_rows.shape[0]):
+                acc += shared_rows[s].float().numpy()
         return torch.from_numpy(acc).to(torch.bfloat16)
 
     mm.mm_moe_ep_dispatch = dispatch
     mm.mm_mega_moe = mega
     mm.mm_moe_expert_ffn = expert_ffn
+    mm.mm_mx_quantize = mx_quantize
     mm.mm_moe_combine = combine
 
 
@@ -106,14 +128,15 @@ def _slices(cfg, rank):
     return slice(rank * per, (rank + 1) * per)
 
 
-def _cpu_rank(rank, port, out):
+def _cpu_rank(rank, port, out, shared):
     import sys
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import torch.distributed as dist
     import routing_permute_mxfp8_gb300 as mm
     from routing_permute_mxfp8_gb300 import ep
-    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem()
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem(shared=shared)
+    sh = _shared(cfg)
     _oracle_fakes(mm, cfg)
     dist.init_process_group("gloo", rank=rank, world_size=W)
     sl = _slices(cfg, rank)
@@ -122,13 +145,17 @@ def _cpu_rank(rank, port, out):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
     xt = t(x[sl].view(np.int16)).view(torch.bfloat16)
     gt = t(gate[sl].view(np.int16)).view(torch.bfloat16)
+    skw = {} if sh is None else dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]),
+                                     shared_weight2=t(sh[2]), shared_weight_scales2=t(sh[3]))
     y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
-                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt)
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, **skw)
     # the same fakes on one rank, no exchange: every expert local
     sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(xt, t(ids[sl]), cfg.e, 1, cfg.dispatch_fmt)
     o = mm.mm_mega_moe(sx, se.view(-1, 1), torch.ones((sx.shape[0], 1)), t(w1), t(w2), t(s1), t(s2), cfg.e,
                        x_scales=ss, dispatch_quant_mode=0, dispatch_quant_out_dtype=cfg.dispatch_fmt)[0]
-    y1 = mm.mm_moe_combine(o, ei, gt)
+    shr = None if sh is None else ep._shared_rows(xt, t(sh[0]), t(sh[2]), t(sh[1]), t(sh[3]), cfg.weight_fmt,
+                                                 cfg.dispatch_fmt, mm.WSCALE_ROWS, "swiglu", (), None)
+    y1 = mm.mm_moe_combine(o, ei, gt, shared_rows=shr)
     out[rank] = (y.view(torch.int16).numpy().copy(), y1.view(torch.int16).numpy().copy())
     dist.barrier()
     dist.destroy_process_group()
@@ -138,18 +165,20 @@ def _check_against_oracle(cfg, x, ids, gate, w, y_bits):
     import oracle
     import synth
     w1, s1, w2, s2 = w
-    y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt)
+    y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt,
+                                      shared=_shared(cfg))
     yg = synth.bf16_bits_to_f32(y_bits.view(np.uint16)).astype(np.float64)
     rel = np.linalg.norm(yg - y_ref) / np.linalg.norm(y_ref)
     mx = np.abs(yg - y_ref).max() / np.abs(y_ref).max()
     assert rel <= 5e-3 and mx <= 2e-2, (rel, mx)
 
 
-def test_ep_exchange_two_gloo_ranks_cpu():
+@pytest.mark.parametrize("shared", [0, 1])
+def test_ep_exchange_two_gloo_ranks_cpu(shared):
     port = _free_port()
     out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
-    mp.spawn(_cpu_rank, args=(port, out), nprocs=W, join=True)
-    cfg, x, ids, gate, w = _problem()
+    mp.spawn(_cpu_rank, args=(port, out, shared), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem(shared=shared)
     ys = []
     for r in range(W):
         y, y1 = out[r]
@@ -158,7 +187,7 @@ def test_ep_exchange_two_gloo_ranks_cpu():
     _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))
 
 
-def _gpu_rank(rank, port, out, a4w4):
+def _gpu_rank(rank, port, out, a4w4, shared):
     import sys
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -166,9 +195,12 @@ def _gpu_rank(rank, port, out, a4w4):
     import routing_permute_mxfp8_gb300 as mm
     from routing_permute_mxfp8_gb300 import ep
     torch.cuda.set_device(0)
-    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem(a4w4)
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem(a4w4, shared)
+    sh = _shared(cfg)
     if cfg.weight_fmt == 296:
         w1, w2 = _pack_fp4(w1), _pack_fp4(w2)
+        if sh is not None:
+            sh = (_pack_fp4(sh[0]), sh[1], _pack_fp4(sh[2]), sh[3])
     dist.init_process_group("gloo", rank=rank, world_size=W)
     sl = _slices(cfg, rank)
     el = cfg.e // W
@@ -177,11 +209,13 @@ def _gpu_rank(rank, port, out, a4w4):
     xt = t(x[sl].view(np.int16)).view(torch.bfloat16)
     gt = t(gate[sl].view(np.int16)).view(torch.bfloat16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    skw = {} if sh is None else dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]),
+                                     shared_weight2=t(sh[2]), shared_weight_scales2=t(sh[3]))
     y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
-                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err)
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err, **skw)
     # single process, all experts on this GPU (ep_world_size = 1)
     y1 = mm.mm_mega_moe(xt, t(ids[sl]), gt, t(w1), t(w2), t(s1), t(s2), cfg.e, weight_dtype=cfg.weight_fmt,
-                        dispatch_quant_out_dtype=cfg.dispatch_fmt)[0]
+                        dispatch_quant_out_dtype=cfg.dispatch_fmt, **skw)[0]
     torch.cuda.synchronize()
     out[rank] = (y.view(torch.int16).cpu().numpy(), y1.view(torch.int16).cpu().numpy(), int(err.item()))
     dist.barrier()
@@ -189,12 +223,13 @@ def _gpu_rank(rank, port, out, a4w4):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("a4w4", [False, True], ids=["a8w8", "a4w4"])
-def test_ep_two_ranks_on_one_gpu_matches_single_process(a4w4):
+@pytest.mark.parametrize("a4w4,shared", [(False, 0), (True, 0), (False, 2), (True, 1)],
+                         ids=["a8w8", "a4w4", "a8w8_shared2", "a4w4_shared1"])
+def test_ep_two_ranks_on_one_gpu_matches_single_process(a4w4, shared):
     port = _free_port()
     out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
-    mp.spawn(_gpu_rank, args=(port, out, a4w4), nprocs=W, join=True)
-    cfg, x, ids, gate, w = _problem(a4w4)
+    mp.spawn(_gpu_rank, args=(port, out, a4w4, shared), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem(a4w4, shared)
     ys = []
     for r in range(W):
         y, y1, err = out[r]

@@ -60,11 +60,12 @@ def test_permute_expert_parallel_and_combine_checked():
     P.test_token_permute_bit_exact(torch.float16, True, -7, 9, False)
     P.test_ep_dispatch_bit_exact(4, 24)
     P.test_ep_dispatch_bit_exact(4, 296)
-
-
-def test_shared_quant_type_checked():
-    P.test_mega_moe_shared_quant_type(296, 296, 24, 24, "swiglu")
-    P.test_mega_moe_shared_quant_type(23, 23, 24, 24, "swiglu")
-    P.test_moe_combine_rows(True)
+    P.test_moe_combine_rows(True, 2)
     P.test_out_of_range_ids_are_left_out_and_flagged()
     P.test_expert_ffn_equals_mega_moe_top1(dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"))
+
+
+def test_shared_quant_type_and_active_range_checked():
+    P.test_mega_moe_shared_quant_type(296, 296, 24, 24, "swiglu")
+    P.test_mega_moe_shared_quant_type(23, 23, 24, 24, "swiglu")
+    P.test_init_routing_active_range(*P.RANGE_CASES[2])

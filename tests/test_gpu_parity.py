@@ -915,11 +915,12 @@ def test_expert_ffn_full_size_equals_mega_moe_top1():
     assert np.array_equal(host(out), host(y))
 
 
-@pytest.mark.parametrize("gate_bf16", [False, True])
-def test_moe_combine_rows(gate_bf16):
+@pytest.mark.parametrize("gate_bf16,n_shared", [(False, 0), (True, 0), (False, 2), (True, 4)])
+def test_moe_combine_rows(gate_bf16, n_shared):
     """mm_moe_combine: fp32 sum in k order of weighted rows chosen by an index
-    (negative: left out), one bf16 rounding -- MegaMoE stage 4."""
-    rng = np.random.default_rng(5)
+    (negative: left out), then the shared experts' rows, one bf16 rounding --
+    MegaMoE stage 4."""
+    rng = np.random.default_rng(5 + n_shared)
     n, k, h, nrows = 200, 6, 384, 900
     rows = rng.standard_normal((nrows, h)).astype(np.float32)
     rows_b = torch.from_numpy(rows).to(torch.bfloat16)
@@ -928,7 +929,9 @@ def test_moe_combine_rows(gate_bf16):
     gt = torch.from_numpy(g)
     if gate_bf16:
         gt = gt.to(torch.bfloat16)
-    y = mm.mm_moe_combine(rows_b.to(DEV), torch.from_numpy(idx).to(DEV), gt.to(DEV))
+    sh_b = torch.from_numpy(rng.standard_normal((n_shared, n, h)).astype(np.float32)).to(torch.bfloat16)
+    y = mm.mm_moe_combine(rows_b.to(DEV), torch.from_numpy(idx).to(DEV), gt.to(DEV),
+                          shared_rows=sh_b.to(DEV) if n_shared else None)
     r = rows_b.float().numpy()
     gw = gt.float().numpy()
     acc = np.zeros((n, h), np.float32)
@@ -937,5 +940,7 @@ def test_moe_combine_rows(gate_bf16):
         ok = ix[:, kk] >= 0
         # a fused multiply-add: the fp32 product is exact in float64, one rounding to fp32
         acc[ok] = (gw[ok, kk:kk + 1].astype(np.float64) * r[ix[ok, kk]] + acc[ok]).astype(np.float32)
+    for s in range(n_shared):   # weight 1: a plain fp32 addition
+        acc = (acc.astype(np.float64) + sh_b[s].float().numpy()).astype(np.float32)
     want = torch.from_numpy(acc).to(torch.bfloat16)
     assert torch.equal(y.cpu(), want)
