@@ -13,6 +13,8 @@ constexpr int kThreads = 128;
 constexpr int kMaxTerms = 36;  // top-K <= 32 plus up to 4 shared experts
 constexpr int kBatch = 8;      // expert rows gathered per round
 
+// kSep: the shared experts' rows come from the caller's o_sh, not from o
+template <bool kSep>
 __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
   __shared__ int32_t rows[kMaxTerms];
   __shared__ float w[kMaxTerms];
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
                                  : static_cast<const float*>(a.gate)[j];
   } else if (threadIdx.x < nterm) {
     const int s = threadIdx.x - a.k;
-    if (a.o_sh) {
+    if (kSep) {
       rows[threadIdx.x] = (int32_t)((int64_t)s * a.n + i);  // the caller's [n_shared, n, h] rows
     } else {
       const int64_t r = (int64_t)a.seg_mprefix[a.n_routed + s] * kBM + i;
@@ -48,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int32_t r = t0 + b < nterm ? rows[t0 + b] : -1;
-        const __nv_bfloat16* src = (t0 + b >= a.k && a.o_sh) ? a.o_sh : a.o;
+        const __nv_bfloat16* src = kSep && t0 + b >= a.k ? a.o_sh : a.o;
         v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -99,7 +101,8 @@ cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_id
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
-  return launch_pdl(k_combine, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
+  if (a.o_sh && a.n_shared > 0) return launch_pdl(k_combine<true>, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
+  return launch_pdl(k_combine<false>, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace mm

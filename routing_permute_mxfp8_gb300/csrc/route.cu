@@ -66,6 +66,8 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
   const int64_t end = start + chunk < rows ? start + chunk : rows;
   bool bad = false;
   const int64_t id_end = (int64_t)num_experts * km.div;
+  // the key is the id itself, and every id without a key is an error
+  const bool plain = km.div == 1 && km.off == 0 && km.limit == num_experts;
   // kIdBatch 32-id steps per round: their loads are all in flight before
   // the first is counted (preloaded: the caller has loaded the first round)
   for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
@@ -73,18 +75,18 @@ __device__ __forceinline__ void route_count_warp(const IdT* __restrict__ ids, in
 #pragma unroll
     for (int b = 0; b < kIdBatch; ++b) {
       if (j0 + 32 * b + lane >= end) break;
-      if (km.div == 1) {
+      if (plain) {
         using UIdT = typename std::make_unsigned<IdT>::type;
-        const UIdT kv = (UIdT)v[b] - (UIdT)km.off;
-        if (kv < (UIdT)num_experts)
-          atomicAdd(&cnt[(int)kv], 1);
-        else if ((UIdT)v[b] >= (UIdT)km.limit)
+        if ((UIdT)v[b] < (UIdT)num_experts)
+          atomicAdd(&cnt[(int)v[b]], 1);
+        else
           bad = true;
       } else {
         const int64_t id = (int64_t)v[b];
-        if (id >= 0 && id < id_end)
-          atomicAdd(&cnt[id / km.div], 1);
-        else
+        const int64_t kk = id - km.off;
+        if (kk >= 0 && kk < id_end)
+          atomicAdd(&cnt[kk / km.div], 1);
+        else if (id < 0 || id >= km.limit)
           bad = true;
       }
     }
@@ -273,6 +275,8 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
   const int key_bits = 32 - __clz(num_experts);  // bits of the largest key + 1
   using UIdT = typename std::make_unsigned<IdT>::type;
   const int64_t id_end = (int64_t)num_experts * km.div;
+  // the key is the id itself, and every id without a key is an error
+  const bool plain = km.div == 1 && km.off == 0 && km.limit == num_experts;
   for (int64_t j0 = start; j0 < end; j0 += 32 * kIdBatch) {
     // the next kIdBatch steps' ids, loaded together (preloaded: the caller
     // has loaded the first round)
@@ -285,14 +289,13 @@ __device__ __forceinline__ void route_scatter_walk(const IdT* __restrict__ ids, 
       const bool in = j < end;
       int key = -1, rem = 0;
       if (in) {
-        if (km.div == 1) {
-          const UIdT kv = (UIdT)v[b] - (UIdT)km.off;
-          if (kv < (UIdT)num_experts) key = (int)kv;
+        if (plain) {
+          if ((UIdT)v[b] < (UIdT)num_experts) key = (int)v[b];
         } else {
-          const int64_t id = (int64_t)v[b];
-          if (id >= 0 && id < id_end) {
-            key = (int)(id / km.div);
-            rem = (int)(id - (int64_t)key * km.div);
+          const int64_t kk = (int64_t)v[b] - km.off;
+          if (kk >= 0 && kk < id_end) {
+            key = (int)(kk / km.div);
+            rem = (int)(kk - (int64_t)key * km.div);
           }
         }
       }
