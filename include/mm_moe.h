@@ -100,7 +100,7 @@ int mm_version(void);
 
 /* ------------------------------------------------------------------------
  * mm_moe_init_routing -- MoeInitRoutingV3, Dropless, active expert range
- * [0, expert_num), quantMode -1 / 2 / 3 (another range, and the key_value
+ * [0, expert_num), quantMode -1 / 2 / 3 / 9 (another range, and the key_value
  * count type: mm_moe_init_routing_v3 below).
  *
  *   sortedRowIdx          = keyValueSort(expertIdx, rowIdx)      (step 1)
@@ -114,13 +114,15 @@ int mm_version(void);
  *                   modes take bf16 or fp16).  Row size in bytes must be a
  *                   multiple of 16.
  * expert_idx        [num_rows, k] int32, values in [0, expert_num).
- * quant_mode        MM_QUANT_NONE (expanded_x has x's type) or an MXFP8 mode
- *                   (expanded_x FP8, h a multiple of 16).
+ * quant_mode        MM_QUANT_NONE (expanded_x has x's type), an MXFP8 mode
+ *                   (expanded_x FP8, h a multiple of 16), or MM_QUANT_MXFP4_E2M1
+ *                   (quantMode 9: expanded_x [num_rows*k, h/2] packed E2M1, two
+ *                   codes per byte, element 2i in bits 0-3).
  * expert_tokens_num_type  0: expert_tokens is the inclusive cumsum of the
  *                   counts; 1: the counts (expertTokensNumType 0 / 1).
  * expanded_x        [num_rows*k, h] output.
  * expanded_scale    [num_rows*k, AlignUp(CeilDiv(h, 32), 2)] E8M0 output in
- *                   MXFP8 modes (padding column 0); ignored otherwise.
+ *                   the MX modes (padding column 0); ignored otherwise.
  * expanded_row_idx  [num_rows*k] int32 scatter index (rowIdxType 1), or NULL.
  * sorted_row_idx    [num_rows*k] int32 gather index (rowIdxType 0), or NULL.
  * expert_tokens     [expert_num] int64, or NULL.  With num_rows = 0 only

@@ -186,7 +186,7 @@ def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_
     rows = n * k
     dev = x.device
     out_dt = x.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
-    expanded_x = torch.empty((rows, h), dtype=out_dt, device=dev)
+    expanded_x = torch.empty((rows, h // 2 if quant_mode == QUANT_MXFP4_E2M1 else h), dtype=out_dt, device=dev)
     scale = (torch.empty((rows, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
              else torch.empty((0,), dtype=torch.uint8, device=dev))
     exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)
@@ -557,7 +557,7 @@ def mm_moe_init_routing_noalloc(x, expert_idx, expert_num: int, quant_mode: int 
     rows = n * k
     dev = x.device
     out_dt = x.dtype if quant_mode == QUANT_NONE else _FP8_TORCH.get(_QUANT_FMT.get(quant_mode), torch.uint8)
-    expanded_x = torch.empty((rows, h), dtype=out_dt, device=dev)
+    expanded_x = torch.empty((rows, h // 2 if quant_mode == QUANT_MXFP4_E2M1 else h), dtype=out_dt, device=dev)
     scale = (torch.empty((rows, _scale_cols(h)), dtype=torch.uint8, device=dev) if quant_mode != QUANT_NONE
              else torch.empty((0,), dtype=torch.uint8, device=dev))
     exp_idx = torch.empty(rows, dtype=torch.int32, device=dev)

@@ -187,7 +187,9 @@ mm_status validate_init_routing(const void* x, int x_dtype, const int32_t* exper
   if (num_rows < 0 || k <= 0 || expert_num <= 0 || expert_num > 10240) return MM_ERR_INVALID_ARG;
   if (num_rows * k >= kSortLimit) return MM_ERR_INVALID_ARG;
   if (h <= 0 || !is_src_dtype(x_dtype)) return MM_ERR_INVALID_ARG;
-  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN)
+  // quantMode -1, 2 / 3 (MXFP8) and 9 (MXFP4 E2M1, two codes per byte)
+  if (quant_mode != MM_QUANT_NONE && quant_mode != MM_QUANT_MXFP8_E5M2 && quant_mode != MM_QUANT_MXFP8_E4M3FN &&
+      quant_mode != MM_QUANT_MXFP4_E2M1)
     return MM_ERR_UNSUPPORTED;
   if (expert_tokens_num_type != 0 && expert_tokens_num_type != 1) return MM_ERR_UNSUPPORTED;
   const bool quant = quant_mode != MM_QUANT_NONE;

@@ -65,6 +65,8 @@ ROUTE_CASES = [
     (16385, 32, 256, 8, 2, "any"),
     (300, 32, 4096, 12, -1, "distinct"),
     (300, 32, 4097, 12, 3, "distinct"),
+    (16384, 7168, 256, 8, 9, "distinct"),        # full routing workload, MXFP4 E2M1 (V3 quantMode 9)
+    (333, 160, 300, 7, 9, "any"),                # MXFP4, ragged H
 ]
 
 
@@ -79,7 +81,7 @@ def _random_route_case(seed):
     rng = np.random.default_rng(2000 + seed)
     e = int(rng.integers(1, 600))
     return (int(rng.integers(1, 5000)), 16 * int(rng.integers(1, 80)), e, int(rng.integers(1, min(e, 16) + 1)),
-            int(rng.choice([-1, 2, 3])), str(rng.choice(["distinct", "any"])))
+            int(rng.choice([-1, 2, 3, 9])), str(rng.choice(["distinct", "any"])))
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -100,9 +102,9 @@ def test_init_routing_bit_exact(n, h, e, k, quant, kind):
         assert np.array_equal(host(srt), r_srt)
         assert np.array_equal(host(exp_idx), r_exp)
         assert np.array_equal(host(tok), np.cumsum(r_cnt) if ttype == 0 else r_cnt)
-    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    fmt = {-1: -1, 2: 23, 3: 24, 9: 296}[quant]
     r_out, r_sc = oracle.permute(x, oracle.DT_BF16, k, r_srt, n * k, fmt=fmt)
-    assert np.array_equal(host(ex), r_out)
+    assert np.array_equal(host(ex), pack_fp4(r_out) if fmt == 296 else r_out)
     if quant != -1:
         assert np.array_equal(host(sc), r_sc)
 
@@ -116,6 +118,7 @@ RANGE_CASES = [
     (4096, 256, 256, 8, 32, 64, 2, True),       # an eighth of the experts; ids -1 and E mixed in
     (70000, 128, 512, 2, 0, 300, 3, False),     # above the cluster kernel's range
     (513, 384, 8, 8, 0, 8, -1, True),           # the full range through the v3 entry point
+    (700, 256, 32, 4, 8, 24, 9, True),          # MXFP4 rows
 ]
 
 
@@ -131,8 +134,10 @@ def test_init_routing_active_range(n, h, e, k, start, end, quant, bad):
         ids[1, 0], ids[n // 2, k - 1] = -1, e
     r_srt, r_exp, r_cnt, r_bad = oracle.route_range(ids, e, start, end)
     avail = int(((ids >= start) & (ids < end)).sum())
-    fmt = {-1: -1, 2: 23, 3: 24}[quant]
+    fmt = {-1: -1, 2: 23, 3: 24, 9: 296}[quant]
     r_out, r_sc = oracle.permute(x, oracle.DT_BF16, k, r_srt, avail, fmt=fmt)
+    if fmt == 296:
+        r_out = pack_fp4(r_out)
     for ttype in (0, 1, 2):
         err = zeros_err()
         ex, exp_idx, tok, sc, srt = mm.mm_moe_init_routing(bf16(x), t(ids), e, quant, ttype,
@@ -162,7 +167,7 @@ def route_path(request):
 
 
 @pytest.mark.parametrize("route_path", list(ROUTE_PATHS), indirect=True)
-@pytest.mark.parametrize("case", [ROUTE_CASES[i] for i in (1, 3, 4, 5, 6, 8, 10, 12)])
+@pytest.mark.parametrize("case", [ROUTE_CASES[i] for i in (1, 3, 4, 5, 6, 8, 10, 12, 15)])
 def test_init_routing_every_path(route_path, case):
     """The cluster kernel, the cooperative grid launch and the four kernels
     give the oracle's bits (E up to 2048, ragged chunks, repeated ids)."""
