@@ -1,4 +1,5 @@
-// Combine (MegaMoE README, A8W8-FP stage 4 at epWorldSize = 1):
+// Combine (MegaMoE README, A8W8-FP stage 4; at epWorldSize = 1 and, on the
+// source rank, with expert parallelism):
 //   Y[i] = sum_k W[i,k] * O[pi(i,k)] + sum_s O_s^shared[i]
 // One block per token.  The expert rows are gathered with 16-byte loads
 // (eight rows in flight per thread), accumulated in fp32 in the order

@@ -1,4 +1,4 @@
-// Grouped block-scaled FP8 GEMMs of the expert FFN on tcgen05 (sm_103a).
+// Grouped block-scaled FP8 / FP4 GEMMs of the expert FFN on tcgen05 (sm_103a).
 //
 // MegaMoE README, A8W8-FP scenario:
 //   stage 2  G_e, U_e = DQ_MX(X_hat_e) . DQ_MX(W1_e^(G|U))   then
@@ -8,7 +8,11 @@
 //   stage 3  O_e = DQ_MX(A_hat_e) . DQ_MX(W2_e)
 // DQ_MX happens inside the MMA: tcgen05.mma kind::mxf8f6f4 with one E8M0
 // scale per 32 k for every row of A and of B (scale_vec::1X).  Weights are
-// FP8 (A8W8-FP) or packed FP4 E2M1 (A8W4-FP), which TMA expands on load.
+// FP8 (A8W8-FP) or packed FP4 E2M1 (A8W4-FP), which TMA expands on load;
+// in the A4W4-FP scenario GEMM1's A (the dispatched tokens) is packed FP4
+// too and A_hat is MXFP8 E4M3.  Shared segments may have their own A type
+// and A_hat type (the shared experts' own input quantisation type): their
+// tiles use a second A tensor map, instruction descriptor and quantiser.
 //
 // Layout.  The expanded rows of every expert (and of each shared expert,
 // which sees all tokens) form a segment padded to a multiple of 128 rows,
@@ -32,7 +36,8 @@
 //   GEMM1: columns [0,128) are gate, [128,256) up, for the same 128
 //          intermediate columns -> swiglu -> one MX group per 32 columns,
 //          entirely within a thread; writes A_hat (FP8) and its scales
-//          directly in GEMM2's operand layouts.
+//          directly in GEMM2's operand layouts (the tile layout of the E8M0
+//          scales that the 32x128b scale copy reads).
 //   GEMM2: fp32 -> bf16 rows of O.
 // Output stores: each warp stages a 32-row x 64-byte block (GEMM1: 64
 // A_hat codes, GEMM2: 32 bf16) in shared memory (64B swizzle, no bank

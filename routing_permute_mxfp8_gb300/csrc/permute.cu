@@ -3,8 +3,9 @@
 //
 // moe_token_permute article, 功能说明 / 返回值说明, and MoeInitRoutingV3
 // step 5: output row d takes the source token of its flattened index; in
-// MXFP8 modes every group of 32 consecutive elements shares one E8M0
-// exponent (MegaMoE README, A8W8-FP stage 1, Q_MX).
+// the MX modes every group of 32 consecutive elements shares one E8M0
+// exponent (MegaMoE README, A8W8-FP stage 1, Q_MX), with FP8 E4M3 / E5M2
+// codes or packed FP4 E2M1 codes (A4W4-FP stage 1, quant_mode 9).
 //
 // The gather is turned around: one warp owns one source token (or a span of
 // its 512-column slices, when tokens are too few to fill the GPU), reads

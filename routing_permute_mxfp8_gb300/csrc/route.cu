@@ -4,8 +4,10 @@
 //   sortedExpertIdx, sortedRowIdx = keyValueSort(expertIdx, rowIdx)
 //   expandedRowIdx[sortedRowIdx[i]] = i
 //   expertTokensCountOrCumsum = Histogram(sortedExpertIdx)
-// The keys are expert ids in [0, E), so one counting pass replaces the two
-// sorts the permute article describes (sort, then argsort of the result):
+// The keys are expert ids in [0, E) (or their place in an active expert
+// range, activeExpertRangeOptional and step 6; or the destination rank of
+// expert parallelism), so one counting pass replaces the two sorts the
+// permute article describes (sort, then argsort of the result):
 //   1. k_route_hist     each warp counts the ids of its contiguous chunk
 //   2. k_route_scan_experts   one warp per expert scans its per-chunk counts
 //                       (exclusive prefix over chunks, in place) and totals
