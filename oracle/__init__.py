@@ -60,7 +60,7 @@ def _load():
     L.orc_expert_row.argtypes = [p, p, i32, p, p, p, p, i32, i64, i64, i32, i32, p, p, p, p]
     L.orc_expert_row.restype = None
     L.orc_mega_moe_tokens.argtypes = [p, p, p, i32, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
-                                      i32, i32, i32, p, i64, p, p, p, p, p, p, i32, p, i32]
+                                      i32, i32, i32, p, i64, p, p, p, p, p, p, i32, p, i32, i32]
     L.orc_mega_moe_tokens.restype = None
     L.orc_act_code.argtypes, L.orc_act_code.restype = [i32], i32
     _lib = L
@@ -252,7 +252,7 @@ def act_format(x_fmt: int) -> int:
 
 def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None,
                     shared=None, shared_w_fmt=None, want_act=False, activation="swiglu", act_params=(),
-                    x_prequant=None, shared_x_fmt=None):
+                    x_prequant=None, shared_x_fmt=None, combine_fmt=None):
     """MegaMoE forward at ep_world_size = 1 for selected tokens (A8W8-FP / A8W4-FP /
     A4W4-FP stages 1-4; x_fmt 296 dispatches MXFP4 E2M1 codes, one per byte).  x_prequant = (codes uint8[N, H], scales uint8[N, ceil(H/32)]):
     pre-quantised pass-through (dispatchQuantMode = 0): X_hat and S_X are the given
@@ -262,7 +262,9 @@ def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None
     w1 uint8[E, 2I, H], s1 uint8[E, 2I, 2*ceil(H/64)], w2 uint8[E, H, I],
     s2 uint8[E, H, 2*ceil(I/64)]; shared = (sw1, ss1, sw2, ss2) with a leading
     shared-expert dimension, or None; shared_x_fmt: the shared experts' own input
-    quantisation type (the parameter table's sharedExpertQuantOutDtype; None: x_fmt).
+    quantisation type (the parameter table's sharedExpertQuantOutDtype; None: x_fmt);
+    combine_fmt: 23 / 24 for combineQuantMode 3 / 4 (routed rows enter the sum as
+    DQ_MX(Q_MX(bf16(O)))), None: no combine quantisation.
     Returns (y float64[T, H], y_bf16 uint16[T, H]) and, with want_act, the
     activation codes uint8[T, K, I] (format act_format(x_fmt)) and scales uint8[T, K, I/32].
     """
@@ -300,7 +302,8 @@ def mega_moe_tokens(x_bf16, ids, gate, w1, s1, w2, s2, x_fmt, w_fmt, tokens=None
         _ptr(arrs[0]), _ptr(arrs[1]), _ptr(gate), gate_is_bf16, _ptr(arrs[2]), _ptr(arrs[3]),
         _ptr(arrs[4]), _ptr(arrs[5]), _ptr(sw[0]), _ptr(sw[1]), _ptr(sw[2]), _ptr(sw[3]), n_sh, h, k,
         e, inter, x_fmt, w_fmt, shared_w_fmt, _ptr(tokens), t, _ptr(y), _ptr(yb), _ptr(aq), _ptr(a_s),
-        _ptr(xq), _ptr(xs), kind, _ptr(p), -1 if shared_x_fmt is None else int(shared_x_fmt))
+        _ptr(xq), _ptr(xs), kind, _ptr(p), -1 if shared_x_fmt is None else int(shared_x_fmt),
+        -1 if combine_fmt is None else int(combine_fmt))
     if want_act:
         return y, yb, aq, a_s
     return y, yb

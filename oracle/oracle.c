@@ -443,6 +443,11 @@ int orc_act_code(int x_code) { return x_code == ORC_E2M1 ? ORC_E4M3 : x_code; }
  * Shared experts quantise their input in shared_x_code (the parameter
  * table's shared-expert quantisation type; < 0: the dispatch type), with
  * their activation in orc_act_code(shared_x_code).
+ * combine_code 23 / 24 (combineQuantMode 3 / 4, the quantisation of the
+ * combine communication between ranks): each routed expert row O, rounded
+ * to bf16 as it leaves GMM2, is sent as Q_MX codes in that type and enters
+ * the sum as DQ_MX of them; < 0: O as computed.  Shared-expert rows are
+ * local to the card and are not quantised.
  * ------------------------------------------------------------------------- */
 void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate, int gate_is_bf16,
                          const uint8_t* w1, const uint8_t* s1, const uint8_t* w2, const uint8_t* s2,
@@ -451,7 +456,8 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
                          int64_t num_experts, int64_t inter, int x_code, int w_code,
                          int shared_w_code, const int64_t* tokens, int64_t n_tok, double* y,
                          uint16_t* y_bf16, uint8_t* aq_out, uint8_t* as_out, const uint8_t* xq_in,
-                         const uint8_t* xs_in, int act, const double* act_p, int shared_x_code) {
+                         const uint8_t* xs_in, int act, const double* act_p, int shared_x_code,
+                         int combine_code) {
   int64_t aw = act_width(act, inter);
   int64_t s1_cols = 2 * ((h + 63) / 64), s2_cols = 2 * ((aw + 63) / 64);
   int64_t w1_sz = 2 * inter * h, w2_sz = h * aw;
@@ -466,6 +472,8 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
     uint8_t* xs = (uint8_t*)malloc((size_t)((h + 31) / 32));
     uint8_t* sxq = (uint8_t*)malloc((size_t)h);
     uint8_t* sxs = (uint8_t*)malloc((size_t)((h + 31) / 32));
+    uint8_t* cq = (uint8_t*)malloc((size_t)h);
+    uint8_t* cs = (uint8_t*)malloc((size_t)((h + 31) / 32));
     uint8_t* aq = (uint8_t*)malloc((size_t)aw);
     uint8_t* as = (uint8_t*)malloc((size_t)i_groups);
     double* o = (double*)malloc(sizeof(double) * (size_t)h);
@@ -484,6 +492,11 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
                               : (double)((const float*)gate)[i * k + kk];
       orc_expert_row(xq, xs, x_code, w1 + e * w1_sz, s1 + e * 2 * inter * s1_cols,
                      w2 + e * w2_sz, s2 + e * h * s2_cols, w_code, h, inter, a_code, act, act_p, aq, as, o);
+      if (combine_code >= 0) {  /* the row on the wire: Q_MX of its bf16 value, then DQ_MX */
+        for (int64_t c = 0; c < h; ++c) o[c] = orc_bf16_value(orc_bf16_round(o[c]));
+        orc_mx_quantize_rows(o, 1, h, combine_code, cq, cs, (h + 31) / 32);
+        dequant_row(cq, cs, h, combine_code, o);
+      }
       if (aq_out) memcpy(aq_out + (t * k + kk) * aw, aq, (size_t)aw);
       if (as_out) memcpy(as_out + (t * k + kk) * i_groups, as, (size_t)i_groups);
       for (int64_t c = 0; c < h; ++c) acc[c] += w * o[c];
@@ -503,6 +516,6 @@ void orc_mega_moe_tokens(const uint16_t* x, const int32_t* ids, const void* gate
       for (int64_t c = 0; c < h; ++c) acc[c] += o[c];
     }
     for (int64_t c = 0; c < h; ++c) y_bf16[t * h + c] = orc_bf16_round(acc[c]);
-    free(xq); free(xs); free(sxq); free(sxs); free(aq); free(as); free(o);
+    free(xq); free(xs); free(sxq); free(sxs); free(cq); free(cs); free(aq); free(as); free(o);
   }
 }

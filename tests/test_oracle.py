@@ -284,7 +284,7 @@ def test_permute_matches_gather(fmt):
 
 
 # ---------------------------------------------------------------- expert FFN
-def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None, shared_xfmt=None):
+def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None, shared_xfmt=None, combine_fmt=None):
     """Grouped-by-expert FFN with numpy matmuls on dequantised operands, from
     the MegaMoE A8W8-FP stage formulas; sort by numpy stable argsort.  The
     activation is re-quantised in the dispatch type, except in the A4W4-FP
@@ -322,6 +322,10 @@ def _numpy_grouped_moe(cfg, x, ids, gate, w, shared=None, shared_fmt=None, share
         if sel.size == 0:
             continue
         aq, o = ffn(xq[rows[sel]], xs[rows[sel]], w1[e], s1[e], w2[e], s2[e], cfg.weight_fmt)
+        if combine_fmt is not None:   # combineQuantMode: the bf16 row as MX codes on the wire
+            ob = torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+            oq, os_ = P.brute_mx_rows(ob, combine_fmt)
+            o = P.dequant_rows(oq, os_, combine_fmt)
         o_all[sel] = o
         aq_all[sel] = aq
     gw = P.bf16_bits_to_f64(gate) if gate.dtype == np.uint16 else gate.astype(np.float64)
@@ -536,6 +540,22 @@ def test_mega_moe_shared_quant_type_matches_numpy(routed, dispatch, shared_w, sh
     y_same, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh,
                                        shared_w_fmt=shared_w)
     assert np.max(np.abs(y_same - y_ref)) > 1e-6 * np.abs(y_ref).max()
+
+
+@pytest.mark.parametrize("cfmt,kw", [(P.E5M2, {}), (P.E4M3, dict(shared=1, routing="zipf")),
+                                     (P.E4M3, dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1))])
+def test_combine_quantisation_matches_numpy(cfmt, kw):
+    """combineQuantMode 3 / 4: each routed row enters the combine as
+    DQ_MX(Q_MX(bf16(O))) in that FP8 type; shared-expert rows stay local."""
+    cfg = synth.CONFIGS["tiny"].scaled(n=16, **kw)
+    x, ids, gate = synth.tokens_bf16(cfg), synth.topk_ids(cfg), synth.topk_weights(cfg)
+    w = _weights(cfg)
+    sh = _weights(cfg, shared=True) if cfg.shared else None
+    y, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh, combine_fmt=cfmt)
+    y_ref, _ = _numpy_grouped_moe(cfg, x, ids, gate, w, shared=sh, combine_fmt=cfmt)
+    assert np.max(np.abs(y - y_ref)) <= 1e-11 * np.abs(y_ref).max()
+    y0, _ = oracle.mega_moe_tokens(x, ids, gate, *w, cfg.dispatch_fmt, cfg.weight_fmt, shared=sh)
+    assert np.max(np.abs(y0 - y)) > 1e-4 * np.abs(y0).max()   # the quantisation shows
 
 
 @pytest.mark.parametrize("kw", [{}, dict(weight_fmt=P.E2M1, dispatch_fmt=P.E2M1)])
