@@ -397,7 +397,11 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  *   order, row_idx = expanded_row_idx of mm_moe_ep_dispatch, shared_rows =
  *   the rank's own shared experts' outputs for its tokens (they take part in
  *   no exchange).
- * expert_rows       [*, h] bf16, h a multiple of 8.
+ * expert_rows       [*, h] bf16 (expert_rows_dtype MM_DT_BFLOAT16), h a multiple
+ *                   of 8; or MXFP8 codes (23 / 24: combineQuantMode 3 / 4, the
+ *                   rows quantised for the exchange) with expert_scales
+ *                   [*, h/32] E8M0, h a multiple of 32: each routed term is
+ *                   DQ_MX of its row.
  * topk_weights      [num_rows, k] fp32 or bf16 (topk_weights_dtype).
  * shared_rows       [n_shared, num_rows, h] bf16, n_shared 0..4 (NULL when 0);
  *                   k + n_shared <= 36.
@@ -409,9 +413,10 @@ mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids
                              int64_t dispatch_quant_out_dtype, uint8_t* send_x, uint8_t* send_scales,
                              int32_t* send_expert, int64_t* rank_counts, int32_t* expanded_row_idx,
                              void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
-mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
-                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, const void* shared_rows,
-                         int64_t n_shared, void* y, void* stream);
+mm_status mm_moe_combine(const void* expert_rows, int expert_rows_dtype, const uint8_t* expert_scales,
+                         const int32_t* row_idx, const void* topk_weights, int topk_weights_dtype,
+                         int64_t num_rows, int64_t h, int64_t k, const void* shared_rows, int64_t n_shared,
+                         void* y, void* stream);
 
 /* ------------------------------------------------------------------------
  * mm_moe_expert_ffn -- the expert side of expert parallelism (MegaMoE README,

@@ -93,7 +93,7 @@ def load():
     L.mm_moe_expert_ffn.argtypes = [p, p, i32, p, i64, i64, p, p, p, p, i32, i32, i64, i64, ctypes.c_char_p, p, i64,
                                     p, p, p, sz, p, p]
     L.mm_moe_ep_dispatch.argtypes = [p, i32, p, i64, i64, i64, i64, i64, i64, p, p, p, p, p, p, sz, p, p]
-    L.mm_moe_combine.argtypes = [p, p, p, i32, i64, i64, i64, p, i64, p, p]
+    L.mm_moe_combine.argtypes = [p, i32, p, p, p, i32, i64, i64, i64, p, i64, p, p]
     for name in ("mm_moe_init_routing_workspace_size", "mm_moe_init_routing", "mm_moe_token_permute_workspace_size",
                  "mm_moe_token_permute", "mm_mega_moe_workspace_size", "mm_mega_moe",
                  "mm_prepared_weight_scales_size", "mm_prepare_weight_scales", "mm_mx_quantize",
@@ -425,12 +425,20 @@ def mm_moe_ep_dispatch(x, topk_ids, moe_expert_num: int, ep_world_size: int,
     return send_x, send_s, send_e, counts, exp_idx
 
 
-def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None, shared_rows=None):
+def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None, shared_rows=None, expert_scales=None,
+                   expert_rows_dtype=None):
     """Y[i] = sum_k W[i,k] * expert_rows[row_idx[i*K + k]] + sum_s shared_rows[s, i] in
     fp32, k in order then s, one bf16 rounding (MegaMoE stage 4); row_idx < 0 leaves
-    a term out.  expert_rows [*, H] bf16, row_idx [N*K] int32, topk_weights [N, K]
-    fp32 / bf16, shared_rows [S, N, H] bf16 or None."""
-    _need_dtype(expert_rows, (torch.bfloat16,), "expert_rows")
+    a term out.  expert_rows [*, H] bf16, or MXFP8 codes (uint8 / torch float8, type
+    expert_rows_dtype) with expert_scales [*, H/32] E8M0 (combineQuantMode 3 / 4);
+    row_idx [N*K] int32, topk_weights [N, K] fp32 / bf16, shared_rows [S, N, H] bf16
+    or None."""
+    quant = expert_scales is not None
+    _need_dtype(expert_rows, _BYTE_DTYPES if quant else (torch.bfloat16,), "expert_rows")
+    if quant:
+        _need_dtype(expert_scales, (torch.uint8,), "expert_scales")
+        _need_cuda(expert_scales)
+    rdt = _fp8_code(expert_rows, expert_rows_dtype) if quant else DT_BF16
     _need_dtype(row_idx, (torch.int32,), "row_idx")
     _need_dtype(topk_weights, (torch.float32, torch.bfloat16), "topk_weights")
     _need_cuda(expert_rows, row_idx, topk_weights)
@@ -446,8 +454,9 @@ def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None, shared_rows=Non
             raise MMError("shared_rows must be [S, N, H]")
         s_num = shared_rows.shape[0]
     y = out if out is not None else torch.empty((n, h), dtype=torch.bfloat16, device=expert_rows.device)
-    _check(load().mm_moe_combine(_ptr(expert_rows), _ptr(row_idx), _ptr(topk_weights), _dt(topk_weights), n, h, k,
-                                 _ptr(shared_rows), s_num, _ptr(y), _stream(expert_rows.device)), "mm_moe_combine")
+    _check(load().mm_moe_combine(_ptr(expert_rows), rdt, _ptr(expert_scales), _ptr(row_idx), _ptr(topk_weights),
+                                 _dt(topk_weights), n, h, k, _ptr(shared_rows), s_num, _ptr(y),
+                                 _stream(expert_rows.device)), "mm_moe_combine")
     return y
 
 

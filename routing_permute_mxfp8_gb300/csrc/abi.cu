@@ -914,23 +914,28 @@ mm_status mm_moe_ep_dispatch(const void* x, int x_dtype, const int32_t* topk_ids
   return cuda_status(e);
 }
 
-mm_status mm_moe_combine(const void* expert_rows, const int32_t* row_idx, const void* topk_weights,
-                         int topk_weights_dtype, int64_t num_rows, int64_t h, int64_t k, const void* shared_rows,
-                         int64_t n_shared, void* y, void* stream) {
+mm_status mm_moe_combine(const void* expert_rows, int expert_rows_dtype, const uint8_t* expert_scales,
+                         const int32_t* row_idx, const void* topk_weights, int topk_weights_dtype, int64_t num_rows,
+                         int64_t h, int64_t k, const void* shared_rows, int64_t n_shared, void* y, void* stream) {
   if (num_rows < 0 || h <= 0 || k <= 0 || n_shared < 0 || n_shared > 4 || k + n_shared > 36)
     return MM_ERR_INVALID_ARG;
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
-  if (h % 8 != 0) return MM_ERR_UNSUPPORTED;
+  // bf16 rows, or MXFP8 rows of the combine exchange (combineQuantMode 3 / 4)
+  const bool q = expert_rows_dtype != MM_DT_BFLOAT16;
+  if (q && !is_fp8(expert_rows_dtype)) return MM_ERR_UNSUPPORTED;
+  if (h % 8 != 0 || (q && h % 32 != 0)) return MM_ERR_UNSUPPORTED;
   if (num_rows == 0) return MM_OK;
   if (!expert_rows || !row_idx || !topk_weights || !y || !aligned16(expert_rows) || !aligned16(y))
     return MM_ERR_INVALID_ARG;
+  if (q && !expert_scales) return MM_ERR_INVALID_ARG;
   if (n_shared > 0 && (!shared_rows || !aligned16(shared_rows))) return MM_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   StageScope sc(MM_STAGE_COMBINE, st);
   const cudaError_t e = launch_combine_rows(
-      static_cast<const __nv_bfloat16*>(expert_rows), row_idx, topk_weights, topk_weights_dtype == MM_DT_BFLOAT16,
-      num_rows, h, (int)k, static_cast<const __nv_bfloat16*>(shared_rows), (int)n_shared,
-      static_cast<__nv_bfloat16*>(y), st);
+      q ? nullptr : static_cast<const __nv_bfloat16*>(expert_rows), row_idx, topk_weights,
+      topk_weights_dtype == MM_DT_BFLOAT16, num_rows, h, (int)k, static_cast<const __nv_bfloat16*>(shared_rows),
+      (int)n_shared, static_cast<__nv_bfloat16*>(y), st, q ? static_cast<const uint8_t*>(expert_rows) : nullptr,
+      q ? expert_scales : nullptr, q ? expert_rows_dtype : 0);
   sc.finish(1);
   return cuda_status(e);
 }

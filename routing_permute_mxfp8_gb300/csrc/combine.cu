@@ -14,8 +14,25 @@ constexpr int kThreads = 128;
 constexpr int kMaxTerms = 36;  // top-K <= 32 plus up to 4 shared experts
 constexpr int kBatch = 8;      // expert rows gathered per round
 
-// kSep: the shared experts' rows come from the caller's o_sh, not from o
-template <bool kSep>
+// 8 FP8 codes (E4M3 / E5M2) -> fp32 times the group's scale 2^(s - 127)
+// (E8M0 code s; 0 is 2^-127, a subnormal): DQ_MX of the combine exchange.
+template <int kFmt>
+__device__ __forceinline__ void fp8x8_dq(uint2 q, uint32_t s, float* f) {
+  const float sc = s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+  const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t p = (__nv_fp8x2_storage_t)((w[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(p, kFmt == MM_DT_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3);
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    f[2 * i] = v.x * sc;
+    f[2 * i + 1] = v.y * sc;
+  }
+}
+
+// kSep: the shared experts' rows come from the caller's o_sh, not from o;
+// kQ: the routed rows are MXFP8 codes of type kQ with E8M0 scales (oq, oq_sf)
+template <bool kSep, int kQ>
 __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
   __shared__ int32_t rows[kMaxTerms];
   __shared__ float w[kMaxTerms];
@@ -48,17 +65,32 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
     // flight at once), then add them in term order
     for (int t0 = 0; t0 < nterm; t0 += kBatch) {
       uint4 v[kBatch];
+      uint32_t qs[kBatch];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int32_t r = t0 + b < nterm ? rows[t0 + b] : -1;
-        const __nv_bfloat16* src = kSep && t0 + b >= a.k ? a.o_sh : a.o;
-        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
+        if (kQ != 0 && t0 + b < a.k) {  // a routed row as MXFP8 codes and its group's scale
+          if (r >= 0) {
+            const uint2 q = __ldg(reinterpret_cast<const uint2*>(a.oq + (int64_t)r * a.h + c));
+            v[b] = make_uint4(q.x, q.y, 0u, 0u);
+            qs[b] = __ldg(a.oq_sf + (int64_t)r * (a.h / 32) + c / 32);
+          } else {
+            v[b] = make_uint4(0u, 0u, 0u, 0u);
+            qs[b] = 0;
+          }
+        } else {
+          const __nv_bfloat16* src = kSep && t0 + b >= a.k ? a.o_sh : a.o;
+          v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
+        }
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         if (t0 + b >= nterm || rows[t0 + b] < 0) continue;
         float f[8];
-        bf16x8_to_f32(v[b], f);
+        if (kQ != 0 && t0 + b < a.k)
+          fp8x8_dq<kQ>(make_uint2(v[b].x, v[b].y), qs[b], f);
+        else
+          bf16x8_to_f32(v[b], f);
         const float wt = w[t0 + b];
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
@@ -81,9 +113,13 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
 
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
                                 int64_t n, int64_t h, int k, const __nv_bfloat16* shared_rows, int n_shared,
-                                __nv_bfloat16* y, cudaStream_t st) {
-  CombineArgs a;
+                                __nv_bfloat16* y, cudaStream_t st, const uint8_t* rows_q, const uint8_t* rows_sf,
+                                int rows_fmt) {
+  CombineArgs a = {};
   a.o = rows;
+  a.oq = rows_q;
+  a.oq_sf = rows_sf;
+  a.oq_fmt = rows_q ? rows_fmt : 0;
   a.o_sh = n_shared > 0 ? shared_rows : nullptr;
   a.pad_row = row_idx;
   a.gate = gate;
@@ -102,8 +138,16 @@ cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_id
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
-  if (a.o_sh && a.n_shared > 0) return launch_pdl(k_combine<true>, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
-  return launch_pdl(k_combine<false>, dim3((unsigned)a.n), dim3(kThreads), 0, st, a);
+  const dim3 g((unsigned)a.n), b(kThreads);
+  const bool sep = a.o_sh && a.n_shared > 0;
+  if (a.oq_fmt == MM_DT_FP8_E5M2)
+    return sep ? launch_pdl(k_combine<true, MM_DT_FP8_E5M2>, g, b, 0, st, a)
+               : launch_pdl(k_combine<false, MM_DT_FP8_E5M2>, g, b, 0, st, a);
+  if (a.oq_fmt == MM_DT_FP8_E4M3FN)
+    return sep ? launch_pdl(k_combine<true, MM_DT_FP8_E4M3FN>, g, b, 0, st, a)
+               : launch_pdl(k_combine<false, MM_DT_FP8_E4M3FN>, g, b, 0, st, a);
+  if (sep) return launch_pdl(k_combine<true, 0>, g, b, 0, st, a);
+  return launch_pdl(k_combine<false, 0>, g, b, 0, st, a);
 }
 
 }  // namespace mm

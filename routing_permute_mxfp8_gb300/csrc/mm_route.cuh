@@ -83,7 +83,8 @@ void set_route_path(int path);
 // fp32 in k order, one bf16 rounding (MegaMoE stage 4 / EP combine).
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* row_idx, const void* gate, int gate_bf16,
                                 int64_t n, int64_t h, int k, const __nv_bfloat16* shared_rows, int n_shared,
-                                __nv_bfloat16* y, cudaStream_t st);
+                                __nv_bfloat16* y, cudaStream_t st, const uint8_t* rows_q = nullptr,
+                                const uint8_t* rows_sf = nullptr, int rows_fmt = 0);
 
 // ---- permute / quantise (permute.cu) -------------------------------------
 struct PermuteArgs {
@@ -152,6 +153,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
 struct CombineArgs {
   const __nv_bfloat16* o;     // [rows_cap, h] expert outputs (padded grouped layout)
   const __nv_bfloat16* o_sh;  // optional [n_shared, n, h] shared-expert rows (else in o at their segments)
+  const uint8_t* oq;          // optional: the routed rows as MXFP8 codes [*, h] (oq_fmt 23 / 24) ...
+  const uint8_t* oq_sf;       // ... with E8M0 scales [*, h / 32] (then o is unused)
+  int oq_fmt;
   const int32_t* pad_row;     // [n*k]
   const void* gate;           // [n, k] fp32 or bf16
   int gate_bf16;

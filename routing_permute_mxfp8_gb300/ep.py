@@ -11,7 +11,8 @@ the experts [r*E/W, (r+1)*E/W):
            passed through, each row's result written at its own position, the
            order in which the rows go back);
   stage 4  the O rows go back to their source ranks in the order they came
-           (the reverse all-to-all), where mm_moe_combine forms
+           (the reverse all-to-all; with combineQuantMode 3 / 4 as MXFP8
+           E5M2 / E4M3 codes and E8M0 scales), where mm_moe_combine forms
            Y[i] = sum_k W[i,k] O[pi(i,k)] in fp32 and rounds once to bf16.
 Shared experts take part in no exchange: each rank runs them on its own
 tokens (quantised in the shared experts' input type, through the expert-side
@@ -50,7 +51,7 @@ def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                 dispatch_quant_out_dtype: int = _mm.DT_FP8_E4M3FN, activation: str = "swiglu",
                 activation_params=(), dev_err=None, shared_weight1=None, shared_weight2=None,
                 shared_weight_scales1=None, shared_weight_scales2=None, shared_weight_dtype=None,
-                shared_expert_quant_out_dtype=None):
+                shared_expert_quant_out_dtype=None, combine_quant_mode: int = 0):
     """MegaMoE forward of this rank's tokens with expert parallelism.
 
     x [N, H] bf16, topk_ids [N, K] int32 (global expert ids), topk_weights [N, K]
@@ -88,8 +89,22 @@ def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                                        dev_err=dev_err)[0]
     else:
         o_rows = torch.empty((0, h), dtype=torch.bfloat16, device=x.device)
-    # stage 4: rows back to their source ranks in send order, then the weighted sum
-    back = _a2a_rows(o_rows, recv_counts, send_counts, group)
+    # stage 4: rows back to their source ranks in send order (MXFP8 codes and
+    # scales under combine quantisation), then the weighted sum
+    if combine_quant_mode not in (0, 3, 4):
+        raise _mm.MMError("combine_quant_mode must be 0, 3 or 4")
+    cfmt = {3: _mm.DT_FP8_E5M2, 4: _mm.DT_FP8_E4M3FN}.get(combine_quant_mode)
+    back_s = None
+    if cfmt is None:
+        back = _a2a_rows(o_rows, recv_counts, send_counts, group)
+    else:
+        if m > 0:
+            oq, os_ = _mm.mm_mx_quantize(o_rows, cfmt, scale_cols=h // 32)
+        else:
+            oq = torch.empty((0, h), dtype=torch.uint8, device=x.device)
+            os_ = torch.empty((0, h // 32), dtype=torch.uint8, device=x.device)
+        back = _a2a_rows(oq, recv_counts, send_counts, group)
+        back_s = _a2a_rows(os_, recv_counts, send_counts, group)
     if n == 0:
         return torch.empty((0, h), dtype=torch.bfloat16, device=x.device)
     shared = None
@@ -99,7 +114,8 @@ def mega_moe_ep(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
                               dispatch_quant_out_dtype if shared_expert_quant_out_dtype is None
                               else shared_expert_quant_out_dtype,
                               weight_scale_layout, activation, activation_params, dev_err)
-    return _mm.mm_moe_combine(back, exp_idx, topk_weights, shared_rows=shared)
+    return _mm.mm_moe_combine(back, exp_idx, topk_weights, shared_rows=shared, expert_scales=back_s,
+                              expert_rows_dtype=cfmt)
 
 
 def _shared_rows(x, w1, w2, s1, s2, w_dtype, x_dtype, layout, activation, activation_params, dev_err):

@@ -102,8 +102,13 @@ def _oracle_fakes(mm, cfg):
                                    s_cols=scale_cols)
         return torch.from_numpy(q), torch.from_numpy(np.ascontiguousarray(sc))
 
-    def combine(rows, idx, gate, out=None, shared_rows=None):
-        r = rows.float().numpy()
+    def combine(rows, idx, gate, out=None, shared_rows=None, expert_scales=None, expert_rows_dtype=None):
+        if expert_scales is not None:   # combine quantisation: DQ_MX of the MXFP8 rows
+            tab = np.array([oracle.fp8_value(c, expert_rows_dtype) for c in range(256)])
+            sc = np.repeat(expert_scales.numpy().astype(np.float64) - 127.0, 32, axis=1)
+            r = (tab[rows.numpy()] * np.exp2(sc)).astype(np.float32)
+        else:
+            r = rows.float().numpy()
         g = gate.float().numpy()
         n, k = g.shape
         acc = np.zeros((n, rows.shape[1]), np.float32)
@@ -128,7 +133,7 @@ def _slices(cfg, rank):
     return slice(rank * per, (rank + 1) * per)
 
 
-def _cpu_rank(rank, port, out, shared):
+def _cpu_rank(rank, port, out, shared, cq):
     import sys
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -148,43 +153,49 @@ def _cpu_rank(rank, port, out, shared):
     skw = {} if sh is None else dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]),
                                      shared_weight2=t(sh[2]), shared_weight_scales2=t(sh[3]))
     y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
-                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, **skw)
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt,
+                       combine_quant_mode=cq, **skw)
     # the same fakes on one rank, no exchange: every expert local
     sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(xt, t(ids[sl]), cfg.e, 1, cfg.dispatch_fmt)
     o = mm.mm_mega_moe(sx, se.view(-1, 1), torch.ones((sx.shape[0], 1)), t(w1), t(w2), t(s1), t(s2), cfg.e,
                        x_scales=ss, dispatch_quant_mode=0, dispatch_quant_out_dtype=cfg.dispatch_fmt)[0]
     shr = None if sh is None else ep._shared_rows(xt, t(sh[0]), t(sh[2]), t(sh[1]), t(sh[3]), cfg.weight_fmt,
                                                  cfg.dispatch_fmt, mm.WSCALE_ROWS, "swiglu", (), None)
-    y1 = mm.mm_moe_combine(o, ei, gt, shared_rows=shr)
+    if cq:
+        cfmt = {3: 23, 4: 24}[cq]
+        oq, os_ = mm.mm_mx_quantize(o, cfmt, scale_cols=cfg.h // 32)
+        y1 = mm.mm_moe_combine(oq, ei, gt, shared_rows=shr, expert_scales=os_, expert_rows_dtype=cfmt)
+    else:
+        y1 = mm.mm_moe_combine(o, ei, gt, shared_rows=shr)
     out[rank] = (y.view(torch.int16).numpy().copy(), y1.view(torch.int16).numpy().copy())
     dist.barrier()
     dist.destroy_process_group()
 
 
-def _check_against_oracle(cfg, x, ids, gate, w, y_bits):
+def _check_against_oracle(cfg, x, ids, gate, w, y_bits, cq=0):
     import oracle
     import synth
     w1, s1, w2, s2 = w
     y_ref, _ = oracle.mega_moe_tokens(x, ids, gate, w1, s1, w2, s2, cfg.dispatch_fmt, cfg.weight_fmt,
-                                      shared=_shared(cfg))
+                                      shared=_shared(cfg), combine_fmt={0: None, 3: 23, 4: 24}[cq])
     yg = synth.bf16_bits_to_f32(y_bits.view(np.uint16)).astype(np.float64)
     rel = np.linalg.norm(yg - y_ref) / np.linalg.norm(y_ref)
     mx = np.abs(yg - y_ref).max() / np.abs(y_ref).max()
     assert rel <= 5e-3 and mx <= 2e-2, (rel, mx)
 
 
-@pytest.mark.parametrize("shared", [0, 1])
-def test_ep_exchange_two_gloo_ranks_cpu(shared):
+@pytest.mark.parametrize("shared,cq", [(0, 0), (1, 0), (1, 4)], ids=["plain", "shared", "shared_combine_e4m3"])
+def test_ep_exchange_two_gloo_ranks_cpu(shared, cq):
     port = _free_port()
     out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
-    mp.spawn(_cpu_rank, args=(port, out, shared), nprocs=W, join=True)
+    mp.spawn(_cpu_rank, args=(port, out, shared, cq), nprocs=W, join=True)
     cfg, x, ids, gate, w = _problem(shared=shared)
     ys = []
     for r in range(W):
         y, y1 = out[r]
         assert np.array_equal(y, y1), r          # exchange changes nothing in the result
         ys.append(y)
-    _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))
+    _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys), cq)
 
 
 def _gpu_rank(rank, port, out, a4w4, shared):
@@ -237,3 +248,60 @@ def test_ep_two_ranks_on_one_gpu_matches_single_process(a4w4, shared):
         assert np.array_equal(y, y1), r
         ys.append(y)
     _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys))
+
+
+def _gpu_rank_combine_quant(rank, port, out, cq):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    import routing_permute_mxfp8_gb300 as mm
+    from routing_permute_mxfp8_gb300 import ep
+    torch.cuda.set_device(0)
+    cfg, x, ids, gate, (w1, s1, w2, s2) = _problem(shared=1)
+    sh = _shared(cfg)
+    dist.init_process_group("gloo", rank=rank, world_size=W)
+    sl = _slices(cfg, rank)
+    el = cfg.e // W
+    mine = slice(rank * el, (rank + 1) * el)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    xt = t(x[sl].view(np.int16)).view(torch.bfloat16)
+    gt = t(gate[sl].view(np.int16)).view(torch.bfloat16)
+    skw = dict(shared_weight1=t(sh[0]), shared_weight_scales1=t(sh[1]), shared_weight2=t(sh[2]),
+               shared_weight_scales2=t(sh[3]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = ep.mega_moe_ep(xt, t(ids[sl]), gt, t(w1[mine]), t(w2[mine]), t(s1[mine]), t(s2[mine]), cfg.e,
+                       weight_dtype=cfg.weight_fmt, dispatch_quant_out_dtype=cfg.dispatch_fmt, dev_err=err,
+                       combine_quant_mode=cq, **skw)
+    # the same kernels on this rank alone, no exchange: every expert local
+    cfmt = {3: 23, 4: 24}[cq]
+    sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(xt, t(ids[sl]), cfg.e, 1, cfg.dispatch_fmt)
+    o = mm.mm_moe_expert_ffn(sx, ss, se, t(w1), t(w2), t(s1), t(s2), cfg.e, x_dtype=cfg.dispatch_fmt,
+                             weight_dtype=cfg.weight_fmt)[0]
+    oq, os_ = mm.mm_mx_quantize(o, cfmt, scale_cols=cfg.h // 32)
+    shr = ep._shared_rows(xt, t(sh[0]), t(sh[2]), t(sh[1]), t(sh[3]), cfg.weight_fmt, cfg.dispatch_fmt,
+                          mm.WSCALE_ROWS, "swiglu", (), None)
+    y1 = mm.mm_moe_combine(oq, ei, gt, shared_rows=shr, expert_scales=os_, expert_rows_dtype=cfmt)
+    torch.cuda.synchronize()
+    out[rank] = (y.view(torch.int16).cpu().numpy(), y1.view(torch.int16).cpu().numpy(), int(err.item()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cq", [3, 4])
+def test_ep_combine_quantisation_two_ranks_on_one_gpu(cq):
+    """combineQuantMode 3 / 4: the returned rows travel as MXFP8 codes and
+    scales; two ranks give the bits of the same kernels on one rank without
+    the exchange, and the oracle's combine-quantised Y within tolerance."""
+    port = _free_port()
+    out = mp.get_context("spawn").Manager().dict()  # no fork after CUDA is initialised
+    mp.spawn(_gpu_rank_combine_quant, args=(port, out, cq), nprocs=W, join=True)
+    cfg, x, ids, gate, w = _problem(shared=1)
+    ys = []
+    for r in range(W):
+        y, y1, err = out[r]
+        assert err == 0
+        assert np.array_equal(y, y1), r
+        ys.append(y)
+    _check_against_oracle(cfg, x, ids, gate, w, np.concatenate(ys), cq)

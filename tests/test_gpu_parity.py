@@ -920,6 +920,32 @@ def test_expert_ffn_full_size_equals_mega_moe_top1():
     assert np.array_equal(host(out), host(y))
 
 
+@pytest.mark.parametrize("fmt,n_shared", [(23, 0), (24, 2)])
+def test_moe_combine_mxfp8_rows(fmt, n_shared):
+    """mm_moe_combine on rows sent as MXFP8 (combineQuantMode 3 / 4): each
+    routed term is DQ_MX of its row (codes and E8M0 scales of the oracle's
+    Q_MX), then the fp32 sum in k order and the shared rows, one bf16 rounding."""
+    rng = np.random.default_rng(11 + fmt)
+    n, k, h, nrows = 150, 5, 512, 600
+    rows = (rng.standard_normal((nrows, h)) * np.exp2(rng.integers(-8, 6, (nrows, 1)))).astype(np.float32)
+    q, sc = oracle.mx_quantize(rows, oracle.DT_F32, fmt, s_cols=h // 32)
+    idx = rng.integers(-1, nrows, size=n * k).astype(np.int32)
+    g = rng.random((n, k)).astype(np.float32)
+    sh_b = torch.from_numpy(rng.standard_normal((n_shared, n, h)).astype(np.float32)).to(torch.bfloat16)
+    y = mm.mm_moe_combine(t(q), t(idx), t(g), expert_scales=t(sc), expert_rows_dtype=fmt,
+                          shared_rows=sh_b.to(DEV) if n_shared else None)
+    tab = np.array([oracle.fp8_value(c, fmt) for c in range(256)])
+    dq = (tab[q] * np.exp2(np.repeat(sc.astype(np.float64) - 127.0, 32, axis=1))).astype(np.float32)
+    acc = np.zeros((n, h), np.float32)
+    ix = idx.reshape(n, k)
+    for kk in range(k):
+        ok = ix[:, kk] >= 0
+        acc[ok] = (g[ok, kk:kk + 1].astype(np.float64) * dq[ix[ok, kk]] + acc[ok]).astype(np.float32)
+    for s_ in range(n_shared):
+        acc = (acc.astype(np.float64) + sh_b[s_].float().numpy()).astype(np.float32)
+    assert torch.equal(y.cpu(), torch.from_numpy(acc).to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("gate_bf16,n_shared", [(False, 0), (True, 0), (False, 2), (True, 4)])
 def test_moe_combine_rows(gate_bf16, n_shared):
     """mm_moe_combine: fp32 sum in k order of weighted rows chosen by an index
