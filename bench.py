@@ -915,12 +915,23 @@ def ep_local_measurements(mm, torch, synth, dist, hbm_peak, W, cfg, steps, world
     back = torch.randn((cfg.n * cfg.k, cfg.h), device="cuda").to(torch.bfloat16)
     y = torch.empty((cfg.n, cfg.h), dtype=torch.bfloat16, device="cuda")
     ms_c, st_c, _ = time_steps(torch, lambda: mm.mm_moe_combine(back, exp_idx, gate, out=y), steps, 3, dist)
+    # combine quantisation (combineQuantMode 4): the expert rank's Q_MX of the rows
+    # it sends back, and the source rank's combine of MXFP8 rows
+    bq, bs = mm.mm_mx_quantize(back, mm.DT_FP8_E4M3FN, scale_cols=cfg.h // 32)
+    ms_q, _, _ = time_steps(torch, lambda: mm.mm_mx_quantize(back, mm.DT_FP8_E4M3FN, scale_cols=cfg.h // 32),
+                            steps, 3, dist)   # one launch a step, timed with the step's events
+    _, st_cq, _ = time_steps(torch, lambda: mm.mm_moe_combine(bq, exp_idx, gate, out=y, expert_scales=bs,
+                                                              expert_rows_dtype=mm.DT_FP8_E4M3FN), steps, 3, dist)
     rows = cfg.n * cfg.k
     d_ms = (st_d["route"][0] + st_d["dispatch"][0]) / steps
     c_ms = st_c["combine"][0] / steps
+    q_ms = ms_q / steps
+    cq_ms = st_cq["combine"][0] / steps
+    q_bytes = rows * cfg.h * 2 + rows * (cfg.h + cfg.h // 32)
+    cq_bytes = rows * (cfg.h + cfg.h // 32) + rows * (4 + gate.element_size()) + cfg.n * cfg.h * 2
     d_bytes = cfg.n * cfg.h * 2 + rows * (4 + 4 + 4 + cfg.h + cfg.h // 32)
     c_bytes = rows * cfg.h * 2 + rows * (4 + gate.element_size()) + cfg.n * cfg.h * 2
-    del x, ids, gate, sx, ss, se, back, y
+    del x, ids, gate, sx, ss, se, back, y, bq, bs
     return {"workload": f"{cfg.name}, ep_world_size {world}, {e_loc} experts per rank",
             "exchange": "not measured (one GPU)",
             "dispatch_ms": d_ms, "dispatch_gbs": d_bytes / (d_ms / 1e3) / 1e9,
@@ -929,6 +940,10 @@ def ep_local_measurements(mm, torch, synth, dist, hbm_peak, W, cfg, steps, world
             "expert_stage_ms": {k: v[0] / steps for k, v in st_e.items() if v[1]},
             "combine_ms": c_ms, "combine_gbs": c_bytes / (c_ms / 1e3) / 1e9,
             "combine_frac": c_bytes / (c_ms / 1e3) / 1e9 / hbm_peak,
+            "combine_quant_e4m3": {"quantise_ms": q_ms, "quantise_gbs": q_bytes / (q_ms / 1e3) / 1e9,
+                                   "combine_ms": cq_ms, "combine_gbs": cq_bytes / (cq_ms / 1e3) / 1e9,
+                                   "combine_frac": cq_bytes / (cq_ms / 1e3) / 1e9 / hbm_peak,
+                                   "exchange_bytes_per_row": cfg.h + cfg.h // 32, "bf16_bytes_per_row": 2 * cfg.h},
             "rank_rows_sent": cnt}
 
 

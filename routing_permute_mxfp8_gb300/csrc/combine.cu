@@ -30,16 +30,11 @@ __device__ __forceinline__ void fp8x8_dq(uint2 q, uint32_t s, float* f) {
   }
 }
 
-// kSep: the shared experts' rows come from the caller's o_sh, not from o;
-// kQ: the routed rows are MXFP8 codes of type kQ with E8M0 scales (oq, oq_sf)
-template <bool kSep, int kQ>
-__global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
-  __shared__ int32_t rows[kMaxTerms];
-  __shared__ float w[kMaxTerms];
-  const int64_t i = blockIdx.x;
+// The rows of token i's terms and their weights in shared memory: routed
+// terms from pad_row, then the shared experts' rows (weight 1).
+template <bool kSep>
+__device__ __forceinline__ void combine_terms(const CombineArgs& a, int64_t i, int32_t* rows, float* w) {
   const int nterm = a.k + a.n_shared;
-  pdl_wait();
-  pdl_trigger();
   if (threadIdx.x < a.k) {
     const int64_t j = i * a.k + threadIdx.x;
     const int32_t r = a.pad_row[j];
@@ -56,6 +51,18 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
     }
     w[threadIdx.x] = 1.0f;
   }
+}
+
+// kSep: the shared experts' rows come from the caller's o_sh, not from o
+template <bool kSep>
+__global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
+  __shared__ int32_t rows[kMaxTerms];
+  __shared__ float w[kMaxTerms];
+  const int64_t i = blockIdx.x;
+  const int nterm = a.k + a.n_shared;
+  pdl_wait();
+  pdl_trigger();
+  combine_terms<kSep>(a, i, rows, w);
   __syncthreads();
   for (int64_t c = (int64_t)threadIdx.x * 8; c < a.h; c += kThreads * 8) {
     float acc[8];
@@ -65,32 +72,17 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
     // flight at once), then add them in term order
     for (int t0 = 0; t0 < nterm; t0 += kBatch) {
       uint4 v[kBatch];
-      uint32_t qs[kBatch];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int32_t r = t0 + b < nterm ? rows[t0 + b] : -1;
-        if (kQ != 0 && t0 + b < a.k) {  // a routed row as MXFP8 codes and its group's scale
-          if (r >= 0) {
-            const uint2 q = __ldg(reinterpret_cast<const uint2*>(a.oq + (int64_t)r * a.h + c));
-            v[b] = make_uint4(q.x, q.y, 0u, 0u);
-            qs[b] = __ldg(a.oq_sf + (int64_t)r * (a.h / 32) + c / 32);
-          } else {
-            v[b] = make_uint4(0u, 0u, 0u, 0u);
-            qs[b] = 0;
-          }
-        } else {
-          const __nv_bfloat16* src = kSep && t0 + b >= a.k ? a.o_sh : a.o;
-          v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
-        }
+        const __nv_bfloat16* src = kSep && t0 + b >= a.k ? a.o_sh : a.o;
+        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         if (t0 + b >= nterm || rows[t0 + b] < 0) continue;
         float f[8];
-        if (kQ != 0 && t0 + b < a.k)
-          fp8x8_dq<kQ>(make_uint2(v[b].x, v[b].y), qs[b], f);
-        else
-          bf16x8_to_f32(v[b], f);
+        bf16x8_to_f32(v[b], f);
         const float wt = w[t0 + b];
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
@@ -106,6 +98,71 @@ __global__ void __launch_bounds__(kThreads) k_combine(CombineArgs a) {
     o.z = *reinterpret_cast<uint32_t*>(&p2);
     o.w = *reinterpret_cast<uint32_t*>(&p3);
     *reinterpret_cast<uint4*>(a.y + i * a.h + c) = o;
+  }
+}
+
+// The routed rows as MXFP8 codes of type kQ with E8M0 scales (oq, oq_sf;
+// the combine exchange under combineQuantMode 3 / 4): 16 codes per thread
+// (one 16-byte load a row, within one 32-element group), DQ_MX in fp32,
+// the same fp32 sum in term order and the one bf16 rounding; the shared
+// experts' rows stay bf16.
+template <bool kSep, int kQ>
+__global__ void __launch_bounds__(kThreads) k_combine_q(CombineArgs a) {
+  __shared__ int32_t rows[kMaxTerms];
+  __shared__ float w[kMaxTerms];
+  const int64_t i = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  combine_terms<kSep>(a, i, rows, w);
+  __syncthreads();
+  for (int64_t c = (int64_t)threadIdx.x * 16; c < a.h; c += kThreads * 16) {
+    float acc[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    for (int t0 = 0; t0 < a.k; t0 += kBatch) {
+      uint4 v[kBatch];
+      uint32_t qs[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int32_t r = t0 + b < a.k ? rows[t0 + b] : -1;
+        v[b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.oq + (int64_t)r * a.h + c)) : make_uint4(0u, 0u, 0u, 0u);
+        qs[b] = r >= 0 ? (uint32_t)__ldg(a.oq_sf + (int64_t)r * (a.h / 32) + c / 32) : 0u;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (t0 + b >= a.k || rows[t0 + b] < 0) continue;
+        float f[16];
+        fp8x8_dq<kQ>(make_uint2(v[b].x, v[b].y), qs[b], f);
+        fp8x8_dq<kQ>(make_uint2(v[b].z, v[b].w), qs[b], f + 8);
+        const float wt = w[t0 + b];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) acc[u] = fmaf(wt, f[u], acc[u]);
+      }
+    }
+    for (int t = a.k; t < a.k + a.n_shared; ++t) {
+      const int32_t r = rows[t];
+      if (r < 0) continue;
+      const __nv_bfloat16* src = (kSep ? a.o_sh : a.o) + (int64_t)r * a.h + c;
+      float f[16];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src)), f);
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src + 8)), f + 8);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) acc[u] = fmaf(1.0f, f[u], acc[u]);
+    }
+    uint4 o[2];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[8 * hlf + 0], acc[8 * hlf + 1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[8 * hlf + 2], acc[8 * hlf + 3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[8 * hlf + 4], acc[8 * hlf + 5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[8 * hlf + 6], acc[8 * hlf + 7]);
+      o[hlf].x = *reinterpret_cast<uint32_t*>(&p0);
+      o[hlf].y = *reinterpret_cast<uint32_t*>(&p1);
+      o[hlf].z = *reinterpret_cast<uint32_t*>(&p2);
+      o[hlf].w = *reinterpret_cast<uint32_t*>(&p3);
+    }
+    *reinterpret_cast<uint4*>(a.y + i * a.h + c) = o[0];
+    *reinterpret_cast<uint4*>(a.y + i * a.h + c + 8) = o[1];
   }
 }
 
@@ -140,14 +197,16 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
   const dim3 g((unsigned)a.n), b(kThreads);
   const bool sep = a.o_sh && a.n_shared > 0;
-  if (a.oq_fmt == MM_DT_FP8_E5M2)
-    return sep ? launch_pdl(k_combine<true, MM_DT_FP8_E5M2>, g, b, 0, st, a)
-               : launch_pdl(k_combine<false, MM_DT_FP8_E5M2>, g, b, 0, st, a);
-  if (a.oq_fmt == MM_DT_FP8_E4M3FN)
-    return sep ? launch_pdl(k_combine<true, MM_DT_FP8_E4M3FN>, g, b, 0, st, a)
-               : launch_pdl(k_combine<false, MM_DT_FP8_E4M3FN>, g, b, 0, st, a);
-  if (sep) return launch_pdl(k_combine<true, 0>, g, b, 0, st, a);
-  return launch_pdl(k_combine<false, 0>, g, b, 0, st, a);
+  if (a.oq_fmt == MM_DT_FP8_E5M2 || a.oq_fmt == MM_DT_FP8_E4M3FN) {
+    if (a.h % 32 != 0) return cudaErrorInvalidValue;
+    if (a.oq_fmt == MM_DT_FP8_E5M2)
+      return sep ? launch_pdl(k_combine_q<true, MM_DT_FP8_E5M2>, g, b, 0, st, a)
+                 : launch_pdl(k_combine_q<false, MM_DT_FP8_E5M2>, g, b, 0, st, a);
+    return sep ? launch_pdl(k_combine_q<true, MM_DT_FP8_E4M3FN>, g, b, 0, st, a)
+               : launch_pdl(k_combine_q<false, MM_DT_FP8_E4M3FN>, g, b, 0, st, a);
+  }
+  if (sep) return launch_pdl(k_combine<true>, g, b, 0, st, a);
+  return launch_pdl(k_combine<false>, g, b, 0, st, a);
 }
 
 }  // namespace mm
