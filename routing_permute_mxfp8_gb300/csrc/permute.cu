@@ -287,12 +287,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) k_permute_prequant(Permut
 template <int kSrc, int kFmt>
 cudaError_t launch_mx_variant(const PermuteArgs& a, int, cudaStream_t st) {
   // split each row's 512-column slices over several warps until there are
-  // about 288 warps per SM (several waves of short warps balance better
-  // than one wave of whole rows)
+  // about 2304 warps per SM (many waves of short warps balance better than
+  // one wave of whole rows); packed FP4 writes half the bytes a slice, so
+  // its warps keep at least two slices to amortise the per-warp
+  // destination loads
   const int64_t slices = (a.h + 511) / 512;
-  int64_t wpt = (int64_t)num_sms() * 288 / a.n;
+  const int64_t max_wpt = kFmt == MM_DT_FP4_E2M1 ? (slices + 1) / 2 : slices;
+  int64_t wpt = (int64_t)num_sms() * 2304 / a.n;
   if (wpt < 1) wpt = 1;
-  if (wpt > slices) wpt = slices;
+  if (wpt > max_wpt) wpt = max_wpt;
   const int64_t span = ceil_div(slices, wpt) * 512;
   wpt = ceil_div(a.h, span);
   if (a.n * wpt > 0x7fffffff - kWarpsPerBlock) return cudaErrorInvalidValue;
@@ -325,7 +328,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t st) {
   if (a.out_fmt < 0) {
     const int esz = a.src_dtype == MM_DT_FLOAT32 ? 4 : 2;
     const int64_t rb = a.h * esz, slices = (rb + 511) / 512;
-    int64_t wpt = (int64_t)num_sms() * 288 / a.n;  // as in launch_mx_variant
+    int64_t wpt = (int64_t)num_sms() * 2304 / a.n;  // as in launch_mx_variant (FP8 outputs)
     if (wpt < 1) wpt = 1;
     if (wpt > slices) wpt = slices;
     const int64_t span = ceil_div(slices, wpt) * 512;
