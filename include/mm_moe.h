@@ -402,6 +402,10 @@ mm_status mm_selftest_wait_timeout(int64_t limit_ns, int32_t* dev_err, void* str
  *                   rows quantised for the exchange) with expert_scales
  *                   [*, h/32] E8M0, h a multiple of 32: each routed term is
  *                   DQ_MX of its row.
+ * row_idx           [num_rows*k] int32; num_rows*k below 16777215, the row
+ *                   limit of mm_moe_ep_dispatch.  Entries >= 0 must index
+ *                   rows of expert_rows: the call is not given that buffer's
+ *                   row count and cannot check them.
  * topk_weights      [num_rows, k] fp32 or bf16 (topk_weights_dtype).
  * shared_rows       [n_shared, num_rows, h] bf16, n_shared 0..4 (NULL when 0);
  *                   k + n_shared <= 36.

@@ -151,6 +151,39 @@ def _need_dtype(t, allowed, what):
         raise MMError(f"{what} must be {names}, got {str(t.dtype).replace('torch.', '')}")
 
 
+def _need(cond, msg):
+    """Shapes the C ABI cannot see: it takes sizes and raw pointers, so a
+    tensor smaller than the sizes it is passed with would be read or written
+    past its end on the GPU.  Mismatches are refused here."""
+    if not cond:
+        raise MMError(msg)
+
+
+def _need_rows_of(idx, n, what, of):
+    _need(idx.dim() in (1, 2) and idx.shape[0] == n, f"{what} must be [N] or [N, K] with N = {of}.shape[0] = {n}")
+
+
+def _need_out(out, shape, what="out"):
+    if out is not None:
+        _need(out.dtype == torch.bfloat16 and tuple(out.shape) == tuple(shape),
+              f"{what} must be a bfloat16 tensor of shape {list(shape)}")
+
+
+def _need_weights(w1, w2, s1, s2, e, h, aw, fp4, what=""):
+    """Expert weights [E, 2I, H] and [E, H, A] (A = I, or 2I under gelu; packed
+    FP4 halves the last dimension), and E8M0 scales holding at least one byte
+    per 32 reduction elements of every output row (the pages' layout or a
+    prepared buffer)."""
+    pk = 2 if fp4 else 1
+    _need(w1.dim() == 3 and w1.shape[0] == e and w1.shape[2] * pk == h,
+          f"{what}weight1 must be [{e}, 2I, {h // pk}], got {list(w1.shape)}")
+    _need(w2.dim() == 3 and w2.shape[0] == e and w2.shape[1] == h and w2.shape[2] * pk == aw,
+          f"{what}weight2 must be [{e}, {h}, {aw // pk}], got {list(w2.shape)}")
+    _need(s1.numel() >= e * w1.shape[1] * (h // 32),
+          f"{what}weight_scales1 holds {s1.numel()} bytes, {e * w1.shape[1] * (h // 32)} needed")
+    _need(s2.numel() >= e * h * (aw // 32), f"{what}weight_scales2 holds {s2.numel()} bytes, {e * h * (aw // 32)} needed")
+
+
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
         if workspace.numel() < nbytes:
@@ -179,6 +212,8 @@ def mm_moe_init_routing(x, expert_idx, expert_num: int, quant_mode: int = QUANT_
     """
     _need_dtype(x, _SRC_DTYPES, "x")
     _need_dtype(expert_idx, (torch.int32,), "expert_idx")
+    _need(x.dim() == 2, "x must be [N, H]")
+    _need_rows_of(expert_idx, x.shape[0], "expert_idx", "x")
     _need_cuda(x, expert_idx)
     L = load()
     n, h = x.shape
@@ -224,6 +259,8 @@ def mm_moe_token_permute(tokens, indices, num_experts: int, num_out_tokens=None,
     [M, CeilDiv(H, 64), 2]."""
     _need_dtype(tokens, _SRC_DTYPES, "tokens")
     _need_dtype(indices, (torch.int32, torch.int64), "indices")
+    _need(tokens.dim() == 2, "tokens must be [N, H]")
+    _need_rows_of(indices, tokens.shape[0], "indices", "tokens")
     _need_cuda(tokens, indices)
     L = load()
     n, h = tokens.shape
@@ -305,19 +342,31 @@ def mm_mega_moe(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, wei
         _need_dtype(t, (torch.uint8,), name)
     if topk_ids.dim() != 2 or tuple(topk_weights.shape) != tuple(topk_ids.shape) or topk_ids.shape[0] != x.shape[0]:
         raise MMError("topk_ids and topk_weights must both be [BS, K] with BS = x.shape[0]")
-    _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
-    L = load()
+    _need(x.dim() == 2, "x must be [BS, H]")
     fp4_x = dispatch_quant_out_dtype == DT_FP4_E2M1
     bs = x.shape[0]
     h = x.shape[1] * 2 if fp4_x and dispatch_quant_mode == 0 else x.shape[1]   # packed FP4 pass-through
     k = topk_ids.shape[1]
     wdt = _fp8_code(weight1, weight_dtype)
+    _need(weight1.dim() == 3, "weight1 must be [E, 2I, H]")
     inter = weight1.shape[1] // 2
     aw = 2 * inter if activation == "gelu" else inter   # width of A_hat
+    _need_weights(weight1, weight2, weight_scales1, weight_scales2, moe_expert_num, h, aw, wdt == DT_FP4_E2M1)
+    shared = (shared_weight1, shared_weight2, shared_weight_scales1, shared_weight_scales2)
     s_num = 0 if shared_weight1 is None else shared_weight1.shape[0]
-    dev = x.device
     swdt = wdt if shared_weight1 is None else _fp8_code(shared_weight1, wdt if shared_weight_dtype is None
                                                          else shared_weight_dtype)
+    if s_num > 0:
+        _need(all(t is not None for t in shared), "shared experts need all four of shared_weight1 / 2 and their scales")
+        _need(shared_weight1.dim() == 3 and shared_weight1.shape[1] == weight1.shape[1],
+              "shared_weight1 must be [S, 2I, H] with the routed experts' 2I")
+        _need_weights(*shared, s_num, h, aw, swdt == DT_FP4_E2M1, what="shared_")
+    if x_scales is not None:
+        _need(x_scales.numel() >= bs * (h // 32), f"x_scales must be [BS, H/32] = [{bs}, {h // 32}]")
+    _need_out(out, (bs, h))
+    _need_cuda(x, topk_ids, topk_weights, weight1, weight2, weight_scales1, weight_scales2)
+    L = load()
+    dev = x.device
     y = out if out is not None else torch.empty((bs, h), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(moe_expert_num, dtype=torch.int32, device=dev)
     exp_idx = torch.empty(bs * k, dtype=torch.int32, device=dev) if want_expanded_row_idx else None
@@ -403,6 +452,8 @@ def mm_moe_ep_dispatch(x, topk_ids, moe_expert_num: int, ep_world_size: int,
     [N*K] int32 position of row j in the send order)."""
     _need_dtype(x, (torch.bfloat16, torch.float16), "x")
     _need_dtype(topk_ids, (torch.int32,), "topk_ids")
+    _need(x.dim() == 2 and topk_ids.dim() == 2 and topk_ids.shape[0] == x.shape[0],
+          "x must be [N, H] and topk_ids [N, K]")
     _need_cuda(x, topk_ids)
     L = load()
     n, h = x.shape
@@ -437,22 +488,25 @@ def mm_moe_combine(expert_rows, row_idx, topk_weights, out=None, shared_rows=Non
     _need_dtype(expert_rows, _BYTE_DTYPES if quant else (torch.bfloat16,), "expert_rows")
     if quant:
         _need_dtype(expert_scales, (torch.uint8,), "expert_scales")
-        _need_cuda(expert_scales)
     rdt = _fp8_code(expert_rows, expert_rows_dtype) if quant else DT_BF16
     _need_dtype(row_idx, (torch.int32,), "row_idx")
     _need_dtype(topk_weights, (torch.float32, torch.bfloat16), "topk_weights")
-    _need_cuda(expert_rows, row_idx, topk_weights)
+    _need(expert_rows.dim() == 2 and topk_weights.dim() == 2, "expert_rows must be [*, H] and topk_weights [N, K]")
     n, k = topk_weights.shape
     h = expert_rows.shape[1]
     if row_idx.numel() != n * k:
         raise MMError("row_idx must hold N*K entries")
+    if quant:
+        _need(tuple(expert_scales.shape) == (expert_rows.shape[0], h // 32),
+              f"expert_scales must be [{expert_rows.shape[0]}, {h // 32}] (one E8M0 byte per 32 codes of each row)")
+    _need_out(out, (n, h))
     s_num = 0
     if shared_rows is not None:
         _need_dtype(shared_rows, (torch.bfloat16,), "shared_rows")
-        _need_cuda(shared_rows)
         if shared_rows.dim() != 3 or tuple(shared_rows.shape[1:]) != (n, h):
             raise MMError("shared_rows must be [S, N, H]")
         s_num = shared_rows.shape[0]
+    _need_cuda(expert_rows, row_idx, topk_weights, expert_scales, out, shared_rows)
     y = out if out is not None else torch.empty((n, h), dtype=torch.bfloat16, device=expert_rows.device)
     _check(load().mm_moe_combine(_ptr(expert_rows), rdt, _ptr(expert_scales), _ptr(row_idx), _ptr(topk_weights),
                                  _dt(topk_weights), n, h, k, _ptr(shared_rows), s_num, _ptr(y),
@@ -478,14 +532,20 @@ def mm_moe_expert_ffn(x, x_scales, expert_ids, weight1, weight2, weight_scales1,
         _need_dtype(t, _BYTE_DTYPES, name)
     for name, t in (("weight_scales1", weight_scales1), ("weight_scales2", weight_scales2)):
         _need_dtype(t, (torch.uint8,), name)
-    _need_cuda(x, x_scales, expert_ids, weight1, weight2, weight_scales1, weight_scales2)
+    _need(x.dim() == 2 and weight1.dim() == 3, "x must be [M, H] and weight1 [E, 2I, H]")
     m = x.shape[0]
     h = x.shape[1] * 2 if x_dtype == DT_FP4_E2M1 else x.shape[1]
     if expert_ids.numel() != m or x_scales.shape[0] != m:
         raise MMError("expert_ids and x_scales must hold one entry / row per row of x")
+    _need(x_scales.numel() >= m * (h // 32), f"x_scales must be [M, H/32] = [{m}, {h // 32}]")
+    inter = weight1.shape[1] // 2
+    aw = 2 * inter if activation == "gelu" else inter
+    _need_weights(weight1, weight2, weight_scales1, weight_scales2, local_experts, h, aw,
+                  _fp8_code(weight1, weight_dtype) == DT_FP4_E2M1)
+    _need_out(out, (m, h))
+    _need_cuda(x, x_scales, expert_ids, weight1, weight2, weight_scales1, weight_scales2)
     L = load()
     dev = x.device
-    inter = weight1.shape[1] // 2
     y = out if out is not None else torch.empty((m, h), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(local_experts, dtype=torch.int32, device=dev)
     need = ctypes.c_size_t(0)
@@ -556,6 +616,8 @@ def mm_moe_init_routing_noalloc(x, expert_idx, expert_num: int, quant_mode: int 
     the GPU race on the shared array; keep them on one stream."""
     _need_dtype(x, _SRC_DTYPES, "x")
     _need_dtype(expert_idx, (torch.int32,), "expert_idx")
+    _need(x.dim() == 2, "x must be [N, H]")
+    _need_rows_of(expert_idx, x.shape[0], "expert_idx", "x")
     _need_cuda(x, expert_idx)
     L = load()
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int

@@ -919,6 +919,7 @@ mm_status mm_moe_combine(const void* expert_rows, int expert_rows_dtype, const u
                          int64_t h, int64_t k, const void* shared_rows, int64_t n_shared, void* y, void* stream) {
   if (num_rows < 0 || h <= 0 || k <= 0 || n_shared < 0 || n_shared > 4 || k + n_shared > 36)
     return MM_ERR_INVALID_ARG;
+  if (num_rows * k >= kSortLimit) return MM_ERR_INVALID_ARG;  // the dispatch's row limit
   if (topk_weights_dtype != MM_DT_FLOAT32 && topk_weights_dtype != MM_DT_BFLOAT16) return MM_ERR_INVALID_ARG;
   // bf16 rows, or MXFP8 rows of the combine exchange (combineQuantMode 3 / 4)
   const bool q = expert_rows_dtype != MM_DT_BFLOAT16;

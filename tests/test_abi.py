@@ -254,3 +254,170 @@ def test_binding_refuses_index_and_data_types_the_abi_would_misread():
         mm.mm_mega_moe(x, ids32, gate, w1, w2, s1, s2.to(torch.int32), 8)
     with pytest.raises(mm.MMError, match="BS = x.shape"):
         mm.mm_mega_moe(x, ids32[:3], gate[:3], w1, w2, s1, s2, 8)
+
+
+def test_expert_parallel_host_rejections(lib):
+    """mm_moe_ep_dispatch, mm_moe_combine and mm_moe_expert_ffn refuse bad
+    arguments with a status before anything is enqueued (MegaMoE README,
+    parameter table: epWorldSize, moeExpertNum, dispatchQuantOutDtype,
+    combineQuantMode; the constraints' "reports an error" rule)."""
+    vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
+
+    def dispatch(n=64, h=256, k=2, e=8, w=2, xdt=27, qdt=24, ptr=1, ws=None, wsb=0, counts=1):
+        return lib.mm_moe_ep_dispatch(vp(ptr), xdt, vp(ptr), n, h, k, e, w, qdt, vp(ptr), vp(ptr), vp(ptr),
+                                      vp(counts), vp(ptr), vp(ws), wsb, None, None)
+    assert dispatch() == 3                 # valid: stops at the missing workspace
+    assert dispatch(qdt=296) == 3          # packed FP4 rows (A4W4-FP)
+    assert dispatch(w=0) == 1              # ep_world_size
+    assert dispatch(w=3) == 1              # E not a multiple of W
+    assert dispatch(k=9) == 1              # top-K above E
+    assert dispatch(k=33, e=64) == 1       # top-K above 32
+    assert dispatch(n=1 << 22, k=4) == 1   # N*K at the sort limit
+    assert dispatch(xdt=0) == 1            # fp32 tokens
+    assert dispatch(qdt=1) == 2            # INT8 is not an MX type
+    assert dispatch(h=192) == 2            # H % 128
+    assert dispatch(ptr=None) == 1         # missing buffers
+    assert lib.mm_moe_ep_dispatch(ctypes.c_void_p(8), 27, vp(1), 64, 256, 2, 8, 2, 24, vp(1), vp(1), vp(1), vp(1),
+                                  vp(1), None, 0, None, None) == 1  # x not 16-byte aligned
+    assert dispatch(n=0, counts=None) == 0  # no rows, nothing to zero
+    n_ws = ctypes.c_size_t(0)
+    assert lib.mm_moe_ep_dispatch_workspace_size(64, 2, 2, ctypes.byref(n_ws)) == 0 and n_ws.value > 0
+    assert lib.mm_moe_ep_dispatch_workspace_size(64, 2, 0, ctypes.byref(n_ws)) == 1
+
+    def combine(rdt=27, sc=None, n=64, h=256, k=2, gdt=0, sh=None, ns=0, y=1, rows=1):
+        return lib.mm_moe_combine(vp(rows), rdt, vp(sc), vp(1), vp(1), gdt, n, h, k, vp(sh), ns, vp(y), None)
+    assert combine(n=0) == 0               # no tokens: nothing to do
+    assert combine(ns=5, sh=1) == 1        # at most 4 shared experts
+    assert combine(k=33, ns=4, sh=1) == 1  # k + n_shared <= 36
+    assert combine(n=1 << 22, k=4) == 1    # N*K at the dispatch's row limit
+    assert combine(gdt=1) == 1             # gating weights fp32 or bf16
+    assert combine(rdt=296, sc=1) == 2     # MXFP4 rows are not a combine quantisation
+    assert combine(h=100) == 2             # H % 8
+    assert combine(rdt=23, sc=1, h=48) == 2  # MXFP8 rows: H % 32
+    assert combine(rdt=24) == 1            # MXFP8 rows without their scales
+    assert combine(ns=1) == 1              # shared experts without their rows
+    assert combine(y=None) == 1
+    assert combine(rows=None) == 1
+    assert lib.mm_moe_combine(vp(1), 27, None, vp(1), vp(1), 0, 64, 256, 2, None, 0, ctypes.c_void_p(24),
+                              None) == 1   # y not 16-byte aligned
+
+    def ffn(rows=64, h=256, xdt=24, wdt=24, e=4, inter=128, xs=1, act=b"swiglu", ws=None, wsb=0, counts=1):
+        return lib.mm_moe_expert_ffn(vp(1), vp(xs), xdt, vp(1), rows, h, vp(1), vp(1), vp(1), vp(1), wdt, 0, e, inter,
+                                     act, None, 0, vp(1), vp(counts), vp(ws), wsb, None, None)
+    assert ffn() == 3                      # valid: stops at the missing workspace
+    assert ffn(xdt=296, wdt=296) == 3      # A4W4-FP rows
+    assert ffn(xdt=296) == 2               # FP4 rows need FP4 weights
+    assert ffn(xdt=1) == 2                 # not an MX type
+    assert ffn(xs=None) == 1               # the received rows' scales are required
+    assert ffn(h=200) == 2                 # H % 128
+    assert ffn(inter=100) == 2             # I % 128
+    assert ffn(e=0) == 1
+    assert ffn(act=b"relu") == 2
+    assert ffn(rows=0, counts=None) == 0   # no rows received
+    n_ws = ctypes.c_size_t(0)
+    assert lib.mm_moe_expert_ffn_workspace_size(64, 256, 4, 128, 0, ctypes.byref(n_ws)) == 0 and n_ws.value > 0
+
+
+def test_quantize_and_scale_preparation_host_rejections(lib):
+    """mm_mx_quantize and the weight-scale preparation check sizes, types and
+    alignment on the host; the prepared layout's size is the pages' scale
+    bytes, with 256-row pairs of GEMM2's output rows padded."""
+    vp = lambda v: None if v is None else ctypes.c_void_p(16 * v)
+
+    def quant(src_dt=27, rows=8, cols=256, out_dt=24, sc_cols=8, ptr=1):
+        return lib.mm_mx_quantize(vp(ptr), src_dt, rows, cols, out_dt, vp(ptr), vp(ptr), sc_cols, None)
+    assert quant(rows=0) == 0              # nothing to do
+    assert quant(rows=-1) == 1
+    assert quant(cols=0) == 1
+    assert quant(src_dt=3) == 1            # int32 source
+    assert quant(out_dt=1) == 1            # INT8 is not an MX type
+    assert quant(cols=40) == 2             # cols % 16
+    assert quant(sc_cols=7) == 1           # fewer scale columns than groups
+    assert quant(ptr=None) == 1
+    size = lambda which, e, n, k: _ws(lib, "mm_prepared_weight_scales_size", which, e, n, k)
+    assert size(1, 2, 512, 256) == (0, 2 * 512 * 256 // 32)
+    assert size(2, 2, 384, 256) == (0, 2 * 2 * 2 * (256 // 128) * 512)   # 384 rows padded to two pairs
+    assert size(3, 2, 512, 256)[0] == 1    # GEMM 1 or 2
+    assert size(1, 2, 512, 200)[0] == 1    # K % 128
+    assert size(1, 2, 384, 256)[0] == 1    # GEMM1 output rows come in gate / up pairs of 128
+    assert lib.mm_prepare_weight_scales(ctypes.c_void_p(2), 1, 2, 512, 256, vp(1), None) == 1  # misaligned
+    assert lib.mm_prepare_weight_scales(None, 1, 2, 512, 256, vp(1), None) == 1
+
+
+def test_binding_refuses_mismatched_shapes():
+    """The C ABI takes sizes and raw pointers, so the binding checks that the
+    tensors agree with the sizes it passes (a smaller tensor would be read past
+    its end on the GPU).  Consistent arguments pass every shape check and stop
+    at the device check, for FP8 and packed FP4 weights, gelu, shared experts,
+    prepared scales and pass-through inputs."""
+    import torch
+    u8 = lambda *s: torch.zeros(s, dtype=torch.uint8)
+    bf = lambda *s: torch.zeros(s, dtype=torch.bfloat16)
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32)
+    f32 = lambda *s: torch.zeros(s, dtype=torch.float32)
+    device = "inputs must be contiguous CUDA tensors"
+
+    def refused(fn, match):
+        with pytest.raises(mm.MMError, match=match):
+            fn()
+
+    # routing, permute, no-allocation routing, expert-parallel dispatch: ids agree with x
+    x, ids = bf(6, 256), i32(6, 2)
+    refused(lambda: mm.mm_moe_init_routing(x, i32(5, 2), 8), "expert_idx must be")
+    refused(lambda: mm.mm_moe_init_routing_noalloc(x, i32(7, 2), 8), "expert_idx must be")
+    refused(lambda: mm.mm_moe_token_permute(x, i32(5), 8), "indices must be")
+    refused(lambda: mm.mm_moe_ep_dispatch(x, i32(5, 2), 8, 2), "topk_ids")
+    refused(lambda: mm.mm_moe_init_routing(x, ids, 8), device)
+    refused(lambda: mm.mm_moe_token_permute(x, i32(6), 8), device)
+    refused(lambda: mm.mm_moe_ep_dispatch(x, ids, 8, 2), device)
+
+    # MegaMoE: E = 8, H = 256, I = 128
+    e, h, i = 8, 256, 128
+    gate = f32(6, 2)
+    w = dict(weight1=u8(e, 2 * i, h), weight2=u8(e, h, i), weight_scales1=u8(e, 2 * i, h // 32),
+             weight_scales2=u8(e, h, i // 32))
+    mega = lambda **kw: mm.mm_mega_moe(kw.pop("x", x), ids, gate, kw.pop("weight1", w["weight1"]),
+                                       kw.pop("weight2", w["weight2"]), kw.pop("weight_scales1", w["weight_scales1"]),
+                                       kw.pop("weight_scales2", w["weight_scales2"]), kw.pop("e", e), **kw)
+    refused(lambda: mega(), device)
+    refused(lambda: mega(e=16), r"weight1 must be \[16")                      # E disagrees with the weights
+    refused(lambda: mega(weight1=u8(e, 2 * i, 512)), "weight1 must be")       # H disagrees with x
+    refused(lambda: mega(weight2=u8(e, h, 2 * i)), "weight2 must be")         # A_hat width
+    refused(lambda: mega(weight_scales2=u8(e, h, 2)), "weight_scales2 holds")
+    refused(lambda: mega(out=bf(6, 128)), "out must be")
+    refused(lambda: mega(weight2=u8(e, h, 2 * i), weight_scales2=u8(e, h, 2 * i // 32), activation="gelu",
+                         activation_params=(3.4e38,)), device)
+    refused(lambda: mega(weight1=u8(e, 2 * i, h // 2), weight2=u8(e, h, i // 2), weight_dtype=296), device)  # FP4
+    refused(lambda: mega(weight1=u8(e, 2 * i, h // 2), weight_dtype=296), "weight2 must be")
+    # prepared buffers of mm_prepared_weight_scales_size bytes (GEMM2's 256 output rows = one pair)
+    prepared = dict(weight_scales1=u8(e * 2 * i * h // 32), weight_scales2=u8(e * 2 * 1 * (i // 128) * 512))
+    refused(lambda: mega(weight_scale_layout=1, **prepared), device)
+    sh = dict(shared_weight1=u8(1, 2 * i, h), shared_weight2=u8(1, h, i), shared_weight_scales1=u8(1, 2 * i, h // 32),
+              shared_weight_scales2=u8(1, h, i // 32))
+    refused(lambda: mega(**sh), device)
+    refused(lambda: mega(**dict(sh, shared_weight_scales2=None)), "shared experts need all four")
+    refused(lambda: mega(**dict(sh, shared_weight2=u8(1, h, 2 * i))), "shared_weight2 must be")
+    refused(lambda: mega(**dict(sh, shared_weight1=u8(1, 2 * i, h // 2), shared_weight2=u8(1, h, i // 2)),
+                         shared_weight_dtype=296), device)
+    xq = u8(6, h)
+    refused(lambda: mega(x=xq, dispatch_quant_mode=0, x_scales=u8(6, h // 32)), device)   # pass-through
+    refused(lambda: mega(x=xq, dispatch_quant_mode=0, x_scales=u8(6, 4)), "x_scales must be")
+
+    # expert side: M = 10 received rows, 4 local experts
+    ffn = lambda **kw: mm.mm_moe_expert_ffn(kw.pop("x", u8(10, h)), kw.pop("x_scales", u8(10, h // 32)), i32(10),
+                                            kw.pop("weight1", u8(4, 2 * i, h)), kw.pop("weight2", u8(4, h, i)),
+                                            u8(4, 2 * i, h // 32), u8(4, h, i // 32), kw.pop("e", 4), **kw)
+    refused(lambda: ffn(), device)
+    refused(lambda: ffn(e=8), "weight1 must be")
+    refused(lambda: ffn(x_scales=u8(10, 2)), "x_scales must be")
+    refused(lambda: ffn(out=bf(10, 128)), "out must be")
+    refused(lambda: ffn(x=u8(10, h // 2), weight1=u8(4, 2 * i, h // 2), weight2=u8(4, h, i // 2), x_dtype=296,
+                        weight_dtype=296), device)
+
+    # combine: 6 tokens, top-K 2, 20 expert rows
+    comb = lambda **kw: mm.mm_moe_combine(kw.pop("rows", bf(20, h)), i32(12), gate, **kw)
+    refused(lambda: comb(), device)
+    refused(lambda: comb(out=bf(6, 128)), "out must be")
+    refused(lambda: comb(rows=u8(20, h), expert_scales=u8(19, h // 32), expert_rows_dtype=24), "expert_scales must be")
+    refused(lambda: comb(rows=u8(20, h), expert_scales=u8(20, h // 32), expert_rows_dtype=24), device)
+    refused(lambda: comb(shared_rows=bf(1, 6, 128)), "shared_rows must be")
