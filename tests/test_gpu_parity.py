@@ -850,6 +850,71 @@ def test_ep_dispatch_bit_exact(w, fmt):
     assert np.array_equal(host(ss), sc[:, :cfg.h // 32])
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", [23, 296])
+def test_ep_dispatch_full_size(fmt):
+    """mm_moe_ep_dispatch at the DeepSeek-V3 prefill batch of one source rank
+    (8192 tokens, hidden 7168, 256 experts, top-K 8, Zipf routing) over 8
+    ranks, with E5M2 rows and with packed FP4 rows (A4W4-FP): counts, scatter
+    index, local expert ids, codes and scales of all 65536 rows bit-exact
+    against the oracle's routing on rank keys and its Q_MX."""
+    cfg = synth.CONFIGS["dsv3_prefill"].scaled(dispatch_fmt=fmt)
+    w = 8
+    el = cfg.e // w
+    x = synth.tokens_bf16(cfg)
+    ids = synth.topk_ids(cfg)
+    err = zeros_err()
+    sx, ss, se, cnt, ei = mm.mm_moe_ep_dispatch(bf16(x), t(ids), cfg.e, w, fmt, dev_err=err)
+    assert host(err)[0] == 0
+    srt, exp, ocnt, bad = oracle.route((ids // el).astype(np.int32), w)
+    assert bad == 0
+    assert np.array_equal(host(cnt), ocnt)
+    assert np.array_equal(host(ei), exp)
+    assert np.array_equal(host(se), ids.reshape(-1)[srt] % el)
+    q, sc = oracle.permute(x, oracle.DT_BF16, cfg.k, srt, srt.size, fmt)
+    assert np.array_equal(host(ss), sc[:, :cfg.h // 32])
+    assert np.array_equal(host(sx), pack_fp4(q) if fmt == 296 else q)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("row_fmt", [27, 24])
+def test_ep_combine_full_size(row_fmt):
+    """mm_moe_combine at the DeepSeek-V3 prefill batch (8192 tokens, top-K 8,
+    hidden 7168, bf16 gates, one block per token as in the step), with the
+    returned rows as bf16 or as MXFP8 E4M3 codes and E8M0 scales from the
+    oracle's Q_MX (combineQuantMode 4), picked by a scatter index that leaves
+    some terms out (-1).  Sampled tokens against the fp64 sum of the oracle's
+    row values, within half a bf16 step of the result plus the fp32
+    accumulation bound (the fp32 order itself is checked bit for bit at small
+    sizes)."""
+    cfg = synth.CONFIGS["dsv3_prefill"]
+    n, k, h = cfg.n, cfg.k, cfg.h
+    nrows = 6000
+    rng = np.random.default_rng(31)
+    rows = (rng.standard_normal((nrows, h), dtype=np.float32) *
+            np.exp2(rng.integers(-6, 6, (nrows, 1))).astype(np.float32))
+    idx = rng.integers(-1, nrows, size=n * k).astype(np.int32)
+    gate = synth.topk_weights(cfg)
+    gw = synth.bf16_bits_to_f32(gate).reshape(n, k).astype(np.float64)
+    if row_fmt == 27:
+        rb = torch.from_numpy(rows).to(torch.bfloat16)
+        vals = rb.float().numpy().astype(np.float64)
+        y = mm.mm_moe_combine(rb.to(DEV), t(idx), bf16(gate))
+    else:
+        q, sc = oracle.mx_quantize(rows, oracle.DT_F32, row_fmt, s_cols=h // 32)
+        tab = np.array([oracle.fp8_value(c, row_fmt) for c in range(256)])
+        vals = tab[q] * np.exp2(np.repeat(sc.astype(np.float64) - 127.0, 32, axis=1))
+        y = mm.mm_moe_combine(t(q), t(idx), bf16(gate), expert_scales=t(sc), expert_rows_dtype=row_fmt)
+    yv = synth.bf16_bits_to_f32(host(y).view(np.uint16)).astype(np.float64)
+    ix = idx.reshape(n, k)
+    for i in (0, 1, 777, 2048, 4095, 5000, 7333, 8191):
+        ok = ix[i] >= 0
+        terms = gw[i, ok, None] * vals[ix[i, ok]]
+        ref = terms.sum(axis=0)
+        bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -20 * np.abs(terms).sum(axis=0)
+        assert np.all(np.abs(yv[i] - ref) <= bound), i
+
+
 @pytest.mark.parametrize("case", [
     dict(n=700, h=512, inter=256, e=8, k=1, routing="zipf"),
     dict(n=300, h=896, inter=384, e=5, k=1, weight_fmt=296, dispatch_fmt=23),
